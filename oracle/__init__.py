@@ -1,0 +1,200 @@
+"""Python access to the CPU oracle (oracle.c).
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the smoke check and by
+the CPU-baseline leg of bench.py.  The library under test never imports it.
+
+The C file is compiled with gcc (-O2 -ffp-contract=off, so that the fp32
+rotary keeps one rounding per operation) into liboracle.so beside it.
+Arrays cross the boundary as numpy buffers; fp16 tensors travel as their
+uint16 bit patterns.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, BAD_ARGUMENT, BAD_DEVICE_DATA = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c -> liboracle.so (plain gcc, no CUDA)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math",
+                           "-std=c11", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            P, I, LL, Dd = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_double
+            L.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            L.oracle_half_to_double.restype = Dd
+            L.oracle_double_to_half.argtypes = [Dd]
+            L.oracle_double_to_half.restype = ctypes.c_uint16
+            L.oracle_rotary.argtypes = [P, P, I, I, I, P, P, I, P, P, I, I, I]
+            L.oracle_rotary.restype = I
+            L.oracle_cache_write.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I]
+            L.oracle_cache_write.restype = I
+            L.oracle_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I,
+                                           Dd, Dd, I, LL, LL, P]
+            L.oracle_attention.restype = I
+            _lib = L
+    return _lib
+
+
+def _np(x, dtype):
+    """torch tensor / numpy array -> C-contiguous numpy array of `dtype`."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu()
+        if dtype == np.uint16:
+            import torch
+            x = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+        else:
+            x = x.contiguous().numpy()
+    return np.ascontiguousarray(x).astype(dtype, copy=False)
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p) if a is not None else None
+
+
+def _check(st, what):
+    if st != OK:
+        raise ValueError(f"oracle {what} failed with status {st}")
+
+
+def half_bits_to_double(bits: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lib().oracle_half_to_double, otypes=[np.float64])
+    return f(bits.astype(np.uint16))
+
+
+def double_to_half_bits(x: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lambda v: lib().oracle_double_to_half(float(v)), otypes=[np.uint16])
+    return f(np.asarray(x, dtype=np.float64))
+
+
+def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
+    """Rotated copy of x ([T, nheads*D] fp16 bits) at positions past_b + j."""
+    xa = _np(x, np.uint16)
+    cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
+    cos_a, sin_a = _np(cos_cache, np.uint16), _np(sin_cache, np.uint16)
+    T = xa.shape[0]
+    y = np.empty_like(xa)
+    st = lib().oracle_rotary(_p(xa), _p(y), T, nheads, head_size, _p(cum_a), _p(past_a),
+                             past_a.shape[0], _p(cos_a), _p(sin_a), cos_a.shape[1],
+                             cos_a.shape[0], interleaved)
+    _check(st, "rotary")
+    return y
+
+
+def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
+                kv_num_heads, head_size, block_size):
+    """Returns (key_cache', value_cache') after writing the new tokens' rows.
+
+    key/value are fp16 bit arrays [T, Hk*D] (key already rotated when rotary
+    is on); the input caches are copied, not modified."""
+    ka, va = _np(key, np.uint16), _np(value, np.uint16)
+    kc = _np(key_cache, np.uint16).copy()
+    vc = _np(value_cache, np.uint16).copy()
+    bt = _np(block_table, np.int32)
+    cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
+    st = lib().oracle_cache_write(_p(ka), _p(va), _p(kc), _p(vc), _p(bt), bt.shape[1],
+                                  _p(cum_a), _p(past_a), past_a.shape[0], ka.shape[0],
+                                  kv_num_heads, head_size, block_size, kc.shape[0])
+    _check(st, "cache_write")
+    return kc, vc
+
+
+def attention(query, key_cache, value_cache, block_table, cum, past, num_heads,
+              kv_num_heads, head_size, block_size, scale, softcap, window,
+              rows=None, threads=None):
+    """fp64 attention output.
+
+    rows=None computes every (t, h) row and returns [T, H, D]; otherwise
+    `rows` is an int array of r = t*H + h and the result is [len(rows), D].
+    Row ranges run on `threads` Python threads (the C call releases the GIL).
+    """
+    qa = _np(query, np.uint16)
+    kc, vc = _np(key_cache, np.uint16), _np(value_cache, np.uint16)
+    bt = _np(block_table, np.int32)
+    cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
+    T, H, D = qa.shape[0], num_heads, head_size
+    B, MB, NB = past_a.shape[0], bt.shape[1], kc.shape[0]
+    L = lib()
+
+    def run(r0, r1, out):
+        st = L.oracle_attention(_p(qa), _p(kc), _p(vc), _p(bt), MB, _p(cum_a), _p(past_a),
+                                B, T, H, kv_num_heads, D, block_size, NB, float(scale),
+                                float(softcap), int(window), r0, r1, _p(out))
+        _check(st, "attention")
+
+    threads = threads or 1
+    if rows is None:
+        out = np.zeros((T * H, D), dtype=np.float64)
+        n = T * H
+        if threads <= 1 or n < 2:
+            run(0, n, out)
+        else:
+            bounds = np.linspace(0, n, min(threads, n) + 1).astype(np.int64)
+            with ThreadPoolExecutor(threads) as ex:
+                list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1]),
+                                          out[bounds[i]:bounds[i + 1]]), range(len(bounds) - 1)))
+        return out.reshape(T, H, D)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.shape[0], D), dtype=np.float64)
+
+    def one(i):
+        run(int(rows[i]), int(rows[i]) + 1, out[i:i + 1])
+
+    if threads <= 1:
+        for i in range(rows.shape[0]):
+            one(i)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(rows.shape[0])))
+    return out
+
+
+def forward(step, threads=None, rows=None):
+    """Whole step on the CPU: rotary (if on), cache write, attention.
+
+    `step` is a dict as produced by workloads.make_step.  Returns a dict with
+    the rotated query bits, the updated caches (uint16 bits) and the fp64
+    output ([T, H, D], or [len(rows), D] when rows is given).
+    """
+    H, Hk, D = step["num_heads"], step["kv_num_heads"], step["head_size"]
+    cum, past = step["cumulative_sequence_lengths"], step["past_sequence_lengths"]
+    q = _np(step["query"], np.uint16)
+    k = _np(step["key"], np.uint16)
+    if step["do_rotary"]:
+        q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D,
+                   step["rotary_interleaved"])
+        k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
+                   step["rotary_interleaved"])
+    kc, vc = cache_write(k, step["value"], step["key_cache"], step["value_cache"],
+                         step["block_table"], cum, past, Hk, D, step["block_size"])
+    out = attention(q, kc, vc, step["block_table"], cum, past, H, Hk, D,
+                    step["block_size"], step["scale"], step["softcap"],
+                    step["local_window_size"], rows=rows, threads=threads)
+    return dict(query_rot=q, key_rot=k, key_cache=kc, value_cache=vc, out=out)
