@@ -1,0 +1,214 @@
+/*
+ * pa.h - C ABI of the GB300 PagedAttention step library.
+ *
+ * One step of a continuous-batching engine's attention layer on one GPU:
+ *   1. (optional) rotary embedding of the new Q and K rows,
+ *   2. reshape_and_cache: the new K/V rows are written into the shared
+ *      paged pool through block_table (in place),
+ *   3. causal grouped-query attention of every packed query token over its
+ *      sequence's cached context, with optional local window and softcap.
+ *
+ * The operation is the one specified by "PagedAttention - CUDA Design
+ * Document" (onnxruntime 1.29.0 docs, contrib_ops/cuda/paged_attention):
+ * section 4 (op contract, input/attribute meaning, in-place cache aliasing),
+ * section 4.7 (no host read of device lengths; host values only size
+ * launches), section 5.1 (derived write slot), section 8 implementation
+ * note P5 (causal bound past + j + 1, window [kv_len - W, kv_len), softcap
+ * softcap * tanh(x * scale / softcap), split-KV with log-sum-exp merge),
+ * section 9 (-1 block entries are unmapped and masked) and section 15
+ * (validation rules); and by "Design: WebGPU PagedAttention" section 3.3
+ * (packed tokens delimited by cumulative_sequence_lengths).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers on the handle's device unless
+ *     stated otherwise; all tensors are dense row-major.  fp16 tensors are
+ *     passed as void* holding IEEE binary16.  int32 tensors as int32_t*.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - The caller owns every tensor.  key_cache and value_cache are updated
+ *     in place (the op's cache outputs alias its cache inputs).  The library
+ *     owns only the workspace allocated by pa_create.
+ *   - pa_cache_write and pa_forward never allocate, never synchronise and
+ *     never copy device data to the host, so they may be captured into a CUDA
+ *     graph (device addresses must then stay fixed across replays).
+ *   - Host-checkable errors return PA_INVALID_ARGUMENT / PA_NOT_SUPPORTED
+ *     before anything is launched; pa_last_error_message() names the
+ *     offending argument.  Device-resident values (lengths, block ids) are
+ *     not read by the host: invalid ones are skipped by the kernels without
+ *     any out-of-bounds access and recorded in a device error word that
+ *     pa_check_device_error() returns.
+ *
+ * Shapes (T = token_count, B = batch, H = num_heads, Hk = kv_num_heads,
+ * D = head_size, bs = block_size, NB = num_blocks, MB = max_blocks_per_seq):
+ *   query        [T, H*D]          fp16
+ *   key, value   [T, Hk*D]         fp16 (new tokens, not yet rotated)
+ *   key_cache    [NB, bs, Hk, D]   fp16, value_cache likewise
+ *   block_table  [B, MB]           int32; entry i of row b = block holding
+ *                                  positions [i*bs, (i+1)*bs) of sequence b,
+ *                                  -1 = not mapped (masked; no write)
+ *   cumulative_sequence_lengths [B+1] int32, cum[0] = 0, cum[B] = T
+ *   past_sequence_lengths       [B]   int32, cached tokens per sequence
+ *   cos_cache, sin_cache [P, rotary_dim/2] fp16 (P = max_rotary_positions)
+ *   output       [T, H*D]          fp16
+ * Token j of sequence b is packed row cum[b] + j and has position
+ * past[b] + j.  Query head h uses kv head h / (H / Hk).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pa_handle_s* pa_handle;
+
+typedef enum {
+  PA_OK = 0,
+  PA_INVALID_ARGUMENT = 1,   /* a host-checkable rule was violated */
+  PA_NOT_SUPPORTED = 2,      /* valid op, but not built here (e.g. head_size 80) */
+  PA_CUDA_ERROR = 3,         /* a CUDA runtime/driver call failed */
+  PA_DEVICE_DATA_ERROR = 4   /* pa_check_device_error found a flagged value */
+} pa_status;
+
+/* Bits of the device error word (pa_check_device_error). */
+enum {
+  PA_DEVERR_CUM = 1,          /* cum[0] != 0, cum not monotone or cum[B] != T */
+  PA_DEVERR_BLOCK_ID = 2,     /* block id outside [-1, NB) (access skipped) */
+  PA_DEVERR_PAST = 4,         /* past < 0 (sequence skipped) */
+  PA_DEVERR_KV_BOUND = 8,     /* past + q_len > kv bound or > MB*bs (sequence skipped) */
+  PA_DEVERR_Q_BOUND = 16,     /* q_len > max_query_len_bound (sequence skipped) */
+  PA_DEVERR_ROTARY_POS = 32,  /* position >= max_rotary_positions (row left unrotated) */
+  PA_DEVERR_TIMEOUT = 64      /* an internal wait exceeded its limit (kernel gave up) */
+};
+
+/* Static description of a layer, fixed for the handle's lifetime
+ * (section 4.5 attributes plus the capacities that size launches, 4.7). */
+typedef struct {
+  int num_heads;          /* H, > 0, multiple of kv_num_heads */
+  int kv_num_heads;       /* Hk, > 0 */
+  int head_size;          /* D, multiple of 8; this build runs 64, 128, 256 */
+  int block_size;         /* bs, power of two >= 16 */
+  int num_blocks;         /* NB, > 0 */
+  int max_blocks_per_seq; /* MB, > 0 (block_table row length) */
+  float scale;            /* 0 => 1/sqrt(D) */
+  float softcap;          /* 0 => off; > 0 => softcap*tanh(x/softcap) */
+  int local_window_size;  /* -1 => off; W >= 1 admits W positions incl. self */
+  int do_rotary;          /* 0/1: rotate Q and K before the write */
+  int rotary_interleaved; /* 0: pairs (i, i+R/2); 1: pairs (2i, 2i+1) */
+  int rotary_dim;         /* R = 2*cos_cache.shape[1]; 0 => D when do_rotary */
+  int max_rotary_positions; /* P = cos_cache.shape[0] (rows of the tables) */
+  int max_batch;          /* capacity for B across every call on the handle */
+  int max_tokens;         /* capacity for T across every call on the handle */
+  int max_query_len_bound; /* 0 => max_tokens; upper bound on any q_len */
+  int max_kv_len_bound;    /* 0 => MB*bs; upper bound on any past + q_len */
+} pa_config;
+
+/* Fills *cfg with the attribute defaults (scale 0, softcap 0, window -1,
+ * no rotary, bounds 0).  Geometry fields are set to 0 and must be filled. */
+PA_API void pa_config_init(pa_config* cfg);
+
+/* Host-only check of a configuration against the validation rules
+ * (section 15): H % Hk == 0, D % 8 == 0, bs a power of two >= 16,
+ * softcap >= 0, window == -1 or >= 1, rotary_dim even and <= D, positive
+ * capacities.  Writes a message naming the field into msg (may be NULL).
+ * Returns PA_INVALID_ARGUMENT or PA_NOT_SUPPORTED on failure.  Touches no GPU. */
+PA_API pa_status pa_validate_config(const pa_config* cfg, char* msg, size_t msg_len);
+
+/* Host-only check of one step's arguments (token_count <= max_tokens,
+ * batch <= max_batch, required pointers non-NULL (query, key, value and
+ * output may be NULL when token_count == 0), rotary tables present iff
+ * do_rotary).  query/output may be NULL when checking pa_cache_write
+ * (pass for_forward = 0).  Touches no GPU. */
+PA_API pa_status pa_check_step(const pa_config* cfg, int for_forward, const void* query,
+                        const void* key, const void* value, const void* key_cache,
+                        const void* value_cache, const int32_t* block_table,
+                        const int32_t* cumulative_sequence_lengths,
+                        const int32_t* past_sequence_lengths, int batch,
+                        int token_count, const void* cos_cache,
+                        const void* sin_cache, const void* output, char* msg,
+                        size_t msg_len);
+
+/* Validates cfg, then allocates the device workspace on the current CUDA
+ * device (work lists, split-KV partials, rotated-query buffer, error word)
+ * sized from the capacities.  May synchronise; never call during capture.
+ * On failure *out is NULL and pa_last_error_message(NULL) explains. */
+PA_API pa_status pa_create(const pa_config* cfg, pa_handle* out);
+
+/* Steps 1-2 only: rotary on K (if do_rotary) and the paged write of K and V
+ * for every new token.  Slot = block_table[b][pos/bs]*bs + pos%bs; a -1
+ * entry writes nothing.  Bit-exact: without rotary the rows are copied;
+ * with rotary each pair is y1 = x1*c - x2*s, y2 = x2*c + x1*s in fp32 with
+ * one rounding per operation, then rounded to fp16. */
+PA_API pa_status pa_cache_write(pa_handle h, const void* key, const void* value,
+                         void* key_cache, void* value_cache,
+                         const int32_t* block_table,
+                         const int32_t* cumulative_sequence_lengths,
+                         const int32_t* past_sequence_lengths, int batch,
+                         int token_count, const void* cos_cache,
+                         const void* sin_cache, void* stream);
+
+/* The whole step: rotary on Q and K (if do_rotary), the paged cache write,
+ * then attention for every packed query row into output.  Row (t, h) of
+ * sequence b attends to positions p in [lo, past_b + j + 1) with
+ * lo = max(0, past_b + j + 1 - W) under a window, skipping positions whose
+ * block entry is -1; x = scale * <q, k_p>, optionally softcapped; output is
+ * the softmax-weighted sum of v_p (0 when no position is admitted).
+ * token_count == 0 returns PA_OK and launches nothing. */
+PA_API pa_status pa_forward(pa_handle h, const void* query, const void* key,
+                     const void* value, void* key_cache, void* value_cache,
+                     const int32_t* block_table,
+                     const int32_t* cumulative_sequence_lengths,
+                     const int32_t* past_sequence_lengths, int batch,
+                     int token_count, const void* cos_cache,
+                     const void* sin_cache, void* output, void* stream);
+
+/* Synchronises the stream of the handle's last call, reads and clears the
+ * device error word into *code (0 = clean).  Returns PA_DEVICE_DATA_ERROR
+ * when *code != 0.  Not capturable. */
+PA_API pa_status pa_check_device_error(pa_handle h, int* code);
+
+/* Message of the last failure on h (or of the last pa_create / validation
+ * failure on this thread when h is NULL).  Never NULL. */
+PA_API const char* pa_last_error_message(pa_handle h);
+
+/* Frees the workspace.  NULL is accepted. */
+PA_API pa_status pa_destroy(pa_handle h);
+
+/* ---- tuning and measurement hooks (set outside capture) ---- */
+enum {
+  PA_OPT_SPLIT_KEYS = 1,      /* > 0: fixed keys per decode split (multiple of 64); 0 = auto */
+  PA_OPT_NO_WINDOW_PRUNE = 2, /* 1: walk the whole context and mask instead of pruning */
+  PA_OPT_KERNEL_TIMING = 3,   /* 1: record CUDA events around each kernel of pa_forward */
+  PA_OPT_DECODE_MAX_ROWS = 4  /* route a sequence to the decode kernel iff q_len*G <= value (1..16, default 16; 0 = never) */
+};
+PA_API pa_status pa_set_option(pa_handle h, int option, int value);
+
+/* Kernel stages of a step, for pa_kernel_time_ms. */
+enum {
+  PA_STAGE_WORKLIST = 0,
+  PA_STAGE_CACHE_WRITE = 1,
+  PA_STAGE_DECODE = 2,
+  PA_STAGE_PREFILL = 3,
+  PA_STAGE_COMBINE = 4,
+  PA_NUM_STAGES = 5
+};
+/* With PA_OPT_KERNEL_TIMING on: synchronises, then returns in *ms the time
+ * between the events recorded on the launch stream around that stage's
+ * kernel in the last pa_forward (-1 when it did not launch). */
+PA_API pa_status pa_kernel_time_ms(pa_handle h, int stage, float* ms);
+
+/* Number of kernels the last pa_forward / pa_cache_write launched. */
+PA_API int pa_last_launch_count(pa_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PA_H_ */

@@ -1,0 +1,249 @@
+"""Python binding of the GB300 PagedAttention step library (libpa_gb300.so).
+
+Argument marshalling only: every function below forwards to the C entry
+point of the same name declared in include/pa.h.  Tensors are passed by
+`data_ptr()`; streams by `torch.cuda.Stream.cuda_stream`.  No computation
+happens here, and there is no fallback: if the shared library is missing
+or fails to load, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
+
+PA_OK, PA_INVALID_ARGUMENT, PA_NOT_SUPPORTED, PA_CUDA_ERROR, PA_DEVICE_DATA_ERROR = range(5)
+STATUS_NAMES = {0: "PA_OK", 1: "PA_INVALID_ARGUMENT", 2: "PA_NOT_SUPPORTED", 3: "PA_CUDA_ERROR",
+                4: "PA_DEVICE_DATA_ERROR"}
+
+PA_DEVERR_CUM, PA_DEVERR_BLOCK_ID, PA_DEVERR_PAST = 1, 2, 4
+PA_DEVERR_KV_BOUND, PA_DEVERR_Q_BOUND, PA_DEVERR_ROTARY_POS, PA_DEVERR_TIMEOUT = 8, 16, 32, 64
+
+PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_MAX_ROWS = 1, 2, 3, 4
+PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
+STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
+
+EXPORTED = ("pa_config_init", "pa_validate_config", "pa_check_step", "pa_create", "pa_cache_write",
+            "pa_forward", "pa_check_device_error", "pa_last_error_message", "pa_destroy",
+            "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count")
+
+
+class pa_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("num_heads", "kv_num_heads", "head_size", "block_size",
+                                            "num_blocks", "max_blocks_per_seq")] + [
+        ("scale", ctypes.c_float), ("softcap", ctypes.c_float)] + [
+        (n, ctypes.c_int) for n in ("local_window_size", "do_rotary", "rotary_interleaved",
+                                    "rotary_dim", "max_rotary_positions", "max_batch", "max_tokens",
+                                    "max_query_len_bound", "max_kv_len_bound")]
+
+
+class PAError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.message = message
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (builds nothing; call build() first)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; run paged_kv_cache_reshape_gb300.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        CFG = ctypes.POINTER(pa_config)
+        L.pa_config_init.argtypes = [CFG]
+        L.pa_config_init.restype = None
+        L.pa_validate_config.argtypes = [CFG, ctypes.c_char_p, S]
+        L.pa_check_step.argtypes = [CFG, I, P, P, P, P, P, P, P, P, I, I, P, P, P, ctypes.c_char_p, S]
+        L.pa_create.argtypes = [CFG, ctypes.POINTER(P)]
+        L.pa_cache_write.argtypes = [P, P, P, P, P, P, P, P, I, I, P, P, P]
+        L.pa_forward.argtypes = [P, P, P, P, P, P, P, P, P, I, I, P, P, P, P]
+        L.pa_check_device_error.argtypes = [P, ctypes.POINTER(I)]
+        L.pa_last_error_message.argtypes = [P]
+        L.pa_last_error_message.restype = ctypes.c_char_p
+        L.pa_destroy.argtypes = [P]
+        L.pa_set_option.argtypes = [P, I, I]
+        L.pa_kernel_time_ms.argtypes = [P, I, ctypes.POINTER(ctypes.c_float)]
+        L.pa_last_launch_count.argtypes = [P]
+        L.pa_last_launch_count.restype = I
+        for n in EXPORTED:
+            if n not in ("pa_config_init", "pa_last_error_message", "pa_last_launch_count"):
+                getattr(L, n).restype = I
+        _lib = L
+    return _lib
+
+
+def build(force: bool = False):
+    from . import builder as _b
+    return _b.build(force=force)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status, handle=None):
+    if status != PA_OK:
+        msg = lib().pa_last_error_message(handle).decode()
+        raise PAError(status, msg)
+
+
+def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
+                max_batch, max_tokens, scale=0.0, softcap=0.0, local_window_size=-1, do_rotary=0,
+                rotary_interleaved=0, rotary_dim=0, max_rotary_positions=0, max_query_len_bound=0,
+                max_kv_len_bound=0) -> pa_config:
+    c = pa_config()
+    lib().pa_config_init(ctypes.byref(c))
+    for k, v in dict(num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
+                     block_size=block_size, num_blocks=num_blocks,
+                     max_blocks_per_seq=max_blocks_per_seq, max_batch=max_batch,
+                     max_tokens=max_tokens, scale=scale, softcap=softcap,
+                     local_window_size=local_window_size, do_rotary=do_rotary,
+                     rotary_interleaved=rotary_interleaved, rotary_dim=rotary_dim,
+                     max_rotary_positions=max_rotary_positions,
+                     max_query_len_bound=max_query_len_bound,
+                     max_kv_len_bound=max_kv_len_bound).items():
+        setattr(c, k, v)
+    return c
+
+
+def pa_validate_config(cfg: pa_config):
+    buf = ctypes.create_string_buffer(512)
+    st = lib().pa_validate_config(ctypes.byref(cfg), buf, 512)
+    return st, buf.value.decode()
+
+
+def pa_check_step(cfg: pa_config, for_forward, query, key, value, key_cache, value_cache,
+                  block_table, cumulative_sequence_lengths, past_sequence_lengths, batch,
+                  token_count, cos_cache, sin_cache, output):
+    """Host-only argument check; pointer arguments are plain integers (or None)."""
+    buf = ctypes.create_string_buffer(512)
+    vp = lambda x: None if x is None else ctypes.c_void_p(x)
+    st = lib().pa_check_step(ctypes.byref(cfg), for_forward, vp(query), vp(key), vp(value),
+                             vp(key_cache), vp(value_cache), vp(block_table),
+                             vp(cumulative_sequence_lengths), vp(past_sequence_lengths), batch,
+                             token_count, vp(cos_cache), vp(sin_cache), vp(output), buf, 512)
+    return st, buf.value.decode()
+
+
+def pa_create(cfg: pa_config):
+    h = ctypes.c_void_p()
+    _check(lib().pa_create(ctypes.byref(cfg), ctypes.byref(h)))
+    return h
+
+
+def pa_destroy(h):
+    _check(lib().pa_destroy(h))
+
+
+def pa_set_option(h, option, value):
+    _check(lib().pa_set_option(h, option, value), h)
+
+
+def pa_cache_write(h, key, value, key_cache, value_cache, block_table,
+                   cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
+                   cos_cache=None, sin_cache=None, stream=None):
+    _check(lib().pa_cache_write(h, _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                _ptr(block_table), _ptr(cumulative_sequence_lengths),
+                                _ptr(past_sequence_lengths), batch, token_count, _ptr(cos_cache),
+                                _ptr(sin_cache), ctypes.c_void_p(stream or 0)), h)
+
+
+def pa_forward(h, query, key, value, key_cache, value_cache, block_table,
+               cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
+               cos_cache, sin_cache, output, stream=None):
+    _check(lib().pa_forward(h, _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache),
+                            _ptr(value_cache), _ptr(block_table),
+                            _ptr(cumulative_sequence_lengths), _ptr(past_sequence_lengths),
+                            batch, token_count, _ptr(cos_cache), _ptr(sin_cache), _ptr(output),
+                            ctypes.c_void_p(stream or 0)), h)
+
+
+def pa_check_device_error(h) -> int:
+    code = ctypes.c_int(0)
+    st = lib().pa_check_device_error(h, ctypes.byref(code))
+    if st not in (PA_OK, PA_DEVICE_DATA_ERROR):
+        _check(st, h)
+    return code.value
+
+
+def pa_kernel_time_ms(h, stage) -> float:
+    ms = ctypes.c_float(-1.0)
+    _check(lib().pa_kernel_time_ms(h, stage, ctypes.byref(ms)), h)
+    return ms.value
+
+
+def pa_last_launch_count(h) -> int:
+    return lib().pa_last_launch_count(h)
+
+
+def pa_last_error_message(h=None) -> str:
+    return lib().pa_last_error_message(h).decode()
+
+
+class PagedAttention:
+    """A handle bound to one layer configuration (owns the device workspace)."""
+
+    def __init__(self, cfg: pa_config):
+        self.cfg = cfg
+        self.handle = pa_create(cfg)
+
+    @classmethod
+    def for_step(cls, step: dict, max_batch: Optional[int] = None, max_tokens: Optional[int] = None,
+                 **bounds):
+        cos = step.get("cos_cache")
+        cfg = make_config(step["num_heads"], step["kv_num_heads"], step["head_size"],
+                          step["block_size"], step["num_blocks"], step["max_blocks_per_seq"],
+                          max_batch or step["batch"], max_tokens or max(step["token_count"], 1),
+                          scale=step["scale"], softcap=step["softcap"],
+                          local_window_size=step["local_window_size"],
+                          do_rotary=step["do_rotary"],
+                          rotary_interleaved=step["rotary_interleaved"],
+                          rotary_dim=step.get("rotary_dim", 0) or 0,
+                          max_rotary_positions=0 if cos is None else cos.shape[0], **bounds)
+        return cls(cfg)
+
+    def forward(self, step: dict, output, stream=None):
+        pa_forward(self.handle, step["query"], step["key"], step["value"], step["key_cache"],
+                   step["value_cache"], step["block_table"], step["cumulative_sequence_lengths"],
+                   step["past_sequence_lengths"], step["batch"], step["token_count"],
+                   step.get("cos_cache"), step.get("sin_cache"), output, stream)
+
+    def cache_write(self, step: dict, stream=None):
+        pa_cache_write(self.handle, step["key"], step["value"], step["key_cache"],
+                       step["value_cache"], step["block_table"],
+                       step["cumulative_sequence_lengths"], step["past_sequence_lengths"],
+                       step["batch"], step["token_count"], step.get("cos_cache"),
+                       step.get("sin_cache"), stream)
+
+    def set_option(self, option, value):
+        pa_set_option(self.handle, option, value)
+
+    def device_error(self) -> int:
+        return pa_check_device_error(self.handle)
+
+    def kernel_time_ms(self, stage) -> float:
+        return pa_kernel_time_ms(self.handle, stage)
+
+    def last_launch_count(self) -> int:
+        return pa_last_launch_count(self.handle)
+
+    def close(self):
+        if self.handle is not None:
+            pa_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

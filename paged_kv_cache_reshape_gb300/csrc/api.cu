@@ -1,0 +1,645 @@
+// Host side of the C ABI: validation, static planning, workspace, tensor
+// maps and the launch sequence of one step.  Nothing here reads a device
+// length: every per-step quantity is derived by the work-list kernel on the
+// GPU, and the host only sizes launches and workspaces from the handle's
+// static capacities ("PagedAttention - CUDA Design Document", section 4.7).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/pa.h"
+#include "step.h"
+
+namespace {
+
+thread_local std::string g_last_msg = "no error";
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+void set_msg(char* msg, size_t len, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_msg = buf;
+  if (msg && len) {
+    strncpy(msg, buf, len - 1);
+    msg[len - 1] = 0;
+  }
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int rot_dim_of(const pa_config& c) {
+  if (!c.do_rotary) return 0;
+  return c.rotary_dim > 0 ? c.rotary_dim : c.head_size;
+}
+
+}  // namespace
+
+struct pa_handle_s {
+  pa_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int G = 1, R = 0;
+  float scale = 0.f;
+  int max_q = 0, max_kv = 0;
+  int dec_ctas_per_sm = 1, dec_grid = 1;
+  size_t dec_smem = 0;
+  int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
+  int prefill_tile_tokens = 1, pre_grid = 1, comb_grid = 1;
+  size_t pre_smem = 0;
+  bool prefill_ready = false;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  pa::SeqInfo* seq = nullptr;
+  int2* dec_items = nullptr;
+  int2* pre_tiles = nullptr;
+  int2* comb_rows = nullptr;
+  pa::Counters* counters = nullptr;
+  int* err = nullptr;
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  __half* q_rot = nullptr;
+  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = pa::kDecodeRows;
+  cudaEvent_t ev[PA_NUM_STAGES][2] = {};
+  bool stage_ran[PA_NUM_STAGES] = {};
+  cudaStream_t last_stream = nullptr;
+  int last_launches = 0;
+  std::string msg = "no error";
+};
+
+namespace {
+
+pa_status fail(pa_handle h, pa_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_msg = buf;
+  if (h) h->msg = buf;
+  return st;
+}
+
+pa_status cuda_fail(pa_handle h, cudaError_t e, const char* what) {
+  return fail(h, PA_CUDA_ERROR, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// 3-D view {D, Hk, NB*bs} of an NHD pool (or {D, H, T} of a packed Q):
+// box {64 channels, `heads` heads, `rows` rows}, 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* base, int D, int heads_total, long long rows_total, int heads_box,
+                int rows_box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads_total, (cuuint64_t)rows_total};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads_total * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)heads_box, (cuuint32_t)rows_box};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+extern "C" {
+
+void pa_config_init(pa_config* c) {
+  if (!c) return;
+  memset(c, 0, sizeof(*c));
+  c->local_window_size = -1;
+}
+
+pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
+  if (!c) {
+    set_msg(msg, len, "config: NULL");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->num_heads <= 0) { set_msg(msg, len, "num_heads must be > 0 (got %d)", c->num_heads); return PA_INVALID_ARGUMENT; }
+  if (c->kv_num_heads <= 0) { set_msg(msg, len, "kv_num_heads must be > 0 (got %d)", c->kv_num_heads); return PA_INVALID_ARGUMENT; }
+  if (c->num_heads % c->kv_num_heads != 0) {
+    set_msg(msg, len, "num_heads %% kv_num_heads must be 0 (got %d %% %d)", c->num_heads, c->kv_num_heads);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->head_size <= 0 || c->head_size % 8 != 0) {
+    set_msg(msg, len, "head_size must be a positive multiple of 8 (got %d)", c->head_size);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (!is_pow2(c->block_size) || c->block_size < 16) {
+    set_msg(msg, len, "block_size must be a power of two >= 16 (got %d)", c->block_size);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->num_blocks <= 0) { set_msg(msg, len, "num_blocks must be > 0 (got %d)", c->num_blocks); return PA_INVALID_ARGUMENT; }
+  if ((long long)c->num_blocks * c->block_size > (1LL << 31) - 1024) {
+    set_msg(msg, len, "num_blocks * block_size must be < 2^31 (got %lld)", (long long)c->num_blocks * c->block_size);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->max_blocks_per_seq <= 0) {
+    set_msg(msg, len, "max_blocks_per_seq must be > 0 (got %d)", c->max_blocks_per_seq);
+    return PA_INVALID_ARGUMENT;
+  }
+  if ((long long)c->max_blocks_per_seq * c->block_size > (1LL << 30)) {
+    set_msg(msg, len, "max_blocks_per_seq * block_size must be <= 2^30");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (!(c->scale >= 0.f) || std::isinf(c->scale)) { set_msg(msg, len, "scale must be finite and >= 0 (got %g)", c->scale); return PA_INVALID_ARGUMENT; }
+  if (!(c->softcap >= 0.f) || std::isinf(c->softcap)) { set_msg(msg, len, "softcap must be finite and >= 0 (got %g)", c->softcap); return PA_INVALID_ARGUMENT; }
+  if (!(c->local_window_size == -1 || c->local_window_size >= 1)) {
+    set_msg(msg, len, "local_window_size must be -1 or >= 1 (got %d)", c->local_window_size);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->do_rotary != 0 && c->do_rotary != 1) { set_msg(msg, len, "do_rotary must be 0 or 1 (got %d)", c->do_rotary); return PA_INVALID_ARGUMENT; }
+  if (c->rotary_interleaved != 0 && c->rotary_interleaved != 1) {
+    set_msg(msg, len, "rotary_interleaved must be 0 or 1 (got %d)", c->rotary_interleaved);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->do_rotary) {
+    int R = rot_dim_of(*c);
+    if (R <= 0 || R % 2 != 0 || R > c->head_size) {
+      set_msg(msg, len, "rotary_dim must be even and in [2, head_size] (got %d)", R);
+      return PA_INVALID_ARGUMENT;
+    }
+    if (c->max_rotary_positions <= 0) {
+      set_msg(msg, len, "max_rotary_positions (cos_cache.shape[0]) must be > 0 with do_rotary");
+      return PA_INVALID_ARGUMENT;
+    }
+  }
+  if (c->max_batch <= 0) { set_msg(msg, len, "max_batch must be > 0 (got %d)", c->max_batch); return PA_INVALID_ARGUMENT; }
+  if (c->max_tokens <= 0) { set_msg(msg, len, "max_tokens must be > 0 (got %d)", c->max_tokens); return PA_INVALID_ARGUMENT; }
+  if (c->max_query_len_bound < 0 || c->max_kv_len_bound < 0) {
+    set_msg(msg, len, "max_query_len_bound and max_kv_len_bound must be >= 0");
+    return PA_INVALID_ARGUMENT;
+  }
+  // Valid, but outside what this build runs.
+  if (c->head_size != 64 && c->head_size != 128 && c->head_size != 256) {
+    set_msg(msg, len, "head_size %d is valid but this build runs 64, 128 and 256", c->head_size);
+    return PA_NOT_SUPPORTED;
+  }
+  if (c->num_heads / c->kv_num_heads > 128) {
+    set_msg(msg, len, "num_heads / kv_num_heads = %d > 128 is not supported", c->num_heads / c->kv_num_heads);
+    return PA_NOT_SUPPORTED;
+  }
+  if (c->do_rotary && rot_dim_of(*c) % 16 != 0) {
+    set_msg(msg, len, "rotary_dim %d is valid but this build needs a multiple of 16", rot_dim_of(*c));
+    return PA_NOT_SUPPORTED;
+  }
+  set_msg(msg, len, "ok");
+  return PA_OK;
+}
+
+pa_status pa_check_step(const pa_config* c, int for_forward, const void* query, const void* key, const void* value,
+                        const void* key_cache, const void* value_cache, const int32_t* block_table,
+                        const int32_t* cum, const int32_t* past, int batch, int token_count, const void* cos_cache,
+                        const void* sin_cache, const void* output, char* msg, size_t len) {
+  pa_status st = pa_validate_config(c, msg, len);
+  if (st != PA_OK) return st;
+  if (batch < 1 || batch > c->max_batch) {
+    set_msg(msg, len, "batch must be in [1, max_batch=%d] (got %d)", c->max_batch, batch);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (token_count < 0 || token_count > c->max_tokens) {
+    set_msg(msg, len, "token_count must be in [0, max_tokens=%d] (got %d)", c->max_tokens, token_count);
+    return PA_INVALID_ARGUMENT;
+  }
+  struct { const void* p; const char* name; int align; bool need; } args[] = {
+      {query, "query", 16, for_forward != 0 && token_count > 0},
+      {key, "key", 16, token_count > 0},
+      {value, "value", 16, token_count > 0},
+      {key_cache, "key_cache", 16, true},
+      {value_cache, "value_cache", 16, true},
+      {block_table, "block_table", 4, true},
+      {cum, "cumulative_sequence_lengths", 4, true},
+      {past, "past_sequence_lengths", 4, true},
+      {output, "output", 16, for_forward != 0 && token_count > 0},
+  };
+  for (auto& a : args) {
+    if (a.need && a.p == nullptr) {
+      set_msg(msg, len, "%s must not be NULL", a.name);
+      return PA_INVALID_ARGUMENT;
+    }
+    if (a.p && (reinterpret_cast<uintptr_t>(a.p) % a.align) != 0) {
+      set_msg(msg, len, "%s must be %d-byte aligned", a.name, a.align);
+      return PA_INVALID_ARGUMENT;
+    }
+  }
+  if (key_cache == value_cache) {
+    set_msg(msg, len, "key_cache and value_cache must be distinct buffers");
+    return PA_INVALID_ARGUMENT;
+  }
+  if ((cos_cache == nullptr) != (sin_cache == nullptr)) {
+    set_msg(msg, len, "cos_cache and sin_cache must be both present or both absent");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->do_rotary && cos_cache == nullptr) {
+    set_msg(msg, len, "cos_cache/sin_cache are required when do_rotary == 1");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (!c->do_rotary && cos_cache != nullptr) {
+    set_msg(msg, len, "cos_cache/sin_cache given but do_rotary == 0");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (cos_cache && ((reinterpret_cast<uintptr_t>(cos_cache) | reinterpret_cast<uintptr_t>(sin_cache)) % 16)) {
+    set_msg(msg, len, "cos_cache and sin_cache must be 16-byte aligned");
+    return PA_INVALID_ARGUMENT;
+  }
+  set_msg(msg, len, "ok");
+  return PA_OK;
+}
+
+pa_status pa_create(const pa_config* cfg, pa_handle* out) {
+  if (!out) return fail(nullptr, PA_INVALID_ARGUMENT, "out must not be NULL");
+  *out = nullptr;
+  char msg[512];
+  pa_status st = pa_validate_config(cfg, msg, sizeof(msg));
+  if (st != PA_OK) return fail(nullptr, st, "%s", msg);
+  pa_handle h = new pa_handle_s();
+  h->cfg = *cfg;
+  const pa_config& c = h->cfg;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaGetDevice"); }
+  e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaDeviceGetAttribute"); }
+  if (!encode_fn()) { delete h; return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled is unavailable"); }
+
+  h->G = c.num_heads / c.kv_num_heads;
+  h->R = rot_dim_of(c);
+  h->scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)c.head_size);
+  const int kv_cap = c.max_blocks_per_seq * c.block_size;
+  h->max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
+  h->max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
+
+  e = pa::decode_configure(c.head_size, &h->dec_ctas_per_sm, &h->dec_smem);
+  if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "decode kernel attributes"); }
+  size_t psmem = 0;
+  h->prefill_ready = pa::prefill_configure(c.head_size, &psmem) == cudaSuccess;
+  cudaGetLastError();
+  h->pre_smem = psmem;
+
+  h->dec_grid = h->num_sms * h->dec_ctas_per_sm;
+  h->target_pairs = std::max(1, (4 * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads);
+  h->cap_dec = h->target_pairs + c.max_batch;
+  h->prefill_tile_tokens = std::max(1, pa::kPrefillRows / h->G);
+  h->cap_pre = (c.max_tokens + h->prefill_tile_tokens - 1) / h->prefill_tile_tokens + c.max_batch;
+  h->cap_comb = c.max_tokens;
+  h->pre_grid = std::max(1, std::min(h->num_sms, h->cap_pre * c.kv_num_heads));
+  h->comb_grid = std::max(1, std::min(h->num_sms * 4, (h->cap_comb * c.num_heads + 7) / 8));
+
+  // Workspace layout (256-byte aligned pieces).
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t D = c.head_size, Hk = c.kv_num_heads;
+  size_t off = 0;
+  size_t o_err = off; off = up(off + 64);
+  size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
+  size_t o_seq = off; off = up(off + sizeof(pa::SeqInfo) * c.max_batch);
+  size_t o_dec = off; off = up(off + sizeof(int2) * h->cap_dec);
+  size_t o_pre = off; off = up(off + sizeof(int2) * h->cap_pre);
+  size_t o_cmb = off; off = up(off + sizeof(int2) * h->cap_comb);
+  size_t o_pml = off; off = up(off + sizeof(float2) * h->cap_dec * Hk * pa::kDecodeRows);
+  size_t o_po = off; off = up(off + sizeof(float) * h->cap_dec * Hk * pa::kDecodeRows * D);
+  size_t o_qr = off;
+  if (c.do_rotary) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * D);
+  h->ws_bytes = off;
+  e = cudaMalloc(&h->ws, h->ws_bytes);
+  if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaMalloc(workspace)"); }
+  e = cudaMemset(h->ws, 0, h->ws_bytes);
+  if (e != cudaSuccess) { cudaFree(h->ws); delete h; return cuda_fail(nullptr, e, "cudaMemset(workspace)"); }
+  uint8_t* w = static_cast<uint8_t*>(h->ws);
+  h->err = reinterpret_cast<int*>(w + o_err);
+  h->counters = reinterpret_cast<pa::Counters*>(w + o_cnt);
+  h->seq = reinterpret_cast<pa::SeqInfo*>(w + o_seq);
+  h->dec_items = reinterpret_cast<int2*>(w + o_dec);
+  h->pre_tiles = reinterpret_cast<int2*>(w + o_pre);
+  h->comb_rows = reinterpret_cast<int2*>(w + o_cmb);
+  h->part_ml = reinterpret_cast<float2*>(w + o_pml);
+  h->part_o = reinterpret_cast<float*>(w + o_po);
+  h->q_rot = c.do_rotary ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
+  for (int i = 0; i < PA_NUM_STAGES; ++i)
+    for (int j = 0; j < 2; ++j) cudaEventCreate(&h->ev[i][j]);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) { pa_destroy(h); return cuda_fail(nullptr, e, "pa_create"); }
+  *out = h;
+  return PA_OK;
+}
+
+pa_status pa_destroy(pa_handle h) {
+  if (!h) return PA_OK;
+  DeviceGuard g(h->device);
+  for (int i = 0; i < PA_NUM_STAGES; ++i)
+    for (int j = 0; j < 2; ++j)
+      if (h->ev[i][j]) cudaEventDestroy(h->ev[i][j]);
+  if (h->ws) cudaFree(h->ws);
+  delete h;
+  return PA_OK;
+}
+
+const char* pa_last_error_message(pa_handle h) { return h ? h->msg.c_str() : g_last_msg.c_str(); }
+
+pa_status pa_set_option(pa_handle h, int option, int value) {
+  if (!h) return fail(nullptr, PA_INVALID_ARGUMENT, "handle must not be NULL");
+  switch (option) {
+    case PA_OPT_SPLIT_KEYS: {
+      if (value < 0 || value % pa::kStageKeys != 0)
+        return fail(h, PA_INVALID_ARGUMENT, "split keys must be 0 or a positive multiple of %d", pa::kStageKeys);
+      if (value > 0) {
+        long long need = (long long)h->cfg.max_batch * ((h->max_kv + value - 1) / value + 1);
+        if (need > h->cap_dec)
+          return fail(h, PA_INVALID_ARGUMENT,
+                      "split keys %d could need %lld decode items; the workspace holds %d", value, need, h->cap_dec);
+      }
+      h->opt_split_keys = value;
+      return PA_OK;
+    }
+    case PA_OPT_NO_WINDOW_PRUNE: h->opt_no_prune = value != 0; return PA_OK;
+    case PA_OPT_KERNEL_TIMING: h->opt_timing = value != 0; return PA_OK;
+    case PA_OPT_DECODE_MAX_ROWS:
+      if (value < 0 || value > pa::kDecodeRows)
+        return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", pa::kDecodeRows);
+      h->opt_dec_rows = value;
+      return PA_OK;
+    default: return fail(h, PA_INVALID_ARGUMENT, "unknown option %d", option);
+  }
+}
+
+int pa_last_launch_count(pa_handle h) { return h ? h->last_launches : 0; }
+
+pa_status pa_kernel_time_ms(pa_handle h, int stage, float* ms) {
+  if (!h || !ms || stage < 0 || stage >= PA_NUM_STAGES) return fail(h, PA_INVALID_ARGUMENT, "bad arguments");
+  *ms = -1.f;
+  if (!h->opt_timing || !h->stage_ran[stage]) return PA_OK;
+  DeviceGuard g(h->device);
+  cudaError_t e = cudaEventSynchronize(h->ev[stage][1]);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventSynchronize");
+  e = cudaEventElapsedTime(ms, h->ev[stage][0], h->ev[stage][1]);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaEventElapsedTime");
+  return PA_OK;
+}
+
+pa_status pa_check_device_error(pa_handle h, int* code) {
+  if (!h || !code) return fail(h, PA_INVALID_ARGUMENT, "bad arguments");
+  DeviceGuard g(h->device);
+  cudaError_t e = cudaStreamSynchronize(h->last_stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpy(error word)");
+  e = cudaMemset(h->err, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemset(error word)");
+  *code = v;
+  if (v) return fail(h, PA_DEVICE_DATA_ERROR, "device data error bits 0x%x", v);
+  return PA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct StageTimer {
+  pa_handle h;
+  int stage;
+  cudaStream_t s;
+  StageTimer(pa_handle h_, int st, cudaStream_t s_) : h(h_), stage(st), s(s_) {
+    if (h->opt_timing) cudaEventRecord(h->ev[stage][0], s);
+  }
+  ~StageTimer() {
+    if (h->opt_timing) {
+      cudaEventRecord(h->ev[stage][1], s);
+      h->stage_ran[stage] = true;
+    }
+  }
+};
+
+pa_status run_cache_write(pa_handle h, const void* query, const void* key, const void* value, void* key_cache,
+                          void* value_cache, const int32_t* block_table, const int32_t* cum, const int32_t* past,
+                          int batch, int token_count, const void* cos_cache, const void* sin_cache,
+                          cudaStream_t s) {
+  const pa_config& c = h->cfg;
+  pa::CacheWriteParams p{};
+  p.key = static_cast<const __half*>(key);
+  p.value = static_cast<const __half*>(value);
+  p.query = static_cast<const __half*>(query);
+  p.q_rot = (query && c.do_rotary) ? h->q_rot : nullptr;
+  p.key_cache = static_cast<__half*>(key_cache);
+  p.value_cache = static_cast<__half*>(value_cache);
+  p.block_table = block_table;
+  p.cum = cum;
+  p.past = past;
+  p.cos_cache = static_cast<const __half*>(cos_cache);
+  p.sin_cache = static_cast<const __half*>(sin_cache);
+  p.batch = batch;
+  p.token_count = token_count;
+  p.H = c.num_heads;
+  p.Hk = c.kv_num_heads;
+  p.D = c.head_size;
+  p.bs = c.block_size;
+  p.NB = c.num_blocks;
+  p.MB = c.max_blocks_per_seq;
+  p.rotary = c.do_rotary;
+  p.interleaved = c.rotary_interleaved;
+  p.rot_dim = h->R;
+  p.rot_positions = c.max_rotary_positions;
+  p.err = h->err;
+  StageTimer t(h, PA_STAGE_CACHE_WRITE, s);
+  cudaError_t e = pa::launch_cache_write(p, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cache write launch");
+  h->last_launches++;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_cache_write(pa_handle h, const void* key, const void* value, void* key_cache, void* value_cache,
+                         const int32_t* block_table, const int32_t* cum, const int32_t* past, int batch,
+                         int token_count, const void* cos_cache, const void* sin_cache, void* stream) {
+  if (!h) return fail(nullptr, PA_INVALID_ARGUMENT, "handle must not be NULL");
+  char msg[512];
+  pa_status st = pa_check_step(&h->cfg, 0, nullptr, key, value, key_cache, value_cache, block_table, cum, past,
+                               batch, token_count, cos_cache, sin_cache, nullptr, msg, sizeof(msg));
+  if (st != PA_OK) return fail(h, st, "%s", msg);
+  h->last_launches = 0;
+  for (bool& r : h->stage_ran) r = false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->last_stream = s;
+  if (token_count == 0) return PA_OK;
+  DeviceGuard g(h->device);
+  return run_cache_write(h, nullptr, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
+                         cos_cache, sin_cache, s);
+}
+
+pa_status pa_forward(pa_handle h, const void* query, const void* key, const void* value, void* key_cache,
+                     void* value_cache, const int32_t* block_table, const int32_t* cum, const int32_t* past,
+                     int batch, int token_count, const void* cos_cache, const void* sin_cache, void* output,
+                     void* stream) {
+  if (!h) return fail(nullptr, PA_INVALID_ARGUMENT, "handle must not be NULL");
+  char msg[512];
+  pa_status st = pa_check_step(&h->cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
+                               token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
+  if (st != PA_OK) return fail(h, st, "%s", msg);
+  h->last_launches = 0;
+  for (bool& r : h->stage_ran) r = false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->last_stream = s;
+  if (token_count == 0) return PA_OK;  // empty step: nothing to launch
+  DeviceGuard g(h->device);
+  const pa_config& c = h->cfg;
+  const int D = c.head_size;
+  const int pool_rows = c.num_blocks * c.block_size;
+  const int box_rows = std::min(c.block_size, pa::kStageKeys);
+
+  CUtensorMap tk, tv;
+  if (!encode_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, 1, box_rows) ||
+      !encode_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, 1, box_rows))
+    return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
+
+  // 1. work list
+  {
+    pa::WorklistParams p{};
+    p.cum = cum;
+    p.past = past;
+    p.batch = batch;
+    p.token_count = token_count;
+    p.group = h->G;
+    p.max_q = h->max_q;
+    p.max_kv = h->max_kv;
+    p.window = c.local_window_size;
+    p.prune = h->opt_no_prune ? 0 : 1;
+    p.dec_max_rows = h->opt_dec_rows;
+    p.prefill_tile_tokens = h->prefill_tile_tokens;
+    p.split_keys_fixed = h->opt_split_keys;
+    p.target_pairs = h->target_pairs;
+    p.cap_dec = h->cap_dec;
+    p.cap_pre = h->cap_pre;
+    p.cap_comb = h->cap_comb;
+    p.seq = h->seq;
+    p.dec_items = h->dec_items;
+    p.pre_tiles = h->pre_tiles;
+    p.comb_rows = h->comb_rows;
+    p.counters = h->counters;
+    p.err = h->err;
+    StageTimer t(h, PA_STAGE_WORKLIST, s);
+    cudaError_t e = pa::launch_worklist(p, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "work-list launch");
+    h->last_launches++;
+  }
+  // 2. rotary + cache write
+  st = run_cache_write(h, query, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
+                       cos_cache, sin_cache, s);
+  if (st != PA_OK) return st;
+  const __half* q_att = c.do_rotary ? h->q_rot : static_cast<const __half*>(query);
+  // 3. split-KV decode
+  {
+    pa::DecodeParams p{};
+    p.q = q_att;
+    p.out = static_cast<__half*>(output);
+    p.block_table = block_table;
+    p.seq = h->seq;
+    p.dec_items = h->dec_items;
+    p.counters = h->counters;
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.err = h->err;
+    p.H = c.num_heads;
+    p.Hk = c.kv_num_heads;
+    p.G = h->G;
+    p.bs = c.block_size;
+    p.MB = c.max_blocks_per_seq;
+    p.NB = c.num_blocks;
+    p.scale = h->scale;
+    p.softcap = c.softcap;
+    p.window = c.local_window_size;
+    p.oob_row = pool_rows;
+    StageTimer t(h, PA_STAGE_DECODE, s);
+    cudaError_t e = pa::launch_decode(D, tk, tv, p, h->dec_grid, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
+    h->last_launches++;
+  }
+  // 4. varlen prefill on tensor memory
+  if (h->prefill_ready) {
+    CUtensorMap tq, tkp, tvp;
+    const int prow = std::min(c.block_size, pa::kPrefillKeys);
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_tile_tokens) ||
+        !encode_map(&tkp, key_cache, D, c.kv_num_heads, pool_rows, 1, prow) ||
+        !encode_map(&tvp, value_cache, D, c.kv_num_heads, pool_rows, 1, prow))
+      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
+    pa::PrefillParams p{};
+    p.out = static_cast<__half*>(output);
+    p.block_table = block_table;
+    p.seq = h->seq;
+    p.pre_tiles = h->pre_tiles;
+    p.counters = h->counters;
+    p.err = h->err;
+    p.H = c.num_heads;
+    p.Hk = c.kv_num_heads;
+    p.G = h->G;
+    p.bs = c.block_size;
+    p.MB = c.max_blocks_per_seq;
+    p.NB = c.num_blocks;
+    p.tile_tokens = h->prefill_tile_tokens;
+    p.scale = h->scale;
+    p.softcap = c.softcap;
+    p.window = c.local_window_size;
+    p.oob_row = pool_rows;
+    StageTimer t(h, PA_STAGE_PREFILL, s);
+    cudaError_t e = pa::launch_prefill(D, tq, tkp, tvp, p, h->pre_grid, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
+    h->last_launches++;
+  }
+  // 5. log-sum-exp combine of split partials
+  {
+    pa::CombineParams p{};
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.seq = h->seq;
+    p.comb_rows = h->comb_rows;
+    p.counters = h->counters;
+    p.out = static_cast<__half*>(output);
+    p.H = c.num_heads;
+    p.Hk = c.kv_num_heads;
+    p.G = h->G;
+    p.D = D;
+    StageTimer t(h, PA_STAGE_COMBINE, s);
+    cudaError_t e = pa::launch_combine(p, h->comb_grid, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->last_launches++;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,168 @@
+// Rotary + reshape_and_cache: one warp per packed token.
+//
+// Slot derivation is the derived-slot rule of "PagedAttention - CUDA Design
+// Document", section 5.1 (owner sequence by binary search over
+// cumulative_sequence_lengths, guarded against rows past cum[B] as section
+// 18.2 asks; position past_b + j; block_table row position / block_size).
+// A -1 block entry means "not mapped" (section 9.3.1): nothing is written.
+// K is rotated before it is stored (section 7.2 / 12.5: the cache holds the
+// already-rotated K); Q is rotated into a workspace for the attention kernels.
+//
+// Rotary arithmetic is fixed so the pool is bit-reproducible: per pair,
+//   y1 = rn(rn(x1*c) - rn(x2*s)),  y2 = rn(rn(x2*c) + rn(x1*s))
+// in fp32 (no fused multiply-add), then fp16 round-to-nearest-even.
+//
+// Every row moves as 16-byte vectors: the NHD pool stores a token's
+// [Hk, D] slice contiguously, so a warp writes one contiguous run of
+// Hk*D*2 bytes per tensor (fully coalesced).
+#include "step.h"
+#include "../../include/pa.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarpsPerBlock = 4;
+
+__device__ __forceinline__ void rotate_pair(__half x1, __half x2, __half c, __half s, __half& y1,
+                                            __half& y2) {
+  float fx1 = __half2float(x1), fx2 = __half2float(x2);
+  float fc = __half2float(c), fs = __half2float(s);
+  float a = __fsub_rn(__fmul_rn(fx1, fc), __fmul_rn(fx2, fs));
+  float b = __fadd_rn(__fmul_rn(fx2, fc), __fmul_rn(fx1, fs));
+  y1 = __float2half_rn(a);
+  y2 = __float2half_rn(b);
+}
+
+union Vec8 {
+  uint4 u;
+  __half h[8];
+};
+
+// Copies (rotate = false) or rotates one [nheads, D] row from src to dst.
+// R % 16 == 0 is checked on the host.
+__device__ void row_transform(const __half* __restrict__ src, __half* __restrict__ dst, int nheads,
+                              int D, bool rotate, int R, int interleaved, const __half* cos_row,
+                              const __half* sin_row, int lane) {
+  const int chunks_per_head = D / 8;
+  if (!rotate) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = __ldg(s4 + i);
+    return;
+  }
+  const int half = R / 2;
+  if (!interleaved) {
+    // Pair chunks: channels [8c, 8c+8) with [half + 8c, half + 8c + 8).
+    const int pairs = half / 8;
+    const int copies = (D - R) / 8;
+    const int per_head = pairs + copies;
+    for (int i = lane; i < nheads * per_head; i += 32) {
+      int h = i / per_head, c = i % per_head;
+      const __half* sh = src + (size_t)h * D;
+      __half* dh = dst + (size_t)h * D;
+      if (c < pairs) {
+        Vec8 a, b, cs, sn, ya, yb;
+        a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
+        b.u = __ldg(reinterpret_cast<const uint4*>(sh + half + 8 * c));
+        cs.u = __ldg(reinterpret_cast<const uint4*>(cos_row + 8 * c));
+        sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
+#pragma unroll
+        for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e]);
+        *reinterpret_cast<uint4*>(dh + 8 * c) = ya.u;
+        *reinterpret_cast<uint4*>(dh + half + 8 * c) = yb.u;
+      } else {
+        int ch = R + 8 * (c - pairs);
+        *reinterpret_cast<uint4*>(dh + ch) = __ldg(reinterpret_cast<const uint4*>(sh + ch));
+      }
+    }
+  } else {
+    // Each 8-channel chunk below R holds four (2i, 2i+1) pairs.
+    const int rchunks = R / 8;
+    for (int i = lane; i < nheads * chunks_per_head; i += 32) {
+      int h = i / chunks_per_head, c = i % chunks_per_head;
+      const __half* sh = src + (size_t)h * D;
+      __half* dh = dst + (size_t)h * D;
+      Vec8 a, y;
+      a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
+      if (c < rchunks) {
+        uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * c));
+        uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * c));
+        const __half* cv = reinterpret_cast<const __half*>(&cu);
+        const __half* sv = reinterpret_cast<const __half*>(&su);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          rotate_pair(a.h[2 * e], a.h[2 * e + 1], cv[e], sv[e], y.h[2 * e], y.h[2 * e + 1]);
+      } else {
+        y.u = a.u;
+      }
+      *reinterpret_cast<uint4*>(dh + 8 * c) = y.u;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheWriteParams p) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= p.token_count) return;
+  // Owner sequence: largest b with cum[b] <= t.
+  int lo = 0, hi = p.batch;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(p.cum + mid) <= t) lo = mid;
+    else hi = mid;
+  }
+  const int b = lo;
+  const int c0 = __ldg(p.cum + b), c1 = __ldg(p.cum + b + 1);
+  const int past = __ldg(p.past + b);
+  if (t < c0 || t >= c1 || c0 < 0) {
+    if (lane == 0) atomicOr(p.err, PA_DEVERR_CUM);
+    return;
+  }
+  if (past < 0) {
+    if (lane == 0) atomicOr(p.err, PA_DEVERR_PAST);
+    return;
+  }
+  const int pos = past + (t - c0);
+  bool rotate = p.rotary != 0;
+  if (rotate && pos >= p.rot_positions) {
+    if (lane == 0) atomicOr(p.err, PA_DEVERR_ROTARY_POS);
+    rotate = false;  // never read past the tables
+  }
+  const int half = p.rot_dim / 2;
+  const __half* cos_row = rotate ? p.cos_cache + (size_t)pos * half : nullptr;
+  const __half* sin_row = rotate ? p.sin_cache + (size_t)pos * half : nullptr;
+
+  if (p.query != nullptr && p.q_rot != nullptr) {
+    const size_t qoff = (size_t)t * p.H * p.D;
+    row_transform(p.query + qoff, p.q_rot + qoff, p.H, p.D, rotate, p.rot_dim, p.interleaved, cos_row,
+                  sin_row, lane);
+  }
+
+  const int row = pos / p.bs;
+  if (row >= p.MB) {
+    if (lane == 0) atomicOr(p.err, PA_DEVERR_KV_BOUND);
+    return;
+  }
+  const int blk = __ldg(p.block_table + (size_t)b * p.MB + row);
+  if (blk == -1) return;  // not mapped: no write
+  if (blk < -1 || blk >= p.NB) {
+    if (lane == 0) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+    return;
+  }
+  const size_t slot = (size_t)blk * p.bs + (pos & (p.bs - 1));
+  const size_t kv_row = (size_t)p.Hk * p.D;
+  row_transform(p.key + (size_t)t * kv_row, p.key_cache + slot * kv_row, p.Hk, p.D, rotate,
+                p.rot_dim, p.interleaved, cos_row, sin_row, lane);
+  row_transform(p.value + (size_t)t * kv_row, p.value_cache + slot * kv_row, p.Hk, p.D, false, 0, 0,
+                nullptr, nullptr, lane);
+}
+
+}  // namespace
+
+cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s) {
+  int blocks = (p.token_count + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  cache_write_kernel<<<blocks, kWarpsPerBlock * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,88 @@
+// Log-sum-exp merge of split-KV partials (flash decoding phase 2):
+//   M = max_s m_s,  out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s
+// with O_s the unnormalised partial output and l_s its softmax sum, skipping
+// empty splits (l_s = 0, m_s = -inf).  This is the merge of the CPU GQA notes
+// (onnxruntime 1.27.0 docs, contrib_ops/cpu/gqa, "Flash Decoding" phase 2)
+// and of PagedDecodeReduce ("PagedAttention - CUDA Design Document", section
+// 8 implementation note P5).  Maxima are kept in log2 units by the decode
+// kernel, hence base-2 exponentials.  A row whose splits are all empty
+// outputs 0.
+//
+// One warp per (packed row, query head); the work list holds only the rows
+// of sequences that were split, so the grid is a small persistent one.
+#include "step.h"
+
+namespace pa {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
+  constexpr int kPer = D / 32;  // channels per lane
+  const int lane = threadIdx.x & 31;
+  const int n = p.counters->n_comb * p.H;
+  for (int idx = blockIdx.x * kWarps + (threadIdx.x >> 5); idx < n; idx += gridDim.x * kWarps) {
+    const int ci = idx / p.H, h = idx - ci * p.H;
+    const int2 tb = p.comb_rows[ci];
+    const SeqInfo si = p.seq[tb.y];
+    const int j = tb.x - si.t0;
+    const int k = h / p.G, g = h - k * p.G;
+    const int r = j * p.G + g;
+    const int ns = si.dec_count;
+    // global max over splits
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) {
+      const size_t row = ((size_t)(si.dec_first + s) * p.Hk + k) * kDecodeRows + r;
+      M = fmaxf(M, p.part_ml[row].x);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    float den = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < ns; ++s) {
+        const size_t row = ((size_t)(si.dec_first + s) * p.Hk + k) * kDecodeRows + r;
+        const float2 ml = p.part_ml[row];
+        if (ml.y == 0.f) continue;  // empty split
+        const float f = exp2f(ml.x - M);
+        den += f * ml.y;
+        const float* po = p.part_o + row * D + lane * kPer;
+        if constexpr (kPer == 8) {
+          const float4 a = *reinterpret_cast<const float4*>(po);
+          const float4 b = *reinterpret_cast<const float4*>(po + 4);
+          acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+          acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
+        } else if constexpr (kPer == 4) {
+          const float4 a = *reinterpret_cast<const float4*>(po);
+          acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < kPer; ++i) acc[i] += f * po[i];
+        }
+      }
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    __half* out = p.out + ((size_t)tb.x * p.H + h) * D + lane * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; i += 2) {
+      *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s) {
+  switch (p.D) {
+    case 64: combine_kernel<64><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 128: combine_kernel<128><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 256: combine_kernel<256><<<grid, kWarps * 32, 0, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

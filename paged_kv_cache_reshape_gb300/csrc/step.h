@@ -1,0 +1,133 @@
+// Internal structures shared by the host planner and the step kernels.
+// Everything per-step that depends on device-resident lengths lives in the
+// work list written by the work-list kernel; the host only sizes launches
+// from static capacities ("PagedAttention - CUDA Design Document",
+// section 4.7, replay-invariance rule).
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kStageKeys = 64;      // keys per decode pipeline stage
+constexpr int kDecodeRows = 16;     // query rows (token x group head) per decode item
+constexpr int kDecodeWarps = 4;     // consumer warps of the decode kernel
+constexpr int kPrefillRows = 128;   // query rows per prefill tile (UMMA M)
+constexpr int kPrefillKeys = 128;   // keys per prefill KV tile (UMMA N of S)
+
+enum Route { kRouteNone = 0, kRouteDecode = 1, kRoutePrefill = 2 };
+
+// Per-sequence facts derived on the device each step.
+struct SeqInfo {
+  int q_len;      // new tokens (0 when the sequence is skipped)
+  int kv_len;     // past + q_len
+  int lo;         // first key position walked (64-aligned window start or 0)
+  int t0;         // first packed row (cum[b])
+  int dec_first;  // first decode item of this sequence
+  int dec_count;  // decode splits (0 unless routed to decode)
+  int pre_first;  // first prefill tile of this sequence
+  int pre_count;  // prefill query tiles (0 unless routed to prefill)
+};
+
+struct Counters {
+  int n_dec;       // decode items (b, split) pairs
+  int n_pre;       // prefill tiles (b, query tile)
+  int n_comb;      // packed rows whose splits need the log-sum-exp merge
+  int split_keys;  // keys per decode split this step
+};
+
+struct WorklistParams {
+  const int* cum;
+  const int* past;
+  int batch, token_count;
+  int group;               // G = H / Hk
+  int max_q, max_kv;       // trusted bounds (already clamped to static limits)
+  int window;              // -1 or >= 1
+  int prune;               // 1: start the walk at the window (block pruning)
+  int dec_max_rows;        // decode route iff q_len * G <= this
+  int prefill_tile_tokens; // tokens per prefill tile
+  int split_keys_fixed;    // > 0 forces keys per split
+  int target_pairs;        // desired number of decode (b, split) items
+  int cap_dec, cap_pre, cap_comb;
+  SeqInfo* seq;
+  int2* dec_items;  // (b, split)
+  int2* pre_tiles;  // (b, tile)
+  int2* comb_rows;  // (t, b)
+  Counters* counters;
+  int* err;
+};
+
+struct CacheWriteParams {
+  const __half* key;    // [T, Hk*D]
+  const __half* value;  // [T, Hk*D]
+  const __half* query;  // [T, H*D] or null (cache write only)
+  __half* q_rot;        // [T, H*D] rotated query (when rotary and query given)
+  __half* key_cache;
+  __half* value_cache;
+  const int* block_table;
+  const int* cum;
+  const int* past;
+  const __half* cos_cache;  // [P, R/2]
+  const __half* sin_cache;
+  int batch, token_count;
+  int H, Hk, D, bs, NB, MB;
+  int rotary, interleaved, rot_dim, rot_positions;
+  int* err;
+};
+
+struct DecodeParams {
+  const __half* q;  // [T, H*D]
+  __half* out;      // [T, H*D]
+  const int* block_table;
+  const SeqInfo* seq;
+  const int2* dec_items;
+  const Counters* counters;
+  float* part_o;    // [items*Hk*16*D]
+  float2* part_ml;  // [items*Hk*16] (max in log2 units, sum)
+  int* err;
+  int H, Hk, G, bs, MB, NB;
+  float scale;       // softmax scale
+  float softcap;     // 0 = off
+  int window;        // -1 or >= 1
+  int oob_row;       // a TMA row coordinate past the pool (zero fill)
+};
+
+struct CombineParams {
+  const float* part_o;
+  const float2* part_ml;
+  const SeqInfo* seq;
+  const int2* comb_rows;
+  const Counters* counters;
+  __half* out;
+  int H, Hk, G, D;
+};
+
+struct PrefillParams {
+  __half* out;
+  const int* block_table;
+  const SeqInfo* seq;
+  const int2* pre_tiles;
+  const Counters* counters;
+  int* err;
+  int H, Hk, G, bs, MB, NB;
+  int tile_tokens;  // tokens per query tile (rows = tile_tokens * G <= 128)
+  float scale;
+  float softcap;
+  int window;
+  int oob_row;
+};
+
+// Launchers (defined in the .cu files).
+cudaError_t launch_worklist(const WorklistParams& p, cudaStream_t s);
+cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s);
+cudaError_t decode_configure(int head_size, int* ctas_per_sm, size_t* smem);
+cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const DecodeParams& p, int grid, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
+cudaError_t prefill_configure(int head_size, size_t* smem);
+cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
+
+}  // namespace pa

@@ -1,0 +1,82 @@
+"""Helpers shared by the GPU parity tests: run one step through the C ABI
+and compare it with the CPU oracle."""
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_reshape_gb300 as pa
+import workloads
+
+RTOL, ATOL = 1e-2, 2e-3   # |gpu - oracle| <= ATOL + RTOL * |oracle|
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def ensure_built():
+    from paged_kv_cache_reshape_gb300 import builder as build
+    build.build()
+
+
+def make(shape, device="cuda", gen_device=None):
+    return workloads.make_step(shape, device=device, gen_device=gen_device)
+
+
+def host_copy(step):
+    """CPU copy of every tensor of a step (the oracle's inputs)."""
+    return {k: (v.detach().cpu().clone() if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
+
+
+def run(step, options=(), max_batch=None, max_tokens=None, **bounds):
+    """pa_forward on `step` (device tensors, pools updated in place)."""
+    ensure_built()
+    op = pa.PagedAttention.for_step(step, max_batch=max_batch, max_tokens=max_tokens, **bounds)
+    for k, v in options:
+        op.set_option(k, v)
+    out = torch.full_like(step["query"], float("nan"))
+    op.forward(step, out)
+    torch.cuda.synchronize()
+    err = op.device_error()
+    return op, out, err
+
+
+def assert_close(got, ref, what="output"):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape
+    assert not np.isnan(got).any(), f"{what}: NaN in GPU result"
+    diff = np.abs(got - ref)
+    bad = diff > ATOL + RTOL * np.abs(ref)
+    big = np.abs(ref) >= 1e-3
+    rel = (diff[big] / np.abs(ref[big])).max() if big.any() else 0.0
+    assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements outside tolerance; "
+                           f"max abs {diff.max():.3g}, max rel {rel:.3g}")
+    return diff.max(), rel
+
+
+def check_full(step_host, step_dev, out, threads=8):
+    """Whole-step parity: both pools bit-exact, every output row within tolerance."""
+    ref = oracle.forward(step_host, threads=threads)
+    assert np.array_equal(bits(step_dev["key_cache"]), ref["key_cache"]), "key_cache pool differs"
+    assert np.array_equal(bits(step_dev["value_cache"]), ref["value_cache"]), "value_cache pool differs"
+    T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
+    return assert_close(out.float().cpu().numpy().reshape(T, H, D), ref["out"])
+
+
+def check_sampled(step_host, step_dev, out, n_rows=192, seed=0, threads=16):
+    """Large-step parity: pools bit-exact, a seeded sample of (t, h) rows."""
+    ref = oracle.forward(step_host, threads=threads, rows=np.zeros(0, dtype=np.int64))
+    assert np.array_equal(bits(step_dev["key_cache"]), ref["key_cache"]), "key_cache pool differs"
+    assert np.array_equal(bits(step_dev["value_cache"]), ref["value_cache"]), "value_cache pool differs"
+    T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.integers(0, T * H, n_rows), [0, T * H - 1]]))
+    o = oracle.attention(ref["query_rot"], ref["key_cache"], ref["value_cache"],
+                         step_host["block_table"], step_host["cumulative_sequence_lengths"],
+                         step_host["past_sequence_lengths"], H, step_host["kv_num_heads"], D,
+                         step_host["block_size"], step_host["scale"], step_host["softcap"],
+                         step_host["local_window_size"], rows=rows, threads=threads)
+    got = out.float().cpu().numpy().reshape(T * H, D)[rows]
+    return assert_close(got, o)

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point include/pa.h declares, and rejects each
+invalid configuration / step with a message naming the argument (one test
+per validation rule, "PagedAttention - CUDA Design Document" sections 15
+and 17.5)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_reshape_gb300 as pa
+from paged_kv_cache_reshape_gb300 import builder as pabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pabuild.build()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    return sorted(set(re.findall(r"^PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_binding_names():
+    assert declared_symbols() == sorted(pa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    L = ctypes.CDLL(pa.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def good(**over):
+    c = pa.make_config(32, 8, 128, 16, 1000, 257, 64, 64)
+    for k, v in over.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_valid_config_passes():
+    assert pa.pa_validate_config(good()) == (pa.PA_OK, "ok")
+
+
+@pytest.mark.parametrize("field,value,status,word", [
+    ("num_heads", 0, pa.PA_INVALID_ARGUMENT, "num_heads"),
+    ("kv_num_heads", 0, pa.PA_INVALID_ARGUMENT, "kv_num_heads"),
+    ("num_heads", 30, pa.PA_INVALID_ARGUMENT, "num_heads % kv_num_heads"),
+    ("head_size", 100, pa.PA_INVALID_ARGUMENT, "head_size"),
+    ("block_size", 8, pa.PA_INVALID_ARGUMENT, "block_size"),
+    ("block_size", 48, pa.PA_INVALID_ARGUMENT, "block_size"),
+    ("num_blocks", 0, pa.PA_INVALID_ARGUMENT, "num_blocks"),
+    ("max_blocks_per_seq", 0, pa.PA_INVALID_ARGUMENT, "max_blocks_per_seq"),
+    ("scale", -1.0, pa.PA_INVALID_ARGUMENT, "scale"),
+    ("softcap", -0.5, pa.PA_INVALID_ARGUMENT, "softcap"),
+    ("local_window_size", 0, pa.PA_INVALID_ARGUMENT, "local_window_size"),
+    ("local_window_size", -2, pa.PA_INVALID_ARGUMENT, "local_window_size"),
+    ("do_rotary", 2, pa.PA_INVALID_ARGUMENT, "do_rotary"),
+    ("rotary_interleaved", 3, pa.PA_INVALID_ARGUMENT, "rotary_interleaved"),
+    ("max_batch", 0, pa.PA_INVALID_ARGUMENT, "max_batch"),
+    ("max_tokens", 0, pa.PA_INVALID_ARGUMENT, "max_tokens"),
+    ("max_kv_len_bound", -1, pa.PA_INVALID_ARGUMENT, "max_kv_len_bound"),
+    ("head_size", 96, pa.PA_NOT_SUPPORTED, "head_size"),
+])
+def test_config_rule(field, value, status, word):
+    st, msg = pa.pa_validate_config(good(**{field: value}))
+    assert st == status and word in msg, (st, msg)
+
+
+def test_rotary_rules():
+    st, msg = pa.pa_validate_config(good(do_rotary=1, max_rotary_positions=0))
+    assert st == pa.PA_INVALID_ARGUMENT and "max_rotary_positions" in msg
+    st, msg = pa.pa_validate_config(good(do_rotary=1, max_rotary_positions=100, rotary_dim=130))
+    assert st == pa.PA_INVALID_ARGUMENT and "rotary_dim" in msg
+    st, msg = pa.pa_validate_config(good(do_rotary=1, max_rotary_positions=100, rotary_dim=24))
+    assert st == pa.PA_NOT_SUPPORTED and "rotary_dim" in msg
+    assert pa.pa_validate_config(good(do_rotary=1, max_rotary_positions=100))[0] == pa.PA_OK
+
+
+A = 1 << 20  # a fake, suitably aligned "device address" (never dereferenced)
+
+
+def step_args(**over):
+    d = dict(for_forward=1, query=A, key=A + 4096, value=A + 8192, key_cache=A + 16384,
+             value_cache=A + 32768, block_table=A + 65536, cumulative_sequence_lengths=A + 70000,
+             past_sequence_lengths=A + 80000, batch=4, token_count=4, cos_cache=None,
+             sin_cache=None, output=A + 90000)
+    d.update(over)
+    return d
+
+
+def check(cfg=None, **over):
+    return pa.pa_check_step(cfg or good(), **step_args(**over))
+
+
+def test_valid_step_passes():
+    assert check() == (pa.PA_OK, "ok")
+
+
+@pytest.mark.parametrize("over,word", [
+    (dict(batch=0), "batch"),
+    (dict(batch=65), "batch"),
+    (dict(token_count=-1), "token_count"),
+    (dict(token_count=65), "token_count"),
+    (dict(query=None), "query"),
+    (dict(output=None), "output"),
+    (dict(key=None), "key"),
+    (dict(value=None), "value"),
+    (dict(key_cache=None), "key_cache"),
+    (dict(block_table=None), "block_table"),
+    (dict(cumulative_sequence_lengths=None), "cumulative_sequence_lengths"),
+    (dict(past_sequence_lengths=None), "past_sequence_lengths"),
+    (dict(query=A + 2), "aligned"),
+    (dict(value_cache=A + 16384), "distinct"),
+    (dict(cos_cache=A + 100000), "both present"),
+    (dict(cos_cache=A + 100000, sin_cache=A + 110000), "do_rotary == 0"),
+])
+def test_step_rule(over, word):
+    st, msg = check(**over)
+    assert st == pa.PA_INVALID_ARGUMENT and word in msg, (st, msg)
+
+
+def test_rotary_tables_required():
+    cfg = good(do_rotary=1, max_rotary_positions=100)
+    st, msg = check(cfg)
+    assert st == pa.PA_INVALID_ARGUMENT and "required" in msg
+    assert check(cfg, cos_cache=A + 100000, sin_cache=A + 110000)[0] == pa.PA_OK
+
+
+def test_cache_write_needs_no_query_or_output():
+    assert check(for_forward=0, query=None, output=None)[0] == pa.PA_OK
+
+
+def test_create_without_gpu_reports_cuda_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_create(good())
+    assert e.value.status == pa.PA_CUDA_ERROR
+    # an invalid config is rejected before any CUDA call
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_create(good(block_size=24))
+    assert e.value.status == pa.PA_INVALID_ARGUMENT and "block_size" in e.value.message

@@ -1,0 +1,134 @@
+"""GPU parity: the C-ABI path against the CPU oracle, element by element.
+
+Bars: the paged pools are bit-exact; the fp16 output is within
+|gpu - oracle| <= 2e-3 + 1e-2 |oracle| (oracle in fp64).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_reshape_gb300 as pa
+import workloads
+from gpu_util import assert_close, bits, check_full, check_sampled, host_copy, make, run
+
+pytestmark = pytest.mark.gpu
+
+cs = workloads.custom_shape
+
+
+def _full(shape, options=(), **kw):
+    step = make(shape, device="cuda", gen_device="cpu")
+    host = host_copy(step)
+    op, out, err = run(step, options=options, **kw)
+    assert err == 0, f"device error {err:#x}"
+    check_full(host, step, out)
+    return op, out
+
+
+SMALL = [
+    workloads.config_shape(0),
+    cs("d128_g4_bs16_decode", 8, 2, 128, 16, [0, 1, 15, 16, 17, 63, 64, 300], [1] * 8, seed=1),
+    cs("d64_mha_bs32_multitok", 4, 4, 64, 32, [0, 33, 100, 7, 64], [4, 1, 3, 2, 4], seed=2),
+    cs("d256_g2_bs64_window_cap", 4, 2, 256, 64, [700, 64, 5, 129], [1, 1, 2, 1], scale=1 / 16,
+       softcap=50.0, local_window_size=100, seed=3),
+    cs("d128_g8_bs16_rotary", 16, 2, 128, 16, [0, 5, 200, 999], [1, 2, 1, 2], do_rotary=1, seed=4),
+    cs("d128_g4_rotary_interleaved_r64", 8, 2, 128, 16, [10, 300], [1, 3], do_rotary=1,
+       rotary_interleaved=1, rotary_dim=64, seed=5),
+    cs("d128_g2_bs128", 4, 2, 128, 128, [0, 127, 128, 500], [1, 1, 1, 1], seed=6),
+    cs("d64_g4_bs256_window1", 8, 2, 64, 256, [300, 600], [1, 2], local_window_size=1, seed=7),
+    cs("zero_len_rows", 8, 4, 128, 16, [40, 0, 90, 12], [1, 0, 1, 0], seed=8),
+    cs("softcap_small_window_edge", 2, 1, 64, 16, [63, 64, 65, 200], [1, 1, 1, 1], softcap=5.0,
+       local_window_size=64, seed=9),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_small_step_matches_oracle(shape):
+    _full(shape)
+
+
+@pytest.mark.parametrize("split_keys", [64, 128, 0])
+def test_split_counts_agree(split_keys):
+    shape = cs("splits", 8, 2, 128, 16, [1000, 70, 2047, 300], [1, 1, 1, 2], seed=11)
+    _full(shape, options=[(pa.PA_OPT_SPLIT_KEYS, split_keys)])
+
+
+def test_unmapped_blocks_are_masked():
+    shape = cs("unmapped", 8, 2, 128, 16, [200, 150], [1, 1], local_window_size=48, seed=12)
+    step = make(shape, device="cpu")
+    step["block_table"][0, 2] = -1       # inside sequence 0's context, below its window
+    step["block_table"][1, 3] = -1       # inside sequence 1's window: positions 48..63 masked
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
+    op, out, err = run(dev)
+    assert err == 0
+    check_full(step, dev, out)
+
+
+def test_large_batch_worklist_chunks():
+    B = 1100
+    rng = np.random.default_rng(13)
+    shape = cs("b1100", 4, 2, 64, 16, rng.integers(0, 40, B), [1] * B, seed=13)
+    _full(shape)
+
+
+def test_empty_step_launches_nothing():
+    shape = cs("empty", 4, 2, 64, 16, [5, 9], [0, 0], seed=14)
+    step = make(shape, device="cuda", gen_device="cpu")
+    op = pa.PagedAttention.for_step(step, max_tokens=4)
+    out = torch.empty(0, 4 * 64, dtype=torch.float16, device="cuda")
+    before = bits(step["key_cache"]).copy()
+    op.forward(step, out)
+    torch.cuda.synchronize()
+    assert op.last_launch_count() == 0
+    assert np.array_equal(before, bits(step["key_cache"]))
+
+
+def test_bad_device_data_is_flagged_not_faulting():
+    shape = cs("bad", 4, 2, 64, 16, [30, 40], [1, 1], seed=15)
+    step = make(shape, device="cpu")
+    step["block_table"][0, 0] = 10_000                   # outside the pool
+    dev = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
+    op, out, err = run(dev)
+    assert err & pa.PA_DEVERR_BLOCK_ID
+    # cum not ending at token_count
+    step2 = make(shape, device="cpu")
+    step2["cumulative_sequence_lengths"][2] = 1
+    dev2 = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in step2.items()}
+    op2, out2, err2 = run(dev2)
+    assert err2 & pa.PA_DEVERR_CUM
+
+
+def test_window_pruning_bit_matches_unpruned():
+    shape = cs("prune", 8, 2, 128, 16, [3000, 1500], [1, 1], local_window_size=256, seed=16)
+    outs = []
+    for no_prune in (0, 1):
+        step = make(shape, device="cuda", gen_device="cpu")
+        op, out, err = run(step, options=[(pa.PA_OPT_NO_WINDOW_PRUNE, no_prune),
+                                          (pa.PA_OPT_SPLIT_KEYS, 4096)])
+        assert err == 0
+        outs.append(bits(out))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_metadata_bound_invariance():
+    shape = cs("bounds", 8, 2, 128, 16, [100, 1000, 37], [1, 1, 1], seed=17)
+    outs = []
+    for bounds in ({}, dict(max_query_len_bound=1, max_kv_len_bound=1001),
+                   dict(max_query_len_bound=64, max_kv_len_bound=4000)):
+        step = make(shape, device="cuda", gen_device="cpu")
+        op, out, err = run(step, max_tokens=64, max_batch=16, **bounds)
+        assert err == 0
+        outs.append(bits(out))
+    # split sizes follow the device-side work, not the bounds
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("index", [1, 3, 4])
+def test_full_size_decode_config(index):
+    shape = workloads.config_shape(index)
+    step = make(shape, device="cuda", gen_device="cuda")
+    host = host_copy(step)
+    op, out, err = run(step)
+    assert err == 0, f"device error {err:#x}"
+    check_sampled(host, step, out, n_rows=160)
