@@ -270,29 +270,53 @@ def run_ours(args, rank, world, local_rank):
     assert op.device_error() == 0, "device error during warm-up"
     launches_per_step = op.last_launch_count()
 
-    # ---- device-timed steps (L2 flushed before each, outside the events)
+    # ---- device-timed steps: one CUDA-graph replay of pa_forward each (the
+    # step is capture-safe: no host sync, no allocation); L2 flushed before
+    # each replay, outside the events.  A second graph, captured with the
+    # library's per-kernel events on, times the decode kernel alone.
+    def capture():
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            op.forward(step, out, stream=cap.cuda_stream)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    run = fwd if args.eager else capture().replay
     op.set_option(pa.PA_OPT_KERNEL_TIMING, 1)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    dec_ms = []
+    run_timed = fwd if args.eager else capture().replay
+    op.set_option(pa.PA_OPT_KERNEL_TIMING, 0)
+
+    def timed_loop(fn, n, sample_decode):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        dec = []
+        for i in range(n):
+            flush.fill_(i)
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+            if sample_decode and (i % 16 == 15 or i == n - 1):
+                dec.append(op.kernel_time_ms(pa.PA_STAGE_DECODE))
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)], dec
+
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
         t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.fill_(i)
-            starts[i].record(stream)
-            fwd()
-            ends[i].record(stream)
-            if i % 64 == 63 or i == args.steps - 1:
-                dec_ms.append(op.kernel_time_ms(pa.PA_STAGE_DECODE))
-        torch.cuda.synchronize()
+        step_ms, _ = timed_loop(run, args.steps, False)
         t_wall = time.perf_counter() - t_wall0
+        op.set_option(pa.PA_OPT_KERNEL_TIMING, 1)
+        _, dec_ms = timed_loop(run_timed, min(args.steps, 256), True)
+        op.set_option(pa.PA_OPT_KERNEL_TIMING, 0)
     if world > 1:
         torch.distributed.barrier()
-    op.set_option(pa.PA_OPT_KERNEL_TIMING, 0)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = statistics.mean(step_ms)
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -346,6 +370,7 @@ def run_ours(args, rank, world, local_rank):
                    "kv_num_heads": shape.kv_num_heads, "head_size": shape.head_size,
                    "block_size": shape.block_size, "attended_kv_bytes_per_step": kv_bytes,
                    "l2": "flushed before every step (write of 2x L2), outside the step's events",
+                   "launch": "eager" if args.eager else "cuda_graph replay of one pa_forward",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel<128>", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
@@ -353,7 +378,7 @@ def run_ours(args, rank, world, local_rank):
                      "launch_ms": dec},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches_per_step * (args.steps + min(args.steps, 256)),
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
@@ -370,6 +395,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch pa_forward directly instead of a graph replay")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -24,6 +24,7 @@ PA_DEVERR_CUM, PA_DEVERR_BLOCK_ID, PA_DEVERR_PAST = 1, 2, 4
 PA_DEVERR_KV_BOUND, PA_DEVERR_Q_BOUND, PA_DEVERR_ROTARY_POS, PA_DEVERR_TIMEOUT = 8, 16, 32, 64
 
 PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_MAX_ROWS = 1, 2, 3, 4
+PA_OPT_DECODE_ITEMS_PER_CTA = 5
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 

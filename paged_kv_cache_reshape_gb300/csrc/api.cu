@@ -84,7 +84,7 @@ struct pa_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   __half* q_rot = nullptr;
-  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = pa::kDecodeRows;
+  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0, opt_items_per_cta = 4;
   cudaEvent_t ev[PA_NUM_STAGES][2] = {};
   bool stage_ran[PA_NUM_STAGES] = {};
   cudaStream_t last_stream = nullptr;
@@ -120,6 +120,23 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int heads_total, long l
   cuuint32_t box[3] = {64, (cuuint32_t)heads_box, (cuuint32_t)rows_box};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// 4-D view of an NHD pool {64 channels, NB*bs rows, D/64 chunks, Hk heads}
+// (strides: row Hk*D*2 bytes, chunk 128 bytes, head D*2 bytes): a box
+// {64, rows, D/64, 1} is one head's page laid out [chunk][row][128 B] with
+// the 128-byte swizzle.  Every addressable byte lies inside the pool.
+bool encode_pool_map(CUtensorMap* m, const void* base, int D, int Hk, long long rows_total, int rows_box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {64, (cuuint64_t)rows_total, (cuuint64_t)(D / 64), (cuuint64_t)Hk};
+  cuuint64_t strides[3] = {(cuuint64_t)Hk * D * 2, 128, (cuuint64_t)D * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)rows_box, (cuuint32_t)(D / 64), 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -298,6 +315,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   if (!encode_fn()) { delete h; return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled is unavailable"); }
 
   h->G = c.num_heads / c.kv_num_heads;
+  h->opt_dec_rows = h->G <= pa::kDecodeRows ? pa::kDecodeRows : 0;  // decode items hold <= 16 rows
   h->R = rot_dim_of(c);
   h->scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)c.head_size);
   const int kv_cap = c.max_blocks_per_seq * c.block_size;
@@ -312,8 +330,9 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->pre_smem = psmem;
 
   h->dec_grid = h->num_sms * h->dec_ctas_per_sm;
-  h->target_pairs = std::max(1, (4 * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads);
-  h->cap_dec = h->target_pairs + c.max_batch;
+  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads);
+  // Room for up to 32 items per CTA (the tuning option's maximum).
+  h->cap_dec = std::max(1, (32 * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads) + c.max_batch;
   h->prefill_tile_tokens = std::max(1, pa::kPrefillRows / h->G);
   h->cap_pre = (c.max_tokens + h->prefill_tile_tokens - 1) / h->prefill_tile_tokens + c.max_batch;
   h->cap_comb = c.max_tokens;
@@ -387,6 +406,11 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
     }
     case PA_OPT_NO_WINDOW_PRUNE: h->opt_no_prune = value != 0; return PA_OK;
     case PA_OPT_KERNEL_TIMING: h->opt_timing = value != 0; return PA_OK;
+    case PA_OPT_DECODE_ITEMS_PER_CTA:
+      if (value < 1 || value > 32) return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be in [1, 32]");
+      h->opt_items_per_cta = value;
+      h->target_pairs = std::max(1, (value * h->dec_grid + h->cfg.kv_num_heads - 1) / h->cfg.kv_num_heads);
+      return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
       if (value < 0 || value > pa::kDecodeRows)
         return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", pa::kDecodeRows);
@@ -429,25 +453,35 @@ pa_status pa_check_device_error(pa_handle h, int* code) {
 
 namespace {
 
+// Records the stage's start/end events on the launch stream.  Inside a
+// stream capture they become external event-record nodes, so the events
+// still measure the kernel when the graph is replayed.
+void record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(s, &cs);
+  if (cs == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else cudaEventRecord(ev, s);
+}
+
 struct StageTimer {
   pa_handle h;
   int stage;
   cudaStream_t s;
   StageTimer(pa_handle h_, int st, cudaStream_t s_) : h(h_), stage(st), s(s_) {
-    if (h->opt_timing) cudaEventRecord(h->ev[stage][0], s);
+    if (h->opt_timing) record(h->ev[stage][0], s);
   }
   ~StageTimer() {
     if (h->opt_timing) {
-      cudaEventRecord(h->ev[stage][1], s);
+      record(h->ev[stage][1], s);
       h->stage_ran[stage] = true;
     }
   }
 };
 
-pa_status run_cache_write(pa_handle h, const void* query, const void* key, const void* value, void* key_cache,
-                          void* value_cache, const int32_t* block_table, const int32_t* cum, const int32_t* past,
-                          int batch, int token_count, const void* cos_cache, const void* sin_cache,
-                          cudaStream_t s) {
+pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const void* key, const void* value,
+                                        void* key_cache, void* value_cache, const int32_t* block_table,
+                                        const int32_t* cum, const int32_t* past, int batch, int token_count,
+                                        const void* cos_cache, const void* sin_cache) {
   const pa_config& c = h->cfg;
   pa::CacheWriteParams p{};
   p.key = static_cast<const __half*>(key);
@@ -473,12 +507,12 @@ pa_status run_cache_write(pa_handle h, const void* query, const void* key, const
   p.interleaved = c.rotary_interleaved;
   p.rot_dim = h->R;
   p.rot_positions = c.max_rotary_positions;
+  // Spread a token over several warps when Q is rotated too: one for the
+  // K/V rows and one per kv_num_heads query heads (same size as a K row).
+  p.q_heads_per_part = c.kv_num_heads;
+  p.parts = 1 + (p.q_rot ? (c.num_heads + c.kv_num_heads - 1) / c.kv_num_heads : 0);
   p.err = h->err;
-  StageTimer t(h, PA_STAGE_CACHE_WRITE, s);
-  cudaError_t e = pa::launch_cache_write(p, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cache write launch");
-  h->last_launches++;
-  return PA_OK;
+  return p;
 }
 
 }  // namespace
@@ -499,8 +533,13 @@ pa_status pa_cache_write(pa_handle h, const void* key, const void* value, void* 
   h->last_stream = s;
   if (token_count == 0) return PA_OK;
   DeviceGuard g(h->device);
-  return run_cache_write(h, nullptr, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
-                         cos_cache, sin_cache, s);
+  pa::CacheWriteParams p = cache_write_params(h, nullptr, key, value, key_cache, value_cache, block_table, cum,
+                                              past, batch, token_count, cos_cache, sin_cache);
+  StageTimer t(h, PA_STAGE_CACHE_WRITE, s);
+  cudaError_t e = pa::launch_cache_write(p, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cache write launch");
+  h->last_launches++;
+  return PA_OK;
 }
 
 pa_status pa_forward(pa_handle h, const void* query, const void* key, const void* value, void* key_cache,
@@ -524,11 +563,11 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   const int box_rows = std::min(c.block_size, pa::kStageKeys);
 
   CUtensorMap tk, tv;
-  if (!encode_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, 1, box_rows) ||
-      !encode_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, 1, box_rows))
+  if (!encode_pool_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, box_rows) ||
+      !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows))
     return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
 
-  // 1. work list
+  // 1+2. prologue: device work list, rotary and the paged cache write
   {
     pa::WorklistParams p{};
     p.cum = cum;
@@ -553,20 +592,23 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.comb_rows = h->comb_rows;
     p.counters = h->counters;
     p.err = h->err;
+    pa::CacheWriteParams cp = cache_write_params(h, query, key, value, key_cache, value_cache, block_table, cum,
+                                                 past, batch, token_count, cos_cache, sin_cache);
     StageTimer t(h, PA_STAGE_WORKLIST, s);
-    cudaError_t e = pa::launch_worklist(p, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "work-list launch");
+    cudaError_t e = pa::launch_prologue(p, cp, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "prologue launch");
     h->last_launches++;
   }
-  // 2. rotary + cache write
-  st = run_cache_write(h, query, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
-                       cos_cache, sin_cache, s);
-  if (st != PA_OK) return st;
   const __half* q_att = c.do_rotary ? h->q_rot : static_cast<const __half*>(query);
   // 3. split-KV decode
   {
+    const int qt = h->G <= pa::kDecodeRows ? pa::kDecodeRows / h->G : 1;
+    CUtensorMap tq;
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, qt))
+      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
     pa::DecodeParams p{};
-    p.q = q_att;
+    p.q_tile_tokens = qt;
+    p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
     p.out = static_cast<__half*>(output);
     p.block_table = block_table;
     p.seq = h->seq;
@@ -586,7 +628,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.window = c.local_window_size;
     p.oob_row = pool_rows;
     StageTimer t(h, PA_STAGE_DECODE, s);
-    cudaError_t e = pa::launch_decode(D, tk, tv, p, h->dec_grid, s);
+    cudaError_t e = pa::launch_decode(D, tk, tv, tq, p, h->dec_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
     h->last_launches++;
   }

@@ -16,6 +16,7 @@
 // [Hk, D] slice contiguously, so a warp writes one contiguous run of
 // Hk*D*2 bytes per tensor (fully coalesced).
 #include "step.h"
+#include "worklist.cuh"
 #include "../../include/pa.h"
 
 namespace pa {
@@ -100,42 +101,47 @@ __device__ void row_transform(const __half* __restrict__ src, __half* __restrict
   }
 }
 
-__global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheWriteParams p) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= p.token_count) return;
+// One warp's share of packed row t.  Part 0 writes the K (rotated) and V
+// rows into the pool; parts 1.. rotate query heads [(part-1)*qh, part*qh)
+// into the rotated-query workspace (only with rotary in pa_forward).  `cum`
+// is the cumulative length array, either the caller's (global) or a
+// shared-memory copy.
+__device__ void write_token(const CacheWriteParams& p, const int* cum, int t, int part, int lane) {
   // Owner sequence: largest b with cum[b] <= t.
   int lo = 0, hi = p.batch;
   while (hi - lo > 1) {
     int mid = (lo + hi) >> 1;
-    if (__ldg(p.cum + mid) <= t) lo = mid;
+    if (cum[mid] <= t) lo = mid;
     else hi = mid;
   }
   const int b = lo;
-  const int c0 = __ldg(p.cum + b), c1 = __ldg(p.cum + b + 1);
+  const int c0 = cum[b], c1 = cum[b + 1];
   const int past = __ldg(p.past + b);
   if (t < c0 || t >= c1 || c0 < 0) {
-    if (lane == 0) atomicOr(p.err, PA_DEVERR_CUM);
+    if (lane == 0 && part == 0) atomicOr(p.err, PA_DEVERR_CUM);
     return;
   }
   if (past < 0) {
-    if (lane == 0) atomicOr(p.err, PA_DEVERR_PAST);
+    if (lane == 0 && part == 0) atomicOr(p.err, PA_DEVERR_PAST);
     return;
   }
   const int pos = past + (t - c0);
   bool rotate = p.rotary != 0;
   if (rotate && pos >= p.rot_positions) {
-    if (lane == 0) atomicOr(p.err, PA_DEVERR_ROTARY_POS);
+    if (lane == 0 && part == 0) atomicOr(p.err, PA_DEVERR_ROTARY_POS);
     rotate = false;  // never read past the tables
   }
   const int half = p.rot_dim / 2;
   const __half* cos_row = rotate ? p.cos_cache + (size_t)pos * half : nullptr;
   const __half* sin_row = rotate ? p.sin_cache + (size_t)pos * half : nullptr;
 
-  if (p.query != nullptr && p.q_rot != nullptr) {
-    const size_t qoff = (size_t)t * p.H * p.D;
-    row_transform(p.query + qoff, p.q_rot + qoff, p.H, p.D, rotate, p.rot_dim, p.interleaved, cos_row,
-                  sin_row, lane);
+  if (part > 0) {
+    const int h0 = (part - 1) * p.q_heads_per_part;
+    const int nh = min(p.q_heads_per_part, p.H - h0);
+    const size_t qoff = ((size_t)t * p.H + h0) * p.D;
+    row_transform(p.query + qoff, p.q_rot + qoff, nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row,
+                  lane);
+    return;
   }
 
   const int row = pos / p.bs;
@@ -157,11 +163,54 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheW
                 nullptr, nullptr, lane);
 }
 
+// Sequences whose cumulative lengths are staged in shared memory (one
+// coalesced read instead of a chain of dependent global reads per token).
+constexpr int kCumCache = 4096;
+
+__device__ const int* stage_cum(const CacheWriteParams& p, int* cum_s) {
+  if (p.batch + 1 > kCumCache) return p.cum;
+  for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cum_s[i] = __ldg(p.cum + i);
+  __syncthreads();
+  return cum_s;
+}
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheWriteParams p) {
+  __shared__ int cum_s[kCumCache];
+  const int* cum = stage_cum(p, cum_s);
+  const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (w < p.token_count * p.parts) write_token(p, cum, w / p.parts, w % p.parts, threadIdx.x & 31);
+}
+
+// The step's prologue in one launch: CTA 0 builds the work list while the
+// other CTAs (32 warps each, one warp per (token, part)) rotate and write
+// the new rows.  The two jobs read only the step's inputs, so they overlap.
+constexpr int kPrologueWarps = worklist::kThreads / 32;
+
+__global__ void __launch_bounds__(worklist::kThreads, 1) prologue_kernel(WorklistParams wp, CacheWriteParams cp) {
+  // Let the attention kernels' CTAs get resident early; they wait for this
+  // grid's completion before reading anything it writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0) {
+    worklist::build(wp);
+    return;
+  }
+  __shared__ int cum_s[kCumCache];
+  const int* cum = stage_cum(cp, cum_s);
+  const int w = (blockIdx.x - 1) * kPrologueWarps + (threadIdx.x >> 5);
+  if (w < cp.token_count * cp.parts) write_token(cp, cum, w / cp.parts, w % cp.parts, threadIdx.x & 31);
+}
+
 }  // namespace
 
 cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s) {
-  int blocks = (p.token_count + kWarpsPerBlock - 1) / kWarpsPerBlock;
+  int blocks = (p.token_count * p.parts + kWarpsPerBlock - 1) / kWarpsPerBlock;
   cache_write_kernel<<<blocks, kWarpsPerBlock * 32, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, cudaStream_t s) {
+  int blocks = 1 + (cp.token_count * cp.parts + kPrologueWarps - 1) / kPrologueWarps;
+  prologue_kernel<<<blocks, worklist::kThreads, 0, s>>>(wp, cp);
   return cudaGetLastError();
 }
 

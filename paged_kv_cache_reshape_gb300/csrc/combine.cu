@@ -10,6 +10,7 @@
 //
 // One warp per (packed row, query head); the work list holds only the rows
 // of sequences that were split, so the grid is a small persistent one.
+#include "ptx.cuh"
 #include "step.h"
 
 namespace pa {
@@ -21,6 +22,7 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
   constexpr int kPer = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // partials and the work list come from the kernels before
   const int n = p.counters->n_comb * p.H;
   for (int idx = blockIdx.x * kWarps + (threadIdx.x >> 5); idx < n; idx += gridDim.x * kWarps) {
     const int ci = idx / p.H, h = idx - ci * p.H;
@@ -33,7 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     // global max over splits
     float M = -INFINITY;
     for (int s = lane; s < ns; s += 32) {
-      const size_t row = ((size_t)(si.dec_first + s) * p.Hk + k) * kDecodeRows + r;
+      const size_t row = ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r;
       M = fmaxf(M, p.part_ml[row].x);
     }
 #pragma unroll
@@ -44,7 +46,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     float den = 0.f;
     if (M != -INFINITY) {
       for (int s = 0; s < ns; ++s) {
-        const size_t row = ((size_t)(si.dec_first + s) * p.Hk + k) * kDecodeRows + r;
+        const size_t row = ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r;
         const float2 ml = p.part_ml[row];
         if (ml.y == 0.f) continue;  // empty split
         const float f = exp2f(ml.x - M);
@@ -77,12 +79,11 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
 
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s) {
   switch (p.D) {
-    case 64: combine_kernel<64><<<grid, kWarps * 32, 0, s>>>(p); break;
-    case 128: combine_kernel<128><<<grid, kWarps * 32, 0, s>>>(p); break;
-    case 256: combine_kernel<256><<<grid, kWarps * 32, 0, s>>>(p); break;
+    case 64: return launch_pdl(combine_kernel<64>, grid, kWarps * 32, 0, s, p);
+    case 128: return launch_pdl(combine_kernel<128>, grid, kWarps * 32, 0, s, p);
+    case 256: return launch_pdl(combine_kernel<256>, grid, kWarps * 32, 0, s, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -12,12 +12,19 @@
 // clamped range).
 //
 // Design for sm_103a (not the pages' CUDA-core kernel):
-//  * persistent grid (a multiple of the SM count); CTAs stride over items;
-//  * one producer warp streams 64-key stages of K and V through a ring of
-//    shared-memory buffers with 3-D TMA boxes {64 ch, 1 head, rows} straight
-//    from the NHD pool (one box per page and 64-channel chunk, 128-byte
-//    swizzle), completion on mbarriers; unmapped pages are fetched from a
-//    row past the pool so TMA zero-fills them without a memory read;
+//  * persistent grid sized from the SM count; a producer warp takes items
+//    from a device queue (full splits first) and posts each 64-key stage's
+//    description in a shared-memory tag next to the data;
+//  * the producer streams K and V through a ring of shared-memory stages
+//    straight from the NHD pool with one 4-D TMA box per page and tensor:
+//    the pool is viewed as {64 channels, pool rows, D/64 chunks, heads} so
+//    a box {64, rows, D/64, 1} lands one head's page as [chunk][row][128 B]
+//    with the 128-byte swizzle; the boxes of a stage are issued by several
+//    lanes at once; the item's 16 query rows come with one 3-D box
+//    {64, G, 16/G} per chunk into a double-buffered Q tile; block ids are
+//    fetched 32 rows at a time by the whole warp one window ahead; unmapped
+//    pages are fetched from a row past the pool so TMA zero-fills them
+//    without reading memory;
 //  * four consumer warps each own 16 keys of every stage and run the two
 //    contractions on tensor cores (m16n8k16 HMMA, fp16 in, fp32 accumulate):
 //    S = Q K^T and O += P V, with an fp32 online softmax whose row max is
@@ -37,20 +44,32 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct DecodeCfg {
-  static constexpr int kChunks = D / 64;                       // 64-channel (128 B) chunks per row
-  static constexpr int kTileBytes = kStageKeys * D * 2;        // K (or V) bytes per stage
-  static constexpr int kStageBytes = 2 * kTileBytes;           // K + V
+  static constexpr int kChunks = D / 64;                 // 64-channel (128 B) chunks per row
+  static constexpr int kTileBytes = kStageKeys * D * 2;  // K (or V) bytes per stage
+  static constexpr int kStageBytes = 2 * kTileBytes;     // K + V
   static constexpr int kStages = (D == 256) ? 3 : (D == 128 ? 3 : 6);
-  static constexpr int kQStride = D + 8;                       // padded Q row (halves)
-  static constexpr int kQBytes = kDecodeRows * kQStride * 2;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kQBytes + 4 * 16 * 8 + kStages * 16 +
-                                    2 * kStages * 8 + 64;
+  static constexpr int kQBytes = kChunks * 2048;         // 16 rows x 128 B per chunk
+  static constexpr int kCtasPerSm = (D == 256) ? 1 : 2;
+  static constexpr int kSmemBytes =
+      1024 + kStages * kStageBytes + 2 * kQBytes + 4 * 16 * 8 + kStages * 64 + (2 * kStages + 4) * 8;
 };
 
 struct StageTag {
-  int mask;  // bit i: box i of the stage was zero-filled (unmapped or past the end)
-  int pad[3];
+  int u;       // item * Hk + k; -1 = no more work
+  int key0;    // first key position of the stage
+  int end;     // split end (exclusive)
+  int flags;   // bits 0..3 zero-filled boxes; bit 8 first stage of the item; bit 9 last stage
+  int R;       // valid query rows (q_len * G)
+  int past;    // past length of the sequence
+  int t0;      // first packed row of the sequence
+  int k;       // kv head
+  int kv_len;  // past + q_len
+  int nsplit;  // splits of the sequence
+  int qi;      // Q buffer
+  int lo_min;  // smallest admitted position of any row (0 without a window)
+  int pad[4];
 };
+constexpr int kFirst = 1 << 8, kLast = 1 << 9;
 
 // Byte offset of 16-byte column `col16` of row `row` inside a 128B-swizzled
 // [rows][128 B] tile whose base is 1024-byte aligned.
@@ -58,19 +77,29 @@ __device__ __forceinline__ uint32_t swz(int row, int col16) {
   return (uint32_t)(row * 128 + ((col16 ^ (row & 7)) << 4));
 }
 
+// Stage tile layout [box][chunk][row][128 B] (box = 2^log_r pool rows):
+// byte offset of (stage key kk, channel chunk, 16-byte column col16).
+template <int kChunks>
+__device__ __forceinline__ uint32_t tile_off(int kk, int chunk, int col16, int log_r) {
+  const int r = kk & ((1 << log_r) - 1), bx = kk >> log_r;
+  return ((uint32_t)(bx * kChunks + chunk) << (log_r + 7)) + swz(r, col16);
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const DecodeParams p) {
+                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   using C = DecodeCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  __half* qs = reinterpret_cast<__half*>(smem + C::kStages * C::kStageBytes);
-  float2* mls = reinterpret_cast<float2*>(smem + C::kStages * C::kStageBytes + C::kQBytes);
+  uint8_t* qbuf = smem + C::kStages * C::kStageBytes;  // [2][kQBytes]
+  float2* mls = reinterpret_cast<float2*>(qbuf + 2 * C::kQBytes);
   StageTag* tags = reinterpret_cast<StageTag*>(mls + 4 * 16);
   uint64_t* full = reinterpret_cast<uint64_t*>(tags + C::kStages);
   uint64_t* empty = full + C::kStages;
+  uint64_t* q_full = empty + C::kStages;
+  uint64_t* q_empty = q_full + 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -78,68 +107,140 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kDecodeWarps);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], kDecodeWarps);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-
-  const int n_work = p.counters->n_dec * p.Hk;
-  const int split_keys = p.counters->split_keys;
-  const int rows_per_box = p.bs < kStageKeys ? p.bs : kStageKeys;
-  const int boxes = kStageKeys / rows_per_box;
+  // Everything below reads the prologue's work list and the pool it wrote.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kDecodeWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int u = blockIdx.x; u < n_work; u += gridDim.x) {
-        const int item = u / p.Hk, k = u - item * p.Hk;
-        const int2 bsplit = p.dec_items[item];
-        const int b = bsplit.x;
-        const SeqInfo si = p.seq[b];
-        const int start = si.lo + bsplit.y * split_keys;
-        const int end = min(si.kv_len, start + split_keys);
-        for (int key0 = start; key0 < end; key0 += kStageKeys) {
-          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+      prefetch_tmap(&tm_q);
+    }
+    const int n_work = p.counters->n_dec * p.Hk;
+    const int split_keys = p.counters->split_keys;
+    const int boxes = kStageKeys >> p.log_box_rows;
+    const int qt = p.q_tile_tokens;
+    const uint32_t q_bytes = C::kChunks * p.G * qt * 128;
+    int stage = 0;
+    uint32_t phase = 0;
+    int quse[2] = {0, 0};
+    int qi = 0;
+    bool ok = true;
+    while (ok) {
+      int u = 0;
+      if (lane == 0) u = atomicAdd(&p.counters->dec_next, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u >= n_work) {
+        if (lane == 0) {
+          if (mbar_wait(&empty[stage], phase ^ 1)) {
+            tags[stage].u = -1;
+            mbar_arrive(&full[stage]);
+          } else {
             atomicOr(p.err, PA_DEVERR_TIMEOUT);
-            return;
-          }
-          int mask = 0;
-          int rowc[kStageKeys / 16];
-          for (int bx = 0; bx < boxes; ++bx) {
-            const int pos = key0 + bx * rows_per_box;
-            int rc = p.oob_row;
-            if (pos < end) {
-              const int blk = __ldg(p.block_table + (size_t)b * p.MB + pos / p.bs);
-              if (blk >= 0 && blk < p.NB) {
-                rc = blk * p.bs + (pos & (p.bs - 1));
-              } else if (blk != -1) {
-                atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-              }
-            }
-            if (rc == p.oob_row) mask |= 1 << bx;
-            rowc[bx] = rc;
-          }
-          tags[stage].mask = mask;
-          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          uint8_t* kdst = stages + stage * C::kStageBytes;
-          uint8_t* vdst = kdst + C::kTileBytes;
-          for (int bx = 0; bx < boxes; ++bx) {
-#pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-              const uint32_t off = c * (kStageKeys * 128) + bx * rows_per_box * 128;
-              tma_load_3d(kdst + off, &tm_k, c * 64, k, rowc[bx], &full[stage]);
-              tma_load_3d(vdst + off, &tm_v, c * 64, k, rowc[bx], &full[stage]);
-            }
-          }
-          if (++stage == C::kStages) {
-            stage = 0;
-            phase ^= 1;
           }
         }
+        break;
       }
+      const int item = u / p.Hk, k = u - item * p.Hk;
+      const int2 bsplit = p.dec_items[item];
+      const int b = bsplit.x;
+      const SeqInfo si = p.seq[b];
+      const int start = si.lo + bsplit.y * split_keys;
+      const int end = min(si.kv_len, start + split_keys);
+      const int past = si.kv_len - si.q_len;
+      const int lo_min = p.window >= 1 ? max(0, past + 1 - p.window) : 0;
+
+      // Query rows of the item: box {64, G, qt} at (chunk, k*G, t0).
+      if (lane == 0) {
+        if (!mbar_wait(&q_empty[qi], (quse[qi] & 1) ^ 1)) {
+          atomicOr(p.err, PA_DEVERR_TIMEOUT);
+          ok = false;
+        } else {
+          mbar_arrive_expect_tx(&q_full[qi], q_bytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(qbuf + qi * C::kQBytes + c * 2048, &tm_q, c * 64, k * p.G, si.t0, &q_full[qi]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      quse[qi]++;
+
+      // Block ids, 32 block-table rows per window, one window ahead.
+      const int* bt_row = p.block_table + (size_t)b * p.MB;
+      auto load_id = [&](int r) -> int {
+        return (r < p.MB && r * p.bs < end) ? __ldg(bt_row + r) : -1;
+      };
+      int win = start / p.bs;
+      int id_cur = load_id(win + lane);
+      int id_nxt = load_id(win + 32 + lane);
+
+      for (int key0 = start; key0 < end; key0 += kStageKeys) {
+        const int rowA = key0 / p.bs;
+        if (rowA >= win + 32) {
+          win += 32;
+          id_cur = id_nxt;
+          id_nxt = load_id(win + 32 + lane);
+        }
+        // Lane 2*bx (K) and 2*bx+1 (V) own box bx of the stage.
+        const int bxl = lane >> 1;
+        const int pos = key0 + (bxl << p.log_box_rows);
+        const int idx = pos / p.bs - win;  // window-relative block row, 0 .. 35
+        const int a = __shfl_sync(0xffffffffu, id_cur, idx & 31);
+        const int n = __shfl_sync(0xffffffffu, id_nxt, idx & 31);
+        const int blk = idx < 32 ? a : n;
+        int rc = p.oob_row;
+        if (bxl < boxes && pos < end) {
+          if (blk >= 0 && blk < p.NB) rc = blk * p.bs + (pos & (p.bs - 1));
+          else if (blk != -1 && (lane & 1) == 0) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+        }
+        const unsigned zb = __ballot_sync(0xffffffffu, bxl < boxes && (lane & 1) == 0 && rc == p.oob_row);
+        int mask = 0;
+        for (int bx = 0; bx < boxes; ++bx) mask |= ((zb >> (2 * bx)) & 1) << bx;
+        if (lane == 0) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            ok = false;
+          } else {
+            StageTag& t = tags[stage];
+            t.u = u;
+            t.key0 = key0;
+            t.end = end;
+            t.flags = mask | (key0 == start ? kFirst : 0) | (key0 + kStageKeys >= end ? kLast : 0);
+            t.R = si.q_len * p.G;
+            t.past = past;
+            t.t0 = si.t0;
+            t.k = k;
+            t.kv_len = si.kv_len;
+            t.nsplit = si.dec_count;
+            t.qi = qi;
+            t.lo_min = lo_min;
+            mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (bxl < boxes) {
+          uint8_t* dst = stages + stage * C::kStageBytes + (lane & 1) * C::kTileBytes +
+                         ((uint32_t)bxl * C::kChunks << (p.log_box_rows + 7));
+          tma_load_4d(dst, (lane & 1) ? &tm_v : &tm_k, 0, rc, 0, k, &full[stage]);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (++stage == C::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      qi ^= 1;
     }
     return;
   }
@@ -150,277 +251,270 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cq = 2 * (lane & 3);
   int stage = 0;
   uint32_t phase = 0;
+  int quse[2] = {0, 0};
   const float scale = p.scale;
   const bool capped = p.softcap > 0.f;
   const float inv_cap = capped ? 1.f / p.softcap : 0.f;
+  const int log_r = p.log_box_rows;
 
-  for (int u = blockIdx.x; u < n_work; u += gridDim.x) {
-    const int item = u / p.Hk, k = u - item * p.Hk;
-    const int2 bsplit = p.dec_items[item];
-    const int b = bsplit.x;
-    const SeqInfo si = p.seq[b];
-    const int start = si.lo + bsplit.y * split_keys;
-    const int end = min(si.kv_len, start + split_keys);
-    const int R = si.q_len * p.G;
-    const int past = si.kv_len - si.q_len;
+  uint32_t qf[(D <= 128) ? D / 16 : 1][4];
+  float m[2], l[2];
+  float o[D / 8][4];
+  int hi0 = -1, hi1 = -1, lo0 = 0, lo1 = 0;
+  const uint8_t* qcur = qbuf;
 
-    // Stage this item's query rows (16 x D, zero past R) into padded smem.
-    for (int i = ctid; i < kDecodeRows * (D / 8); i += kDecodeWarps * 32) {
-      const int r = i / (D / 8), c8 = i % (D / 8);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < R) {
-        const int t = si.t0 + r / p.G, h = k * p.G + r % p.G;
-        v = __ldg(reinterpret_cast<const uint4*>(p.q + ((size_t)t * p.H + h) * D + c8 * 8));
-      }
-      *reinterpret_cast<uint4*>(qs + r * C::kQStride + c8 * 8) = v;
+  while (true) {
+    if (!mbar_wait(&full[stage], phase)) {
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+      return;
     }
-    named_bar(1, kDecodeWarps * 32);
+    const StageTag tg = tags[stage];
+    if (tg.u < 0) break;
 
-    uint32_t qf[(D <= 128) ? D / 16 : 1][4];
-    if constexpr (D <= 128) {
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int row = (mi & 1) * 8 + ri, col = ks * 16 + (mi >> 1) * 8;
-        ldsm_x4(smem_u32(qs + row * C::kQStride + col), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-      }
-    }
-
-    // Per-row causal and window bounds (rows beyond R admit nothing).
-    int hi0 = -1, hi1 = -1, lo0 = 0, lo1 = 0;
-    if (r0 < R) {
-      hi0 = past + r0 / p.G;  // last admitted position
-      lo0 = p.window >= 1 ? max(0, hi0 + 1 - p.window) : 0;
-    }
-    if (r1 < R) {
-      hi1 = past + r1 / p.G;
-      lo1 = p.window >= 1 ? max(0, hi1 + 1 - p.window) : 0;
-    }
-    // Keys outside [lo_min, kv_len) are never admitted by any row; their V
-    // rows are zeroed in shared memory before use so stale bytes (e.g. NaN
-    // in a partly filled last block) cannot leak through a zero weight.
-    const int lo_min = p.window >= 1 ? max(0, past + 1 - p.window) : 0;
-
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[D / 8][4];
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-    int last_stage = stage;
-    for (int key0 = start; key0 < end; key0 += kStageKeys) {
-      if (!mbar_wait(&full[stage], phase)) {
+    if (tg.flags & kFirst) {
+      // New item: its query tile, row bounds and a fresh softmax state.
+      if (!mbar_wait(&q_full[tg.qi], quse[tg.qi] & 1)) {
         if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
         return;
       }
-      const int mask = tags[stage].mask;
-      uint8_t* kt = stages + stage * C::kStageBytes;
-      uint8_t* vt = kt + C::kTileBytes;
-      const int kw = key0 + warp * 16;  // first key position of this warp
-
-      // Zero V rows of never-admitted keys among this warp's 16.
-      const bool edge = (kw + 16 > si.kv_len) || (kw < lo_min);
-      if (edge) {
-        for (int i = lane; i < 16 * C::kChunks * 8; i += 32) {
-          const int kr = i / (C::kChunks * 8), rem = i % (C::kChunks * 8);
-          const int pos = kw + kr;
-          if (pos >= si.kv_len || pos < lo_min) {
-            const int c = rem >> 3, col16 = rem & 7;
-            *reinterpret_cast<uint4*>(vt + c * (kStageKeys * 128) + (warp * 16 + kr) * 128 + col16 * 16) =
-                make_uint4(0, 0, 0, 0);
-          }
-        }
-        __syncwarp();
-      }
-
-      if (kw < end && kw + 16 > lo_min) {
-        // ---- S = Q K^T for 16 rows x 16 keys
-        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      quse[tg.qi]++;
+      qcur = qbuf + tg.qi * C::kQBytes;
+      if constexpr (D <= 128) {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int row = (mi & 1) * 8 + ri;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t a[4];
-          if constexpr (D <= 128) {
-            a[0] = qf[ks][0]; a[1] = qf[ks][1]; a[2] = qf[ks][2]; a[3] = qf[ks][3];
-          } else {
-            const int mi = lane >> 3, ri = lane & 7;
-            const int row = (mi & 1) * 8 + ri, col = ks * 16 + (mi >> 1) * 8;
-            ldsm_x4(smem_u32(qs + row * C::kQStride + col), a[0], a[1], a[2], a[3]);
-          }
-          const int mi = lane >> 3, ri = lane & 7;
-          const int key = warp * 16 + (mi >> 1) * 8 + ri;
-          const int d16 = ks * 16 + (mi & 1) * 8;
-          const uint32_t addr = smem_u32(kt + (d16 >> 6) * (kStageKeys * 128) + swz(key, (d16 & 63) >> 3));
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          hmma16816(s[0], a, b0, b1);
-          hmma16816(s[1], a, b2, b3);
+          const int col = ks * 16 + (mi >> 1) * 8;
+          ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), qf[ks][0], qf[ks][1],
+                  qf[ks][2], qf[ks][3]);
         }
-        // ---- scale, softcap, mask; row max
-        float tmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int pos = kw + nt * 8 + cq + (e & 1);
-            const int hi = (e < 2) ? hi0 : hi1;
-            const int lo = (e < 2) ? lo0 : lo1;
-            const int box = (pos - key0) / rows_per_box;
-            const bool ok = pos < end && pos <= hi && pos >= lo && !((mask >> box) & 1);
-            float x = s[nt][e] * scale;
-            if (capped) x = p.softcap * tanhf(x * inv_cap);
-            x *= kLog2e;
-            x = ok ? x : -INFINITY;
-            s[nt][e] = x;
-            tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
-          }
-        }
-        float alpha[2], muse[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
-          tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
-          const float mn = fmaxf(m[i], tmax[i]);
-          muse[i] = (mn == -INFINITY) ? 0.f : mn;
-          alpha[i] = exp2f(m[i] - muse[i]);
-          m[i] = mn;
-        }
-        float rs[2] = {0.f, 0.f};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float pv = exp2f(s[nt][e] - muse[e >> 1]);
-            s[nt][e] = pv;
-            rs[e >> 1] += pv;
-          }
-        }
-        l[0] = l[0] * alpha[0] + rs[0];
-        l[1] = l[1] * alpha[1] + rs[1];
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          o[i][0] *= alpha[0];
-          o[i][1] *= alpha[0];
-          o[i][2] *= alpha[1];
-          o[i][3] *= alpha[1];
-        }
-        uint32_t pa[4];
-        pa[0] = pack_half2(s[0][0], s[0][1]);
-        pa[1] = pack_half2(s[0][2], s[0][3]);
-        pa[2] = pack_half2(s[1][0], s[1][1]);
-        pa[3] = pack_half2(s[1][2], s[1][3]);
-        // ---- O += P V
-#pragma unroll
-        for (int nd = 0; nd < D / 16; ++nd) {
-          const int mi = lane >> 3, ri = lane & 7;
-          const int key = warp * 16 + (mi & 1) * 8 + ri;
-          const int d = nd * 16 + (mi >> 1) * 8;
-          const uint32_t addr = smem_u32(vt + (d >> 6) * (kStageKeys * 128) + swz(key, (d & 63) >> 3));
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(addr, b0, b1, b2, b3);
-          hmma16816(o[2 * nd], pa, b0, b1);
-          hmma16816(o[2 * nd + 1], pa, b2, b3);
-        }
-      }
-      last_stage = stage;
-      const bool last = key0 + kStageKeys >= end;
-      if (!last) {
-        if (edge) fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (lane == 0) mbar_arrive(&q_empty[tg.qi]);
       }
-      if (++stage == C::kStages) {
-        stage = 0;
-        phase ^= 1;
+      hi0 = hi1 = -1;
+      lo0 = lo1 = 0;
+      if (r0 < tg.R) {
+        hi0 = tg.past + r0 / p.G;  // last admitted position of the row
+        lo0 = p.window >= 1 ? max(0, hi0 + 1 - p.window) : 0;
+      }
+      if (r1 < tg.R) {
+        hi1 = tg.past + r1 / p.G;
+        lo1 = p.window >= 1 ? max(0, hi1 + 1 - p.window) : 0;
+      }
+      m[0] = m[1] = -INFINITY;
+      l[0] = l[1] = 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+
+    const int key0 = tg.key0, end = tg.end, mask = tg.flags & 0xff;
+    uint8_t* kt = stages + stage * C::kStageBytes;
+    uint8_t* vt = kt + C::kTileBytes;
+    const int kw = key0 + warp * 16;  // first key position of this warp
+
+    // Keys outside [lo_min, kv_len) are never admitted by any row; their V
+    // rows are zeroed in shared memory so stale bytes (e.g. NaN in a partly
+    // filled last block) cannot leak through a zero weight.
+    const bool edge = (kw + 16 > tg.kv_len) || (kw < tg.lo_min);
+    if (edge) {
+      for (int i = lane; i < 16 * C::kChunks * 8; i += 32) {
+        const int kr = i / (C::kChunks * 8), rem = i % (C::kChunks * 8);
+        const int pos = kw + kr;
+        if (pos >= tg.kv_len || pos < tg.lo_min) {
+          const int c = rem >> 3, col16 = rem & 7;
+          *reinterpret_cast<uint4*>(vt + tile_off<C::kChunks>(warp * 16 + kr, c, col16, log_r)) =
+              make_uint4(0, 0, 0, 0);
+        }
+      }
+      __syncwarp();
+    }
+
+    if (kw < end && kw + 16 > tg.lo_min) {
+      // ---- S = Q K^T for 16 rows x 16 keys
+      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a[4];
+        if constexpr (D <= 128) {
+          a[0] = qf[ks][0];
+          a[1] = qf[ks][1];
+          a[2] = qf[ks][2];
+          a[3] = qf[ks][3];
+        } else {
+          const int row = (mi & 1) * 8 + ri, col = ks * 16 + (mi >> 1) * 8;
+          ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), a[0], a[1], a[2], a[3]);
+        }
+        const int key = warp * 16 + (mi >> 1) * 8 + ri;
+        const int d16 = ks * 16 + (mi & 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_u32(kt + tile_off<C::kChunks>(key, d16 >> 6, (d16 & 63) >> 3, log_r)), b0, b1, b2, b3);
+        hmma16816(s[0], a, b0, b1);
+        hmma16816(s[1], a, b2, b3);
+      }
+      // ---- scale, softcap, mask; row max
+      float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int pos = kw + nt * 8 + cq + (e & 1);
+          const int hi = (e < 2) ? hi0 : hi1;
+          const int lo = (e < 2) ? lo0 : lo1;
+          const int box = (pos - key0) >> log_r;
+          const bool ok = pos < end && pos <= hi && pos >= lo && !((mask >> box) & 1);
+          float x = s[nt][e] * scale;
+          if (capped) x = p.softcap * tanhf(x * inv_cap);
+          x *= kLog2e;
+          x = ok ? x : -INFINITY;
+          s[nt][e] = x;
+          tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
+        }
+      }
+      float alpha[2], muse[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
+        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
+        const float mn = fmaxf(m[i], tmax[i]);
+        muse[i] = (mn == -INFINITY) ? 0.f : mn;
+        alpha[i] = exp2f(m[i] - muse[i]);
+        m[i] = mn;
+      }
+      float rs[2] = {0.f, 0.f};
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pv = exp2f(s[nt][e] - muse[e >> 1]);
+          s[nt][e] = pv;
+          rs[e >> 1] += pv;
+        }
+      }
+      l[0] = l[0] * alpha[0] + rs[0];
+      l[1] = l[1] * alpha[1] + rs[1];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= alpha[0];
+        o[i][1] *= alpha[0];
+        o[i][2] *= alpha[1];
+        o[i][3] *= alpha[1];
+      }
+      uint32_t pa[4];
+      pa[0] = pack_half2(s[0][0], s[0][1]);
+      pa[1] = pack_half2(s[0][2], s[0][3]);
+      pa[2] = pack_half2(s[1][0], s[1][1]);
+      pa[3] = pack_half2(s[1][2], s[1][3]);
+      // ---- O += P V
+#pragma unroll
+      for (int nd = 0; nd < D / 16; ++nd) {
+        const int key = warp * 16 + (mi & 1) * 8 + ri;
+        const int d = nd * 16 + (mi >> 1) * 8;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, d >> 6, (d & 63) >> 3, log_r)), b0, b1, b2, b3);
+        hmma16816(o[2 * nd], pa, b0, b1);
+        hmma16816(o[2 * nd + 1], pa, b2, b3);
       }
     }
 
-    // ---- merge the four warps through the last stage's buffer
+    if (!(tg.flags & kLast)) {
+      if (edge) fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    } else {
+      // ---- end of item: merge the four warps through this stage's buffer
+      float lt[2] = {l[0], l[1]};
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      l[i] += __shfl_xor_sync(0xffffffffu, l[i], 1);
-      l[i] += __shfl_xor_sync(0xffffffffu, l[i], 2);
-    }
-    named_bar(1, kDecodeWarps * 32);  // every warp is done reading the stage
-    float* mrg = reinterpret_cast<float*>(stages + last_stage * C::kStageBytes);
-    float* mw = mrg + warp * 16 * D;
+      for (int i = 0; i < 2; ++i) {
+        lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], 1);
+        lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], 2);
+      }
+      named_bar(1, kDecodeWarps * 32);  // every warp is done reading the stage
+      float* mrg = reinterpret_cast<float*>(kt);
+      float* mw = mrg + warp * 16 * D;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      const int d = i * 8 + cq;
-      *reinterpret_cast<float2*>(mw + r0 * D + d) = make_float2(o[i][0], o[i][1]);
-      *reinterpret_cast<float2*>(mw + r1 * D + d) = make_float2(o[i][2], o[i][3]);
-    }
-    if ((lane & 3) == 0) {
-      mls[warp * 16 + r0] = make_float2(m[0], l[0]);
-      mls[warp * 16 + r1] = make_float2(m[1], l[1]);
-    }
-    named_bar(1, kDecodeWarps * 32);
-    const int nsplit = si.dec_count;
-    for (int e = ctid; e < R * D; e += kDecodeWarps * 32) {
-      const int r = e / D, d = e - r * D;
-      float M = -INFINITY;
+      for (int i = 0; i < D / 8; ++i) {
+        const int d = i * 8 + cq;
+        *reinterpret_cast<float2*>(mw + r0 * D + d) = make_float2(o[i][0], o[i][1]);
+        *reinterpret_cast<float2*>(mw + r1 * D + d) = make_float2(o[i][2], o[i][3]);
+      }
+      if ((lane & 3) == 0) {
+        mls[warp * 16 + r0] = make_float2(m[0], lt[0]);
+        mls[warp * 16 + r1] = make_float2(m[1], lt[1]);
+      }
+      named_bar(1, kDecodeWarps * 32);
+      for (int e = ctid; e < tg.R * D; e += kDecodeWarps * 32) {
+        const int r = e / D, d = e - r * D;
+        float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, mls[w * 16 + r].x);
-      float acc = 0.f, den = 0.f;
-      if (M != -INFINITY) {
+        for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, mls[w * 16 + r].x);
+        float acc = 0.f, den = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) {
-          const float2 ml = mls[w * 16 + r];
-          const float f = exp2f(ml.x - M);
-          den += f * ml.y;
-          acc += f * mrg[(w * 16 + r) * D + d];
+          for (int w = 0; w < kDecodeWarps; ++w) {
+            const float2 ml = mls[w * 16 + r];
+            const float f = exp2f(ml.x - M);
+            den += f * ml.y;
+            acc += f * mrg[(w * 16 + r) * D + d];
+          }
+        }
+        if (tg.nsplit == 1) {
+          const int t = tg.t0 + r / p.G, h = tg.k * p.G + r % p.G;
+          p.out[((size_t)t * p.H + h) * D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+        } else {
+          const size_t row = (size_t)tg.u * kDecodeRows + r;
+          p.part_o[row * D + d] = acc;
+          if (d == 0) p.part_ml[row] = make_float2(M, den);
         }
       }
-      if (nsplit == 1) {
-        const int t = si.t0 + r / p.G, h = k * p.G + r % p.G;
-        p.out[((size_t)t * p.H + h) * D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
-      } else {
-        const size_t row = (size_t)u * kDecodeRows + r;
-        p.part_o[row * D + d] = acc;
-        if (d == 0) p.part_ml[row] = make_float2(M, den);
+      fence_proxy_async_smem();
+      named_bar(1, kDecodeWarps * 32);
+      if (lane == 0) {
+        mbar_arrive(&empty[stage]);
+        if constexpr (D > 128) mbar_arrive(&q_empty[tg.qi]);
       }
     }
-    fence_proxy_async_smem();
-    named_bar(1, kDecodeWarps * 32);
-    if (lane == 0) mbar_arrive(&empty[last_stage]);
+    if (++stage == C::kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
   }
 }
 
 template <int D>
-cudaError_t configure_d(size_t* smem) {
+cudaError_t configure_d(size_t* smem, int* ctas) {
   *smem = DecodeCfg<D>::kSmemBytes;
-  return cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)DecodeCfg<D>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DecodeCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D>, kThreads, *smem);
+  *ctas = n > 0 ? n : 1;
+  return e;
 }
 
 }  // namespace
 
 cudaError_t decode_configure(int head_size, int* ctas_per_sm, size_t* smem) {
-  cudaError_t e;
   switch (head_size) {
-    case 64: e = configure_d<64>(smem); break;
-    case 128: e = configure_d<128>(smem); break;
-    case 256: e = configure_d<256>(smem); break;
+    case 64: return configure_d<64>(smem, ctas_per_sm);
+    case 128: return configure_d<128>(smem, ctas_per_sm);
+    case 256: return configure_d<256>(smem, ctas_per_sm);
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  int n = 0;
-  switch (head_size) {
-    case 64: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, kThreads, *smem); break;
-    case 128: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, kThreads, *smem); break;
-    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<256>, kThreads, *smem); break;
-  }
-  *ctas_per_sm = n > 0 ? n : 1;
-  return e;
 }
 
-cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                          int grid, cudaStream_t s) {
+cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                          const DecodeParams& p, int grid, cudaStream_t s) {
   switch (head_size) {
-    case 64: decode_kernel<64><<<grid, kThreads, DecodeCfg<64>::kSmemBytes, s>>>(tk, tv, p); break;
-    case 128: decode_kernel<128><<<grid, kThreads, DecodeCfg<128>::kSmemBytes, s>>>(tk, tv, p); break;
-    case 256: decode_kernel<256><<<grid, kThreads, DecodeCfg<256>::kSmemBytes, s>>>(tk, tv, p); break;
+    case 64: return launch_pdl(decode_kernel<64>, grid, kThreads, DecodeCfg<64>::kSmemBytes, s, tk, tv, tq, p);
+    case 128: return launch_pdl(decode_kernel<128>, grid, kThreads, DecodeCfg<128>::kSmemBytes, s, tk, tv, tq, p);
+    case 256: return launch_pdl(decode_kernel<256>, grid, kThreads, DecodeCfg<256>::kSmemBytes, s, tk, tv, tq, p);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace pa

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pa {
 
 constexpr int kStageKeys = 64;      // keys per decode pipeline stage
@@ -20,22 +22,34 @@ constexpr int kPrefillKeys = 128;   // keys per prefill KV tile (UMMA N of S)
 enum Route { kRouteNone = 0, kRouteDecode = 1, kRoutePrefill = 2 };
 
 // Per-sequence facts derived on the device each step.
+// Decode items are listed full splits first (every split of every sequence
+// but its last), then the last, usually shorter, split of each sequence, so
+// the dynamic item queue hands out the long items first.
 struct SeqInfo {
   int q_len;      // new tokens (0 when the sequence is skipped)
   int kv_len;     // past + q_len
   int lo;         // first key position walked (64-aligned window start or 0)
   int t0;         // first packed row (cum[b])
-  int dec_first;  // first decode item of this sequence
+  int dec_first;  // item index of split 0 (splits 0..dec_count-2 are consecutive)
   int dec_count;  // decode splits (0 unless routed to decode)
+  int dec_last;   // item index of split dec_count-1
   int pre_first;  // first prefill tile of this sequence
   int pre_count;  // prefill query tiles (0 unless routed to prefill)
+  int pad[3];
 };
+
+__host__ __device__ inline int dec_item_of_split(const SeqInfo& s, int split) {
+  return split == s.dec_count - 1 ? s.dec_last : s.dec_first + split;
+}
 
 struct Counters {
   int n_dec;       // decode items (b, split) pairs
   int n_pre;       // prefill tiles (b, query tile)
   int n_comb;      // packed rows whose splits need the log-sum-exp merge
   int split_keys;  // keys per decode split this step
+  int dec_next;    // decode work queue head (reset to 0 by the work-list kernel)
+  int pre_next;    // prefill work queue head (reset to 0 by the work-list kernel)
+  int pad[2];
 };
 
 struct WorklistParams {
@@ -74,16 +88,17 @@ struct CacheWriteParams {
   int batch, token_count;
   int H, Hk, D, bs, NB, MB;
   int rotary, interleaved, rot_dim, rot_positions;
+  int parts;             // warps per token: 1 (K/V) + query parts when rotating Q
+  int q_heads_per_part;  // query heads per query part
   int* err;
 };
 
 struct DecodeParams {
-  const __half* q;  // [T, H*D]
   __half* out;      // [T, H*D]
   const int* block_table;
   const SeqInfo* seq;
   const int2* dec_items;
-  const Counters* counters;
+  Counters* counters;  // n_dec, split_keys, and the item queue head
   float* part_o;    // [items*Hk*16*D]
   float2* part_ml;  // [items*Hk*16] (max in log2 units, sum)
   int* err;
@@ -92,6 +107,8 @@ struct DecodeParams {
   float softcap;     // 0 = off
   int window;        // -1 or >= 1
   int oob_row;       // a TMA row coordinate past the pool (zero fill)
+  int q_tile_tokens; // tokens per query TMA box (16 / G)
+  int log_box_rows;  // log2(min(block_size, 64)): pool rows per TMA box
 };
 
 struct CombineParams {
@@ -119,12 +136,32 @@ struct PrefillParams {
   int oob_row;
 };
 
+// Launch with the programmatic stream-serialization attribute, so the
+// kernel's CTAs may become resident while the previous kernel on the stream
+// finishes; the kernel calls griddepcontrol.wait before touching its
+// predecessor's results.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (defined in the .cu files).
-cudaError_t launch_worklist(const WorklistParams& p, cudaStream_t s);
 cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s);
+cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, cudaStream_t s);
 cudaError_t decode_configure(int head_size, int* ctas_per_sm, size_t* smem);
 cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const DecodeParams& p, int grid, cudaStream_t s);
+                          const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -8,16 +8,17 @@
 // One CTA of 1024 threads walks the batch in chunks of 1024 sequences with a
 // carried block scan, so there is no cap on the batch size (the design's
 // section 18.3 names the 256-sequence BlockScan cap as a defect).
+#pragma once
 #include "step.h"
 #include "../../include/pa.h"
 
 namespace pa {
-namespace {
+namespace worklist {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 1024;  // the builder runs in one CTA of this size
 
 struct Int3 {
-  int a, b, c;
+  int a, b, c, d;  // full decode splits, prefill tiles, combine rows, last decode splits
 };
 
 // Exclusive scan of three counters across the block; returns the prefix and
@@ -32,10 +33,12 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
     int a = __shfl_up_sync(0xffffffffu, inc.a, o);
     int b = __shfl_up_sync(0xffffffffu, inc.b, o);
     int c = __shfl_up_sync(0xffffffffu, inc.c, o);
+    int d = __shfl_up_sync(0xffffffffu, inc.d, o);
     if (lane >= o) {
       inc.a += a;
       inc.b += b;
       inc.c += c;
+      inc.d += d;
     }
   }
   if (lane == 31) warp_sums[warp] = inc;
@@ -48,19 +51,21 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
       int a = __shfl_up_sync(0xffffffffu, wi.a, o);
       int b = __shfl_up_sync(0xffffffffu, wi.b, o);
       int c = __shfl_up_sync(0xffffffffu, wi.c, o);
+      int d = __shfl_up_sync(0xffffffffu, wi.d, o);
       if (lane >= o) {
         wi.a += a;
         wi.b += b;
         wi.c += c;
+        wi.d += d;
       }
     }
-    warp_sums[lane] = Int3{wi.a - w.a, wi.b - w.b, wi.c - w.c};
+    warp_sums[lane] = Int3{wi.a - w.a, wi.b - w.b, wi.c - w.c, wi.d - w.d};
     if (lane == 31) total = wi;
   }
   __syncthreads();
   *tot = total;
   Int3 base = warp_sums[warp];
-  Int3 out{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c};
+  Int3 out{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c, base.d + inc.d - v.d};
   __syncthreads();
   return out;
 }
@@ -116,7 +121,78 @@ __device__ Lens read_lens(const WorklistParams& p, int b, int* err_bits) {
   return L;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) worklist_kernel(WorklistParams p) {
+__device__ int split_keys_for(const WorklistParams& p, long long total) {
+  if (p.split_keys_fixed > 0) return p.split_keys_fixed;
+  long long per = (total + p.target_pairs - 1) / max(p.target_pairs, 1);
+  per = (per + kStageKeys - 1) / kStageKeys * kStageKeys;
+  return (int)min(max(per, (long long)kStageKeys), (long long)(1 << 30));
+}
+
+__device__ void write_counters(const WorklistParams& p, bool overflow, Int3 tot, int split_keys, int* err_bits) {
+  Counters c;
+  if (overflow) *err_bits |= PA_DEVERR_KV_BOUND;
+  c.n_dec = overflow ? 0 : tot.a + tot.d;
+  c.n_pre = overflow ? 0 : tot.b;
+  c.n_comb = overflow ? 0 : tot.c;
+  c.split_keys = split_keys;
+  c.dec_next = 0;
+  c.pre_next = 0;
+  c.pad[0] = c.pad[1] = 0;
+  *p.counters = c;
+}
+
+// Batches of at most one CTA's width: every sequence stays in its thread's
+// registers from the length read to the item writes (one pass).
+__device__ void build_small(const WorklistParams& p) {
+  int err_bits = 0;
+  const int b = threadIdx.x;
+  Lens L{0, 0, 0, 0, kRouteNone};
+  if (b < p.batch) L = read_lens(p, b, &err_bits);
+  const long long span = (L.route == kRouteDecode) ? (long long)(L.past + L.q - L.lo) : 0;
+  const int split_keys = split_keys_for(p, block_sum_ll(span));
+  Int3 cnt{0, 0, 0, 0};
+  if (L.route == kRouteDecode) {
+    const int n = (L.past + L.q - L.lo + split_keys - 1) / split_keys;
+    cnt.a = n - 1;
+    cnt.d = 1;
+    if (n > 1) cnt.c = L.q;
+  } else if (L.route == kRoutePrefill) {
+    cnt.b = (L.q + p.prefill_tile_tokens - 1) / p.prefill_tile_tokens;
+  }
+  Int3 tot;
+  const Int3 pre = block_exclusive_scan3(cnt, &tot);
+  const bool overflow = tot.a + tot.d > p.cap_dec || tot.b > p.cap_pre || tot.c > p.cap_comb;
+  if (b < p.batch) {
+    SeqInfo si;
+    si.q_len = L.q;
+    si.kv_len = L.past + L.q;
+    si.lo = L.lo;
+    si.t0 = L.t0;
+    si.dec_first = pre.a;
+    si.dec_count = cnt.a + cnt.d;
+    si.dec_last = tot.a + pre.d;
+    si.pre_first = pre.b;
+    si.pre_count = cnt.b;
+    si.pad[0] = pre.c;
+    si.pad[1] = si.pad[2] = 0;
+    p.seq[b] = si;
+    if (!overflow) {
+      for (int s = 0; s < cnt.a; ++s) p.dec_items[si.dec_first + s] = make_int2(b, s);
+      if (cnt.d) p.dec_items[si.dec_last] = make_int2(b, cnt.a);
+      for (int j = 0; j < cnt.c; ++j) p.comb_rows[pre.c + j] = make_int2(L.t0 + j, b);
+      for (int s = 0; s < cnt.b; ++s) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
+    }
+  }
+  if (threadIdx.x == 0) write_counters(p, overflow, tot, split_keys, &err_bits);
+  if (err_bits) atomicOr(p.err, err_bits);
+}
+
+// Body of the builder; must be executed by all kThreads threads of one CTA.
+__device__ void build(const WorklistParams& p) {
+  if (p.batch <= kThreads) {
+    build_small(p);
+    return;
+  }
   int err_bits = 0;
   // Pass 1: total decode span, which sets the keys per split.
   long long span = 0;
@@ -128,26 +204,23 @@ __global__ void __launch_bounds__(kThreads, 1) worklist_kernel(WorklistParams p)
       if (L.route == kRouteDecode) span += (long long)(L.past + L.q - L.lo);
     }
   }
-  long long total = block_sum_ll(span);
-  int split_keys = p.split_keys_fixed;
-  if (split_keys <= 0) {
-    long long per = (total + p.target_pairs - 1) / max(p.target_pairs, 1);
-    per = (per + kStageKeys - 1) / kStageKeys * kStageKeys;
-    split_keys = (int)min(max(per, (long long)kStageKeys), (long long)(1 << 30));
-  }
+  const int split_keys = split_keys_for(p, block_sum_ll(span));
 
-  // Pass 2: counts, scans, work items.
-  Int3 carry{0, 0, 0};
+  // Pass 2: counts and scans; the items are written in pass 3 once the
+  // number of full decode splits (which precede every last split) is known.
+  Int3 carry{0, 0, 0, 0};
   for (int base = 0; base < p.batch; base += kThreads) {
     int b = base + threadIdx.x;
     Lens L{0, 0, 0, 0, kRouteNone};
-    Int3 cnt{0, 0, 0};
+    Int3 cnt{0, 0, 0, 0};
     if (b < p.batch) {
       L = read_lens(p, b, &err_bits);
       if (L.route == kRouteDecode) {
         int kv = L.past + L.q;
-        cnt.a = (kv - L.lo + split_keys - 1) / split_keys;
-        if (cnt.a > 1) cnt.c = L.q;
+        int n = (kv - L.lo + split_keys - 1) / split_keys;
+        cnt.a = n - 1;
+        cnt.d = 1;
+        if (n > 1) cnt.c = L.q;
       } else if (L.route == kRoutePrefill) {
         cnt.b = (L.q + p.prefill_tile_tokens - 1) / p.prefill_tile_tokens;
       }
@@ -161,43 +234,40 @@ __global__ void __launch_bounds__(kThreads, 1) worklist_kernel(WorklistParams p)
       si.lo = L.lo;
       si.t0 = L.t0;
       si.dec_first = carry.a + pre.a;
-      si.dec_count = cnt.a;
+      si.dec_count = cnt.a + cnt.d;
+      si.dec_last = carry.d + pre.d;  // offset by the full-split total in pass 3
       si.pre_first = carry.b + pre.b;
       si.pre_count = cnt.b;
+      si.pad[0] = carry.c + pre.c;    // first combine row
+      si.pad[1] = si.pad[2] = 0;
       p.seq[b] = si;
-      // Capacity guards: the host sized every list from static bounds that
-      // these counts cannot exceed for validated lengths; if one ever would,
-      // nothing is written past the list and the whole step is dropped below.
-      for (int s = 0; s < cnt.a; ++s)
-        if (si.dec_first + s < p.cap_dec) p.dec_items[si.dec_first + s] = make_int2(b, s);
-      for (int s = 0; s < cnt.b; ++s)
-        if (si.pre_first + s < p.cap_pre) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
-      int c0 = carry.c + pre.c;
-      for (int j = 0; j < cnt.c; ++j)
-        if (c0 + j < p.cap_comb) p.comb_rows[c0 + j] = make_int2(L.t0 + j, b);
     }
     carry.a += tot.a;
     carry.b += tot.b;
     carry.c += tot.c;
+    carry.d += tot.d;
   }
-  if (threadIdx.x == 0) {
-    Counters c;
-    bool overflow = carry.a > p.cap_dec || carry.b > p.cap_pre || carry.c > p.cap_comb;
-    if (overflow) err_bits |= PA_DEVERR_KV_BOUND;
-    c.n_dec = overflow ? 0 : carry.a;
-    c.n_pre = overflow ? 0 : carry.b;
-    c.n_comb = overflow ? 0 : carry.c;
-    c.split_keys = split_keys;
-    *p.counters = c;
+  const int n_full = carry.a;
+  const bool overflow = carry.a + carry.d > p.cap_dec || carry.b > p.cap_pre || carry.c > p.cap_comb;
+  __syncthreads();
+  // Pass 3: work items (skipped entirely if a list would overflow).
+  if (!overflow) {
+    for (int b = threadIdx.x; b < p.batch; b += kThreads) {
+      SeqInfo si = p.seq[b];
+      if (si.dec_count > 0) {
+        si.dec_last += n_full;
+        p.seq[b].dec_last = si.dec_last;
+        for (int s = 0; s + 1 < si.dec_count; ++s) p.dec_items[si.dec_first + s] = make_int2(b, s);
+        p.dec_items[si.dec_last] = make_int2(b, si.dec_count - 1);
+        if (si.dec_count > 1)
+          for (int j = 0; j < si.q_len; ++j) p.comb_rows[si.pad[0] + j] = make_int2(si.t0 + j, b);
+      }
+      for (int s = 0; s < si.pre_count; ++s) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
+    }
   }
+  if (threadIdx.x == 0) write_counters(p, overflow, carry, split_keys, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
 }
 
-}  // namespace
-
-cudaError_t launch_worklist(const WorklistParams& p, cudaStream_t s) {
-  worklist_kernel<<<1, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
-}
-
+}  // namespace worklist
 }  // namespace pa
