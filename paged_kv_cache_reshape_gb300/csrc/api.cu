@@ -635,7 +635,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   // 4. varlen prefill on tensor memory
   if (h->prefill_ready) {
     CUtensorMap tq, tkp, tvp;
-    const int prow = std::min(c.block_size, pa::kPrefillKeys);
+    const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_tile_tokens) ||
         !encode_map(&tkp, key_cache, D, c.kv_num_heads, pool_rows, 1, prow) ||
         !encode_map(&tvp, value_cache, D, c.kv_num_heads, pool_rows, 1, prow))
@@ -654,6 +654,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.MB = c.max_blocks_per_seq;
     p.NB = c.num_blocks;
     p.tile_tokens = h->prefill_tile_tokens;
+    p.log_page_rows = 31 - __builtin_clz((unsigned)prow);
     p.scale = h->scale;
     p.softcap = c.softcap;
     p.window = c.local_window_size;

@@ -101,6 +101,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
   uint64_t* q_full = empty + C::kStages;
   uint64_t* q_empty = q_full + 2;
 
+  // Everything below reads the prologue's work list and the pool it wrote.
+  griddep_wait();
+  if ((int)blockIdx.x >= p.counters->n_dec * p.Hk) return;  // no item for this CTA
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -114,8 +118,6 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
     fence_mbar_init();
   }
   __syncthreads();
-  // Everything below reads the prologue's work list and the pool it wrote.
-  griddep_wait();
   griddep_launch_dependents();
 
   if (warp == kDecodeWarps) {

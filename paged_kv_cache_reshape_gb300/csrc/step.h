@@ -126,10 +126,11 @@ struct PrefillParams {
   const int* block_table;
   const SeqInfo* seq;
   const int2* pre_tiles;
-  const Counters* counters;
+  Counters* counters;  // n_pre and the tile queue head
   int* err;
   int H, Hk, G, bs, MB, NB;
   int tile_tokens;  // tokens per query tile (rows = tile_tokens * G <= 128)
+  int log_page_rows;  // log2(min(block_size, keys per KV tile)): pool rows per TMA box
   float scale;
   float softcap;
   int window;
@@ -164,6 +165,7 @@ cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMa
                           const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);
+int prefill_keys_per_tile(int head_size);
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 

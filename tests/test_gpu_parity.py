@@ -132,3 +132,41 @@ def test_full_size_decode_config(index):
     op, out, err = run(step)
     assert err == 0, f"device error {err:#x}"
     check_sampled(host, step, out, n_rows=160)
+
+
+# ------------------------------------------------------------ prefill path
+PREFILL = [
+    cs("pf_d128_g4_bs32_long", 8, 2, 128, 32, [0, 70, 5], [300, 45, 129], seed=31),
+    cs("pf_d64_mha_bs16", 4, 4, 64, 16, [0, 200], [150, 33], seed=32),
+    cs("pf_d256_g2_bs64_window_cap", 4, 2, 256, 64, [0, 100], [200, 70], scale=1 / 16, softcap=50.0,
+       local_window_size=97, seed=33),
+    cs("pf_d128_g8_bs16_rotary", 16, 2, 128, 16, [3, 0], [40, 17], do_rotary=1, seed=34),
+    cs("pf_d128_g1_bs128_window", 4, 4, 128, 128, [0, 250], [260, 7], local_window_size=130, seed=35),
+    cs("pf_d128_g4_bs256", 8, 2, 128, 256, [0, 511], [257, 2], seed=36),
+    cs("pf_g3_rows_not_pow2", 6, 2, 64, 16, [0, 9], [50, 20], seed=37),
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL, ids=lambda s: s.name)
+def test_prefill_step_matches_oracle(shape):
+    _full(shape)
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_small_step_through_prefill_kernel(shape):
+    _full(shape, options=[(pa.PA_OPT_DECODE_MAX_ROWS, 0)])
+
+
+def test_mixed_routing_in_one_step():
+    # tiny mixed step with decode for <= 4 rows: sequence 0 (5 tokens x 2 heads)
+    # goes to the tensor-core prefill kernel, the others to split-KV decode
+    _full(workloads.config_shape(0), options=[(pa.PA_OPT_DECODE_MAX_ROWS, 4)])
+
+
+def test_full_size_mixed_step():
+    shape = workloads.config_shape(2)
+    step = make(shape, device="cuda", gen_device="cuda")
+    host = host_copy(step)
+    op, out, err = run(step)
+    assert err == 0, f"device error {err:#x}"
+    check_sampled(host, step, out, n_rows=160)
