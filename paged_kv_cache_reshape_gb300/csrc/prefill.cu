@@ -8,8 +8,8 @@
 //   softmax          one thread per row reads its S row from TMEM, applies
 //                    scale, softcap, the causal bound past + j + 1, the
 //                    window [kv_len - W, kv_len) and -1 blocks, keeps the
-//                    running max / sum in fp32, rescales its O row in TMEM
-//                    when the max grows, and writes P (fp16) to shared memory
+//                    running max / sum in fp32 and writes P (fp16) to shared
+//                    memory
 //   O += P V         tcgen05.mma, M=128, N=head_size, K=keys -> TMEM
 // then O / l is written as fp16.  This is the online-softmax flash
 // iteration of the CPU GQA notes (onnxruntime 1.27.0 docs,
@@ -19,11 +19,17 @@
 // (section 18.1), a KV tile may span several pages: each page is its own
 // TMA box, so any power-of-two block_size >= 16 works.
 //
+// The running max is kept lazily: a row rescales its O accumulator (a TMEM
+// read-modify-write) only when its max grows by more than 2^8, so P stays
+// below 256 and the final O / l is unchanged (both carry the same factor).
+//
 // Warp roles (192 threads, one CTA per SM, persistent over a device queue):
 //   warps 0-3  softmax + epilogue (thread = query row = TMEM lane)
-//   warp 4     TMA producer: tile descriptions, Q tile, K/V tiles (2 stages)
+//   warp 4     TMA producer: tile descriptions, Q tile (double-buffered for
+//              head_size <= 128), K/V tiles (2 stages; one lane per box)
 //   warp 5     TMEM owner and MMA issuer (one elected thread)
-// S for KV tile i+1 is computed while the softmax warps work on tile i.
+// S for KV tile i+1 is computed while the softmax warps work on tile i, and
+// the softmax computes P for tile i while P V of tile i-1 is still running.
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -34,18 +40,20 @@ namespace {
 constexpr int kThreads = 6 * 32;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
 
 template <int D>
 struct PrefillCfg {
   static constexpr int kKeys = (D == 256) ? 64 : 128;   // keys per KV tile
   static constexpr int kChunks = D / 64;                // 128-byte channel chunks
+  static constexpr int kQBufs = (D == 256) ? 1 : 2;     // Q tiles in flight
   static constexpr int kQBytes = kPrefillRows * D * 2;  // [chunk][128 rows][128 B]
   static constexpr int kPBytes = kPrefillRows * kKeys * 2;
   static constexpr int kTileBytes = kKeys * D * 2;      // K or V tile [chunk][keys][128 B]
   static constexpr int kStages = 2;
   static constexpr int kSCol = 0, kOCol = kKeys;        // TMEM columns of S and O
   static constexpr int kTmemCols = (kKeys + D <= 256) ? 256 : 512;
-  static constexpr int kDataBytes = kQBytes + kPBytes + kStages * 2 * kTileBytes;
+  static constexpr int kDataBytes = kQBufs * kQBytes + kPBytes + kStages * 2 * kTileBytes;
   static constexpr int kSmemBytes = 1024 + kDataBytes + 1024;
 };
 
@@ -65,7 +73,7 @@ struct TileInfo {
 struct Ctrl {
   TileInfo info[2];
   uint32_t kv_mask[2];  // per stage: bit p = page p zero-filled (unmapped / past the end)
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[2], kv_empty[2];
   uint64_t s_full, s_free, p_full, o_done;
   uint64_t info_full[2], info_empty[2];
@@ -84,7 +92,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
-template <int D>
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -92,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KEYS = C::kKeys;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;
-  uint8_t* p_s = q_s + C::kQBytes;
-  uint8_t* kv_s = p_s + C::kPBytes;  // stage st: K at st*2*tile, V right after
+  uint8_t* q_s = smem;                          // [kQBufs][kQBytes]
+  uint8_t* p_s = q_s + C::kQBufs * C::kQBytes;  // [kPBytes]
+  uint8_t* kv_s = p_s + C::kPBytes;             // stage st: K at st*2*tile, V right after
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::kDataBytes);
   volatile int* abort = &ctl->abort;
 
@@ -106,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(&ctl->q_full, 1);
-    mbar_init(&ctl->q_empty, 1);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->q_full[i], 1);
+      mbar_init(&ctl->q_empty[i], 1);
       mbar_init(&ctl->kv_full[i], 1);
       mbar_init(&ctl->kv_empty[i], 1);
       mbar_init(&ctl->info_full[i], 1);
@@ -139,32 +153,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      const uint32_t q_bytes = C::kChunks * p.G * p.tile_tokens * 128;
-      uint32_t g = 0;
-      int last_q = -1;  // last tile whose Q load was issued
-      for (uint32_t tt = 0;; ++tt) {
-        const int slot = tt & 1;
-        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) break;
-        const int u = atomicAdd(&p.counters->pre_next, 1);
-        TileInfo& ti = ctl->info[slot];
-        if (u >= n_work) {
+    }
+    const uint32_t q_bytes = C::kChunks * p.G * p.tile_tokens * 128;
+    uint32_t g = 0;
+    int last_q = -1;  // last tile whose Q load was issued
+    bool ok = true;
+    for (uint32_t tt = 0; ok; ++tt) {
+      const int slot = tt & 1;
+      int u = 0;
+      if (lane == 0) {
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
+        else u = atomicAdd(&p.counters->pre_next, 1);
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u == -2) break;
+      TileInfo& ti = ctl->info[slot];
+      if (u >= n_work) {
+        if (lane == 0) {
           ti.u = -1;
           mbar_arrive(&ctl->info_full[slot]);
-          break;
         }
-        const int tile = u / p.Hk, k = u - tile * p.Hk;
-        const int2 bq = p.pre_tiles[tile];
-        const SeqInfo si = p.seq[bq.x];
-        const int q0 = bq.y * p.tile_tokens;
-        const int ntok = min(p.tile_tokens, si.q_len - q0);
-        const int pos0 = si.kv_len - si.q_len + q0;
-        const int hi_end = pos0 + ntok;  // one past the last row's last admitted key
-        const int lo_min = p.window >= 1 ? max(0, pos0 + 1 - p.window) : 0;
-        const int key_lo = lo_min & ~(KEYS - 1);
-        const int n_kv = (hi_end - key_lo + KEYS - 1) / KEYS;
+        break;
+      }
+      const int tile = u / p.Hk, k = u - tile * p.Hk;
+      const int2 bq = p.pre_tiles[tile];
+      const SeqInfo si = p.seq[bq.x];
+      const int q0 = bq.y * p.tile_tokens;
+      const int ntok = min(p.tile_tokens, si.q_len - q0);
+      const int pos0 = si.kv_len - si.q_len + q0;
+      const int hi_end = pos0 + ntok;  // one past the last row's last admitted key
+      const int lo_min = p.window >= 1 ? max(0, pos0 + 1 - p.window) : 0;
+      const int key_lo = lo_min & ~(KEYS - 1);
+      const int n_kv = (hi_end - key_lo + KEYS - 1) / KEYS;
+      const int t0 = si.t0 + q0;
+      if (lane == 0) {
         ti.u = u;
         ti.k = k;
-        ti.t0 = si.t0 + q0;
+        ti.t0 = t0;
         ti.ntok = ntok;
         ti.pos0 = pos0;
         ti.key_lo = key_lo;
@@ -172,59 +197,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         ti.kv_len = si.kv_len;
         ti.lo_min = lo_min;
         mbar_arrive(&ctl->info_full[slot]);
-
         // Q tile: box {64, G, tile_tokens} per channel chunk.
-        if (!wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err)) break;
-        mbar_arrive_expect_tx(&ctl->q_full, q_bytes);
-        last_q = (int)tt;
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(q_s + c * (kPrefillRows * 128), &tm_q, c * 64, k * p.G, ti.t0, &ctl->q_full);
+        const int qb = tt % C::kQBufs;
+        if (!wait_or_abort(&ctl->q_empty[qb], ((tt / C::kQBufs) & 1) ^ 1, abort, p.err)) {
+          ok = false;
+        } else {
+          mbar_arrive_expect_tx(&ctl->q_full[qb], q_bytes);
+          last_q = (int)tt;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(q_s + qb * C::kQBytes + c * (kPrefillRows * 128), &tm_q, c * 64, k * p.G, t0,
+                        &ctl->q_full[qb]);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
 
-        // K/V tiles, one 3-D box {64, 1, R} per page and channel chunk.
-        const int* bt_row = p.block_table + (size_t)bq.x * p.MB;
-        bool ok = true;
-        for (int i = 0; i < n_kv && ok; ++i, ++g) {
-          const int st = g & 1;
+      // Block ids, 32 block-table rows at a time, one per lane.
+      const int* bt_row = p.block_table + (size_t)bq.x * p.MB;
+      auto load_id = [&](int r) -> int {
+        return (r < p.MB && r * p.bs < hi_end) ? __ldg(bt_row + r) : -1;
+      };
+      int win = key_lo / p.bs;
+      int id = load_id(win + lane);
+      for (int i = 0; i < n_kv; ++i, ++g) {
+        const int st = g & 1;
+        const int key0 = key_lo + i * KEYS;
+        if ((key0 + KEYS - 1) / p.bs >= win + 32) {
+          win = key0 / p.bs;
+          id = load_id(win + lane);
+        }
+        // lane pg < pages resolves page pg of this tile
+        const int pos = key0 + (lane << log_r);
+        const int idx = pos / p.bs - win;
+        const int blk = __shfl_sync(0xffffffffu, id, idx & 31);
+        int rc = p.oob_row;
+        if (lane < pages && pos < hi_end) {
+          if (blk >= 0 && blk < p.NB) rc = blk * p.bs + (pos & (p.bs - 1));
+          else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
+        if (lane == 0) {
           if (!wait_or_abort(&ctl->kv_empty[st], ((g >> 1) & 1) ^ 1, abort, p.err)) {
             ok = false;
-            break;
-          }
-          const int key0 = key_lo + i * KEYS;
-          int rowc[8];
-          uint32_t mask = 0;
-          for (int pg = 0; pg < pages; ++pg) {
-            const int pos = key0 + (pg << log_r);
-            int rc = p.oob_row;
-            if (pos < hi_end) {
-              const int blk = __ldg(bt_row + pos / p.bs);
-              if (blk >= 0 && blk < p.NB) rc = blk * p.bs + (pos & (p.bs - 1));
-              else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-            }
-            if (rc == p.oob_row) mask |= 1u << pg;
-            rowc[pg] = rc;
-          }
-          ctl->kv_mask[st] = mask;
-          mbar_arrive_expect_tx(&ctl->kv_full[st], 2 * C::kTileBytes);
-          uint8_t* ks = kv_s + st * 2 * C::kTileBytes;
-          uint8_t* vs = ks + C::kTileBytes;
-          for (int pg = 0; pg < pages; ++pg) {
-            for (int c = 0; c < C::kChunks; ++c) {
-              const uint32_t off = c * (KEYS * 128) + (pg << log_r) * 128;
-              tma_load_3d(ks + off, &tm_k, c * 64, k, rowc[pg], &ctl->kv_full[st]);
-              tma_load_3d(vs + off, &tm_v, c * 64, k, rowc[pg], &ctl->kv_full[st]);
-            }
+          } else {
+            ctl->kv_mask[st] = mask;
+            mbar_arrive_expect_tx(&ctl->kv_full[st], 2 * C::kTileBytes);
           }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-      }
-      if (*abort) {
-        // Gave up: let the copies already issued land before the CTA exits.
-        for (uint32_t i = 0; i < kWaitLimit && last_q >= 0 && !mbar_try_wait(&ctl->q_full, last_q & 1); ++i) {
+        // one box {64, 1, R} per (page, chunk, K|V); lane -> (page, chunk, tensor)
+        const int lp = lane / (2 * C::kChunks), lc = (lane >> 1) % C::kChunks;
+        const int prc = __shfl_sync(0xffffffffu, rc, lp & 31);
+        if (lp < pages) {
+          uint8_t* dst = kv_s + st * 2 * C::kTileBytes + (lane & 1) * C::kTileBytes + lc * (KEYS * 128) +
+                         ((uint32_t)lp << (log_r + 7));
+          tma_load_3d(dst, (lane & 1) ? &tm_v : &tm_k, lc * 64, k, prc, &ctl->kv_full[st]);
         }
-        for (int d = 1; d <= 2 && (int)g - d >= 0; ++d) {
-          const uint32_t gl = g - d;
-          for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->kv_full[gl & 1], (gl >> 1) & 1); ++i) {
-          }
+      }
+    }
+    if (lane == 0 && *abort) {
+      // Gave up: let the copies already issued land before the CTA exits.
+      for (uint32_t i = 0; i < kWaitLimit && last_q >= 0 &&
+                           !mbar_try_wait(&ctl->q_full[last_q % C::kQBufs], (last_q / C::kQBufs) & 1);
+           ++i) {
+      }
+      for (int d = 1; d <= 2 && (int)g - d >= 0; ++d) {
+        const uint32_t gl = g - d;
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->kv_full[gl & 1], (gl >> 1) & 1); ++i) {
         }
       }
     }
@@ -233,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, KEYS, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
-      const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
+      const uint32_t p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
       uint32_t g = 0, s_issued = 0, v = 0;
       bool ok = true;
       for (uint32_t tt = 0; ok; ++tt) {
@@ -241,8 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
         const TileInfo ti = ctl->info[slot];
         if (ti.u < 0) break;
-        if (!wait_or_abort(&ctl->q_full, tt & 1, abort, p.err)) break;
+        const int qb = tt % C::kQBufs;
+        if (!wait_or_abort(&ctl->q_full[qb], (tt / C::kQBufs) & 1, abort, p.err)) break;
         tc_fence_after();
+        const uint32_t q_addr = smem_u32(q_s + qb * C::kQBytes);
         // S(i) = Q K_i^T into TMEM columns [kSCol, kSCol + KEYS)
         auto issue_s = [&](uint32_t gi, bool last) -> bool {
           const int st = gi & 1;
@@ -257,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_f16(tmem + C::kSCol, a, b, idesc_s, ks > 0);
           }
           umma_commit(&ctl->s_full);
-          if (last) umma_commit(&ctl->q_empty);
+          if (last) umma_commit(&ctl->q_empty[qb]);
           ++s_issued;
           return true;
         };
@@ -298,10 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ----------------------------------------------------- softmax warps
     const int r = threadIdx.x;  // query row == TMEM lane
     const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    const bool capped = p.softcap > 0.f;
-    const float scale_log2 = p.scale * kLog2e;
-    const float inv_cap = capped ? 1.f / p.softcap : 0.f;
-    const float cap_log2 = p.softcap * kLog2e;
+    // Scores become log2-domain logits: x * mul (softcap applies its own).
+    const float mul = CAP ? 1.f : p.scale * kLog2e;
+    const float cap_in = CAP ? p.scale / p.softcap : 0.f;
+    const float cap_out = CAP ? p.softcap * kLog2e : 0.f;
     uint32_t g = 0, s_cnt = 0, v = 0;
     float x[KEYS];
     for (uint32_t tt = 0;; ++tt) {
@@ -313,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_ok = j < ti.ntok;
       const int hi = ti.pos0 + j;                            // last admitted position
       const int lo = p.window >= 1 ? hi + 1 - p.window : 0;  // first admitted position
-      float m = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY;  // reference max (log2 units) of P and O
+      float l = 0.f;
       bool ok = true;
       for (int i = 0; i < ti.n_kv; ++i) {
         const uint32_t gi = g + i;
@@ -333,32 +376,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->s_free);
 
-        // scale, softcap, masks, row max (log2 units)
-        const uint32_t mask = ctl->kv_mask[st];
-        const bool interior = row_ok && mask == 0 && key0 + KEYS - 1 <= hi && key0 >= lo;
-        float tmax = -INFINITY;
-        if (interior && !capped) {
+        if constexpr (CAP) {
 #pragma unroll
-          for (int c = 0; c < KEYS; ++c) {
-            x[c] *= scale_log2;
-            tmax = fmaxf(tmax, x[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < KEYS; ++c) {
-            const int pos = key0 + c;
-            const bool keep = row_ok && pos <= hi && pos >= lo && !((mask >> (c >> log_r)) & 1);
-            float y = capped ? cap_log2 * tanhf(x[c] * p.scale * inv_cap) : x[c] * scale_log2;
-            y = keep ? y : -INFINITY;
-            x[c] = y;
-            tmax = fmaxf(tmax, y);
-          }
+          for (int c = 0; c < KEYS; ++c) x[c] = cap_out * tanhf(x[c] * cap_in);
         }
-        const float m_new = fmaxf(m, tmax);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = exp2f(m - m_use);
+        // Admitted columns of this tile for this row: [c_lo, c_hi] minus
+        // zero-filled pages.
+        const uint32_t mask = ctl->kv_mask[st];
+        const int c_lo = row_ok ? max(lo - key0, 0) : KEYS;
+        const int c_hi = row_ok ? min(hi - key0, KEYS - 1) : -1;
+        if (c_lo > 0 || c_hi < KEYS - 1) {
+#pragma unroll
+          for (int c = 0; c < KEYS; ++c) x[c] = (c >= c_lo && c <= c_hi) ? x[c] : -INFINITY;
+        }
+        if (mask != 0) {
+#pragma unroll
+          for (int c = 0; c < KEYS; ++c) x[c] = ((mask >> (c >> log_r)) & 1) ? -INFINITY : x[c];
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < KEYS; ++c) tmax = fmaxf(tmax, x[c]);
+        const float cand = tmax * mul;
+        float alpha = 1.f;
+        if (cand > m_ref + kLazyRescale || (m_ref == -INFINITY && cand != -INFINITY)) {
+          alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - cand);
+          m_ref = cand;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < KEYS; ++c) {
+          const float e = ex2(fmaf(x[c], mul, -m_use));
+          x[c] = e;
+          rs += e;
+        }
+        l = l * alpha + rs;
+        // PV(i-1) must be done before O is rescaled and P is overwritten.
         if (i > 0) {
-          // PV(i-1) must be done before O is rescaled and P is overwritten.
           if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err)) {
             ok = false;
             break;
@@ -377,15 +431,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
           }
         }
-        float rs = 0.f;
-#pragma unroll
-        for (int c = 0; c < KEYS; ++c) {
-          const float e = exp2f(x[c] - m_use);
-          x[c] = e;
-          rs += e;
-        }
-        l = l * alpha + rs;
-        m = m_new;
         // Never-admitted keys of an edge tile: zero their V rows so stale
         // bytes (a partly filled last block) cannot leak through P = 0.
         if (key0 + KEYS > ti.kv_len || key0 < ti.lo_min) {
@@ -456,12 +501,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+template <int D, bool CAP>
+cudaError_t configure_dc() {
+  static_assert(sizeof(Ctrl) <= 1024, "control block");
+  static_assert(PrefillCfg<D>::kSmemBytes <= 227 * 1024, "shared memory");
+  return cudaFuncSetAttribute(prefill_kernel<D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)PrefillCfg<D>::kSmemBytes);
+}
+
 template <int D>
 cudaError_t configure_d(size_t* smem) {
   *smem = PrefillCfg<D>::kSmemBytes;
-  static_assert(sizeof(Ctrl) <= 1024, "control block");
-  return cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)PrefillCfg<D>::kSmemBytes);
+  cudaError_t e = configure_dc<D, false>();
+  return e != cudaSuccess ? e : configure_dc<D, true>();
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                     int grid, cudaStream_t s) {
+  if (p.softcap > 0.f)
+    return launch_pdl(prefill_kernel<D, true>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return launch_pdl(prefill_kernel<D, false>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -480,9 +540,9 @@ int prefill_keys_per_tile(int head_size) { return head_size == 256 ? 64 : 128; }
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int grid, cudaStream_t s) {
   switch (head_size) {
-    case 64: return launch_pdl(prefill_kernel<64>, grid, kThreads, PrefillCfg<64>::kSmemBytes, s, tq, tk, tv, p);
-    case 128: return launch_pdl(prefill_kernel<128>, grid, kThreads, PrefillCfg<128>::kSmemBytes, s, tq, tk, tv, p);
-    case 256: return launch_pdl(prefill_kernel<256>, grid, kThreads, PrefillCfg<256>::kSmemBytes, s, tq, tk, tv, p);
+    case 64: return launch_d<64>(tq, tk, tv, p, grid, s);
+    case 128: return launch_d<128>(tq, tk, tv, p, grid, s);
+    case 256: return launch_d<256>(tq, tk, tv, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
