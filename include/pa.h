@@ -182,6 +182,41 @@ PA_API const char* pa_last_error_message(pa_handle h);
 /* Frees the workspace.  NULL is accepted. */
 PA_API pa_status pa_destroy(pa_handle h);
 
+/* The whole step (as pa_forward) for callers that cannot allocate device
+ * memory: code running inside CUDA stream capture, under a memory pool
+ * they do not own, in an allocation-free serving loop, or that simply has
+ * no handle.  The design pages have no counterpart to this call.
+ *
+ * It needs no pa_create: cfg is passed on every call, and every scratch
+ * buffer (work lists, split-KV partials, the rotated-query buffer, the
+ * device error word) lives in one file-scope device array of 64 MiB that
+ * each GPU loading this library holds until the process exits.  The call
+ * makes no cudaMalloc/cudaFree and no other allocation; the caller still
+ * passes every input and the output.  Capacities (max_batch, max_tokens,
+ * head counts, head_size, do_rotary) whose scratch would exceed 64 MiB are
+ * rejected with PA_INVALID_ARGUMENT and a message giving the size needed.
+ *
+ * device_error: optional caller-owned device int32 that receives the
+ * PA_DEVERR_* bits (OR-ed; the caller clears it).  When NULL the bits go
+ * to a word inside the shared scratch, cleared at the start of each call,
+ * that the caller cannot read.
+ *
+ * The first call on a device does a one-time set-up with that device
+ * current (looks up the array's device address with cudaGetSymbolAddress,
+ * sets the kernels' shared-memory attributes); make that first call before
+ * any stream capture.  All calls share the one scratch array, which keeps
+ * the last call's contents: calls that can overlap on the GPU (different
+ * streams, or concurrent graphs) race on it and must be serialised by the
+ * caller. */
+PA_API pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query, const void* key,
+                                     const void* value, void* key_cache, void* value_cache,
+                                     const int32_t* block_table,
+                                     const int32_t* cumulative_sequence_lengths,
+                                     const int32_t* past_sequence_lengths, int batch,
+                                     int token_count, const void* cos_cache,
+                                     const void* sin_cache, void* output,
+                                     int32_t* device_error, void* stream);
+
 /* ---- tuning and measurement hooks (set outside capture) ---- */
 enum {
   PA_OPT_SPLIT_KEYS = 1,      /* > 0: fixed keys per decode split (multiple of 64); 0 = auto */

@@ -30,7 +30,7 @@ STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 
 EXPORTED = ("pa_config_init", "pa_validate_config", "pa_check_step", "pa_create", "pa_cache_write",
             "pa_forward", "pa_check_device_error", "pa_last_error_message", "pa_destroy",
-            "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count")
+            "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count", "pa_forward_no_alloc")
 
 
 class pa_config(ctypes.Structure):
@@ -74,6 +74,7 @@ def lib():
         L.pa_destroy.argtypes = [P]
         L.pa_set_option.argtypes = [P, I, I]
         L.pa_kernel_time_ms.argtypes = [P, I, ctypes.POINTER(ctypes.c_float)]
+        L.pa_forward_no_alloc.argtypes = [CFG, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P]
         L.pa_last_launch_count.argtypes = [P]
         L.pa_last_launch_count.restype = I
         for n in EXPORTED:
@@ -167,6 +168,19 @@ def pa_forward(h, query, key, value, key_cache, value_cache, block_table,
                             _ptr(cumulative_sequence_lengths), _ptr(past_sequence_lengths),
                             batch, token_count, _ptr(cos_cache), _ptr(sin_cache), _ptr(output),
                             ctypes.c_void_p(stream or 0)), h)
+
+
+def pa_forward_no_alloc(cfg: pa_config, query, key, value, key_cache, value_cache, block_table,
+                        cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
+                        cos_cache, sin_cache, output, device_error=None, stream=None):
+    """The whole step without a handle or any device allocation (scratch in a
+    static device array); see include/pa.h for its limits and sharing rules."""
+    _check(lib().pa_forward_no_alloc(ctypes.byref(cfg), _ptr(query), _ptr(key), _ptr(value),
+                                     _ptr(key_cache), _ptr(value_cache), _ptr(block_table),
+                                     _ptr(cumulative_sequence_lengths),
+                                     _ptr(past_sequence_lengths), batch, token_count,
+                                     _ptr(cos_cache), _ptr(sin_cache), _ptr(output),
+                                     _ptr(device_error), ctypes.c_void_p(stream or 0)))
 
 
 def pa_check_device_error(h) -> int:

@@ -686,3 +686,257 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// pa_forward_no_alloc: the whole step without pa_create, for callers that
+// cannot allocate device memory.  All scratch (work lists, split-KV partials,
+// the rotated-query buffer, the error word) is carved from one file-scope
+// device array below, so the call allocates nothing.
+namespace {
+
+// Size of the static scratch; every GPU that loads this library holds it.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+__device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+struct NoAllocDevice {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  const char* what = "";
+  unsigned char* scratch = nullptr;  // device address of g_no_alloc_scratch
+  int num_sms = 0;
+  int dec_ctas[3] = {1, 1, 1};  // decode CTAs per SM for head_size 64, 128, 256
+  bool prefill_ok = false;
+};
+NoAllocDevice g_no_alloc_dev[kMaxDevices];
+
+int head_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
+
+// One-time set-up on the current device: the scratch array's device
+// address (the host-side symbol is not a device pointer), the SM count and
+// the kernels' shared-memory attributes.
+NoAllocDevice* no_alloc_setup(int dev) {
+  NoAllocDevice* d = &g_no_alloc_dev[dev];
+  std::call_once(d->once, [d, dev] {
+    void* ptr = nullptr;
+    d->err = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
+    if (d->err != cudaSuccess) { d->what = "cudaGetSymbolAddress(scratch)"; return; }
+    d->scratch = static_cast<unsigned char*>(ptr);
+    d->err = cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (d->err != cudaSuccess) { d->what = "cudaDeviceGetAttribute"; return; }
+    size_t smem = 0;
+    for (int D : {64, 128, 256})
+      if (d->err == cudaSuccess) d->err = pa::decode_configure(D, &d->dec_ctas[head_index(D)], &smem);
+    if (d->err != cudaSuccess) { d->what = "decode kernel attributes"; return; }
+    d->prefill_ok = pa::prefill_configure(64, &smem) == cudaSuccess &&
+                    pa::prefill_configure(128, &smem) == cudaSuccess &&
+                    pa::prefill_configure(256, &smem) == cudaSuccess;
+    cudaGetLastError();
+    if (!encode_fn()) { d->err = cudaErrorNotSupported; d->what = "cuTensorMapEncodeTiled lookup"; }
+  });
+  return d;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query, const void* key, const void* value,
+                                         void* key_cache, void* value_cache, const int32_t* block_table,
+                                         const int32_t* cum, const int32_t* past, int batch, int token_count,
+                                         const void* cos_cache, const void* sin_cache, void* output,
+                                         int32_t* device_error, void* stream) {
+  char msg[512];
+  pa_status st = pa_check_step(cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
+                               token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
+  if (st != PA_OK) return fail(nullptr, st, "%s", msg);
+  if (device_error && reinterpret_cast<uintptr_t>(device_error) % 4)
+    return fail(nullptr, PA_INVALID_ARGUMENT, "device_error must be 4-byte aligned");
+  if (token_count == 0) return PA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(nullptr, PA_NOT_SUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  NoAllocDevice* nd = no_alloc_setup(dev);
+  if (nd->err != cudaSuccess) return cuda_fail(nullptr, nd->err, nd->what);
+
+  const pa_config& c = *cfg;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = c.head_size, H = c.num_heads, Hk = c.kv_num_heads;
+  const int G = H / Hk, R = rot_dim_of(c);
+  const float scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)D);
+  const int kv_cap = c.max_blocks_per_seq * c.block_size;
+  const int max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
+  const int max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
+  const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
+  const int target_pairs = std::max(1, (4 * dec_grid + Hk - 1) / Hk);
+  const int cap_dec = target_pairs + c.max_batch;
+  const int tile_tokens = std::max(1, pa::kPrefillRows / G);
+  const int cap_pre = (c.max_tokens + tile_tokens - 1) / tile_tokens + c.max_batch;
+  const int cap_comb = c.max_tokens;
+
+  // Scratch layout (256-byte aligned pieces), checked against the maximum.
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  const size_t o_err = off; off = up(off + 64);
+  const size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
+  const size_t o_seq = off; off = up(off + sizeof(pa::SeqInfo) * c.max_batch);
+  const size_t o_dec = off; off = up(off + sizeof(int2) * cap_dec);
+  const size_t o_pre = off; off = up(off + sizeof(int2) * cap_pre);
+  const size_t o_cmb = off; off = up(off + sizeof(int2) * cap_comb);
+  const size_t o_pml = off; off = up(off + sizeof(float2) * (size_t)cap_dec * Hk * pa::kDecodeRows);
+  const size_t o_po = off; off = up(off + sizeof(float) * (size_t)cap_dec * Hk * pa::kDecodeRows * D);
+  const size_t o_qr = off;
+  if (c.do_rotary) off = up(off + 2 * (size_t)c.max_tokens * H * D);
+  if (off > kNoAllocScratchBytes)
+    return fail(nullptr, PA_INVALID_ARGUMENT,
+                "these capacities need %zu bytes of scratch; the static scratch holds %zu bytes "
+                "(lower max_batch / max_tokens or use pa_create)",
+                off, kNoAllocScratchBytes);
+  unsigned char* w = nd->scratch;
+  int* err = device_error ? device_error : reinterpret_cast<int*>(w + o_err);
+  pa::Counters* counters = reinterpret_cast<pa::Counters*>(w + o_cnt);
+  pa::SeqInfo* seq = reinterpret_cast<pa::SeqInfo*>(w + o_seq);
+  int2* dec_items = reinterpret_cast<int2*>(w + o_dec);
+  int2* pre_tiles = reinterpret_cast<int2*>(w + o_pre);
+  int2* comb_rows = reinterpret_cast<int2*>(w + o_cmb);
+  float2* part_ml = reinterpret_cast<float2*>(w + o_pml);
+  float* part_o = reinterpret_cast<float*>(w + o_po);
+  __half* q_rot = c.do_rotary ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
+  if (!device_error) {
+    e = cudaMemsetAsync(err, 0, sizeof(int), s);  // the shared error word starts clean
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemsetAsync(error word)");
+  }
+
+  const int pool_rows = c.num_blocks * c.block_size;
+  const int box_rows = std::min(c.block_size, pa::kStageKeys);
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(&tk, key_cache, D, Hk, pool_rows, box_rows) ||
+      !encode_pool_map(&tv, value_cache, D, Hk, pool_rows, box_rows))
+    return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
+
+  pa::WorklistParams wp{};
+  wp.cum = cum;
+  wp.past = past;
+  wp.batch = batch;
+  wp.token_count = token_count;
+  wp.group = G;
+  wp.max_q = max_q;
+  wp.max_kv = max_kv;
+  wp.window = c.local_window_size;
+  wp.prune = 1;
+  wp.dec_max_rows = G <= pa::kDecodeRows ? pa::kDecodeRows : 0;
+  wp.prefill_tile_tokens = tile_tokens;
+  wp.split_keys_fixed = 0;
+  wp.target_pairs = target_pairs;
+  wp.cap_dec = cap_dec;
+  wp.cap_pre = cap_pre;
+  wp.cap_comb = cap_comb;
+  wp.seq = seq;
+  wp.dec_items = dec_items;
+  wp.pre_tiles = pre_tiles;
+  wp.comb_rows = comb_rows;
+  wp.counters = counters;
+  wp.err = err;
+  pa::CacheWriteParams cp{};
+  cp.key = static_cast<const __half*>(key);
+  cp.value = static_cast<const __half*>(value);
+  cp.query = static_cast<const __half*>(query);
+  cp.q_rot = q_rot;
+  cp.key_cache = static_cast<__half*>(key_cache);
+  cp.value_cache = static_cast<__half*>(value_cache);
+  cp.block_table = block_table;
+  cp.cum = cum;
+  cp.past = past;
+  cp.cos_cache = static_cast<const __half*>(cos_cache);
+  cp.sin_cache = static_cast<const __half*>(sin_cache);
+  cp.batch = batch;
+  cp.token_count = token_count;
+  cp.H = H;
+  cp.Hk = Hk;
+  cp.D = D;
+  cp.bs = c.block_size;
+  cp.NB = c.num_blocks;
+  cp.MB = c.max_blocks_per_seq;
+  cp.rotary = c.do_rotary;
+  cp.interleaved = c.rotary_interleaved;
+  cp.rot_dim = R;
+  cp.rot_positions = c.max_rotary_positions;
+  cp.q_heads_per_part = Hk;
+  cp.parts = 1 + (q_rot ? (H + Hk - 1) / Hk : 0);
+  cp.err = err;
+  e = pa::launch_prologue(wp, cp, s);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "prologue launch");
+
+  const __half* q_att = c.do_rotary ? q_rot : static_cast<const __half*>(query);
+  const int qt = G <= pa::kDecodeRows ? pa::kDecodeRows / G : 1;
+  CUtensorMap tq;
+  if (!encode_map(&tq, q_att, D, H, token_count, G, qt))
+    return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
+  pa::DecodeParams dp{};
+  dp.q_tile_tokens = qt;
+  dp.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
+  dp.out = static_cast<__half*>(output);
+  dp.block_table = block_table;
+  dp.seq = seq;
+  dp.dec_items = dec_items;
+  dp.counters = counters;
+  dp.part_o = part_o;
+  dp.part_ml = part_ml;
+  dp.err = err;
+  dp.H = H;
+  dp.Hk = Hk;
+  dp.G = G;
+  dp.bs = c.block_size;
+  dp.MB = c.max_blocks_per_seq;
+  dp.NB = c.num_blocks;
+  dp.scale = scale;
+  dp.softcap = c.softcap;
+  dp.window = c.local_window_size;
+  dp.oob_row = pool_rows;
+  e = pa::launch_decode(D, tk, tv, tq, dp, dec_grid, s);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "decode launch");
+
+  if (nd->prefill_ok) {
+    CUtensorMap tqp, tkp, tvp;
+    const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
+    if (!encode_map(&tqp, q_att, D, H, token_count, G, tile_tokens) ||
+        !encode_map(&tkp, key_cache, D, Hk, pool_rows, 1, prow) ||
+        !encode_map(&tvp, value_cache, D, Hk, pool_rows, 1, prow))
+      return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
+    pa::PrefillParams pp{};
+    pp.out = static_cast<__half*>(output);
+    pp.block_table = block_table;
+    pp.seq = seq;
+    pp.pre_tiles = pre_tiles;
+    pp.counters = counters;
+    pp.err = err;
+    pp.H = H;
+    pp.Hk = Hk;
+    pp.G = G;
+    pp.bs = c.block_size;
+    pp.MB = c.max_blocks_per_seq;
+    pp.NB = c.num_blocks;
+    pp.tile_tokens = tile_tokens;
+    pp.log_page_rows = 31 - __builtin_clz((unsigned)prow);
+    pp.scale = scale;
+    pp.softcap = c.softcap;
+    pp.window = c.local_window_size;
+    pp.oob_row = pool_rows;
+    e = pa::launch_prefill(D, tqp, tkp, tvp, pp, std::max(1, std::min(nd->num_sms, cap_pre * Hk)), s);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "prefill launch");
+  }
+
+  pa::CombineParams mp{};
+  mp.part_o = part_o;
+  mp.part_ml = part_ml;
+  mp.seq = seq;
+  mp.comb_rows = comb_rows;
+  mp.counters = counters;
+  mp.out = static_cast<__half*>(output);
+  mp.H = H;
+  mp.Hk = Hk;
+  mp.G = G;
+  mp.D = D;
+  e = pa::launch_combine(mp, std::max(1, std::min(nd->num_sms * 4, (cap_comb * H + 7) / 8)), s);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "combine launch");
+  return PA_OK;
+}
