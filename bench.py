@@ -1,28 +1,36 @@
 """Benchmark of one PagedAttention step on GB300 (one JSON line on stdout).
 
-Workload: the Llama-3-8B-shaped decode step (batch 64, 32 query / 8 kv
-heads, head_size 128, block_size 16, one new token per sequence, past
+Default workload: the Llama-3-8B-shaped decode step (batch 64, 32 query /
+8 kv heads, head_size 128, block_size 16, one new token per sequence, past
 lengths uniform 512..4096, pool 20 % larger than needed with shuffled
 blocks), seeded synthetic fp16 inputs.  A step is one pa_forward: the
-work-list build, the paged cache write of the 64 new K/V rows and the
-split-KV attention with its combine.
+prologue (device work list + paged cache write of the new K/V rows), the
+split-KV attention with its combine, and the tensor-core prefill for any
+sequence with more query rows than a decode item holds.
 
-value   = attended K/V bytes of the step / device time of the step (GB/s);
-          attended bytes = sum_b admitted_b * kv_heads * head_size * 2 (K, V)
-          * 2 bytes, each KV element counted once per step.
-e2e     = the same metric through the C ABI with host inputs: pinned host
-          Q/K/V, block table and lengths copied in and the output copied out
-          inside the timed region; the paged pool is resident device state.
-roofline= the decode kernel's algorithmic bytes (attended K/V + Q + output)
-          over its own event-timed duration, against the measured copy
-          bandwidth.
-cpu_baseline = the fp64 CPU oracle on the host cores over a bounded sample
-          of the same step's sequences.
+--workload selects another step shape (for profiling): `mixed` (16 prompts
+of 1024 tokens + 240 decodes, block_size 32), `long_window` (Gemma-2-shaped
+window 4096 / softcap 50 decode), `rotary_decode` (Llama-70B-shaped decode
+with rotary), `prefill` (16 prompts of 1024 tokens alone), `tiny`.
+
+value    decode workloads: attended K/V bytes of the step / step time (GB/s),
+         each admitted K and V element counted once per kv head; workloads
+         with prompts: packed tokens of the step / step time (tokens/s).
+e2e      the same metric through the C ABI with host inputs: pinned host
+         Q/K/V, block table and lengths copied in and the output copied out
+         inside the timed region; the paged pool is resident device state.
+roofline the dominant kernel's algorithmic work over its own event-timed
+         duration: decode = attended K/V + Q + output bytes of the decode
+         sequences against the measured copy bandwidth; prefill = causal
+         FLOPs 4 * D * H * sum(admitted keys) against the measured dense
+         16-bit matmul rate (fp16 and bf16 share one nominal rate).
+cpu_baseline  the fp64 CPU oracle on the host cores over a bounded sample of
+         the same step's sequences.
 
 --impl reference times the oracle alone (the pages ship no runnable
 implementation; the oracle is the reference arm).  Under torchrun (N > 1)
 each rank runs an independent replica on its own GPU ("replicas only":
-the step has no cross-GPU exchange); value sums the ranks' bytes over the
+the step has no cross-GPU exchange); value sums the ranks' work over the
 slowest rank's time.
 """
 
@@ -41,35 +49,51 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "decode attended-KV GB/s (% of 8 TB/s HBM); mixed-batch tokens/s"
-UNIT = "GB/s"
-WORKLOAD_INDEX = 1
 NOMINAL_HBM_GBS = 8000.0
-FALLBACK_HBM_GBS = 6800.0
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+DECODE_ROWS = 16  # query rows of one decode item: q_len * G <= 16 goes to the decode kernel
 
 
-def attended_kv_bytes(step) -> int:
-    """Bytes of K and V the step must read: per sequence the keys its last
-    token admits (min(L_b, W) under a window), per kv head, K and V, fp16."""
+def workload_shape(name):
+    import workloads
+    index = {"tiny": 0, "decode": 1, "mixed": 2, "long_window": 3, "rotary_decode": 4}
+    if name in index:
+        return workloads.config_shape(index[name])
+    if name == "prefill":
+        return workloads.custom_shape("prefill_16x1024_h32_kv8_d128_bs32", 32, 8, 128, 32, [0] * 16,
+                                      [1024] * 16, seed=2)
+    raise ValueError(name)
+
+
+def seq_lengths(step):
     past = step["past_sequence_lengths"].cpu().tolist()
     cum = step["cumulative_sequence_lengths"].cpu().tolist()
-    W = step["local_window_size"]
-    keys = 0
-    for b, p in enumerate(past):
-        q = cum[b + 1] - cum[b]
-        if q:
-            L = p + q
-            keys += min(L, W) if W >= 1 else L
-    return keys * step["kv_num_heads"] * step["head_size"] * 2 * 2
+    return past, [cum[b + 1] - cum[b] for b in range(len(past))]
 
 
-def seq_kv_bytes(step, b) -> int:
-    past = int(step["past_sequence_lengths"][b])
-    cum = step["cumulative_sequence_lengths"]
-    q = int(cum[b + 1] - cum[b])
-    W = step["local_window_size"]
-    L = past + q
-    adm = (min(L, W) if W >= 1 else L) if q else 0
-    return adm * step["kv_num_heads"] * step["head_size"] * 4
+def admitted(pos, W):
+    return min(pos + 1, W) if W >= 1 else pos + 1
+
+
+def work_of(step, seqs=None):
+    """Algorithmic work of (a subset of) the step's sequences."""
+    past, q = seq_lengths(step)
+    W, G = step["local_window_size"], step["num_heads"] // step["kv_num_heads"]
+    Hk, H, D = step["kv_num_heads"], step["num_heads"], step["head_size"]
+    w = dict(kv_bytes=0, dec_kv_bytes=0, dec_qo_bytes=0, pre_flops=0, tokens=0)
+    for b in (range(len(past)) if seqs is None else seqs):
+        if q[b] == 0:
+            continue
+        L = past[b] + q[b]
+        kv = (min(L, W) if W >= 1 else L) * Hk * D * 4
+        w["kv_bytes"] += kv
+        w["tokens"] += q[b]
+        if q[b] * G <= DECODE_ROWS:
+            w["dec_kv_bytes"] += kv
+            w["dec_qo_bytes"] += 2 * q[b] * H * D * 2
+        else:
+            w["pre_flops"] += 4 * D * H * sum(admitted(past[b] + j, W) for j in range(q[b]))
+    return w
 
 
 def measured_peaks():
@@ -77,23 +101,24 @@ def measured_peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def decode_traffic():
-    """DRAM bytes per decode launch from the committed ncu summary, or None
-    when the decode kernel source changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
-    src = os.path.join(ROOT, "paged_kv_cache_reshape_gb300", "csrc", "decode.cu")
+def committed_traffic(kernel_file, workload):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "paged_kv_cache_reshape_gb300", "csrc", kernel_file)
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        d = json.load(f)
+        entries = json.load(f)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if d.get("decode_cu_sha256") != sha or d.get("workload") != "llama3_8b_decode_b64_h32_kv8_d128_bs16":
-        return None
-    return d.get("dram_bytes_per_launch")
+    for e in entries:
+        if e.get("source") == kernel_file and e.get("source_sha256") == sha and e.get("workload") == workload:
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -106,6 +131,7 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -125,8 +151,6 @@ class ClockSampler:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
             self.out = out
-        else:
-            self.out = ""
 
     def summary(self):
         sm, mx, reasons = [], [], set()
@@ -149,37 +173,49 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(step_host, budget_s=12.0):
-    """The oracle (as it stands) on the host cores, over whole sequences of the
-    step until the time budget is spent.  Returns (GB/s, cores, sample text)."""
+def max_over_ranks(x, world, device="cpu"):
+    """The slowest rank's time (all_reduce MAX); identity on one rank."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def metric_of(work, unit, seconds):
+    return (work["kv_bytes"] / 1e9 if unit == "GB/s" else work["tokens"]) / seconds
+
+
+def oracle_sample(step, budget_s, start_seq=0):
+    """Runs the oracle's attention over whole sequences of the step from
+    start_seq on (wrapping) until budget_s is spent.  Returns (seconds,
+    sequences done, work of those sequences, next sequence, cores)."""
     import numpy as np
 
     import oracle
 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    H = step_host["num_heads"]
-    cum = step_host["cumulative_sequence_lengths"]
-    B = step_host["batch"]
-    # Rotary / cache write of the whole step first (part of the oracle's step).
-    base = oracle.forward(step_host, rows=np.zeros(0, dtype=np.int64))
+    H, B = step["num_heads"], step["batch"]
+    cum = step["cumulative_sequence_lengths"]
+    if "_oracle_base" not in step:
+        step["_oracle_base"] = oracle.forward(step, rows=np.zeros(0, dtype=np.int64))
+    base = step["_oracle_base"]
     t0 = time.perf_counter()
-    done, nbytes = 0, 0
-    for b in range(B):
+    seqs = []
+    b = start_seq
+    while True:
         rows = np.arange(int(cum[b]) * H, int(cum[b + 1]) * H, dtype=np.int64)
         if rows.size:
-            oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"],
-                             step_host["block_table"], cum, step_host["past_sequence_lengths"], H,
-                             step_host["kv_num_heads"], step_host["head_size"],
-                             step_host["block_size"], step_host["scale"], step_host["softcap"],
-                             step_host["local_window_size"], rows=rows, threads=cores)
-        nbytes += seq_kv_bytes(step_host, b)
-        done += 1
-        if time.perf_counter() - t0 > budget_s:
+            oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"], step["block_table"],
+                             cum, step["past_sequence_lengths"], H, step["kv_num_heads"], step["head_size"],
+                             step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
+                             rows=rows, threads=cores)
+        seqs.append(b)
+        b = (b + 1) % B
+        if time.perf_counter() - t0 > budget_s or len(seqs) >= B:
             break
-    dt = time.perf_counter() - t0
-    sample = (f"attention of {done} of {B} sequences (all {H} heads each) of the step, "
-              f"{dt:.1f} s, {nbytes / 1e6:.1f} MB attended K/V")
-    return nbytes / dt / 1e9, cores, sample
+    return time.perf_counter() - t0, seqs, work_of(step, seqs), b, cores
 
 
 def run_reference(args, rank, world):
@@ -188,49 +224,31 @@ def run_reference(args, rank, world):
     per-step time budget chosen so the run ends within a few minutes."""
     if rank != 0:
         return
-    import numpy as np
-
-    import oracle
     import workloads
 
-    shape = workloads.config_shape(WORKLOAD_INDEX)
+    shape = workload_shape(args.workload)
     step = workloads.make_step(shape, device="cpu")
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    H, B = step["num_heads"], step["batch"]
-    cum = step["cumulative_sequence_lengths"]
-    base = oracle.forward(step, rows=np.zeros(0, dtype=np.int64))
+    unit = "GB/s" if work_of(step)["pre_flops"] == 0 else "tokens/s"
     budget = min(args.ref_budget, max(0.02, 150.0 / (args.steps + args.warmup)))
-    b = 0
-    tot_bytes, tot_t, seqs = 0, 0.0, 0
+    b, tot_t, done, cores = 0, 0.0, 0, 1
+    acc = dict(kv_bytes=0, tokens=0)
     for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        nbytes = 0
-        while True:
-            rows = np.arange(int(cum[b]) * H, int(cum[b + 1]) * H, dtype=np.int64)
-            oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"],
-                             step["block_table"], cum, step["past_sequence_lengths"], H,
-                             step["kv_num_heads"], step["head_size"], step["block_size"],
-                             step["scale"], step["softcap"], step["local_window_size"], rows=rows,
-                             threads=cores)
-            nbytes += seq_kv_bytes(step, b)
-            b = (b + 1) % B
-            if i >= args.warmup:
-                seqs += 1
-            if time.perf_counter() - t0 > budget:
-                break
+        dt, seqs, w, b, cores = oracle_sample(step, budget, b)
         if i >= args.warmup:
-            tot_bytes += nbytes
-            tot_t += time.perf_counter() - t0
-    value = tot_bytes / tot_t / 1e9
-    sample = (f"{seqs} sequence-steps of the step's 64 sequences (all {H} heads each), "
-              f"about {budget:.2f} s per step, {tot_t:.1f} s timed")
+            tot_t += dt
+            done += len(seqs)
+            acc["kv_bytes"] += w["kv_bytes"]
+            acc["tokens"] += w["tokens"]
+    value = metric_of(acc, unit, tot_t)
+    sample = (f"{done} sequence-steps of the step's {step['batch']} sequences (all {step['num_heads']} "
+              f"heads each), about {budget:.2f} s per step, {tot_t:.1f} s timed")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": shape.name, "sample": "bounded"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -245,14 +263,15 @@ def run_ours(args, rank, world, local_rank):
     builder.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    shape = workloads.config_shape(WORKLOAD_INDEX)
+    shape = workload_shape(args.workload)
     step = workloads.make_step(shape, device=dev, gen_device=str(dev))
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
-    kv_bytes = attended_kv_bytes(host)
-    T, H, D = step["token_count"], step["num_heads"], step["head_size"]
-    decode_alg_bytes = kv_bytes + 2 * T * H * D * 2  # + Q read + output write
-
-    op = pa.PagedAttention.for_step(step)
+    work = work_of(host)
+    unit = "tokens/s" if work["pre_flops"] > 0 else "GB/s"
+    _, qlens = seq_lengths(host)
+    # Replay-wide bound on query length (the op's attention_metadata): for a
+    # decode step it lets the host skip launching the prefill kernel.
+    op = pa.PagedAttention.for_step(step, max_query_len_bound=max(qlens))
     out = torch.empty_like(step["query"])
     stream = torch.cuda.current_stream(dev)
     sid = stream.cuda_stream
@@ -273,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- device-timed steps: one CUDA-graph replay of pa_forward each (the
     # step is capture-safe: no host sync, no allocation); L2 flushed before
     # each replay, outside the events.  A second graph, captured with the
-    # library's per-kernel events on, times the decode kernel alone.
+    # library's per-kernel events on, times the kernels alone.
     def capture():
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
@@ -291,19 +310,22 @@ def run_ours(args, rank, world, local_rank):
     run_timed = fwd if args.eager else capture().replay
     op.set_option(pa.PA_OPT_KERNEL_TIMING, 0)
 
-    def timed_loop(fn, n, sample_decode):
+    def timed_loop(fn, n, sample_kernels):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        dec = []
+        ker = {pa.PA_STAGE_DECODE: [], pa.PA_STAGE_PREFILL: []}
         for i in range(n):
             flush.fill_(i)
             starts[i].record(stream)
             fn()
             ends[i].record(stream)
-            if sample_decode and (i % 16 == 15 or i == n - 1):
-                dec.append(op.kernel_time_ms(pa.PA_STAGE_DECODE))
+            if sample_kernels and (i % 16 == 15 or i == n - 1):
+                for s in ker:
+                    v = op.kernel_time_ms(s)
+                    if v >= 0:
+                        ker[s].append(v)
         torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)], dec
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)], ker
 
     if world > 1:
         torch.distributed.barrier()
@@ -313,22 +335,34 @@ def run_ours(args, rank, world, local_rank):
         step_ms, _ = timed_loop(run, args.steps, False)
         t_wall = time.perf_counter() - t_wall0
         op.set_option(pa.PA_OPT_KERNEL_TIMING, 1)
-        _, dec_ms = timed_loop(run_timed, min(args.steps, 256), True)
+        _, ker_ms = timed_loop(run_timed, min(args.steps, 256), True)
         op.set_option(pa.PA_OPT_KERNEL_TIMING, 0)
     if world > 1:
         torch.distributed.barrier()
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * kv_bytes / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    value = world * metric_of(work, unit, ms * 1e-3)
 
-    # ---- decode kernel alone: events around it inside pa_forward, same stream
-    dec = statistics.mean(dec_ms)
-    peak, peak_kind = measured_peaks()
-    achieved = decode_alg_bytes / (dec * 1e-3) / 1e9
-    traffic = decode_traffic()
+    hbm, tflops, peak_kind = measured_peaks()
+    rooflines = {}
+    if ker_ms[pa.PA_STAGE_DECODE] and work["dec_kv_bytes"]:
+        t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
+        alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
+        rooflines["decode"] = {
+            "bound": "hbm", "kernel": f"decode_kernel<{shape.head_size}>", "achieved": alg / (t * 1e-3) / 1e9,
+            "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+            "frac": alg / (t * 1e-3) / 1e9 / hbm,
+            "traffic": committed_traffic("decode.cu", shape.name), "algorithmic_bytes_per_launch": alg,
+            "launch_ms": t}
+    if ker_ms[pa.PA_STAGE_PREFILL] and work["pre_flops"]:
+        t = statistics.mean(ker_ms[pa.PA_STAGE_PREFILL])
+        ach = work["pre_flops"] / (t * 1e-3) / 1e12
+        rooflines["prefill"] = {
+            "bound": "tensor", "kernel": f"prefill_kernel<{shape.head_size}>", "achieved": ach, "peak": tflops,
+            "peak_kind": f"{peak_kind} bf16 matmul burst; fp16 has the same nominal dense rate",
+            "unit": "TFLOP/s", "frac": ach / tflops,
+            "traffic": committed_traffic("prefill.cu", shape.name),
+            "algorithmic_flops_per_launch": work["pre_flops"], "launch_ms": t}
+    dominant = max(rooflines, key=lambda k: rooflines[k]["launch_ms"]) if rooflines else None
 
     # ---- end to end through the C ABI with host buffers
     names = ["query", "key", "value", "block_table", "cumulative_sequence_lengths", "past_sequence_lengths"]
@@ -336,7 +370,7 @@ def run_ours(args, rank, world, local_rank):
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = out_host.numel() * out_host.element_size()
-    e_steps = max(10, args.steps // 4)
+    e_steps = max(10, min(args.steps, 500))
     es = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(e_steps)]
     for i in range(e_steps + 3):
@@ -351,40 +385,41 @@ def run_ours(args, rank, world, local_rank):
         if k >= 0:
             ee[k].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = statistics.mean(s.elapsed_time(e) for s, e in zip(es, ee))
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = world * kv_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in zip(es, ee)), world, dev)
+    e2e = world * metric_of(work, unit, e2e_ms * 1e-3)
     assert op.device_error() == 0, "device error in the timed region"
 
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "pct_of_8tbs_hbm": 100.0 * value / world / NOMINAL_HBM_GBS,
-        "config": {"workload": shape.name, "batch": shape.batch, "num_heads": shape.num_heads,
-                   "kv_num_heads": shape.kv_num_heads, "head_size": shape.head_size,
-                   "block_size": shape.block_size, "attended_kv_bytes_per_step": kv_bytes,
+        "config": {"workload": shape.name, "batch": shape.batch, "token_count": shape.token_count,
+                   "num_heads": shape.num_heads, "kv_num_heads": shape.kv_num_heads,
+                   "head_size": shape.head_size, "block_size": shape.block_size,
+                   "attended_kv_bytes_per_step": work["kv_bytes"], "prefill_flops_per_step": work["pre_flops"],
                    "l2": "flushed before every step (write of 2x L2), outside the step's events",
                    "launch": "eager" if args.eager else "cuda_graph replay of one pa_forward",
                    "parallelism": "replicas" if world > 1 else "single"},
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel<128>", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": decode_alg_bytes,
-                     "launch_ms": dec},
-        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+        "roofline": rooflines.get(dominant),
         "gpu_launches": launches_per_step * (args.steps + min(args.steps, 256)),
+        "e2e": {"value": e2e, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
         "clocks": clk.summary(),
         "wall_s_timed_region": t_wall,
     }
+    if unit == "GB/s":
+        line["pct_of_8tbs_hbm"] = 100.0 * value / world / NOMINAL_HBM_GBS
+    for k, r in rooflines.items():
+        if k != dominant:
+            line[f"roofline_{k}"] = r
     if not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline(host, budget_s=args.ref_budget)
-        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        dt, seqs, w, _, cores = oracle_sample(host, args.ref_budget)
+        sample = (f"attention of {len(seqs)} of {host['batch']} sequences (all {host['num_heads']} heads each) "
+                  f"of the step, {dt:.1f} s")
+        line["cpu_baseline"] = {"value": metric_of(w, unit, dt), "unit": unit, "cores": cores, "kind": "oracle",
+                                "sample": sample}
     print(json.dumps(line), flush=True)
 
 
@@ -394,6 +429,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "mixed", "long_window", "rotary_decode", "prefill", "tiny"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch pa_forward directly instead of a graph replay")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")

@@ -632,8 +632,9 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
     h->last_launches++;
   }
-  // 4. varlen prefill on tensor memory
-  if (h->prefill_ready) {
+  // 4. varlen prefill on tensor memory (skipped when the query-length bound
+  // already routes every sequence to the decode kernel)
+  if (h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows) {
     CUtensorMap tq, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_tile_tokens) ||

@@ -137,9 +137,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
     int quse[2] = {0, 0};
     int qi = 0;
     bool ok = true;
-    while (ok) {
-      int u = 0;
-      if (lane == 0) u = atomicAdd(&p.counters->dec_next, 1);
+    for (int it = 0; ok; ++it) {
+      // First item: this CTA's own index; then the shared queue.
+      int u = blockIdx.x;
+      if (it > 0 && lane == 0) u = gridDim.x + atomicAdd(&p.counters->dec_next, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
       if (u >= n_work) {
         if (lane == 0) {

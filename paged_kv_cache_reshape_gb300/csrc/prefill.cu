@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = tt & 1;
       int u = 0;
       if (lane == 0) {
+        // First tile: this CTA's own index; then the shared queue.
         if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
-        else u = atomicAdd(&p.counters->pre_next, 1);
+        else u = tt == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
       }
       u = __shfl_sync(0xffffffffu, u, 0);
       if (u == -2) break;

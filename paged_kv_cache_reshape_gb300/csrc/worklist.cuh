@@ -162,6 +162,24 @@ __device__ void build_small(const WorklistParams& p) {
   Int3 tot;
   const Int3 pre = block_exclusive_scan3(cnt, &tot);
   const bool overflow = tot.a + tot.d > p.cap_dec || tot.b > p.cap_pre || tot.c > p.cap_comb;
+  // Last splits, longest first: they are the only items shorter than
+  // split_keys, so handing them out in decreasing size keeps the dynamic
+  // queue's tail short.  Bucket = 64-key groups, counting sort.
+  __shared__ int hist[kThreads];
+  hist[threadIdx.x] = 0;
+  __syncthreads();
+  int bucket = 0, rank = 0;
+  if (cnt.d) {
+    const int last = L.past + L.q - L.lo - cnt.a * split_keys;  // keys of the last split, >= 1
+    bucket = kThreads - 1 - min(kThreads - 1, (last - 1) / kStageKeys);
+    rank = atomicAdd(&hist[bucket], 1);
+  }
+  __syncthreads();
+  Int3 htot;
+  const Int3 hpre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
+  __syncthreads();
+  hist[threadIdx.x] = hpre.a;
+  __syncthreads();
   if (b < p.batch) {
     SeqInfo si;
     si.q_len = L.q;
@@ -170,7 +188,7 @@ __device__ void build_small(const WorklistParams& p) {
     si.t0 = L.t0;
     si.dec_first = pre.a;
     si.dec_count = cnt.a + cnt.d;
-    si.dec_last = tot.a + pre.d;
+    si.dec_last = tot.a + (cnt.d ? hist[bucket] + rank : 0);
     si.pre_first = pre.b;
     si.pre_count = cnt.b;
     si.pad[0] = pre.c;
@@ -180,9 +198,25 @@ __device__ void build_small(const WorklistParams& p) {
       for (int s = 0; s < cnt.a; ++s) p.dec_items[si.dec_first + s] = make_int2(b, s);
       if (cnt.d) p.dec_items[si.dec_last] = make_int2(b, cnt.a);
       for (int j = 0; j < cnt.c; ++j) p.comb_rows[pre.c + j] = make_int2(L.t0 + j, b);
-      for (int s = 0; s < cnt.b; ++s) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
     }
   }
+  // Prefill tiles, costliest first (cost ~ the tile's last position, in
+  // 64-key buckets): the same counting sort over every tile of every sequence.
+  __syncthreads();
+  hist[threadIdx.x] = 0;
+  __syncthreads();
+  auto tile_bucket = [&](int s) {
+    const int pos_end = L.past + min((s + 1) * p.prefill_tile_tokens, L.q);
+    return kThreads - 1 - min(kThreads - 1, pos_end / kStageKeys);
+  };
+  for (int s = 0; s < cnt.b; ++s) atomicAdd(&hist[tile_bucket(s)], 1);
+  __syncthreads();
+  const Int3 ppre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
+  __syncthreads();
+  hist[threadIdx.x] = ppre.a;
+  __syncthreads();
+  if (!overflow)
+    for (int s = 0; s < cnt.b; ++s) p.pre_tiles[atomicAdd(&hist[tile_bucket(s)], 1)] = make_int2(b, s);
   if (threadIdx.x == 0) write_counters(p, overflow, tot, split_keys, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
 }
