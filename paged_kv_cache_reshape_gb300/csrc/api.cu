@@ -70,7 +70,7 @@ struct pa_handle_s {
   int dec_ctas_per_sm = 1, dec_grid = 1;
   size_t dec_smem = 0;
   int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
-  int prefill_tile_tokens = 1, pre_grid = 1, comb_grid = 1;
+  int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
   size_t pre_smem = 0;
   bool prefill_ready = false;
   void* ws = nullptr;
@@ -333,7 +333,10 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads);
   // Room for up to 32 items per CTA (the tuning option's maximum).
   h->cap_dec = std::max(1, (32 * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads) + c.max_batch;
-  h->prefill_tile_tokens = std::max(1, pa::kPrefillRows / h->G);
+  // Prefill work units: unit tokens (the work list's tiles) and the tokens
+  // of one 128-row query tile (the Q TMA box).
+  h->prefill_tile_tokens = pa::prefill_unit_tokens(c.head_size, h->G);
+  h->prefill_q_tokens = std::max(1, pa::kPrefillRows / h->G);
   h->cap_pre = (c.max_tokens + h->prefill_tile_tokens - 1) / h->prefill_tile_tokens + c.max_batch;
   h->cap_comb = c.max_tokens;
   h->pre_grid = std::max(1, std::min(h->num_sms, h->cap_pre * c.kv_num_heads));
@@ -637,7 +640,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   if (h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows) {
     CUtensorMap tq, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
-    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_tile_tokens) ||
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_q_tokens) ||
         !encode_map(&tkp, key_cache, D, c.kv_num_heads, pool_rows, 1, prow) ||
         !encode_map(&tvp, value_cache, D, c.kv_num_heads, pool_rows, 1, prow))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
@@ -654,7 +657,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.bs = c.block_size;
     p.MB = c.max_blocks_per_seq;
     p.NB = c.num_blocks;
-    p.tile_tokens = h->prefill_tile_tokens;
+    p.tile_tokens = h->prefill_q_tokens;
     p.log_page_rows = 31 - __builtin_clz((unsigned)prow);
     p.scale = h->scale;
     p.softcap = c.softcap;
@@ -770,7 +773,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
   const int target_pairs = std::max(1, (4 * dec_grid + Hk - 1) / Hk);
   const int cap_dec = target_pairs + c.max_batch;
-  const int tile_tokens = std::max(1, pa::kPrefillRows / G);
+  const int tile_tokens = pa::prefill_unit_tokens(D, G);
+  const int q_tokens = std::max(1, pa::kPrefillRows / G);
   const int cap_pre = (c.max_tokens + tile_tokens - 1) / tile_tokens + c.max_batch;
   const int cap_comb = c.max_tokens;
 
@@ -899,7 +903,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   if (nd->prefill_ok) {
     CUtensorMap tqp, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
-    if (!encode_map(&tqp, q_att, D, H, token_count, G, tile_tokens) ||
+    if (!encode_map(&tqp, q_att, D, H, token_count, G, q_tokens) ||
         !encode_map(&tkp, key_cache, D, Hk, pool_rows, 1, prow) ||
         !encode_map(&tvp, value_cache, D, Hk, pool_rows, 1, prow))
       return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
@@ -916,7 +920,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
     pp.bs = c.block_size;
     pp.MB = c.max_blocks_per_seq;
     pp.NB = c.num_blocks;
-    pp.tile_tokens = tile_tokens;
+    pp.tile_tokens = q_tokens;
     pp.log_page_rows = 31 - __builtin_clz((unsigned)prow);
     pp.scale = scale;
     pp.softcap = c.softcap;

@@ -527,7 +527,7 @@ cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 
 }  // namespace
 
-cudaError_t prefill_configure(int head_size, size_t* smem) {
+cudaError_t prefill_single_configure(int head_size, size_t* smem) {
   switch (head_size) {
     case 64: return configure_d<64>(smem);
     case 128: return configure_d<128>(smem);
@@ -536,9 +536,9 @@ cudaError_t prefill_configure(int head_size, size_t* smem) {
   }
 }
 
-int prefill_keys_per_tile(int head_size) { return head_size == 256 ? 64 : 128; }
+int prefill_single_keys_per_tile(int head_size) { return head_size == 256 ? 64 : 128; }
 
-cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_prefill_single(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int grid, cudaStream_t s) {
   switch (head_size) {
     case 64: return launch_d<64>(tq, tk, tv, p, grid, s);

@@ -129,7 +129,7 @@ struct PrefillParams {
   Counters* counters;  // n_pre and the tile queue head
   int* err;
   int H, Hk, G, bs, MB, NB;
-  int tile_tokens;  // tokens per query tile (rows = tile_tokens * G <= 128)
+  int tile_tokens;  // tokens per 128-row query tile (rows = tile_tokens * G <= 128)
   int log_page_rows;  // log2(min(block_size, keys per KV tile)): pool rows per TMA box
   float scale;
   float softcap;
@@ -166,6 +166,14 @@ cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMa
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);
 int prefill_keys_per_tile(int head_size);
+int prefill_unit_tokens(int head_size, int group);  // tokens per prefill work unit
+cudaError_t prefill_single_configure(int head_size, size_t* smem);
+int prefill_single_keys_per_tile(int head_size);
+cudaError_t launch_prefill_single(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
+cudaError_t prefill_pair_configure(int head_size);
+cudaError_t launch_prefill_pair(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 
