@@ -388,9 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) x[c] = ((mask >> (c >> log_r)) & 1) ? -INFINITY : x[c];
         }
-        float tmax = -INFINITY;
+        // Row max as a tree (a 64-long dependent chain would dominate).
+        float mx[16];
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) tmax = fmaxf(tmax, x[c]);
+        for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(x[c], x[c + 16]), fmaxf(x[c + 32], x[c + 48]));
+#pragma unroll
+        for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+          for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+        const float tmax = mx[0];
         const float cand = tmax * mul;
         float alpha = 1.f;
         if (cand > m_ref + kLazyRescale || (m_ref == -INFINITY && cand != -INFINITY)) {
@@ -398,15 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = cand;
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float rs = 0.f;
+        float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[kKeys / 2];
 #pragma unroll
         for (int c = 0; c < kKeys; c += 2) {
           const float e0 = ex2(fmaf(x[c], mul, -m_use));
           const float e1 = ex2(fmaf(x[c + 1], mul, -m_use));
-          rs += e0 + e1;
+          sums[(c >> 1) & 7] += e0 + e1;
           pk[c / 2] = pack_half2(e0, e1);
         }
+        const float rs = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
         l = l * alpha + rs;
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           float o[32];
