@@ -8,16 +8,23 @@
 // core is kept busy:
 //   * a unit is 256 query rows of one sequence and kv head: tile A (the
 //     first 128/G tokens) and tile B (the next 128/G), G heads per token;
-//     every 64-key K/V tile fetched is used by both tiles;
+//     every 128-key K/V tile fetched is used by both tiles;
+//   * S = Q K^T runs as M=128, N=128 MMAs: at N=128 the tensor core reads
+//     8 KB of shared memory per 64-cycle MMA, within the 128 B/clk port
+//     (at N=64 it would read 6 KB per 32 cycles and wait on shared memory);
 //   * two softmax warpgroups, one per tile, alternate: while one computes
-//     P for its tile the tensor core runs the other tile's S and PV;
+//     P for its tile the tensor core runs the other tile's PV and next S;
 //   * P goes back into tensor memory (fp16 pairs over the tile's S columns)
 //     and feeds the PV MMA as its A operand, so it never touches shared
 //     memory; MMAs issued by one thread complete in order, so S(i+1) may
 //     reuse the columns once PV(i) is issued, and a wait on S(i+1) also
 //     covers PV(i);
-//   * TMEM: S_A, S_B (64 columns each), O_A, O_B (head_size each);
-//   * shared memory: Q double-buffered (both tiles), 3 K/V stages of 64 keys.
+//   * the softmax does two fp32 lanes per instruction (f32x2 FMA/ADD), a
+//     three-input max, and evaluates part of its exponentials with a
+//     polynomial on the FMA pipe so the MUFU unit is not the limit;
+//   * TMEM: S_A, S_B (128 columns each), O_A, O_B (head_size each);
+//   * shared memory: Q double-buffered (both tiles), a ring of K and V tile
+//     slots loaded in the order they are used: K0 V0 K1 V1 ...
 //
 // Roles (320 threads, one CTA per SM, persistent over a device queue):
 //   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B (thread = row =
@@ -31,23 +38,28 @@ namespace {
 
 constexpr int kThreads = 10 * 32;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
-constexpr int kKeys = 64;     // keys per K/V tile
-constexpr int kStages = 3;
+constexpr int kKeys = 128;  // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
+#ifndef PA_PREFILL_POLY_OF_4
+#define PA_PREFILL_POLY_OF_4 0  // exponential pairs out of every 4 evaluated by the polynomial
+#endif
+constexpr int kPolyOf4 = PA_PREFILL_POLY_OF_4;
+constexpr int kSmemLimit = 227 * 1024;
 
 template <int D>
 struct PairCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kQTileBytes = kPrefillRows * D * 2;  // one 128-row tile [chunk][row][128 B]
   static constexpr int kQBufBytes = 2 * kQTileBytes;         // tiles A and B
-  static constexpr int kKVBytes = kKeys * D * 2;             // K or V tile [chunk][key][128 B]
-  static constexpr int kStageBytes = 2 * kKVBytes;
+  static constexpr int kSlotBytes = kKeys * D * 2;           // one K or V tile [chunk][key][128 B]
+  static constexpr int kSlotsFit = (kSmemLimit - 2048 - 2 * kQBufBytes) / kSlotBytes;
+  static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
   // TMEM columns of S (and P) and of O for tile X (0 = A, 1 = B)
   static __host__ __device__ constexpr int s_col(int X) { return X * kKeys; }
   static __host__ __device__ constexpr int o_col(int X) { return 2 * kKeys + X * D; }
-  static constexpr int kTmemCols = (2 * kKeys + 2 * D <= 256) ? 256 : 512;
-  static constexpr int kDataBytes = 2 * kQBufBytes + kStages * kStageBytes;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kDataBytes = 2 * kQBufBytes + kSlots * kSlotBytes;
   static constexpr int kSmemBytes = 1024 + kDataBytes + 1024;
 };
 
@@ -61,16 +73,19 @@ struct UnitInfo {
   int n_kv[2];  // K/V tiles needed by A and by B (n_kv[1] >= n_kv[0])
   int kv_len;   // past + q_len of the sequence
   int lo_min;   // smallest position any row admits
-  int pad[5];
+  int b;        // sequence (row of the block table)
+  int pad[4];
 };
 
+constexpr int kInfoRing = 4;  // units published ahead of their use
+
 struct Ctrl {
-  UnitInfo info[2];
-  uint32_t kv_mask[kStages];
+  UnitInfo info[kInfoRing];
+  uint32_t kv_mask[8];  // per V slot: the tile's pages that are unmapped
   uint64_t q_full[2], q_empty[2];
-  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t full[8], empty[8];
   uint64_t s_full[2], p_full[2], o_done[2];
-  uint64_t info_full[2], info_empty[2];
+  uint64_t info_full[kInfoRing], info_empty[kInfoRing];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -92,15 +107,101 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "elect.sync _|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
+// Maximum of N values as a tree of three-input max.
+template <int N>
+__device__ __forceinline__ float max_tree(const float* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else {
+    constexpr int M = (N + 2) / 3;
+    float w[M];
+#pragma unroll
+    for (int k = 0; k < M; ++k) {
+      if (3 * k + 2 < N) w[k] = max3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+      else if (3 * k + 1 < N) w[k] = fmaxf(v[3 * k], v[3 * k + 1]);
+      else w[k] = v[3 * k];
+    }
+    return max_tree<M>(w);
+  }
+}
+
+// Two fp32 lanes in one 64-bit register (Blackwell f32x2 arithmetic).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unf2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// 2^x for a pair, on the FMA pipe: x = j + f with j = round(x) and
+// f in [-1/2, 1/2]; 2^f from the degree-3 polynomial that minimises the
+// largest relative error on that interval (Remez exchange: 7.5e-5, under
+// half an fp16 ulp), and j added to its exponent bits.  Arguments are
+// clamped at -120, so a masked -inf gives 2^-120, which rounds to fp16 0.
+__device__ __forceinline__ void exp2_poly(uint64_t x, float& e0, float& e1) {
+  float a, b;
+  unf2(x, a, b);
+  const uint64_t v = f2(fmaxf(a, -120.f), fmaxf(b, -120.f));
+  const uint64_t round_c = f2(12582912.f, 12582912.f);  // 1.5 * 2^23: adding it rounds to an integer
+  const uint64_t t = add2(v, round_c);
+  const uint64_t f = sub2(v, sub2(t, round_c));
+  uint64_t q = fma2(f, f2(0.0551716685f, 0.0551716685f), f2(0.242611125f, 0.242611125f));
+  q = fma2(q, f, f2(0.693260968f, 0.693260968f));
+  q = fma2(q, f, f2(0.999928057f, 0.999928057f));
+  float q0, q1, t0, t1;
+  unf2(q, q0, q1);
+  unf2(t, t0, t1);
+  // the low mantissa bits of t hold j (two's complement); shifted into the
+  // exponent field they scale 2^f by 2^j
+  e0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  e1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const PrefillParams p) {
   using C = PairCfg<D>;
+  constexpr int S = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;                       // [2 buffers][tiles A, B]
-  uint8_t* kv_s = q_s + 2 * C::kQBufBytes;   // [stage][K, V]
+  uint8_t* q_s = smem;                       // [2 buffers][tiles A, B]; later the tiles' output staging
+  uint8_t* kv_s = q_s + 2 * C::kQBufBytes;   // [slot]: K_i is load 2i, V_i load 2i+1
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::kDataBytes);
   volatile int* abort = &ctl->abort;
 
@@ -112,16 +213,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
-      mbar_init(&ctl->q_empty[i], 1);
+      mbar_init(&ctl->q_empty[i], 2);  // the output stores of tiles A and B
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], 4);
       mbar_init(&ctl->o_done[i], 1);
-      mbar_init(&ctl->info_full[i], 1);
-      mbar_init(&ctl->info_empty[i], 1 + 8);  // MMA thread + 8 softmax warps
     }
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&ctl->kv_full[i], 1);
-      mbar_init(&ctl->kv_empty[i], 1);
+    for (int i = 0; i < kInfoRing; ++i) {
+      mbar_init(&ctl->info_full[i], 1);
+      mbar_init(&ctl->info_empty[i], 1 + 8);  // MMA warp + 8 softmax warps
+    }
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&ctl->full[i], 1);
+      mbar_init(&ctl->empty[i], 1);
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
@@ -135,39 +238,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  const int log_r = p.log_page_rows;  // log2(min(block_size, 64))
+  const int log_r = p.log_page_rows;  // log2(min(block_size, 128))
   const int pages = kKeys >> log_r;
   const int tq = p.tile_tokens;       // tokens per 128-row tile
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
+    // Publishes unit t+1 (and loads its Q as soon as its buffer is free)
+    // while it streams unit t's K/V tiles, so a unit never starts by waiting
+    // for the work queue or for its queries.
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
+      prefetch_tmap(&tm_o);
     }
     const uint32_t q_bytes = C::kChunks * p.G * tq * 128;
-    uint32_t g = 0;
-    int last_q = -1;
+    uint32_t n_loads = 0, q_loads = 0;  // K/V slot loads and Q loads issued so far
     bool ok = true;
-    for (uint32_t tt = 0; ok; ++tt) {
-      const int slot = tt & 1;
-      int u = 0;
-      if (lane == 0) {
-        // First unit: this CTA's own index; then the shared queue.
-        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
-        else u = tt == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
-      }
-      u = __shfl_sync(0xffffffffu, u, 0);
-      if (u == -2) break;
-      UnitInfo& ui = ctl->info[slot];
-      if (u >= n_work) {
-        if (lane == 0) {
-          ui.u = -1;
-          mbar_arrive(&ctl->info_full[slot]);
-        }
-        break;
-      }
+    // Every lane computes the same description of unit u.
+    auto fetch = [&](int u, UnitInfo& f) {
+      f.u = -1;
+      if (u >= n_work) return;
       const int tile = u / p.Hk, k = u - tile * p.Hk;
       const int2 bq = p.pre_tiles[tile];
       const SeqInfo si = p.seq[bq.x];
@@ -177,48 +269,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos0 = si.kv_len - si.q_len + q0;
       const int lo_min = p.window >= 1 ? max(0, pos0 + 1 - p.window) : 0;
       const int key_lo = lo_min & ~(kKeys - 1);
-      const int nA = (pos0 + ntA - key_lo + kKeys - 1) / kKeys;
-      const int nB = ntB > 0 ? (pos0 + nt - key_lo + kKeys - 1) / kKeys : nA;
-      const int hi_end = pos0 + nt;
-      const int t0 = si.t0 + q0;
+      f.u = u;
+      f.k = k;
+      f.b = bq.x;
+      f.t0 = si.t0 + q0;
+      f.ntok[0] = ntA;
+      f.ntok[1] = ntB;
+      f.pos0 = pos0;
+      f.key_lo = key_lo;
+      f.n_kv[0] = (pos0 + ntA - key_lo + kKeys - 1) / kKeys;
+      f.n_kv[1] = ntB > 0 ? (pos0 + nt - key_lo + kKeys - 1) / kKeys : f.n_kv[0];
+      f.kv_len = si.kv_len;
+      f.lo_min = lo_min;
+    };
+    auto publish = [&](uint32_t t, const UnitInfo& f) -> bool {
+      const int slot = t % kInfoRing;
       if (lane == 0) {
-        ui.u = u;
-        ui.k = k;
-        ui.t0 = t0;
-        ui.ntok[0] = ntA;
-        ui.ntok[1] = ntB;
-        ui.pos0 = pos0;
-        ui.key_lo = key_lo;
-        ui.n_kv[0] = nA;
-        ui.n_kv[1] = nB;
-        ui.kv_len = si.kv_len;
-        ui.lo_min = lo_min;
-        mbar_arrive(&ctl->info_full[slot]);
-        const int qb = tt & 1;
-        if (!wait_or_abort(&ctl->q_empty[qb], ((tt >> 1) & 1) ^ 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->info_empty[slot], ((t / kInfoRing) & 1) ^ 1, abort, p.err)) {
           ok = false;
         } else {
-          mbar_arrive_expect_tx(&ctl->q_full[qb], 2 * q_bytes);
-          last_q = (int)tt;
-          uint8_t* qd = q_s + qb * C::kQBufBytes;
-          for (int half = 0; half < 2; ++half)
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(qd + half * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, k * p.G,
-                          t0 + half * tq, &ctl->q_full[qb]);
+          ctl->info[slot] = f;
+          mbar_arrive(&ctl->info_full[slot]);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      return ok;
+    };
+    // Q tiles of unit t into buffer t & 1 once the output of unit t-2 has
+    // left it; `block` = wait for that, else only test.  True once issued.
+    auto load_q = [&](uint32_t t, const UnitInfo& f, bool block) -> bool {
+      const int qb = t & 1;
+      const uint32_t par = ((t >> 1) & 1) ^ 1;
+      int issued = 0;
+      if (lane == 0) {
+        const bool free_buf = block ? wait_or_abort(&ctl->q_empty[qb], par, abort, p.err)
+                                    : mbar_test_wait(&ctl->q_empty[qb], par);
+        if (free_buf) {
+          mbar_arrive_expect_tx(&ctl->q_full[qb], 2 * q_bytes);
+          uint8_t* qd = q_s + qb * C::kQBufBytes;
+          for (int half = 0; half < 2; ++half)
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(qd + half * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, f.k * p.G,
+                          f.t0 + half * tq, &ctl->q_full[qb]);
+          issued = 1;
+        } else if (block) {
+          ok = false;
+        }
+      }
+      issued = __shfl_sync(0xffffffffu, issued, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      q_loads += issued;
+      return issued != 0;
+    };
+    // One K or V tile into the next ring slot: lane l copies page
+    // l / chunks, 64-column chunk l % chunks (a box of {64, 1, page rows}).
+    auto load_tile = [&](const CUtensorMap* tm, int k, int rc, bool is_v, uint32_t mask) -> bool {
+      const int slot = n_loads % S;
+      if (lane == 0) {
+        if (!wait_or_abort(&ctl->empty[slot], ((n_loads / S) & 1) ^ 1, abort, p.err)) {
+          ok = false;
+        } else {
+          if (is_v) ctl->kv_mask[slot] = mask;
+          mbar_arrive_expect_tx(&ctl->full[slot], C::kSlotBytes);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) return false;
+      const int lp = lane / C::kChunks, lc = lane % C::kChunks;
+      const int prc = __shfl_sync(0xffffffffu, rc, lp & 31);
+      if (lp < pages) {
+        uint8_t* dst = kv_s + slot * C::kSlotBytes + lc * (kKeys * 128) + ((uint32_t)lp << (log_r + 7));
+        tma_load_3d(dst, tm, lc * 64, k, prc, &ctl->full[slot]);
+      }
+      ++n_loads;
+      return true;
+    };
+    UnitInfo cur, nxt;
+    fetch(blockIdx.x, cur);  // first unit: this CTA's own index, then the shared queue
+    if (publish(0, cur) && cur.u >= 0) load_q(0, cur, true);
+    for (uint32_t tt = 0; ok && cur.u >= 0; ++tt) {
+      int u2 = 0;
+      if (lane == 0) u2 = (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
+      fetch(__shfl_sync(0xffffffffu, u2, 0), nxt);
+      if (!publish(tt + 1, nxt)) break;
+      bool q_next = nxt.u < 0;
 
-      const int* bt_row = p.block_table + (size_t)bq.x * p.MB;
+      const int hi_end = cur.pos0 + cur.ntok[0] + cur.ntok[1];
+      const int* bt_row = p.block_table + (size_t)cur.b * p.MB;
       auto load_id = [&](int r) -> int {
         return (r < p.MB && r * p.bs < hi_end) ? __ldg(bt_row + r) : -1;
       };
-      int win = key_lo / p.bs;
+      int win = cur.key_lo / p.bs;
       int id = load_id(win + lane);
-      for (int i = 0; i < nB; ++i, ++g) {
-        const int st = g % kStages;
-        const int key0 = key_lo + i * kKeys;
+      for (int i = 0; i < cur.n_kv[1]; ++i) {
+        const int key0 = cur.key_lo + i * kKeys;
         if ((key0 + kKeys - 1) / p.bs >= win + 32) {
           win = key0 / p.bs;
           id = load_id(win + lane);
@@ -232,110 +376,120 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
-        if (lane == 0) {
-          if (!wait_or_abort(&ctl->kv_empty[st], ((g / kStages) & 1) ^ 1, abort, p.err)) {
-            ok = false;
-          } else {
-            ctl->kv_mask[st] = mask;
-            mbar_arrive_expect_tx(&ctl->kv_full[st], C::kStageBytes);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        // one box {64, 1, R} per (page, chunk, K|V)
-        const int lp = lane / (2 * C::kChunks), lc = (lane >> 1) % C::kChunks;
-        const int prc = __shfl_sync(0xffffffffu, rc, lp & 31);
-        if (lp < pages) {
-          uint8_t* dst = kv_s + st * C::kStageBytes + (lane & 1) * C::kKVBytes + lc * (kKeys * 128) +
-                         ((uint32_t)lp << (log_r + 7));
-          tma_load_3d(dst, (lane & 1) ? &tm_v : &tm_k, lc * 64, k, prc, &ctl->kv_full[st]);
-        }
+        if (!load_tile(&tm_k, cur.k, rc, false, 0) || !load_tile(&tm_v, cur.k, rc, true, mask)) break;
+        if (!q_next) q_next = load_q(tt + 1, nxt, false);
       }
+      if (!ok || (!q_next && !load_q(tt + 1, nxt, true))) break;
+      cur = nxt;
     }
     if (lane == 0 && *abort) {
       // Gave up: let the copies already issued land before the CTA exits.
-      for (uint32_t i = 0; i < kWaitLimit && last_q >= 0 &&
-                           !mbar_try_wait(&ctl->q_full[last_q & 1], (last_q >> 1) & 1);
-           ++i) {
+      if (q_loads > 0) {
+        const uint32_t t = q_loads - 1;
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->q_full[t & 1], (t >> 1) & 1); ++i) {
+        }
       }
-      for (int d = 1; d <= kStages && (int)g - d >= 0; ++d) {
-        const uint32_t gl = g - d;
-        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->kv_full[gl % kStages], (gl / kStages) & 1);
-             ++i) {
+      for (int d = 1; d <= S && (int)n_loads - d >= 0; ++d) {
+        const uint32_t n = n_loads - d;
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->full[n % S], (n / S) & 1); ++i) {
         }
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, kKeys, 0, 0);
-      constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
-      const uint32_t kv_addr = smem_u32(kv_s);
-      uint32_t g = 0, pcnt[2] = {0, 0};
-      bool ok = true;
-      for (uint32_t tt = 0; ok; ++tt) {
-        const int slot = tt & 1;
-        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
-        const UnitInfo ui = ctl->info[slot];
-        if (ui.u < 0) break;
-        const int qb = tt & 1;
-        if (!wait_or_abort(&ctl->q_full[qb], (tt >> 1) & 1, abort, p.err)) break;
+    // The whole warp runs this loop, so the descriptors stay warp-uniform;
+    // one elected lane issues the tcgen05 instructions (and their commits).
+    constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, kKeys, 0, 0);
+    constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
+    const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);           // K-major Q and K, + (address >> 4)
+    const uint64_t desc_v = smem_desc_sw128(0, kKeys * 128, 1024);  // MN-major V, + (address >> 4)
+    const uint32_t kv_addr = smem_u32(kv_s);
+    const bool leader = elect_one();
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort, p.err));
+    };
+    uint32_t g = 0, pcnt[2] = {0, 0};
+    bool ok = true;
+    for (uint32_t tt = 0; ok; ++tt) {
+      const int slot = tt % kInfoRing;
+      if (!wait_all(&ctl->info_full[slot], (tt / kInfoRing) & 1)) break;
+      const UnitInfo& ui = ctl->info[slot];
+      if (ui.u < 0) break;
+      const int nA = ui.n_kv[0], n_last = ui.n_kv[1];
+      const int qb = tt & 1;
+      if (!wait_all(&ctl->q_full[qb], (tt >> 1) & 1)) break;
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(q_s + qb * C::kQBufBytes);
+      // S_X(i) = Q_X K_i^T.  K_i is released after tile B's S.
+      auto issue_s = [&](int X, int i) -> bool {
+        const uint32_t n = 2 * (g + i);
+        const int st = n % S;
+        if (!wait_all(&ctl->full[st], (n / S) & 1)) return false;
         tc_fence_after();
-        const uint32_t q_addr = smem_u32(q_s + qb * C::kQBufBytes);
-        const int n_last = ui.n_kv[1];
-        // S_X(i) = Q_X K_i^T; the unit's last S releases the Q buffer.
-        auto issue_s = [&](int X, int i) -> bool {
-          const uint32_t gi = g + i;
-          const int st = gi % kStages;
-          if (!wait_or_abort(&ctl->kv_full[st], (gi / kStages) & 1, abort, p.err)) return false;
-          tc_fence_after();
-          const uint32_t kb = kv_addr + st * C::kStageBytes;
-          const uint32_t qa = q_addr + X * C::kQTileBytes;
+        const uint64_t a0 = desc_k + ((q_addr + X * C::kQTileBytes) >> 4);
+        const uint64_t b0 = desc_k + ((kv_addr + st * C::kSlotBytes) >> 4);
+        if (leader) {
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t a = smem_desc_sw128(qa + (ks >> 2) * (kPrefillRows * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(kb + (ks >> 2) * (kKeys * 128) + (ks & 3) * 32, 16, 1024);
-            umma_f16(tmem + C::s_col(X), a, b, idesc_s, ks > 0);
-          }
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_f16(tmem + C::s_col(X), a0 + (((ks >> 2) * (kPrefillRows * 128) + (ks & 3) * 32) >> 4),
+                     b0 + (((ks >> 2) * (kKeys * 128) + (ks & 3) * 32) >> 4), idesc_s, ks > 0);
           umma_commit(&ctl->s_full[X]);
-          if (X == 1 && i == n_last - 1) umma_commit(&ctl->q_empty[qb]);
-          return true;
-        };
-        // O_X += P_X(i) V_i with P_X read from TMEM (fp16 pairs over S_X).
-        auto issue_pv = [&](int X, int i) -> bool {
-          if (!wait_or_abort(&ctl->p_full[X], pcnt[X] & 1, abort, p.err)) return false;
-          ++pcnt[X];
-          tc_fence_after();
-          const int st = (g + i) % kStages;
-          const uint32_t vb = kv_addr + st * C::kStageBytes + C::kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t b = smem_desc_sw128(vb + kk * 16 * 128, kKeys * 128, 1024);
-            umma_f16_ts(tmem + C::o_col(X), tmem + C::s_col(X) + kk * 8, b, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          return true;
-        };
-        if (!issue_s(0, 0) || !issue_s(1, 0)) break;
-        for (int i = 0; i < n_last && ok; ++i) {
-          if (i < ui.n_kv[0]) {
-            if (!issue_pv(0, i)) { ok = false; break; }
-            if (i == ui.n_kv[0] - 1) umma_commit(&ctl->o_done[0]);
-            else if (!issue_s(0, i + 1)) { ok = false; break; }
-          }
-          if (!issue_pv(1, i)) { ok = false; break; }
-          umma_commit(&ctl->kv_empty[(g + i) % kStages]);
-          if (i == n_last - 1) umma_commit(&ctl->o_done[1]);
-          else if (!issue_s(1, i + 1)) { ok = false; break; }
+          if (X == 1) umma_commit(&ctl->empty[st]);
         }
-        g += n_last;
-        if (!ok) break;
-        mbar_arrive(&ctl->info_empty[slot]);
+        __syncwarp();
+        return true;
+      };
+      // O_X += P_X(i) V_i with P_X read from TMEM (fp16 pairs over S_X).
+      // V_i is released after tile B's PV.
+      auto issue_pv = [&](int X, int i) -> bool {
+        if (!wait_all(&ctl->p_full[X], pcnt[X] & 1)) return false;
+        ++pcnt[X];
+        const uint32_t n = 2 * (g + i) + 1;
+        const int st = n % S;
+        if (!wait_all(&ctl->full[st], (n / S) & 1)) return false;
+        tc_fence_after();
+        const uint64_t b0 = desc_v + ((kv_addr + st * C::kSlotBytes) >> 4);
+        if (leader) {
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            umma_f16_ts(tmem + C::o_col(X), tmem + C::s_col(X) + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          if (X == 1) umma_commit(&ctl->empty[st]);
+        }
+        __syncwarp();
+        return true;
+      };
+      if (!issue_s(0, 0) || !issue_s(1, 0)) break;
+      for (int i = 0; i < n_last && ok; ++i) {
+        if (i < nA) {
+          if (!issue_pv(0, i)) { ok = false; break; }
+          if (i == nA - 1) {
+            if (leader) umma_commit(&ctl->o_done[0]);
+          } else if (!issue_s(0, i + 1)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!issue_pv(1, i)) { ok = false; break; }
+        if (i == n_last - 1) {
+          if (leader) umma_commit(&ctl->o_done[1]);
+        } else if (!issue_s(1, i + 1)) {
+          ok = false;
+          break;
+        }
       }
-      // Drain: every MMA issued above has completed before TMEM is freed.
+      g += n_last;
+      if (!ok) break;
+      __syncwarp();
+      if (leader) mbar_arrive(&ctl->info_empty[slot]);
+    }
+    // Drain: every MMA issued above has completed before TMEM is freed.
+    if (leader) {
       umma_commit(&ctl->drain);
       for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->drain, 0); ++i) {
       }
     }
+    __syncwarp();
   } else {
     // ----------------------------------------------------- softmax warps
     const int X = warp >> 2;                  // 0: tile A, 1: tile B
@@ -344,12 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = CAP ? 1.f : p.scale * kLog2e;
     const float cap_in = CAP ? p.scale / p.softcap : 0.f;
     const float cap_out = CAP ? p.softcap * kLog2e : 0.f;
+    const bool storer = r == 0;               // issues the tile's output store
     uint32_t g = 0, scnt = 0, ocnt = 0;
     float x[kKeys];
     for (uint32_t tt = 0;; ++tt) {
-      const int slot = tt & 1;
-      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
-      const UnitInfo ui = ctl->info[slot];
+      const int slot = tt % kInfoRing;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err)) break;
+      const UnitInfo& ui = ctl->info[slot];  // read in place: registers are scarce here
       if (ui.u < 0) break;
       const int j = r / p.G;
       const bool row_ok = j < ui.ntok[X];
@@ -359,25 +514,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int i = 0; i < n_x; ++i) {
-        const uint32_t gi = g + i;
-        const int st = gi % kStages;
+        const uint32_t nv = 2 * (g + i) + 1;
+        const int sv = nv % S;
         const int key0 = ui.key_lo + i * kKeys;
-        // s_full(i) also covers PV(i-1): MMAs complete in issue order.
+        // s_full(i) also covers PV(i-1): MMAs complete in issue order.  The
+        // V slot carries the tile's page mask (and its rows may need zeros).
         if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->kv_full[st], (gi / kStages) & 1, abort, p.err)) {
+            !wait_or_abort(&ctl->full[sv], (nv / S) & 1, abort, p.err)) {
           ok = false;
           break;
         }
         ++scnt;
         tc_fence_after();
-        tmem_ld32(lane_addr + C::s_col(X), x);
-        tmem_ld32(lane_addr + C::s_col(X) + 32, x + 32);
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 32) tmem_ld32(lane_addr + C::s_col(X) + c, x + c);
         tmem_ld_wait();
         if constexpr (CAP) {
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) x[c] = cap_out * tanhf(x[c] * cap_in);
         }
-        const uint32_t mask = ctl->kv_mask[st];
+        const uint32_t mask = ctl->kv_mask[sv];
         const int c_lo = row_ok ? max(lo - key0, 0) : kKeys;
         const int c_hi = row_ok ? min(hi - key0, kKeys - 1) : -1;
         if (c_lo > 0 || c_hi < kKeys - 1) {
@@ -388,33 +544,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) x[c] = ((mask >> (c >> log_r)) & 1) ? -INFINITY : x[c];
         }
-        // Row max as a tree (a 64-long dependent chain would dominate).
-        float mx[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) mx[c] = fmaxf(fmaxf(x[c], x[c + 16]), fmaxf(x[c + 32], x[c + 48]));
-#pragma unroll
-        for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-          for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-        const float tmax = mx[0];
-        const float cand = tmax * mul;
+        const float cand = max_tree<kKeys>(x) * mul;
         float alpha = 1.f;
         if (cand > m_ref + kLazyRescale || (m_ref == -INFINITY && cand != -INFINITY)) {
           alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - cand);
           m_ref = cand;
         }
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        float sums[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[kKeys / 2];
+        const uint64_t mul2 = f2(mul, mul), neg_m2 = f2(-m_use, -m_use);
+        uint64_t sum2[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int c = 0; c < kKeys; c += 2) {
-          const float e0 = ex2(fmaf(x[c], mul, -m_use));
-          const float e1 = ex2(fmaf(x[c + 1], mul, -m_use));
-          sums[(c >> 1) & 7] += e0 + e1;
-          pk[c / 2] = pack_half2(e0, e1);
+        for (int h = 0; h < kKeys; h += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint64_t arg = fma2(f2(x[h + 2 * q], x[h + 2 * q + 1]), mul2, neg_m2);
+            float e0, e1;
+            if ((q & 3) < kPolyOf4) {
+              exp2_poly(arg, e0, e1);
+            } else {
+              float a0, a1;
+              unf2(arg, a0, a1);
+              e0 = ex2(a0);
+              e1 = ex2(a1);
+            }
+            sum2[q & 3] = add2(sum2[q & 3], f2(e0, e1));
+            pk[q] = pack_half2(e0, e1);
+          }
+          // P_X -> TMEM over S_X: keys h..h+31 as 16 columns of fp16 pairs
+          tmem_st16(lane_addr + C::s_col(X) + h / 2, pk);
         }
-        const float rs = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-        l = l * alpha + rs;
+        float s0, s1, s2, s3;
+        unf2(add2(sum2[0], sum2[1]), s0, s1);
+        unf2(add2(sum2[2], sum2[3]), s2, s3);
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           float o[32];
 #pragma unroll 1
@@ -429,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Never-admitted keys of an edge tile: zero their V rows (tile A does
         // it while it uses the tile, tile B for the tiles A skips).
         if ((X == 0 || i >= ui.n_kv[0]) && (key0 + kKeys > ui.kv_len || key0 < ui.lo_min)) {
-          uint8_t* vs = kv_s + st * C::kStageBytes + C::kKVBytes;
+          uint8_t* vs = kv_s + sv * C::kSlotBytes;
           for (int idx = r; idx < kKeys * C::kChunks * 8; idx += 128) {
             const int kr = idx / (C::kChunks * 8), rem = idx % (C::kChunks * 8);
             const int pos = key0 + kr;
@@ -441,19 +604,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
         }
-        // P_X -> TMEM over S_X (32 columns of fp16 pairs)
-        tmem_st32(lane_addr + C::s_col(X), reinterpret_cast<const float*>(pk));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full[X]);
       }
       if (!ok) break;
-      // epilogue: O_X / l -> fp16 output rows
+      // Epilogue: O_X / l -> fp16 rows.  A full tile is staged in its half of
+      // the unit's Q buffer (every S of the unit has completed once o_done
+      // fires) and leaves in one TMA store per 64 columns; a ragged tile is
+      // stored row by row.  The buffer is released when its stores have read it.
       if (!wait_or_abort(&ctl->o_done[X], ocnt & 1, abort, p.err)) break;
       ++ocnt;
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      const int qb = tt & 1;
+      const bool full = ui.ntok[X] == tq;
+      uint8_t* stage = q_s + qb * C::kQBufBytes + X * C::kQTileBytes;
       const int t = ui.t0 + X * tq + j, h = ui.k * p.G + (r - j * p.G);
       __half* dst = p.out + ((size_t)t * p.H + h) * D;
 #pragma unroll 1
@@ -461,23 +628,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[32];
         tmem_ld32(lane_addr + C::o_col(X) + 32 * c, o);
         tmem_ld_wait();
-        if (row_ok) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-            w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-            w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-            w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
+          w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
+          w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
+          w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+          if (full) {
+            // [64-column chunk][row][128 B], 16-byte units swizzled by row % 8
+            const int unit = (c & 1) * 4 + q;
+            *reinterpret_cast<uint4*>(stage + (c >> 1) * (kPrefillRows * 128) + r * 128 +
+                                      ((unit ^ (r & 7)) << 4)) = w;
+          } else if (row_ok) {
             *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
           }
         }
       }
       tc_fence_before();
+      if (full) {
+        fence_proxy_async_smem();
+        named_bar(1 + X, 128);
+        if (storer) {
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_store_3d(&tm_o, stage + c * (kPrefillRows * 128), c * 64, ui.k * p.G, ui.t0 + X * tq);
+          bulk_commit();
+          bulk_wait_read();
+        }
+      }
+      if (storer) mbar_arrive(&ctl->q_empty[qb]);
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
       g += ui.n_kv[1];
     }
+    if (storer) bulk_wait();  // the output is written before the CTA exits
   }
 
   tc_fence_before();
@@ -491,17 +675,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool CAP>
 cudaError_t configure_dc() {
   static_assert(sizeof(Ctrl) <= 1024, "control block");
-  static_assert(PairCfg<D>::kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(PairCfg<D>::kSmemBytes <= kSmemLimit, "shared memory");
+  static_assert(PairCfg<D>::kSlots >= 3, "K/V ring");
+  static_assert(2 * kKeys + 2 * D <= PairCfg<D>::kTmemCols, "tensor memory");
   return cudaFuncSetAttribute(prefill_pair_kernel<D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PairCfg<D>::kSmemBytes);
 }
 
 template <int D>
-cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                     int grid, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                     const PrefillParams& p, int grid, cudaStream_t s) {
   if (p.softcap > 0.f)
-    return launch_pdl(prefill_pair_kernel<D, true>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
-  return launch_pdl(prefill_pair_kernel<D, false>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+    return launch_pdl(prefill_pair_kernel<D, true>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, to, p);
+  return launch_pdl(prefill_pair_kernel<D, false>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, to, p);
 }
 
 }  // namespace
@@ -520,10 +706,10 @@ cudaError_t prefill_pair_configure(int head_size) {
 }
 
 cudaError_t launch_prefill_pair(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const PrefillParams& p, int grid, cudaStream_t s) {
+                                const CUtensorMap& to, const PrefillParams& p, int grid, cudaStream_t s) {
   switch (head_size) {
-    case 64: return launch_d<64>(tq, tk, tv, p, grid, s);
-    case 128: return launch_d<128>(tq, tk, tv, p, grid, s);
+    case 64: return launch_d<64>(tq, tk, tv, to, p, grid, s);
+    case 128: return launch_d<128>(tq, tk, tv, to, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -550,8 +736,8 @@ int prefill_unit_tokens(int head_size, int group) {
 }
 
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int grid, cudaStream_t s) {
-  if (prefill_uses_pairs(head_size)) return launch_prefill_pair(head_size, tq, tk, tv, p, grid, s);
+                           const CUtensorMap& to, const PrefillParams& p, int grid, cudaStream_t s) {
+  if (prefill_uses_pairs(head_size)) return launch_prefill_pair(head_size, tq, tk, tv, to, p, grid, s);
   return launch_prefill_single(head_size, tq, tk, tv, p, grid, s);
 }
 
