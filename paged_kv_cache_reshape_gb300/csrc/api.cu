@@ -638,12 +638,11 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   // 4. varlen prefill on tensor memory (skipped when the query-length bound
   // already routes every sequence to the decode kernel)
   if (h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows) {
-    CUtensorMap tq, tkp, tvp, to;
+    CUtensorMap tq, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_q_tokens) ||
         !encode_map(&tkp, key_cache, D, c.kv_num_heads, pool_rows, 1, prow) ||
-        !encode_map(&tvp, value_cache, D, c.kv_num_heads, pool_rows, 1, prow) ||
-        !encode_map(&to, output, D, c.num_heads, token_count, h->G, h->prefill_q_tokens))
+        !encode_map(&tvp, value_cache, D, c.kv_num_heads, pool_rows, 1, prow))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
     pa::PrefillParams p{};
     p.out = static_cast<__half*>(output);
@@ -665,7 +664,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.window = c.local_window_size;
     p.oob_row = pool_rows;
     StageTimer t(h, PA_STAGE_PREFILL, s);
-    cudaError_t e = pa::launch_prefill(D, tq, tkp, tvp, to, p, h->pre_grid, s);
+    cudaError_t e = pa::launch_prefill(D, tq, tkp, tvp, p, h->pre_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
     h->last_launches++;
   }
@@ -902,12 +901,11 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "decode launch");
 
   if (nd->prefill_ok) {
-    CUtensorMap tqp, tkp, tvp, top;
+    CUtensorMap tqp, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tqp, q_att, D, H, token_count, G, q_tokens) ||
         !encode_map(&tkp, key_cache, D, Hk, pool_rows, 1, prow) ||
-        !encode_map(&tvp, value_cache, D, Hk, pool_rows, 1, prow) ||
-        !encode_map(&top, output, D, H, token_count, G, q_tokens))
+        !encode_map(&tvp, value_cache, D, Hk, pool_rows, 1, prow))
       return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
     pa::PrefillParams pp{};
     pp.out = static_cast<__half*>(output);
@@ -928,7 +926,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
     pp.softcap = c.softcap;
     pp.window = c.local_window_size;
     pp.oob_row = pool_rows;
-    e = pa::launch_prefill(D, tqp, tkp, tvp, top, pp, std::max(1, std::min(nd->num_sms, cap_pre * Hk)), s);
+    e = pa::launch_prefill(D, tqp, tkp, tvp, pp, std::max(1, std::min(nd->num_sms, cap_pre * Hk)), s);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "prefill launch");
   }
 

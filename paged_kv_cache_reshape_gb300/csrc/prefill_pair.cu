@@ -26,9 +26,12 @@
 //   * shared memory: Q double-buffered (both tiles), a ring of K and V tile
 //     slots loaded in the order they are used: K0 V0 K1 V1 ...
 //
-// Roles (320 threads, one CTA per SM, persistent over a device queue):
-//   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B (thread = row =
-//   TMEM lane), warp 8 TMA producer, warp 9 TMEM owner + MMA issuer.
+// Roles (512 threads = 4 warpgroups, one CTA per SM, persistent over a
+// device queue; registers moved between warpgroups with setmaxnreg):
+//   warpgroup 0 / 1: softmax of tile A / B (thread = row = TMEM lane);
+//   warpgroup 2: epilogue of both tiles: reads O from TMEM (releasing it to
+//     the next unit at once), divides by the row sums, stores the output;
+//   warpgroup 3: warp 12 TMA producer, warp 13 TMEM owner + MMA issuer.
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -36,8 +39,11 @@
 namespace pa {
 namespace {
 
-constexpr int kThreads = 10 * 32;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 16 * 32;
+constexpr int kEpiWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
+// Registers per thread after the split (launch: 65536 / 512 = 128 each).
+constexpr int kRegSoftmax = 184, kRegEpilogue = 64, kRegControl = 80;
+static_assert(2 * kRegSoftmax + kRegEpilogue + kRegControl == 4 * 128, "register split");
 constexpr int kKeys = 128;  // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
@@ -46,21 +52,21 @@ constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated be
 #endif
 constexpr int kPolyOf4 = PA_PREFILL_POLY_OF_4;
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kCtrlBytes = 2048;
 
 template <int D>
 struct PairCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kQTileBytes = kPrefillRows * D * 2;  // one 128-row tile [chunk][row][128 B]
-  static constexpr int kQBufBytes = 2 * kQTileBytes;         // tiles A and B
   static constexpr int kSlotBytes = kKeys * D * 2;           // one K or V tile [chunk][key][128 B]
-  static constexpr int kSlotsFit = (kSmemLimit - 2048 - 2 * kQBufBytes) / kSlotBytes;
+  static constexpr int kSlotsFit = (kSmemLimit - 1024 - kCtrlBytes - 2 * kQTileBytes) / kSlotBytes;
   static constexpr int kSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
   // TMEM columns of S (and P) and of O for tile X (0 = A, 1 = B)
   static __host__ __device__ constexpr int s_col(int X) { return X * kKeys; }
   static __host__ __device__ constexpr int o_col(int X) { return 2 * kKeys + X * D; }
   static constexpr int kTmemCols = 512;
-  static constexpr int kDataBytes = 2 * kQBufBytes + kSlots * kSlotBytes;
-  static constexpr int kSmemBytes = 1024 + kDataBytes + 1024;
+  static constexpr int kDataBytes = 2 * kQTileBytes + kSlots * kSlotBytes;
+  static constexpr int kSmemBytes = 1024 + kDataBytes + kCtrlBytes;
 };
 
 struct UnitInfo {
@@ -82,13 +88,15 @@ constexpr int kInfoRing = 4;  // units published ahead of their use
 struct Ctrl {
   UnitInfo info[kInfoRing];
   uint32_t kv_mask[8];  // per V slot: the tile's pages that are unmapped
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[2], q_empty[2];  // per tile (A, B): its Q buffer
   uint64_t full[8], empty[8];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t l_full[2], l_empty[2];
   uint64_t info_full[kInfoRing], info_empty[kInfoRing];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  float l_row[2][kPrefillRows];  // per tile: the softmax row sums of the unit, for the epilogue
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
@@ -105,6 +113,15 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
 
 // True in exactly one lane of the (converged) warp.
@@ -194,14 +211,14 @@ __device__ __forceinline__ void exp2_poly(uint64_t x, float& e0, float& e1) {
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const __grid_constant__ CUtensorMap tm_v,
                         const PrefillParams p) {
   using C = PairCfg<D>;
   constexpr int S = C::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;                       // [2 buffers][tiles A, B]; later the tiles' output staging
-  uint8_t* kv_s = q_s + 2 * C::kQBufBytes;   // [slot]: K_i is load 2i, V_i load 2i+1
+  uint8_t* q_s = smem;                       // [tile A, tile B]
+  uint8_t* kv_s = q_s + 2 * C::kQTileBytes;  // [slot]: K_i is load 2i, V_i load 2i+1
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + C::kDataBytes);
   volatile int* abort = &ctl->abort;
 
@@ -213,14 +230,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->q_full[i], 1);
-      mbar_init(&ctl->q_empty[i], 2);  // the output stores of tiles A and B
+      mbar_init(&ctl->q_empty[i], 1);
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->p_full[i], 4);
       mbar_init(&ctl->o_done[i], 1);
+      mbar_init(&ctl->o_free[i], 4);
+      mbar_init(&ctl->l_full[i], 4);
+      mbar_init(&ctl->l_empty[i], 4);
     }
     for (int i = 0; i < kInfoRing; ++i) {
       mbar_init(&ctl->info_full[i], 1);
-      mbar_init(&ctl->info_empty[i], 1 + 8);  // MMA warp + 8 softmax warps
+      mbar_init(&ctl->info_empty[i], 1 + 8 + 4);  // MMA warp, softmax and epilogue warps
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(&ctl->full[i], 1);
@@ -242,7 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pages = kKeys >> log_r;
   const int tq = p.tile_tokens;       // tokens per 128-row tile
 
-  if (warp == kProducerWarp) {
+  // Register split: each warpgroup resizes at the top of its own branch
+  // (the allocator budgets a branch from the setmaxnreg that dominates it).
+  if (warp >= kProducerWarp) {
+   regs_dec<kRegControl>();
+   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     // Publishes unit t+1 (and loads its Q as soon as its buffer is free)
     // while it streams unit t's K/V tiles, so a unit never starts by waiting
@@ -251,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_o);
     }
     const uint32_t q_bytes = C::kChunks * p.G * tq * 128;
     uint32_t n_loads = 0, q_loads = 0;  // K/V slot loads and Q loads issued so far
@@ -295,31 +318,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       return ok;
     };
-    // Q tiles of unit t into buffer t & 1 once the output of unit t-2 has
-    // left it; `block` = wait for that, else only test.  True once issued.
-    auto load_q = [&](uint32_t t, const UnitInfo& f, bool block) -> bool {
-      const int qb = t & 1;
-      const uint32_t par = ((t >> 1) & 1) ^ 1;
-      int issued = 0;
+    // Q tile X of unit t into its buffer once the last S of tile X of unit
+    // t-1 has completed.
+    auto load_q = [&](uint32_t t, int X, const UnitInfo& f) -> bool {
       if (lane == 0) {
-        const bool free_buf = block ? wait_or_abort(&ctl->q_empty[qb], par, abort, p.err)
-                                    : mbar_test_wait(&ctl->q_empty[qb], par);
-        if (free_buf) {
-          mbar_arrive_expect_tx(&ctl->q_full[qb], 2 * q_bytes);
-          uint8_t* qd = q_s + qb * C::kQBufBytes;
-          for (int half = 0; half < 2; ++half)
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_3d(qd + half * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, f.k * p.G,
-                          f.t0 + half * tq, &ctl->q_full[qb]);
-          issued = 1;
-        } else if (block) {
+        if (!wait_or_abort(&ctl->q_empty[X], (t & 1) ^ 1, abort, p.err)) {
           ok = false;
+        } else {
+          mbar_arrive_expect_tx(&ctl->q_full[X], q_bytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(q_s + X * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, f.k * p.G,
+                        f.t0 + X * tq, &ctl->q_full[X]);
         }
       }
-      issued = __shfl_sync(0xffffffffu, issued, 0);
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      q_loads += issued;
-      return issued != 0;
+      q_loads += ok ? 1 : 0;
+      return ok;
     };
     // One K or V tile into the next ring slot: lane l copies page
     // l / chunks, 64-column chunk l % chunks (a box of {64, 1, page rows}).
@@ -344,15 +358,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_loads;
       return true;
     };
+    // Per unit: K0, Q_A, V0, Q_B, then the other K/V tiles.  The Q waits
+    // depend only on the previous unit's S MMAs, whose K tiles are already
+    // issued.
     UnitInfo cur, nxt;
     fetch(blockIdx.x, cur);  // first unit: this CTA's own index, then the shared queue
-    if (publish(0, cur) && cur.u >= 0) load_q(0, cur, true);
+    publish(0, cur);
     for (uint32_t tt = 0; ok && cur.u >= 0; ++tt) {
       int u2 = 0;
       if (lane == 0) u2 = (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
       fetch(__shfl_sync(0xffffffffu, u2, 0), nxt);
       if (!publish(tt + 1, nxt)) break;
-      bool q_next = nxt.u < 0;
 
       const int hi_end = cur.pos0 + cur.ntok[0] + cur.ntok[1];
       const int* bt_row = p.block_table + (size_t)cur.b * p.MB;
@@ -376,17 +392,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
-        if (!load_tile(&tm_k, cur.k, rc, false, 0) || !load_tile(&tm_v, cur.k, rc, true, mask)) break;
-        if (!q_next) q_next = load_q(tt + 1, nxt, false);
+        if (!load_tile(&tm_k, cur.k, rc, false, 0) || (i == 0 && !load_q(tt, 0, cur)) ||
+            !load_tile(&tm_v, cur.k, rc, true, mask) || (i == 0 && !load_q(tt, 1, cur)))
+          break;
       }
-      if (!ok || (!q_next && !load_q(tt + 1, nxt, true))) break;
+      if (!ok) break;
       cur = nxt;
     }
     if (lane == 0 && *abort) {
       // Gave up: let the copies already issued land before the CTA exits.
-      if (q_loads > 0) {
-        const uint32_t t = q_loads - 1;
-        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->q_full[t & 1], (t >> 1) & 1); ++i) {
+      for (int d = 1; d <= 2 && (int)q_loads - d >= 0; ++d) {
+        const uint32_t n = q_loads - d;  // Q loads alternate A, B
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->q_full[n & 1], (n >> 1) & 1); ++i) {
         }
       }
       for (int d = 1; d <= S && (int)n_loads - d >= 0; ++d) {
@@ -395,68 +412,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    // The whole warp runs this loop, so the descriptors stay warp-uniform;
-    // one elected lane issues the tcgen05 instructions (and their commits).
+    // One lane, elected with elect.sync, runs the whole loop: it waits on
+    // the barriers alone (a warp-wide wait and vote per barrier costs several
+    // times more) and issues the tcgen05 instructions.
     constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, kKeys, 0, 0);
     constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
     const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);           // K-major Q and K, + (address >> 4)
     const uint64_t desc_v = smem_desc_sw128(0, kKeys * 128, 1024);  // MN-major V, + (address >> 4)
     const uint32_t kv_addr = smem_u32(kv_s);
     const bool leader = elect_one();
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort, p.err));
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return wait_or_abort(bar, parity, abort, p.err);
     };
     uint32_t g = 0, pcnt[2] = {0, 0};
-    bool ok = true;
+    bool ok = leader;
     for (uint32_t tt = 0; ok; ++tt) {
       const int slot = tt % kInfoRing;
-      if (!wait_all(&ctl->info_full[slot], (tt / kInfoRing) & 1)) break;
+      if (!wait_bar(&ctl->info_full[slot], (tt / kInfoRing) & 1)) break;
       const UnitInfo& ui = ctl->info[slot];
       if (ui.u < 0) break;
       const int nA = ui.n_kv[0], n_last = ui.n_kv[1];
-      const int qb = tt & 1;
-      if (!wait_all(&ctl->q_full[qb], (tt >> 1) & 1)) break;
-      tc_fence_after();
-      const uint32_t q_addr = smem_u32(q_s + qb * C::kQBufBytes);
-      // S_X(i) = Q_X K_i^T.  K_i is released after tile B's S.
+      const uint32_t q_addr = smem_u32(q_s);
+      // S_X(i) = Q_X K_i^T.  K_i is released after tile B's S, Q_X after
+      // the unit's last S_X.
       auto issue_s = [&](int X, int i) -> bool {
         const uint32_t n = 2 * (g + i);
         const int st = n % S;
-        if (!wait_all(&ctl->full[st], (n / S) & 1)) return false;
+        if (i == 0 && !wait_bar(&ctl->q_full[X], tt & 1)) return false;
+        if (!wait_bar(&ctl->full[st], (n / S) & 1)) return false;
         tc_fence_after();
         const uint64_t a0 = desc_k + ((q_addr + X * C::kQTileBytes) >> 4);
         const uint64_t b0 = desc_k + ((kv_addr + st * C::kSlotBytes) >> 4);
-        if (leader) {
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_f16(tmem + C::s_col(X), a0 + (((ks >> 2) * (kPrefillRows * 128) + (ks & 3) * 32) >> 4),
-                     b0 + (((ks >> 2) * (kKeys * 128) + (ks & 3) * 32) >> 4), idesc_s, ks > 0);
-          umma_commit(&ctl->s_full[X]);
-          if (X == 1) umma_commit(&ctl->empty[st]);
-        }
-        __syncwarp();
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_f16(tmem + C::s_col(X), a0 + (((ks >> 2) * (kPrefillRows * 128) + (ks & 3) * 32) >> 4),
+                   b0 + (((ks >> 2) * (kKeys * 128) + (ks & 3) * 32) >> 4), idesc_s, ks > 0);
+        umma_commit(&ctl->s_full[X]);
+        if (X == 1) umma_commit(&ctl->empty[st]);
+        if (i == (X ? n_last : nA) - 1) umma_commit(&ctl->q_empty[X]);
         return true;
       };
       // O_X += P_X(i) V_i with P_X read from TMEM (fp16 pairs over S_X).
       // V_i is released after tile B's PV.
       auto issue_pv = [&](int X, int i) -> bool {
-        if (!wait_all(&ctl->p_full[X], pcnt[X] & 1)) return false;
+        if (!wait_bar(&ctl->p_full[X], pcnt[X] & 1)) return false;
         ++pcnt[X];
+        // the unit's first PV overwrites O_X: the epilogue has read the last unit's
+        if (i == 0 && tt > 0 && !wait_bar(&ctl->o_free[X], (tt - 1) & 1)) return false;
         const uint32_t n = 2 * (g + i) + 1;
         const int st = n % S;
-        if (!wait_all(&ctl->full[st], (n / S) & 1)) return false;
+        if (!wait_bar(&ctl->full[st], (n / S) & 1)) return false;
         tc_fence_after();
         const uint64_t b0 = desc_v + ((kv_addr + st * C::kSlotBytes) >> 4);
-        if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            umma_f16_ts(tmem + C::o_col(X), tmem + C::s_col(X) + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-          if (X == 1) umma_commit(&ctl->empty[st]);
-        }
-        __syncwarp();
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma_f16_ts(tmem + C::o_col(X), tmem + C::s_col(X) + kk * 8, b0 + ((kk * 16 * 128) >> 4), idesc_o,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        if (X == 1) umma_commit(&ctl->empty[st]);
         return true;
       };
       if (!issue_s(0, 0) || !issue_s(1, 0)) break;
@@ -464,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < nA) {
           if (!issue_pv(0, i)) { ok = false; break; }
           if (i == nA - 1) {
-            if (leader) umma_commit(&ctl->o_done[0]);
+            umma_commit(&ctl->o_done[0]);
           } else if (!issue_s(0, i + 1)) {
             ok = false;
             break;
@@ -472,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!issue_pv(1, i)) { ok = false; break; }
         if (i == n_last - 1) {
-          if (leader) umma_commit(&ctl->o_done[1]);
+          umma_commit(&ctl->o_done[1]);
         } else if (!issue_s(1, i + 1)) {
           ok = false;
           break;
@@ -480,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       g += n_last;
       if (!ok) break;
-      __syncwarp();
-      if (leader) mbar_arrive(&ctl->info_empty[slot]);
+      mbar_arrive(&ctl->info_empty[slot]);
     }
     // Drain: every MMA issued above has completed before TMEM is freed.
     if (leader) {
@@ -490,7 +503,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else {
+   }
+  } else if (warp < kEpiWarp0) {
+    regs_inc<kRegSoftmax>();
     // ----------------------------------------------------- softmax warps
     const int X = warp >> 2;                  // 0: tile A, 1: tile B
     const int r = threadIdx.x & 127;          // query row == TMEM lane
@@ -498,8 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float mul = CAP ? 1.f : p.scale * kLog2e;
     const float cap_in = CAP ? p.scale / p.softcap : 0.f;
     const float cap_out = CAP ? p.softcap * kLog2e : 0.f;
-    const bool storer = r == 0;               // issues the tile's output store
-    uint32_t g = 0, scnt = 0, ocnt = 0;
+    uint32_t g = 0, scnt = 0;
     float x[kKeys];
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt % kInfoRing;
@@ -610,58 +624,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&ctl->p_full[X]);
       }
       if (!ok) break;
-      // Epilogue: O_X / l -> fp16 rows.  A full tile is staged in its half of
-      // the unit's Q buffer (every S of the unit has completed once o_done
-      // fires) and leaves in one TMA store per 64 columns; a ragged tile is
-      // stored row by row.  The buffer is released when its stores have read it.
-      if (!wait_or_abort(&ctl->o_done[X], ocnt & 1, abort, p.err)) break;
-      ++ocnt;
-      tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
-      const int qb = tt & 1;
-      const bool full = ui.ntok[X] == tq;
-      uint8_t* stage = q_s + qb * C::kQBufBytes + X * C::kQTileBytes;
-      const int t = ui.t0 + X * tq + j, h = ui.k * p.G + (r - j * p.G);
-      __half* dst = p.out + ((size_t)t * p.H + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32(lane_addr + C::o_col(X) + 32 * c, o);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 w;
-          w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-          w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-          w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-          w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
-          if (full) {
-            // [64-column chunk][row][128 B], 16-byte units swizzled by row % 8
-            const int unit = (c & 1) * 4 + q;
-            *reinterpret_cast<uint4*>(stage + (c >> 1) * (kPrefillRows * 128) + r * 128 +
-                                      ((unit ^ (r & 7)) << 4)) = w;
-          } else if (row_ok) {
-            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
-          }
-        }
-      }
-      tc_fence_before();
-      if (full) {
-        fence_proxy_async_smem();
-        named_bar(1 + X, 128);
-        if (storer) {
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_store_3d(&tm_o, stage + c * (kPrefillRows * 128), c * 64, ui.k * p.G, ui.t0 + X * tq);
-          bulk_commit();
-          bulk_wait_read();
-        }
-      }
-      if (storer) mbar_arrive(&ctl->q_empty[qb]);
+      // The row sum goes to the epilogue warpgroup (its previous value has
+      // been read once l_empty completes).
+      if (!wait_or_abort(&ctl->l_empty[X], (tt & 1) ^ 1, abort, p.err)) break;
+      ctl->l_row[X][r] = l;
       __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->l_full[X]);
       if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
       g += ui.n_kv[1];
     }
-    if (storer) bulk_wait();  // the output is written before the CTA exits
+  } else {
+    regs_dec<kRegEpilogue>();
+    // ---------------------------------------------------------- epilogue
+    // For each tile of the unit: O_X / l -> fp16 output rows.  O is read
+    // from TMEM 32 columns at a time; after the last read it is released to
+    // the next unit's first PV.
+    const int r = threadIdx.x - kEpiWarp0 * 32;  // row == TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    uint32_t ocnt[2] = {0, 0};
+    for (uint32_t tt = 0;; ++tt) {
+      const int slot = tt % kInfoRing;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err)) break;
+      const UnitInfo& ui = ctl->info[slot];
+      if (ui.u < 0) break;
+      const int j = r / p.G;
+      bool ok = true;
+      for (int X = 0; X < 2 && ok; ++X) {
+        if (!wait_or_abort(&ctl->o_done[X], ocnt[X] & 1, abort, p.err) ||
+            !wait_or_abort(&ctl->l_full[X], tt & 1, abort, p.err)) {
+          ok = false;
+          break;
+        }
+        ++ocnt[X];
+        tc_fence_after();
+        const float l = ctl->l_row[X][r];
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->l_empty[X]);
+        const bool row_ok = j < ui.ntok[X];
+        const int t = ui.t0 + X * tq + j, h = ui.k * p.G + (r - j * p.G);
+        __half* dst = p.out + ((size_t)t * p.H + h) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_addr + C::o_col(X) + 32 * c, o);
+          tmem_ld_wait();
+          if (c == D / 32 - 1) {
+            // O_X is read: the next unit's first PV may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->o_free[X]);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 w;
+              w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
+              w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
+              w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
+              w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+              *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
+            }
+          }
+        }
+      }
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
+    }
   }
 
   tc_fence_before();
@@ -674,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, bool CAP>
 cudaError_t configure_dc() {
-  static_assert(sizeof(Ctrl) <= 1024, "control block");
+  static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
   static_assert(PairCfg<D>::kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(PairCfg<D>::kSlots >= 3, "K/V ring");
   static_assert(2 * kKeys + 2 * D <= PairCfg<D>::kTmemCols, "tensor memory");
@@ -683,11 +713,11 @@ cudaError_t configure_dc() {
 }
 
 template <int D>
-cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
-                     const PrefillParams& p, int grid, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                     int grid, cudaStream_t s) {
   if (p.softcap > 0.f)
-    return launch_pdl(prefill_pair_kernel<D, true>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, to, p);
-  return launch_pdl(prefill_pair_kernel<D, false>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, to, p);
+    return launch_pdl(prefill_pair_kernel<D, true>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return launch_pdl(prefill_pair_kernel<D, false>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -706,10 +736,10 @@ cudaError_t prefill_pair_configure(int head_size) {
 }
 
 cudaError_t launch_prefill_pair(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                const CUtensorMap& to, const PrefillParams& p, int grid, cudaStream_t s) {
+                                const PrefillParams& p, int grid, cudaStream_t s) {
   switch (head_size) {
-    case 64: return launch_d<64>(tq, tk, tv, to, p, grid, s);
-    case 128: return launch_d<128>(tq, tk, tv, to, p, grid, s);
+    case 64: return launch_d<64>(tq, tk, tv, p, grid, s);
+    case 128: return launch_d<128>(tq, tk, tv, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -736,8 +766,8 @@ int prefill_unit_tokens(int head_size, int group) {
 }
 
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const CUtensorMap& to, const PrefillParams& p, int grid, cudaStream_t s) {
-  if (prefill_uses_pairs(head_size)) return launch_prefill_pair(head_size, tq, tk, tv, to, p, grid, s);
+                           const PrefillParams& p, int grid, cudaStream_t s) {
+  if (prefill_uses_pairs(head_size)) return launch_prefill_pair(head_size, tq, tk, tv, p, grid, s);
   return launch_prefill_single(head_size, tq, tk, tv, p, grid, s);
 }
 

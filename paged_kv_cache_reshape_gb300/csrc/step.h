@@ -173,12 +173,8 @@ cudaError_t launch_prefill_single(int head_size, const CUtensorMap& tq, const CU
                                   const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 cudaError_t prefill_pair_configure(int head_size);
 cudaError_t launch_prefill_pair(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, int grid,
-                                cudaStream_t s);
-// `to`: the output as a tensor map of the same geometry as the query map
-// (used by the two-tile kernel for full tiles).
+                                const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 cudaError_t launch_prefill(int head_size, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, const CUtensorMap& to, const PrefillParams& p, int grid,
-                           cudaStream_t s);
+                           const CUtensorMap& tv, const PrefillParams& p, int grid, cudaStream_t s);
 
 }  // namespace pa
