@@ -31,7 +31,8 @@
 //   warpgroup 0 / 1: softmax of tile A / B (thread = row = TMEM lane);
 //   warpgroup 2: epilogue of both tiles: reads O from TMEM (releasing it to
 //     the next unit at once), divides by the row sums, stores the output;
-//   warpgroup 3: warp 12 TMA producer, warp 13 TMEM owner + MMA issuer.
+//   warpgroup 3: warp 12 K/V producer (TMA), warp 13 TMEM owner + MMA
+//     issuer, warp 14 work fetcher (device queue -> unit ring, Q loads).
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -40,7 +41,7 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 16 * 32;
-constexpr int kEpiWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
+constexpr int kEpiWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13, kFetchWarp = 14;
 // Registers per thread after the split (launch: 65536 / 512 = 128 each).
 constexpr int kRegSoftmax = 184, kRegEpilogue = 64, kRegControl = 80;
 static_assert(2 * kRegSoftmax + kRegEpilogue + kRegControl == 4 * 128, "register split");
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kInfoRing; ++i) {
       mbar_init(&ctl->info_full[i], 1);
-      mbar_init(&ctl->info_empty[i], 1 + 8 + 4);  // MMA warp, softmax and epilogue warps
+      mbar_init(&ctl->info_empty[i], 1 + 8 + 4 + 1);  // MMA, softmax, epilogue and K/V producer warps
     }
     for (int i = 0; i < S; ++i) {
       mbar_init(&ctl->full[i], 1);
@@ -266,75 +267,87 @@ __global__ void __launch_bounds__(kThreads, 1)
   // (the allocator budgets a branch from the setmaxnreg that dominates it).
   if (warp >= kProducerWarp) {
    regs_dec<kRegControl>();
-   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    // Publishes unit t+1 (and loads its Q as soon as its buffer is free)
-    // while it streams unit t's K/V tiles, so a unit never starts by waiting
-    // for the work queue or for its queries.
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-    }
+   if (warp == kFetchWarp) {
+    // ------------------------------------------------------------ fetcher
+    // Takes units from the device queue, publishes them in the unit ring
+    // (up to kInfoRing - 1 ahead of their use) and loads their Q tiles as
+    // soon as the previous unit's last S MMAs on it have completed.  Kept apart
+    // from the K/V producer: the queue atomic and the two dependent global
+    // loads per unit would otherwise stall the K/V stream.
+    if (lane == 0) prefetch_tmap(&tm_q);
     const uint32_t q_bytes = C::kChunks * p.G * tq * 128;
-    uint32_t n_loads = 0, q_loads = 0;  // K/V slot loads and Q loads issued so far
+    uint32_t q_loads = 0;  // Q tile loads issued so far (A, B, A, B, ...)
     bool ok = true;
-    // Every lane computes the same description of unit u.
-    auto fetch = [&](int u, UnitInfo& f) {
+    for (uint32_t tt = 0; ok; ++tt) {
+      int u = 0;
+      if (lane == 0) u = tt == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+      UnitInfo f;
       f.u = -1;
-      if (u >= n_work) return;
-      const int tile = u / p.Hk, k = u - tile * p.Hk;
-      const int2 bq = p.pre_tiles[tile];
-      const SeqInfo si = p.seq[bq.x];
-      const int q0 = bq.y * 2 * tq;
-      const int nt = min(2 * tq, si.q_len - q0);
-      const int ntA = min(tq, nt), ntB = nt - ntA;
-      const int pos0 = si.kv_len - si.q_len + q0;
-      const int lo_min = p.window >= 1 ? max(0, pos0 + 1 - p.window) : 0;
-      const int key_lo = lo_min & ~(kKeys - 1);
-      f.u = u;
-      f.k = k;
-      f.b = bq.x;
-      f.t0 = si.t0 + q0;
-      f.ntok[0] = ntA;
-      f.ntok[1] = ntB;
-      f.pos0 = pos0;
-      f.key_lo = key_lo;
-      f.n_kv[0] = (pos0 + ntA - key_lo + kKeys - 1) / kKeys;
-      f.n_kv[1] = ntB > 0 ? (pos0 + nt - key_lo + kKeys - 1) / kKeys : f.n_kv[0];
-      f.kv_len = si.kv_len;
-      f.lo_min = lo_min;
-    };
-    auto publish = [&](uint32_t t, const UnitInfo& f) -> bool {
-      const int slot = t % kInfoRing;
+      if (u < n_work) {
+        const int tile = u / p.Hk, k = u - tile * p.Hk;
+        const int2 bq = p.pre_tiles[tile];
+        const SeqInfo si = p.seq[bq.x];
+        const int q0 = bq.y * 2 * tq;
+        const int nt = min(2 * tq, si.q_len - q0);
+        const int ntA = min(tq, nt), ntB = nt - ntA;
+        const int pos0 = si.kv_len - si.q_len + q0;
+        const int lo_min = p.window >= 1 ? max(0, pos0 + 1 - p.window) : 0;
+        const int key_lo = lo_min & ~(kKeys - 1);
+        f.u = u;
+        f.k = k;
+        f.b = bq.x;
+        f.t0 = si.t0 + q0;
+        f.ntok[0] = ntA;
+        f.ntok[1] = ntB;
+        f.pos0 = pos0;
+        f.key_lo = key_lo;
+        f.n_kv[0] = (pos0 + ntA - key_lo + kKeys - 1) / kKeys;
+        f.n_kv[1] = ntB > 0 ? (pos0 + nt - key_lo + kKeys - 1) / kKeys : f.n_kv[0];
+        f.kv_len = si.kv_len;
+        f.lo_min = lo_min;
+      }
+      const int slot = tt % kInfoRing;
       if (lane == 0) {
-        if (!wait_or_abort(&ctl->info_empty[slot], ((t / kInfoRing) & 1) ^ 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt / kInfoRing) & 1) ^ 1, abort, p.err)) {
           ok = false;
         } else {
           ctl->info[slot] = f;
           mbar_arrive(&ctl->info_full[slot]);
         }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      return ok;
-    };
-    // Q tile X of unit t into its buffer once the last S of tile X of unit
-    // t-1 has completed.
-    auto load_q = [&](uint32_t t, int X, const UnitInfo& f) -> bool {
-      if (lane == 0) {
-        if (!wait_or_abort(&ctl->q_empty[X], (t & 1) ^ 1, abort, p.err)) {
-          ok = false;
-        } else {
-          mbar_arrive_expect_tx(&ctl->q_full[X], q_bytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(q_s + X * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, f.k * p.G,
-                        f.t0 + X * tq, &ctl->q_full[X]);
+        // Q tile X of unit tt into its buffer once unit tt-1's S_X MMAs are done
+        for (int X = 0; X < 2 && ok && f.u >= 0; ++X) {
+          if (!wait_or_abort(&ctl->q_empty[X], (tt & 1) ^ 1, abort, p.err)) {
+            ok = false;
+          } else {
+            mbar_arrive_expect_tx(&ctl->q_full[X], q_bytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_3d(q_s + X * C::kQTileBytes + c * (kPrefillRows * 128), &tm_q, c * 64, f.k * p.G,
+                          f.t0 + X * tq, &ctl->q_full[X]);
+            ++q_loads;
+          }
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      q_loads += ok ? 1 : 0;
-      return ok;
-    };
+      if (f.u < 0) break;
+    }
+    if (lane == 0 && *abort) {
+      // Gave up: let the copies already issued land before the CTA exits.
+      for (int d = 1; d <= 2 && (int)q_loads - d >= 0; ++d) {
+        const uint32_t n = q_loads - d;
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->q_full[n & 1], (n >> 1) & 1); ++i) {
+        }
+      }
+    }
+   } else if (warp == kProducerWarp) {
+    // ------------------------------------------------------- K/V producer
+    // Streams the K and V tiles of every published unit through the ring.
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+    }
+    uint32_t n_loads = 0;  // K/V slot loads issued so far
+    bool ok = true;
     // One K or V tile into the next ring slot: lane l copies page
     // l / chunks, 64-column chunk l % chunks (a box of {64, 1, page rows}).
     auto load_tile = [&](const CUtensorMap* tm, int k, int rc, bool is_v, uint32_t mask) -> bool {
@@ -358,18 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++n_loads;
       return true;
     };
-    // Per unit: K0, Q_A, V0, Q_B, then the other K/V tiles.  The Q waits
-    // depend only on the previous unit's S MMAs, whose K tiles are already
-    // issued.
-    UnitInfo cur, nxt;
-    fetch(blockIdx.x, cur);  // first unit: this CTA's own index, then the shared queue
-    publish(0, cur);
-    for (uint32_t tt = 0; ok && cur.u >= 0; ++tt) {
-      int u2 = 0;
-      if (lane == 0) u2 = (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
-      fetch(__shfl_sync(0xffffffffu, u2, 0), nxt);
-      if (!publish(tt + 1, nxt)) break;
-
+    for (uint32_t tt = 0; ok; ++tt) {
+      const int slot = tt % kInfoRing;
+      int got = 1;
+      if (lane == 0) got = wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, got, 0)) break;
+      const UnitInfo cur = ctl->info[slot];
+      if (cur.u < 0) break;
       const int hi_end = cur.pos0 + cur.ntok[0] + cur.ntok[1];
       const int* bt_row = p.block_table + (size_t)cur.b * p.MB;
       auto load_id = [&](int r) -> int {
@@ -392,20 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
-        if (!load_tile(&tm_k, cur.k, rc, false, 0) || (i == 0 && !load_q(tt, 0, cur)) ||
-            !load_tile(&tm_v, cur.k, rc, true, mask) || (i == 0 && !load_q(tt, 1, cur)))
-          break;
+        if (!load_tile(&tm_k, cur.k, rc, false, 0) || !load_tile(&tm_v, cur.k, rc, true, mask)) break;
       }
       if (!ok) break;
-      cur = nxt;
+      if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
     }
     if (lane == 0 && *abort) {
       // Gave up: let the copies already issued land before the CTA exits.
-      for (int d = 1; d <= 2 && (int)q_loads - d >= 0; ++d) {
-        const uint32_t n = q_loads - d;  // Q loads alternate A, B
-        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->q_full[n & 1], (n >> 1) & 1); ++i) {
-        }
-      }
       for (int d = 1; d <= S && (int)n_loads - d >= 0; ++d) {
         const uint32_t n = n_loads - d;
         for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->full[n % S], (n / S) & 1); ++i) {
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t n = 2 * (g + i);
         const int st = n % S;
         if (i == 0 && !wait_bar(&ctl->q_full[X], tt & 1)) return false;
-        if (!wait_bar(&ctl->full[st], (n / S) & 1)) return false;
+        // tile A's S(i) already waited for K_i (this thread, same phase)
+        if ((X == 0 || i >= nA) && !wait_bar(&ctl->full[st], (n / S) & 1)) return false;
         tc_fence_after();
         const uint64_t a0 = desc_k + ((q_addr + X * C::kQTileBytes) >> 4);
         const uint64_t b0 = desc_k + ((kv_addr + st * C::kSlotBytes) >> 4);
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i == 0 && tt > 0 && !wait_bar(&ctl->o_free[X], (tt - 1) & 1)) return false;
         const uint32_t n = 2 * (g + i) + 1;
         const int st = n % S;
-        if (!wait_bar(&ctl->full[st], (n / S) & 1)) return false;
+        if ((X == 0 || i >= nA) && !wait_bar(&ctl->full[st], (n / S) & 1)) return false;
         tc_fence_after();
         const uint64_t b0 = desc_v + ((kv_addr + st * C::kSlotBytes) >> 4);
 #pragma unroll

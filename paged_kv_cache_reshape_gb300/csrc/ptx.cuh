@@ -189,6 +189,13 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Copies a 128-row x 256-bit block (16 fp16 per row) from shared memory,
+// described like an MMA operand, into TMEM lanes 0-127, 8 columns from
+// `taddr`: the layout an A operand read from TMEM expects.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrives (once) on `bar` when every tcgen05.mma issued so far by this
 // thread has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
