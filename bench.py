@@ -356,11 +356,15 @@ def run_ours(args, rank, world, local_rank):
     if ker_ms[pa.PA_STAGE_PREFILL] and work["pre_flops"]:
         t = statistics.mean(ker_ms[pa.PA_STAGE_PREFILL])
         ach = work["pre_flops"] / (t * 1e-3) / 1e12
+        # head_size 64/128 run the two-tile kernel, 256 the one-tile kernel
+        pair = shape.head_size <= 128
         rooflines["prefill"] = {
-            "bound": "tensor", "kernel": f"prefill_kernel<{shape.head_size}>", "achieved": ach, "peak": tflops,
+            "bound": "tensor",
+            "kernel": f"prefill_pair_kernel<{shape.head_size}>" if pair else f"prefill_kernel<{shape.head_size}>",
+            "achieved": ach, "peak": tflops,
             "peak_kind": f"{peak_kind} bf16 matmul burst; fp16 has the same nominal dense rate",
             "unit": "TFLOP/s", "frac": ach / tflops,
-            "traffic": committed_traffic("prefill.cu", shape.name),
+            "traffic": committed_traffic("prefill_pair.cu" if pair else "prefill.cu", shape.name),
             "algorithmic_flops_per_launch": work["pre_flops"], "launch_ms": t}
     dominant = max(rooflines, key=lambda k: rooflines[k]["launch_ms"]) if rooflines else None
 
