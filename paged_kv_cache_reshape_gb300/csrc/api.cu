@@ -84,7 +84,7 @@ struct pa_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   __half* q_rot = nullptr;
-  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0, opt_items_per_cta = 4;
+  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0, opt_items_per_cta = pa::kDecodeItemsPerCta;
   cudaEvent_t ev[PA_NUM_STAGES][2] = {};
   bool stage_ran[PA_NUM_STAGES] = {};
   cudaStream_t last_stream = nullptr;
@@ -771,7 +771,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   const int max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
   const int max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
   const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
-  const int target_pairs = std::max(1, (4 * dec_grid + Hk - 1) / Hk);
+  const int target_pairs = std::max(1, (pa::kDecodeItemsPerCta * dec_grid + Hk - 1) / Hk);
   const int cap_dec = target_pairs + c.max_batch;
   const int tile_tokens = pa::prefill_unit_tokens(D, G);
   const int q_tokens = std::max(1, pa::kPrefillRows / G);

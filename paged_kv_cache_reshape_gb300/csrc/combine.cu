@@ -18,6 +18,23 @@ namespace {
 
 constexpr int kWarps = 8;
 
+// Adds f * (8 or 4 or kPer floats at po) into acc.
+template <int kPer>
+__device__ __forceinline__ void axpy(float* acc, float f, const float* po) {
+  if constexpr (kPer == 8) {
+    const float4 a = *reinterpret_cast<const float4*>(po);
+    const float4 b = *reinterpret_cast<const float4*>(po + 4);
+    acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+    acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
+  } else if constexpr (kPer == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(po);
+    acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] += f * po[i];
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
   constexpr int kPer = D / 32;  // channels per lane
@@ -32,37 +49,49 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     const int k = h / p.G, g = h - k * p.G;
     const int r = j * p.G + g;
     const int ns = si.dec_count;
-    // global max over splits
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) {
-      const size_t row = ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r;
-      M = fmaxf(M, p.part_ml[row].x);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    auto row_of = [&](int s) -> size_t { return ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r; };
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
     float den = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < ns; ++s) {
-        const size_t row = ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r;
-        const float2 ml = p.part_ml[row];
-        if (ml.y == 0.f) continue;  // empty split
-        const float f = exp2f(ml.x - M);
-        den += f * ml.y;
-        const float* po = p.part_o + row * D + lane * kPer;
-        if constexpr (kPer == 8) {
-          const float4 a = *reinterpret_cast<const float4*>(po);
-          const float4 b = *reinterpret_cast<const float4*>(po + 4);
-          acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
-          acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
-        } else if constexpr (kPer == 4) {
-          const float4 a = *reinterpret_cast<const float4*>(po);
-          acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
-        } else {
+    if (ns <= 32) {
+      // Lane s holds split s's (m, l); the weights reach every lane by
+      // shuffle and the partial rows are loaded four splits at a time.
+      const float2 ml = lane < ns ? p.part_ml[row_of(lane)] : make_float2(-INFINITY, 0.f);
+      float M = ml.x;
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) acc[i] += f * po[i];
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f_own = (M != -INFINITY && ml.y != 0.f) ? exp2f(ml.x - M) : 0.f;  // 0 for empty splits
+      float dl = f_own * ml.y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+      den = dl;
+      for (int s0 = 0; s0 < ns; s0 += 4) {
+        float f[4];
+        const float* po[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int s = min(s0 + q, ns - 1);
+          f[q] = __shfl_sync(0xffffffffu, f_own, s);
+          if (s0 + q >= ns) f[q] = 0.f;
+          po[q] = p.part_o + row_of(s) * D + lane * kPer;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (f[q] != 0.f) axpy<kPer>(acc, f[q], po[q]);
+      }
+    } else {
+      float M = -INFINITY;
+      for (int s = lane; s < ns; s += 32) M = fmaxf(M, p.part_ml[row_of(s)].x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      if (M != -INFINITY) {
+        for (int s = 0; s < ns; ++s) {
+          const float2 ml = p.part_ml[row_of(s)];
+          if (ml.y == 0.f) continue;  // empty split
+          const float f = exp2f(ml.x - M);
+          den += f * ml.y;
+          axpy<kPer>(acc, f, p.part_o + row_of(s) * D + lane * kPer);
         }
       }
     }

@@ -16,6 +16,10 @@ namespace pa {
 constexpr int kStageKeys = 64;      // keys per decode pipeline stage
 constexpr int kDecodeRows = 16;     // query rows (token x group head) per decode item
 constexpr int kDecodeWarps = 4;     // consumer warps of the decode kernel
+// Decode work items per decode CTA the automatic split size aims for: 2
+// measured best on the Llama-3-8B- and Llama-70B-shaped decode steps (fewer
+// split sequences to merge, the dynamic queue still balances the tail).
+constexpr int kDecodeItemsPerCta = 2;
 constexpr int kPrefillRows = 128;   // query rows per prefill tile (UMMA M)
 constexpr int kPrefillKeys = 128;   // keys per prefill KV tile (UMMA N of S)
 
