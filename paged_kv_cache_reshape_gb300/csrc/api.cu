@@ -18,6 +18,17 @@
 
 namespace {
 
+// Rates of the SM split's cost model (choose_split in worklist.cuh),
+// measured on the mixed 16 x 1024 + 240-decode step: the two-tile prefill
+// kernel's rate (772 TFLOP/s on 152 SMs), the decode kernel's bytes per SM
+// when it runs on part of the SMs (51-66 GB/s for 56-112 SMs; the per-SM TMA
+// inbound ceiling is about 74 GB/s), and the copy bandwidth.  A forced sweep
+// of the prefill SMs on that step: 32 -> 894 us, 40 -> 815, 48 -> 829,
+// 64 -> 884; without the split 842 us.
+constexpr float kPrefillFlopsPerSmUs = 5.0e6f;
+constexpr float kDecodeBytesPerSmUs = 55.0e3f;
+constexpr float kHbmBytesPerUs = 6.7e6f;
+
 thread_local std::string g_last_msg = "no error";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -570,9 +581,23 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
       !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows))
     return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
 
+  // The prefill kernel launches unless the query-length bound already routes
+  // every sequence to the decode kernel.  When it does, it goes first and
+  // the decode kernel runs beside it on the SMs the work list leaves it.
+  const bool pre_launch = h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows;
+
   // 1+2. prologue: device work list, rotary and the paged cache write
   {
     pa::WorklistParams p{};
+    p.split_sms = (pre_launch && !h->opt_timing) ? h->num_sms : 0;  // timed kernels run alone
+    p.pre_grid = h->pre_grid;
+    p.dec_grid = h->dec_grid;
+    p.dec_ctas_per_sm = h->dec_ctas_per_sm;
+    p.dec_bytes_per_key = (float)c.kv_num_heads * D * 4;
+    p.pre_flops_per_pair = 4.f * D * c.num_heads;
+    p.pre_rate_sm = kPrefillFlopsPerSmUs;
+    p.dec_rate_sm = kDecodeBytesPerSmUs;
+    p.hbm_rate = kHbmBytesPerUs;
     p.cum = cum;
     p.past = past;
     p.batch = batch;
@@ -603,41 +628,9 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     h->last_launches++;
   }
   const __half* q_att = c.do_rotary ? h->q_rot : static_cast<const __half*>(query);
-  // 3. split-KV decode
-  {
-    const int qt = h->G <= pa::kDecodeRows ? pa::kDecodeRows / h->G : 1;
-    CUtensorMap tq;
-    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, qt))
-      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
-    pa::DecodeParams p{};
-    p.q_tile_tokens = qt;
-    p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
-    p.out = static_cast<__half*>(output);
-    p.block_table = block_table;
-    p.seq = h->seq;
-    p.dec_items = h->dec_items;
-    p.counters = h->counters;
-    p.part_o = h->part_o;
-    p.part_ml = h->part_ml;
-    p.err = h->err;
-    p.H = c.num_heads;
-    p.Hk = c.kv_num_heads;
-    p.G = h->G;
-    p.bs = c.block_size;
-    p.MB = c.max_blocks_per_seq;
-    p.NB = c.num_blocks;
-    p.scale = h->scale;
-    p.softcap = c.softcap;
-    p.window = c.local_window_size;
-    p.oob_row = pool_rows;
-    StageTimer t(h, PA_STAGE_DECODE, s);
-    cudaError_t e = pa::launch_decode(D, tk, tv, tq, p, h->dec_grid, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
-    h->last_launches++;
-  }
-  // 4. varlen prefill on tensor memory (skipped when the query-length bound
+  // 3. varlen prefill on tensor memory (skipped when the query-length bound
   // already routes every sequence to the decode kernel)
-  if (h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows) {
+  if (pre_launch) {
     CUtensorMap tq, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, h->prefill_q_tokens) ||
@@ -668,6 +661,39 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     if (e != cudaSuccess) return cuda_fail(h, e, "prefill launch");
     h->last_launches++;
   }
+  // 4. split-KV decode (beside the prefill when both run)
+  {
+    const int qt = h->G <= pa::kDecodeRows ? pa::kDecodeRows / h->G : 1;
+    CUtensorMap tq;
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->G, qt))
+      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
+    pa::DecodeParams p{};
+    p.q_tile_tokens = qt;
+    p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
+    p.out = static_cast<__half*>(output);
+    p.block_table = block_table;
+    p.seq = h->seq;
+    p.dec_items = h->dec_items;
+    p.counters = h->counters;
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.err = h->err;
+    p.H = c.num_heads;
+    p.Hk = c.kv_num_heads;
+    p.G = h->G;
+    p.bs = c.block_size;
+    p.MB = c.max_blocks_per_seq;
+    p.NB = c.num_blocks;
+    p.scale = h->scale;
+    p.softcap = c.softcap;
+    p.window = c.local_window_size;
+    p.oob_row = pool_rows;
+    p.wait_prologue = pre_launch ? 0 : 1;
+    StageTimer t(h, PA_STAGE_DECODE, s);
+    cudaError_t e = pa::launch_decode(D, tk, tv, tq, p, h->dec_grid, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");
+    h->last_launches++;
+  }
   // 5. log-sum-exp combine of split partials
   {
     pa::CombineParams p{};
@@ -681,6 +707,9 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.Hk = c.kv_num_heads;
     p.G = h->G;
     p.D = D;
+    p.pre_exit = &h->counters->pre_exit;
+    p.pre_expected = pre_launch ? h->pre_grid : 0;
+    p.err = h->err;
     StageTimer t(h, PA_STAGE_COMBINE, s);
     cudaError_t e = pa::launch_combine(p, h->comb_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
@@ -839,6 +868,13 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.dec_items = dec_items;
   wp.pre_tiles = pre_tiles;
   wp.comb_rows = comb_rows;
+  // no SM split here: the decode kernel follows the prologue, the prefill
+  // kernel the decode kernel, each with every CTA working
+  const int pre_grid_na = std::max(1, std::min(nd->num_sms, cap_pre * Hk));
+  wp.split_sms = 0;
+  wp.pre_grid = pre_grid_na;
+  wp.dec_grid = dec_grid;
+  wp.dec_ctas_per_sm = std::max(1, dec_grid / nd->num_sms);
   wp.counters = counters;
   wp.err = err;
   pa::CacheWriteParams cp{};
@@ -897,6 +933,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   dp.softcap = c.softcap;
   dp.window = c.local_window_size;
   dp.oob_row = pool_rows;
+  dp.wait_prologue = 1;
   e = pa::launch_decode(D, tk, tv, tq, dp, dec_grid, s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "decode launch");
 
@@ -926,7 +963,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
     pp.softcap = c.softcap;
     pp.window = c.local_window_size;
     pp.oob_row = pool_rows;
-    e = pa::launch_prefill(D, tqp, tkp, tvp, pp, std::max(1, std::min(nd->num_sms, cap_pre * Hk)), s);
+    e = pa::launch_prefill(D, tqp, tkp, tvp, pp, pre_grid_na, s);
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "prefill launch");
   }
 
@@ -941,6 +978,9 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   mp.Hk = Hk;
   mp.G = G;
   mp.D = D;
+  mp.pre_exit = &counters->pre_exit;
+  mp.pre_expected = 0;  // the prefill kernel is this kernel's predecessor
+  mp.err = err;
   e = pa::launch_combine(mp, std::max(1, std::min(nd->num_sms * 4, (cap_comb * H + 7) / 8)), s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "combine launch");
   return PA_OK;

@@ -12,6 +12,7 @@
 // of sequences that were split, so the grid is a small persistent one.
 #include "ptx.cuh"
 #include "step.h"
+#include "../../include/pa.h"
 
 namespace pa {
 namespace {
@@ -40,6 +41,15 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
   constexpr int kPer = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31;
   griddep_wait();  // partials and the work list come from the kernels before
+  // The prefill kernel may still run beside the decode kernel: the step
+  // ends only after every prefill CTA has (CTA 0 waits, bounded).
+  if (p.pre_expected > 0 && blockIdx.x == 0 && threadIdx.x == 0) {
+    const volatile int* done = p.pre_exit;
+    uint32_t i = 0;
+    for (; i < kWaitLimit && *done < p.pre_expected; ++i) __nanosleep(64);
+    if (i == kWaitLimit) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+    __threadfence();
+  }
   const int n = p.counters->n_comb * p.H;
   for (int idx = blockIdx.x * kWarps + (threadIdx.x >> 5); idx < n; idx += gridDim.x * kWarps) {
     const int ci = idx / p.H, h = idx - ci * p.H;

@@ -102,8 +102,12 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
   uint64_t* q_empty = q_full + 2;
 
   // Everything below reads the prologue's work list and the pool it wrote.
-  griddep_wait();
-  if ((int)blockIdx.x >= p.counters->n_dec * p.Hk) return;  // no item for this CTA
+  // Launched right after the prologue it waits for it; launched after the
+  // prefill kernel (which waited for the prologue before letting this kernel
+  // start) it runs beside the prefill on the SMs the prefill left free.
+  if (p.wait_prologue) griddep_wait();
+  const int active = min(p.counters->dec_ctas, p.counters->n_dec * p.Hk);
+  if ((int)blockIdx.x >= active) return;  // no item, or an SM kept for the prefill
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
     for (int it = 0; ok; ++it) {
       // First item: this CTA's own index; then the shared queue.
       int u = blockIdx.x;
-      if (it > 0 && lane == 0) u = gridDim.x + atomicAdd(&p.counters->dec_next, 1);
+      if (it > 0 && lane == 0) u = active + atomicAdd(&p.counters->dec_next, 1);
       u = __shfl_sync(0xffffffffu, u, 0);
       if (u >= n_work) {
         if (lane == 0) {

@@ -115,8 +115,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The work list and the pool come from the prologue.  Steps without
   // prefill work (and CTAs beyond the work) leave before touching TMEM.
   griddep_wait();
+  griddep_launch_dependents();  // the decode kernel may start on the SMs this grid leaves free
   const int n_work = p.counters->n_pre * p.Hk;
-  if ((int)blockIdx.x >= n_work) return;
+  // CTAs beyond the work or beyond the work list's SM split leave at once
+  // (counted, so the step's last kernel can wait for every prefill CTA).
+  const int active = min(n_work, p.counters->pre_ctas);
+  if ((int)blockIdx.x >= active) {
+    if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         // First tile: this CTA's own index; then the shared queue.
         if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
-        else u = tt == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(&p.counters->pre_next, 1);
+        else u = tt == 0 ? (int)blockIdx.x : active + atomicAdd(&p.counters->pre_next, 1);
       }
       u = __shfl_sync(0xffffffffu, u, 0);
       if (u == -2) break;
@@ -494,12 +501,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  __threadfence();  // this CTA's output rows are visible before it is counted done
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
 }
 
 template <int D, bool CAP>

@@ -53,7 +53,10 @@ struct Counters {
   int split_keys;  // keys per decode split this step
   int dec_next;    // decode work queue head (reset to 0 by the work-list kernel)
   int pre_next;    // prefill work queue head (reset to 0 by the work-list kernel)
-  int pad[2];
+  int pre_ctas;    // prefill CTAs that take work this step; the others exit at once
+  int dec_ctas;    // decode CTAs that take work this step
+  int pre_exit;    // prefill CTAs finished this step (the combine kernel waits for all)
+  int pad[3];
 };
 
 struct WorklistParams {
@@ -69,6 +72,18 @@ struct WorklistParams {
   int split_keys_fixed;    // > 0 forces keys per split
   int target_pairs;        // desired number of decode (b, split) items
   int cap_dec, cap_pre, cap_comb;
+  // SM split between the prefill and decode kernels.  With split_sms > 0
+  // the prefill kernel is launched first, one CTA per SM, and the work list
+  // decides how many of its CTAs keep working; the others exit, and the
+  // decode kernel, launched next, runs on the SMs they free, concurrently.
+  int split_sms;             // SMs to share (0: no split, every CTA works)
+  int pre_grid, dec_grid;    // launched CTAs of the two kernels
+  int dec_ctas_per_sm;
+  float dec_bytes_per_key;   // Hk * D * 4 (K and V, once per kv head)
+  float pre_flops_per_pair;  // 4 * D * H per (query token, admitted key)
+  float pre_rate_sm;         // prefill FLOP per us per SM
+  float dec_rate_sm;         // decode bytes per us per SM
+  float hbm_rate;            // bytes per us
   SeqInfo* seq;
   int2* dec_items;  // (b, split)
   int2* pre_tiles;  // (b, tile)
@@ -113,6 +128,10 @@ struct DecodeParams {
   int oob_row;       // a TMA row coordinate past the pool (zero fill)
   int q_tile_tokens; // tokens per query TMA box (16 / G)
   int log_box_rows;  // log2(min(block_size, 64)): pool rows per TMA box
+  int wait_prologue; // 1: the launch before is the prologue (griddepcontrol.wait
+                     // on it); 0: it is the prefill kernel, which has waited for
+                     // the prologue before letting this kernel start, and this
+                     // kernel must not wait for it to finish
 };
 
 struct CombineParams {
@@ -123,6 +142,9 @@ struct CombineParams {
   const Counters* counters;
   __half* out;
   int H, Hk, G, D;
+  int* pre_exit;     // counter of finished prefill CTAs
+  int pre_expected;  // prefill CTAs launched this step (0: none)
+  int* err;
 };
 
 struct PrefillParams {

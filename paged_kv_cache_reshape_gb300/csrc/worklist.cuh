@@ -121,6 +121,12 @@ __device__ Lens read_lens(const WorklistParams& p, int b, int* err_bits) {
   return L;
 }
 
+// (query token, admitted key) pairs of a prefill-routed sequence, for the
+// SM split's cost model (the window's cut is ignored: an estimate).
+__device__ long long prefill_pairs(const Lens& L) {
+  return L.route == kRoutePrefill ? (long long)L.q * (L.past + (L.q + 1) / 2) : 0;
+}
+
 __device__ int split_keys_for(const WorklistParams& p, long long total) {
   if (p.split_keys_fixed > 0) return p.split_keys_fixed;
   long long per = (total + p.target_pairs - 1) / max(p.target_pairs, 1);
@@ -128,7 +134,35 @@ __device__ int split_keys_for(const WorklistParams& p, long long total) {
   return (int)min(max(per, (long long)kStageKeys), (long long)(1 << 30));
 }
 
-__device__ void write_counters(const WorklistParams& p, bool overflow, Int3 tot, int split_keys, int* err_bits) {
+// SM split for a step with both decode and prefill work: the prefill CTAs
+// kept, P, minimise max(prefill time on P SMs, decode time on the rest),
+// with prefill time = FLOPs / (P * per-SM rate) and decode time = K/V bytes
+// / min(HBM rate, SMs * per-SM rate).  Without one of the two kinds of
+// work, or without a split, every launched CTA takes work.
+__device__ void choose_split(const WorklistParams& p, long long dec_keys, long long pre_pairs, Counters* c) {
+  c->pre_ctas = p.pre_grid;
+  c->dec_ctas = p.dec_grid;
+  c->pre_exit = 0;
+  if (p.split_sms < 2 || dec_keys <= 0 || pre_pairs <= 0) return;
+  const float F = (float)pre_pairs * p.pre_flops_per_pair;
+  const float B = (float)dec_keys * p.dec_bytes_per_key;
+  int best = 1;
+  float best_t = 3.0e38f;
+  for (int P = 1; P < p.split_sms; ++P) {
+    const float t_pre = F / ((float)P * p.pre_rate_sm);
+    const float t_dec = B / fminf(p.hbm_rate, (float)(p.split_sms - P) * p.dec_rate_sm);
+    const float t = fmaxf(t_pre, t_dec);
+    if (t < best_t) {
+      best_t = t;
+      best = P;
+    }
+  }
+  c->pre_ctas = min(best, p.pre_grid);
+  c->dec_ctas = max(1, min(p.dec_grid, (p.split_sms - c->pre_ctas) * p.dec_ctas_per_sm));
+}
+
+__device__ void write_counters(const WorklistParams& p, bool overflow, Int3 tot, int split_keys, long long dec_keys,
+                               long long pre_pairs, int* err_bits) {
   Counters c;
   if (overflow) *err_bits |= PA_DEVERR_KV_BOUND;
   c.n_dec = overflow ? 0 : tot.a + tot.d;
@@ -137,7 +171,8 @@ __device__ void write_counters(const WorklistParams& p, bool overflow, Int3 tot,
   c.split_keys = split_keys;
   c.dec_next = 0;
   c.pre_next = 0;
-  c.pad[0] = c.pad[1] = 0;
+  choose_split(p, dec_keys, pre_pairs, &c);
+  c.pad[0] = c.pad[1] = c.pad[2] = 0;
   *p.counters = c;
 }
 
@@ -149,7 +184,9 @@ __device__ void build_small(const WorklistParams& p) {
   Lens L{0, 0, 0, 0, kRouteNone};
   if (b < p.batch) L = read_lens(p, b, &err_bits);
   const long long span = (L.route == kRouteDecode) ? (long long)(L.past + L.q - L.lo) : 0;
-  const int split_keys = split_keys_for(p, block_sum_ll(span));
+  const long long dec_keys = block_sum_ll(span);
+  const long long pre_pairs = block_sum_ll(prefill_pairs(L));
+  const int split_keys = split_keys_for(p, dec_keys);
   Int3 cnt{0, 0, 0, 0};
   if (L.route == kRouteDecode) {
     const int n = (L.past + L.q - L.lo + split_keys - 1) / split_keys;
@@ -217,7 +254,7 @@ __device__ void build_small(const WorklistParams& p) {
   __syncthreads();
   if (!overflow)
     for (int s = 0; s < cnt.b; ++s) p.pre_tiles[atomicAdd(&hist[tile_bucket(s)], 1)] = make_int2(b, s);
-  if (threadIdx.x == 0) write_counters(p, overflow, tot, split_keys, &err_bits);
+  if (threadIdx.x == 0) write_counters(p, overflow, tot, split_keys, dec_keys, pre_pairs, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
 }
 
@@ -229,16 +266,19 @@ __device__ void build(const WorklistParams& p) {
   }
   int err_bits = 0;
   // Pass 1: total decode span, which sets the keys per split.
-  long long span = 0;
+  long long span = 0, pairs = 0;
   for (int base = 0; base < p.batch; base += kThreads) {
     int b = base + threadIdx.x;
     if (b < p.batch) {
       int dummy = 0;
       Lens L = read_lens(p, b, &dummy);
       if (L.route == kRouteDecode) span += (long long)(L.past + L.q - L.lo);
+      pairs += prefill_pairs(L);
     }
   }
-  const int split_keys = split_keys_for(p, block_sum_ll(span));
+  const long long dec_keys = block_sum_ll(span);
+  const long long pre_pairs = block_sum_ll(pairs);
+  const int split_keys = split_keys_for(p, dec_keys);
 
   // Pass 2: counts and scans; the items are written in pass 3 once the
   // number of full decode splits (which precede every last split) is known.
@@ -299,7 +339,7 @@ __device__ void build(const WorklistParams& p) {
       for (int s = 0; s < si.pre_count; ++s) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
     }
   }
-  if (threadIdx.x == 0) write_counters(p, overflow, carry, split_keys, &err_bits);
+  if (threadIdx.x == 0) write_counters(p, overflow, carry, split_keys, dec_keys, pre_pairs, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
 }
 
