@@ -19,12 +19,13 @@
 //     memory; MMAs issued by one thread complete in order, so S(i+1) may
 //     reuse the columns once PV(i) is issued, and a wait on S(i+1) also
 //     covers PV(i);
-//   * the softmax does two fp32 lanes per instruction (f32x2 FMA/ADD), a
-//     three-input max, and evaluates part of its exponentials with a
-//     polynomial on the FMA pipe so the MUFU unit is not the limit;
+//   * the softmax does two fp32 lanes per instruction (f32x2 FMA/ADD) and a
+//     three-input max; part of its exponentials can go to a polynomial on
+//     the FMA pipe instead of the MUFU unit (PA_PREFILL_POLY_OF_4; off by
+//     default, as every fraction measured slower);
 //   * TMEM: S_A, S_B (128 columns each), O_A, O_B (head_size each);
-//   * shared memory: Q double-buffered (both tiles), a ring of K and V tile
-//     slots loaded in the order they are used: K0 V0 K1 V1 ...
+//   * shared memory: one Q buffer per tile, a ring of K and V tile slots
+//     loaded in the order they are used: K0 V0 K1 V1 ...
 //
 // Roles (512 threads = 4 warpgroups, one CTA per SM, persistent over a
 // device queue; registers moved between warpgroups with setmaxnreg):
@@ -85,10 +86,18 @@ struct UnitInfo {
 };
 
 constexpr int kInfoRing = 4;  // units published ahead of their use
+// Page masks of the K/V tiles in flight, each published with an mbarrier
+// arrive before the tile's K load is issued.  The producer runs at most
+// kSlots / 2 + 1 tiles ahead of the softmax warpgroups (it reuses a slot only
+// after the MMAs that read it, which follow the softmax of older tiles), so
+// an entry is rewritten only after both warpgroups have read it and a
+// barrier never runs a full phase ahead of its reader.
+constexpr int kMaskRing = 8;
 
 struct Ctrl {
   UnitInfo info[kInfoRing];
-  uint32_t kv_mask[8];  // per V slot: the tile's pages that are unmapped
+  uint32_t kv_mask[kMaskRing];   // per K/V tile (tile number mod ring): its pages that are unmapped
+  uint64_t mask_full[kMaskRing];  // one arrive per publication
   uint64_t q_full[2], q_empty[2];  // per tile (A, B): its Q buffer
   uint64_t full[8], empty[8];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
@@ -254,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->full[i], 1);
       mbar_init(&ctl->empty[i], 1);
     }
+    for (int i = 0; i < kMaskRing; ++i) mbar_init(&ctl->mask_full[i], 1);
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
@@ -363,7 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_or_abort(&ctl->empty[slot], ((n_loads / S) & 1) ^ 1, abort, p.err)) {
           ok = false;
         } else {
-          if (is_v) ctl->kv_mask[slot] = mask;
+          if (!is_v) {
+            ctl->kv_mask[(n_loads >> 1) % kMaskRing] = mask;
+            mbar_arrive(&ctl->mask_full[(n_loads >> 1) % kMaskRing]);
+          }
           mbar_arrive_expect_tx(&ctl->full[slot], C::kSlotBytes);
         }
       }
@@ -407,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
-        if (!load_tile(&tm_k, cur.k, rc, false, 0) || !load_tile(&tm_v, cur.k, rc, true, mask)) break;
+        if (!load_tile(&tm_k, cur.k, rc, false, mask) || !load_tile(&tm_v, cur.k, rc, true, 0)) break;
       }
       if (!ok) break;
       if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
@@ -527,28 +540,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt % kInfoRing;
       if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err)) break;
-      const UnitInfo& ui = ctl->info[slot];  // read in place: registers are scarce here
+      const UnitInfo& ui = ctl->info[slot];
       if (ui.u < 0) break;
+      // The unit's fields, read once (shared-memory loads are slow while
+      // the tensor core streams operands)
       const int j = r / p.G;
       const bool row_ok = j < ui.ntok[X];
       const int hi = ui.pos0 + X * tq + j;                   // last admitted position
       const int lo = p.window >= 1 ? hi + 1 - p.window : 0;  // first admitted position
       const int n_x = ui.n_kv[X];
+      const int key_lo = ui.key_lo;
+      // Tiles whose never-admitted keys need zero V rows: tile A does it
+      // while it uses the tile, tile B for the tiles A skips.
+      const int vz_from = X == 0 ? 0 : ui.n_kv[0];
+      const int vz_kv_len = ui.kv_len, vz_lo_min = ui.lo_min;
       float m_ref = -INFINITY, l = 0.f;
       bool ok = true;
       for (int i = 0; i < n_x; ++i) {
-        const uint32_t nv = 2 * (g + i) + 1;
+        const uint32_t nv = 2 * (g + i) + 1, tile = g + i;
         const int sv = nv % S;
-        const int key0 = ui.key_lo + i * kKeys;
+        const int key0 = key_lo + i * kKeys;
         // s_full(i) also covers PV(i-1): MMAs complete in issue order.  The
-        // V slot carries the tile's page mask (and its rows may need zeros).
+        // page mask was published before the tile's K load.
         if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->full[sv], (nv / S) & 1, abort, p.err)) {
+            !wait_or_abort(&ctl->mask_full[tile % kMaskRing], (tile / kMaskRing) & 1, abort, p.err)) {
           ok = false;
           break;
         }
         ++scnt;
         tc_fence_after();
+        const uint32_t mask = ctl->kv_mask[tile % kMaskRing];
 #pragma unroll
         for (int c = 0; c < kKeys; c += 32) tmem_ld32(lane_addr + C::s_col(X) + c, x + c);
         tmem_ld_wait();
@@ -556,7 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kKeys; ++c) x[c] = cap_out * tanhf(x[c] * cap_in);
         }
-        const uint32_t mask = ctl->kv_mask[sv];
         const int c_lo = row_ok ? max(lo - key0, 0) : kKeys;
         const int c_hi = row_ok ? min(hi - key0, kKeys - 1) : -1;
         if (c_lo > 0 || c_hi < kKeys - 1) {
@@ -597,10 +617,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P_X -> TMEM over S_X: keys h..h+31 as 16 columns of fp16 pairs
           tmem_st16(lane_addr + C::s_col(X) + h / 2, pk);
         }
-        float s0, s1, s2, s3;
-        unf2(add2(sum2[0], sum2[1]), s0, s1);
-        unf2(add2(sum2[2], sum2[3]), s2, s3);
-        l = l * alpha + ((s0 + s1) + (s2 + s3));
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           float o[32];
 #pragma unroll 1
@@ -612,14 +628,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(lane_addr + C::o_col(X) + 32 * c, o);
           }
         }
-        // Never-admitted keys of an edge tile: zero their V rows (tile A does
-        // it while it uses the tile, tile B for the tiles A skips).
-        if ((X == 0 || i >= ui.n_kv[0]) && (key0 + kKeys > ui.kv_len || key0 < ui.lo_min)) {
+        if (i >= vz_from && (key0 + kKeys > vz_kv_len || key0 < vz_lo_min)) {
           uint8_t* vs = kv_s + sv * C::kSlotBytes;
+          if (!wait_or_abort(&ctl->full[sv], (nv / S) & 1, abort, p.err)) {
+            ok = false;
+            break;
+          }
           for (int idx = r; idx < kKeys * C::kChunks * 8; idx += 128) {
             const int kr = idx / (C::kChunks * 8), rem = idx % (C::kChunks * 8);
             const int pos = key0 + kr;
-            if (pos >= ui.kv_len || pos < ui.lo_min) {
+            if (pos >= vz_kv_len || pos < vz_lo_min) {
               const int c = rem >> 3, col16 = rem & 7;
               *reinterpret_cast<uint4*>(vs + c * (kKeys * 128) + kr * 128 + ((col16 ^ (kr & 7)) << 4)) =
                   make_uint4(0, 0, 0, 0);
@@ -631,6 +649,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->p_full[X]);
+        // the row sum is off the path to the PV MMA
+        float s0, s1, s2, s3;
+        unf2(add2(sum2[0], sum2[1]), s0, s1);
+        unf2(add2(sum2[2], sum2[3]), s2, s3);
+        l = l * alpha + ((s0 + s1) + (s2 + s3));
       }
       if (!ok) break;
       // The row sum goes to the epilogue warpgroup (its previous value has
@@ -718,6 +741,7 @@ cudaError_t configure_dc() {
   static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
   static_assert(PairCfg<D>::kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(PairCfg<D>::kSlots >= 3, "K/V ring");
+  static_assert(PairCfg<D>::kSlots / 2 + 2 <= kMaskRing, "page mask ring");
   static_assert(2 * kKeys + 2 * D <= PairCfg<D>::kTmemCols, "tensor memory");
   return cudaFuncSetAttribute(prefill_pair_kernel<D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PairCfg<D>::kSmemBytes);
