@@ -26,6 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, BAD_ARGUMENT, BAD_DEVICE_DATA = 0, 1, 2
+CACHE_FP16, CACHE_INT8, CACHE_FP8 = 0, 1, 2
 
 
 def build(force: bool = False) -> str:
@@ -57,6 +58,17 @@ def lib():
             L.oracle_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                            Dd, Dd, I, LL, LL, P]
             L.oracle_attention.restype = I
+            L.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            L.oracle_e4m3_to_double.restype = Dd
+            L.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+            L.oracle_float_to_e4m3.restype = ctypes.c_uint8
+            L.oracle_quantize.argtypes = [ctypes.c_uint16, ctypes.c_float, I]
+            L.oracle_quantize.restype = ctypes.c_uint8
+            L.oracle_cache_write_quant.argtypes = [P, P, P, P, P, P, I, I, P, I, P, P, I, I, I, I, I, I]
+            L.oracle_cache_write_quant.restype = I
+            L.oracle_attention_ex.argtypes = [P, P, P, I, P, P, I, P, P, I, P, P, I, I, I, I, I, I, I,
+                                              Dd, Dd, I, LL, LL, P]
+            L.oracle_attention_ex.restype = I
             _lib = L
     return _lib
 
@@ -94,6 +106,23 @@ def double_to_half_bits(x: np.ndarray) -> np.ndarray:
     return f(np.asarray(x, dtype=np.float64))
 
 
+def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lambda c: lib().oracle_e4m3_to_double(int(c)), otypes=[np.float64])
+    return f(np.asarray(codes, dtype=np.uint8))
+
+
+def float_to_e4m3(x: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lambda v: lib().oracle_float_to_e4m3(float(v)), otypes=[np.uint8])
+    return f(np.asarray(x, dtype=np.float32))
+
+
+def quantize(bits: np.ndarray, scale: float, cache_dtype: int) -> np.ndarray:
+    """8-bit codes of fp16 values (bit patterns) under one scale."""
+    f = np.vectorize(lambda h: lib().oracle_quantize(int(h), float(scale), int(cache_dtype)),
+                     otypes=[np.uint8])
+    return f(np.asarray(bits, dtype=np.uint16))
+
+
 def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
     """Rotated copy of x ([T, nheads*D] fp16 bits) at positions past_b + j."""
     xa = _np(x, np.uint16)
@@ -109,11 +138,28 @@ def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
 
 
 def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
-                kv_num_heads, head_size, block_size):
+                kv_num_heads, head_size, block_size, cache_dtype=CACHE_FP16,
+                k_scale=None, v_scale=None, per_channel=False):
     """Returns (key_cache', value_cache') after writing the new tokens' rows.
 
     key/value are fp16 bit arrays [T, Hk*D] (key already rotated when rotary
-    is on); the input caches are copied, not modified."""
+    is on); the input caches are copied, not modified.  With an 8-bit
+    cache_dtype the caches are uint8 code arrays and k_scale / v_scale fp32
+    arrays ([1], or [Hk*D] when per_channel)."""
+    if cache_dtype != CACHE_FP16:
+        ka, va = _np(key, np.uint16), _np(value, np.uint16)
+        kc = _np(key_cache, np.uint8).copy()
+        vc = _np(value_cache, np.uint8).copy()
+        ks, vs = _np(k_scale, np.float32), _np(v_scale, np.float32)
+        bt = _np(block_table, np.int32)
+        cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
+        st = lib().oracle_cache_write_quant(_p(ka), _p(va), _p(kc), _p(vc), _p(ks), _p(vs),
+                                            int(bool(per_channel)), int(cache_dtype), _p(bt),
+                                            bt.shape[1], _p(cum_a), _p(past_a), past_a.shape[0],
+                                            ka.shape[0], kv_num_heads, head_size, block_size,
+                                            kc.shape[0])
+        _check(st, "cache_write_quant")
+        return kc, vc
     ka, va = _np(key, np.uint16), _np(value, np.uint16)
     kc = _np(key_cache, np.uint16).copy()
     vc = _np(value_cache, np.uint16).copy()
@@ -128,15 +174,22 @@ def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
 
 def attention(query, key_cache, value_cache, block_table, cum, past, num_heads,
               kv_num_heads, head_size, block_size, scale, softcap, window,
-              rows=None, threads=None):
+              rows=None, threads=None, cache_dtype=CACHE_FP16, k_scale=None,
+              v_scale=None, per_channel=False, head_sink=None):
     """fp64 attention output.
 
     rows=None computes every (t, h) row and returns [T, H, D]; otherwise
     `rows` is an int array of r = t*H + h and the result is [len(rows), D].
     Row ranges run on `threads` Python threads (the C call releases the GIL).
+    8-bit caches are code arrays dequantized with k_scale / v_scale;
+    head_sink ([H] fp16) adds the sink term to every row's denominator.
     """
     qa = _np(query, np.uint16)
-    kc, vc = _np(key_cache, np.uint16), _np(value_cache, np.uint16)
+    cdt = np.uint16 if cache_dtype == CACHE_FP16 else np.uint8
+    kc, vc = _np(key_cache, cdt), _np(value_cache, cdt)
+    ks = _np(k_scale, np.float32) if k_scale is not None else None
+    vs = _np(v_scale, np.float32) if v_scale is not None else None
+    sk = _np(head_sink, np.uint16) if head_sink is not None else None
     bt = _np(block_table, np.int32)
     cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
     T, H, D = qa.shape[0], num_heads, head_size
@@ -144,9 +197,10 @@ def attention(query, key_cache, value_cache, block_table, cum, past, num_heads,
     L = lib()
 
     def run(r0, r1, out):
-        st = L.oracle_attention(_p(qa), _p(kc), _p(vc), _p(bt), MB, _p(cum_a), _p(past_a),
-                                B, T, H, kv_num_heads, D, block_size, NB, float(scale),
-                                float(softcap), int(window), r0, r1, _p(out))
+        st = L.oracle_attention_ex(_p(qa), _p(kc), _p(vc), int(cache_dtype), _p(ks), _p(vs),
+                                   int(bool(per_channel)), _p(sk), _p(bt), MB, _p(cum_a),
+                                   _p(past_a), B, T, H, kv_num_heads, D, block_size, NB,
+                                   float(scale), float(softcap), int(window), r0, r1, _p(out))
         _check(st, "attention")
 
     threads = threads or 1
@@ -192,9 +246,13 @@ def forward(step, threads=None, rows=None):
                    step["rotary_interleaved"])
         k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
                    step["rotary_interleaved"])
+    cdt = step.get("cache_dtype", CACHE_FP16)
+    quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
+                 per_channel=step.get("per_channel", False))
     kc, vc = cache_write(k, step["value"], step["key_cache"], step["value_cache"],
-                         step["block_table"], cum, past, Hk, D, step["block_size"])
+                         step["block_table"], cum, past, Hk, D, step["block_size"], **quant)
     out = attention(q, kc, vc, step["block_table"], cum, past, H, Hk, D,
                     step["block_size"], step["scale"], step["softcap"],
-                    step["local_window_size"], rows=rows, threads=threads)
+                    step["local_window_size"], rows=rows, threads=threads,
+                    head_sink=step.get("head_sink"), **quant)
     return dict(query_rot=q, key_rot=k, key_cache=kc, value_cache=vc, out=out)

@@ -21,7 +21,19 @@
  *     (q_len_b = cum[b+1] - cum[b]) and section 4.1 (GQA head grouping by
  *     n_reps = num_heads / kv_num_heads);
  *   - onnxruntime issue 29714 (cuDNN SDPA decode tier), section 4.3 item 7:
- *     a row with no admitted key outputs 0, not NaN.
+ *     a row with no admitted key outputs 0, not NaN;
+ *   - "PagedAttention - CUDA Design Document" section 8 (quantized cache:
+ *     int8 or float8 e4m3fn codes, symmetric, dequantized as code * scale,
+ *     PER_TENSOR scale [1] or PER_CHANNEL scale [kv_num_heads * head_size],
+ *     K and V quantized as they are written) and section 6.1 (head_sink: one
+ *     extra logit s_h per query head that enters the softmax denominator only,
+ *     m = max(s_h, max_j x_j)).
+ *
+ * Quantize-on-write reading.  The pages fix dequantization (x = q * scale,
+ * zero point 0) but not the rounding of the write.  This oracle takes the
+ * plainest one: y = x / scale in fp32 (IEEE division), then int8 = y rounded
+ * to nearest-even and saturated to [-128, 127], e4m3fn = y rounded to
+ * nearest-even and saturated to the largest finite value (+-448).
  *
  * Precision.  Attention is evaluated in fp64 from exactly converted fp16
  * inputs: scores, max, exponentials, the weighted sum and the normaliser are
@@ -39,6 +51,7 @@
  * cum [B+1]; past [B]; cos/sin [P, R/2].
  */
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -87,6 +100,75 @@ uint16_t oracle_double_to_half(double x) {
   }
   if (ee > 15) return sign | 0x7c00;
   return sign | (uint16_t)((ee + 15) << 10) | (uint16_t)((int)m - 1024);
+}
+
+/* ---- float8 e4m3fn, written from the format definition ---- */
+
+/* Exact e4m3fn -> double.  1 sign bit, 4 exponent bits (bias 7), 3 fraction
+ * bits; exponent 0 is subnormal (fraction * 2^-9); there is no infinity and
+ * the one NaN pattern per sign is exponent 15 with fraction 7. */
+double oracle_e4m3_to_double(uint8_t c) {
+  int sign = (c >> 7) & 1;
+  int e = (c >> 3) & 0xf;
+  int f = c & 7;
+  double v;
+  if (e == 15 && f == 7) {
+    v = NAN;
+  } else if (e == 0) {
+    v = ldexp((double)f, -9);
+  } else {
+    v = ldexp((double)(8 + f), e - 10);
+  }
+  return sign ? -v : v;
+}
+
+/* fp32 -> e4m3fn, round to nearest, ties to even; finite values beyond the
+ * largest finite magnitude (448) and infinities saturate to +-448; NaN maps
+ * to the NaN pattern. */
+uint8_t oracle_float_to_e4m3(float x) {
+  if (isnan(x)) return 0x7f;
+  uint8_t sign = signbit(x) ? 0x80 : 0;
+  double a = fabs((double)x);
+  if (a >= 448.0) return sign | 0x7e;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal quantum is 2^-9; scaling by 2^9 is exact */
+    double m = nearbyint(ldexp(a, 9));
+    return sign | (uint8_t)m; /* m == 8 encodes the smallest normal */
+  }
+  int e;
+  (void)frexp(a, &e); /* a = f * 2^e with f in [0.5, 1) */
+  double m = nearbyint(ldexp(a, 4 - e)); /* significand in [8, 16] */
+  int ee = e - 1;
+  if (m == 16.0) {
+    m = 8.0;
+    ee += 1;
+  }
+  if (ee > 8 || (ee == 8 && m > 14.0)) return sign | 0x7e;
+  return sign | (uint8_t)((ee + 7) << 3) | (uint8_t)((int)m - 8);
+}
+
+/* Cache element types: fp16 (no quantization), int8, float8 e4m3fn. */
+#define ORACLE_CACHE_FP16 0
+#define ORACLE_CACHE_INT8 1
+#define ORACLE_CACHE_FP8 2
+
+/* Code of fp16 value h under scale s (reading stated in the header). */
+uint8_t oracle_quantize(uint16_t h, float s, int cache_dtype) {
+  float y = (float)oracle_half_to_double(h) / s;
+  if (cache_dtype == ORACLE_CACHE_FP8) return oracle_float_to_e4m3(y);
+  float r = nearbyintf(y);
+  if (r > 127.0f) r = 127.0f;
+  if (r < -128.0f) r = -128.0f;
+  return (uint8_t)(int8_t)r;
+}
+
+/* Value of cache element i of a row (fp16 bits or an 8-bit code), as a
+ * double: code * scale for the 8-bit types. */
+static double cache_value(const void* row, int i, int cache_dtype, double scale) {
+  if (cache_dtype == ORACLE_CACHE_FP16) return oracle_half_to_double(((const uint16_t*)row)[i]);
+  uint8_t c = ((const uint8_t*)row)[i];
+  if (cache_dtype == ORACLE_CACHE_INT8) return (double)(int8_t)c * scale;
+  return oracle_e4m3_to_double(c) * scale;
 }
 
 /* ---- sequence bookkeeping (WebGPU design section 3.3) ---- */
@@ -187,6 +269,39 @@ int oracle_cache_write(const uint16_t* key, const uint16_t* value,
   return ORACLE_OK;
 }
 
+/* Quantized write (CUDA design section 8.4): as oracle_cache_write, but
+ * every element is stored as its 8-bit code under the element's scale:
+ * per_channel = 0 -> scale[0]; per_channel = 1 -> scale[k * D + c]. */
+int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
+                             uint8_t* key_cache, uint8_t* value_cache,
+                             const float* k_scale, const float* v_scale,
+                             int per_channel, int cache_dtype,
+                             const int32_t* block_table, int MB,
+                             const int32_t* cum, const int32_t* past, int B, int T,
+                             int Hk, int D, int bs, int NB) {
+  int st = check_lengths(cum, past, B, T);
+  if (st) return st;
+  if (cache_dtype != ORACLE_CACHE_INT8 && cache_dtype != ORACLE_CACHE_FP8) return ORACLE_BAD_ARGUMENT;
+  size_t row = (size_t)Hk * D;
+  for (int b = 0; b < B; ++b) {
+    for (int t = cum[b]; t < cum[b + 1]; ++t) {
+      int pos = past[b] + (t - cum[b]);
+      int i = pos / bs;
+      if (i >= MB) return ORACLE_BAD_DEVICE_DATA;
+      int blk = block_table[(size_t)b * MB + i];
+      if (blk == -1) continue;
+      if (blk < -1 || blk >= NB) return ORACLE_BAD_DEVICE_DATA;
+      size_t slot = (size_t)blk * bs + pos % bs;
+      for (size_t e = 0; e < row; ++e) {
+        size_t si = per_channel ? e : 0; /* e = k * D + c */
+        key_cache[slot * row + e] = oracle_quantize(key[(size_t)t * row + e], k_scale[si], cache_dtype);
+        value_cache[slot * row + e] = oracle_quantize(value[(size_t)t * row + e], v_scale[si], cache_dtype);
+      }
+    }
+  }
+  return ORACLE_OK;
+}
+
 /* ---- attention (CUDA design section 8 note P5, section 9) ---- */
 
 /* Output rows r in [row_begin, row_end), r = t * H + h, each D doubles in
@@ -198,12 +313,18 @@ int oracle_cache_write(const uint16_t* key, const uint16_t* value,
  * optionally x_p = softcap * tanh(x_p / softcap); out = sum_p w_p V_p / sum_p w_p
  * with w_p = exp(x_p - max_p x_p); no admitted position gives out = 0.
  * scale == 0 selects 1/sqrt(D). */
-int oracle_attention(const uint16_t* query, const uint16_t* key_cache,
-                     const uint16_t* value_cache, const int32_t* block_table,
-                     int MB, const int32_t* cum, const int32_t* past, int B,
-                     int T, int H, int Hk, int D, int bs, int NB, double scale,
-                     double softcap, int window, long long row_begin,
-                     long long row_end, double* out) {
+/* General form.  key_cache / value_cache hold fp16 bits (cache_dtype 0)
+ * or 8-bit codes dequantized as code * scale with k_scale / v_scale indexed
+ * by [k * D + c] (per_channel = 1) or [0]; head_sink ([H] fp16, may be NULL)
+ * adds exp(s_h - m) to the denominator, m = max(s_h, max_p x_p). */
+int oracle_attention_ex(const uint16_t* query, const void* key_cache,
+                        const void* value_cache, int cache_dtype,
+                        const float* k_scale, const float* v_scale, int per_channel,
+                        const uint16_t* head_sink, const int32_t* block_table,
+                        int MB, const int32_t* cum, const int32_t* past, int B,
+                        int T, int H, int Hk, int D, int bs, int NB, double scale,
+                        double softcap, int window, long long row_begin,
+                        long long row_end, double* out) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
   if (Hk <= 0 || H % Hk != 0) return ORACLE_BAD_ARGUMENT;
@@ -212,6 +333,8 @@ int oracle_attention(const uint16_t* query, const uint16_t* key_cache,
   if (row_begin < 0 || row_end > (long long)T * H || row_begin > row_end)
     return ORACLE_BAD_ARGUMENT;
   if (scale == 0.0) scale = 1.0 / sqrt((double)D);
+  if (cache_dtype != ORACLE_CACHE_FP16 && (k_scale == NULL || v_scale == NULL)) return ORACLE_BAD_ARGUMENT;
+  size_t esize = cache_dtype == ORACLE_CACHE_FP16 ? 2 : 1;
   int G = H / Hk;
   double q[1024];
   if (D > 1024) return ORACLE_BAD_ARGUMENT;
@@ -236,32 +359,50 @@ int oracle_attention(const uint16_t* query, const uint16_t* key_cache,
       int blk = block_table[(size_t)b * MB + p / bs];
       if (blk == -1) continue;
       if (blk < -1 || blk >= NB) return ORACLE_BAD_DEVICE_DATA;
-      const uint16_t* kr = key_cache + (((size_t)blk * bs + p % bs) * Hk + k) * D;
+      const void* kr = (const uint8_t*)key_cache + (((size_t)blk * bs + p % bs) * Hk + k) * D * esize;
       double x = 0.0;
-      for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(kr[c]);
+      for (int c = 0; c < D; ++c)
+        x += q[c] * cache_value(kr, c, cache_dtype, k_scale ? k_scale[per_channel ? k * D + c : 0] : 1.0);
       x *= scale;
       if (softcap > 0.0) x = softcap * tanh(x / softcap);
       if (x > xmax) xmax = x;
       any = 1;
     }
     if (!any) continue; /* fully masked row: output stays 0 */
+    double sink = head_sink ? oracle_half_to_double(head_sink[h]) : -INFINITY;
+    if (sink > xmax) xmax = sink;
     /* pass 2: weights and the weighted sum of V */
     double denom = 0.0;
     for (int p = lo; p < kv_len; ++p) {
       int blk = block_table[(size_t)b * MB + p / bs];
       if (blk == -1) continue;
       size_t slot = (size_t)blk * bs + p % bs;
-      const uint16_t* kr = key_cache + (slot * Hk + k) * D;
-      const uint16_t* vr = value_cache + (slot * Hk + k) * D;
+      const void* kr = (const uint8_t*)key_cache + (slot * Hk + k) * D * esize;
+      const void* vr = (const uint8_t*)value_cache + (slot * Hk + k) * D * esize;
       double x = 0.0;
-      for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(kr[c]);
+      for (int c = 0; c < D; ++c)
+        x += q[c] * cache_value(kr, c, cache_dtype, k_scale ? k_scale[per_channel ? k * D + c : 0] : 1.0);
       x *= scale;
       if (softcap > 0.0) x = softcap * tanh(x / softcap);
       double w = exp(x - xmax);
       denom += w;
-      for (int c = 0; c < D; ++c) o[c] += w * oracle_half_to_double(vr[c]);
+      for (int c = 0; c < D; ++c)
+        o[c] += w * cache_value(vr, c, cache_dtype, v_scale ? v_scale[per_channel ? k * D + c : 0] : 1.0);
     }
+    if (head_sink) denom += exp(sink - xmax); /* the sink's term: denominator only */
     for (int c = 0; c < D; ++c) o[c] /= denom;
   }
   return ORACLE_OK;
+}
+
+/* fp16 cache, no sink. */
+int oracle_attention(const uint16_t* query, const uint16_t* key_cache,
+                     const uint16_t* value_cache, const int32_t* block_table,
+                     int MB, const int32_t* cum, const int32_t* past, int B,
+                     int T, int H, int Hk, int D, int bs, int NB, double scale,
+                     double softcap, int window, long long row_begin,
+                     long long row_end, double* out) {
+  return oracle_attention_ex(query, key_cache, value_cache, ORACLE_CACHE_FP16, NULL, NULL, 0, NULL,
+                             block_table, MB, cum, past, B, T, H, Hk, D, bs, NB, scale, softcap,
+                             window, row_begin, row_end, out);
 }
