@@ -51,6 +51,15 @@
  *   output       [T, H*D]          fp16
  * Token j of sequence b is packed row cum[b] + j and has position
  * past[b] + j.  Query head h uses kv head h / (H / Hk).
+ *
+ * Quantized cache (section 8): with cache_dtype PA_CACHE_INT8 or
+ * PA_CACHE_FP8_E4M3 the pools hold one signed 8-bit code per element,
+ * [NB, bs, Hk, D] bytes, with zero point 0: element value = code * scale.
+ * k_scale / v_scale are fp32, [1] (PA_QUANT_PER_TENSOR) or [Hk, D]
+ * (PA_QUANT_PER_CHANNEL: kv head k's channel c uses scale[k*D + c]).
+ * head_sink (section 6) is an optional fp16 [H]: one extra logit per query
+ * head that enters the softmax denominator only.  Both arrive through
+ * pa_extra_inputs (pa_cache_write_ex / pa_forward_ex).
  */
 #ifndef PA_H_
 #define PA_H_
@@ -89,6 +98,14 @@ enum {
   PA_DEVERR_TIMEOUT = 64      /* an internal wait exceeded its limit (kernel gave up) */
 };
 
+/* Cache element types (section 8.2, T_CACHE).  8-bit codes are signed and
+ * zero-symmetric; writing a value x stores code = Q(x / scale) with the
+ * division in fp32 and Q = round to nearest-even saturated to [-128, 127]
+ * (int8) or to +-448 (e4m3fn). */
+enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2 };
+/* Scale granularity (section 8.2, k_quant_type / v_quant_type). */
+enum { PA_QUANT_NONE = 0, PA_QUANT_PER_TENSOR = 1, PA_QUANT_PER_CHANNEL = 2 };
+
 /* Static description of a layer, fixed for the handle's lifetime
  * (section 4.5 attributes plus the capacities that size launches, 4.7). */
 typedef struct {
@@ -109,17 +126,26 @@ typedef struct {
   int max_tokens;         /* capacity for T across every call on the handle */
   int max_query_len_bound; /* 0 => max_tokens; upper bound on any q_len */
   int max_kv_len_bound;    /* 0 => MB*bs; upper bound on any past + q_len */
+  int cache_dtype;         /* PA_CACHE_*: element type of key_cache / value_cache */
+  int k_quant_type;        /* PA_QUANT_*: NONE for fp16 caches, else PER_TENSOR / PER_CHANNEL */
+  int v_quant_type;        /* must equal k_quant_type */
 } pa_config;
 
 /* Fills *cfg with the attribute defaults (scale 0, softcap 0, window -1,
- * no rotary, bounds 0).  Geometry fields are set to 0 and must be filled. */
+ * no rotary, bounds 0, fp16 cache).  Geometry fields are set to 0 and must
+ * be filled. */
 PA_API void pa_config_init(pa_config* cfg);
 
 /* Host-only check of a configuration against the validation rules
  * (section 15): H % Hk == 0, D % 8 == 0, bs a power of two >= 16,
  * softcap >= 0, window == -1 or >= 1, rotary_dim even and <= D, positive
- * capacities.  Writes a message naming the field into msg (may be NULL).
- * Returns PA_INVALID_ARGUMENT or PA_NOT_SUPPORTED on failure.  Touches no GPU. */
+ * capacities, quantization NONE exactly for fp16 caches.  Writes a message
+ * naming the field into msg (may be NULL).  Returns PA_INVALID_ARGUMENT or
+ * PA_NOT_SUPPORTED on failure.  Not built (PA_NOT_SUPPORTED): 8-bit caches
+ * with head_size 64, with k_quant_type != v_quant_type, or with a
+ * query-length bound (max_query_len_bound, else max_tokens) times
+ * num_heads / kv_num_heads above 16 (8-bit caches run the decode kernel
+ * only).  Touches no GPU. */
 PA_API pa_status pa_validate_config(const pa_config* cfg, char* msg, size_t msg_len);
 
 /* Host-only check of one step's arguments (token_count <= max_tokens,
@@ -170,6 +196,41 @@ PA_API pa_status pa_forward(pa_handle h, const void* query, const void* key,
                      int token_count, const void* cos_cache,
                      const void* sin_cache, void* output, void* stream);
 
+/* Optional inputs of the op contract (section 4, inputs 11, 14, 15).  Any
+ * pointer may be NULL where its feature is off. */
+typedef struct {
+  const void* head_sink;  /* [H] fp16, device; NULL = no sink */
+  const float* k_scale;   /* device fp32, [1] or [Hk*D]; required iff cache_dtype != PA_CACHE_FP16 */
+  const float* v_scale;   /* likewise for value_cache */
+} pa_extra_inputs;
+
+/* pa_cache_write with the optional inputs (extra may be NULL).  With an
+ * 8-bit cache the written rows are quantized (after rotary) under
+ * k_scale / v_scale as stated at PA_CACHE_INT8; bit-exact. */
+PA_API pa_status pa_cache_write_ex(pa_handle h, const void* key, const void* value,
+                                   void* key_cache, void* value_cache,
+                                   const int32_t* block_table,
+                                   const int32_t* cumulative_sequence_lengths,
+                                   const int32_t* past_sequence_lengths, int batch,
+                                   int token_count, const void* cos_cache,
+                                   const void* sin_cache, const pa_extra_inputs* extra,
+                                   void* stream);
+
+/* pa_forward with the optional inputs (extra may be NULL).  8-bit caches
+ * are read at their stored width: the K scale is folded into the query
+ * (q * k_scale[c], rounded to fp16) and the V scale into the output
+ * (section 8.5 phase 3).  head_sink s_h adds exp(s_h - m) to the softmax
+ * denominator of every row of head h, m = max(s_h, max logit) (section
+ * 6.1); a row with no admitted key still outputs 0. */
+PA_API pa_status pa_forward_ex(pa_handle h, const void* query, const void* key,
+                               const void* value, void* key_cache, void* value_cache,
+                               const int32_t* block_table,
+                               const int32_t* cumulative_sequence_lengths,
+                               const int32_t* past_sequence_lengths, int batch,
+                               int token_count, const void* cos_cache,
+                               const void* sin_cache, const pa_extra_inputs* extra,
+                               void* output, void* stream);
+
 /* Synchronises the stream of the handle's last call, reads and clears the
  * device error word into *code (0 = clean).  Returns PA_DEVICE_DATA_ERROR
  * when *code != 0.  Not capturable. */
@@ -200,6 +261,9 @@ PA_API pa_status pa_destroy(pa_handle h);
  * PA_DEVERR_* bits (OR-ed; the caller clears it).  When NULL the bits go
  * to a word inside the shared scratch, cleared at the start of each call,
  * that the caller cannot read.
+ *
+ * It runs fp16 caches without head_sink; an 8-bit cache_dtype returns
+ * PA_NOT_SUPPORTED (pa_forward_ex takes the quantized cache and the sink).
  *
  * The first call on a device does a one-time set-up with that device
  * current (looks up the array's device address with cudaGetSymbolAddress,

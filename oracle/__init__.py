@@ -248,7 +248,7 @@ def forward(step, threads=None, rows=None):
                    step["rotary_interleaved"])
     cdt = step.get("cache_dtype", CACHE_FP16)
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
-                 per_channel=step.get("per_channel", False))
+                 per_channel=step.get("quant_type", 0) == 2)
     kc, vc = cache_write(k, step["value"], step["key_cache"], step["value_cache"],
                          step["block_table"], cum, past, Hk, D, step["block_size"], **quant)
     out = attention(q, kc, vc, step["block_table"], cum, past, H, Hk, D,

@@ -27,10 +27,13 @@ PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_M
 PA_OPT_DECODE_ITEMS_PER_CTA = 5
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
+PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 = 0, 1, 2
+PA_QUANT_NONE, PA_QUANT_PER_TENSOR, PA_QUANT_PER_CHANNEL = 0, 1, 2
 
 EXPORTED = ("pa_config_init", "pa_validate_config", "pa_check_step", "pa_create", "pa_cache_write",
             "pa_forward", "pa_check_device_error", "pa_last_error_message", "pa_destroy",
-            "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count", "pa_forward_no_alloc")
+            "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count", "pa_forward_no_alloc",
+            "pa_cache_write_ex", "pa_forward_ex")
 
 
 class pa_config(ctypes.Structure):
@@ -39,7 +42,12 @@ class pa_config(ctypes.Structure):
         ("scale", ctypes.c_float), ("softcap", ctypes.c_float)] + [
         (n, ctypes.c_int) for n in ("local_window_size", "do_rotary", "rotary_interleaved",
                                     "rotary_dim", "max_rotary_positions", "max_batch", "max_tokens",
-                                    "max_query_len_bound", "max_kv_len_bound")]
+                                    "max_query_len_bound", "max_kv_len_bound", "cache_dtype",
+                                    "k_quant_type", "v_quant_type")]
+
+
+class pa_extra_inputs(ctypes.Structure):
+    _fields_ = [("head_sink", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class PAError(RuntimeError):
@@ -75,6 +83,9 @@ def lib():
         L.pa_set_option.argtypes = [P, I, I]
         L.pa_kernel_time_ms.argtypes = [P, I, ctypes.POINTER(ctypes.c_float)]
         L.pa_forward_no_alloc.argtypes = [CFG, P, P, P, P, P, P, P, P, I, I, P, P, P, P, P]
+        X = ctypes.POINTER(pa_extra_inputs)
+        L.pa_cache_write_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, P, P, X, P]
+        L.pa_forward_ex.argtypes = [P, P, P, P, P, P, P, P, P, I, I, P, P, X, P, P]
         L.pa_last_launch_count.argtypes = [P]
         L.pa_last_launch_count.restype = I
         for n in EXPORTED:
@@ -102,7 +113,7 @@ def _check(status, handle=None):
 def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
                 max_batch, max_tokens, scale=0.0, softcap=0.0, local_window_size=-1, do_rotary=0,
                 rotary_interleaved=0, rotary_dim=0, max_rotary_positions=0, max_query_len_bound=0,
-                max_kv_len_bound=0) -> pa_config:
+                max_kv_len_bound=0, cache_dtype=0, k_quant_type=0, v_quant_type=0) -> pa_config:
     c = pa_config()
     lib().pa_config_init(ctypes.byref(c))
     for k, v in dict(num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
@@ -113,7 +124,8 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                      rotary_interleaved=rotary_interleaved, rotary_dim=rotary_dim,
                      max_rotary_positions=max_rotary_positions,
                      max_query_len_bound=max_query_len_bound,
-                     max_kv_len_bound=max_kv_len_bound).items():
+                     max_kv_len_bound=max_kv_len_bound, cache_dtype=cache_dtype,
+                     k_quant_type=k_quant_type, v_quant_type=v_quant_type).items():
         setattr(c, k, v)
     return c
 
@@ -170,6 +182,39 @@ def pa_forward(h, query, key, value, key_cache, value_cache, block_table,
                             ctypes.c_void_p(stream or 0)), h)
 
 
+def _extra(head_sink=None, k_scale=None, v_scale=None):
+    if head_sink is None and k_scale is None and v_scale is None:
+        return None
+    x = pa_extra_inputs()
+    x.head_sink = None if head_sink is None else head_sink.data_ptr()
+    x.k_scale = None if k_scale is None else k_scale.data_ptr()
+    x.v_scale = None if v_scale is None else v_scale.data_ptr()
+    return ctypes.byref(x)
+
+
+def pa_cache_write_ex(h, key, value, key_cache, value_cache, block_table,
+                      cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
+                      cos_cache=None, sin_cache=None, head_sink=None, k_scale=None, v_scale=None,
+                      stream=None):
+    _check(lib().pa_cache_write_ex(h, _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
+                                   _ptr(block_table), _ptr(cumulative_sequence_lengths),
+                                   _ptr(past_sequence_lengths), batch, token_count, _ptr(cos_cache),
+                                   _ptr(sin_cache), _extra(head_sink, k_scale, v_scale),
+                                   ctypes.c_void_p(stream or 0)), h)
+
+
+def pa_forward_ex(h, query, key, value, key_cache, value_cache, block_table,
+                  cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
+                  cos_cache, sin_cache, output, head_sink=None, k_scale=None, v_scale=None,
+                  stream=None):
+    _check(lib().pa_forward_ex(h, _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache),
+                               _ptr(value_cache), _ptr(block_table),
+                               _ptr(cumulative_sequence_lengths), _ptr(past_sequence_lengths),
+                               batch, token_count, _ptr(cos_cache), _ptr(sin_cache),
+                               _extra(head_sink, k_scale, v_scale), _ptr(output),
+                               ctypes.c_void_p(stream or 0)), h)
+
+
 def pa_forward_no_alloc(cfg: pa_config, query, key, value, key_cache, value_cache, block_table,
                         cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
                         cos_cache, sin_cache, output, device_error=None, stream=None):
@@ -224,21 +269,27 @@ class PagedAttention:
                           do_rotary=step["do_rotary"],
                           rotary_interleaved=step["rotary_interleaved"],
                           rotary_dim=step.get("rotary_dim", 0) or 0,
-                          max_rotary_positions=0 if cos is None else cos.shape[0], **bounds)
+                          max_rotary_positions=0 if cos is None else cos.shape[0],
+                          cache_dtype=step.get("cache_dtype", 0),
+                          k_quant_type=step.get("quant_type", 0), v_quant_type=step.get("quant_type", 0),
+                          **bounds)
         return cls(cfg)
 
     def forward(self, step: dict, output, stream=None):
-        pa_forward(self.handle, step["query"], step["key"], step["value"], step["key_cache"],
-                   step["value_cache"], step["block_table"], step["cumulative_sequence_lengths"],
-                   step["past_sequence_lengths"], step["batch"], step["token_count"],
-                   step.get("cos_cache"), step.get("sin_cache"), output, stream)
+        pa_forward_ex(self.handle, step["query"], step["key"], step["value"], step["key_cache"],
+                      step["value_cache"], step["block_table"], step["cumulative_sequence_lengths"],
+                      step["past_sequence_lengths"], step["batch"], step["token_count"],
+                      step.get("cos_cache"), step.get("sin_cache"), output,
+                      head_sink=step.get("head_sink"), k_scale=step.get("k_scale"),
+                      v_scale=step.get("v_scale"), stream=stream)
 
     def cache_write(self, step: dict, stream=None):
-        pa_cache_write(self.handle, step["key"], step["value"], step["key_cache"],
-                       step["value_cache"], step["block_table"],
-                       step["cumulative_sequence_lengths"], step["past_sequence_lengths"],
-                       step["batch"], step["token_count"], step.get("cos_cache"),
-                       step.get("sin_cache"), stream)
+        pa_cache_write_ex(self.handle, step["key"], step["value"], step["key_cache"],
+                          step["value_cache"], step["block_table"],
+                          step["cumulative_sequence_lengths"], step["past_sequence_lengths"],
+                          step["batch"], step["token_count"], step.get("cos_cache"),
+                          step.get("sin_cache"), head_sink=step.get("head_sink"),
+                          k_scale=step.get("k_scale"), v_scale=step.get("v_scale"), stream=stream)
 
     def set_option(self, option, value):
         pa_set_option(self.handle, option, value)

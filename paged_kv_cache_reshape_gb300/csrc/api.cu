@@ -140,14 +140,18 @@ bool encode_map(CUtensorMap* m, const void* base, int D, int heads_total, long l
 // (strides: row Hk*D*2 bytes, chunk 128 bytes, head D*2 bytes): a box
 // {64, rows, D/64, 1} is one head's page laid out [chunk][row][128 B] with
 // the 128-byte swizzle.  Every addressable byte lies inside the pool.
-bool encode_pool_map(CUtensorMap* m, const void* base, int D, int Hk, long long rows_total, int rows_box) {
+// With 8-bit elements (eb = 1) a chunk holds 128 channels.
+bool encode_pool_map(CUtensorMap* m, const void* base, int D, int Hk, long long rows_total, int rows_box,
+                     int eb = 2) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[4] = {64, (cuuint64_t)rows_total, (cuuint64_t)(D / 64), (cuuint64_t)Hk};
-  cuuint64_t strides[3] = {(cuuint64_t)Hk * D * 2, 128, (cuuint64_t)D * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)rows_box, (cuuint32_t)(D / 64), 1};
+  const int per_chunk = 128 / eb;
+  cuuint64_t dims[4] = {(cuuint64_t)per_chunk, (cuuint64_t)rows_total, (cuuint64_t)(D / per_chunk), (cuuint64_t)Hk};
+  cuuint64_t strides[3] = {(cuuint64_t)Hk * D * eb, 128, (cuuint64_t)D * eb};
+  cuuint32_t box[4] = {(cuuint32_t)per_chunk, (cuuint32_t)rows_box, (cuuint32_t)(D / per_chunk), 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = fn(m, eb == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                  const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -234,6 +238,23 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "max_query_len_bound and max_kv_len_bound must be >= 0");
     return PA_INVALID_ARGUMENT;
   }
+  if (c->cache_dtype < PA_CACHE_FP16 || c->cache_dtype > PA_CACHE_FP8_E4M3) {
+    set_msg(msg, len, "cache_dtype must be PA_CACHE_FP16, PA_CACHE_INT8 or PA_CACHE_FP8_E4M3 (got %d)", c->cache_dtype);
+    return PA_INVALID_ARGUMENT;
+  }
+  for (int qt : {c->k_quant_type, c->v_quant_type})
+    if (qt < PA_QUANT_NONE || qt > PA_QUANT_PER_CHANNEL) {
+      set_msg(msg, len, "k_quant_type / v_quant_type must be PA_QUANT_NONE, PER_TENSOR or PER_CHANNEL (got %d)", qt);
+      return PA_INVALID_ARGUMENT;
+    }
+  if (c->cache_dtype == PA_CACHE_FP16 && (c->k_quant_type != PA_QUANT_NONE || c->v_quant_type != PA_QUANT_NONE)) {
+    set_msg(msg, len, "k_quant_type / v_quant_type must be PA_QUANT_NONE with an fp16 cache");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->cache_dtype != PA_CACHE_FP16 && (c->k_quant_type == PA_QUANT_NONE || c->v_quant_type == PA_QUANT_NONE)) {
+    set_msg(msg, len, "an 8-bit cache needs k_quant_type and v_quant_type PER_TENSOR or PER_CHANNEL");
+    return PA_INVALID_ARGUMENT;
+  }
   // Valid, but outside what this build runs.
   if (c->head_size != 64 && c->head_size != 128 && c->head_size != 256) {
     set_msg(msg, len, "head_size %d is valid but this build runs 64, 128 and 256", c->head_size);
@@ -246,6 +267,23 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
   if (c->do_rotary && rot_dim_of(*c) % 16 != 0) {
     set_msg(msg, len, "rotary_dim %d is valid but this build needs a multiple of 16", rot_dim_of(*c));
     return PA_NOT_SUPPORTED;
+  }
+  if (c->cache_dtype != PA_CACHE_FP16) {
+    if (c->k_quant_type != c->v_quant_type) {
+      set_msg(msg, len, "k_quant_type and v_quant_type must match in this build");
+      return PA_NOT_SUPPORTED;
+    }
+    if (c->head_size == 64) {
+      set_msg(msg, len, "8-bit caches are built for head_size 128 and 256 (got 64)");
+      return PA_NOT_SUPPORTED;
+    }
+    const long long qb = c->max_query_len_bound > 0 ? std::min(c->max_query_len_bound, c->max_tokens) : c->max_tokens;
+    if (qb * (c->num_heads / c->kv_num_heads) > pa::kDecodeRows) {
+      set_msg(msg, len,
+              "8-bit caches run the decode kernel only: max_query_len_bound (else max_tokens) * num_heads / "
+              "kv_num_heads must be <= %d (got %lld)", pa::kDecodeRows, qb * (c->num_heads / c->kv_num_heads));
+      return PA_NOT_SUPPORTED;
+    }
   }
   set_msg(msg, len, "ok");
   return PA_OK;
@@ -333,7 +371,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
   h->max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
 
-  e = pa::decode_configure(c.head_size, &h->dec_ctas_per_sm, &h->dec_smem);
+  e = pa::decode_configure(c.head_size, c.cache_dtype, &h->dec_ctas_per_sm, &h->dec_smem);
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "decode kernel attributes"); }
   size_t psmem = 0;
   h->prefill_ready = pa::prefill_configure(c.head_size, &psmem) == cudaSuccess;
@@ -366,7 +404,8 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   size_t o_pml = off; off = up(off + sizeof(float2) * h->cap_dec * Hk * pa::kDecodeRows);
   size_t o_po = off; off = up(off + sizeof(float) * h->cap_dec * Hk * pa::kDecodeRows * D);
   size_t o_qr = off;
-  if (c.do_rotary) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * D);
+  const bool q_copy = c.do_rotary || c.cache_dtype != PA_CACHE_FP16;  // rotated and/or times k_scale
+  if (q_copy) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * D);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaMalloc(workspace)"); }
@@ -381,7 +420,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->comb_rows = reinterpret_cast<int2*>(w + o_cmb);
   h->part_ml = reinterpret_cast<float2*>(w + o_pml);
   h->part_o = reinterpret_cast<float*>(w + o_po);
-  h->q_rot = c.do_rotary ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
+  h->q_rot = q_copy ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
   for (int i = 0; i < PA_NUM_STAGES; ++i)
     for (int j = 0; j < 2; ++j) cudaEventCreate(&h->ev[i][j]);
   e = cudaDeviceSynchronize();
@@ -426,6 +465,8 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
       h->target_pairs = std::max(1, (value * h->dec_grid + h->cfg.kv_num_heads - 1) / h->cfg.kv_num_heads);
       return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
+      if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)
+        return fail(h, PA_NOT_SUPPORTED, "8-bit caches route every sequence to the decode kernel");
       if (value < 0 || value > pa::kDecodeRows)
         return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", pa::kDecodeRows);
       h->opt_dec_rows = value;
@@ -495,15 +536,21 @@ struct StageTimer {
 pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const void* key, const void* value,
                                         void* key_cache, void* value_cache, const int32_t* block_table,
                                         const int32_t* cum, const int32_t* past, int batch, int token_count,
-                                        const void* cos_cache, const void* sin_cache) {
+                                        const void* cos_cache, const void* sin_cache, const pa_extra_inputs* x) {
   const pa_config& c = h->cfg;
+  const bool quant = c.cache_dtype != PA_CACHE_FP16;
   pa::CacheWriteParams p{};
   p.key = static_cast<const __half*>(key);
   p.value = static_cast<const __half*>(value);
   p.query = static_cast<const __half*>(query);
-  p.q_rot = (query && c.do_rotary) ? h->q_rot : nullptr;
-  p.key_cache = static_cast<__half*>(key_cache);
-  p.value_cache = static_cast<__half*>(value_cache);
+  p.q_rot = (query && (c.do_rotary || quant)) ? h->q_rot : nullptr;
+  p.key_cache = key_cache;
+  p.value_cache = value_cache;
+  p.cache_type = c.cache_dtype;
+  p.per_channel = c.k_quant_type == PA_QUANT_PER_CHANNEL;
+  p.k_scale = quant ? x->k_scale : nullptr;
+  p.v_scale = quant ? x->v_scale : nullptr;
+  p.q_scale = (query && quant) ? 1 : 0;
   p.block_table = block_table;
   p.cum = cum;
   p.past = past;
@@ -529,6 +576,23 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   return p;
 }
 
+const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr};
+
+// The optional inputs against the configuration: scales exactly for 8-bit
+// caches, element alignment.
+pa_status check_extra(pa_handle h, const pa_extra_inputs* x) {
+  const bool quant = h->cfg.cache_dtype != PA_CACHE_FP16;
+  if (quant && (!x->k_scale || !x->v_scale))
+    return fail(h, PA_INVALID_ARGUMENT, "k_scale and v_scale are required with an 8-bit cache");
+  if (!quant && (x->k_scale || x->v_scale))
+    return fail(h, PA_INVALID_ARGUMENT, "k_scale / v_scale given but the cache is fp16");
+  if ((reinterpret_cast<uintptr_t>(x->k_scale) | reinterpret_cast<uintptr_t>(x->v_scale)) % 4)
+    return fail(h, PA_INVALID_ARGUMENT, "k_scale and v_scale must be 4-byte aligned");
+  if (reinterpret_cast<uintptr_t>(x->head_sink) % 2)
+    return fail(h, PA_INVALID_ARGUMENT, "head_sink must be 2-byte aligned");
+  return PA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -536,11 +600,22 @@ extern "C" {
 pa_status pa_cache_write(pa_handle h, const void* key, const void* value, void* key_cache, void* value_cache,
                          const int32_t* block_table, const int32_t* cum, const int32_t* past, int batch,
                          int token_count, const void* cos_cache, const void* sin_cache, void* stream) {
+  return pa_cache_write_ex(h, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
+                           cos_cache, sin_cache, nullptr, stream);
+}
+
+pa_status pa_cache_write_ex(pa_handle h, const void* key, const void* value, void* key_cache, void* value_cache,
+                            const int32_t* block_table, const int32_t* cum, const int32_t* past, int batch,
+                            int token_count, const void* cos_cache, const void* sin_cache,
+                            const pa_extra_inputs* extra, void* stream) {
   if (!h) return fail(nullptr, PA_INVALID_ARGUMENT, "handle must not be NULL");
   char msg[512];
   pa_status st = pa_check_step(&h->cfg, 0, nullptr, key, value, key_cache, value_cache, block_table, cum, past,
                                batch, token_count, cos_cache, sin_cache, nullptr, msg, sizeof(msg));
   if (st != PA_OK) return fail(h, st, "%s", msg);
+  const pa_extra_inputs* x = extra ? extra : &kNoExtra;
+  st = check_extra(h, x);
+  if (st != PA_OK) return st;
   h->last_launches = 0;
   for (bool& r : h->stage_ran) r = false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -548,7 +623,7 @@ pa_status pa_cache_write(pa_handle h, const void* key, const void* value, void* 
   if (token_count == 0) return PA_OK;
   DeviceGuard g(h->device);
   pa::CacheWriteParams p = cache_write_params(h, nullptr, key, value, key_cache, value_cache, block_table, cum,
-                                              past, batch, token_count, cos_cache, sin_cache);
+                                              past, batch, token_count, cos_cache, sin_cache, x);
   StageTimer t(h, PA_STAGE_CACHE_WRITE, s);
   cudaError_t e = pa::launch_cache_write(p, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cache write launch");
@@ -560,11 +635,24 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
                      void* value_cache, const int32_t* block_table, const int32_t* cum, const int32_t* past,
                      int batch, int token_count, const void* cos_cache, const void* sin_cache, void* output,
                      void* stream) {
+  return pa_forward_ex(h, query, key, value, key_cache, value_cache, block_table, cum, past, batch, token_count,
+                       cos_cache, sin_cache, nullptr, output, stream);
+}
+
+pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const void* value, void* key_cache,
+                        void* value_cache, const int32_t* block_table, const int32_t* cum, const int32_t* past,
+                        int batch, int token_count, const void* cos_cache, const void* sin_cache,
+                        const pa_extra_inputs* extra, void* output, void* stream) {
   if (!h) return fail(nullptr, PA_INVALID_ARGUMENT, "handle must not be NULL");
   char msg[512];
   pa_status st = pa_check_step(&h->cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
                                token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
   if (st != PA_OK) return fail(h, st, "%s", msg);
+  const pa_extra_inputs* x = extra ? extra : &kNoExtra;
+  st = check_extra(h, x);
+  if (st != PA_OK) return st;
+  const bool quant = h->cfg.cache_dtype != PA_CACHE_FP16;
+  const __half* sink = static_cast<const __half*>(x->head_sink);
   h->last_launches = 0;
   for (bool& r : h->stage_ran) r = false;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -577,14 +665,16 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   const int box_rows = std::min(c.block_size, pa::kStageKeys);
 
   CUtensorMap tk, tv;
-  if (!encode_pool_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, box_rows) ||
-      !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows))
+  const int eb = quant ? 1 : 2;
+  if (!encode_pool_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, box_rows, eb) ||
+      !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows, eb))
     return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
 
   // The prefill kernel launches unless the query-length bound already routes
-  // every sequence to the decode kernel.  When it does, it goes first and
-  // the decode kernel runs beside it on the SMs the work list leaves it.
-  const bool pre_launch = h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows;
+  // every sequence to the decode kernel (always so for 8-bit caches).  When
+  // it does, it goes first and the decode kernel runs beside it on the SMs
+  // the work list leaves it.
+  const bool pre_launch = !quant && h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows;
 
   // 1+2. prologue: device work list, rotary and the paged cache write
   {
@@ -621,13 +711,13 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.counters = h->counters;
     p.err = h->err;
     pa::CacheWriteParams cp = cache_write_params(h, query, key, value, key_cache, value_cache, block_table, cum,
-                                                 past, batch, token_count, cos_cache, sin_cache);
+                                                 past, batch, token_count, cos_cache, sin_cache, x);
     StageTimer t(h, PA_STAGE_WORKLIST, s);
     cudaError_t e = pa::launch_prologue(p, cp, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prologue launch");
     h->last_launches++;
   }
-  const __half* q_att = c.do_rotary ? h->q_rot : static_cast<const __half*>(query);
+  const __half* q_att = (c.do_rotary || quant) ? h->q_rot : static_cast<const __half*>(query);
   // 3. varlen prefill on tensor memory (skipped when the query-length bound
   // already routes every sequence to the decode kernel)
   if (pre_launch) {
@@ -639,6 +729,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the prefill maps");
     pa::PrefillParams p{};
     p.out = static_cast<__half*>(output);
+    p.head_sink = sink;
     p.block_table = block_table;
     p.seq = h->seq;
     p.pre_tiles = h->pre_tiles;
@@ -671,6 +762,10 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
     p.q_tile_tokens = qt;
     p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
     p.out = static_cast<__half*>(output);
+    p.head_sink = sink;
+    p.cache_type = c.cache_dtype;
+    p.per_channel = c.v_quant_type == PA_QUANT_PER_CHANNEL;
+    p.v_scale = x->v_scale;
     p.block_table = block_table;
     p.seq = h->seq;
     p.dec_items = h->dec_items;
@@ -697,6 +792,7 @@ pa_status pa_forward(pa_handle h, const void* query, const void* key, const void
   // 5. log-sum-exp combine of split partials
   {
     pa::CombineParams p{};
+    p.head_sink = sink;
     p.part_o = h->part_o;
     p.part_ml = h->part_ml;
     p.seq = h->seq;
@@ -759,7 +855,7 @@ NoAllocDevice* no_alloc_setup(int dev) {
     if (d->err != cudaSuccess) { d->what = "cudaDeviceGetAttribute"; return; }
     size_t smem = 0;
     for (int D : {64, 128, 256})
-      if (d->err == cudaSuccess) d->err = pa::decode_configure(D, &d->dec_ctas[head_index(D)], &smem);
+      if (d->err == cudaSuccess) d->err = pa::decode_configure(D, PA_CACHE_FP16, &d->dec_ctas[head_index(D)], &smem);
     if (d->err != cudaSuccess) { d->what = "decode kernel attributes"; return; }
     d->prefill_ok = pa::prefill_configure(64, &smem) == cudaSuccess &&
                     pa::prefill_configure(128, &smem) == cudaSuccess &&
@@ -781,6 +877,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   pa_status st = pa_check_step(cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
                                token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
   if (st != PA_OK) return fail(nullptr, st, "%s", msg);
+  if (cfg->cache_dtype != PA_CACHE_FP16)
+    return fail(nullptr, PA_NOT_SUPPORTED, "pa_forward_no_alloc runs fp16 caches; use pa_forward_ex for 8-bit ones");
   if (device_error && reinterpret_cast<uintptr_t>(device_error) % 4)
     return fail(nullptr, PA_INVALID_ARGUMENT, "device_error must be 4-byte aligned");
   if (token_count == 0) return PA_OK;
@@ -882,8 +980,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   cp.value = static_cast<const __half*>(value);
   cp.query = static_cast<const __half*>(query);
   cp.q_rot = q_rot;
-  cp.key_cache = static_cast<__half*>(key_cache);
-  cp.value_cache = static_cast<__half*>(value_cache);
+  cp.key_cache = key_cache;
+  cp.value_cache = value_cache;
   cp.block_table = block_table;
   cp.cum = cum;
   cp.past = past;

@@ -15,6 +15,14 @@
 // Every row moves as 16-byte vectors: the NHD pool stores a token's
 // [Hk, D] slice contiguously, so a warp writes one contiguous run of
 // Hk*D*2 bytes per tensor (fully coalesced).
+//
+// 8-bit caches (section 8.4, quantize as the rows are scattered): each fp16
+// value x (after rotary) is stored as the code of y = x / scale, the
+// division in fp32 (IEEE), rounded to nearest-even and saturated to
+// [-128, 127] (int8) or to +-448 (e4m3fn); scale is k_scale / v_scale[0] or
+// [k*D + c] per channel.  The query copy for attention is then multiplied by
+// the K scale (fp32 product rounded to fp16), which folds the K
+// dequantization into Q (section 8.5 phase 3).
 #include "step.h"
 #include "worklist.cuh"
 #include "../../include/pa.h"
@@ -39,16 +47,66 @@ union Vec8 {
   __half h[8];
 };
 
-// Copies (rotate = false) or rotates one [nheads, D] row from src to dst.
-// R % 16 == 0 is checked on the host.
-__device__ void row_transform(const __half* __restrict__ src, __half* __restrict__ dst, int nheads,
-                              int D, bool rotate, int R, int interleaved, const __half* cos_row,
-                              const __half* sin_row, int lane) {
+// Emitters: where the eight fp16 values of channels [ch, ch + 8) of head h
+// of a transformed row go.
+struct EmitHalf {  // fp16 row
+  __half* dst;
+  int D;
+  __device__ void operator()(int h, int ch, const Vec8& v) const {
+    *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = v.u;
+  }
+};
+
+__device__ __forceinline__ uint32_t code8(__half x, float s, int type) {
+  const float y = __fdiv_rn(__half2float(x), s);
+  if (type == kCacheI8) {
+    const int r = min(max(__float2int_rn(y), -128), 127);
+    return (uint32_t)r & 0xffu;
+  }
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(0.f), "f"(y));  // low byte <- y
+  return c & 0xffu;
+}
+
+struct EmitCode {  // 8-bit codes; scale[0] or scale[(head0 + h) * D + c]
+  uint8_t* dst;
+  int D, type, per_channel, head0;
+  const float* scale;
+  __device__ void operator()(int h, int ch, const Vec8& v) const {
+    const float* sc = scale + (per_channel ? (size_t)(head0 + h) * D + ch : 0);
+    uint32_t w[2] = {0, 0};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e >> 2] |= code8(v.h[e], __ldg(sc + (per_channel ? e : 0)), type) << (8 * (e & 3));
+    *reinterpret_cast<uint2*>(dst + (size_t)h * D + ch) = make_uint2(w[0], w[1]);
+  }
+};
+
+struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query heads head0 + h)
+  __half* dst;
+  int D, G, per_channel, head0;
+  const float* scale;
+  __device__ void operator()(int h, int ch, const Vec8& v) const {
+    const float* sc = scale + (per_channel ? (size_t)((head0 + h) / G) * D + ch : 0);
+    Vec8 y;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(__fmul_rn(__half2float(v.h[e]), __ldg(sc + (per_channel ? e : 0))));
+    *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = y.u;
+  }
+};
+
+// Copies (rotate = false) or rotates one [nheads, D] row of src and hands
+// every 8-channel group to `emit`.  R % 16 == 0 is checked on the host.
+template <typename Emit>
+__device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
+                              int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane) {
   const int chunks_per_head = D / 8;
   if (!rotate) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-    for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = __ldg(s4 + i);
+    for (int i = lane; i < nheads * chunks_per_head; i += 32) {
+      Vec8 v;
+      v.u = __ldg(s4 + i);
+      emit(i / chunks_per_head, 8 * (i % chunks_per_head), v);
+    }
     return;
   }
   const int half = R / 2;
@@ -60,7 +118,6 @@ __device__ void row_transform(const __half* __restrict__ src, __half* __restrict
     for (int i = lane; i < nheads * per_head; i += 32) {
       int h = i / per_head, c = i % per_head;
       const __half* sh = src + (size_t)h * D;
-      __half* dh = dst + (size_t)h * D;
       if (c < pairs) {
         Vec8 a, b, cs, sn, ya, yb;
         a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
@@ -69,11 +126,13 @@ __device__ void row_transform(const __half* __restrict__ src, __half* __restrict
         sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
 #pragma unroll
         for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e]);
-        *reinterpret_cast<uint4*>(dh + 8 * c) = ya.u;
-        *reinterpret_cast<uint4*>(dh + half + 8 * c) = yb.u;
+        emit(h, 8 * c, ya);
+        emit(h, half + 8 * c, yb);
       } else {
         int ch = R + 8 * (c - pairs);
-        *reinterpret_cast<uint4*>(dh + ch) = __ldg(reinterpret_cast<const uint4*>(sh + ch));
+        Vec8 v;
+        v.u = __ldg(reinterpret_cast<const uint4*>(sh + ch));
+        emit(h, ch, v);
       }
     }
   } else {
@@ -82,7 +141,6 @@ __device__ void row_transform(const __half* __restrict__ src, __half* __restrict
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       int h = i / chunks_per_head, c = i % chunks_per_head;
       const __half* sh = src + (size_t)h * D;
-      __half* dh = dst + (size_t)h * D;
       Vec8 a, y;
       a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
       if (c < rchunks) {
@@ -96,7 +154,7 @@ __device__ void row_transform(const __half* __restrict__ src, __half* __restrict
       } else {
         y.u = a.u;
       }
-      *reinterpret_cast<uint4*>(dh + 8 * c) = y.u;
+      emit(h, 8 * c, y);
     }
   }
 }
@@ -139,8 +197,12 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     const int h0 = (part - 1) * p.q_heads_per_part;
     const int nh = min(p.q_heads_per_part, p.H - h0);
     const size_t qoff = ((size_t)t * p.H + h0) * p.D;
-    row_transform(p.query + qoff, p.q_rot + qoff, nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row,
-                  lane);
+    if (p.q_scale)
+      row_transform(p.query + qoff, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale},
+                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
+    else
+      row_transform(p.query + qoff, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
+                    cos_row, sin_row, lane);
     return;
   }
 
@@ -157,10 +219,22 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   }
   const size_t slot = (size_t)blk * p.bs + (pos & (p.bs - 1));
   const size_t kv_row = (size_t)p.Hk * p.D;
-  row_transform(p.key + (size_t)t * kv_row, p.key_cache + slot * kv_row, p.Hk, p.D, rotate,
-                p.rot_dim, p.interleaved, cos_row, sin_row, lane);
-  row_transform(p.value + (size_t)t * kv_row, p.value_cache + slot * kv_row, p.Hk, p.D, false, 0, 0,
-                nullptr, nullptr, lane);
+  if (p.cache_type == kCacheF16) {
+    row_transform(p.key + (size_t)t * kv_row, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
+    row_transform(p.value + (size_t)t * kv_row,
+                  EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false, 0, 0,
+                  nullptr, nullptr, lane);
+  } else {
+    row_transform(p.key + (size_t)t * kv_row,
+                  EmitCode{static_cast<uint8_t*>(p.key_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
+                           p.k_scale},
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
+    row_transform(p.value + (size_t)t * kv_row,
+                  EmitCode{static_cast<uint8_t*>(p.value_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
+                           p.v_scale},
+                  p.Hk, p.D, false, 0, 0, nullptr, nullptr, lane);
+  }
 }
 
 // Sequences whose cumulative lengths are staged in shared memory (one

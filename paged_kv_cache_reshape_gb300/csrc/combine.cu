@@ -6,7 +6,8 @@
 // and of PagedDecodeReduce ("PagedAttention - CUDA Design Document", section
 // 8 implementation note P5).  Maxima are kept in log2 units by the decode
 // kernel, hence base-2 exponentials.  A row whose splits are all empty
-// outputs 0.
+// outputs 0.  With head_sink (same CUDA design, section 6.1) the row's
+// denominator also gets exp(s_h - M), the sink in log2 units.
 //
 // One warp per (packed row, query head); the work list holds only the rows
 // of sequences that were split, so the grid is a small persistent one.
@@ -18,6 +19,7 @@ namespace pa {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr float kLog2eC = 1.4426950408889634f;
 
 // Adds f * (8 or 4 or kPer floats at po) into acc.
 template <int kPer>
@@ -76,6 +78,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
       den = dl;
+      if (p.head_sink && M != -INFINITY) den += exp2f(__half2float(p.head_sink[h]) * kLog2eC - M);
       for (int s0 = 0; s0 < ns; s0 += 4) {
         float f[4];
         const float* po[4];
@@ -103,6 +106,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
           den += f * ml.y;
           axpy<kPer>(acc, f, p.part_o + row_of(s) * D + lane * kPer);
         }
+        if (p.head_sink) den += exp2f(__half2float(p.head_sink[h]) * kLog2eC - M);
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;

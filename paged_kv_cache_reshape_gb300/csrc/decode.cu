@@ -31,7 +31,19 @@
 //    reduced with warp shuffles;
 //  * at the end of an item the four warps' (m, l, O) are merged through the
 //    last stage's buffer; a single-split sequence writes fp16 output
-//    directly, otherwise fp32 partials go to the combine kernel.
+//    directly, otherwise fp32 partials go to the combine kernel;
+//  * 8-bit caches (int8 / e4m3fn codes, section 8.5 phase 3) are read at
+//    their stored width: the pool view has 128 channels per 128-byte chunk;
+//    K fragments come from ldmatrix on the code bytes (each lane gets four
+//    consecutive channels of one key), which fixes the order in which the
+//    16 channels of an m16n8k16 step are contracted, and the Q fragments
+//    (already times k_scale, written by the prologue) are loaded in that
+//    same order; V fragments come from a transposed ldmatrix (two keys x two
+//    channels per lane), split into an even-channel and an odd-channel MMA;
+//    codes become fp16 pairs with one byte permute and one conversion; the
+//    V scale multiplies the merged output;
+//  * head_sink (section 6.1) adds exp(s_h - M) to the final denominator of a
+//    single-split row (split rows get it in the combine kernel).
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -42,16 +54,23 @@ namespace {
 constexpr int kThreads = (kDecodeWarps + 1) * 32;  // 4 consumer warps + 1 producer warp
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+template <int D, int CT>
 struct DecodeCfg {
-  static constexpr int kChunks = D / 64;                 // 64-channel (128 B) chunks per row
-  static constexpr int kTileBytes = kStageKeys * D * 2;  // K (or V) bytes per stage
-  static constexpr int kStageBytes = 2 * kTileBytes;     // K + V
-  static constexpr int kStages = (D == 256) ? 3 : (D == 128 ? 3 : 6);
-  static constexpr int kQBytes = kChunks * 2048;         // 16 rows x 128 B per chunk
+  static constexpr int kEb = CT == kCacheF16 ? 2 : 1;      // bytes per cache element
+  static constexpr int kChunks = D * kEb / 128;             // 128-byte chunks per K/V row
+  static constexpr int kQChunks = D / 64;                   // 128-byte chunks per fp16 query row
+  static constexpr int kTileBytes = kStageKeys * D * kEb;   // K (or V) bytes per stage
+  static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
+  static constexpr int kStages = CT == kCacheF16 ? ((D == 256) ? 3 : (D == 128 ? 3 : 6)) : 4;
+  static constexpr int kQBytes = kQChunks * 2048;           // 16 rows x 128 B per chunk
   static constexpr int kCtasPerSm = (D == 256) ? 1 : 2;
-  static constexpr int kSmemBytes =
-      1024 + kStages * kStageBytes + 2 * kQBytes + 4 * 16 * 8 + kStages * 64 + (2 * kStages + 4) * 8;
+  // End-of-item merge: the four warps' 16 x D fp32 partial outputs.  An
+  // fp16 stage holds exactly that much and is reused; an 8-bit stage is half
+  // the size, so 8-bit caches get their own region.
+  static constexpr int kMergeBytes = kDecodeWarps * 16 * D * 4;
+  static constexpr int kOwnMerge = kMergeBytes > kStageBytes ? kMergeBytes : 0;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOwnMerge + 2 * kQBytes + 4 * 16 * 8 +
+                                    kStages * 64 + (2 * kStages + 4) * 8;
 };
 
 struct StageTag {
@@ -85,15 +104,49 @@ __device__ __forceinline__ uint32_t tile_off(int kk, int chunk, int col16, int l
   return ((uint32_t)(bx * kChunks + chunk) << (log_r + 7)) + swz(r, col16);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
+// Two 8-bit codes of w (bytes LO and HI; LO goes to the low half) as an
+// fp16 pair.  int8: the code byte plus 128 becomes the low mantissa byte of
+// 1024 + code + 128, exact in fp16, and 1152 is subtracted.
+template <int CT, int LO, int HI>
+__device__ __forceinline__ uint32_t deq2(uint32_t w) {
+  if constexpr (CT == kCacheI8) {
+    const uint32_t x = __byte_perm(w, 0x64646464u, 0x4040u | LO | (HI << 8)) ^ 0x00800080u;
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2(__half(1152.f), __half(1152.f)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const uint32_t x = __byte_perm(w, 0u, LO | (HI << 4));
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(x));
+    return r;
+  }
+}
+
+// Query fragment of one m16n8k16 step in the channel order of the 8-bit K
+// fragments: lane (g = lane/4, j = lane%4) holds channels 16ks + 4j .. 4j+3
+// of rows g and g+8 (a0/a2 and a1/a3).
+__device__ __forceinline__ void q_frag_perm(const uint8_t* q, int ks, int lane, uint32_t* a) {
+  const int c = ks * 16 + 4 * (lane & 3);
+  const int r0 = lane >> 2, r1 = r0 + 8;
+  const uint32_t off = (c >> 6) * 2048 + ((c & 7) * 2);
+  const uint2 x0 = *reinterpret_cast<const uint2*>(q + off + swz(r0, (c & 63) >> 3));
+  const uint2 x1 = *reinterpret_cast<const uint2*>(q + off + swz(r1, (c & 63) >> 3));
+  a[0] = x0.x;
+  a[2] = x0.y;
+  a[1] = x1.x;
+  a[3] = x1.y;
+}
+
+template <int D, int CT>
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-  using C = DecodeCfg<D>;
+  using C = DecodeCfg<D, CT>;
+  constexpr bool kQ8 = CT != kCacheF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint8_t* qbuf = smem + C::kStages * C::kStageBytes;  // [2][kQBytes]
+  uint8_t* merge = smem + C::kStages * C::kStageBytes;  // [kOwnMerge] (8-bit caches)
+  uint8_t* qbuf = merge + C::kOwnMerge;                  // [2][kQBytes]
   float2* mls = reinterpret_cast<float2*>(qbuf + 2 * C::kQBytes);
   StageTag* tags = reinterpret_cast<StageTag*>(mls + 4 * 16);
   uint64_t* full = reinterpret_cast<uint64_t*>(tags + C::kStages);
@@ -135,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
     const int split_keys = p.counters->split_keys;
     const int boxes = kStageKeys >> p.log_box_rows;
     const int qt = p.q_tile_tokens;
-    const uint32_t q_bytes = C::kChunks * p.G * qt * 128;
+    const uint32_t q_bytes = C::kQChunks * p.G * qt * 128;
     int stage = 0;
     uint32_t phase = 0;
     int quse[2] = {0, 0};
@@ -173,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
           ok = false;
         } else {
           mbar_arrive_expect_tx(&q_full[qi], q_bytes);
-          for (int c = 0; c < C::kChunks; ++c)
+          for (int c = 0; c < C::kQChunks; ++c)
             tma_load_3d(qbuf + qi * C::kQBytes + c * 2048, &tm_q, c * 64, k * p.G, si.t0, &q_full[qi]);
         }
       }
@@ -291,9 +344,13 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
         const int row = (mi & 1) * 8 + ri;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const int col = ks * 16 + (mi >> 1) * 8;
-          ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), qf[ks][0], qf[ks][1],
-                  qf[ks][2], qf[ks][3]);
+          if constexpr (kQ8) {
+            q_frag_perm(qcur, ks, lane, qf[ks]);
+          } else {
+            const int col = ks * 16 + (mi >> 1) * 8;
+            ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), qf[ks][0], qf[ks][1],
+                    qf[ks][2], qf[ks][3]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_empty[tg.qi]);
@@ -340,6 +397,32 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
       // ---- S = Q K^T for 16 rows x 16 keys
       float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       const int mi = lane >> 3, ri = lane & 7;
+      if constexpr (kQ8) {
+        // one ldmatrix per 32 channels: matrix mi = keys (mi&1)*8.., channels +16*(mi>>1)
+#pragma unroll
+        for (int ks2 = 0; ks2 < D / 32; ++ks2) {
+          const int key = warp * 16 + (mi & 1) * 8 + ri;
+          const int c = ks2 * 32 + (mi >> 1) * 16;
+          uint32_t kb[4];
+          ldsm_x4(smem_u32(kt + tile_off<C::kChunks>(key, c >> 7, (c & 127) >> 4, log_r)), kb[0], kb[1], kb[2],
+                  kb[3]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int ks = 2 * ks2 + hh;
+            uint32_t a[4];
+            if constexpr (D <= 128) {
+              a[0] = qf[ks][0];
+              a[1] = qf[ks][1];
+              a[2] = qf[ks][2];
+              a[3] = qf[ks][3];
+            } else {
+              q_frag_perm(qcur, ks, lane, a);
+            }
+            hmma16816(s[0], a, deq2<CT, 0, 1>(kb[2 * hh]), deq2<CT, 2, 3>(kb[2 * hh]));
+            hmma16816(s[1], a, deq2<CT, 0, 1>(kb[2 * hh + 1]), deq2<CT, 2, 3>(kb[2 * hh + 1]));
+          }
+        }
+      } else
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a[4];
@@ -413,6 +496,24 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
       pa[2] = pack_half2(s[1][0], s[1][1]);
       pa[3] = pack_half2(s[1][2], s[1][3]);
       // ---- O += P V
+      if constexpr (kQ8) {
+        // matrix mi = keys (mi&1)*8.., channels +16*(mi>>1); lane gets keys
+        // 2j, 2j+1 of channels 2n', 2n'+1: o[4g+2hh] collects the even
+        // channels 32g+16hh+2n', o[4g+2hh+1] the odd ones
+#pragma unroll
+        for (int g = 0; g < D / 32; ++g) {
+          const int key = warp * 16 + (mi & 1) * 8 + ri;
+          const int c = g * 32 + (mi >> 1) * 16;
+          uint32_t vb[4];
+          ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, c >> 7, (c & 127) >> 4, log_r)), vb[0], vb[1], vb[2],
+                    vb[3]);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            hmma16816(o[4 * g + 2 * hh], pa, deq2<CT, 0, 2>(vb[2 * hh]), deq2<CT, 0, 2>(vb[2 * hh + 1]));
+            hmma16816(o[4 * g + 2 * hh + 1], pa, deq2<CT, 1, 3>(vb[2 * hh]), deq2<CT, 1, 3>(vb[2 * hh + 1]));
+          }
+        }
+      } else
 #pragma unroll
       for (int nd = 0; nd < D / 16; ++nd) {
         const int key = warp * 16 + (mi & 1) * 8 + ri;
@@ -437,13 +538,23 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
         lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], 2);
       }
       named_bar(1, kDecodeWarps * 32);  // every warp is done reading the stage
-      float* mrg = reinterpret_cast<float*>(kt);
+      float* mrg = reinterpret_cast<float*>(C::kOwnMerge ? merge : kt);
       float* mw = mrg + warp * 16 * D;
+      if constexpr (kQ8) {
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        const int d = i * 8 + cq;
-        *reinterpret_cast<float2*>(mw + r0 * D + d) = make_float2(o[i][0], o[i][1]);
-        *reinterpret_cast<float2*>(mw + r1 * D + d) = make_float2(o[i][2], o[i][3]);
+        for (int i = 0; i < D / 8; i += 2) {
+          // o[i] even channels, o[i+1] odd ones: four consecutive channels
+          const int d = (i >> 2) * 32 + ((i >> 1) & 1) * 16 + 2 * cq;
+          *reinterpret_cast<float4*>(mw + r0 * D + d) = make_float4(o[i][0], o[i + 1][0], o[i][1], o[i + 1][1]);
+          *reinterpret_cast<float4*>(mw + r1 * D + d) = make_float4(o[i][2], o[i + 1][2], o[i][3], o[i + 1][3]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          const int d = i * 8 + cq;
+          *reinterpret_cast<float2*>(mw + r0 * D + d) = make_float2(o[i][0], o[i][1]);
+          *reinterpret_cast<float2*>(mw + r1 * D + d) = make_float2(o[i][2], o[i][3]);
+        }
       }
       if ((lane & 3) == 0) {
         mls[warp * 16 + r0] = make_float2(m[0], lt[0]);
@@ -465,8 +576,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
             acc += f * mrg[(w * 16 + r) * D + d];
           }
         }
+        if constexpr (kQ8) acc *= __ldg(p.v_scale + (p.per_channel ? tg.k * D + d : 0));
         if (tg.nsplit == 1) {
           const int t = tg.t0 + r / p.G, h = tg.k * p.G + r % p.G;
+          if (p.head_sink && M != -INFINITY) den += exp2f(__half2float(p.head_sink[h]) * kLog2e - M);
           p.out[((size_t)t * p.H + h) * D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
         } else {
           const size_t row = (size_t)tg.u * kDecodeRows + r;
@@ -488,38 +601,65 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D>::kCtasPerSm)
   }
 }
 
-template <int D>
+template <int D, int CT>
 cudaError_t configure_d(size_t* smem, int* ctas) {
-  *smem = DecodeCfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)DecodeCfg<D>::kSmemBytes);
+  using C = DecodeCfg<D, CT>;
+  static_assert(C::kOwnMerge >= C::kMergeBytes || C::kStageBytes >= C::kMergeBytes, "merge buffer");
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(C::kCtasPerSm == 1 || 2 * C::kSmemBytes <= 228 * 1024 - 2 * 1024, "two CTAs per SM");
+  *smem = C::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, CT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(decode_kernel<D, CT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D>, kThreads, *smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, CT>, kThreads, *smem);
   *ctas = n > 0 ? n : 1;
   return e;
 }
 
+template <int D, int CT>
+cudaError_t launch_dc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const DecodeParams& p,
+                      int grid, cudaStream_t s) {
+  return launch_pdl(decode_kernel<D, CT>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
+}
+
 }  // namespace
 
-cudaError_t decode_configure(int head_size, int* ctas_per_sm, size_t* smem) {
+// 8-bit caches are built for head_size 128 and 256.
+cudaError_t decode_configure(int head_size, int cache_type, int* ctas_per_sm, size_t* smem) {
+  if (cache_type == kCacheF16) {
+    switch (head_size) {
+      case 64: return configure_d<64, kCacheF16>(smem, ctas_per_sm);
+      case 128: return configure_d<128, kCacheF16>(smem, ctas_per_sm);
+      case 256: return configure_d<256, kCacheF16>(smem, ctas_per_sm);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  const bool i8 = cache_type == kCacheI8;
   switch (head_size) {
-    case 64: return configure_d<64>(smem, ctas_per_sm);
-    case 128: return configure_d<128>(smem, ctas_per_sm);
-    case 256: return configure_d<256>(smem, ctas_per_sm);
+    case 128: return i8 ? configure_d<128, kCacheI8>(smem, ctas_per_sm) : configure_d<128, kCacheE4M3>(smem, ctas_per_sm);
+    case 256: return i8 ? configure_d<256, kCacheI8>(smem, ctas_per_sm) : configure_d<256, kCacheE4M3>(smem, ctas_per_sm);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                           const DecodeParams& p, int grid, cudaStream_t s) {
+  if (p.cache_type == kCacheF16) {
+    switch (head_size) {
+      case 64: return launch_dc<64, kCacheF16>(tk, tv, tq, p, grid, s);
+      case 128: return launch_dc<128, kCacheF16>(tk, tv, tq, p, grid, s);
+      case 256: return launch_dc<256, kCacheF16>(tk, tv, tq, p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  const bool i8 = p.cache_type == kCacheI8;
   switch (head_size) {
-    case 64: return launch_pdl(decode_kernel<64>, grid, kThreads, DecodeCfg<64>::kSmemBytes, s, tk, tv, tq, p);
-    case 128: return launch_pdl(decode_kernel<128>, grid, kThreads, DecodeCfg<128>::kSmemBytes, s, tk, tv, tq, p);
-    case 256: return launch_pdl(decode_kernel<256>, grid, kThreads, DecodeCfg<256>::kSmemBytes, s, tk, tv, tq, p);
+    case 128: return i8 ? launch_dc<128, kCacheI8>(tk, tv, tq, p, grid, s) : launch_dc<128, kCacheE4M3>(tk, tv, tq, p, grid, s);
+    case 256: return i8 ? launch_dc<256, kCacheI8>(tk, tv, tq, p, grid, s) : launch_dc<256, kCacheE4M3>(tk, tv, tq, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

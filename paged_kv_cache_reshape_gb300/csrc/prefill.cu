@@ -473,8 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: O / l -> fp16 output rows
       if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err)) break;
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const int t = ti.t0 + j, h = ti.k * p.G + (r - j * p.G);
+      // head_sink (section 6.1): exp(s_h - m) joins the denominator
+      if (p.head_sink && m_ref != -INFINITY) l += ex2(__half2float(p.head_sink[h]) * kLog2e - m_ref);
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
       __half* dst = p.out + ((size_t)t * p.H + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {

@@ -656,6 +656,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + ((s0 + s1) + (s2 + s3));
       }
       if (!ok) break;
+      // head_sink (section 6.1): one more denominator term, exp(s_h - m), in
+      // log2 units relative to the row's reference maximum
+      if (p.head_sink && m_ref != -INFINITY)
+        l += ex2(__half2float(p.head_sink[ui.k * p.G + (r - j * p.G)]) * kLog2e - m_ref);
       // The row sum goes to the epilogue warpgroup (its previous value has
       // been read once l_empty completes).
       if (!wait_or_abort(&ctl->l_empty[X], (tt & 1) ^ 1, abort, p.err)) break;

@@ -92,13 +92,20 @@ struct WorklistParams {
   int* err;
 };
 
+// Cache element types (pa.h PA_CACHE_*).
+enum CacheType { kCacheF16 = 0, kCacheI8 = 1, kCacheE4M3 = 2 };
+
 struct CacheWriteParams {
   const __half* key;    // [T, Hk*D]
   const __half* value;  // [T, Hk*D]
   const __half* query;  // [T, H*D] or null (cache write only)
-  __half* q_rot;        // [T, H*D] rotated query (when rotary and query given)
-  __half* key_cache;
-  __half* value_cache;
+  __half* q_rot;        // [T, H*D] query for attention (rotated and/or times k_scale)
+  void* key_cache;      // fp16 or 8-bit codes (cache_type)
+  void* value_cache;
+  int cache_type;       // CacheType
+  int per_channel;      // scales [Hk*D] (1) or [1] (0)
+  const float* k_scale; // 8-bit caches: quantization / dequantization scales
+  const float* v_scale;
   const int* block_table;
   const int* cum;
   const int* past;
@@ -107,13 +114,18 @@ struct CacheWriteParams {
   int batch, token_count;
   int H, Hk, D, bs, NB, MB;
   int rotary, interleaved, rot_dim, rot_positions;
-  int parts;             // warps per token: 1 (K/V) + query parts when rotating Q
+  int q_scale;           // 1: the query copy is multiplied by k_scale (8-bit caches)
+  int parts;             // warps per token: 1 (K/V) + query parts when Q is transformed
   int q_heads_per_part;  // query heads per query part
   int* err;
 };
 
 struct DecodeParams {
   __half* out;      // [T, H*D]
+  const __half* head_sink;  // [H] or null
+  const float* v_scale;     // 8-bit caches: [1] or [Hk*D]
+  int per_channel;
+  int cache_type;
   const int* block_table;
   const SeqInfo* seq;
   const int2* dec_items;
@@ -135,6 +147,7 @@ struct DecodeParams {
 };
 
 struct CombineParams {
+  const __half* head_sink;  // [H] or null
   const float* part_o;
   const float2* part_ml;
   const SeqInfo* seq;
@@ -149,6 +162,7 @@ struct CombineParams {
 
 struct PrefillParams {
   __half* out;
+  const __half* head_sink;  // [H] or null
   const int* block_table;
   const SeqInfo* seq;
   const int2* pre_tiles;
@@ -186,7 +200,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Launchers (defined in the .cu files).
 cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s);
 cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, cudaStream_t s);
-cudaError_t decode_configure(int head_size, int* ctas_per_sm, size_t* smem);
+cudaError_t decode_configure(int head_size, int cache_type, int* ctas_per_sm, size_t* smem);
 cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);

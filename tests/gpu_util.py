@@ -15,13 +15,20 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
+def raw(t):
+    """Bytes of a tensor or numpy array (fp16 pools and 8-bit code pools alike)."""
+    if isinstance(t, torch.Tensor):
+        return t.detach().cpu().contiguous().view(torch.uint8).numpy().reshape(-1)
+    return np.ascontiguousarray(t).view(np.uint8).reshape(-1)
+
+
 def ensure_built():
     from paged_kv_cache_reshape_gb300 import builder as build
     build.build()
 
 
-def make(shape, device="cuda", gen_device=None):
-    return workloads.make_step(shape, device=device, gen_device=gen_device)
+def make(shape, device="cuda", gen_device=None, **kw):
+    return workloads.make_step(shape, device=device, gen_device=gen_device, **kw)
 
 
 def host_copy(step):
@@ -59,8 +66,8 @@ def assert_close(got, ref, what="output"):
 def check_full(step_host, step_dev, out, threads=8):
     """Whole-step parity: both pools bit-exact, every output row within tolerance."""
     ref = oracle.forward(step_host, threads=threads)
-    assert np.array_equal(bits(step_dev["key_cache"]), ref["key_cache"]), "key_cache pool differs"
-    assert np.array_equal(bits(step_dev["value_cache"]), ref["value_cache"]), "value_cache pool differs"
+    assert np.array_equal(raw(step_dev["key_cache"]), raw(ref["key_cache"])), "key_cache pool differs"
+    assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
     T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
     return assert_close(out.float().cpu().numpy().reshape(T, H, D), ref["out"])
 
@@ -68,8 +75,8 @@ def check_full(step_host, step_dev, out, threads=8):
 def check_sampled(step_host, step_dev, out, n_rows=192, seed=0, threads=16):
     """Large-step parity: pools bit-exact, a seeded sample of (t, h) rows."""
     ref = oracle.forward(step_host, threads=threads, rows=np.zeros(0, dtype=np.int64))
-    assert np.array_equal(bits(step_dev["key_cache"]), ref["key_cache"]), "key_cache pool differs"
-    assert np.array_equal(bits(step_dev["value_cache"]), ref["value_cache"]), "value_cache pool differs"
+    assert np.array_equal(raw(step_dev["key_cache"]), raw(ref["key_cache"])), "key_cache pool differs"
+    assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
     T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
     rng = np.random.default_rng(seed)
     rows = np.unique(np.concatenate([rng.integers(0, T * H, n_rows), [0, T * H - 1]]))
@@ -77,6 +84,9 @@ def check_sampled(step_host, step_dev, out, n_rows=192, seed=0, threads=16):
                          step_host["block_table"], step_host["cumulative_sequence_lengths"],
                          step_host["past_sequence_lengths"], H, step_host["kv_num_heads"], D,
                          step_host["block_size"], step_host["scale"], step_host["softcap"],
-                         step_host["local_window_size"], rows=rows, threads=threads)
+                         step_host["local_window_size"], rows=rows, threads=threads,
+                         cache_dtype=step_host.get("cache_dtype", 0), k_scale=step_host.get("k_scale"),
+                         v_scale=step_host.get("v_scale"), per_channel=step_host.get("quant_type", 0) == 2,
+                         head_sink=step_host.get("head_sink"))
     got = out.float().cpu().numpy().reshape(T * H, D)[rows]
     return assert_close(got, o)

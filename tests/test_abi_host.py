@@ -72,6 +72,36 @@ def test_config_rule(field, value, status, word):
     assert st == status and word in msg, (st, msg)
 
 
+@pytest.mark.parametrize("over,status,word", [
+    (dict(cache_dtype=3), pa.PA_INVALID_ARGUMENT, "cache_dtype"),
+    (dict(k_quant_type=4), pa.PA_INVALID_ARGUMENT, "k_quant_type"),
+    (dict(k_quant_type=pa.PA_QUANT_PER_TENSOR, v_quant_type=pa.PA_QUANT_PER_TENSOR),
+     pa.PA_INVALID_ARGUMENT, "fp16 cache"),
+    (dict(cache_dtype=pa.PA_CACHE_INT8), pa.PA_INVALID_ARGUMENT, "8-bit cache needs"),
+    (dict(cache_dtype=pa.PA_CACHE_INT8, k_quant_type=pa.PA_QUANT_PER_TENSOR,
+          v_quant_type=pa.PA_QUANT_PER_CHANNEL, max_query_len_bound=1), pa.PA_NOT_SUPPORTED, "must match"),
+    (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
+          v_quant_type=pa.PA_QUANT_PER_TENSOR, head_size=64, max_query_len_bound=1), pa.PA_NOT_SUPPORTED,
+     "head_size"),
+    (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
+          v_quant_type=pa.PA_QUANT_PER_TENSOR), pa.PA_NOT_SUPPORTED, "decode kernel only"),
+    (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
+          v_quant_type=pa.PA_QUANT_PER_TENSOR, max_query_len_bound=5), pa.PA_NOT_SUPPORTED,
+     "decode kernel only"),
+])
+def test_quantized_cache_rules(over, status, word):
+    st, msg = pa.pa_validate_config(good(**over))
+    assert st == status and word in msg, (st, msg)
+
+
+def test_quantized_decode_config_passes():
+    for cdt in (pa.PA_CACHE_INT8, pa.PA_CACHE_FP8_E4M3):
+        for qt in (pa.PA_QUANT_PER_TENSOR, pa.PA_QUANT_PER_CHANNEL):
+            st, msg = pa.pa_validate_config(good(cache_dtype=cdt, k_quant_type=qt, v_quant_type=qt,
+                                                 max_query_len_bound=4))
+            assert st == pa.PA_OK, msg
+
+
 def test_rotary_rules():
     st, msg = pa.pa_validate_config(good(do_rotary=1, max_rotary_positions=0))
     assert st == pa.PA_INVALID_ARGUMENT and "max_rotary_positions" in msg

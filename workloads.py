@@ -22,6 +22,13 @@ Pool contents: the slots holding positions [0, past_b) of every sequence are
 N(0,1) fp16; every other slot (the new positions before the write, the 20 %
 spare blocks, the tail of each last block) holds the fp16 NaN pattern
 0x7E00, so a kernel that reads a slot it should not read produces NaN.
+
+8-bit pools (quantized cache, CUDA design section 8): past slots hold random
+codes (int8: a normal of standard deviation 32 drawn as integers and clipped
+to +-127; e4m3fn: random sign, exponent field 0..10 and fraction bits, so
+magnitudes up to 15), unused slots the code 0x80 (int8 -128, a loud value)
+or 0x7F (e4m3fn NaN); k_scale / v_scale are fp32 [1] or [Hk*D], drawn
+around 1/32 (int8) or 1/16 (e4m3fn).  head_sink is fp16 [H], N(0, 2^2).
 """
 
 from __future__ import annotations
@@ -128,12 +135,20 @@ def _fill_sentinel(t: torch.Tensor) -> torch.Tensor:
     return t.view(torch.int16).fill_(NAN_SENTINEL_BITS).view(torch.float16)
 
 
-def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None):
+CACHE_FP16, CACHE_INT8, CACHE_FP8 = 0, 1, 2
+QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL = 0, 1, 2
+
+
+def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
+              cache_dtype: int = CACHE_FP16, quant_type: int = QUANT_NONE,
+              head_sink: bool = False):
     """Build every input tensor of one step on `device`.
 
     Random values are drawn with a torch.Generator on `gen_device` (default:
     `device`), so a CPU run and a CUDA run of the same shape share lengths
     and block tables (drawn on the CPU) but not necessarily values.
+    cache_dtype / quant_type select 8-bit pools with their scales; head_sink
+    adds a per-head sink input.
     """
     gen_device = gen_device or str(device)
     H, Hk, D, bs = shape.num_heads, shape.kv_num_heads, shape.head_size, shape.block_size
@@ -171,20 +186,35 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None):
     key = randn(T, Hk * D)
     value = randn(T, Hk * D)
 
-    key_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
-    value_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
+    if cache_dtype == CACHE_FP16:
+        key_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
+        value_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
+        draw = randn
+    else:
+        fill = 0x80 if cache_dtype == CACHE_INT8 else 0x7F
+        key_cache = torch.full((NB, bs, Hk, D), fill, dtype=torch.uint8, device=device)
+        value_cache = torch.full((NB, bs, Hk, D), fill, dtype=torch.uint8, device=device)
+
+        def draw(*size):
+            if cache_dtype == CACHE_INT8:
+                v = torch.randn(*size, generator=vg, device=gen_device).mul(32.0).round().clamp(-127, 127)
+                return v.to(torch.int8).view(torch.uint8).to(device)
+            sign = torch.randint(0, 2, size, generator=vg, device=gen_device)
+            expo = torch.randint(0, 11, size, generator=vg, device=gen_device)
+            frac = torch.randint(0, 8, size, generator=vg, device=gen_device)
+            return (sign * 128 + expo * 8 + frac).to(torch.uint8).to(device)
     # Past content, laid out block by block: row i of a sequence's block table
     # names the block holding its positions [i*bs, (i+1)*bs).
     for b in range(B):
         full, rem = divmod(past[b], bs)
         if full:
             ids = bt[b, :full].to(torch.int64).to(device)
-            key_cache[ids] = randn(full, bs, Hk, D)
-            value_cache[ids] = randn(full, bs, Hk, D)
+            key_cache[ids] = draw(full, bs, Hk, D)
+            value_cache[ids] = draw(full, bs, Hk, D)
         if rem:
             blk = int(bt[b, full])
-            key_cache[blk, :rem] = randn(rem, Hk, D)
-            value_cache[blk, :rem] = randn(rem, Hk, D)
+            key_cache[blk, :rem] = draw(rem, Hk, D)
+            value_cache[blk, :rem] = draw(rem, Hk, D)
 
     out = dict(
         query=query, key=key, value=value,
@@ -203,6 +233,17 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None):
         R = shape.rotary_dim or D
         cos, sin = rotary_tables(MB * bs, R)
         out.update(cos_cache=cos.to(device), sin_cache=sin.to(device), rotary_dim=R)
+    if cache_dtype != CACHE_FP16:
+        sg = torch.Generator().manual_seed(4000 + shape.seed)
+        n = Hk * D if quant_type == QUANT_PER_CHANNEL else 1
+        base = 1.0 / 32.0 if cache_dtype == CACHE_INT8 else 1.0 / 16.0
+        ks = base * (0.8 + 0.4 * torch.rand(n, generator=sg))
+        vs = base * (0.8 + 0.4 * torch.rand(n, generator=sg))
+        out.update(cache_dtype=cache_dtype, quant_type=quant_type,
+                   k_scale=ks.float().to(device), v_scale=vs.float().to(device))
+    if head_sink:
+        hg = torch.Generator().manual_seed(5000 + shape.seed)
+        out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).half().to(device))
     return out
 
 
