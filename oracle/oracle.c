@@ -32,8 +32,9 @@
  * Quantize-on-write reading.  The pages fix dequantization (x = q * scale,
  * zero point 0) but not the rounding of the write.  This oracle takes the
  * plainest one: y = x / scale in fp32 (IEEE division), then int8 = y rounded
- * to nearest-even and saturated to [-128, 127], e4m3fn = y rounded to
- * nearest-even and saturated to the largest finite value (+-448).
+ * to nearest-even and saturated to [-128, 127] (NaN -> 0: int8 has no NaN),
+ * e4m3fn = y rounded to nearest-even and saturated to the largest finite
+ * value (+-448; NaN stays NaN).
  *
  * Precision.  Attention is evaluated in fp64 from exactly converted fp16
  * inputs: scores, max, exponentials, the weighted sum and the normaliser are
@@ -157,6 +158,7 @@ uint8_t oracle_quantize(uint16_t h, float s, int cache_dtype) {
   float y = (float)oracle_half_to_double(h) / s;
   if (cache_dtype == ORACLE_CACHE_FP8) return oracle_float_to_e4m3(y);
   float r = nearbyintf(y);
+  if (r != r) r = 0.0f; /* int8 has no NaN: a NaN value stores code 0 */
   if (r > 127.0f) r = 127.0f;
   if (r < -128.0f) r = -128.0f;
   return (uint8_t)(int8_t)r;

@@ -74,6 +74,11 @@ def test_int8_quantize_matches_numpy(scale):
     assert np.array_equal(got, ref)
 
 
+def test_int8_quantize_nan_and_infinity():
+    x = np.array([np.nan, np.inf, -np.inf], dtype=np.float16).view(np.uint16)
+    assert list(oracle.quantize(x, 0.5, oracle.CACHE_INT8)) == [0, 127, 128]
+
+
 @pytest.mark.parametrize("scale", [1.0, 0.0123, 0.25])
 def test_fp8_quantize_matches_torch(scale):
     rng = np.random.default_rng(3)
