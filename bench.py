@@ -11,7 +11,10 @@ sequence with more query rows than a decode item holds.
 --workload selects another step shape (for profiling): `mixed` (16 prompts
 of 1024 tokens + 240 decodes, block_size 32), `long_window` (Gemma-2-shaped
 window 4096 / softcap 50 decode), `rotary_decode` (Llama-70B-shaped decode
-with rotary), `prefill` (16 prompts of 1024 tokens alone), `tiny`.
+with rotary), `prefill` (16 prompts of 1024 tokens alone), `tiny`,
+`decode_fp8` / `decode_int8` (the default decode step over an e4m3fn / int8
+paged cache with per-channel scales; its K/V bytes count one byte per
+element).
 
 value    decode workloads: attended K/V bytes of the step / step time (GB/s),
          each admitted K and V element counted once per kv head; workloads
@@ -54,15 +57,33 @@ FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 DECODE_ROWS = 16  # query rows of one decode item: q_len * G <= 16 goes to the decode kernel
 
 
+# 8-bit cache variants of the Llama-3-8B-shaped decode step (per-channel
+# scales, the quantized cache of the CUDA design, section 8)
+QUANT_WORKLOADS = {"decode_fp8": 2, "decode_int8": 1}
+
+
 def workload_shape(name):
     import workloads
     index = {"tiny": 0, "decode": 1, "mixed": 2, "long_window": 3, "rotary_decode": 4}
+    if name in QUANT_WORKLOADS:
+        return workloads.config_shape(1)
     if name in index:
         return workloads.config_shape(index[name])
     if name == "prefill":
         return workloads.custom_shape("prefill_16x1024_h32_kv8_d128_bs32", 32, 8, 128, 32, [0] * 16,
                                       [1024] * 16, seed=2)
     raise ValueError(name)
+
+
+def workload_options(name):
+    """make_step keywords of a workload (8-bit cache variants)."""
+    if name in QUANT_WORKLOADS:
+        return dict(cache_dtype=QUANT_WORKLOADS[name], quant_type=2)
+    return {}
+
+
+def shape_name(name, shape):
+    return shape.name + ({2: "_e4m3_cache", 1: "_int8_cache"}[QUANT_WORKLOADS[name]] if name in QUANT_WORKLOADS else "")
 
 
 def seq_lengths(step):
@@ -80,12 +101,13 @@ def work_of(step, seqs=None):
     past, q = seq_lengths(step)
     W, G = step["local_window_size"], step["num_heads"] // step["kv_num_heads"]
     Hk, H, D = step["kv_num_heads"], step["num_heads"], step["head_size"]
+    eb = 1 if step.get("cache_dtype", 0) else 2  # bytes per cache element
     w = dict(kv_bytes=0, dec_kv_bytes=0, dec_qo_bytes=0, pre_flops=0, tokens=0)
     for b in (range(len(past)) if seqs is None else seqs):
         if q[b] == 0:
             continue
         L = past[b] + q[b]
-        kv = (min(L, W) if W >= 1 else L) * Hk * D * 4
+        kv = (min(L, W) if W >= 1 else L) * Hk * D * 2 * eb
         w["kv_bytes"] += kv
         w["tokens"] += q[b]
         if q[b] * G <= DECODE_ROWS:
@@ -210,7 +232,9 @@ def oracle_sample(step, budget_s, start_seq=0):
             oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"], step["block_table"],
                              cum, step["past_sequence_lengths"], H, step["kv_num_heads"], step["head_size"],
                              step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
-                             rows=rows, threads=cores)
+                             rows=rows, threads=cores, cache_dtype=step.get("cache_dtype", 0),
+                             k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
+                             per_channel=step.get("quant_type", 0) == 2, head_sink=step.get("head_sink"))
         seqs.append(b)
         b = (b + 1) % B
         if time.perf_counter() - t0 > budget_s or len(seqs) >= B:
@@ -227,7 +251,7 @@ def run_reference(args, rank, world):
     import workloads
 
     shape = workload_shape(args.workload)
-    step = workloads.make_step(shape, device="cpu")
+    step = workloads.make_step(shape, device="cpu", **workload_options(args.workload))
     unit = "GB/s" if work_of(step)["pre_flops"] == 0 else "tokens/s"
     budget = min(args.ref_budget, max(0.02, 150.0 / (args.steps + args.warmup)))
     b, tot_t, done, cores = 0, 0.0, 0, 1
@@ -246,7 +270,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": shape.name, "sample": "bounded"},
+        "data": "synthetic", "config": {"workload": shape_name(args.workload, shape), "sample": "bounded"},
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -264,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     shape = workload_shape(args.workload)
-    step = workloads.make_step(shape, device=dev, gen_device=str(dev))
+    step = workloads.make_step(shape, device=dev, gen_device=str(dev), **workload_options(args.workload))
     host = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
     work = work_of(host)
     unit = "tokens/s" if work["pre_flops"] > 0 else "GB/s"
@@ -347,11 +371,13 @@ def run_ours(args, rank, world, local_rank):
     if ker_ms[pa.PA_STAGE_DECODE] and work["dec_kv_bytes"]:
         t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
         alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
+        ct = {0: "", 1: ", int8", 2: ", e4m3"}[host.get("cache_dtype", 0)]
         rooflines["decode"] = {
-            "bound": "hbm", "kernel": f"decode_kernel<{shape.head_size}>", "achieved": alg / (t * 1e-3) / 1e9,
+            "bound": "hbm", "kernel": f"decode_kernel<{shape.head_size}{ct}>", "achieved": alg / (t * 1e-3) / 1e9,
             "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
             "frac": alg / (t * 1e-3) / 1e9 / hbm,
-            "traffic": committed_traffic("decode.cu", shape.name), "algorithmic_bytes_per_launch": alg,
+            "traffic": committed_traffic("decode.cu", shape_name(args.workload, shape)),
+            "algorithmic_bytes_per_launch": alg,
             "launch_ms": t}
     if ker_ms[pa.PA_STAGE_PREFILL] and work["pre_flops"]:
         t = statistics.mean(ker_ms[pa.PA_STAGE_PREFILL])
@@ -399,7 +425,8 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": shape.name, "batch": shape.batch, "token_count": shape.token_count,
+        "config": {"workload": shape_name(args.workload, shape), "batch": shape.batch,
+                   "token_count": shape.token_count,
                    "num_heads": shape.num_heads, "kv_num_heads": shape.kv_num_heads,
                    "head_size": shape.head_size, "block_size": shape.block_size,
                    "attended_kv_bytes_per_step": work["kv_bytes"], "prefill_flops_per_step": work["pre_flops"],
@@ -434,7 +461,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "mixed", "long_window", "rotary_decode", "prefill", "tiny"])
+                    choices=["decode", "mixed", "long_window", "rotary_decode", "prefill", "tiny"]
+                    + sorted(QUANT_WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch pa_forward directly instead of a graph replay")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")

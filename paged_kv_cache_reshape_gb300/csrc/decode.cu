@@ -53,6 +53,7 @@ namespace {
 
 constexpr int kThreads = (kDecodeWarps + 1) * 32;  // 4 consumer warps + 1 producer warp
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
 
 template <int D, int CT>
 struct DecodeCfg {
@@ -113,10 +114,18 @@ __device__ __forceinline__ uint32_t deq2(uint32_t w) {
     const uint32_t x = __byte_perm(w, 0x64646464u, 0x4040u | LO | (HI << 8)) ^ 0x00800080u;
     const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2(__half(1152.f), __half(1152.f)));
     return *reinterpret_cast<const uint32_t*>(&h);
+  } else if constexpr (LO == 0 && HI == 1) {  // the low half as it is
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(w));
+    return r;
+  } else if constexpr (LO == 2 && HI == 3) {  // the high half as it is
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, hi;\n\t}" : "=r"(r) : "r"(w));
+    return r;
   } else {
     const uint32_t x = __byte_perm(w, 0u, LO | (HI << 4));
     uint32_t r;
-    asm("{\n\t.reg .b16 lo;\n\tcvt.u16.u32 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(x));
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(r) : "r"(x));
     return r;
   }
 }
@@ -461,15 +470,20 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
           tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
         }
       }
+      // Lazy rescale: the reference max m moves only when a score exceeds
+      // it by more than 2^kLazyRescale, so P stays <= 256 and O is rescaled
+      // on few stages (the final merge works with any reference).
       float alpha[2], muse[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
         tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
-        const float mn = fmaxf(m[i], tmax[i]);
-        muse[i] = (mn == -INFINITY) ? 0.f : mn;
-        alpha[i] = exp2f(m[i] - muse[i]);
-        m[i] = mn;
+        alpha[i] = 1.f;
+        if (tmax[i] > m[i] + kLazyRescale) {  // also the first finite score (m = -inf)
+          alpha[i] = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - tmax[i]);
+          m[i] = tmax[i];
+        }
+        muse[i] = (m[i] == -INFINITY) ? 0.f : m[i];
       }
       float rs[2] = {0.f, 0.f};
 #pragma unroll
@@ -483,12 +497,14 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
       }
       l[0] = l[0] * alpha[0] + rs[0];
       l[1] = l[1] * alpha[1] + rs[1];
+      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        o[i][0] *= alpha[0];
-        o[i][1] *= alpha[0];
-        o[i][2] *= alpha[1];
-        o[i][3] *= alpha[1];
+        for (int i = 0; i < D / 8; ++i) {
+          o[i][0] *= alpha[0];
+          o[i][1] *= alpha[0];
+          o[i][2] *= alpha[1];
+          o[i][3] *= alpha[1];
+        }
       }
       uint32_t pa[4];
       pa[0] = pack_half2(s[0][0], s[0][1]);
