@@ -53,7 +53,7 @@ def lib():
             L.oracle_double_to_half.restype = ctypes.c_uint16
             L.oracle_rotary.argtypes = [P, P, I, I, I, P, P, I, P, P, I, I, I]
             L.oracle_rotary.restype = I
-            L.oracle_cache_write.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I]
+            L.oracle_cache_write.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, P]
             L.oracle_cache_write.restype = I
             L.oracle_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I,
                                            Dd, Dd, I, LL, LL, P]
@@ -64,7 +64,7 @@ def lib():
             L.oracle_float_to_e4m3.restype = ctypes.c_uint8
             L.oracle_quantize.argtypes = [ctypes.c_uint16, ctypes.c_float, I]
             L.oracle_quantize.restype = ctypes.c_uint8
-            L.oracle_cache_write_quant.argtypes = [P, P, P, P, P, P, I, I, P, I, P, P, I, I, I, I, I, I]
+            L.oracle_cache_write_quant.argtypes = [P, P, P, P, P, P, I, I, P, I, P, P, I, I, I, I, I, I, P]
             L.oracle_cache_write_quant.restype = I
             L.oracle_attention_ex.argtypes = [P, P, P, I, P, P, I, P, P, I, P, P, I, I, I, I, I, I, I,
                                               Dd, Dd, I, LL, LL, P]
@@ -139,13 +139,15 @@ def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
 
 def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
                 kv_num_heads, head_size, block_size, cache_dtype=CACHE_FP16,
-                k_scale=None, v_scale=None, per_channel=False):
+                k_scale=None, v_scale=None, per_channel=False, slot_mapping=None):
     """Returns (key_cache', value_cache') after writing the new tokens' rows.
 
     key/value are fp16 bit arrays [T, Hk*D] (key already rotated when rotary
     is on); the input caches are copied, not modified.  With an 8-bit
     cache_dtype the caches are uint8 code arrays and k_scale / v_scale fp32
-    arrays ([1], or [Hk*D] when per_channel)."""
+    arrays ([1], or [Hk*D] when per_channel).  slot_mapping ([T] int32, -1 =
+    no write) replaces the slot derivation when given."""
+    sm = _np(slot_mapping, np.int32) if slot_mapping is not None else None
     if cache_dtype != CACHE_FP16:
         ka, va = _np(key, np.uint16), _np(value, np.uint16)
         kc = _np(key_cache, np.uint8).copy()
@@ -157,7 +159,7 @@ def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
                                             int(bool(per_channel)), int(cache_dtype), _p(bt),
                                             bt.shape[1], _p(cum_a), _p(past_a), past_a.shape[0],
                                             ka.shape[0], kv_num_heads, head_size, block_size,
-                                            kc.shape[0])
+                                            kc.shape[0], _p(sm))
         _check(st, "cache_write_quant")
         return kc, vc
     ka, va = _np(key, np.uint16), _np(value, np.uint16)
@@ -167,7 +169,7 @@ def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
     cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
     st = lib().oracle_cache_write(_p(ka), _p(va), _p(kc), _p(vc), _p(bt), bt.shape[1],
                                   _p(cum_a), _p(past_a), past_a.shape[0], ka.shape[0],
-                                  kv_num_heads, head_size, block_size, kc.shape[0])
+                                  kv_num_heads, head_size, block_size, kc.shape[0], _p(sm))
     _check(st, "cache_write")
     return kc, vc
 
@@ -250,7 +252,8 @@ def forward(step, threads=None, rows=None):
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)
     kc, vc = cache_write(k, step["value"], step["key_cache"], step["value_cache"],
-                         step["block_table"], cum, past, Hk, D, step["block_size"], **quant)
+                         step["block_table"], cum, past, Hk, D, step["block_size"],
+                         slot_mapping=step.get("slot_mapping"), **quant)
     out = attention(q, kc, vc, step["block_table"], cum, past, H, Hk, D,
                     step["block_size"], step["scale"], step["softcap"],
                     step["local_window_size"], rows=rows, threads=threads,

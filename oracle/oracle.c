@@ -240,30 +240,51 @@ int oracle_rotary(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
   return ORACLE_OK;
 }
 
-/* ---- reshape_and_cache (CUDA design section 5.1, derived slot) ---- */
+/* ---- reshape_and_cache (CUDA design section 5.1 derived slot, 5.2
+ * explicit slot_mapping) ---- */
+
+/* Destination slot of packed row t of sequence b at position pos, or -1 for
+ * no write.  With slot_mapping (section 5.2) the entry is authoritative:
+ * -1 skips the row, other values must lie in [0, NB*bs).  Without it the
+ * slot is derived from block_table (section 5.1).  Returns -2 for bad
+ * device data. */
+static long long write_slot(const int32_t* slot_mapping, const int32_t* block_table, int MB, int b, int t,
+                            int pos, int bs, int NB) {
+  if (slot_mapping) {
+    long long s = slot_mapping[t];
+    if (s == -1) return -1;
+    if (s < 0 || s >= (long long)NB * bs) return -2;
+    return s;
+  }
+  int i = pos / bs;
+  if (i >= MB) return -2;
+  int blk = block_table[(size_t)b * MB + i];
+  if (blk == -1) return -1;
+  if (blk < -1 || blk >= NB) return -2;
+  return (long long)blk * bs + pos % bs;
+}
 
 /* For every new token t of sequence b (position past_b + j):
  *   block_id = block_table[b][pos / bs], slot = block_id * bs + pos % bs,
  *   key_cache[slot, k, :] = key[t, k, :], value_cache likewise.
  * A -1 entry means "not mapped": nothing is written for that token.
- * Other out-of-range entries are bad device data. */
+ * Other out-of-range entries are bad device data.  slot_mapping (may be
+ * NULL) replaces the derivation: slot = slot_mapping[t], -1 = no write. */
 int oracle_cache_write(const uint16_t* key, const uint16_t* value,
                        uint16_t* key_cache, uint16_t* value_cache,
                        const int32_t* block_table, int MB,
                        const int32_t* cum, const int32_t* past, int B, int T,
-                       int Hk, int D, int bs, int NB) {
+                       int Hk, int D, int bs, int NB, const int32_t* slot_mapping) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
   size_t row = (size_t)Hk * D;
   for (int b = 0; b < B; ++b) {
     for (int t = cum[b]; t < cum[b + 1]; ++t) {
       int pos = past[b] + (t - cum[b]);
-      int i = pos / bs;
-      if (i >= MB) return ORACLE_BAD_DEVICE_DATA;
-      int blk = block_table[(size_t)b * MB + i];
-      if (blk == -1) continue;
-      if (blk < -1 || blk >= NB) return ORACLE_BAD_DEVICE_DATA;
-      size_t slot = (size_t)blk * bs + pos % bs;
+      long long ws = write_slot(slot_mapping, block_table, MB, b, t, pos, bs, NB);
+      if (ws == -1) continue;
+      if (ws < 0) return ORACLE_BAD_DEVICE_DATA;
+      size_t slot = (size_t)ws;
       memcpy(key_cache + slot * row, key + (size_t)t * row, row * sizeof(uint16_t));
       memcpy(value_cache + slot * row, value + (size_t)t * row, row * sizeof(uint16_t));
     }
@@ -280,7 +301,7 @@ int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
                              int per_channel, int cache_dtype,
                              const int32_t* block_table, int MB,
                              const int32_t* cum, const int32_t* past, int B, int T,
-                             int Hk, int D, int bs, int NB) {
+                             int Hk, int D, int bs, int NB, const int32_t* slot_mapping) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
   if (cache_dtype != ORACLE_CACHE_INT8 && cache_dtype != ORACLE_CACHE_FP8) return ORACLE_BAD_ARGUMENT;
@@ -288,12 +309,10 @@ int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
   for (int b = 0; b < B; ++b) {
     for (int t = cum[b]; t < cum[b + 1]; ++t) {
       int pos = past[b] + (t - cum[b]);
-      int i = pos / bs;
-      if (i >= MB) return ORACLE_BAD_DEVICE_DATA;
-      int blk = block_table[(size_t)b * MB + i];
-      if (blk == -1) continue;
-      if (blk < -1 || blk >= NB) return ORACLE_BAD_DEVICE_DATA;
-      size_t slot = (size_t)blk * bs + pos % bs;
+      long long ws = write_slot(slot_mapping, block_table, MB, b, t, pos, bs, NB);
+      if (ws == -1) continue;
+      if (ws < 0) return ORACLE_BAD_DEVICE_DATA;
+      size_t slot = (size_t)ws;
       for (size_t e = 0; e < row; ++e) {
         size_t si = per_channel ? e : 0; /* e = k * D + c */
         key_cache[slot * row + e] = oracle_quantize(key[(size_t)t * row + e], k_scale[si], cache_dtype);
