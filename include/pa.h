@@ -95,7 +95,8 @@ enum {
   PA_DEVERR_KV_BOUND = 8,     /* past + q_len > kv bound or > MB*bs (sequence skipped) */
   PA_DEVERR_Q_BOUND = 16,     /* q_len > max_query_len_bound (sequence skipped) */
   PA_DEVERR_ROTARY_POS = 32,  /* position >= max_rotary_positions (row left unrotated) */
-  PA_DEVERR_TIMEOUT = 64      /* an internal wait exceeded its limit (kernel gave up) */
+  PA_DEVERR_TIMEOUT = 64,     /* an internal wait exceeded its limit (kernel gave up) */
+  PA_DEVERR_SLOT = 128        /* slot_mapping entry outside [-1, NB*bs) (row not written) */
 };
 
 /* Cache element types (section 8.2, T_CACHE).  8-bit codes are signed and
@@ -202,11 +203,20 @@ typedef struct {
   const void* head_sink;  /* [H] fp16, device; NULL = no sink */
   const float* k_scale;   /* device fp32, [1] or [Hk*D]; required iff cache_dtype != PA_CACHE_FP16 */
   const float* v_scale;   /* likewise for value_cache */
+  const int32_t* slot_mapping; /* [T] int32, device; NULL = derive the write slot from block_table */
 } pa_extra_inputs;
 
 /* pa_cache_write with the optional inputs (extra may be NULL).  With an
  * 8-bit cache the written rows are quantized (after rotary) under
- * k_scale / v_scale as stated at PA_CACHE_INT8; bit-exact. */
+ * k_scale / v_scale as stated at PA_CACHE_INT8; bit-exact.
+ * slot_mapping (section 5.2) is authoritative for the write: packed row t
+ * goes to flat slot slot_mapping[t] of the pool viewed as [NB*bs, Hk, D];
+ * -1 writes nothing (the row's query still attends); values outside
+ * [-1, NB*bs) write nothing and set PA_DEVERR_SLOT.  block_table still
+ * defines what every sequence reads (positions [i*bs, (i+1)*bs) of row b),
+ * so a runtime can recycle blocks, e.g. a ring of ceil(W/bs)+1 blocks per
+ * sequence under a local window W with -1 entries below the window
+ * (section 9.3). */
 PA_API pa_status pa_cache_write_ex(pa_handle h, const void* key, const void* value,
                                    void* key_cache, void* value_cache,
                                    const int32_t* block_table,

@@ -22,6 +22,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_INVALID_ARGUMENT", 2: "PA_NOT_SUPPORTED", 3: 
 
 PA_DEVERR_CUM, PA_DEVERR_BLOCK_ID, PA_DEVERR_PAST = 1, 2, 4
 PA_DEVERR_KV_BOUND, PA_DEVERR_Q_BOUND, PA_DEVERR_ROTARY_POS, PA_DEVERR_TIMEOUT = 8, 16, 32, 64
+PA_DEVERR_SLOT = 128
 
 PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_MAX_ROWS = 1, 2, 3, 4
 PA_OPT_DECODE_ITEMS_PER_CTA = 5
@@ -47,7 +48,8 @@ class pa_config(ctypes.Structure):
 
 
 class pa_extra_inputs(ctypes.Structure):
-    _fields_ = [("head_sink", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
+    _fields_ = [("head_sink", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("slot_mapping", ctypes.c_void_p)]
 
 
 class PAError(RuntimeError):
@@ -182,36 +184,37 @@ def pa_forward(h, query, key, value, key_cache, value_cache, block_table,
                             ctypes.c_void_p(stream or 0)), h)
 
 
-def _extra(head_sink=None, k_scale=None, v_scale=None):
-    if head_sink is None and k_scale is None and v_scale is None:
+def _extra(head_sink=None, k_scale=None, v_scale=None, slot_mapping=None):
+    if head_sink is None and k_scale is None and v_scale is None and slot_mapping is None:
         return None
     x = pa_extra_inputs()
     x.head_sink = None if head_sink is None else head_sink.data_ptr()
     x.k_scale = None if k_scale is None else k_scale.data_ptr()
     x.v_scale = None if v_scale is None else v_scale.data_ptr()
+    x.slot_mapping = None if slot_mapping is None else slot_mapping.data_ptr()
     return ctypes.byref(x)
 
 
 def pa_cache_write_ex(h, key, value, key_cache, value_cache, block_table,
                       cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
                       cos_cache=None, sin_cache=None, head_sink=None, k_scale=None, v_scale=None,
-                      stream=None):
+                      slot_mapping=None, stream=None):
     _check(lib().pa_cache_write_ex(h, _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
                                    _ptr(block_table), _ptr(cumulative_sequence_lengths),
                                    _ptr(past_sequence_lengths), batch, token_count, _ptr(cos_cache),
-                                   _ptr(sin_cache), _extra(head_sink, k_scale, v_scale),
+                                   _ptr(sin_cache), _extra(head_sink, k_scale, v_scale, slot_mapping),
                                    ctypes.c_void_p(stream or 0)), h)
 
 
 def pa_forward_ex(h, query, key, value, key_cache, value_cache, block_table,
                   cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
                   cos_cache, sin_cache, output, head_sink=None, k_scale=None, v_scale=None,
-                  stream=None):
+                  slot_mapping=None, stream=None):
     _check(lib().pa_forward_ex(h, _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache),
                                _ptr(value_cache), _ptr(block_table),
                                _ptr(cumulative_sequence_lengths), _ptr(past_sequence_lengths),
                                batch, token_count, _ptr(cos_cache), _ptr(sin_cache),
-                               _extra(head_sink, k_scale, v_scale), _ptr(output),
+                               _extra(head_sink, k_scale, v_scale, slot_mapping), _ptr(output),
                                ctypes.c_void_p(stream or 0)), h)
 
 
@@ -281,7 +284,7 @@ class PagedAttention:
                       step["past_sequence_lengths"], step["batch"], step["token_count"],
                       step.get("cos_cache"), step.get("sin_cache"), output,
                       head_sink=step.get("head_sink"), k_scale=step.get("k_scale"),
-                      v_scale=step.get("v_scale"), stream=stream)
+                      v_scale=step.get("v_scale"), slot_mapping=step.get("slot_mapping"), stream=stream)
 
     def cache_write(self, step: dict, stream=None):
         pa_cache_write_ex(self.handle, step["key"], step["value"], step["key_cache"],
@@ -289,7 +292,8 @@ class PagedAttention:
                           step["cumulative_sequence_lengths"], step["past_sequence_lengths"],
                           step["batch"], step["token_count"], step.get("cos_cache"),
                           step.get("sin_cache"), head_sink=step.get("head_sink"),
-                          k_scale=step.get("k_scale"), v_scale=step.get("v_scale"), stream=stream)
+                          k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
+                          slot_mapping=step.get("slot_mapping"), stream=stream)
 
     def set_option(self, option, value):
         pa_set_option(self.handle, option, value)

@@ -551,6 +551,7 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.k_scale = quant ? x->k_scale : nullptr;
   p.v_scale = quant ? x->v_scale : nullptr;
   p.q_scale = (query && quant) ? 1 : 0;
+  p.slot_mapping = x->slot_mapping;
   p.block_table = block_table;
   p.cum = cum;
   p.past = past;
@@ -576,7 +577,7 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   return p;
 }
 
-const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr};
+const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr, nullptr};
 
 // The optional inputs against the configuration: scales exactly for 8-bit
 // caches, element alignment.
@@ -590,6 +591,8 @@ pa_status check_extra(pa_handle h, const pa_extra_inputs* x) {
     return fail(h, PA_INVALID_ARGUMENT, "k_scale and v_scale must be 4-byte aligned");
   if (reinterpret_cast<uintptr_t>(x->head_sink) % 2)
     return fail(h, PA_INVALID_ARGUMENT, "head_sink must be 2-byte aligned");
+  if (reinterpret_cast<uintptr_t>(x->slot_mapping) % 4)
+    return fail(h, PA_INVALID_ARGUMENT, "slot_mapping must be 4-byte aligned");
   return PA_OK;
 }
 

@@ -5,6 +5,8 @@
 // cumulative_sequence_lengths, guarded against rows past cum[B] as section
 // 18.2 asks; position past_b + j; block_table row position / block_size).
 // A -1 block entry means "not mapped" (section 9.3.1): nothing is written.
+// An explicit slot_mapping (section 5.2) replaces the derivation for the
+// write (-1 = no write); the block table still defines what is read.
 // K is rotated before it is stored (section 7.2 / 12.5: the cache holds the
 // already-rotated K); Q is rotated into a workspace for the attention kernels.
 //
@@ -206,18 +208,30 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     return;
   }
 
-  const int row = pos / p.bs;
-  if (row >= p.MB) {
-    if (lane == 0) atomicOr(p.err, PA_DEVERR_KV_BOUND);
-    return;
+  size_t slot;
+  if (p.slot_mapping) {
+    // explicit slot (section 5.2): authoritative, -1 = no write
+    const int s = __ldg(p.slot_mapping + t);
+    if (s == -1) return;
+    if (s < -1 || (long long)s >= (long long)p.NB * p.bs) {
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_SLOT);
+      return;
+    }
+    slot = (size_t)s;
+  } else {
+    const int row = pos / p.bs;
+    if (row >= p.MB) {
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_KV_BOUND);
+      return;
+    }
+    const int blk = __ldg(p.block_table + (size_t)b * p.MB + row);
+    if (blk == -1) return;  // not mapped: no write
+    if (blk < -1 || blk >= p.NB) {
+      if (lane == 0) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+      return;
+    }
+    slot = (size_t)blk * p.bs + (pos & (p.bs - 1));
   }
-  const int blk = __ldg(p.block_table + (size_t)b * p.MB + row);
-  if (blk == -1) return;  // not mapped: no write
-  if (blk < -1 || blk >= p.NB) {
-    if (lane == 0) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
-    return;
-  }
-  const size_t slot = (size_t)blk * p.bs + (pos & (p.bs - 1));
   const size_t kv_row = (size_t)p.Hk * p.D;
   if (p.cache_type == kCacheF16) {
     row_transform(p.key + (size_t)t * kv_row, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},

@@ -106,6 +106,7 @@ struct CacheWriteParams {
   int per_channel;      // scales [Hk*D] (1) or [1] (0)
   const float* k_scale; // 8-bit caches: quantization / dequantization scales
   const float* v_scale;
+  const int* slot_mapping;  // [T] explicit write slots (-1 = no write) or null
   const int* block_table;
   const int* cum;
   const int* past;

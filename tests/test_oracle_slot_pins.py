@@ -10,7 +10,7 @@ sections 5.2 and 9.3), each against something other than the oracle:
   * ring buffer: a sequence held in N = ceil(W / bs) + 1 recycled blocks,
     table entries below the live range -1, gives the same attention as the
     full cache with the same window, over several decode steps (section
-    9.3.5); W >= L with recycling disabled equals full attention
+    9.3.5); with W >= L the ring never recycles and equals full attention
 """
 
 import math
