@@ -69,6 +69,8 @@ def lib():
             L.oracle_attention_ex.argtypes = [P, P, P, I, P, P, I, P, P, I, P, P, I, I, I, I, I, I, I,
                                               Dd, Dd, I, LL, LL, P]
             L.oracle_attention_ex.restype = I
+            L.oracle_qk_norm.argtypes = [P, P, I, I, I, P, ctypes.c_float]
+            L.oracle_qk_norm.restype = I
             _lib = L
     return _lib
 
@@ -121,6 +123,23 @@ def quantize(bits: np.ndarray, scale: float, cache_dtype: int) -> np.ndarray:
     f = np.vectorize(lambda h: lib().oracle_quantize(int(h), float(scale), int(cache_dtype)),
                      otypes=[np.uint8])
     return f(np.asarray(bits, dtype=np.uint16))
+
+
+def qk_norm(x, nheads, head_size, weight, eps):
+    """Per-head RMS-normalized copy of x ([T, nheads*D] fp16 bits)."""
+    xa = _np(x, np.uint16)
+    wa = _np(weight, np.uint16)
+    y = np.empty_like(xa)
+    _check(lib().oracle_qk_norm(_p(xa), _p(y), xa.shape[0], nheads, head_size, _p(wa), float(eps)), "qk_norm")
+    return y
+
+
+def split_packed_qkv(query, num_heads, kv_num_heads, head_size):
+    """(q, k, v) views of packed rows [T, (H + 2*Hk) * D] (fp16 bits)."""
+    qa = _np(query, np.uint16)
+    H, Hk, D = num_heads, kv_num_heads, head_size
+    return (np.ascontiguousarray(qa[:, :H * D]), np.ascontiguousarray(qa[:, H * D:(H + Hk) * D]),
+            np.ascontiguousarray(qa[:, (H + Hk) * D:]))
 
 
 def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
@@ -241,8 +260,14 @@ def forward(step, threads=None, rows=None):
     """
     H, Hk, D = step["num_heads"], step["kv_num_heads"], step["head_size"]
     cum, past = step["cumulative_sequence_lengths"], step["past_sequence_lengths"]
-    q = _np(step["query"], np.uint16)
-    k = _np(step["key"], np.uint16)
+    if step.get("key") is None:  # packed QKV rows
+        q, k, v = split_packed_qkv(step["query"], H, Hk, D)
+    else:
+        q, k, v = _np(step["query"], np.uint16), _np(step["key"], np.uint16), _np(step["value"], np.uint16)
+    if step.get("q_norm_weight") is not None:
+        eps = step.get("qk_norm_epsilon", 1e-6)
+        q = qk_norm(q, H, D, step["q_norm_weight"], eps)
+        k = qk_norm(k, Hk, D, step["k_norm_weight"], eps)
     if step["do_rotary"]:
         q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D,
                    step["rotary_interleaved"])
@@ -251,7 +276,7 @@ def forward(step, threads=None, rows=None):
     cdt = step.get("cache_dtype", CACHE_FP16)
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)
-    kc, vc = cache_write(k, step["value"], step["key_cache"], step["value_cache"],
+    kc, vc = cache_write(k, v, step["key_cache"], step["value_cache"],
                          step["block_table"], cum, past, Hk, D, step["block_size"],
                          slot_mapping=step.get("slot_mapping"), **quant)
     out = attention(q, kc, vc, step["block_table"], cum, past, H, Hk, D,
