@@ -60,6 +60,16 @@
  * head_sink (section 6) is an optional fp16 [H]: one extra logit per query
  * head that enters the softmax denominator only.  Both arrive through
  * pa_extra_inputs (pa_cache_write_ex / pa_forward_ex).
+ *
+ * Packed QKV (section 4): with packed_qkv the query argument holds rows
+ * [T, (H + 2*Hk)*D] = [Q heads | K heads | V heads] and key / value are NULL.
+ * QK-Norm (section 7): with qk_norm every head of Q and K is replaced, before
+ * rotary and before K is cached, by
+ *   y[c] = fp16((x[c] * r) * w[c]),  r = 1 / sqrt(sum_j x[j]^2 / D + eps),
+ * w = q_norm_weight / k_norm_weight ([D] fp16, shared by all heads); the
+ * fp32 sum of squares runs in a fixed order (channel c in partial c mod 32,
+ * partials combined by an xor butterfly 16, 8, 4, 2, 1), IEEE square root
+ * and reciprocal, so the cached K is bit-reproducible.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -130,11 +140,14 @@ typedef struct {
   int cache_dtype;         /* PA_CACHE_*: element type of key_cache / value_cache */
   int k_quant_type;        /* PA_QUANT_*: NONE for fp16 caches, else PER_TENSOR / PER_CHANNEL */
   int v_quant_type;        /* must equal k_quant_type */
+  int packed_qkv;          /* 1: pa_forward's query rows are [Q heads | K heads | V heads], key/value NULL */
+  int qk_norm;             /* 1: QK-Norm of Q and K before rotary (q/k_norm_weight required) */
+  float qk_norm_epsilon;   /* > 0 (default 1e-6) */
 } pa_config;
 
 /* Fills *cfg with the attribute defaults (scale 0, softcap 0, window -1,
- * no rotary, bounds 0, fp16 cache).  Geometry fields are set to 0 and must
- * be filled. */
+ * no rotary, bounds 0, fp16 cache, no packed QKV, no QK-Norm, QK-Norm
+ * epsilon 1e-6).  Geometry fields are set to 0 and must be filled. */
 PA_API void pa_config_init(pa_config* cfg);
 
 /* Host-only check of a configuration against the validation rules
@@ -204,6 +217,8 @@ typedef struct {
   const float* k_scale;   /* device fp32, [1] or [Hk*D]; required iff cache_dtype != PA_CACHE_FP16 */
   const float* v_scale;   /* likewise for value_cache */
   const int32_t* slot_mapping; /* [T] int32, device; NULL = derive the write slot from block_table */
+  const void* q_norm_weight;   /* [D] fp16, device; required iff qk_norm (with k_norm_weight) */
+  const void* k_norm_weight;   /* [D] fp16, device */
 } pa_extra_inputs;
 
 /* pa_cache_write with the optional inputs (extra may be NULL).  With an

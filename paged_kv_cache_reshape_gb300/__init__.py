@@ -44,12 +44,14 @@ class pa_config(ctypes.Structure):
         (n, ctypes.c_int) for n in ("local_window_size", "do_rotary", "rotary_interleaved",
                                     "rotary_dim", "max_rotary_positions", "max_batch", "max_tokens",
                                     "max_query_len_bound", "max_kv_len_bound", "cache_dtype",
-                                    "k_quant_type", "v_quant_type")]
+                                    "k_quant_type", "v_quant_type", "packed_qkv", "qk_norm")] + [
+        ("qk_norm_epsilon", ctypes.c_float)]
 
 
 class pa_extra_inputs(ctypes.Structure):
     _fields_ = [("head_sink", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
-                ("slot_mapping", ctypes.c_void_p)]
+                ("slot_mapping", ctypes.c_void_p), ("q_norm_weight", ctypes.c_void_p),
+                ("k_norm_weight", ctypes.c_void_p)]
 
 
 class PAError(RuntimeError):
@@ -115,7 +117,8 @@ def _check(status, handle=None):
 def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_blocks_per_seq,
                 max_batch, max_tokens, scale=0.0, softcap=0.0, local_window_size=-1, do_rotary=0,
                 rotary_interleaved=0, rotary_dim=0, max_rotary_positions=0, max_query_len_bound=0,
-                max_kv_len_bound=0, cache_dtype=0, k_quant_type=0, v_quant_type=0) -> pa_config:
+                max_kv_len_bound=0, cache_dtype=0, k_quant_type=0, v_quant_type=0, packed_qkv=0,
+                qk_norm=0, qk_norm_epsilon=1e-6) -> pa_config:
     c = pa_config()
     lib().pa_config_init(ctypes.byref(c))
     for k, v in dict(num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
@@ -127,7 +130,8 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                      max_rotary_positions=max_rotary_positions,
                      max_query_len_bound=max_query_len_bound,
                      max_kv_len_bound=max_kv_len_bound, cache_dtype=cache_dtype,
-                     k_quant_type=k_quant_type, v_quant_type=v_quant_type).items():
+                     k_quant_type=k_quant_type, v_quant_type=v_quant_type, packed_qkv=packed_qkv,
+                     qk_norm=qk_norm, qk_norm_epsilon=qk_norm_epsilon).items():
         setattr(c, k, v)
     return c
 
@@ -184,10 +188,13 @@ def pa_forward(h, query, key, value, key_cache, value_cache, block_table,
                             ctypes.c_void_p(stream or 0)), h)
 
 
-def _extra(head_sink=None, k_scale=None, v_scale=None, slot_mapping=None):
-    if head_sink is None and k_scale is None and v_scale is None and slot_mapping is None:
+def _extra(head_sink=None, k_scale=None, v_scale=None, slot_mapping=None, q_norm_weight=None,
+           k_norm_weight=None):
+    if all(v is None for v in (head_sink, k_scale, v_scale, slot_mapping, q_norm_weight, k_norm_weight)):
         return None
     x = pa_extra_inputs()
+    x.q_norm_weight = None if q_norm_weight is None else q_norm_weight.data_ptr()
+    x.k_norm_weight = None if k_norm_weight is None else k_norm_weight.data_ptr()
     x.head_sink = None if head_sink is None else head_sink.data_ptr()
     x.k_scale = None if k_scale is None else k_scale.data_ptr()
     x.v_scale = None if v_scale is None else v_scale.data_ptr()
@@ -198,23 +205,25 @@ def _extra(head_sink=None, k_scale=None, v_scale=None, slot_mapping=None):
 def pa_cache_write_ex(h, key, value, key_cache, value_cache, block_table,
                       cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
                       cos_cache=None, sin_cache=None, head_sink=None, k_scale=None, v_scale=None,
-                      slot_mapping=None, stream=None):
+                      slot_mapping=None, q_norm_weight=None, k_norm_weight=None, stream=None):
     _check(lib().pa_cache_write_ex(h, _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache),
                                    _ptr(block_table), _ptr(cumulative_sequence_lengths),
                                    _ptr(past_sequence_lengths), batch, token_count, _ptr(cos_cache),
-                                   _ptr(sin_cache), _extra(head_sink, k_scale, v_scale, slot_mapping),
+                                   _ptr(sin_cache),
+                                   _extra(head_sink, k_scale, v_scale, slot_mapping, q_norm_weight, k_norm_weight),
                                    ctypes.c_void_p(stream or 0)), h)
 
 
 def pa_forward_ex(h, query, key, value, key_cache, value_cache, block_table,
                   cumulative_sequence_lengths, past_sequence_lengths, batch, token_count,
                   cos_cache, sin_cache, output, head_sink=None, k_scale=None, v_scale=None,
-                  slot_mapping=None, stream=None):
+                  slot_mapping=None, q_norm_weight=None, k_norm_weight=None, stream=None):
     _check(lib().pa_forward_ex(h, _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache),
                                _ptr(value_cache), _ptr(block_table),
                                _ptr(cumulative_sequence_lengths), _ptr(past_sequence_lengths),
                                batch, token_count, _ptr(cos_cache), _ptr(sin_cache),
-                               _extra(head_sink, k_scale, v_scale, slot_mapping), _ptr(output),
+                               _extra(head_sink, k_scale, v_scale, slot_mapping, q_norm_weight, k_norm_weight),
+                               _ptr(output),
                                ctypes.c_void_p(stream or 0)), h)
 
 
@@ -275,7 +284,9 @@ class PagedAttention:
                           max_rotary_positions=0 if cos is None else cos.shape[0],
                           cache_dtype=step.get("cache_dtype", 0),
                           k_quant_type=step.get("quant_type", 0), v_quant_type=step.get("quant_type", 0),
-                          **bounds)
+                          packed_qkv=int(step.get("key") is None),
+                          qk_norm=int(step.get("q_norm_weight") is not None),
+                          qk_norm_epsilon=step.get("qk_norm_epsilon", 1e-6), **bounds)
         return cls(cfg)
 
     def forward(self, step: dict, output, stream=None):
@@ -284,7 +295,9 @@ class PagedAttention:
                       step["past_sequence_lengths"], step["batch"], step["token_count"],
                       step.get("cos_cache"), step.get("sin_cache"), output,
                       head_sink=step.get("head_sink"), k_scale=step.get("k_scale"),
-                      v_scale=step.get("v_scale"), slot_mapping=step.get("slot_mapping"), stream=stream)
+                      v_scale=step.get("v_scale"), slot_mapping=step.get("slot_mapping"),
+                      q_norm_weight=step.get("q_norm_weight"), k_norm_weight=step.get("k_norm_weight"),
+                      stream=stream)
 
     def cache_write(self, step: dict, stream=None):
         pa_cache_write_ex(self.handle, step["key"], step["value"], step["key_cache"],
@@ -293,7 +306,8 @@ class PagedAttention:
                           step["batch"], step["token_count"], step.get("cos_cache"),
                           step.get("sin_cache"), head_sink=step.get("head_sink"),
                           k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
-                          slot_mapping=step.get("slot_mapping"), stream=stream)
+                          slot_mapping=step.get("slot_mapping"), q_norm_weight=step.get("q_norm_weight"),
+                          k_norm_weight=step.get("k_norm_weight"), stream=stream)
 
     def set_option(self, option, value):
         pa_set_option(self.handle, option, value)

@@ -176,6 +176,7 @@ void pa_config_init(pa_config* c) {
   if (!c) return;
   memset(c, 0, sizeof(*c));
   c->local_window_size = -1;
+  c->qk_norm_epsilon = 1e-6f;
 }
 
 pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
@@ -255,6 +256,18 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "an 8-bit cache needs k_quant_type and v_quant_type PER_TENSOR or PER_CHANNEL");
     return PA_INVALID_ARGUMENT;
   }
+  if (c->packed_qkv != 0 && c->packed_qkv != 1) {
+    set_msg(msg, len, "packed_qkv must be 0 or 1 (got %d)", c->packed_qkv);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->qk_norm != 0 && c->qk_norm != 1) {
+    set_msg(msg, len, "qk_norm must be 0 or 1 (got %d)", c->qk_norm);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->qk_norm && !(c->qk_norm_epsilon > 0.f && std::isfinite(c->qk_norm_epsilon))) {
+    set_msg(msg, len, "qk_norm_epsilon must be finite and > 0 (got %g)", c->qk_norm_epsilon);
+    return PA_INVALID_ARGUMENT;
+  }
   // Valid, but outside what this build runs.
   if (c->head_size != 64 && c->head_size != 128 && c->head_size != 256) {
     set_msg(msg, len, "head_size %d is valid but this build runs 64, 128 and 256", c->head_size);
@@ -266,6 +279,10 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
   }
   if (c->do_rotary && rot_dim_of(*c) % 16 != 0) {
     set_msg(msg, len, "rotary_dim %d is valid but this build needs a multiple of 16", rot_dim_of(*c));
+    return PA_NOT_SUPPORTED;
+  }
+  if (c->qk_norm && c->kv_num_heads > 32) {
+    set_msg(msg, len, "qk_norm is built for kv_num_heads <= 32 (got %d)", c->kv_num_heads);
     return PA_NOT_SUPPORTED;
   }
   if (c->cache_dtype != PA_CACHE_FP16) {
@@ -303,10 +320,15 @@ pa_status pa_check_step(const pa_config* c, int for_forward, const void* query, 
     set_msg(msg, len, "token_count must be in [0, max_tokens=%d] (got %d)", c->max_tokens, token_count);
     return PA_INVALID_ARGUMENT;
   }
+  const bool packed = for_forward != 0 && c->packed_qkv;
+  if (packed && (key || value)) {
+    set_msg(msg, len, "key and value must be NULL with packed_qkv (the query rows hold Q, K and V)");
+    return PA_INVALID_ARGUMENT;
+  }
   struct { const void* p; const char* name; int align; bool need; } args[] = {
       {query, "query", 16, for_forward != 0 && token_count > 0},
-      {key, "key", 16, token_count > 0},
-      {value, "value", 16, token_count > 0},
+      {key, "key", 16, !packed && token_count > 0},
+      {value, "value", 16, !packed && token_count > 0},
       {key_cache, "key_cache", 16, true},
       {value_cache, "value_cache", 16, true},
       {block_table, "block_table", 4, true},
@@ -404,7 +426,8 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   size_t o_pml = off; off = up(off + sizeof(float2) * h->cap_dec * Hk * pa::kDecodeRows);
   size_t o_po = off; off = up(off + sizeof(float) * h->cap_dec * Hk * pa::kDecodeRows * D);
   size_t o_qr = off;
-  const bool q_copy = c.do_rotary || c.cache_dtype != PA_CACHE_FP16;  // rotated and/or times k_scale
+  // rotated, normalized, unpacked and/or times k_scale
+  const bool q_copy = c.do_rotary || c.cache_dtype != PA_CACHE_FP16 || c.packed_qkv || c.qk_norm;
   if (q_copy) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * D);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws, h->ws_bytes);
@@ -543,7 +566,7 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.key = static_cast<const __half*>(key);
   p.value = static_cast<const __half*>(value);
   p.query = static_cast<const __half*>(query);
-  p.q_rot = (query && (c.do_rotary || quant)) ? h->q_rot : nullptr;
+  p.q_rot = (query && (c.do_rotary || quant || c.packed_qkv || c.qk_norm)) ? h->q_rot : nullptr;
   p.key_cache = key_cache;
   p.value_cache = value_cache;
   p.cache_type = c.cache_dtype;
@@ -552,6 +575,12 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.v_scale = quant ? x->v_scale : nullptr;
   p.q_scale = (query && quant) ? 1 : 0;
   p.slot_mapping = x->slot_mapping;
+  p.packed = (query && c.packed_qkv) ? 1 : 0;
+  p.q_stride = (p.packed ? c.num_heads + 2 * c.kv_num_heads : c.num_heads) * c.head_size;
+  p.qk_norm = c.qk_norm;
+  p.qk_eps = c.qk_norm_epsilon;
+  p.q_norm_w = static_cast<const __half*>(x->q_norm_weight);
+  p.k_norm_w = static_cast<const __half*>(x->k_norm_weight);
   p.block_table = block_table;
   p.cum = cum;
   p.past = past;
@@ -577,7 +606,7 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   return p;
 }
 
-const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr, nullptr};
+const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
 
 // The optional inputs against the configuration: scales exactly for 8-bit
 // caches, element alignment.
@@ -593,6 +622,12 @@ pa_status check_extra(pa_handle h, const pa_extra_inputs* x) {
     return fail(h, PA_INVALID_ARGUMENT, "head_sink must be 2-byte aligned");
   if (reinterpret_cast<uintptr_t>(x->slot_mapping) % 4)
     return fail(h, PA_INVALID_ARGUMENT, "slot_mapping must be 4-byte aligned");
+  if (h->cfg.qk_norm && (!x->q_norm_weight || !x->k_norm_weight))
+    return fail(h, PA_INVALID_ARGUMENT, "q_norm_weight and k_norm_weight are both required with qk_norm");
+  if (!h->cfg.qk_norm && (x->q_norm_weight || x->k_norm_weight))
+    return fail(h, PA_INVALID_ARGUMENT, "q_norm_weight / k_norm_weight given but qk_norm is 0");
+  if ((reinterpret_cast<uintptr_t>(x->q_norm_weight) | reinterpret_cast<uintptr_t>(x->k_norm_weight)) % 16)
+    return fail(h, PA_INVALID_ARGUMENT, "q_norm_weight and k_norm_weight must be 16-byte aligned");
   return PA_OK;
 }
 
@@ -720,7 +755,8 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     if (e != cudaSuccess) return cuda_fail(h, e, "prologue launch");
     h->last_launches++;
   }
-  const __half* q_att = (c.do_rotary || quant) ? h->q_rot : static_cast<const __half*>(query);
+  const __half* q_att = (c.do_rotary || quant || c.packed_qkv || c.qk_norm) ? h->q_rot
+                                                                          : static_cast<const __half*>(query);
   // 3. varlen prefill on tensor memory (skipped when the query-length bound
   // already routes every sequence to the decode kernel)
   if (pre_launch) {
@@ -880,8 +916,9 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   pa_status st = pa_check_step(cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
                                token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
   if (st != PA_OK) return fail(nullptr, st, "%s", msg);
-  if (cfg->cache_dtype != PA_CACHE_FP16)
-    return fail(nullptr, PA_NOT_SUPPORTED, "pa_forward_no_alloc runs fp16 caches; use pa_forward_ex for 8-bit ones");
+  if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->packed_qkv || cfg->qk_norm)
+    return fail(nullptr, PA_NOT_SUPPORTED,
+                "pa_forward_no_alloc runs fp16 caches without packed QKV or QK-Norm; use pa_forward_ex");
   if (device_error && reinterpret_cast<uintptr_t>(device_error) % 4)
     return fail(nullptr, PA_INVALID_ARGUMENT, "device_error must be 4-byte aligned");
   if (token_count == 0) return PA_OK;
@@ -982,6 +1019,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   cp.key = static_cast<const __half*>(key);
   cp.value = static_cast<const __half*>(value);
   cp.query = static_cast<const __half*>(query);
+  cp.q_stride = H * D;
   cp.q_rot = q_rot;
   cp.key_cache = key_cache;
   cp.value_cache = value_cache;

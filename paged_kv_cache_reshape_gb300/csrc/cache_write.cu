@@ -25,6 +25,14 @@
 // [k*D + c] per channel.  The query copy for attention is then multiplied by
 // the K scale (fp32 product rounded to fp16), which folds the K
 // dequantization into Q (section 8.5 phase 3).
+//
+// QK-Norm (section 7, before rotary; the normalized K is what is cached):
+// each head's factor r = 1 / sqrt(sum x^2 / D + eps) is reduced by the warp
+// in a fixed order (channel c accumulates in lane c mod 32, k ascending,
+// then an xor butterfly 16, 8, 4, 2, 1; no fused multiply-add; IEEE square
+// root and reciprocal), and every loaded channel becomes fp16((x * r) * w).
+// Packed QKV rows (section 4) are read in place: Q, K and V heads of token
+// t start at t*(H+2Hk)*D, + H*D and + (H+Hk)*D.
 #include "step.h"
 #include "worklist.cuh"
 #include "../../include/pa.h"
@@ -96,18 +104,49 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
   }
 };
 
+// QK-Norm factors of the nheads heads of one row (all lanes return, lane 0
+// stores rn[h]); the fixed reduction order stated at the top of the file.
+__device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, float eps, float* rn, int lane) {
+  for (int h = 0; h < nheads; ++h) {
+    float acc = 0.f;
+    for (int c = lane; c < D; c += 32) {
+      const float x = __half2float(__ldg(src + (size_t)h * D + c));
+      acc = __fadd_rn(acc, __fmul_rn(x, x));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    const float v = __fadd_rn(__fmul_rn(acc, 1.f / (float)D), eps);
+    if (lane == 0) rn[h] = __frcp_rn(__fsqrt_rn(v));
+  }
+  __syncwarp();
+}
+
 // Copies (rotate = false) or rotates one [nheads, D] row of src and hands
-// every 8-channel group to `emit`.  R % 16 == 0 is checked on the host.
+// every 8-channel group to `emit`.  With rn (QK-Norm factors per head) and
+// nw (the [D] weight), every loaded value is first normalized.  R % 16 == 0
+// is checked on the host.
 template <typename Emit>
 __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
-                              int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane) {
+                              int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
+                              const float* rn = nullptr, const __half* nw = nullptr) {
   const int chunks_per_head = D / 8;
+  auto ld8 = [&](int h, int ch) -> Vec8 {
+    Vec8 v;
+    v.u = __ldg(reinterpret_cast<const uint4*>(src + (size_t)h * D + ch));
+    if (rn) {
+      const float r = rn[h];
+      Vec8 w;
+      w.u = __ldg(reinterpret_cast<const uint4*>(nw + ch));
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        v.h[e] = __float2half_rn(__fmul_rn(__fmul_rn(__half2float(v.h[e]), r), __half2float(w.h[e])));
+    }
+    return v;
+  };
   if (!rotate) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
-      Vec8 v;
-      v.u = __ldg(s4 + i);
-      emit(i / chunks_per_head, 8 * (i % chunks_per_head), v);
+      const int h = i / chunks_per_head, ch = 8 * (i % chunks_per_head);
+      emit(h, ch, ld8(h, ch));
     }
     return;
   }
@@ -119,11 +158,8 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
     const int per_head = pairs + copies;
     for (int i = lane; i < nheads * per_head; i += 32) {
       int h = i / per_head, c = i % per_head;
-      const __half* sh = src + (size_t)h * D;
       if (c < pairs) {
-        Vec8 a, b, cs, sn, ya, yb;
-        a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
-        b.u = __ldg(reinterpret_cast<const uint4*>(sh + half + 8 * c));
+        Vec8 a = ld8(h, 8 * c), b = ld8(h, half + 8 * c), cs, sn, ya, yb;
         cs.u = __ldg(reinterpret_cast<const uint4*>(cos_row + 8 * c));
         sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
 #pragma unroll
@@ -132,9 +168,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
         emit(h, half + 8 * c, yb);
       } else {
         int ch = R + 8 * (c - pairs);
-        Vec8 v;
-        v.u = __ldg(reinterpret_cast<const uint4*>(sh + ch));
-        emit(h, ch, v);
+        emit(h, ch, ld8(h, ch));
       }
     }
   } else {
@@ -142,9 +176,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
     const int rchunks = R / 8;
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       int h = i / chunks_per_head, c = i % chunks_per_head;
-      const __half* sh = src + (size_t)h * D;
-      Vec8 a, y;
-      a.u = __ldg(reinterpret_cast<const uint4*>(sh + 8 * c));
+      Vec8 a = ld8(h, 8 * c), y;
       if (c < rchunks) {
         uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * c));
         uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * c));
@@ -166,7 +198,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
 // into the rotated-query workspace (only with rotary in pa_forward).  `cum`
 // is the cumulative length array, either the caller's (global) or a
 // shared-memory copy.
-__device__ void write_token(const CacheWriteParams& p, const int* cum, int t, int part, int lane) {
+__device__ void write_token(const CacheWriteParams& p, const int* cum, int t, int part, int lane, float* rn) {
   // Owner sequence: largest b with cum[b] <= t.
   int lo = 0, hi = p.batch;
   while (hi - lo > 1) {
@@ -198,13 +230,19 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   if (part > 0) {
     const int h0 = (part - 1) * p.q_heads_per_part;
     const int nh = min(p.q_heads_per_part, p.H - h0);
+    const __half* qsrc = p.query + (size_t)t * p.q_stride + (size_t)h0 * p.D;
     const size_t qoff = ((size_t)t * p.H + h0) * p.D;
+    const float* qrn = nullptr;
+    if (p.qk_norm) {
+      norm_factors(qsrc, nh, p.D, p.qk_eps, rn, lane);
+      qrn = rn;
+    }
     if (p.q_scale)
-      row_transform(p.query + qoff, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale},
-                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
+      row_transform(qsrc, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale},
+                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, qrn, p.q_norm_w);
     else
-      row_transform(p.query + qoff, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
-                    cos_row, sin_row, lane);
+      row_transform(qsrc, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
+                    cos_row, sin_row, lane, qrn, p.q_norm_w);
     return;
   }
 
@@ -233,18 +271,25 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     slot = (size_t)blk * p.bs + (pos & (p.bs - 1));
   }
   const size_t kv_row = (size_t)p.Hk * p.D;
+  const __half* ksrc = p.packed ? p.query + (size_t)t * p.q_stride + (size_t)p.H * p.D : p.key + (size_t)t * kv_row;
+  const __half* vsrc =
+      p.packed ? p.query + (size_t)t * p.q_stride + (size_t)(p.H + p.Hk) * p.D : p.value + (size_t)t * kv_row;
+  const float* krn = nullptr;
+  if (p.qk_norm) {
+    norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane);
+    krn = rn;
+  }
   if (p.cache_type == kCacheF16) {
-    row_transform(p.key + (size_t)t * kv_row, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},
-                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
-    row_transform(p.value + (size_t)t * kv_row,
-                  EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false, 0, 0,
-                  nullptr, nullptr, lane);
+    row_transform(ksrc, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w);
+    row_transform(vsrc, EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false, 0,
+                  0, nullptr, nullptr, lane);
   } else {
-    row_transform(p.key + (size_t)t * kv_row,
+    row_transform(ksrc,
                   EmitCode{static_cast<uint8_t*>(p.key_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
                            p.k_scale},
-                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane);
-    row_transform(p.value + (size_t)t * kv_row,
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w);
+    row_transform(vsrc,
                   EmitCode{static_cast<uint8_t*>(p.value_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
                            p.v_scale},
                   p.Hk, p.D, false, 0, 0, nullptr, nullptr, lane);
@@ -262,11 +307,17 @@ __device__ const int* stage_cum(const CacheWriteParams& p, int* cum_s) {
   return cum_s;
 }
 
+// QK-Norm factors: one slot per head of a warp's row (kv_num_heads <= 32
+// is checked on the host when QK-Norm is on).
+constexpr int kMaxNormHeads = 32;
+
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheWriteParams p) {
   __shared__ int cum_s[kCumCache];
+  __shared__ float rn_s[kWarpsPerBlock][kMaxNormHeads];
   const int* cum = stage_cum(p, cum_s);
   const int w = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (w < p.token_count * p.parts) write_token(p, cum, w / p.parts, w % p.parts, threadIdx.x & 31);
+  if (w < p.token_count * p.parts)
+    write_token(p, cum, w / p.parts, w % p.parts, threadIdx.x & 31, rn_s[threadIdx.x >> 5]);
 }
 
 // The step's prologue in one launch: CTA 0 builds the work list while the
@@ -283,9 +334,11 @@ __global__ void __launch_bounds__(worklist::kThreads, 1) prologue_kernel(Worklis
     return;
   }
   __shared__ int cum_s[kCumCache];
+  __shared__ float rn_s[kPrologueWarps][kMaxNormHeads];
   const int* cum = stage_cum(cp, cum_s);
   const int w = (blockIdx.x - 1) * kPrologueWarps + (threadIdx.x >> 5);
-  if (w < cp.token_count * cp.parts) write_token(cp, cum, w / cp.parts, w % cp.parts, threadIdx.x & 31);
+  if (w < cp.token_count * cp.parts)
+    write_token(cp, cum, w / cp.parts, w % cp.parts, threadIdx.x & 31, rn_s[threadIdx.x >> 5]);
 }
 
 }  // namespace

@@ -107,6 +107,12 @@ struct CacheWriteParams {
   const float* k_scale; // 8-bit caches: quantization / dequantization scales
   const float* v_scale;
   const int* slot_mapping;  // [T] explicit write slots (-1 = no write) or null
+  int packed;               // query rows hold [Q | K | V] (key / value unused)
+  int q_stride;             // elements per query input row: H*D, or (H+2Hk)*D when packed
+  int qk_norm;              // QK-Norm of Q and K before rotary
+  float qk_eps;
+  const __half* q_norm_w;   // [D]
+  const __half* k_norm_w;   // [D]
   const int* block_table;
   const int* cum;
   const int* past;

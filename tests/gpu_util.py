@@ -42,7 +42,8 @@ def run(step, options=(), max_batch=None, max_tokens=None, **bounds):
     op = pa.PagedAttention.for_step(step, max_batch=max_batch, max_tokens=max_tokens, **bounds)
     for k, v in options:
         op.set_option(k, v)
-    out = torch.full_like(step["query"], float("nan"))
+    out = torch.full((step["token_count"], step["num_heads"] * step["head_size"]), float("nan"),
+                     dtype=torch.float16, device=step["query"].device)
     op.forward(step, out)
     torch.cuda.synchronize()
     err = op.device_error()

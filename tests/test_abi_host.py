@@ -94,6 +94,27 @@ def test_quantized_cache_rules(over, status, word):
     assert st == status and word in msg, (st, msg)
 
 
+@pytest.mark.parametrize("over,status,word", [
+    (dict(packed_qkv=2), pa.PA_INVALID_ARGUMENT, "packed_qkv"),
+    (dict(qk_norm=3), pa.PA_INVALID_ARGUMENT, "qk_norm"),
+    (dict(qk_norm=1, qk_norm_epsilon=0.0), pa.PA_INVALID_ARGUMENT, "qk_norm_epsilon"),
+    (dict(qk_norm=1, qk_norm_epsilon=-1e-6), pa.PA_INVALID_ARGUMENT, "qk_norm_epsilon"),
+    (dict(qk_norm=1, num_heads=64, kv_num_heads=64), pa.PA_NOT_SUPPORTED, "kv_num_heads <= 32"),
+])
+def test_packed_and_qk_norm_rules(over, status, word):
+    st, msg = pa.pa_validate_config(good(**over))
+    assert st == status and word in msg, (st, msg)
+
+
+def test_packed_qkv_wants_no_key_or_value():
+    cfg = good(packed_qkv=1)
+    st, msg = pa.pa_check_step(cfg, **step_args())
+    assert st == pa.PA_INVALID_ARGUMENT and "packed_qkv" in msg, msg
+    assert pa.pa_check_step(cfg, **step_args(key=None, value=None))[0] == pa.PA_OK
+    # the cache write alone still takes key and value
+    assert pa.pa_check_step(cfg, **step_args(for_forward=0, query=None, output=None))[0] == pa.PA_OK
+
+
 def test_quantized_decode_config_passes():
     for cdt in (pa.PA_CACHE_INT8, pa.PA_CACHE_FP8_E4M3):
         for qt in (pa.PA_QUANT_PER_TENSOR, pa.PA_QUANT_PER_CHANNEL):

@@ -141,14 +141,16 @@ QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL = 0, 1, 2
 
 def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
               cache_dtype: int = CACHE_FP16, quant_type: int = QUANT_NONE,
-              head_sink: bool = False):
+              head_sink: bool = False, qk_norm: bool = False, packed_qkv: bool = False):
     """Build every input tensor of one step on `device`.
 
     Random values are drawn with a torch.Generator on `gen_device` (default:
     `device`), so a CPU run and a CUDA run of the same shape share lengths
     and block tables (drawn on the CPU) but not necessarily values.
     cache_dtype / quant_type select 8-bit pools with their scales; head_sink
-    adds a per-head sink input.
+    adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16,
+    1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
+    query tensor with key and value None.
     """
     gen_device = gen_device or str(device)
     H, Hk, D, bs = shape.num_heads, shape.kv_num_heads, shape.head_size, shape.block_size
@@ -244,6 +246,14 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     if head_sink:
         hg = torch.Generator().manual_seed(5000 + shape.seed)
         out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).half().to(device))
+    if qk_norm:
+        ng = torch.Generator().manual_seed(6000 + shape.seed)
+        out.update(q_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).half().to(device),
+                   k_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).half().to(device),
+                   qk_norm_epsilon=1e-6)
+    if packed_qkv:
+        out.update(query=torch.cat([out["query"], out["key"], out["value"]], dim=1).contiguous(),
+                   key=None, value=None)
     return out
 
 
