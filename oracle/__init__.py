@@ -71,6 +71,10 @@ def lib():
             L.oracle_attention_ex.restype = I
             L.oracle_qk_norm.argtypes = [P, P, I, I, I, P, ctypes.c_float]
             L.oracle_qk_norm.restype = I
+            L.oracle_rotary_offset.argtypes = [P, P, I, I, I, P, P, I, P, P, I, I, I, I]
+            L.oracle_rotary_offset.restype = I
+            L.oracle_attention_latent.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, Dd, Dd, I, LL, LL, P]
+            L.oracle_attention_latent.restype = I
             _lib = L
     return _lib
 
@@ -142,18 +146,52 @@ def split_packed_qkv(query, num_heads, kv_num_heads, head_size):
             np.ascontiguousarray(qa[:, (H + Hk) * D:]))
 
 
-def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved):
-    """Rotated copy of x ([T, nheads*D] fp16 bits) at positions past_b + j."""
+def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved, offset=0):
+    """Rotated copy of x ([T, nheads*D] fp16 bits) at positions past_b + j;
+    the rotated channels are [offset, offset + 2 * cos_cache.shape[1])."""
     xa = _np(x, np.uint16)
     cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
     cos_a, sin_a = _np(cos_cache, np.uint16), _np(sin_cache, np.uint16)
     T = xa.shape[0]
     y = np.empty_like(xa)
-    st = lib().oracle_rotary(_p(xa), _p(y), T, nheads, head_size, _p(cum_a), _p(past_a),
-                             past_a.shape[0], _p(cos_a), _p(sin_a), cos_a.shape[1],
-                             cos_a.shape[0], interleaved)
+    st = lib().oracle_rotary_offset(_p(xa), _p(y), T, nheads, head_size, _p(cum_a), _p(past_a),
+                                    past_a.shape[0], _p(cos_a), _p(sin_a), cos_a.shape[1],
+                                    cos_a.shape[0], interleaved, int(offset))
     _check(st, "rotary")
     return y
+
+
+def attention_latent(query, latent_cache, block_table, cum, past, num_heads, head_size, v_head_size,
+                     block_size, scale, softcap, window, rows=None, threads=None):
+    """fp64 absorbed latent attention ([T, H, Dv], or [len(rows), Dv])."""
+    qa = _np(query, np.uint16)
+    lc = _np(latent_cache, np.uint16)
+    bt = _np(block_table, np.int32)
+    cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
+    T, H, D, Dv = qa.shape[0], num_heads, head_size, v_head_size
+    B, MB, NB = past_a.shape[0], bt.shape[1], lc.shape[0]
+    L = lib()
+
+    def run(r0, r1, out):
+        st = L.oracle_attention_latent(_p(qa), _p(lc), _p(bt), MB, _p(cum_a), _p(past_a), B, T, H, D, Dv,
+                                       block_size, NB, float(scale), float(softcap), int(window), r0, r1,
+                                       _p(out))
+        _check(st, "attention_latent")
+
+    threads = threads or 1
+    if rows is None:
+        n = T * H
+        out = np.zeros((n, Dv), dtype=np.float64)
+        bounds = np.linspace(0, n, max(1, min(threads, n)) + 1).astype(np.int64)
+        with ThreadPoolExecutor(max(1, threads)) as ex:
+            list(ex.map(lambda i: run(int(bounds[i]), int(bounds[i + 1]), out[bounds[i]:bounds[i + 1]]),
+                        range(len(bounds) - 1)))
+        return out.reshape(T, H, Dv)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.zeros((rows.shape[0], Dv), dtype=np.float64)
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        list(ex.map(lambda i: run(int(rows[i]), int(rows[i]) + 1, out[i:i + 1]), range(rows.shape[0])))
+    return out
 
 
 def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
@@ -260,6 +298,18 @@ def forward(step, threads=None, rows=None):
     """
     H, Hk, D = step["num_heads"], step["kv_num_heads"], step["head_size"]
     cum, past = step["cumulative_sequence_lengths"], step["past_sequence_lengths"]
+    if step.get("kv_cache_layout", 0) == 1:  # one latent cache (CUDA design section 12)
+        q, k = _np(step["query"], np.uint16), _np(step["key"], np.uint16)
+        if step["do_rotary"]:
+            off = step.get("rotary_offset", 0)
+            q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D, step["rotary_interleaved"], off)
+            k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], 1, D, step["rotary_interleaved"], off)
+        kc, _ = cache_write(k, k, step["key_cache"], step["key_cache"], step["block_table"], cum, past, 1, D,
+                            step["block_size"], slot_mapping=step.get("slot_mapping"))
+        out = attention_latent(q, kc, step["block_table"], cum, past, H, D, step["v_head_size"],
+                               step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
+                               rows=rows, threads=threads)
+        return dict(query_rot=q, key_rot=k, key_cache=kc, value_cache=None, out=out)
     if step.get("key") is None:  # packed QKV rows
         q, k, v = split_packed_qkv(step["query"], H, Hk, D)
     else:

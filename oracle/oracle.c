@@ -26,6 +26,9 @@
  *     RMS normalization of Q and K, before rotary, the normalized K cached)
  *     and section 4 (packed QKV: query rows [Q heads | K heads | V heads]
  *     when key and value are absent);
+ *   - "PagedAttention - CUDA Design Document" section 12 (multi-head latent
+ *     attention: one cache of latent rows, V = their first v_head_size
+ *     channels, rotary over channels [rotary_offset, rotary_offset + R));
  *   - "PagedAttention - CUDA Design Document" section 8 (quantized cache:
  *     int8 or float8 e4m3fn codes, symmetric, dequantized as code * scale,
  *     PER_TENSOR scale [1] or PER_CHANNEL scale [kv_num_heads * head_size],
@@ -205,13 +208,30 @@ static int check_lengths(const int32_t* cum, const int32_t* past, int B, int T) 
  * half_rot = cos_cache.shape[1], so rotary_dim R = 2*half_rot; channels
  * >= R are copied.  interleaved = 0 pairs (i, i + R/2), interleaved = 1
  * pairs (2i, 2i + 1). */
+int oracle_rotary_offset(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
+                         const int32_t* cum, const int32_t* past, int B,
+                         const uint16_t* cos_cache, const uint16_t* sin_cache,
+                         int half_rot, int max_position, int interleaved, int offset);
+
+/* Rotary at channel offset 0 (the common case). */
 int oracle_rotary(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
                   const int32_t* cum, const int32_t* past, int B,
                   const uint16_t* cos_cache, const uint16_t* sin_cache,
                   int half_rot, int max_position, int interleaved) {
+  return oracle_rotary_offset(x, y, T, nheads, D, cum, past, B, cos_cache, sin_cache, half_rot, max_position,
+                              interleaved, 0);
+}
+
+/* Rotary over channels [offset, offset + 2*half_rot) of every head (CUDA
+ * design section 12.5, rotary_offset; the pairs are taken inside that
+ * range), every other channel copied. */
+int oracle_rotary_offset(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
+                         const int32_t* cum, const int32_t* past, int B,
+                         const uint16_t* cos_cache, const uint16_t* sin_cache,
+                         int half_rot, int max_position, int interleaved, int offset) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
-  if (2 * half_rot > D || half_rot < 0) return ORACLE_BAD_ARGUMENT;
+  if (offset < 0 || offset + 2 * half_rot > D || half_rot < 0) return ORACLE_BAD_ARGUMENT;
   for (int t = 0; t < T; ++t) {
     int b = owner_of_row(cum, B, t);
     int pos = past[b] + (t - cum[b]);
@@ -223,8 +243,8 @@ int oracle_rotary(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
       if (D > 1024) return ORACLE_BAD_ARGUMENT;
       memcpy(tmp, xr, sizeof(uint16_t) * D);
       for (int i = 0; i < half_rot; ++i) {
-        int i1 = interleaved ? 2 * i : i;
-        int i2 = interleaved ? 2 * i + 1 : i + half_rot;
+        int i1 = offset + (interleaved ? 2 * i : i);
+        int i2 = offset + (interleaved ? 2 * i + 1 : i + half_rot);
         float x1 = (float)oracle_half_to_double(xr[i1]);
         float x2 = (float)oracle_half_to_double(xr[i2]);
         float c = (float)oracle_half_to_double(cos_cache[(size_t)pos * half_rot + i]);
@@ -464,6 +484,65 @@ int oracle_attention_ex(const uint16_t* query, const void* key_cache,
     }
     if (head_sink) denom += exp(sink - xmax); /* the sink's term: denominator only */
     for (int c = 0; c < D; ++c) o[c] /= denom;
+  }
+  return ORACLE_OK;
+}
+
+/* Absorbed multi-head latent attention (CUDA design section 12): one cache
+ * [NB, bs, 1, D] (D = latent width + rotary width), every query head h of
+ * row t attends with x_p = scale * <q[t,h,0:D], L_p[0:D]> (optionally
+ * softcapped) and the output is the softmax-weighted sum of L_p[0:Dv], the
+ * first Dv channels of the same cached rows.  Masks as oracle_attention_ex.
+ * out holds Dv doubles per row. */
+int oracle_attention_latent(const uint16_t* query, const uint16_t* latent_cache, const int32_t* block_table,
+                            int MB, const int32_t* cum, const int32_t* past, int B, int T, int H, int D, int Dv,
+                            int bs, int NB, double scale, double softcap, int window, long long row_begin,
+                            long long row_end, double* out) {
+  int st = check_lengths(cum, past, B, T);
+  if (st) return st;
+  if (Dv < 1 || Dv > D || D > 1024 || scale <= 0.0) return ORACLE_BAD_ARGUMENT;
+  if (!(window == -1 || window >= 1) || softcap < 0) return ORACLE_BAD_ARGUMENT;
+  if (row_begin < 0 || row_end > (long long)T * H || row_begin > row_end) return ORACLE_BAD_ARGUMENT;
+  double q[1024];
+  for (long long r = row_begin; r < row_end; ++r) {
+    int t = (int)(r / H), h = (int)(r % H);
+    int b = owner_of_row(cum, B, t);
+    int pos = past[b] + (t - cum[b]);
+    int kv_len = pos + 1;
+    int lo = (window >= 1 && kv_len - window > 0) ? kv_len - window : 0;
+    double* o = out + (size_t)(r - row_begin) * Dv;
+    for (int c = 0; c < D; ++c) q[c] = oracle_half_to_double(query[((size_t)t * H + h) * D + c]);
+    for (int c = 0; c < Dv; ++c) o[c] = 0.0;
+    double xmax = -INFINITY;
+    int any = 0;
+    for (int p = lo; p < kv_len; ++p) {
+      if (p / bs >= MB) return ORACLE_BAD_DEVICE_DATA;
+      int blk = block_table[(size_t)b * MB + p / bs];
+      if (blk == -1) continue;
+      if (blk < -1 || blk >= NB) return ORACLE_BAD_DEVICE_DATA;
+      const uint16_t* lr = latent_cache + ((size_t)blk * bs + p % bs) * D;
+      double x = 0.0;
+      for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(lr[c]);
+      x *= scale;
+      if (softcap > 0.0) x = softcap * tanh(x / softcap);
+      if (x > xmax) xmax = x;
+      any = 1;
+    }
+    if (!any) continue;
+    double denom = 0.0;
+    for (int p = lo; p < kv_len; ++p) {
+      int blk = block_table[(size_t)b * MB + p / bs];
+      if (blk == -1) continue;
+      const uint16_t* lr = latent_cache + ((size_t)blk * bs + p % bs) * D;
+      double x = 0.0;
+      for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(lr[c]);
+      x *= scale;
+      if (softcap > 0.0) x = softcap * tanh(x / softcap);
+      double w = exp(x - xmax);
+      denom += w;
+      for (int c = 0; c < Dv; ++c) o[c] += w * oracle_half_to_double(lr[c]);
+    }
+    for (int c = 0; c < Dv; ++c) o[c] /= denom;
   }
   return ORACLE_OK;
 }

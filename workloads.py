@@ -141,7 +141,8 @@ QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL = 0, 1, 2
 
 def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
               cache_dtype: int = CACHE_FP16, quant_type: int = QUANT_NONE,
-              head_sink: bool = False, qk_norm: bool = False, packed_qkv: bool = False):
+              head_sink: bool = False, qk_norm: bool = False, packed_qkv: bool = False,
+              latent_v_head_size: int = 0):
     """Build every input tensor of one step on `device`.
 
     Random values are drawn with a torch.Generator on `gen_device` (default:
@@ -150,7 +151,11 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     cache_dtype / quant_type select 8-bit pools with their scales; head_sink
     adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16,
     1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
-    query tensor with key and value None.
+    query tensor with key and value None.  latent_v_head_size > 0 makes a
+    multi-head latent attention step (CUDA design section 12): one kv head,
+    key rows of head_size latent channels, value and value_cache None, V the
+    first latent_v_head_size channels, rotary (if on) over the last
+    rotary_dim channels.
     """
     gen_device = gen_device or str(device)
     H, Hk, D, bs = shape.num_heads, shape.kv_num_heads, shape.head_size, shape.block_size
@@ -254,6 +259,11 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     if packed_qkv:
         out.update(query=torch.cat([out["query"], out["key"], out["value"]], dim=1).contiguous(),
                    key=None, value=None)
+    if latent_v_head_size:
+        if Hk != 1:
+            raise ValueError("a latent cache has one kv head")
+        out.update(value=None, value_cache=None, kv_cache_layout=1, v_head_size=latent_v_head_size,
+                   rotary_offset=(D - (out["rotary_dim"] or 0)) if shape.do_rotary else 0)
     return out
 
 
