@@ -114,6 +114,14 @@ enum {
  * division in fp32 and Q = round to nearest-even saturated to [-128, 127]
  * (int8) or to +-448 (e4m3fn). */
 enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2 };
+/* Cache layout (section 12).  LATENT: one cache key_cache [NB, bs, 1, D] of
+ * latent rows (value and value_cache NULL, kv_num_heads 1); every query
+ * head attends with its D channels and the output is the weighted sum of
+ * the first v_head_size channels of the same rows (absorbed multi-head
+ * latent attention); an explicit scale is required.  Built: D = 576,
+ * v_head_size = 512, num_heads <= 16 or a multiple of 16, one query token
+ * per sequence (max_query_len_bound = 1), fp16 cache; output [T, H*512]. */
+enum { PA_LAYOUT_SEPARATE = 0, PA_LAYOUT_LATENT = 1 };
 /* Scale granularity (section 8.2, k_quant_type / v_quant_type). */
 enum { PA_QUANT_NONE = 0, PA_QUANT_PER_TENSOR = 1, PA_QUANT_PER_CHANNEL = 2 };
 
@@ -143,6 +151,9 @@ typedef struct {
   int packed_qkv;          /* 1: pa_forward's query rows are [Q heads | K heads | V heads], key/value NULL */
   int qk_norm;             /* 1: QK-Norm of Q and K before rotary (q/k_norm_weight required) */
   float qk_norm_epsilon;   /* > 0 (default 1e-6) */
+  int kv_cache_layout;     /* PA_LAYOUT_SEPARATE (key_cache + value_cache) or PA_LAYOUT_LATENT */
+  int v_head_size;         /* 0 => head_size; != head_size only with PA_LAYOUT_LATENT */
+  int rotary_offset;       /* first rotated channel of a head (multiple of 8; latent: v_head_size) */
 } pa_config;
 
 /* Fills *cfg with the attribute defaults (scale 0, softcap 0, window -1,

@@ -30,6 +30,7 @@ PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_S
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 = 0, 1, 2
 PA_QUANT_NONE, PA_QUANT_PER_TENSOR, PA_QUANT_PER_CHANNEL = 0, 1, 2
+PA_LAYOUT_SEPARATE, PA_LAYOUT_LATENT = 0, 1
 
 EXPORTED = ("pa_config_init", "pa_validate_config", "pa_check_step", "pa_create", "pa_cache_write",
             "pa_forward", "pa_check_device_error", "pa_last_error_message", "pa_destroy",
@@ -45,7 +46,8 @@ class pa_config(ctypes.Structure):
                                     "rotary_dim", "max_rotary_positions", "max_batch", "max_tokens",
                                     "max_query_len_bound", "max_kv_len_bound", "cache_dtype",
                                     "k_quant_type", "v_quant_type", "packed_qkv", "qk_norm")] + [
-        ("qk_norm_epsilon", ctypes.c_float)]
+        ("qk_norm_epsilon", ctypes.c_float)] + [
+        (n, ctypes.c_int) for n in ("kv_cache_layout", "v_head_size", "rotary_offset")]
 
 
 class pa_extra_inputs(ctypes.Structure):
@@ -118,7 +120,8 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                 max_batch, max_tokens, scale=0.0, softcap=0.0, local_window_size=-1, do_rotary=0,
                 rotary_interleaved=0, rotary_dim=0, max_rotary_positions=0, max_query_len_bound=0,
                 max_kv_len_bound=0, cache_dtype=0, k_quant_type=0, v_quant_type=0, packed_qkv=0,
-                qk_norm=0, qk_norm_epsilon=1e-6) -> pa_config:
+                qk_norm=0, qk_norm_epsilon=1e-6, kv_cache_layout=0, v_head_size=0,
+                rotary_offset=0) -> pa_config:
     c = pa_config()
     lib().pa_config_init(ctypes.byref(c))
     for k, v in dict(num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
@@ -131,7 +134,8 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                      max_query_len_bound=max_query_len_bound,
                      max_kv_len_bound=max_kv_len_bound, cache_dtype=cache_dtype,
                      k_quant_type=k_quant_type, v_quant_type=v_quant_type, packed_qkv=packed_qkv,
-                     qk_norm=qk_norm, qk_norm_epsilon=qk_norm_epsilon).items():
+                     qk_norm=qk_norm, qk_norm_epsilon=qk_norm_epsilon, kv_cache_layout=kv_cache_layout,
+                     v_head_size=v_head_size, rotary_offset=rotary_offset).items():
         setattr(c, k, v)
     return c
 
@@ -285,6 +289,8 @@ class PagedAttention:
                           cache_dtype=step.get("cache_dtype", 0),
                           k_quant_type=step.get("quant_type", 0), v_quant_type=step.get("quant_type", 0),
                           packed_qkv=int(step.get("key") is None),
+                          kv_cache_layout=step.get("kv_cache_layout", 0), v_head_size=step.get("v_head_size", 0),
+                          rotary_offset=step.get("rotary_offset", 0),
                           qk_norm=int(step.get("q_norm_weight") is not None),
                           qk_norm_epsilon=step.get("qk_norm_epsilon", 1e-6), **bounds)
         return cls(cfg)

@@ -79,6 +79,8 @@ struct pa_handle_s {
   float scale = 0.f;
   int max_q = 0, max_kv = 0;
   int dec_ctas_per_sm = 1, dec_grid = 1;
+  bool latent = false;
+  int groups = 1, dv = 0;  // decode work-list groups (kv heads, or 16-head groups of a latent step), output width
   size_t dec_smem = 0;
   int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
@@ -256,6 +258,43 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "an 8-bit cache needs k_quant_type and v_quant_type PER_TENSOR or PER_CHANNEL");
     return PA_INVALID_ARGUMENT;
   }
+  if (c->kv_cache_layout != PA_LAYOUT_SEPARATE && c->kv_cache_layout != PA_LAYOUT_LATENT) {
+    set_msg(msg, len, "kv_cache_layout must be PA_LAYOUT_SEPARATE or PA_LAYOUT_LATENT (got %d)", c->kv_cache_layout);
+    return PA_INVALID_ARGUMENT;
+  }
+  const bool latent = c->kv_cache_layout == PA_LAYOUT_LATENT;
+  if (c->v_head_size < 0 || c->v_head_size > c->head_size) {
+    set_msg(msg, len, "v_head_size must be in [0, head_size] (got %d)", c->v_head_size);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (!latent && c->v_head_size != 0 && c->v_head_size != c->head_size) {
+    set_msg(msg, len, "v_head_size != head_size requires kv_cache_layout LATENT");
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->rotary_offset < 0 || c->rotary_offset % 8 != 0 ||
+      (c->do_rotary && c->rotary_offset + rot_dim_of(*c) > c->head_size)) {
+    set_msg(msg, len, "rotary_offset must be a multiple of 8 with rotary_offset + rotary_dim <= head_size (got %d)",
+            c->rotary_offset);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (latent) {
+    if (c->kv_num_heads != 1) {
+      set_msg(msg, len, "kv_cache_layout LATENT requires kv_num_heads == 1 (got %d)", c->kv_num_heads);
+      return PA_INVALID_ARGUMENT;
+    }
+    if (c->v_head_size != 0 && c->v_head_size != c->head_size && !(c->scale > 0.f)) {
+      set_msg(msg, len, "v_head_size != head_size needs an explicit scale (1/sqrt(head_size) is not the model's)");
+      return PA_INVALID_ARGUMENT;
+    }
+    if (c->qk_norm || c->packed_qkv) {
+      set_msg(msg, len, "kv_cache_layout LATENT takes neither qk_norm nor packed_qkv");
+      return PA_INVALID_ARGUMENT;
+    }
+    if (c->k_quant_type != PA_QUANT_NONE || c->v_quant_type != PA_QUANT_NONE || c->cache_dtype != PA_CACHE_FP16) {
+      set_msg(msg, len, "a quantized latent cache is not built (fp16 only)");
+      return PA_NOT_SUPPORTED;
+    }
+  }
   if (c->packed_qkv != 0 && c->packed_qkv != 1) {
     set_msg(msg, len, "packed_qkv must be 0 or 1 (got %d)", c->packed_qkv);
     return PA_INVALID_ARGUMENT;
@@ -269,6 +308,25 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     return PA_INVALID_ARGUMENT;
   }
   // Valid, but outside what this build runs.
+  if (latent) {
+    const int dv = c->v_head_size ? c->v_head_size : c->head_size;
+    const long long qb =
+        c->max_query_len_bound > 0 ? std::min(c->max_query_len_bound, c->max_tokens) : c->max_tokens;
+    if (c->head_size != 576 || dv != 512) {
+      set_msg(msg, len, "the latent layout is built for head_size 576, v_head_size 512 (got %d, %d)", c->head_size, dv);
+      return PA_NOT_SUPPORTED;
+    }
+    if (c->num_heads > 16 && c->num_heads % 16 != 0) {
+      set_msg(msg, len, "the latent layout is built for num_heads <= 16 or a multiple of 16 (got %d)", c->num_heads);
+      return PA_NOT_SUPPORTED;
+    }
+    if (qb != 1) {
+      set_msg(msg, len, "the latent layout runs decode steps only: max_query_len_bound (else max_tokens) must be 1");
+      return PA_NOT_SUPPORTED;
+    }
+    set_msg(msg, len, "ok");
+    return PA_OK;
+  }
   if (c->head_size != 64 && c->head_size != 128 && c->head_size != 256) {
     set_msg(msg, len, "head_size %d is valid but this build runs 64, 128 and 256", c->head_size);
     return PA_NOT_SUPPORTED;
@@ -321,6 +379,11 @@ pa_status pa_check_step(const pa_config* c, int for_forward, const void* query, 
     return PA_INVALID_ARGUMENT;
   }
   const bool packed = for_forward != 0 && c->packed_qkv;
+  const bool latent = c->kv_cache_layout == PA_LAYOUT_LATENT;
+  if (latent && (value || value_cache)) {
+    set_msg(msg, len, "value and value_cache must be NULL with kv_cache_layout LATENT");
+    return PA_INVALID_ARGUMENT;
+  }
   if (packed && (key || value)) {
     set_msg(msg, len, "key and value must be NULL with packed_qkv (the query rows hold Q, K and V)");
     return PA_INVALID_ARGUMENT;
@@ -328,9 +391,9 @@ pa_status pa_check_step(const pa_config* c, int for_forward, const void* query, 
   struct { const void* p; const char* name; int align; bool need; } args[] = {
       {query, "query", 16, for_forward != 0 && token_count > 0},
       {key, "key", 16, !packed && token_count > 0},
-      {value, "value", 16, !packed && token_count > 0},
+      {value, "value", 16, !packed && !latent && token_count > 0},
       {key_cache, "key_cache", 16, true},
-      {value_cache, "value_cache", 16, true},
+      {value_cache, "value_cache", 16, !latent},
       {block_table, "block_table", 4, true},
       {cum, "cumulative_sequence_lengths", 4, true},
       {past, "past_sequence_lengths", 4, true},
@@ -346,7 +409,7 @@ pa_status pa_check_step(const pa_config* c, int for_forward, const void* query, 
       return PA_INVALID_ARGUMENT;
     }
   }
-  if (key_cache == value_cache) {
+  if (!latent && key_cache == value_cache) {
     set_msg(msg, len, "key_cache and value_cache must be distinct buffers");
     return PA_INVALID_ARGUMENT;
   }
@@ -385,7 +448,12 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaDeviceGetAttribute"); }
   if (!encode_fn()) { delete h; return fail(nullptr, PA_CUDA_ERROR, "cuTensorMapEncodeTiled is unavailable"); }
 
-  h->G = c.num_heads / c.kv_num_heads;
+  h->latent = c.kv_cache_layout == PA_LAYOUT_LATENT;
+  // A latent step works on groups of 16 query heads of one token (rows of a
+  // decode item); the group plays the part of a kv head in the work list.
+  h->G = h->latent ? pa::kDecodeRows : c.num_heads / c.kv_num_heads;
+  h->groups = h->latent ? std::max(1, c.num_heads / pa::kDecodeRows) : c.kv_num_heads;
+  h->dv = h->latent ? 512 : c.head_size;
   h->opt_dec_rows = h->G <= pa::kDecodeRows ? pa::kDecodeRows : 0;  // decode items hold <= 16 rows
   h->R = rot_dim_of(c);
   h->scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)c.head_size);
@@ -393,17 +461,22 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
   h->max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
 
-  e = pa::decode_configure(c.head_size, c.cache_dtype, &h->dec_ctas_per_sm, &h->dec_smem);
+  if (h->latent) {
+    e = pa::mla_configure(&h->dec_smem);
+    h->dec_ctas_per_sm = 1;
+  } else {
+    e = pa::decode_configure(c.head_size, c.cache_dtype, &h->dec_ctas_per_sm, &h->dec_smem);
+  }
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "decode kernel attributes"); }
   size_t psmem = 0;
-  h->prefill_ready = pa::prefill_configure(c.head_size, &psmem) == cudaSuccess;
+  h->prefill_ready = !h->latent && pa::prefill_configure(c.head_size, &psmem) == cudaSuccess;
   cudaGetLastError();
   h->pre_smem = psmem;
 
   h->dec_grid = h->num_sms * h->dec_ctas_per_sm;
-  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads);
+  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->groups - 1) / h->groups);
   // Room for up to 32 items per CTA (the tuning option's maximum).
-  h->cap_dec = std::max(1, (32 * h->dec_grid + c.kv_num_heads - 1) / c.kv_num_heads) + c.max_batch;
+  h->cap_dec = std::max(1, (32 * h->dec_grid + h->groups - 1) / h->groups) + c.max_batch;
   // Prefill work units: unit tokens (the work list's tiles) and the tokens
   // of one 128-row query tile (the Q TMA box).
   h->prefill_tile_tokens = pa::prefill_unit_tokens(c.head_size, h->G);
@@ -415,7 +488,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
 
   // Workspace layout (256-byte aligned pieces).
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
-  const size_t D = c.head_size, Hk = c.kv_num_heads;
+  const size_t D = h->dv, Hk = h->groups;  // split partials: [items, groups or kv heads, 16 rows, output width]
   size_t off = 0;
   size_t o_err = off; off = up(off + 64);
   size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
@@ -428,7 +501,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   size_t o_qr = off;
   // rotated, normalized, unpacked and/or times k_scale
   const bool q_copy = c.do_rotary || c.cache_dtype != PA_CACHE_FP16 || c.packed_qkv || c.qk_norm;
-  if (q_copy) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * D);
+  if (q_copy) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * c.head_size);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws, h->ws_bytes);
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "cudaMalloc(workspace)"); }
@@ -485,7 +558,7 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
     case PA_OPT_DECODE_ITEMS_PER_CTA:
       if (value < 1 || value > 32) return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be in [1, 32]");
       h->opt_items_per_cta = value;
-      h->target_pairs = std::max(1, (value * h->dec_grid + h->cfg.kv_num_heads - 1) / h->cfg.kv_num_heads);
+      h->target_pairs = std::max(1, (value * h->dec_grid + h->groups - 1) / h->groups);
       return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
       if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)
@@ -598,6 +671,7 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.interleaved = c.rotary_interleaved;
   p.rot_dim = h->R;
   p.rot_positions = c.max_rotary_positions;
+  p.rot_offset = c.rotary_offset;
   // Spread a token over several warps when Q is rotated too: one for the
   // K/V rows and one per kv_num_heads query heads (same size as a K row).
   p.q_heads_per_part = c.kv_num_heads;
@@ -622,6 +696,8 @@ pa_status check_extra(pa_handle h, const pa_extra_inputs* x) {
     return fail(h, PA_INVALID_ARGUMENT, "head_sink must be 2-byte aligned");
   if (reinterpret_cast<uintptr_t>(x->slot_mapping) % 4)
     return fail(h, PA_INVALID_ARGUMENT, "slot_mapping must be 4-byte aligned");
+  if (h->cfg.kv_cache_layout == PA_LAYOUT_LATENT && x->head_sink)
+    return fail(h, PA_INVALID_ARGUMENT, "head_sink is not taken with kv_cache_layout LATENT");
   if (h->cfg.qk_norm && (!x->q_norm_weight || !x->k_norm_weight))
     return fail(h, PA_INVALID_ARGUMENT, "q_norm_weight and k_norm_weight are both required with qk_norm");
   if (!h->cfg.qk_norm && (x->q_norm_weight || x->k_norm_weight))
@@ -705,7 +781,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   CUtensorMap tk, tv;
   const int eb = quant ? 1 : 2;
   if (!encode_pool_map(&tk, key_cache, D, c.kv_num_heads, pool_rows, box_rows, eb) ||
-      !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows, eb))
+      (!h->latent && !encode_pool_map(&tv, value_cache, D, c.kv_num_heads, pool_rows, box_rows, eb)))
     return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
 
   // The prefill kernel launches unless the query-length bound already routes
@@ -757,6 +833,58 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   }
   const __half* q_att = (c.do_rotary || quant || c.packed_qkv || c.qk_norm) ? h->q_rot
                                                                           : static_cast<const __half*>(query);
+  if (h->latent) {
+    // 3'. latent decode (one 16-head group of one token per item), then the
+    // log-sum-exp combine of its split partials
+    const int qt = 1;
+    CUtensorMap tq;
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, pa::kDecodeRows, qt))
+      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
+    pa::MlaParams p{};
+    p.out = static_cast<__half*>(output);
+    p.block_table = block_table;
+    p.seq = h->seq;
+    p.dec_items = h->dec_items;
+    p.counters = h->counters;
+    p.part_o = h->part_o;
+    p.part_ml = h->part_ml;
+    p.err = h->err;
+    p.H = c.num_heads;
+    p.groups = h->groups;
+    p.bs = c.block_size;
+    p.MB = c.max_blocks_per_seq;
+    p.NB = c.num_blocks;
+    p.scale = h->scale;
+    p.softcap = c.softcap;
+    p.window = c.local_window_size;
+    p.oob_row = pool_rows;
+    p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
+    {
+      StageTimer t(h, PA_STAGE_DECODE, s);
+      cudaError_t e = pa::launch_mla_decode(tk, tq, p, h->dec_grid, s);
+      if (e != cudaSuccess) return cuda_fail(h, e, "latent decode launch");
+      h->last_launches++;
+    }
+    pa::CombineParams mp{};
+    mp.part_o = h->part_o;
+    mp.part_ml = h->part_ml;
+    mp.seq = h->seq;
+    mp.comb_rows = h->comb_rows;
+    mp.counters = h->counters;
+    mp.out = static_cast<__half*>(output);
+    mp.H = c.num_heads;
+    mp.Hk = h->groups;
+    mp.G = pa::kDecodeRows;
+    mp.D = h->dv;
+    mp.pre_exit = &h->counters->pre_exit;
+    mp.pre_expected = 0;
+    mp.err = h->err;
+    StageTimer t(h, PA_STAGE_COMBINE, s);
+    cudaError_t e = pa::launch_combine(mp, h->comb_grid, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
+    h->last_launches++;
+    return PA_OK;
+  }
   // 3. varlen prefill on tensor memory (skipped when the query-length bound
   // already routes every sequence to the decode kernel)
   if (pre_launch) {

@@ -128,7 +128,7 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
 template <typename Emit>
 __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
                               int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
-                              const float* rn = nullptr, const __half* nw = nullptr) {
+                              const float* rn = nullptr, const __half* nw = nullptr, int off = 0) {
   const int chunks_per_head = D / 8;
   auto ld8 = [&](int h, int ch) -> Vec8 {
     Vec8 v;
@@ -152,34 +152,36 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
   }
   const int half = R / 2;
   if (!interleaved) {
-    // Pair chunks: channels [8c, 8c+8) with [half + 8c, half + 8c + 8).
+    // Pair chunks: channels off + [8c, 8c+8) with off + [half + 8c, half + 8c + 8);
+    // the chunks outside [off, off + R) are copied.
     const int pairs = half / 8;
     const int copies = (D - R) / 8;
     const int per_head = pairs + copies;
     for (int i = lane; i < nheads * per_head; i += 32) {
       int h = i / per_head, c = i % per_head;
       if (c < pairs) {
-        Vec8 a = ld8(h, 8 * c), b = ld8(h, half + 8 * c), cs, sn, ya, yb;
+        Vec8 a = ld8(h, off + 8 * c), b = ld8(h, off + half + 8 * c), cs, sn, ya, yb;
         cs.u = __ldg(reinterpret_cast<const uint4*>(cos_row + 8 * c));
         sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
 #pragma unroll
         for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e]);
-        emit(h, 8 * c, ya);
-        emit(h, half + 8 * c, yb);
+        emit(h, off + 8 * c, ya);
+        emit(h, off + half + 8 * c, yb);
       } else {
-        int ch = R + 8 * (c - pairs);
+        const int cc = 8 * (c - pairs);
+        const int ch = cc < off ? cc : cc + R;
         emit(h, ch, ld8(h, ch));
       }
     }
   } else {
-    // Each 8-channel chunk below R holds four (2i, 2i+1) pairs.
-    const int rchunks = R / 8;
+    // Each 8-channel chunk of [off, off + R) holds four (2i, 2i+1) pairs.
+    const int rchunks = R / 8, c0 = off / 8;
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       int h = i / chunks_per_head, c = i % chunks_per_head;
       Vec8 a = ld8(h, 8 * c), y;
-      if (c < rchunks) {
-        uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * c));
-        uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * c));
+      if (c >= c0 && c < c0 + rchunks) {
+        uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * (c - c0)));
+        uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * (c - c0)));
         const __half* cv = reinterpret_cast<const __half*>(&cu);
         const __half* sv = reinterpret_cast<const __half*>(&su);
 #pragma unroll
@@ -239,10 +241,11 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     }
     if (p.q_scale)
       row_transform(qsrc, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale},
-                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, qrn, p.q_norm_w);
+                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, qrn, p.q_norm_w,
+                    p.rot_offset);
     else
       row_transform(qsrc, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
-                    cos_row, sin_row, lane, qrn, p.q_norm_w);
+                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset);
     return;
   }
 
@@ -281,9 +284,11 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   }
   if (p.cache_type == kCacheF16) {
     row_transform(ksrc, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},
-                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w);
-    row_transform(vsrc, EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false, 0,
-                  0, nullptr, nullptr, lane);
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
+                  p.rot_offset);
+    if (p.value_cache)  // none for a latent cache (V is part of the latent rows)
+      row_transform(vsrc, EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false,
+                    0, 0, nullptr, nullptr, lane);
   } else {
     row_transform(ksrc,
                   EmitCode{static_cast<uint8_t*>(p.key_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,

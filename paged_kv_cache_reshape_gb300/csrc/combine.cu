@@ -125,6 +125,7 @@ cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s) {
     case 64: return launch_pdl(combine_kernel<64>, grid, kWarps * 32, 0, s, p);
     case 128: return launch_pdl(combine_kernel<128>, grid, kWarps * 32, 0, s, p);
     case 256: return launch_pdl(combine_kernel<256>, grid, kWarps * 32, 0, s, p);
+    case 512: return launch_pdl(combine_kernel<512>, grid, kWarps * 32, 0, s, p);
     default: return cudaErrorInvalidValue;
   }
 }

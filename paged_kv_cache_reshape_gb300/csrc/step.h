@@ -121,6 +121,7 @@ struct CacheWriteParams {
   int batch, token_count;
   int H, Hk, D, bs, NB, MB;
   int rotary, interleaved, rot_dim, rot_positions;
+  int rot_offset;        // first rotated channel (latent rows rotate their last rot_dim channels)
   int q_scale;           // 1: the query copy is multiplied by k_scale (8-bit caches)
   int parts;             // warps per token: 1 (K/V) + query parts when Q is transformed
   int q_heads_per_part;  // query heads per query part
@@ -184,6 +185,23 @@ struct PrefillParams {
   int oob_row;
 };
 
+struct MlaParams {
+  __half* out;           // [T, H, 512]
+  const int* block_table;
+  const SeqInfo* seq;
+  const int2* dec_items;
+  Counters* counters;
+  float* part_o;         // [items * groups * 16 * 512]
+  float2* part_ml;       // [items * groups * 16]
+  int* err;
+  int H, groups;         // query heads, groups of 16 heads
+  int bs, MB, NB;
+  float scale, softcap;
+  int window;
+  int oob_row;
+  int log_box_rows;      // log2(min(block_size, 64))
+};
+
 // Launch with the programmatic stream-serialization attribute, so the
 // kernel's CTAs may become resident while the previous kernel on the stream
 // finishes; the kernel calls griddepcontrol.wait before touching its
@@ -211,6 +229,9 @@ cudaError_t decode_configure(int head_size, int cache_type, int* ctas_per_sm, si
 cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
+cudaError_t mla_configure(size_t* smem);
+cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const MlaParams& p, int grid,
+                              cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);
 int prefill_keys_per_tile(int head_size);
 int prefill_unit_tokens(int head_size, int group);  // tokens per prefill work unit

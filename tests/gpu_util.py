@@ -42,7 +42,8 @@ def run(step, options=(), max_batch=None, max_tokens=None, **bounds):
     op = pa.PagedAttention.for_step(step, max_batch=max_batch, max_tokens=max_tokens, **bounds)
     for k, v in options:
         op.set_option(k, v)
-    out = torch.full((step["token_count"], step["num_heads"] * step["head_size"]), float("nan"),
+    width = step.get("v_head_size") or step["head_size"]
+    out = torch.full((step["token_count"], step["num_heads"] * width), float("nan"),
                      dtype=torch.float16, device=step["query"].device)
     op.forward(step, out)
     torch.cuda.synchronize()
@@ -68,8 +69,10 @@ def check_full(step_host, step_dev, out, threads=8):
     """Whole-step parity: both pools bit-exact, every output row within tolerance."""
     ref = oracle.forward(step_host, threads=threads)
     assert np.array_equal(raw(step_dev["key_cache"]), raw(ref["key_cache"])), "key_cache pool differs"
-    assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
-    T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
+    if ref["value_cache"] is not None:
+        assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
+    T, H = step_host["token_count"], step_host["num_heads"]
+    D = step_host.get("v_head_size") or step_host["head_size"]
     return assert_close(out.float().cpu().numpy().reshape(T, H, D), ref["out"])
 
 

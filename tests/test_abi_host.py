@@ -115,6 +115,47 @@ def test_packed_qkv_wants_no_key_or_value():
     assert pa.pa_check_step(cfg, **step_args(for_forward=0, query=None, output=None))[0] == pa.PA_OK
 
 
+def latent(**over):
+    c = pa.make_config(16, 1, 576, 64, 1000, 65, 32, 32, scale=0.07, kv_cache_layout=pa.PA_LAYOUT_LATENT,
+                       v_head_size=512, max_query_len_bound=1)
+    for k, v in over.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("over,status,word", [
+    (dict(kv_cache_layout=2), pa.PA_INVALID_ARGUMENT, "kv_cache_layout"),
+    (dict(kv_num_heads=2), pa.PA_INVALID_ARGUMENT, "kv_num_heads == 1"),
+    (dict(scale=0.0), pa.PA_INVALID_ARGUMENT, "explicit scale"),
+    (dict(v_head_size=600), pa.PA_INVALID_ARGUMENT, "v_head_size"),
+    (dict(qk_norm=1), pa.PA_INVALID_ARGUMENT, "qk_norm"),
+    (dict(rotary_offset=4), pa.PA_INVALID_ARGUMENT, "rotary_offset"),
+    (dict(do_rotary=1, rotary_dim=64, rotary_offset=528, max_rotary_positions=100), pa.PA_INVALID_ARGUMENT,
+     "rotary_offset"),
+    (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=1, v_quant_type=1), pa.PA_NOT_SUPPORTED, "latent"),
+    (dict(head_size=512, v_head_size=448), pa.PA_NOT_SUPPORTED, "576"),
+    (dict(num_heads=24), pa.PA_NOT_SUPPORTED, "multiple of 16"),
+    (dict(max_query_len_bound=2), pa.PA_NOT_SUPPORTED, "decode steps only"),
+])
+def test_latent_rules(over, status, word):
+    st, msg = pa.pa_validate_config(latent(**over))
+    assert st == status and word in msg, (st, msg)
+
+
+def test_latent_config_passes_and_separate_rejects_other_v_width():
+    assert pa.pa_validate_config(latent())[0] == pa.PA_OK
+    assert pa.pa_validate_config(latent(num_heads=128))[0] == pa.PA_OK
+    st, msg = pa.pa_validate_config(good(v_head_size=64))
+    assert st == pa.PA_INVALID_ARGUMENT and "LATENT" in msg
+
+
+def test_latent_step_wants_no_value():
+    cfg = latent()
+    st, msg = pa.pa_check_step(cfg, **step_args())
+    assert st == pa.PA_INVALID_ARGUMENT and "LATENT" in msg
+    assert pa.pa_check_step(cfg, **step_args(value=None, value_cache=None))[0] == pa.PA_OK
+
+
 def test_quantized_decode_config_passes():
     for cdt in (pa.PA_CACHE_INT8, pa.PA_CACHE_FP8_E4M3):
         for qt in (pa.PA_QUANT_PER_TENSOR, pa.PA_QUANT_PER_CHANNEL):
