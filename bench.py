@@ -14,7 +14,9 @@ window 4096 / softcap 50 decode), `rotary_decode` (Llama-70B-shaped decode
 with rotary), `prefill` (16 prompts of 1024 tokens alone), `tiny`,
 `decode_fp8` / `decode_int8` (the default decode step over an e4m3fn / int8
 paged cache with per-channel scales; its K/V bytes count one byte per
-element).
+element), `mla_decode` (DeepSeek-V3-shaped latent decode: 64 sequences,
+128 heads, one 576-channel latent cache, block_size 64, past lengths
+U{512..4096}; its K/V bytes are the latent rows, read once).
 
 value    decode workloads: attended K/V bytes of the step / step time (GB/s),
          each admitted K and V element counted once per kv head; workloads
@@ -62,11 +64,21 @@ DECODE_ROWS = 16  # query rows of one decode item: q_len * G <= 16 goes to the d
 QUANT_WORKLOADS = {"decode_fp8": 2, "decode_int8": 1}
 
 
+MLA_SCALE = 0.0723  # an explicit softmax scale (the latent width is not the model's head width)
+
+
 def workload_shape(name):
+    import torch
+
     import workloads
     index = {"tiny": 0, "decode": 1, "mixed": 2, "long_window": 3, "rotary_decode": 4}
     if name in QUANT_WORKLOADS:
         return workloads.config_shape(1)
+    if name == "mla_decode":
+        g = torch.Generator().manual_seed(3000 + 77)
+        past = torch.randint(512, 4097, (64,), generator=g).tolist()
+        return workloads.custom_shape("deepseek_v3_latent_decode_b64_h128_d576_dv512_bs64", 128, 1, 576, 64, past,
+                                      [1] * 64, scale=MLA_SCALE, do_rotary=1, rotary_dim=64, seed=77)
     if name in index:
         return workloads.config_shape(index[name])
     if name == "prefill":
@@ -79,6 +91,8 @@ def workload_options(name):
     """make_step keywords of a workload (8-bit cache variants)."""
     if name in QUANT_WORKLOADS:
         return dict(cache_dtype=QUANT_WORKLOADS[name], quant_type=2)
+    if name == "mla_decode":
+        return dict(latent_v_head_size=512)
     return {}
 
 
@@ -102,15 +116,22 @@ def work_of(step, seqs=None):
     W, G = step["local_window_size"], step["num_heads"] // step["kv_num_heads"]
     Hk, H, D = step["kv_num_heads"], step["num_heads"], step["head_size"]
     eb = 1 if step.get("cache_dtype", 0) else 2  # bytes per cache element
-    w = dict(kv_bytes=0, dec_kv_bytes=0, dec_qo_bytes=0, pre_flops=0, tokens=0)
+    latent = step.get("kv_cache_layout", 0) == 1
+    Dv = step.get("v_head_size") or D
+    w = dict(kv_bytes=0, dec_kv_bytes=0, dec_qo_bytes=0, pre_flops=0, tokens=0, dec_flops=0)
     for b in (range(len(past)) if seqs is None else seqs):
         if q[b] == 0:
             continue
         L = past[b] + q[b]
-        kv = (min(L, W) if W >= 1 else L) * Hk * D * 2 * eb
+        adm = min(L, W) if W >= 1 else L
+        kv = adm * D * 2 if latent else adm * Hk * D * 2 * eb  # latent rows serve as K and V
         w["kv_bytes"] += kv
         w["tokens"] += q[b]
-        if q[b] * G <= DECODE_ROWS:
+        if latent:
+            w["dec_kv_bytes"] += kv
+            w["dec_qo_bytes"] += q[b] * H * (D + Dv) * 2
+            w["dec_flops"] += 2 * q[b] * H * adm * (D + Dv)
+        elif q[b] * G <= DECODE_ROWS:
             w["dec_kv_bytes"] += kv
             w["dec_qo_bytes"] += 2 * q[b] * H * D * 2
         else:
@@ -228,7 +249,12 @@ def oracle_sample(step, budget_s, start_seq=0):
     b = start_seq
     while True:
         rows = np.arange(int(cum[b]) * H, int(cum[b + 1]) * H, dtype=np.int64)
-        if rows.size:
+        if rows.size and step.get("kv_cache_layout", 0) == 1:
+            oracle.attention_latent(base["query_rot"], base["key_cache"], step["block_table"], cum,
+                                    step["past_sequence_lengths"], H, step["head_size"], step["v_head_size"],
+                                    step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
+                                    rows=rows, threads=cores)
+        elif rows.size:
             oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"], step["block_table"],
                              cum, step["past_sequence_lengths"], H, step["kv_num_heads"], step["head_size"],
                              step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
@@ -296,7 +322,8 @@ def run_ours(args, rank, world, local_rank):
     # Replay-wide bound on query length (the op's attention_metadata): for a
     # decode step it lets the host skip launching the prefill kernel.
     op = pa.PagedAttention.for_step(step, max_query_len_bound=max(qlens))
-    out = torch.empty_like(step["query"])
+    out_width = step["num_heads"] * (step.get("v_head_size") or step["head_size"])
+    out = torch.empty(step["token_count"], out_width, dtype=torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sid = stream.cuda_stream
 
@@ -372,8 +399,16 @@ def run_ours(args, rank, world, local_rank):
         t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
         alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
         ct = {0: "", 1: ", int8", 2: ", e4m3"}[host.get("cache_dtype", 0)]
+        kname = "mla_decode_kernel" if host.get("kv_cache_layout", 0) == 1 else f"decode_kernel<{shape.head_size}{ct}>"
+        if work["dec_flops"]:
+            ach = work["dec_flops"] / (t * 1e-3) / 1e12
+            rooflines["decode_tensor"] = {
+                "bound": "tensor", "kernel": kname, "achieved": ach, "peak": tflops,
+                "peak_kind": f"{peak_kind} bf16 matmul burst (the kernel runs m16n8k16 fp16 HMMA)",
+                "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
+                "algorithmic_flops_per_launch": work["dec_flops"], "launch_ms": t - 1e-9}
         rooflines["decode"] = {
-            "bound": "hbm", "kernel": f"decode_kernel<{shape.head_size}{ct}>", "achieved": alg / (t * 1e-3) / 1e9,
+            "bound": "hbm", "kernel": kname, "achieved": alg / (t * 1e-3) / 1e9,
             "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
             "frac": alg / (t * 1e-3) / 1e9 / hbm,
             "traffic": committed_traffic("decode.cu", shape_name(args.workload, shape)),
@@ -395,7 +430,8 @@ def run_ours(args, rank, world, local_rank):
     dominant = max(rooflines, key=lambda k: rooflines[k]["launch_ms"]) if rooflines else None
 
     # ---- end to end through the C ABI with host buffers
-    names = ["query", "key", "value", "block_table", "cumulative_sequence_lengths", "past_sequence_lengths"]
+    names = [n for n in ("query", "key", "value", "block_table", "cumulative_sequence_lengths",
+                         "past_sequence_lengths") if step.get(n) is not None]
     pinned = {n: step[n].cpu().pin_memory() for n in names}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
@@ -462,7 +498,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "mixed", "long_window", "rotary_decode", "prefill", "tiny"]
-                    + sorted(QUANT_WORKLOADS))
+                    + sorted(QUANT_WORKLOADS) + ["mla_decode"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch pa_forward directly instead of a graph replay")
     ap.add_argument("--ref-budget", type=float, default=12.0, help="seconds of oracle work per sample")

@@ -33,6 +33,8 @@
 // root and reciprocal), and every loaded channel becomes fp16((x * r) * w).
 // Packed QKV rows (section 4) are read in place: Q, K and V heads of token
 // t start at t*(H+2Hk)*D, + H*D and + (H+Hk)*D.
+#include <type_traits>
+
 #include "step.h"
 #include "worklist.cuh"
 #include "../../include/pa.h"
@@ -144,6 +146,14 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
     return v;
   };
   if (!rotate) {
+    if constexpr (std::is_same<Emit, EmitHalf>::value) {
+      if (!rn) {  // plain copy of a contiguous [nheads, D] row
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        uint4* d4 = reinterpret_cast<uint4*>(emit.dst);
+        for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = __ldg(s4 + i);
+        return;
+      }
+    }
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       const int h = i / chunks_per_head, ch = 8 * (i % chunks_per_head);
       emit(h, ch, ld8(h, ch));

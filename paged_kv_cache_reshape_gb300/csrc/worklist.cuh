@@ -185,7 +185,8 @@ __device__ void build_small(const WorklistParams& p) {
   if (b < p.batch) L = read_lens(p, b, &err_bits);
   const long long span = (L.route == kRouteDecode) ? (long long)(L.past + L.q - L.lo) : 0;
   const long long dec_keys = block_sum_ll(span);
-  const long long pre_pairs = block_sum_ll(prefill_pairs(L));
+  // the prefill side of the SM split's cost model (no split: not needed)
+  const long long pre_pairs = p.split_sms >= 2 ? block_sum_ll(prefill_pairs(L)) : 0;
   const int split_keys = split_keys_for(p, dec_keys);
   Int3 cnt{0, 0, 0, 0};
   if (L.route == kRouteDecode) {
@@ -277,7 +278,7 @@ __device__ void build(const WorklistParams& p) {
     }
   }
   const long long dec_keys = block_sum_ll(span);
-  const long long pre_pairs = block_sum_ll(pairs);
+  const long long pre_pairs = p.split_sms >= 2 ? block_sum_ll(pairs) : 0;
   const int split_keys = split_keys_for(p, dec_keys);
 
   // Pass 2: counts and scans; the items are written in pass 3 once the
