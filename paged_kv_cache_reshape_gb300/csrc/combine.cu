@@ -42,7 +42,18 @@ template <int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
   constexpr int kPer = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31;
-  griddep_wait();  // partials and the work list come from the kernels before
+  // The work list (row count, rows, sequence info) is the prologue's, which
+  // had completed before the decode kernel let this grid start: this warp's
+  // first row is read before waiting for the decode kernel's partials.
+  const int n = p.counters->n_comb * p.H;
+  const int first = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  int2 tb0 = make_int2(0, 0);
+  SeqInfo si0{};
+  if (first < n) {
+    tb0 = p.comb_rows[first / p.H];
+    si0 = p.seq[tb0.y];
+  }
+  griddep_wait();  // the partials come from the decode kernel
   // The prefill kernel may still run beside the decode kernel: the step
   // ends only after every prefill CTA has (CTA 0 waits, bounded).
   if (p.pre_expected > 0 && blockIdx.x == 0 && threadIdx.x == 0) {
@@ -52,11 +63,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     if (i == kWaitLimit) atomicOr(p.err, PA_DEVERR_TIMEOUT);
     __threadfence();
   }
-  const int n = p.counters->n_comb * p.H;
-  for (int idx = blockIdx.x * kWarps + (threadIdx.x >> 5); idx < n; idx += gridDim.x * kWarps) {
+  for (int idx = first; idx < n; idx += gridDim.x * kWarps) {
     const int ci = idx / p.H, h = idx - ci * p.H;
-    const int2 tb = p.comb_rows[ci];
-    const SeqInfo si = p.seq[tb.y];
+    const int2 tb = idx == first ? tb0 : p.comb_rows[ci];
+    const SeqInfo si = idx == first ? si0 : p.seq[tb.y];
     const int j = tb.x - si.t0;
     const int k = h / p.G, g = h - k * p.G;
     const int r = j * p.G + g;

@@ -239,22 +239,25 @@ __device__ void build_small(const WorklistParams& p) {
     }
   }
   // Prefill tiles, costliest first (cost ~ the tile's last position, in
-  // 64-key buckets): the same counting sort over every tile of every sequence.
-  __syncthreads();
-  hist[threadIdx.x] = 0;
-  __syncthreads();
-  auto tile_bucket = [&](int s) {
-    const int pos_end = L.past + min((s + 1) * p.prefill_tile_tokens, L.q);
-    return kThreads - 1 - min(kThreads - 1, pos_end / kStageKeys);
-  };
-  for (int s = 0; s < cnt.b; ++s) atomicAdd(&hist[tile_bucket(s)], 1);
-  __syncthreads();
-  const Int3 ppre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
-  __syncthreads();
-  hist[threadIdx.x] = ppre.a;
-  __syncthreads();
-  if (!overflow)
-    for (int s = 0; s < cnt.b; ++s) p.pre_tiles[atomicAdd(&hist[tile_bucket(s)], 1)] = make_int2(b, s);
+  // 64-key buckets): the same counting sort over every tile of every
+  // sequence (skipped by the whole block when no sequence has a tile).
+  if (tot.b > 0) {
+    __syncthreads();
+    hist[threadIdx.x] = 0;
+    __syncthreads();
+    auto tile_bucket = [&](int s) {
+      const int pos_end = L.past + min((s + 1) * p.prefill_tile_tokens, L.q);
+      return kThreads - 1 - min(kThreads - 1, pos_end / kStageKeys);
+    };
+    for (int s = 0; s < cnt.b; ++s) atomicAdd(&hist[tile_bucket(s)], 1);
+    __syncthreads();
+    const Int3 ppre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
+    __syncthreads();
+    hist[threadIdx.x] = ppre.a;
+    __syncthreads();
+    if (!overflow)
+      for (int s = 0; s < cnt.b; ++s) p.pre_tiles[atomicAdd(&hist[tile_bucket(s)], 1)] = make_int2(b, s);
+  }
   if (threadIdx.x == 0) write_counters(p, overflow, tot, split_keys, dec_keys, pre_pairs, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
 }
