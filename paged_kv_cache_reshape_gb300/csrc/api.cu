@@ -81,6 +81,7 @@ struct pa_handle_s {
   int dec_ctas_per_sm = 1, dec_grid = 1;
   bool latent = false;
   int groups = 1, dv = 0;  // decode work-list groups (kv heads, or 16-head groups of a latent step), output width
+  int unit_groups = 1;     // decode CTA work units per (sequence, split)
   size_t dec_smem = 0;
   int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
@@ -474,9 +475,12 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->pre_smem = psmem;
 
   h->dec_grid = h->num_sms * h->dec_ctas_per_sm;
-  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->groups - 1) / h->groups);
+  // decode CTA work units per (sequence, split): kv heads, or the 32-head
+  // groups of a latent step
+  h->unit_groups = h->latent ? pa::mla_item_groups(h->groups) : h->groups;
+  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
   // Room for up to 32 items per CTA (the tuning option's maximum).
-  h->cap_dec = std::max(1, (32 * h->dec_grid + h->groups - 1) / h->groups) + c.max_batch;
+  h->cap_dec = std::max(1, (32 * h->dec_grid + h->unit_groups - 1) / h->unit_groups) + c.max_batch;
   // Prefill work units: unit tokens (the work list's tiles) and the tokens
   // of one 128-row query tile (the Q TMA box).
   h->prefill_tile_tokens = pa::prefill_unit_tokens(c.head_size, h->G);
@@ -558,7 +562,7 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
     case PA_OPT_DECODE_ITEMS_PER_CTA:
       if (value < 1 || value > 32) return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be in [1, 32]");
       h->opt_items_per_cta = value;
-      h->target_pairs = std::max(1, (value * h->dec_grid + h->groups - 1) / h->groups);
+      h->target_pairs = std::max(1, (value * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
       return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
       if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)

@@ -125,15 +125,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int N>
-__device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
-}
-
 // True in exactly one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;

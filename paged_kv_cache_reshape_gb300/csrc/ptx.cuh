@@ -110,6 +110,18 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Register split between warpgroups: every warp of a warpgroup resizes its
+// registers per thread to N (a multiple of 8 in [24, 256]); the sum over the
+// CTA's warpgroups must stay within the registers the CTA was launched with.
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while its predecessor runs;
 // griddep_wait() blocks until the predecessor grid has completed and its

@@ -185,6 +185,10 @@ struct PrefillParams {
   int oob_row;
 };
 
+// Work-list groups of one latent decode item: each item covers 32 query
+// heads (two of the 16-head groups its partials are laid out by).
+__host__ __device__ inline int mla_item_groups(int groups16) { return (groups16 + 1) / 2; }
+
 struct MlaParams {
   __half* out;           // [T, H, 512]
   const int* block_table;
@@ -194,7 +198,7 @@ struct MlaParams {
   float* part_o;         // [items * groups * 16 * 512]
   float2* part_ml;       // [items * groups * 16]
   int* err;
-  int H, groups;         // query heads, groups of 16 heads
+  int H, groups;         // query heads, groups of 16 heads (32 heads per work item)
   int bs, MB, NB;
   float scale, softcap;
   int window;

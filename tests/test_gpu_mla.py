@@ -29,6 +29,9 @@ SHAPES = [
     cs("mla_h128_groups", 128, 1, 576, 64, [40, 513], [1, 1], scale=SCALE, do_rotary=1, rotary_dim=64, seed=74),
     cs("mla_h16_window_cap", 16, 1, 576, 64, [700, 64, 129], [1, 1, 1], scale=SCALE, softcap=30.0,
        local_window_size=100, seed=75),
+    # 48 heads: the second 32-head group of an item holds one valid 16-head half
+    cs("mla_h48_half_group", 48, 1, 576, 32, [0, 100, 1500], [1, 1, 1], scale=SCALE, do_rotary=1,
+       rotary_dim=64, seed=77),
 ]
 
 
@@ -41,9 +44,10 @@ def test_latent_decode_matches_oracle(shape):
     check_full(host, step, out)
 
 
+@pytest.mark.parametrize("heads", [32, 48])
 @pytest.mark.parametrize("split_keys", [64, 192])
-def test_latent_split_merge(split_keys):
-    shape = cs("mla_splits", 32, 1, 576, 64, [1000, 70, 2047, 300], [1] * 4, scale=SCALE, do_rotary=1,
+def test_latent_split_merge(split_keys, heads):
+    shape = cs("mla_splits", heads, 1, 576, 64, [1000, 70, 2047, 300], [1] * 4, scale=SCALE, do_rotary=1,
                rotary_dim=64, seed=76)
     step = _step(shape)
     host = host_copy(step)
