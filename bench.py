@@ -421,7 +421,8 @@ def run_ours(args, rank, world, local_rank):
             "bound": "hbm", "kernel": kname, "achieved": alg / (t * 1e-3) / 1e9,
             "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
             "frac": alg / (t * 1e-3) / 1e9 / hbm,
-            "traffic": committed_traffic("decode.cu", shape_name(args.workload, shape)),
+            "traffic": committed_traffic("mla.cu" if host.get("kv_cache_layout", 0) == 1 else "decode.cu",
+                                         shape_name(args.workload, shape)),
             "algorithmic_bytes_per_launch": alg,
             "launch_ms": t}
     if ker_ms[pa.PA_STAGE_PREFILL] and work["pre_flops"]:

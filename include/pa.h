@@ -298,8 +298,9 @@ PA_API pa_status pa_destroy(pa_handle h);
  * to a word inside the shared scratch, cleared at the start of each call,
  * that the caller cannot read.
  *
- * It runs fp16 caches without head_sink; an 8-bit cache_dtype returns
- * PA_NOT_SUPPORTED (pa_forward_ex takes the quantized cache and the sink).
+ * It runs separate fp16 K/V caches without head_sink; an 8-bit
+ * cache_dtype, packed_qkv, qk_norm or kv_cache_layout PA_LAYOUT_LATENT
+ * returns PA_NOT_SUPPORTED (pa_forward_ex takes all of them and the sink).
  *
  * The first call on a device does a one-time set-up with that device
  * current (looks up the array's device address with cudaGetSymbolAddress,

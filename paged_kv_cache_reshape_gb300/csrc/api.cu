@@ -1048,9 +1048,10 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   pa_status st = pa_check_step(cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
                                token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
   if (st != PA_OK) return fail(nullptr, st, "%s", msg);
-  if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->packed_qkv || cfg->qk_norm)
+  if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->packed_qkv || cfg->qk_norm || cfg->kv_cache_layout != PA_LAYOUT_SEPARATE)
     return fail(nullptr, PA_NOT_SUPPORTED,
-                "pa_forward_no_alloc runs fp16 caches without packed QKV or QK-Norm; use pa_forward_ex");
+                "pa_forward_no_alloc runs separate fp16 K/V caches without packed QKV or QK-Norm (no latent "
+                "layout); use pa_forward_ex");
   if (device_error && reinterpret_cast<uintptr_t>(device_error) % 4)
     return fail(nullptr, PA_INVALID_ARGUMENT, "device_error must be 4-byte aligned");
   if (token_count == 0) return PA_OK;

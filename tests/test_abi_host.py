@@ -156,6 +156,19 @@ def test_latent_step_wants_no_value():
     assert pa.pa_check_step(cfg, **step_args(value=None, value_cache=None))[0] == pa.PA_OK
 
 
+def test_no_alloc_rejects_latent_layout():
+    """The handle-less entry point runs the separate K/V layout only; a latent
+    step is refused on the host, before any device work."""
+    a = step_args(value=None, value_cache=None)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    st = pa.lib().pa_forward_no_alloc(ctypes.byref(latent()), P(a["query"]), P(a["key"]), None,
+                                      P(a["key_cache"]), None, P(a["block_table"]),
+                                      P(a["cumulative_sequence_lengths"]), P(a["past_sequence_lengths"]), 4, 4,
+                                      None, None, P(a["output"]), None, ctypes.c_void_p(0))
+    assert st == pa.PA_NOT_SUPPORTED
+    assert "latent" in pa.lib().pa_last_error_message(None).decode()
+
+
 def test_quantized_decode_config_passes():
     for cdt in (pa.PA_CACHE_INT8, pa.PA_CACHE_FP8_E4M3):
         for qt in (pa.PA_QUANT_PER_TENSOR, pa.PA_QUANT_PER_CHANNEL):
