@@ -26,6 +26,7 @@ PA_DEVERR_SLOT = 128
 
 PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_MAX_ROWS = 1, 2, 3, 4
 PA_OPT_DECODE_ITEMS_PER_CTA = 5
+PA_OPT_LATENT_TCGEN05 = 6
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 = 0, 1, 2

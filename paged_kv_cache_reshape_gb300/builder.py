@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa_gb300.so")
-SOURCES = ["api.cu", "cache_write.cu", "decode.cu", "combine.cu", "prefill.cu", "prefill_pair.cu", "mla.cu"]
+SOURCES = ["api.cu", "cache_write.cu", "decode.cu", "combine.cu", "prefill.cu", "prefill_pair.cu", "mla.cu",
+           "mla_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

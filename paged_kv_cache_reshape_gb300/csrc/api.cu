@@ -82,6 +82,8 @@ struct pa_handle_s {
   bool latent = false;
   int groups = 1, dv = 0;  // decode work-list groups (kv heads, or 16-head groups of a latent step), output width
   int unit_groups = 1;     // decode CTA work units per (sequence, split)
+  bool mla_tc_ready = false;  // the tcgen05 latent kernel can serve this handle (query heads a multiple of 128)
+  bool mla_tc = false;        // ... and PA_OPT_LATENT_TCGEN05 selected it
   size_t dec_smem = 0;
   int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
@@ -463,7 +465,10 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
 
   if (h->latent) {
+    h->mla_tc_ready = c.num_heads % 128 == 0;
     e = pa::mla_configure(&h->dec_smem);
+    size_t tc_smem = 0;
+    if (e == cudaSuccess && h->mla_tc_ready) e = pa::mla_tc_configure(&tc_smem);
     h->dec_ctas_per_sm = 1;
   } else {
     e = pa::decode_configure(c.head_size, c.cache_dtype, &h->dec_ctas_per_sm, &h->dec_smem);
@@ -478,9 +483,13 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   // decode CTA work units per (sequence, split): kv heads, or the 32-head
   // groups of a latent step
   h->unit_groups = h->latent ? pa::mla_item_groups(h->groups) : h->groups;
+  // work units per item of the tcgen05 latent kernel: 128-head tiles x value halves
+  const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : h->unit_groups;
   h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
   // Room for up to 32 items per CTA (the tuning option's maximum).
-  h->cap_dec = std::max(1, (32 * h->dec_grid + h->unit_groups - 1) / h->unit_groups) + c.max_batch;
+  // (sized for whichever latent kernel makes the most items)
+  const int ug_min = std::min(h->unit_groups, tc_units);
+  h->cap_dec = std::max(1, (32 * h->dec_grid + ug_min - 1) / ug_min) + c.max_batch;
   // Prefill work units: unit tokens (the work list's tiles) and the tokens
   // of one 128-row query tile (the Q TMA box).
   h->prefill_tile_tokens = pa::prefill_unit_tokens(c.head_size, h->G);
@@ -559,6 +568,14 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
     }
     case PA_OPT_NO_WINDOW_PRUNE: h->opt_no_prune = value != 0; return PA_OK;
     case PA_OPT_KERNEL_TIMING: h->opt_timing = value != 0; return PA_OK;
+    case PA_OPT_LATENT_TCGEN05:
+      if (value != 0 && !h->mla_tc_ready)
+        return fail(h, PA_NOT_SUPPORTED, "the tcgen05 latent kernel needs kv_cache_layout LATENT and a multiple of "
+                                         "128 query heads");
+      h->mla_tc = value != 0;
+      h->unit_groups = h->mla_tc ? 2 * (h->cfg.num_heads / 128) : pa::mla_item_groups(h->groups);
+      h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
+      return PA_OK;
     case PA_OPT_DECODE_ITEMS_PER_CTA:
       if (value < 1 || value > 32) return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be in [1, 32]");
       h->opt_items_per_cta = value;
@@ -838,12 +855,16 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   const __half* q_att = (c.do_rotary || quant || c.packed_qkv || c.qk_norm) ? h->q_rot
                                                                           : static_cast<const __half*>(query);
   if (h->latent) {
-    // 3'. latent decode (one 16-head group of one token per item), then the
-    // log-sum-exp combine of its split partials
+    // 3'. latent decode (tensor-core units of 128 heads and half the value
+    // channels, or items of 32 heads), then the log-sum-exp combine of its
+    // split partials
     const int qt = 1;
-    CUtensorMap tq;
-    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, pa::kDecodeRows, qt))
+    const int tile_rows = std::min(c.block_size, 32);
+    CUtensorMap tq, tl;
+    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->mla_tc ? 128 : pa::kDecodeRows, qt))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
+    if (h->mla_tc && !encode_map(&tl, key_cache, D, 1, pool_rows, 1, tile_rows))
+      return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the latent pool");
     pa::MlaParams p{};
     p.out = static_cast<__half*>(output);
     p.block_table = block_table;
@@ -863,9 +884,11 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.window = c.local_window_size;
     p.oob_row = pool_rows;
     p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
+    p.log_tile_rows = 31 - __builtin_clz((unsigned)tile_rows);
     {
       StageTimer t(h, PA_STAGE_DECODE, s);
-      cudaError_t e = pa::launch_mla_decode(tk, tq, p, h->dec_grid, s);
+      cudaError_t e = h->mla_tc ? pa::launch_mla_tc(tq, tl, p, h->dec_grid, s)
+                                : pa::launch_mla_decode(tk, tq, p, h->dec_grid, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "latent decode launch");
       h->last_launches++;
     }

@@ -1,0 +1,517 @@
+// Multi-head latent attention decode on tcgen05 tensor cores, for steps
+// whose query-head count is a multiple of 128 (the DeepSeek-V3 shape): the
+// absorbed form of "PagedAttention - CUDA Design Document", section 12 (one
+// latent row of 576 channels per key shared by every query head, V = its
+// first 512 channels, explicit scale), with the masks of section 8
+// implementation note P5 (causal bound, window, softcap, -1 blocks).
+//
+// A work unit is (sequence, split of its keys, 128 query heads of its one
+// new token, half of the 512 value channels).  The 128 heads are the M rows
+// of the MMAs:
+//   S = Q K^T      M=128, N=32 keys, K=576 (36 MMAs), into TMEM
+//   softmax        one thread per head row (TMEM lane), fp32, lazy rescale
+//                  (2^8), P written back over S as fp16 pairs
+//   O += P V       M=128, N=256 channels, K=32 keys, A = P from TMEM, B =
+//                  the same latent tile in shared memory read as V
+// The full 128 x 512 fp32 output would fill all 512 TMEM columns, leaving
+// none for S, so the two halves of the value channels go to two units (two
+// CTAs), each recomputing S; they read the same latent tiles, the second
+// read mostly from L2.
+//
+// Shared memory: the unit's Q (128 rows x 576 channels, 144 KB, one buffer,
+// reloaded after the unit's last S) and a 2-deep ring of 32-key latent
+// tiles (36 KB each, [chunk][key][128 B], 128-byte swizzle, one TMA box per
+// page and chunk).  TMEM: S/P of even and odd tiles at columns 0 and 32, O
+// at 256.  MMAs issued by one thread complete in order, so S(i+1), issued
+// ahead of PV(i), may reuse the columns of S/P(i-1) once PV(i-1) is issued.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over the device
+// queue): warps 0-3 softmax and epilogue, warp 4 TMA producer, warp 5 TMEM
+// owner and MMA issuer.  Split units write fp32 partials laid out like the
+// other decode kernels' (16 rows per item and 16-head group) for the
+// combine kernel.
+#include "ptx.cuh"
+#include "step.h"
+#include "../../include/pa.h"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 576, kDV = 512, kHalf = kDV / 2;
+constexpr int kChunks = kD / 64;                  // 9 chunks of 64 channels
+constexpr int kKeys = 32;                         // keys per latent tile
+constexpr int kRows = 128;                        // query heads per unit (MMA M)
+constexpr int kThreads = 6 * 32;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kQBytes = kChunks * kRows * 128;    // [chunk][head][128 B]
+constexpr int kTileBytes = kChunks * kKeys * 128; // [chunk][key][128 B]
+constexpr int kStages = 2;
+constexpr int kOCol = 256;                        // TMEM columns: S/P at 0 and 32, O at 256
+constexpr int kTmemCols = 512;
+constexpr int kDataBytes = kQBytes + kStages * kTileBytes;
+constexpr int kSmemBytes = 1024 + kDataBytes + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyRescale = 8.f;
+
+struct UnitInfo {
+  int u;       // work unit; -1 = no more work
+  int ht;      // 128-head tile
+  int half;    // value channels [half * 256, half * 256 + 256)
+  int item;    // (sequence, split) work item
+  int t0;      // packed row of the sequence's new token
+  int past;    // its position: the last admitted key
+  int key0;    // first key of the split (a multiple of 32)
+  int end;     // split end (exclusive)
+  int n_kv;    // latent tiles of the split
+  int lo_min;  // smallest admitted position (window), 0 without one
+  int kv_len;  // past + 1
+  int nsplit;  // splits of the sequence
+  int pad[4];
+};
+
+struct Ctrl {
+  UnitInfo info[2];
+  uint32_t kv_mask[kStages];  // per stage: bit p = page p zero-filled (unmapped / past the end)
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t s_full[2], p_full, o_done;
+  uint64_t info_full[2], info_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort) return false;
+  }
+  *abort = 1;
+  atomicOr(err, PA_DEVERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool CAP>
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_l,
+                  const MlaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem;             // [kQBytes]
+  uint8_t* kv_s = q_s + kQBytes;   // [kStages][kTileBytes]
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kDataBytes);
+  volatile int* abort = &ctl->abort;
+
+  griddep_wait();  // the work list and the latent rows come from the prologue
+  const int n_ht = p.H / kRows;
+  const int per_item = 2 * n_ht;  // units per (sequence, split)
+  const int n_work = p.counters->n_dec * per_item;
+  const int active = min(p.counters->dec_ctas, n_work);
+  if ((int)blockIdx.x >= active) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->kv_full[i], 1);
+      mbar_init(&ctl->kv_empty[i], 1);
+      mbar_init(&ctl->s_full[i], 1);
+      mbar_init(&ctl->info_full[i], 1);
+      mbar_init(&ctl->info_empty[i], 1 + 4);  // MMA thread + 4 softmax warps
+    }
+    mbar_init(&ctl->p_full, 4);
+    mbar_init(&ctl->o_done, 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  griddep_launch_dependents();
+  const uint32_t tmem = ctl->tmem_base;
+  const int log_r = p.log_tile_rows;  // log2(min(block_size, 32)): pool rows per TMA box
+  const int pages = kKeys >> log_r;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_l);
+    }
+    const int split_keys = p.counters->split_keys;
+    uint32_t g = 0;     // latent tiles loaded so far
+    int q_loads = 0;    // Q loads issued so far
+    bool ok = true;
+    for (uint32_t tt = 0; ok; ++tt) {
+      const int slot = tt & 1;
+      int u = 0;
+      if (lane == 0) {
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
+        else u = tt == 0 ? (int)blockIdx.x : active + atomicAdd(&p.counters->dec_next, 1);
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u == -2) break;
+      UnitInfo& ti = ctl->info[slot];
+      if (u >= n_work) {
+        if (lane == 0) {
+          ti.u = -1;
+          mbar_arrive(&ctl->info_full[slot]);
+        }
+        break;
+      }
+      const int item = u / per_item, rest = u - item * per_item;
+      const int ht = rest >> 1, half = rest & 1;
+      const int2 bsplit = p.dec_items[item];
+      const SeqInfo si = p.seq[bsplit.x];
+      const int start = si.lo + bsplit.y * split_keys;
+      const int end = min(si.kv_len, start + split_keys);
+      const int past = si.kv_len - si.q_len;
+      const int n_kv = (end - start + kKeys - 1) / kKeys;
+      if (lane == 0) {
+        ti.u = u;
+        ti.ht = ht;
+        ti.half = half;
+        ti.item = item;
+        ti.t0 = si.t0;
+        ti.past = past;
+        ti.key0 = start;
+        ti.end = end;
+        ti.n_kv = n_kv;
+        ti.lo_min = p.window >= 1 ? max(0, past + 1 - p.window) : 0;
+        ti.kv_len = si.kv_len;
+        ti.nsplit = si.dec_count;
+        mbar_arrive(&ctl->info_full[slot]);
+        // Q: 128 heads of the token, one box {64, 128, 1} per chunk; the
+        // buffer is free once the previous unit's last S MMAs completed.
+        if (!wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err)) {
+          ok = false;
+        } else {
+          mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+          ++q_loads;
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_3d(q_s + c * (kRows * 128), &tm_q, c * 64, ht * kRows, si.t0, &ctl->q_full);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+
+      // Block ids, 32 block-table rows at a time, one per lane.
+      const int* bt_row = p.block_table + (size_t)bsplit.x * p.MB;
+      auto load_id = [&](int r) -> int { return (r < p.MB && r * p.bs < end) ? __ldg(bt_row + r) : -1; };
+      int win = start / p.bs;
+      int id = load_id(win + lane);
+      for (int i = 0; i < n_kv; ++i, ++g) {
+        const int st = g & 1;
+        const int key0 = start + i * kKeys;
+        if ((key0 + kKeys - 1) / p.bs >= win + 32) {
+          win = key0 / p.bs;
+          id = load_id(win + lane);
+        }
+        // lane pg < pages resolves page pg of this tile
+        const int pos = key0 + (lane << log_r);
+        const int idx = pos / p.bs - win;
+        const int blk = __shfl_sync(0xffffffffu, id, idx & 31);
+        int rc = p.oob_row;
+        if (lane < pages && pos < end) {
+          if (blk >= 0 && blk < p.NB) rc = blk * p.bs + (pos & (p.bs - 1));
+          else if (blk != -1) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
+        if (lane == 0) {
+          if (!wait_or_abort(&ctl->kv_empty[st], ((g >> 1) & 1) ^ 1, abort, p.err)) {
+            ok = false;
+          } else {
+            ctl->kv_mask[st] = mask;
+            mbar_arrive_expect_tx(&ctl->kv_full[st], kTileBytes);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        // one box {64, 1, 2^log_r} per (page, chunk); lane -> (page, chunk)
+        for (int base = 0; base < pages * kChunks; base += 32) {
+          const int bx = base + lane;
+          const int lp = min(bx / kChunks, 31), lc = bx % kChunks;
+          const int prc = __shfl_sync(0xffffffffu, rc, lp);
+          if (bx < pages * kChunks)
+            tma_load_3d(kv_s + st * kTileBytes + lc * (kKeys * 128) + ((uint32_t)lp << (log_r + 7)), &tm_l,
+                        lc * 64, 0, prc, &ctl->kv_full[st]);
+        }
+      }
+    }
+    if (lane == 0 && *abort) {
+      // Gave up: let the copies already issued land before the CTA exits.
+      for (uint32_t i = 0; i < kWaitLimit && q_loads > 0 && !mbar_try_wait(&ctl->q_full, (q_loads - 1) & 1); ++i) {
+      }
+      for (int d = 1; d <= 2 && (int)g - d >= 0; ++d) {
+        const uint32_t gl = g - d;
+        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->kv_full[gl & 1], (gl >> 1) & 1); ++i) {
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_f16(kRows, kKeys, 0, 0);
+      constexpr uint32_t idesc_o = umma_idesc_f16(kRows, kHalf, 0, 1);
+      const uint64_t desc_v = smem_desc_sw128(0, kKeys * 128, 1024);  // MN-major V, + (address >> 4)
+      const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s);
+      uint32_t g = 0, v = 0;
+      bool ok = true;
+      for (uint32_t tt = 0; ok; ++tt) {
+        const int slot = tt & 1;
+        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+        const UnitInfo ti = ctl->info[slot];
+        if (ti.u < 0) break;
+        if (!wait_or_abort(&ctl->q_full, tt & 1, abort, p.err)) break;
+        tc_fence_after();
+        // S(gi) = Q K_gi^T into TMEM columns [32 (gi & 1), +32): the columns
+        // of S/P(gi - 2), whose PV was issued before this.
+        auto issue_s = [&](uint32_t gi, bool last) -> bool {
+          const int st = gi & 1;
+          if (!wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) return false;
+          tc_fence_after();
+          const uint32_t kb = kv_addr + st * kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kD / 16; ++ks) {
+            const uint64_t a = smem_desc_sw128(q_addr + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
+            const uint64_t b = smem_desc_sw128(kb + (ks >> 2) * (kKeys * 128) + (ks & 3) * 32, 16, 1024);
+            umma_f16(tmem + 32 * st, a, b, idesc_s, ks > 0 ? 1u : 0u);
+          }
+          umma_commit(&ctl->s_full[st]);
+          if (last) umma_commit(&ctl->q_empty);
+          return true;
+        };
+        if (!issue_s(g, ti.n_kv == 1)) break;
+        for (int i = 0; i < ti.n_kv; ++i) {
+          const uint32_t gi = g + i;
+          const int st = gi & 1;
+          // S(gi + 1) goes ahead of PV(gi): it runs while the softmax works
+          // on tile gi (its columns held P(gi - 1), whose PV is issued).
+          if (i + 1 < ti.n_kv && !issue_s(gi + 1, i + 2 == ti.n_kv)) {
+            ok = false;
+            break;
+          }
+          if (!wait_or_abort(&ctl->p_full, v & 1, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          ++v;
+          tc_fence_after();
+          // O += P(gi) V(gi): P from TMEM (fp16 pairs over S), V = this
+          // half's four channel chunks of the same latent tile.
+          const uint32_t vb = kv_addr + st * kTileBytes + ti.half * (kHalf / 64) * (kKeys * 128);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            umma_f16_ts(tmem + kOCol, tmem + 32 * st + kk * 8, desc_v + ((vb + kk * 16 * 128) >> 4), idesc_o,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&ctl->kv_empty[st]);
+          umma_commit(&ctl->o_done);
+        }
+        g += ti.n_kv;
+        if (!ok) break;
+        mbar_arrive(&ctl->info_empty[slot]);
+      }
+      // Drain: every MMA issued above has completed before TMEM is freed.
+      umma_commit(&ctl->drain);
+      for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->drain, 0); ++i) {
+      }
+    }
+  } else {
+    // ----------------------------------------------------- softmax warps
+    const int r = threadIdx.x;  // head row within the unit == TMEM lane
+    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+    // Scores become log2-domain logits: x * mul (softcap applies its own).
+    const float mul = CAP ? 1.f : p.scale * kLog2e;
+    const float cap_in = CAP ? p.scale / p.softcap : 0.f;
+    const float cap_out = CAP ? p.softcap * kLog2e : 0.f;
+    uint32_t g = 0, v = 0;
+    float x[kKeys];
+    for (uint32_t tt = 0;; ++tt) {
+      const int slot = tt & 1;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+      const UnitInfo ti = ctl->info[slot];
+      if (ti.u < 0) break;
+      const int hi = ti.past;                                // last admitted position
+      const int lo = p.window >= 1 ? hi + 1 - p.window : 0;  // first admitted position
+      float m_ref = -INFINITY;  // reference max (log2 units) of P and O
+      float l = 0.f;
+      bool ok = true;
+      for (int i = 0; i < ti.n_kv; ++i) {
+        const uint32_t gi = g + i;
+        const int st = gi & 1;
+        const int key0 = ti.key0 + i * kKeys;
+        if (!wait_or_abort(&ctl->s_full[st], (gi >> 1) & 1, abort, p.err) ||
+            !wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_ld32(lane_addr + 32 * st, x);
+        tmem_ld_wait();
+        if constexpr (CAP) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) x[c] = cap_out * tanhf(x[c] * cap_in);
+        }
+        // Admitted columns of this tile: [c_lo, c_hi] minus zero-filled pages.
+        const uint32_t mask = ctl->kv_mask[st];
+        const int c_lo = max(lo - key0, 0);
+        const int c_hi = min(min(hi, ti.end - 1) - key0, kKeys - 1);
+        if (c_lo > 0 || c_hi < kKeys - 1) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) x[c] = (c >= c_lo && c <= c_hi) ? x[c] : -INFINITY;
+        }
+        if (mask != 0) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) x[c] = ((mask >> (c >> log_r)) & 1) ? -INFINITY : x[c];
+        }
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) tmax = fmaxf(tmax, x[c]);
+        const float cand = tmax * mul;
+        float alpha = 1.f;
+        if (cand > m_ref + kLazyRescale || (m_ref == -INFINITY && cand != -INFINITY)) {
+          alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - cand);
+          m_ref = cand;
+        }
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        float rs = 0.f;
+        uint32_t pk[kKeys / 2];
+#pragma unroll
+        for (int c = 0; c < kKeys; c += 2) {
+          const float e0 = ex2(fmaf(x[c], mul, -m_use)), e1 = ex2(fmaf(x[c + 1], mul, -m_use));
+          rs += e0 + e1;
+          pk[c / 2] = pack_half2(e0, e1);
+        }
+        l = l * alpha + rs;
+        // PV(gi - 1) must be done before O is rescaled.
+        if (i > 0) {
+          if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            float o[32];
+#pragma unroll 1
+            for (int c = 0; c < kHalf / 32; ++c) {
+              tmem_ld32(lane_addr + kOCol + 32 * c, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tmem_st32(lane_addr + kOCol + 32 * c, o);
+            }
+          }
+        }
+        // Never-admitted keys of an edge tile: zero their rows of this
+        // half's value channels so stale bytes (a partly filled last block)
+        // cannot leak through P = 0.
+        if (key0 + kKeys > ti.kv_len || key0 < ti.lo_min) {
+          uint8_t* vs = kv_s + st * kTileBytes + ti.half * (kHalf / 64) * (kKeys * 128);
+          for (int idx = r; idx < kKeys * (kHalf / 64) * 8; idx += 128) {
+            const int kr = idx / ((kHalf / 64) * 8), rem = idx % ((kHalf / 64) * 8);
+            const int pos = key0 + kr;
+            if (pos >= ti.kv_len || pos < ti.lo_min) {
+              const int c = rem >> 3, col16 = rem & 7;
+              *reinterpret_cast<uint4*>(vs + c * (kKeys * 128) + kr * 128 + ((col16 ^ (kr & 7)) << 4)) =
+                  make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        // P -> TMEM over S: keys 0..31 as 16 columns of fp16 pairs
+        tmem_st16(lane_addr + 32 * st, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full);
+      }
+      if (!ok) break;
+      // epilogue: O / l -> fp16 output rows, or fp32 partials of a split
+      if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err)) break;
+      tc_fence_after();
+      const int h = ti.ht * kRows + r;
+      const int c0 = ti.half * kHalf;
+      if (ti.nsplit == 1) {
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        __half* dst = p.out + ((size_t)ti.t0 * p.H + h) * kDV + c0;
+#pragma unroll 1
+        for (int c = 0; c < kHalf / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_addr + kOCol + 32 * c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 w;
+            w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
+            w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
+            w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
+            w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
+          }
+        }
+      } else {
+        // rows of 16-head group h / 16 of the item, as the combine kernel reads them
+        const size_t prow = ((size_t)ti.item * p.groups + h / kDecodeRows) * kDecodeRows + h % kDecodeRows;
+        float* dst = p.part_o + prow * kDV + c0;
+#pragma unroll 1
+        for (int c = 0; c < kHalf / 32; ++c) {
+          float o[32];
+          tmem_ld32(lane_addr + kOCol + 32 * c, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(dst + 32 * c + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2],
+                                                                           o[4 * q + 3]);
+        }
+        if (ti.half == 0) p.part_ml[prow] = make_float2(m_ref, l);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->info_empty[slot]);
+      g += ti.n_kv;
+      v += ti.n_kv;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool CAP>
+cudaError_t configure_cap() {
+  static_assert(sizeof(Ctrl) <= 1024, "control block");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  return cudaFuncSetAttribute(mla_tc_kernel<CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+}  // namespace
+
+cudaError_t mla_tc_configure(size_t* smem) {
+  *smem = kSmemBytes;
+  cudaError_t e = configure_cap<false>();
+  return e != cudaSuccess ? e : configure_cap<true>();
+}
+
+cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tl, const MlaParams& p, int grid,
+                          cudaStream_t s) {
+  if (p.softcap > 0.f) return launch_pdl(mla_tc_kernel<true>, grid, kThreads, kSmemBytes, s, tq, tl, p);
+  return launch_pdl(mla_tc_kernel<false>, grid, kThreads, kSmemBytes, s, tq, tl, p);
+}
+
+}  // namespace pa

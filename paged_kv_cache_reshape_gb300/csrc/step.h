@@ -204,6 +204,7 @@ struct MlaParams {
   int window;
   int oob_row;
   int log_box_rows;      // log2(min(block_size, 64))
+  int log_tile_rows;     // log2(min(block_size, 32)): pool rows per box of the tensor-core kernel
 };
 
 // Launch with the programmatic stream-serialization attribute, so the
@@ -234,6 +235,12 @@ cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMa
                           const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
 cudaError_t mla_configure(size_t* smem);
+// Latent decode on tcgen05 (query heads a multiple of 128): units of 128 heads
+// and half of the value channels; Q map boxes {64, 128 heads, 1 token}, pool
+// map boxes {64, 1, min(block_size, 32) rows}.
+cudaError_t mla_tc_configure(size_t* smem);
+cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tl, const MlaParams& p, int grid,
+                          cudaStream_t s);
 cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const MlaParams& p, int grid,
                               cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);

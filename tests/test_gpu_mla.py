@@ -32,31 +32,61 @@ SHAPES = [
     # 48 heads: the second 32-head group of an item holds one valid 16-head half
     cs("mla_h48_half_group", 48, 1, 576, 32, [0, 100, 1500], [1, 1, 1], scale=SCALE, do_rotary=1,
        rotary_dim=64, seed=77),
+    # multiples of 128 heads also run the tcgen05 kernel (option): two pages
+    # per 32-key tile, window + softcap, unmapped and partly filled pages;
+    # 256 heads
+    cs("mla_tc_h128_bs16_window_cap", 128, 1, 576, 16, [700, 5, 129, 0, 31], [1] * 5, scale=SCALE, softcap=30.0,
+       local_window_size=100, do_rotary=1, rotary_dim=64, seed=78),
+    cs("mla_tc_h128_bs64", 128, 1, 576, 64, [0, 1, 31, 32, 63, 64, 65, 1000], [1] * 8, scale=SCALE, seed=79),
+    cs("mla_tc_h256_bs32", 256, 1, 576, 32, [300, 1000, 17], [1, 1, 1], scale=SCALE, do_rotary=1, rotary_dim=64,
+       seed=80),
 ]
 
 
+def _kernel_options(kernel, heads):
+    if kernel == "tcgen05":
+        if heads % 128:
+            pytest.skip("the tcgen05 latent kernel serves multiples of 128 heads")
+        return [(pa.PA_OPT_LATENT_TCGEN05, 1)]
+    return []
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: s.name)
-def test_latent_decode_matches_oracle(shape):
+def test_latent_decode_matches_oracle(shape, kernel):
+    opts = _kernel_options(kernel, shape.num_heads)
     step = _step(shape)
     host = host_copy(step)
-    _, out, err = run(step, max_query_len_bound=1)
+    _, out, err = run(step, options=opts, max_query_len_bound=1)
     assert err == 0
     check_full(host, step, out)
 
 
-@pytest.mark.parametrize("heads", [32, 48])
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("heads", [32, 48, 128])
 @pytest.mark.parametrize("split_keys", [64, 192])
-def test_latent_split_merge(split_keys, heads):
+def test_latent_split_merge(split_keys, heads, kernel):
+    opts = _kernel_options(kernel, heads)
     shape = cs("mla_splits", heads, 1, 576, 64, [1000, 70, 2047, 300], [1] * 4, scale=SCALE, do_rotary=1,
                rotary_dim=64, seed=76)
     step = _step(shape)
     host = host_copy(step)
-    _, out, err = run(step, options=[(pa.PA_OPT_SPLIT_KEYS, split_keys)], max_query_len_bound=1)
+    _, out, err = run(step, options=[(pa.PA_OPT_SPLIT_KEYS, split_keys)] + opts, max_query_len_bound=1)
     assert err == 0
     check_full(host, step, out)
 
 
-def test_latent_full_size_step_sampled():
+def test_tcgen05_latent_option_rules():
+    step = _step(cs("mla_opt_h32", 32, 1, 576, 64, [10], [1], scale=SCALE, seed=81))
+    op = pa.PagedAttention.for_step(step, max_query_len_bound=1)
+    with pytest.raises(pa.PAError) as e:
+        op.set_option(pa.PA_OPT_LATENT_TCGEN05, 1)
+    assert e.value.status == pa.PA_NOT_SUPPORTED
+    op.set_option(pa.PA_OPT_LATENT_TCGEN05, 0)
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+def test_latent_full_size_step_sampled(kernel):
     """DeepSeek-V3-shaped decode: 128 heads, 576/512 latent, block_size 64,
     32 sequences with past lengths U{512..4096} (sampled rows)."""
     g = torch.Generator().manual_seed(77)
@@ -65,7 +95,7 @@ def test_latent_full_size_step_sampled():
                seed=77)
     step = _step(shape)
     host = host_copy(step)
-    _, out, err = run(step, max_query_len_bound=1)
+    _, out, err = run(step, options=_kernel_options(kernel, 128), max_query_len_bound=1)
     assert err == 0
     from gpu_util import assert_close, raw
     import numpy as np
