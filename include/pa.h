@@ -324,7 +324,9 @@ enum {
   PA_OPT_NO_WINDOW_PRUNE = 2, /* 1: walk the whole context and mask instead of pruning */
   PA_OPT_KERNEL_TIMING = 3,   /* 1: record CUDA events around each kernel of pa_forward */
   PA_OPT_DECODE_MAX_ROWS = 4, /* route a sequence to the decode kernel iff q_len*G <= value (1..16, default 16; 0 = never) */
-  PA_OPT_DECODE_ITEMS_PER_CTA = 5, /* target decode work items per decode CTA when splits are sized automatically (1..32, default 2) */
+  PA_OPT_DECODE_ITEMS_PER_CTA = 5, /* target decode work items per decode CTA when splits are sized automatically:
+                                      1..32, or 0 (default) = per step, 1 when the step's sequences x kv heads
+                                      (latent: x work units per sequence) fill the decode grid, else 2 */
   PA_OPT_LATENT_TCGEN05 = 6   /* 1: latent layout with a multiple of 128 query heads runs the tcgen05 latent
                                  kernel (units of 128 heads x half the value channels) instead of the default
                                  mma.sync kernel (items of 32 heads); PA_NOT_SUPPORTED on other handles */

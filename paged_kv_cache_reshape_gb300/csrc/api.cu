@@ -85,7 +85,7 @@ struct pa_handle_s {
   bool mla_tc_ready = false;  // the tcgen05 latent kernel can serve this handle (query heads a multiple of 128)
   bool mla_tc = false;        // ... and PA_OPT_LATENT_TCGEN05 selected it
   size_t dec_smem = 0;
-  int target_pairs = 1, cap_dec = 1, cap_pre = 1, cap_comb = 1;
+  int cap_dec = 1, cap_pre = 1, cap_comb = 1;
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
   size_t pre_smem = 0;
   bool prefill_ready = false;
@@ -100,7 +100,8 @@ struct pa_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   __half* q_rot = nullptr;
-  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0, opt_items_per_cta = pa::kDecodeItemsPerCta;
+  int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0;
+  int opt_items_per_cta = 0;  // 0: chosen per step (target_pairs_for)
   cudaEvent_t ev[PA_NUM_STAGES][2] = {};
   bool stage_ran[PA_NUM_STAGES] = {};
   cudaStream_t last_stream = nullptr;
@@ -119,6 +120,17 @@ pa_status fail(pa_handle h, pa_status st, const char* fmt, ...) {
   g_last_msg = buf;
   if (h) h->msg = buf;
   return st;
+}
+
+// Decode (sequence, split) items the work list aims for.  Splits balance
+// the decode CTAs' load but cost a merge; measured on GB300: one item per CTA
+// is best once the unsplit work units (sequences x kv heads, or latent units)
+// fill the grid, two when they do not (few long sequences).
+int target_pairs_for(pa_handle h, int batch) {
+  const int ug = h->unit_groups;
+  int ipc = h->opt_items_per_cta;
+  if (ipc <= 0) ipc = (long long)batch * ug >= h->dec_grid ? 1 : pa::kDecodeItemsPerCta;
+  return std::max(1, (ipc * h->dec_grid + ug - 1) / ug);
 }
 
 pa_status cuda_fail(pa_handle h, cudaError_t e, const char* what) {
@@ -485,7 +497,6 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->unit_groups = h->latent ? pa::mla_item_groups(h->groups) : h->groups;
   // work units per item of the tcgen05 latent kernel: 128-head tiles x value halves
   const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : h->unit_groups;
-  h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
   // Room for up to 32 items per CTA (the tuning option's maximum).
   // (sized for whichever latent kernel makes the most items)
   const int ug_min = std::min(h->unit_groups, tc_units);
@@ -574,12 +585,11 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
                                          "128 query heads");
       h->mla_tc = value != 0;
       h->unit_groups = h->mla_tc ? 2 * (h->cfg.num_heads / 128) : pa::mla_item_groups(h->groups);
-      h->target_pairs = std::max(1, (h->opt_items_per_cta * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
       return PA_OK;
     case PA_OPT_DECODE_ITEMS_PER_CTA:
-      if (value < 1 || value > 32) return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be in [1, 32]");
+      if (value < 0 || value > 32)
+        return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be 0 (automatic) or in [1, 32]");
       h->opt_items_per_cta = value;
-      h->target_pairs = std::max(1, (value * h->dec_grid + h->unit_groups - 1) / h->unit_groups);
       return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
       if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)
@@ -835,7 +845,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.dec_max_rows = h->opt_dec_rows;
     p.prefill_tile_tokens = h->prefill_tile_tokens;
     p.split_keys_fixed = h->opt_split_keys;
-    p.target_pairs = h->target_pairs;
+    p.target_pairs = target_pairs_for(h, batch);
     p.cap_dec = h->cap_dec;
     p.cap_pre = h->cap_pre;
     p.cap_comb = h->cap_comb;
