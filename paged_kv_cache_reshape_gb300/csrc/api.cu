@@ -858,7 +858,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     pa::CacheWriteParams cp = cache_write_params(h, query, key, value, key_cache, value_cache, block_table, cum,
                                                  past, batch, token_count, cos_cache, sin_cache, x);
     StageTimer t(h, PA_STAGE_WORKLIST, s);
-    cudaError_t e = pa::launch_prologue(p, cp, s);
+    cudaError_t e = pa::launch_prologue(p, cp, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prologue launch");
     h->last_launches++;
   }
@@ -1209,7 +1209,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   cp.q_heads_per_part = Hk;
   cp.parts = 1 + (q_rot ? (H + Hk - 1) / Hk : 0);
   cp.err = err;
-  e = pa::launch_prologue(wp, cp, s);
+  e = pa::launch_prologue(wp, cp, nd->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "prologue launch");
 
   const __half* q_att = c.do_rotary ? q_rot : static_cast<const __half*>(query);

@@ -33,6 +33,7 @@
 // root and reciprocal), and every loaded channel becomes fp16((x * r) * w).
 // Packed QKV rows (section 4) are read in place: Q, K and V heads of token
 // t start at t*(H+2Hk)*D, + H*D and + (H+Hk)*D.
+#include <algorithm>
 #include <type_traits>
 
 #include "step.h"
@@ -336,11 +337,13 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) cache_write_kernel(CacheW
 }
 
 // The step's prologue in one launch: CTA 0 builds the work list while the
-// other CTAs (32 warps each, one warp per (token, part)) rotate and write
-// the new rows.  The two jobs read only the step's inputs, so they overlap.
-constexpr int kPrologueWarps = worklist::kThreads / 32;
+// other CTAs (wpb writing warps each, one warp per (token, part)) rotate
+// and write the new rows.  The two jobs read only the step's inputs, so
+// they overlap.
+constexpr int kPrologueWarps = worklist::kThreads / 32;  // at most this many writing warps per block
 
-__global__ void __launch_bounds__(worklist::kThreads, 1) prologue_kernel(WorklistParams wp, CacheWriteParams cp) {
+__global__ void __launch_bounds__(worklist::kThreads, 1) prologue_kernel(WorklistParams wp, CacheWriteParams cp,
+                                                                         int wpb) {
   // Let the attention kernels' CTAs get resident early; they wait for this
   // grid's completion before reading anything it writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -351,7 +354,8 @@ __global__ void __launch_bounds__(worklist::kThreads, 1) prologue_kernel(Worklis
   __shared__ int cum_s[kCumCache];
   __shared__ float rn_s[kPrologueWarps][kMaxNormHeads];
   const int* cum = stage_cum(cp, cum_s);
-  const int w = (blockIdx.x - 1) * kPrologueWarps + (threadIdx.x >> 5);
+  if ((threadIdx.x >> 5) >= wpb) return;  // wpb writing warps per block
+  const int w = (blockIdx.x - 1) * wpb + (threadIdx.x >> 5);
   if (w < cp.token_count * cp.parts)
     write_token(cp, cum, w / cp.parts, w % cp.parts, threadIdx.x & 31, rn_s[threadIdx.x >> 5]);
 }
@@ -364,9 +368,14 @@ cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, cudaStream_t s) {
-  int blocks = 1 + (cp.token_count * cp.parts + kPrologueWarps - 1) / kPrologueWarps;
-  prologue_kernel<<<blocks, worklist::kThreads, 0, s>>>(wp, cp);
+cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, int num_sms, cudaStream_t s) {
+  // Few warps per block while the warps fit the free SMs (their conversions
+  // then run on separate SMs), up to 32 per block for large steps.
+  const long long warps = (long long)cp.token_count * cp.parts;
+  const int spread = std::max(1, num_sms - 1);
+  const int wpb = (int)std::min<long long>(kPrologueWarps, std::max<long long>(1, (warps + spread - 1) / spread));
+  const int blocks = 1 + (int)((warps + wpb - 1) / wpb);
+  prologue_kernel<<<blocks, worklist::kThreads, 0, s>>>(wp, cp, wpb);
   return cudaGetLastError();
 }
 
