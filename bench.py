@@ -409,19 +409,23 @@ def run_ours(args, rank, world, local_rank):
         t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
         alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
         ct = {0: "", 1: ", int8", 2: ", e4m3"}[host.get("cache_dtype", 0)]
-        kname = "mla_decode_kernel" if host.get("kv_cache_layout", 0) == 1 else f"decode_kernel<{shape.head_size}{ct}>"
+        latent = host.get("kv_cache_layout", 0) == 1
+        latent_tc = latent and shape.num_heads % 128 == 0  # the tcgen05 latent kernel serves these
+        kname = (("mla_tc_kernel" if latent_tc else "mla_decode_kernel") if latent
+                 else f"decode_kernel<{shape.head_size}{ct}>")
         if work["dec_flops"]:
             ach = work["dec_flops"] / (t * 1e-3) / 1e12
             rooflines["decode_tensor"] = {
                 "bound": "tensor", "kernel": kname, "achieved": ach, "peak": tflops,
-                "peak_kind": f"{peak_kind} bf16 matmul burst (the kernel runs m16n8k16 fp16 HMMA)",
+                "peak_kind": f"{peak_kind} bf16 matmul burst (the kernel runs "
+                             + ("tcgen05 kind::f16 MMAs)" if latent_tc else "m16n8k16 fp16 HMMA)"),
                 "unit": "TFLOP/s", "frac": ach / tflops, "traffic": None,
                 "algorithmic_flops_per_launch": work["dec_flops"], "launch_ms": t - 1e-9}
         rooflines["decode"] = {
             "bound": "hbm", "kernel": kname, "achieved": alg / (t * 1e-3) / 1e9,
             "peak": hbm, "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
             "frac": alg / (t * 1e-3) / 1e9 / hbm,
-            "traffic": committed_traffic("mla.cu" if host.get("kv_cache_layout", 0) == 1 else "decode.cu",
+            "traffic": committed_traffic(("mla_tc.cu" if latent_tc else "mla.cu") if latent else "decode.cu",
                                          shape_name(args.workload, shape)),
             "algorithmic_bytes_per_launch": alg,
             "launch_ms": t}

@@ -327,9 +327,10 @@ enum {
   PA_OPT_DECODE_ITEMS_PER_CTA = 5, /* target decode work items per decode CTA when splits are sized automatically:
                                       1..32, or 0 (default) = per step, 1 when the step's sequences x kv heads
                                       (latent: x work units per sequence) fill the decode grid, else 2 */
-  PA_OPT_LATENT_TCGEN05 = 6   /* 1: latent layout with a multiple of 128 query heads runs the tcgen05 latent
-                                 kernel (units of 128 heads x half the value channels) instead of the default
-                                 mma.sync kernel (items of 32 heads); PA_NOT_SUPPORTED on other handles */
+  PA_OPT_LATENT_TCGEN05 = 6   /* latent layout: 1 (the default when the query heads are a multiple of 128)
+                                 runs the tcgen05 latent kernel (units of 128 heads x half the value
+                                 channels), 0 the mma.sync kernel (items of 32 heads, any head count);
+                                 1 on other handles is PA_NOT_SUPPORTED */
 };
 PA_API pa_status pa_set_option(pa_handle h, int option, int value);
 

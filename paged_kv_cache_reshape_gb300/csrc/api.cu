@@ -83,7 +83,7 @@ struct pa_handle_s {
   int groups = 1, dv = 0;  // decode work-list groups (kv heads, or 16-head groups of a latent step), output width
   int unit_groups = 1;     // decode CTA work units per (sequence, split)
   bool mla_tc_ready = false;  // the tcgen05 latent kernel can serve this handle (query heads a multiple of 128)
-  bool mla_tc = false;        // ... and PA_OPT_LATENT_TCGEN05 selected it
+  bool mla_tc = false;        // ... and runs (the default; PA_OPT_LATENT_TCGEN05 = 0 selects the mma.sync kernel)
   size_t dec_smem = 0;
   int cap_dec = 1, cap_pre = 1, cap_comb = 1;
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
@@ -494,12 +494,13 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->dec_grid = h->num_sms * h->dec_ctas_per_sm;
   // decode CTA work units per (sequence, split): kv heads, or the 32-head
   // groups of a latent step
-  h->unit_groups = h->latent ? pa::mla_item_groups(h->groups) : h->groups;
   // work units per item of the tcgen05 latent kernel: 128-head tiles x value halves
-  const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : h->unit_groups;
+  const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : 1;
+  h->mla_tc = h->mla_tc_ready;
+  h->unit_groups = h->mla_tc ? tc_units : h->latent ? pa::mla_item_groups(h->groups) : h->groups;
   // Room for up to 32 items per CTA (the tuning option's maximum).
   // (sized for whichever latent kernel makes the most items)
-  const int ug_min = std::min(h->unit_groups, tc_units);
+  const int ug_min = h->mla_tc_ready ? std::min(tc_units, pa::mla_item_groups(h->groups)) : h->unit_groups;
   h->cap_dec = std::max(1, (32 * h->dec_grid + ug_min - 1) / ug_min) + c.max_batch;
   // Prefill work units: unit tokens (the work list's tiles) and the tokens
   // of one 128-row query tile (the Q TMA box).

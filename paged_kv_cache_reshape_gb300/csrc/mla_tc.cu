@@ -8,22 +8,27 @@
 // A work unit is (sequence, split of its keys, 128 query heads of its one
 // new token, half of the 512 value channels).  The 128 heads are the M rows
 // of the MMAs:
-//   S = Q K^T      M=128, N=32 keys, K=576 (36 MMAs), into TMEM
+//   S = Q K^T      M=128, N=32 keys, K=576: 24 MMAs with Q's first 384
+//                  channels read from TMEM, 12 with the last 192 from shared
+//                  memory
 //   softmax        one thread per head row (TMEM lane), fp32, lazy rescale
 //                  (2^8), P written back over S as fp16 pairs
 //   O += P V       M=128, N=256 channels, K=32 keys, A = P from TMEM, B =
 //                  the same latent tile in shared memory read as V
-// The full 128 x 512 fp32 output would fill all 512 TMEM columns, leaving
-// none for S, so the two halves of the value channels go to two units (two
-// CTAs), each recomputing S; they read the same latent tiles, the second
-// read mostly from L2.
+// The full 128 x 512 fp32 output would fill all 512 TMEM columns, so the two
+// halves of the value channels go to two units (two CTAs), each recomputing
+// S; they read the same latent tiles, the second read mostly from L2.
 //
-// Shared memory: the unit's Q (128 rows x 576 channels, 144 KB, one buffer,
-// reloaded after the unit's last S) and a 2-deep ring of 32-key latent
-// tiles (36 KB each, [chunk][key][128 B], 128-byte swizzle, one TMA box per
-// page and chunk).  TMEM: S/P of even and odd tiles at columns 0 and 32, O
-// at 256.  MMAs issued by one thread complete in order, so S(i+1), issued
-// ahead of PV(i), may reuse the columns of S/P(i-1) once PV(i-1) is issued.
+// TMEM (512 columns): Q channels 0..383 as fp16 pairs [0, 192), S/P of even
+// and odd tiles [192, 224) and [224, 256), O [256, 512).  Shared memory: Q
+// channels 384..575 (48 KB) and a 4-deep ring of 32-key latent tiles (36 KB
+// each, [chunk][key][128 B], 128-byte swizzle, one TMA box per page and
+// chunk).  At a unit's start, once the previous unit's tiles are consumed,
+// Q's TMEM part is staged through the first three ring slots and copied
+// into TMEM (tcgen05.cp, in issue order before the unit's first S), then
+// the ring refills from slot 0.  MMAs issued by one thread complete in
+// order, so S(i+1), issued ahead of PV(i), may reuse the columns of
+// S/P(i-1) once PV(i-1) is issued.
 //
 // Warp roles (192 threads, one CTA per SM, persistent over the device
 // queue): warps 0-3 softmax and epilogue, warp 4 TMA producer, warp 5 TMEM
@@ -39,19 +44,24 @@ namespace {
 
 constexpr int kD = 576, kDV = 512, kHalf = kDV / 2;
 constexpr int kChunks = kD / 64;                  // 9 chunks of 64 channels
+constexpr int kQTChunks = 6;                      // Q chunks held in TMEM (channels 0..383)
+constexpr int kQSChunks = kChunks - kQTChunks;    // Q chunks read from shared memory
 constexpr int kKeys = 32;                         // keys per latent tile
 constexpr int kRows = 128;                        // query heads per unit (MMA M)
 constexpr int kThreads = 6 * 32;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
-constexpr int kQBytes = kChunks * kRows * 128;    // [chunk][head][128 B]
+constexpr int kQChunkBytes = kRows * 128;         // one chunk of Q [head][128 B]
+constexpr int kQSBytes = kQSChunks * kQChunkBytes;
 constexpr int kTileBytes = kChunks * kKeys * 128; // [chunk][key][128 B]
-constexpr int kStages = 2;
-constexpr int kOCol = 256;                        // TMEM columns: S/P at 0 and 32, O at 256
+constexpr int kStages = 4;
+constexpr int kQCol = 0, kSCol = kQTChunks * 4 * 8, kOCol = 256;  // TMEM columns
 constexpr int kTmemCols = 512;
-constexpr int kDataBytes = kQBytes + kStages * kTileBytes;
+constexpr int kDataBytes = kQSBytes + kStages * kTileBytes;
 constexpr int kSmemBytes = 1024 + kDataBytes + 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.f;
+static_assert(kQTChunks * kQChunkBytes <= 3 * kTileBytes, "Q staging fits the first ring slots");
+static_assert(kSCol + 64 <= kOCol, "TMEM columns");
 
 struct UnitInfo {
   int u;       // work unit; -1 = no more work
@@ -72,7 +82,7 @@ struct UnitInfo {
 struct Ctrl {
   UnitInfo info[2];
   uint32_t kv_mask[kStages];  // per stage: bit p = page p zero-filled (unmapped / past the end)
-  uint64_t q_full, q_empty;
+  uint64_t q_full, q_empty, q_staged;  // Q loaded; Q's shared-memory part free; Q's TMEM part copied
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[2], p_full, o_done;
   uint64_t info_full[2], info_empty[2];
@@ -97,14 +107,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Ring slot of tile i of a unit: the first tile goes to the slot that does
+// not stage Q, so its load overlaps the Q copy into TMEM.
+__device__ __forceinline__ int slot_of(int i) { return (i + kStages - 1) % kStages; }
+
 template <bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_l,
                   const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* q_s = smem;             // [kQBytes]
-  uint8_t* kv_s = q_s + kQBytes;   // [kStages][kTileBytes]
+  uint8_t* qs_s = smem;             // Q channels 384..575 [chunk][head][128 B]
+  uint8_t* kv_s = qs_s + kQSBytes;  // [kStages][kTileBytes]; slots 0-2 also stage Q channels 0..383
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kDataBytes);
   volatile int* abort = &ctl->abort;
 
@@ -119,9 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->q_empty, 1);
-    for (int i = 0; i < 2; ++i) {
+    mbar_init(&ctl->q_staged, 1);
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&ctl->kv_full[i], 1);
       mbar_init(&ctl->kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->s_full[i], 1);
       mbar_init(&ctl->info_full[i], 1);
       mbar_init(&ctl->info_empty[i], 1 + 4);  // MMA thread + 4 softmax warps
@@ -151,8 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm_l);
     }
     const int split_keys = p.counters->split_keys;
-    uint32_t g = 0;     // latent tiles loaded so far
-    int q_loads = 0;    // Q loads issued so far
+    uint32_t sp = 0, used = 0;  // per ring slot (bit): parity of its loads so far, any load issued
+    int q_loads = 0;
     bool ok = true;
     for (uint32_t tt = 0; ok; ++tt) {
       const int slot = tt & 1;
@@ -193,15 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         ti.kv_len = si.kv_len;
         ti.nsplit = si.dec_count;
         mbar_arrive(&ctl->info_full[slot]);
-        // Q: 128 heads of the token, one box {64, 128, 1} per chunk; the
-        // buffer is free once the previous unit's last S MMAs completed.
-        if (!wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err)) {
-          ok = false;
-        } else {
-          mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
+        // Q: the previous unit's tiles are all consumed (the staging slots
+        // are free) and its last S has completed (Q's shared-memory part is
+        // free); one box {64, 128, 1} per chunk.
+        for (int st = 0; st < kStages && ok; ++st)
+          ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err);
+        if (ok) ok = wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&ctl->q_full, kChunks * kQChunkBytes);
           ++q_loads;
           for (int c = 0; c < kChunks; ++c)
-            tma_load_3d(q_s + c * (kRows * 128), &tm_q, c * 64, ht * kRows, si.t0, &ctl->q_full);
+            tma_load_3d(c < kQTChunks ? kv_s + c * kQChunkBytes : qs_s + (c - kQTChunks) * kQChunkBytes, &tm_q,
+                        c * 64, ht * kRows, si.t0, &ctl->q_full);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -212,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_id = [&](int r) -> int { return (r < p.MB && r * p.bs < end) ? __ldg(bt_row + r) : -1; };
       int win = start / p.bs;
       int id = load_id(win + lane);
-      for (int i = 0; i < n_kv; ++i, ++g) {
-        const int st = g & 1;
+      for (int i = 0; i < n_kv; ++i) {
+        const int st = slot_of(i);
         const int key0 = start + i * kKeys;
         if ((key0 + kKeys - 1) / p.bs >= win + 32) {
           win = key0 / p.bs;
@@ -230,15 +250,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
         if (lane == 0) {
-          if (!wait_or_abort(&ctl->kv_empty[st], ((g >> 1) & 1) ^ 1, abort, p.err)) {
-            ok = false;
-          } else {
+          // the slots that staged Q are reused once its copy into TMEM is done
+          if (i == 1) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err);
+          if (ok) ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err);
+          if (ok) {
             ctl->kv_mask[st] = mask;
             mbar_arrive_expect_tx(&ctl->kv_full[st], kTileBytes);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        sp ^= 1u << st;
+        used |= 1u << st;
         // one box {64, 1, 2^log_r} per (page, chunk); lane -> (page, chunk)
         for (int base = 0; base < pages * kChunks; base += 32) {
           const int bx = base + lane;
@@ -249,25 +272,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lc * 64, 0, prc, &ctl->kv_full[st]);
         }
       }
+      // The next unit's Q overwrites the staging slots: a one-tile unit has
+      // not waited for its copy into TMEM yet.
+      if (ok && n_kv < 2) {
+        if (lane == 0) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
     }
     if (lane == 0 && *abort) {
       // Gave up: let the copies already issued land before the CTA exits.
       for (uint32_t i = 0; i < kWaitLimit && q_loads > 0 && !mbar_try_wait(&ctl->q_full, (q_loads - 1) & 1); ++i) {
       }
-      for (int d = 1; d <= 2 && (int)g - d >= 0; ++d) {
-        const uint32_t gl = g - d;
-        for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->kv_full[gl & 1], (gl >> 1) & 1); ++i) {
+      for (int st = 0; st < kStages; ++st)
+        for (uint32_t i = 0;
+             i < kWaitLimit && ((used >> st) & 1) && !mbar_try_wait(&ctl->kv_full[st], ((sp >> st) & 1) ^ 1); ++i) {
         }
-      }
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (one elect.sync-chosen lane: MMAs issued under it cost far fewer
+    // cycles than under a lane-index branch)
+    if (elect_one()) {
       constexpr uint32_t idesc_s = umma_idesc_f16(kRows, kKeys, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_f16(kRows, kHalf, 0, 1);
+      const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);          // K-major, + (address >> 4)
       const uint64_t desc_v = smem_desc_sw128(0, kKeys * 128, 1024);  // MN-major V, + (address >> 4)
-      const uint32_t q_addr = smem_u32(q_s), kv_addr = smem_u32(kv_s);
-      uint32_t g = 0, v = 0;
+      const uint32_t qs_addr = smem_u32(qs_s), kv_addr = smem_u32(kv_s);
+      uint32_t sp = 0;       // per ring slot (bit): parity of the tiles taken so far
+      uint32_t g = 0, v = 0;  // tiles (S buffers) and PVs so far
       bool ok = true;
       for (uint32_t tt = 0; ok; ++tt) {
         const int slot = tt & 1;
@@ -276,30 +308,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ti.u < 0) break;
         if (!wait_or_abort(&ctl->q_full, tt & 1, abort, p.err)) break;
         tc_fence_after();
-        // S(gi) = Q K_gi^T into TMEM columns [32 (gi & 1), +32): the columns
-        // of S/P(gi - 2), whose PV was issued before this.
-        auto issue_s = [&](uint32_t gi, bool last) -> bool {
-          const int st = gi & 1;
-          if (!wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) return false;
+        // Q channels 0..383 into TMEM (after the previous unit's last S in
+        // issue order); the staging slots are free once the copies complete.
+#pragma unroll
+        for (int ks = 0; ks < kQTChunks * 4; ++ks)
+          tmem_cp_128x256b(tmem + kQCol + 8 * ks, desc_k + ((kv_addr + (ks >> 2) * kQChunkBytes + (ks & 3) * 32) >> 4));
+        umma_commit(&ctl->q_staged);
+        // S(gi) = Q K^T into S buffer gi & 1: the columns of S/P(gi - 2),
+        // whose PV was issued before this.
+        auto issue_s = [&](uint32_t gi, int i, bool last) -> bool {
+          const int st = slot_of(i);
+          if (!wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err)) return false;
+          sp ^= 1u << st;
           tc_fence_after();
           const uint32_t kb = kv_addr + st * kTileBytes;
+          const uint32_t sc = tmem + kSCol + 32 * (gi & 1);
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ++ks) {
-            const uint64_t a = smem_desc_sw128(q_addr + (ks >> 2) * (kRows * 128) + (ks & 3) * 32, 16, 1024);
-            const uint64_t b = smem_desc_sw128(kb + (ks >> 2) * (kKeys * 128) + (ks & 3) * 32, 16, 1024);
-            umma_f16(tmem + 32 * st, a, b, idesc_s, ks > 0 ? 1u : 0u);
+            const uint64_t b = desc_k + ((kb + (ks >> 2) * (kKeys * 128) + (ks & 3) * 32) >> 4);
+            if (ks < kQTChunks * 4) {
+              umma_f16_ts(sc, tmem + kQCol + 8 * ks, b, idesc_s, ks > 0 ? 1u : 0u);
+            } else {
+              const int kq = ks - kQTChunks * 4;
+              const uint64_t a = desc_k + ((qs_addr + (kq >> 2) * kQChunkBytes + (kq & 3) * 32) >> 4);
+              umma_f16(sc, a, b, idesc_s, 1u);
+            }
           }
-          umma_commit(&ctl->s_full[st]);
+          umma_commit(&ctl->s_full[gi & 1]);
           if (last) umma_commit(&ctl->q_empty);
           return true;
         };
-        if (!issue_s(g, ti.n_kv == 1)) break;
+        if (!issue_s(g, 0, ti.n_kv == 1)) break;
         for (int i = 0; i < ti.n_kv; ++i) {
           const uint32_t gi = g + i;
-          const int st = gi & 1;
+          const int st = slot_of(i);
           // S(gi + 1) goes ahead of PV(gi): it runs while the softmax works
-          // on tile gi (its columns held P(gi - 1), whose PV is issued).
-          if (i + 1 < ti.n_kv && !issue_s(gi + 1, i + 2 == ti.n_kv)) {
+          // on tile gi.
+          if (i + 1 < ti.n_kv && !issue_s(gi + 1, i + 1, i + 2 == ti.n_kv)) {
             ok = false;
             break;
           }
@@ -314,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vb = kv_addr + st * kTileBytes + ti.half * (kHalf / 64) * (kKeys * 128);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
-            umma_f16_ts(tmem + kOCol, tmem + 32 * st + kk * 8, desc_v + ((vb + kk * 16 * 128) >> 4), idesc_o,
-                        (i > 0 || kk > 0) ? 1u : 0u);
+            umma_f16_ts(tmem + kOCol, tmem + kSCol + 32 * (gi & 1) + kk * 8, desc_v + ((vb + kk * 16 * 128) >> 4),
+                        idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&ctl->kv_empty[st]);
           umma_commit(&ctl->o_done);
         }
@@ -323,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mbar_arrive(&ctl->info_empty[slot]);
       }
-      // Drain: every MMA issued above has completed before TMEM is freed.
+      // Drain: every MMA and copy issued above has completed before TMEM is freed.
       umma_commit(&ctl->drain);
       for (uint32_t i = 0; i < kWaitLimit && !mbar_try_wait(&ctl->drain, 0); ++i) {
       }
@@ -337,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cap_in = CAP ? p.scale / p.softcap : 0.f;
     const float cap_out = CAP ? p.softcap * kLog2e : 0.f;
     uint32_t g = 0, v = 0;
+    uint32_t sp = 0;  // per ring slot (bit): parity of the tiles taken so far
     float x[kKeys];
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt & 1;
@@ -350,15 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int i = 0; i < ti.n_kv; ++i) {
         const uint32_t gi = g + i;
-        const int st = gi & 1;
+        const int sb = gi & 1;        // S buffer
+        const int st = slot_of(i);    // ring slot of the tile
         const int key0 = ti.key0 + i * kKeys;
-        if (!wait_or_abort(&ctl->s_full[st], (gi >> 1) & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->s_full[sb], (gi >> 1) & 1, abort, p.err) ||
+            !wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err)) {
           ok = false;
           break;
         }
+        sp ^= 1u << st;
         tc_fence_after();
-        tmem_ld32(lane_addr + 32 * st, x);
+        tmem_ld32(lane_addr + kSCol + 32 * sb, x);
         tmem_ld_wait();
         if constexpr (CAP) {
 #pragma unroll
@@ -431,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
         }
         // P -> TMEM over S: keys 0..31 as 16 columns of fp16 pairs
-        tmem_st16(lane_addr + 32 * st, pk);
+        tmem_st16(lane_addr + kSCol + 32 * sb, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();

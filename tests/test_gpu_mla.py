@@ -48,7 +48,7 @@ def _kernel_options(kernel, heads):
         if heads % 128:
             pytest.skip("the tcgen05 latent kernel serves multiples of 128 heads")
         return [(pa.PA_OPT_LATENT_TCGEN05, 1)]
-    return []
+    return [(pa.PA_OPT_LATENT_TCGEN05, 0)]
 
 
 @pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
