@@ -847,6 +847,11 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.prefill_tile_tokens = h->prefill_tile_tokens;
     p.split_keys_fixed = h->opt_split_keys;
     p.target_pairs = target_pairs_for(h, batch);
+    // A split of a tcgen05 latent unit leaves 128 heads x 256 channels of
+    // fp32 partials to merge; below 2048 keys the merge costs more than the
+    // balance gains (measured on the DeepSeek-V3-shaped step: automatic
+    // ~1984 keys 109 us, 2048 97 us, no split 136 us).
+    p.min_split_keys = h->mla_tc ? 2048 : pa::kStageKeys;
     p.cap_dec = h->cap_dec;
     p.cap_pre = h->cap_pre;
     p.cap_comb = h->cap_comb;
@@ -1166,6 +1171,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.prefill_tile_tokens = tile_tokens;
   wp.split_keys_fixed = 0;
   wp.target_pairs = target_pairs;
+  wp.min_split_keys = pa::kStageKeys;
   wp.cap_dec = cap_dec;
   wp.cap_pre = cap_pre;
   wp.cap_comb = cap_comb;

@@ -71,6 +71,7 @@ struct WorklistParams {
   int prefill_tile_tokens; // tokens per prefill tile
   int split_keys_fixed;    // > 0 forces keys per split
   int target_pairs;        // desired number of decode (b, split) items
+  int min_split_keys;      // smallest automatic split (a multiple of 64)
   int cap_dec, cap_pre, cap_comb;
   // SM split between the prefill and decode kernels.  With split_sms > 0
   // the prefill kernel is launched first, one CTA per SM, and the work list

@@ -131,7 +131,7 @@ __device__ int split_keys_for(const WorklistParams& p, long long total) {
   if (p.split_keys_fixed > 0) return p.split_keys_fixed;
   long long per = (total + p.target_pairs - 1) / max(p.target_pairs, 1);
   per = (per + kStageKeys - 1) / kStageKeys * kStageKeys;
-  return (int)min(max(per, (long long)kStageKeys), (long long)(1 << 30));
+  return (int)min(max(per, (long long)max(p.min_split_keys, kStageKeys)), (long long)(1 << 30));
 }
 
 // SM split for a step with both decode and prefill work: the prefill CTAs
