@@ -704,10 +704,18 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.rot_dim = h->R;
   p.rot_positions = c.max_rotary_positions;
   p.rot_offset = c.rotary_offset;
+  // A latent query copy keeps only the 64-channel chunks that hold rotated
+  // channels; the latent kernels read the others from the query itself.
+  p.q_keep_lo = 0;
+  p.q_keep_hi = c.head_size;
+  if (h->latent && c.do_rotary) {
+    p.q_keep_lo = c.rotary_offset / 64 * 64;
+    p.q_keep_hi = (c.rotary_offset + h->R + 63) / 64 * 64;
+  }
   // Spread a token over several warps when Q is rotated too: one for the
   // K/V rows and one per kv_num_heads query heads (same size as a K row).
   p.q_heads_per_part = c.kv_num_heads;
-  p.parts = 1 + (p.q_rot ? (c.num_heads + c.kv_num_heads - 1) / c.kv_num_heads : 0);
+  p.parts = 1 + (p.q_rot ? (c.num_heads + p.q_heads_per_part - 1) / p.q_heads_per_part : 0);
   p.err = h->err;
   return p;
 }
@@ -876,9 +884,15 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     // split partials
     const int qt = 1;
     const int tile_rows = std::min(c.block_size, 32);
-    CUtensorMap tq, tl;
-    if (!encode_map(&tq, q_att, D, c.num_heads, token_count, h->mla_tc ? 128 : pa::kDecodeRows, qt))
+    const int q_rows = h->mla_tc ? 128 : pa::kDecodeRows;
+    // with rotary the query's rotated chunks come from the copy, the rest
+    // from the query itself
+    const bool q_split = q_att != static_cast<const __half*>(query);
+    CUtensorMap tq, tqr, tl;
+    if (!encode_map(&tq, query, D, c.num_heads, token_count, q_rows, qt) ||
+        (q_split && !encode_map(&tqr, q_att, D, c.num_heads, token_count, q_rows, qt)))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
+    if (!q_split) tqr = tq;
     if (h->mla_tc && !encode_map(&tl, key_cache, D, 1, pool_rows, 1, tile_rows))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the latent pool");
     pa::MlaParams p{};
@@ -901,10 +915,12 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.oob_row = pool_rows;
     p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
     p.log_tile_rows = 31 - __builtin_clz((unsigned)tile_rows);
+    p.qr_lo = q_split ? c.rotary_offset / 64 : 0;
+    p.qr_hi = q_split ? (c.rotary_offset + h->R + 63) / 64 : 0;
     {
       StageTimer t(h, PA_STAGE_DECODE, s);
-      cudaError_t e = h->mla_tc ? pa::launch_mla_tc(tq, tl, p, h->dec_grid, s)
-                                : pa::launch_mla_decode(tk, tq, p, h->dec_grid, s);
+      cudaError_t e = h->mla_tc ? pa::launch_mla_tc(tq, tqr, tl, p, h->dec_grid, s)
+                                : pa::launch_mla_decode(tk, tq, tqr, p, h->dec_grid, s);
       if (e != cudaSuccess) return cuda_fail(h, e, "latent decode launch");
       h->last_launches++;
     }

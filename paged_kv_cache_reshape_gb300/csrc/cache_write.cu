@@ -127,11 +127,15 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
 // Copies (rotate = false) or rotates one [nheads, D] row of src and hands
 // every 8-channel group to `emit`.  With rn (QK-Norm factors per head) and
 // nw (the [D] weight), every loaded value is first normalized.  R % 16 == 0
-// is checked on the host.
+// is checked on the host.  Channels outside [keep_lo, keep_hi) that are not
+// rotated are not emitted at all (a latent query's copy keeps only the
+// 64-channel chunks that hold its rotated channels).
 template <typename Emit>
 __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
                               int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
-                              const float* rn = nullptr, const __half* nw = nullptr, int off = 0) {
+                              const float* rn = nullptr, const __half* nw = nullptr, int off = 0, int keep_lo = 0,
+                              int keep_hi = 1 << 30) {
+  const bool keep_all = keep_lo <= 0 && keep_hi >= D;
   const int chunks_per_head = D / 8;
   auto ld8 = [&](int h, int ch) -> Vec8 {
     Vec8 v;
@@ -148,7 +152,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
   };
   if (!rotate) {
     if constexpr (std::is_same<Emit, EmitHalf>::value) {
-      if (!rn) {  // plain copy of a contiguous [nheads, D] row
+      if (!rn && keep_all) {  // plain copy of a contiguous [nheads, D] row
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(emit.dst);
         for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = __ldg(s4 + i);
@@ -157,7 +161,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
     }
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       const int h = i / chunks_per_head, ch = 8 * (i % chunks_per_head);
-      emit(h, ch, ld8(h, ch));
+      if (ch >= keep_lo && ch < keep_hi) emit(h, ch, ld8(h, ch));
     }
     return;
   }
@@ -181,7 +185,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
       } else {
         const int cc = 8 * (c - pairs);
         const int ch = cc < off ? cc : cc + R;
-        emit(h, ch, ld8(h, ch));
+        if (ch >= keep_lo && ch < keep_hi) emit(h, ch, ld8(h, ch));
       }
     }
   } else {
@@ -189,8 +193,10 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
     const int rchunks = R / 8, c0 = off / 8;
     for (int i = lane; i < nheads * chunks_per_head; i += 32) {
       int h = i / chunks_per_head, c = i % chunks_per_head;
+      const bool rot = c >= c0 && c < c0 + rchunks;
+      if (!rot && (8 * c < keep_lo || 8 * c >= keep_hi)) continue;
       Vec8 a = ld8(h, 8 * c), y;
-      if (c >= c0 && c < c0 + rchunks) {
+      if (rot) {
         uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * (c - c0)));
         uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * (c - c0)));
         const __half* cv = reinterpret_cast<const __half*>(&cu);
@@ -256,7 +262,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
                     p.rot_offset);
     else
       row_transform(qsrc, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
-                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset);
+                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset, p.q_keep_lo, p.q_keep_hi);
     return;
   }
 

@@ -79,6 +79,7 @@ __device__ __forceinline__ uint32_t tile_off(int kk, int chunk, int col16, int l
 
 __global__ void __launch_bounds__(kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tm_l, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_qr,
                       const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_l);
       prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_qr);
     }
     const int split_keys = p.counters->split_keys;
     const int boxes = kKeys >> p.log_box_rows;
@@ -160,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&q_full[qi], kQBytes);
           for (int c = 0; c < kChunks; ++c)
             for (int w = 0; w < 2; ++w)  // rows past H (a group beyond the heads) read as zeros
-              tma_load_3d(qbuf + qi * kQBytes + c * 4096 + w * 2048, &tm_q, c * 64, hg * 32 + w * 16, si.t0,
+              tma_load_3d(qbuf + qi * kQBytes + c * 4096 + w * 2048, c >= p.qr_lo && c < p.qr_hi ? &tm_qr : &tm_q,
+                          c * 64, hg * 32 + w * 16, si.t0,
                           &q_full[qi]);
         }
       }
@@ -456,9 +459,9 @@ cudaError_t mla_configure(size_t* smem) {
   return cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
 }
 
-cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const MlaParams& p, int grid,
-                              cudaStream_t s) {
-  return launch_pdl(mla_decode_kernel, grid, kThreads, kSmemBytes, s, tl, tq, p);
+cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const CUtensorMap& tqr, const MlaParams& p,
+                              int grid, cudaStream_t s) {
+  return launch_pdl(mla_decode_kernel, grid, kThreads, kSmemBytes, s, tl, tq, tqr, p);
 }
 
 }  // namespace pa

@@ -113,8 +113,8 @@ __device__ __forceinline__ int slot_of(int i) { return (i + kStages - 1) % kStag
 
 template <bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_l,
-                  const MlaParams p) {
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qr,
+                  const __grid_constant__ CUtensorMap tm_l, const MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs_s = smem;             // Q channels 384..575 [chunk][head][128 B]
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_qr);
       prefetch_tmap(&tm_l);
     }
     const int split_keys = p.counters->split_keys;
@@ -220,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&ctl->q_full, kChunks * kQChunkBytes);
           ++q_loads;
           for (int c = 0; c < kChunks; ++c)
-            tma_load_3d(c < kQTChunks ? kv_s + c * kQChunkBytes : qs_s + (c - kQTChunks) * kQChunkBytes, &tm_q,
-                        c * 64, ht * kRows, si.t0, &ctl->q_full);
+            tma_load_3d(c < kQTChunks ? kv_s + c * kQChunkBytes : qs_s + (c - kQTChunks) * kQChunkBytes,
+                        c >= p.qr_lo && c < p.qr_hi ? &tm_qr : &tm_q, c * 64, ht * kRows, si.t0, &ctl->q_full);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -556,10 +557,10 @@ cudaError_t mla_tc_configure(size_t* smem) {
   return e != cudaSuccess ? e : configure_cap<true>();
 }
 
-cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tl, const MlaParams& p, int grid,
-                          cudaStream_t s) {
-  if (p.softcap > 0.f) return launch_pdl(mla_tc_kernel<true>, grid, kThreads, kSmemBytes, s, tq, tl, p);
-  return launch_pdl(mla_tc_kernel<false>, grid, kThreads, kSmemBytes, s, tq, tl, p);
+cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tqr, const CUtensorMap& tl, const MlaParams& p,
+                          int grid, cudaStream_t s) {
+  if (p.softcap > 0.f) return launch_pdl(mla_tc_kernel<true>, grid, kThreads, kSmemBytes, s, tq, tqr, tl, p);
+  return launch_pdl(mla_tc_kernel<false>, grid, kThreads, kSmemBytes, s, tq, tqr, tl, p);
 }
 
 }  // namespace pa

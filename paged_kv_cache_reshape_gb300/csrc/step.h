@@ -123,6 +123,9 @@ struct CacheWriteParams {
   int H, Hk, D, bs, NB, MB;
   int rotary, interleaved, rot_dim, rot_positions;
   int rot_offset;        // first rotated channel (latent rows rotate their last rot_dim channels)
+  int q_keep_lo, q_keep_hi;  // channels of the query copy written besides the rotated ones (latent:
+                             // the 64-channel chunks holding them; the kernels read the rest from
+                             // the query itself)
   int q_scale;           // 1: the query copy is multiplied by k_scale (8-bit caches)
   int parts;             // warps per token: 1 (K/V) + query parts when Q is transformed
   int q_heads_per_part;  // query heads per query part
@@ -206,6 +209,8 @@ struct MlaParams {
   int oob_row;
   int log_box_rows;      // log2(min(block_size, 64))
   int log_tile_rows;     // log2(min(block_size, 32)): pool rows per box of the tensor-core kernel
+  int qr_lo, qr_hi;      // query chunks [qr_lo, qr_hi) read from the rotated copy (map tm_qr),
+                         // the others from the query (map tm_q)
 };
 
 // Launch with the programmatic stream-serialization attribute, so the
@@ -242,9 +247,11 @@ cudaError_t mla_configure(size_t* smem);
 // and half of the value channels; Q map boxes {64, 128 heads, 1 token}, pool
 // map boxes {64, 1, min(block_size, 32) rows}.
 cudaError_t mla_tc_configure(size_t* smem);
-cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tl, const MlaParams& p, int grid,
+cudaError_t launch_mla_tc(const CUtensorMap& tq, const CUtensorMap& tqr, const CUtensorMap& tl, const MlaParams& p,
+                          int grid,
                           cudaStream_t s);
-cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const MlaParams& p, int grid,
+cudaError_t launch_mla_decode(const CUtensorMap& tl, const CUtensorMap& tq, const CUtensorMap& tqr, const MlaParams& p,
+                              int grid,
                               cudaStream_t s);
 cudaError_t prefill_configure(int head_size, size_t* smem);
 int prefill_keys_per_tile(int head_size);
