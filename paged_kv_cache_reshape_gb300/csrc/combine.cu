@@ -21,17 +21,19 @@ namespace {
 constexpr int kWarps = 8;
 constexpr float kLog2eC = 1.4426950408889634f;
 
-// Adds f * (8 or 4 or kPer floats at po) into acc.
+// Adds f * (the kPer floats at po) into acc, in 16-byte loads when kPer
+// is a multiple of 4.
 template <int kPer>
 __device__ __forceinline__ void axpy(float* acc, float f, const float* po) {
-  if constexpr (kPer == 8) {
-    const float4 a = *reinterpret_cast<const float4*>(po);
-    const float4 b = *reinterpret_cast<const float4*>(po + 4);
-    acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
-    acc[4] += f * b.x; acc[5] += f * b.y; acc[6] += f * b.z; acc[7] += f * b.w;
-  } else if constexpr (kPer == 4) {
-    const float4 a = *reinterpret_cast<const float4*>(po);
-    acc[0] += f * a.x; acc[1] += f * a.y; acc[2] += f * a.z; acc[3] += f * a.w;
+  if constexpr (kPer % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < kPer; i += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(po + i);
+      acc[i] += f * a.x;
+      acc[i + 1] += f * a.y;
+      acc[i + 2] += f * a.z;
+      acc[i + 3] += f * a.w;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] += f * po[i];
@@ -121,9 +123,17 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     __half* out = p.out + ((size_t)tb.x * p.H + h) * D + lane * kPer;
+    if constexpr (kPer % 8 == 0) {
 #pragma unroll
-    for (int i = 0; i < kPer; i += 2) {
-      *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+      for (int i = 0; i < kPer; i += 8)
+        *reinterpret_cast<uint4*>(out + i) =
+            make_uint4(pack_half2(acc[i] * inv, acc[i + 1] * inv), pack_half2(acc[i + 2] * inv, acc[i + 3] * inv),
+                       pack_half2(acc[i + 4] * inv, acc[i + 5] * inv), pack_half2(acc[i + 6] * inv, acc[i + 7] * inv));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kPer; i += 2) {
+        *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
+      }
     }
   }
 }
