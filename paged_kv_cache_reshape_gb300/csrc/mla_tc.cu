@@ -444,14 +444,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c / 2] = pack_half2(e0, e1);
         }
         l = l * alpha + rs;
-        // PV(gi - 1) must be done before O is rescaled.
-        if (i > 0) {
+        // PV(gi - 1) must be done before O is rescaled; P(gi) goes to the
+        // other S buffer, so without a rescale the warp does not wait.  (A
+        // skipped wait is safe: o_done cannot run a phase ahead of the one
+        // waited for next, since PV(gi) needs this warp's P(gi).)
+        if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          {
             float o[32];
 #pragma unroll 1
             for (int c = 0; c < kHalf / 32; ++c) {

@@ -170,3 +170,20 @@ def test_full_size_mixed_step():
     op, out, err = run(step)
     assert err == 0, f"device error {err:#x}"
     check_sampled(host, step, out, n_rows=160)
+
+
+@pytest.mark.parametrize("items", [0, 1, 2, 7, 32])
+def test_items_per_cta_option(items):
+    """PA_OPT_DECODE_ITEMS_PER_CTA: 0 (chosen per step from the batch) and
+    fixed counts size the splits differently; every choice is correct."""
+    shape = cs("items_per_cta", 8, 2, 128, 16, [3000, 70, 2047, 300, 1], [1, 1, 2, 1, 1], seed=91)
+    _full(shape, options=[(pa.PA_OPT_DECODE_ITEMS_PER_CTA, items)])
+
+
+def test_items_per_cta_option_range():
+    step = make(cs("items_rule", 8, 2, 128, 16, [10], [1], seed=92), device="cuda", gen_device="cpu")
+    op = pa.PagedAttention.for_step(step, max_query_len_bound=1)
+    for bad in (-1, 33):
+        with pytest.raises(pa.PAError) as e:
+            op.set_option(pa.PA_OPT_DECODE_ITEMS_PER_CTA, bad)
+        assert e.value.status == pa.PA_INVALID_ARGUMENT
