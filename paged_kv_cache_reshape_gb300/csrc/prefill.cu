@@ -278,7 +278,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (one elect.sync-chosen lane: MMAs issued under it cost far fewer
+    // cycles than under a lane-index branch)
+    if (elect_one()) {
       constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, KEYS, 0, 0);
       constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
       const uint32_t p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
