@@ -70,3 +70,33 @@ def test_graph_replay_with_growing_context(window, softcap):
         assert np.array_equal(bits(dev["key_cache"]), kc), f"step {i}: key pool"
         assert np.array_equal(bits(dev["value_cache"]), vc), f"step {i}: value pool"
         assert_close(out.float().cpu().numpy().reshape(T, H, D), ref, what=f"step {i}")
+
+
+@pytest.mark.parametrize("heads", [128, 32])
+def test_latent_step_replays_in_a_graph(heads):
+    """A latent step (tcgen05 kernel at 128 heads, mma.sync at 32) captured
+    once and replayed with new query values gives the eager outputs bit for
+    bit (the cache write is idempotent for the same new rows)."""
+    shape = workloads.custom_shape("latent_graph", heads, 1, 576, 64, [300, 2500, 17, 1200], [1] * 4,
+                                   scale=0.0723, do_rotary=1, rotary_dim=64, seed=23)
+    dev = workloads.make_step(shape, device="cuda", gen_device="cpu", latent_v_head_size=512)
+    op = pa.PagedAttention.for_step(dev, max_query_len_bound=1)
+    out = torch.zeros(4, heads * 512, dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    op.forward(dev, out, stream=s.cuda_stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        op.forward(dev, out, stream=s.cuda_stream)
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(7)
+    for _ in range(2):
+        dev["query"].copy_(torch.randn(dev["query"].shape, generator=gen).half())
+        eager = torch.zeros_like(out)
+        op.forward(dev, eager, stream=s.cuda_stream)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert op.device_error() == 0
+        assert torch.equal(out, eager)
