@@ -1010,6 +1010,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.window = c.local_window_size;
     p.oob_row = pool_rows;
     p.wait_prologue = pre_launch ? 0 : 1;
+    p.bt_lines = p.wait_prologue ? (int)(((long long)batch * c.max_blocks_per_seq + 31) / 32) : 0;
     StageTimer t(h, PA_STAGE_DECODE, s);
     cudaError_t e = pa::launch_decode(D, tk, tv, tq, p, h->dec_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "decode launch");

@@ -163,14 +163,9 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
   uint64_t* q_full = empty + C::kStages;
   uint64_t* q_empty = q_full + 2;
 
-  // Everything below reads the prologue's work list and the pool it wrote.
-  // Launched right after the prologue it waits for it; launched after the
-  // prefill kernel (which waited for the prologue before letting this kernel
-  // start) it runs beside the prefill on the SMs the prefill left free.
-  if (p.wait_prologue) griddep_wait();
-  const int active = min(p.counters->dec_ctas, p.counters->n_dec * p.Hk);
-  if ((int)blockIdx.x >= active) return;  // no item, or an SM kept for the prefill
-
+  // What does not read the prologue's results is done before waiting for
+  // it: barriers, tensor-map prefetch, and this CTA's slice of the block
+  // table (a step input) pulled into L2 for the first items' page lookups.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -183,16 +178,27 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
     }
     fence_mbar_init();
   }
+  if (warp == kDecodeWarps && lane == 0) {
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_q);
+  }
+  if (p.bt_lines > 0)
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.bt_lines; i += gridDim.x * kThreads)
+      prefetch_l2(p.block_table + (size_t)i * 32);
+
+  // Everything below reads the prologue's work list and the pool it wrote.
+  // Launched right after the prologue it waits for it; launched after the
+  // prefill kernel (which waited for the prologue before letting this kernel
+  // start) it runs beside the prefill on the SMs the prefill left free.
+  if (p.wait_prologue) griddep_wait();
+  const int active = min(p.counters->dec_ctas, p.counters->n_dec * p.Hk);
+  if ((int)blockIdx.x >= active) return;  // no item, or an SM kept for the prefill
   __syncthreads();
   griddep_launch_dependents();
 
   if (warp == kDecodeWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      prefetch_tmap(&tm_q);
-    }
     const int n_work = p.counters->n_dec * p.Hk;
     const int split_keys = p.counters->split_keys;
     const int boxes = kStageKeys >> p.log_box_rows;

@@ -121,6 +121,11 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Pulls the 128-byte line holding p into L2 (a hint; nothing is returned).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Register split between warpgroups: every warp of a warpgroup resizes its
 // registers per thread to N (a multiple of 8 in [24, 256]); the sum over the
 // CTA's warpgroups must stay within the registers the CTA was launched with.

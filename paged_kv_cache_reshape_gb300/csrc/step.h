@@ -152,6 +152,7 @@ struct DecodeParams {
   int oob_row;       // a TMA row coordinate past the pool (zero fill)
   int q_tile_tokens; // tokens per query TMA box (16 / G)
   int log_box_rows;  // log2(min(block_size, 64)): pool rows per TMA box
+  int bt_lines;      // 128-byte lines of the block table (batch rows) to pull into L2 first; 0 = none
   int wait_prologue; // 1: the launch before is the prologue (griddepcontrol.wait
                      // on it); 0: it is the prefill kernel, which has waited for
                      // the prologue before letting this kernel start, and this
