@@ -915,6 +915,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.oob_row = pool_rows;
     p.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
     p.log_tile_rows = 31 - __builtin_clz((unsigned)tile_rows);
+    p.bt_lines = (int)(((long long)batch * c.max_blocks_per_seq + 31) / 32);
     p.qr_lo = q_split ? c.rotary_offset / 64 : 0;
     p.qr_hi = q_split ? (c.rotary_offset + h->R + 63) / 64 : 0;
     {

@@ -122,13 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + kDataBytes);
   volatile int* abort = &ctl->abort;
 
-  griddep_wait();  // the work list and the latent rows come from the prologue
-  const int n_ht = p.H / kRows;
-  const int per_item = 2 * n_ht;  // units per (sequence, split)
-  const int n_work = p.counters->n_dec * per_item;
-  const int active = min(p.counters->dec_ctas, n_work);
-  if ((int)blockIdx.x >= active) return;
-
+  // Barriers, tensor-map prefetch and an L2 prefetch of the block table (a
+  // step input) before waiting for the prologue; TMEM only once this CTA
+  // knows it has work.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
@@ -149,6 +145,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     ctl->abort = 0;
     fence_mbar_init();
   }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_qr);
+    prefetch_tmap(&tm_l);
+  }
+  for (int i = blockIdx.x * kThreads + threadIdx.x; i < p.bt_lines; i += gridDim.x * kThreads)
+    prefetch_l2(p.block_table + (size_t)i * 32);
+
+  griddep_wait();  // the work list and the latent rows come from the prologue
+  const int n_ht = p.H / kRows;
+  const int per_item = 2 * n_ht;  // units per (sequence, split)
+  const int n_work = p.counters->n_dec * per_item;
+  const int active = min(p.counters->dec_ctas, n_work);
+  if ((int)blockIdx.x >= active) return;
+
   if (warp == kMmaWarp) {
     tmem_alloc(&ctl->tmem_base, kTmemCols);
     tmem_relinquish();
@@ -163,11 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_qr);
-      prefetch_tmap(&tm_l);
-    }
     const int split_keys = p.counters->split_keys;
     uint32_t sp = 0, used = 0;  // per ring slot (bit): parity of its loads so far, any load issued
     int q_loads = 0;

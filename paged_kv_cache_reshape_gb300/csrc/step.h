@@ -210,6 +210,7 @@ struct MlaParams {
   int oob_row;
   int log_box_rows;      // log2(min(block_size, 64))
   int log_tile_rows;     // log2(min(block_size, 32)): pool rows per box of the tensor-core kernel
+  int bt_lines;          // 128-byte lines of the block table (batch rows) to pull into L2 first
   int qr_lo, qr_hi;      // query chunks [qr_lo, qr_hi) read from the rotated copy (map tm_qr),
                          // the others from the query (map tm_q)
 };
