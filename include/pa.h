@@ -130,7 +130,7 @@ enum { PA_QUANT_NONE = 0, PA_QUANT_PER_TENSOR = 1, PA_QUANT_PER_CHANNEL = 2 };
 typedef struct {
   int num_heads;          /* H, > 0, multiple of kv_num_heads */
   int kv_num_heads;       /* Hk, > 0 */
-  int head_size;          /* D, multiple of 8; this build runs 64, 128, 256 */
+  int head_size;          /* D, multiple of 8; the library runs 64, 128, 256 (576 with the latent layout) */
   int block_size;         /* bs, power of two >= 16 */
   int num_blocks;         /* NB, > 0 */
   int max_blocks_per_seq; /* MB, > 0 (block_table row length) */

@@ -322,7 +322,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "qk_norm_epsilon must be finite and > 0 (got %g)", c->qk_norm_epsilon);
     return PA_INVALID_ARGUMENT;
   }
-  // Valid, but outside what this build runs.
+  // Valid, but outside what this library runs.
   if (latent) {
     const int dv = c->v_head_size ? c->v_head_size : c->head_size;
     const long long qb =
@@ -343,7 +343,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     return PA_OK;
   }
   if (c->head_size != 64 && c->head_size != 128 && c->head_size != 256) {
-    set_msg(msg, len, "head_size %d is valid but this build runs 64, 128 and 256", c->head_size);
+    set_msg(msg, len, "head_size %d is valid but this library runs 64, 128 and 256", c->head_size);
     return PA_NOT_SUPPORTED;
   }
   if (c->num_heads / c->kv_num_heads > 128) {
@@ -351,7 +351,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     return PA_NOT_SUPPORTED;
   }
   if (c->do_rotary && rot_dim_of(*c) % 16 != 0) {
-    set_msg(msg, len, "rotary_dim %d is valid but this build needs a multiple of 16", rot_dim_of(*c));
+    set_msg(msg, len, "rotary_dim %d is valid but this library needs a multiple of 16", rot_dim_of(*c));
     return PA_NOT_SUPPORTED;
   }
   if (c->qk_norm && c->kv_num_heads > 32) {
@@ -360,7 +360,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
   }
   if (c->cache_dtype != PA_CACHE_FP16) {
     if (c->k_quant_type != c->v_quant_type) {
-      set_msg(msg, len, "k_quant_type and v_quant_type must match in this build");
+      set_msg(msg, len, "k_quant_type and v_quant_type must match in this library");
       return PA_NOT_SUPPORTED;
     }
     if (c->head_size == 64) {
