@@ -4,6 +4,8 @@ Design Document", section 12), each against something other than the oracle:
   * latent attention -> torch scaled_dot_product_attention in fp64 with K the
                         576-channel latent rows (one kv head shared by every
                         query head) and V their first 512 channels
+  * window + softcap -> the masks and cap * tanh(scale * q.k / cap) written
+                        out on the dense latent rows, fp64 softmax
   * offset rotary    -> complex multiplication of the channels
                         [offset, offset + R) by the tables' cos + i sin (numpy
                         complex128) within one fp16 ulp, every other channel
@@ -45,6 +47,33 @@ def test_latent_attention_matches_sdpa():
         mask = torch.arange(L)[None, :] <= int(past[b]) + j
         ref = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask, scale=0.07)[0].transpose(0, 1)
         np.testing.assert_allclose(res["out"][t0:t1], ref.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_latent_attention_with_window_and_softcap():
+    """Window (each row admits [pos + 1 - W, pos]) and softcap
+    (cap * tanh(scale * q.k / cap)) written out on the dense latent rows:
+    explicit fp64 scores, masks and softmax, V = the first 512 channels."""
+    H, D, Dv, bs, W, cap, scale = 4, 576, 512, 16, 20, 5.0, 0.07
+    shape = workloads.custom_shape("mla_pin_wc", H, 1, D, bs, [50, 3], [2, 1], scale=scale, softcap=cap,
+                                   local_window_size=W, seed=62)
+    step = workloads.make_step(shape, latent_v_head_size=Dv)
+    res = oracle.forward(step)
+    kc = torch.from_numpy(res["key_cache"].view(np.float16).astype(np.float32)).double()
+    bt, cum, past = step["block_table"], step["cumulative_sequence_lengths"], step["past_sequence_lengths"]
+    q = torch.from_numpy(res["query_rot"].view(np.float16).astype(np.float32)).double().view(-1, H, D)
+    for b in range(step["batch"]):
+        t0, t1 = int(cum[b]), int(cum[b + 1])
+        L = int(past[b]) + (t1 - t0)
+        rows = torch.stack([kc[int(bt[b, p // bs]), p % bs, 0] for p in range(L)])  # [L, D]
+        for j in range(t1 - t0):
+            pos = int(past[b]) + j
+            keys = torch.arange(L)
+            ok = (keys <= pos) & (keys >= pos + 1 - W)
+            sc = cap * torch.tanh(scale * (q[t0 + j] @ rows.T) / cap)                # [H, L]
+            sc = sc.masked_fill(~ok[None, :], float("-inf"))
+            p = torch.softmax(sc, dim=-1)
+            ref = p @ rows[:, :Dv]                                                     # [H, Dv]
+            np.testing.assert_allclose(res["out"][t0 + j], ref.numpy(), rtol=1e-10, atol=1e-12)
 
 
 def test_offset_rotary_matches_complex_rotation():
