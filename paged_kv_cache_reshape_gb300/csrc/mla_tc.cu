@@ -91,22 +91,6 @@ struct Ctrl {
   int abort;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023) == 1023 && *abort) return false;
-  }
-  *abort = 1;
-  atomicOr(err, PA_DEVERR_TIMEOUT);
-  return false;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Ring slot of tile i of a unit: the first tile goes to the slot that does
 // not stage Q, so its load overlaps the Q copy into TMEM.
 __device__ __forceinline__ int slot_of(int i) { return (i + kStages - 1) % kStages; }

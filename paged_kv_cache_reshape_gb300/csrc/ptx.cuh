@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 // Iteration cap for every mbarrier wait.  try_wait suspends the thread for
@@ -119,6 +121,25 @@ __device__ __forceinline__ bool elect_one() {
       "selp.u32 %0, 1, 0, P;\n\t}\n"
       : "=r"(pred));
   return pred != 0;
+}
+
+// Bounded mbarrier wait of the tcgen05 kernels: gives up (returns false)
+// when another role of the CTA has set *abort, or after kWaitLimit polls,
+// setting *abort and PA_DEVERR_TIMEOUT itself.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 1023) == 1023 && *abort) return false;
+  }
+  *abort = 1;
+  atomicOr(err, PA_DEVERR_TIMEOUT);
+  return false;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Pulls the 128-byte line holding p into L2 (a hint; nothing is returned).
