@@ -20,8 +20,10 @@ from concurrent.futures import ThreadPoolExecutor
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# PA_ORACLE_SOURCE names another copy of oracle.c (the pin-strength test runs
+# the pins against deliberately broken copies); its library is built beside it.
+_SRC = os.environ.get("PA_ORACLE_SOURCE") or os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(os.path.dirname(os.path.abspath(_SRC)), "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
