@@ -269,35 +269,24 @@ int oracle_rotary_offset(const uint16_t* x, uint16_t* y, int T, int nheads, int 
 /* RMS normalization of every head of every row of x ([T, nheads*D] fp16),
  * written as fp16 to y (may alias x): per head
  *   y[c] = fp16( (x[c] * r) * w[c] ),  r = 1 / sqrt(sum_j x[j]^2 / D + eps),
- * the sum of squares in fp32.  The pages fix the formula, not the order of
- * the fp32 sum; this oracle takes one fixed order, which a 32-lane warp
- * reproduces exactly: partial sums s_l = sum over k of x[l + 32k]^2 for
- * l = 0..31 (k ascending, one rounding per multiply and per add), then
- * s_l += s_(l xor o) for o = 16, 8, 4, 2, 1 (every lane ends with the same
- * value); the mean is the sum times 1/D (exact: D is a power of two), then
- * + eps, IEEE square root, IEEE reciprocal.  For D < 32 lanes past D hold 0. */
+ * the sum of squares in fp32.  The pages fix the formula and an fp32 sum,
+ * not its order; this oracle takes the plainest one: one running fp32 sum
+ * over the channels in ascending order, one rounding per square and per
+ * add.  The mean is the sum times 1/D (exact: D is a power of two), then
+ * + eps, IEEE square root, IEEE reciprocal. */
 int oracle_qk_norm(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const uint16_t* w, float eps) {
   if (D <= 0 || D > 1024 || (D & (D - 1)) != 0) return ORACLE_BAD_ARGUMENT;
   for (int t = 0; t < T; ++t) {
     for (int h = 0; h < nheads; ++h) {
       const uint16_t* xr = x + ((size_t)t * nheads + h) * D;
       uint16_t* yr = y + ((size_t)t * nheads + h) * D;
-      float part[32];
-      for (int l = 0; l < 32; ++l) {
-        float acc = 0.0f;
-        for (int c = l; c < D; c += 32) {
-          float v = (float)oracle_half_to_double(xr[c]);
-          float sq = v * v;
-          acc = acc + sq;
-        }
-        part[l] = acc;
+      float sum = 0.0f;
+      for (int c = 0; c < D; ++c) {
+        float v = (float)oracle_half_to_double(xr[c]);
+        float sq = v * v;
+        sum = sum + sq;
       }
-      for (int o = 16; o >= 1; o >>= 1) {
-        float nxt[32];
-        for (int l = 0; l < 32; ++l) nxt[l] = part[l] + part[l ^ o];
-        memcpy(part, nxt, sizeof(nxt));
-      }
-      float mean = part[0] * (1.0f / (float)D);
+      float mean = sum * (1.0f / (float)D);
       float v = mean + eps;
       float r = 1.0f / sqrtf(v);
       uint16_t tmp[1024];

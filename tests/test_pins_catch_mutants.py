@@ -9,7 +9,8 @@ plausibly make: the GQA head map, the causal and window bounds, softcap
 without its outer factor, the default 1/sqrt(D) scale, the head_sink term,
 the sign and pairing of the rotation and its channel offset, the slot
 derivation, the binary16 and e4m3fn roundings, int8 rounding and
-clipping, the per-channel scale index, the QK-Norm epsilon and weight, and
+clipping, the per-channel scale index, the QK-Norm epsilon, weight and the
+order and precision of its sum of squares, and
 the latent layout (scores over all 576 channels, values from the first
 512).
 """
@@ -56,6 +57,9 @@ MUTANTS = [
      "oracle_quantize(key[(size_t)t * row + e], v_scale[si]", 1, None),
     ("QK-Norm without epsilon", "float v = mean + eps;", "float v = mean;", 1, None),
     ("QK-Norm without weight", "float b = a * (float)oracle_half_to_double(w[c]);", "float b = a;", 1, None),
+    ("QK-Norm sum from the last channel", "for (int c = 0; c < D; ++c) {\n        float v = (float)oracle_half_to_double(xr[c]);",
+     "for (int c = D - 1; c >= 0; --c) {\n        float v = (float)oracle_half_to_double(xr[c]);", 1, None),
+    ("QK-Norm sum in fp64", "float sum = 0.0f;", "double sum = 0.0;", 1, None),
     ("latent V from the last channels", "o[c] += w * oracle_half_to_double(lr[c]);",
      "o[c] += w * oracle_half_to_double(lr[c + D - Dv]);", 1, None),
     ("latent scores over the V channels only", "for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(lr[c]);",
