@@ -67,9 +67,9 @@
  * rotary and before K is cached, by
  *   y[c] = fp16((x[c] * r) * w[c]),  r = 1 / sqrt(sum_j x[j]^2 / D + eps),
  * w = q_norm_weight / k_norm_weight ([D] fp16, shared by all heads); the
- * fp32 sum of squares runs in a fixed order (channel c in partial c mod 32,
- * partials combined by an xor butterfly 16, 8, 4, 2, 1), IEEE square root
- * and reciprocal, so the cached K is bit-reproducible.
+ * fp32 sum of squares is one running sum over the channels in ascending
+ * order (one rounding per square and per add), then IEEE square root and
+ * reciprocal, so the cached K is bit-reproducible.
  */
 #ifndef PA_H_
 #define PA_H_
@@ -105,7 +105,7 @@ enum {
   PA_DEVERR_KV_BOUND = 8,     /* past + q_len > kv bound or > MB*bs (sequence skipped) */
   PA_DEVERR_Q_BOUND = 16,     /* q_len > max_query_len_bound (sequence skipped) */
   PA_DEVERR_ROTARY_POS = 32,  /* position >= max_rotary_positions (row left unrotated) */
-  PA_DEVERR_TIMEOUT = 64,     /* an internal wait exceeded its limit (kernel gave up) */
+  PA_DEVERR_TIMEOUT = 64,     /* an internal wait exceeded its limit (kernel gave up; see pa_last_wait_site) */
   PA_DEVERR_SLOT = 128        /* slot_mapping entry outside [-1, NB*bs) (row not written) */
 };
 
@@ -269,8 +269,24 @@ PA_API pa_status pa_forward_ex(pa_handle h, const void* query, const void* key,
 
 /* Synchronises the stream of the handle's last call, reads and clears the
  * device error word into *code (0 = clean).  Returns PA_DEVICE_DATA_ERROR
- * when *code != 0.  Not capturable. */
+ * when *code != 0.  Not capturable.  With PA_DEVERR_TIMEOUT set, the message
+ * (pa_last_error_message) and pa_last_wait_site name the wait that gave up. */
 PA_API pa_status pa_check_device_error(pa_handle h, int* code);
+
+/* Wait sites.  Every bounded wait inside the library's kernels has an id
+ * (kernel << 8) | index; the first wait of a step that gives up records
+ * it beside the error word.  Kernel parts of the id: */
+enum {
+  PA_SITE_DECODE = 1 << 8,
+  PA_SITE_COMBINE = 2 << 8,        /* index 1: the PA_OPT_WAIT_PROBE wait */
+  PA_SITE_PREFILL = 3 << 8,        /* one-tile prefill (head_size 256) */
+  PA_SITE_PREFILL_PAIR = 4 << 8,   /* two-tile prefill (head_size 64, 128) */
+  PA_SITE_LATENT = 5 << 8,         /* latent decode, mma.sync */
+  PA_SITE_LATENT_TC = 6 << 8       /* latent decode, tcgen05 */
+};
+/* The wait-site id read (and cleared) by the last pa_check_device_error on
+ * h; 0 when no wait gave up. */
+PA_API int pa_last_wait_site(pa_handle h);
 
 /* Message of the last failure on h (or of the last pa_create / validation
  * failure on this thread when h is NULL).  Never NULL. */
@@ -296,7 +312,7 @@ PA_API pa_status pa_destroy(pa_handle h);
  * device_error: optional caller-owned device int32 that receives the
  * PA_DEVERR_* bits (OR-ed; the caller clears it).  When NULL the bits go
  * to a word inside the shared scratch, cleared at the start of each call,
- * that the caller cannot read.
+ * that the caller cannot read (so is the wait-site id of a timeout).
  *
  * It runs separate fp16 K/V caches without head_sink; an 8-bit
  * cache_dtype, packed_qkv, qk_norm or kv_cache_layout PA_LAYOUT_LATENT
@@ -327,10 +343,17 @@ enum {
   PA_OPT_DECODE_ITEMS_PER_CTA = 5, /* target decode work items per decode CTA when splits are sized automatically:
                                       1..32, or 0 (default) = per step, 1 when the step's sequences x kv heads
                                       (latent: x work units per sequence) fill the decode grid, else 2 */
-  PA_OPT_LATENT_TCGEN05 = 6   /* latent layout: 1 (the default when the query heads are a multiple of 128)
+  PA_OPT_LATENT_TCGEN05 = 6,  /* latent layout: 1 (the default when the query heads are a multiple of 128)
                                  runs the tcgen05 latent kernel (units of 128 heads x half the value
                                  channels), 0 the mma.sync kernel (items of 32 heads, any head count);
                                  1 on other handles is PA_NOT_SUPPORTED */
+  PA_OPT_PREFILL_SMS = 7,     /* steps with prompts and decode rows: the prefill kernel runs on P SMs and the
+                                 decode kernel beside it on the rest; 0 (default) = P from the step's own work
+                                 (cost model), -1 = no split (every prefill CTA works, the decode kernel
+                                 fills SMs as they free), > 0 = P fixed (at most SMs - 1) */
+  PA_OPT_WAIT_PROBE = 8       /* 1: the combine kernel also runs a bounded wait (2 ms) on a flag nothing sets,
+                                 so that the step ends with PA_DEVERR_TIMEOUT at site PA_SITE_COMBINE | 1
+                                 (a check of the timeout path; the step's outputs are unaffected) */
 };
 PA_API pa_status pa_set_option(pa_handle h, int option, int value);
 
@@ -352,6 +375,16 @@ PA_API pa_status pa_kernel_time_ms(pa_handle h, int stage, float* ms);
 
 /* Number of kernels the last pa_forward / pa_cache_write launched. */
 PA_API int pa_last_launch_count(pa_handle h);
+
+/* What the device work list of the last pa_forward on h decided (an
+ * inspection hook for tests and tuning; synchronises, not capturable):
+ * counts[PA_STEP_COUNTS] receives decode work items (sequence, split),
+ * prefill tiles, packed rows merged by the combine kernel, keys per decode
+ * split, prefill CTAs kept and decode CTAs kept (with the SM split of a
+ * mixed step their sum is at most the SM count times the decode CTAs per
+ * SM; without it they are the launched grids). */
+enum { PA_STEP_COUNTS = 6 };
+PA_API pa_status pa_last_step_counts(pa_handle h, int32_t* counts);
 
 #ifdef __cplusplus
 }

@@ -321,10 +321,11 @@ def forward(step, threads=None, rows=None):
         q = qk_norm(q, H, D, step["q_norm_weight"], eps)
         k = qk_norm(k, Hk, D, step["k_norm_weight"], eps)
     if step["do_rotary"]:
+        off = step.get("rotary_offset", 0)  # first rotated channel of a head
         q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D,
-                   step["rotary_interleaved"])
+                   step["rotary_interleaved"], off)
         k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
-                   step["rotary_interleaved"])
+                   step["rotary_interleaved"], off)
     cdt = step.get("cache_dtype", CACHE_FP16)
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)

@@ -27,6 +27,11 @@ PA_DEVERR_SLOT = 128
 PA_OPT_SPLIT_KEYS, PA_OPT_NO_WINDOW_PRUNE, PA_OPT_KERNEL_TIMING, PA_OPT_DECODE_MAX_ROWS = 1, 2, 3, 4
 PA_OPT_DECODE_ITEMS_PER_CTA = 5
 PA_OPT_LATENT_TCGEN05 = 6
+PA_OPT_PREFILL_SMS, PA_OPT_WAIT_PROBE = 7, 8
+PA_SITE_DECODE, PA_SITE_COMBINE, PA_SITE_PREFILL, PA_SITE_PREFILL_PAIR, PA_SITE_LATENT, PA_SITE_LATENT_TC = (
+    k << 8 for k in range(1, 7))
+PA_STEP_COUNTS = 6
+STEP_COUNT_NAMES = ("n_dec", "n_pre", "n_comb", "split_keys", "pre_ctas", "dec_ctas")
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 = 0, 1, 2
@@ -36,7 +41,7 @@ PA_LAYOUT_SEPARATE, PA_LAYOUT_LATENT = 0, 1
 EXPORTED = ("pa_config_init", "pa_validate_config", "pa_check_step", "pa_create", "pa_cache_write",
             "pa_forward", "pa_check_device_error", "pa_last_error_message", "pa_destroy",
             "pa_set_option", "pa_kernel_time_ms", "pa_last_launch_count", "pa_forward_no_alloc",
-            "pa_cache_write_ex", "pa_forward_ex")
+            "pa_cache_write_ex", "pa_forward_ex", "pa_last_wait_site", "pa_last_step_counts")
 
 
 class pa_config(ctypes.Structure):
@@ -95,6 +100,8 @@ def lib():
         L.pa_forward_ex.argtypes = [P, P, P, P, P, P, P, P, P, I, I, P, P, X, P, P]
         L.pa_last_launch_count.argtypes = [P]
         L.pa_last_launch_count.restype = I
+        L.pa_last_wait_site.argtypes = [P]
+        L.pa_last_step_counts.argtypes = [P, ctypes.POINTER(I)]
         for n in EXPORTED:
             if n not in ("pa_config_init", "pa_last_error_message", "pa_last_launch_count"):
                 getattr(L, n).restype = I
@@ -263,6 +270,16 @@ def pa_last_launch_count(h) -> int:
     return lib().pa_last_launch_count(h)
 
 
+def pa_last_wait_site(h) -> int:
+    return lib().pa_last_wait_site(h)
+
+
+def pa_last_step_counts(h) -> dict:
+    out = (ctypes.c_int * PA_STEP_COUNTS)()
+    _check(lib().pa_last_step_counts(h, out), h)
+    return dict(zip(STEP_COUNT_NAMES, list(out)))
+
+
 def pa_last_error_message(h=None) -> str:
     return lib().pa_last_error_message(h).decode()
 
@@ -327,6 +344,12 @@ class PagedAttention:
 
     def last_launch_count(self) -> int:
         return pa_last_launch_count(self.handle)
+
+    def last_wait_site(self) -> int:
+        return pa_last_wait_site(self.handle)
+
+    def last_step_counts(self) -> dict:
+        return pa_last_step_counts(self.handle)
 
     def close(self):
         if self.handle is not None:

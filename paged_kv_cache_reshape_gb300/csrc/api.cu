@@ -64,9 +64,31 @@ void set_msg(char* msg, size_t len, const char* fmt, ...) {
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
+// Kernel of a wait-site id (site >> 8; the PA_SITE_* values of pa.h).
+const char* wait_kernel_name(int k) {
+  switch (k) {
+    case 1: return "decode";
+    case 2: return "combine";
+    case 3: return "one-tile prefill";
+    case 4: return "two-tile prefill";
+    case 5: return "latent mma.sync";
+    case 6: return "latent tcgen05";
+    default: return "unknown";
+  }
+}
+
 int rot_dim_of(const pa_config& c) {
   if (!c.do_rotary) return 0;
   return c.rotary_dim > 0 ? c.rotary_dim : c.head_size;
+}
+
+// Whether attention reads a transformed copy of the query (rotated, QK-Norm
+// normalized, unpacked from QKV rows, or times per-channel K scales) rather
+// than the query itself.  A single per-tensor K scale multiplies the score
+// scale instead (exact, CUDA design section 8.5 phase 3).
+bool query_copied(const pa_config& c) {
+  const bool per_channel_k = c.cache_dtype != PA_CACHE_FP16 && c.k_quant_type == PA_QUANT_PER_CHANNEL;
+  return c.do_rotary || per_channel_k || c.packed_qkv || c.qk_norm;
 }
 
 }  // namespace
@@ -102,6 +124,9 @@ struct pa_handle_s {
   __half* q_rot = nullptr;
   int opt_split_keys = 0, opt_no_prune = 0, opt_timing = 0, opt_dec_rows = 0;
   int opt_items_per_cta = 0;  // 0: chosen per step (target_pairs_for)
+  int opt_prefill_sms = 0;    // SM split of mixed steps: 0 cost model, -1 none, > 0 prefill CTAs kept
+  int opt_wait_probe = 0;     // 1: the combine kernel runs its bounded wait on a flag nothing sets
+  int last_site = 0;          // wait site read by the last pa_check_device_error
   cudaEvent_t ev[PA_NUM_STAGES][2] = {};
   bool stage_ran[PA_NUM_STAGES] = {};
   cudaStream_t last_stream = nullptr;
@@ -525,7 +550,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   size_t o_po = off; off = up(off + sizeof(float) * h->cap_dec * Hk * pa::kDecodeRows * D);
   size_t o_qr = off;
   // rotated, normalized, unpacked and/or times k_scale
-  const bool q_copy = c.do_rotary || c.cache_dtype != PA_CACHE_FP16 || c.packed_qkv || c.qk_norm;
+  const bool q_copy = query_copied(c);
   if (q_copy) off = up(off + 2 * (size_t)c.max_tokens * c.num_heads * c.head_size);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws, h->ws_bytes);
@@ -592,6 +617,13 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
         return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be 0 (automatic) or in [1, 32]");
       h->opt_items_per_cta = value;
       return PA_OK;
+    case PA_OPT_PREFILL_SMS:
+      if (value < -1 || value >= h->num_sms)
+        return fail(h, PA_INVALID_ARGUMENT, "prefill SMs must be -1 (no split), 0 (cost model) or in [1, %d]",
+                    h->num_sms - 1);
+      h->opt_prefill_sms = value;
+      return PA_OK;
+    case PA_OPT_WAIT_PROBE: h->opt_wait_probe = value != 0; return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
       if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)
         return fail(h, PA_NOT_SUPPORTED, "8-bit caches route every sequence to the decode kernel");
@@ -622,13 +654,32 @@ pa_status pa_check_device_error(pa_handle h, int* code) {
   DeviceGuard g(h->device);
   cudaError_t e = cudaStreamSynchronize(h->last_stream);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
-  int v = 0;
-  e = cudaMemcpy(&v, h->err, sizeof(int), cudaMemcpyDeviceToHost);
+  int v[2] = {0, 0};  // error bits, first wait site that gave up
+  e = cudaMemcpy(v, h->err, sizeof(v), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpy(error word)");
-  e = cudaMemset(h->err, 0, sizeof(int));
+  e = cudaMemset(h->err, 0, sizeof(v));
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemset(error word)");
-  *code = v;
-  if (v) return fail(h, PA_DEVICE_DATA_ERROR, "device data error bits 0x%x", v);
+  *code = v[0];
+  h->last_site = v[1];
+  if (v[0] && v[1])
+    return fail(h, PA_DEVICE_DATA_ERROR, "device data error bits 0x%x; a wait gave up at site 0x%x (%s kernel, wait %d)",
+                v[0], v[1], wait_kernel_name(v[1] >> 8), v[1] & 0xff);
+  if (v[0]) return fail(h, PA_DEVICE_DATA_ERROR, "device data error bits 0x%x", v[0]);
+  return PA_OK;
+}
+
+int pa_last_wait_site(pa_handle h) { return h ? h->last_site : 0; }
+
+pa_status pa_last_step_counts(pa_handle h, int32_t* counts) {
+  if (!h || !counts) return fail(h, PA_INVALID_ARGUMENT, "bad arguments");
+  DeviceGuard g(h->device);
+  cudaError_t e = cudaStreamSynchronize(h->last_stream);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  pa::Counters c;
+  e = cudaMemcpy(&c, h->counters, sizeof(c), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpy(counters)");
+  const int32_t v[PA_STEP_COUNTS] = {c.n_dec, c.n_pre, c.n_comb, c.split_keys, c.pre_ctas, c.dec_ctas};
+  memcpy(counts, v, sizeof(v));
   return PA_OK;
 }
 
@@ -661,24 +712,31 @@ struct StageTimer {
   }
 };
 
-pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const void* key, const void* value,
-                                        void* key_cache, void* value_cache, const int32_t* block_table,
-                                        const int32_t* cum, const int32_t* past, int batch, int token_count,
-                                        const void* cos_cache, const void* sin_cache, const pa_extra_inputs* x) {
-  const pa_config& c = h->cfg;
+// Parameters of the prologue's rotary / cache-write warps.  Shared by the
+// handle's steps and the entry point without a handle, so the two cannot
+// drift apart: q_ws is the query-copy workspace (rotated, normalized,
+// unpacked and/or times k_scale), used whenever the query is transformed.
+pa::CacheWriteParams cache_write_params(const pa_config& c, __half* q_ws, int* err, const void* query,
+                                        const void* key, const void* value, void* key_cache, void* value_cache,
+                                        const int32_t* block_table, const int32_t* cum, const int32_t* past,
+                                        int batch, int token_count, const void* cos_cache, const void* sin_cache,
+                                        const pa_extra_inputs* x) {
   const bool quant = c.cache_dtype != PA_CACHE_FP16;
+  const bool latent = c.kv_cache_layout == PA_LAYOUT_LATENT;
+  const int R = rot_dim_of(c);
+  const bool q_scaled = quant && c.k_quant_type == PA_QUANT_PER_CHANNEL;
   pa::CacheWriteParams p{};
   p.key = static_cast<const __half*>(key);
   p.value = static_cast<const __half*>(value);
   p.query = static_cast<const __half*>(query);
-  p.q_rot = (query && (c.do_rotary || quant || c.packed_qkv || c.qk_norm)) ? h->q_rot : nullptr;
+  p.q_rot = (query && query_copied(c)) ? q_ws : nullptr;
   p.key_cache = key_cache;
   p.value_cache = value_cache;
   p.cache_type = c.cache_dtype;
   p.per_channel = c.k_quant_type == PA_QUANT_PER_CHANNEL;
   p.k_scale = quant ? x->k_scale : nullptr;
   p.v_scale = quant ? x->v_scale : nullptr;
-  p.q_scale = (query && quant) ? 1 : 0;
+  p.q_scale = (query && q_scaled) ? 1 : 0;
   p.slot_mapping = x->slot_mapping;
   p.packed = (query && c.packed_qkv) ? 1 : 0;
   p.q_stride = (p.packed ? c.num_heads + 2 * c.kv_num_heads : c.num_heads) * c.head_size;
@@ -701,22 +759,22 @@ pa::CacheWriteParams cache_write_params(pa_handle h, const void* query, const vo
   p.MB = c.max_blocks_per_seq;
   p.rotary = c.do_rotary;
   p.interleaved = c.rotary_interleaved;
-  p.rot_dim = h->R;
+  p.rot_dim = R;
   p.rot_positions = c.max_rotary_positions;
   p.rot_offset = c.rotary_offset;
   // A latent query copy keeps only the 64-channel chunks that hold rotated
   // channels; the latent kernels read the others from the query itself.
   p.q_keep_lo = 0;
   p.q_keep_hi = c.head_size;
-  if (h->latent && c.do_rotary) {
+  if (latent && c.do_rotary) {
     p.q_keep_lo = c.rotary_offset / 64 * 64;
-    p.q_keep_hi = (c.rotary_offset + h->R + 63) / 64 * 64;
+    p.q_keep_hi = (c.rotary_offset + R + 63) / 64 * 64;
   }
   // Spread a token over several warps when Q is rotated too: one for the
   // K/V rows and one per kv_num_heads query heads (same size as a K row).
   p.q_heads_per_part = c.kv_num_heads;
   p.parts = 1 + (p.q_rot ? (c.num_heads + p.q_heads_per_part - 1) / p.q_heads_per_part : 0);
-  p.err = h->err;
+  p.err = err;
   return p;
 }
 
@@ -776,8 +834,8 @@ pa_status pa_cache_write_ex(pa_handle h, const void* key, const void* value, voi
   h->last_stream = s;
   if (token_count == 0) return PA_OK;
   DeviceGuard g(h->device);
-  pa::CacheWriteParams p = cache_write_params(h, nullptr, key, value, key_cache, value_cache, block_table, cum,
-                                              past, batch, token_count, cos_cache, sin_cache, x);
+  pa::CacheWriteParams p = cache_write_params(h->cfg, h->q_rot, h->err, nullptr, key, value, key_cache, value_cache,
+                                              block_table, cum, past, batch, token_count, cos_cache, sin_cache, x);
   StageTimer t(h, PA_STAGE_CACHE_WRITE, s);
   cudaError_t e = pa::launch_cache_write(p, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cache write launch");
@@ -828,12 +886,17 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   // every sequence to the decode kernel (always so for 8-bit caches).  When
   // it does, it goes first and the decode kernel runs beside it on the SMs
   // the work list leaves it.
-  const bool pre_launch = !quant && h->prefill_ready && (long long)h->max_q * h->G > h->opt_dec_rows;
+  const bool needs_prefill = !h->latent && !quant && (long long)h->max_q * h->G > h->opt_dec_rows;
+  if (needs_prefill && !h->prefill_ready)
+    return fail(h, PA_NOT_SUPPORTED,
+                "the query-length bound routes rows to the prefill kernel, which is not available on this device");
+  const bool pre_launch = needs_prefill;
 
   // 1+2. prologue: device work list, rotary and the paged cache write
   {
     pa::WorklistParams p{};
-    p.split_sms = (pre_launch && !h->opt_timing) ? h->num_sms : 0;  // timed kernels run alone
+    p.split_sms = (pre_launch && !h->opt_timing && h->opt_prefill_sms >= 0) ? h->num_sms : 0;  // timed kernels run alone
+    p.force_pre_ctas = std::max(0, h->opt_prefill_sms);
     p.pre_grid = h->pre_grid;
     p.dec_grid = h->dec_grid;
     p.dec_ctas_per_sm = h->dec_ctas_per_sm;
@@ -869,15 +932,15 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.comb_rows = h->comb_rows;
     p.counters = h->counters;
     p.err = h->err;
-    pa::CacheWriteParams cp = cache_write_params(h, query, key, value, key_cache, value_cache, block_table, cum,
-                                                 past, batch, token_count, cos_cache, sin_cache, x);
+    pa::CacheWriteParams cp = cache_write_params(h->cfg, h->q_rot, h->err, query, key, value, key_cache,
+                                                 value_cache, block_table, cum, past, batch, token_count, cos_cache,
+                                                 sin_cache, x);
     StageTimer t(h, PA_STAGE_WORKLIST, s);
     cudaError_t e = pa::launch_prologue(p, cp, h->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "prologue launch");
     h->last_launches++;
   }
-  const __half* q_att = (c.do_rotary || quant || c.packed_qkv || c.qk_norm) ? h->q_rot
-                                                                          : static_cast<const __half*>(query);
+  const __half* q_att = query_copied(c) ? h->q_rot : static_cast<const __half*>(query);
   if (h->latent) {
     // 3'. latent decode (tensor-core units of 128 heads and half the value
     // channels, or items of 32 heads), then the log-sum-exp combine of its
@@ -904,6 +967,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.part_o = h->part_o;
     p.part_ml = h->part_ml;
     p.err = h->err;
+    p.err_site = h->err + 1;
     p.H = c.num_heads;
     p.groups = h->groups;
     p.bs = c.block_size;
@@ -936,9 +1000,9 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     mp.Hk = h->groups;
     mp.G = pa::kDecodeRows;
     mp.D = h->dv;
-    mp.pre_exit = &h->counters->pre_exit;
-    mp.pre_expected = 0;
     mp.err = h->err;
+    mp.err_site = h->err + 1;
+    mp.probe_flag = h->opt_wait_probe ? h->err + 2 : nullptr;
     StageTimer t(h, PA_STAGE_COMBINE, s);
     cudaError_t e = pa::launch_combine(mp, h->comb_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
@@ -962,6 +1026,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.pre_tiles = h->pre_tiles;
     p.counters = h->counters;
     p.err = h->err;
+    p.err_site = h->err + 1;
     p.H = c.num_heads;
     p.Hk = c.kv_num_heads;
     p.G = h->G;
@@ -993,6 +1058,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.cache_type = c.cache_dtype;
     p.per_channel = c.v_quant_type == PA_QUANT_PER_CHANNEL;
     p.v_scale = x->v_scale;
+    p.k_scale_tensor = (quant && c.k_quant_type == PA_QUANT_PER_TENSOR) ? x->k_scale : nullptr;
     p.block_table = block_table;
     p.seq = h->seq;
     p.dec_items = h->dec_items;
@@ -1000,6 +1066,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.part_o = h->part_o;
     p.part_ml = h->part_ml;
     p.err = h->err;
+    p.err_site = h->err + 1;
     p.H = c.num_heads;
     p.Hk = c.kv_num_heads;
     p.G = h->G;
@@ -1031,9 +1098,9 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.Hk = c.kv_num_heads;
     p.G = h->G;
     p.D = D;
-    p.pre_exit = &h->counters->pre_exit;
-    p.pre_expected = pre_launch ? h->pre_grid : 0;
     p.err = h->err;
+    p.err_site = h->err + 1;
+    p.probe_flag = h->opt_wait_probe ? h->err + 2 : nullptr;
     StageTimer t(h, PA_STAGE_COMBINE, s);
     cudaError_t e = pa::launch_combine(p, h->comb_grid, s);
     if (e != cudaSuccess) return cuda_fail(h, e, "combine launch");
@@ -1057,41 +1124,47 @@ __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes]
 
 constexpr int kMaxDevices = 64;
 struct NoAllocDevice {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  const char* what = "";
+  bool ready = false;                // set-up done (a failed set-up is retried on the next call)
   unsigned char* scratch = nullptr;  // device address of g_no_alloc_scratch
   int num_sms = 0;
   int dec_ctas[3] = {1, 1, 1};  // decode CTAs per SM for head_size 64, 128, 256
   bool prefill_ok = false;
 };
 NoAllocDevice g_no_alloc_dev[kMaxDevices];
+std::mutex g_no_alloc_mu;
 
 int head_index(int D) { return D == 64 ? 0 : (D == 128 ? 1 : 2); }
 
-// One-time set-up on the current device: the scratch array's device
-// address (the host-side symbol is not a device pointer), the SM count and
-// the kernels' shared-memory attributes.
-NoAllocDevice* no_alloc_setup(int dev) {
+// Set-up on the current device, once it succeeds: the scratch array's
+// device address (the host-side symbol is not a device pointer), the SM
+// count and the kernels' shared-memory attributes.  Returns cudaSuccess or
+// the failing call's error (*what names it); a failure leaves the device
+// not ready, so a later call tries again.
+cudaError_t no_alloc_setup(int dev, NoAllocDevice** out, const char** what) {
+  std::lock_guard<std::mutex> lock(g_no_alloc_mu);
   NoAllocDevice* d = &g_no_alloc_dev[dev];
-  std::call_once(d->once, [d, dev] {
-    void* ptr = nullptr;
-    d->err = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
-    if (d->err != cudaSuccess) { d->what = "cudaGetSymbolAddress(scratch)"; return; }
-    d->scratch = static_cast<unsigned char*>(ptr);
-    d->err = cudaDeviceGetAttribute(&d->num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (d->err != cudaSuccess) { d->what = "cudaDeviceGetAttribute"; return; }
-    size_t smem = 0;
-    for (int D : {64, 128, 256})
-      if (d->err == cudaSuccess) d->err = pa::decode_configure(D, PA_CACHE_FP16, &d->dec_ctas[head_index(D)], &smem);
-    if (d->err != cudaSuccess) { d->what = "decode kernel attributes"; return; }
-    d->prefill_ok = pa::prefill_configure(64, &smem) == cudaSuccess &&
-                    pa::prefill_configure(128, &smem) == cudaSuccess &&
-                    pa::prefill_configure(256, &smem) == cudaSuccess;
-    cudaGetLastError();
-    if (!encode_fn()) { d->err = cudaErrorNotSupported; d->what = "cuTensorMapEncodeTiled lookup"; }
-  });
-  return d;
+  *out = d;
+  if (d->ready) return cudaSuccess;
+  NoAllocDevice n;
+  void* ptr = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
+  if (e != cudaSuccess) { *what = "cudaGetSymbolAddress(scratch)"; return e; }
+  n.scratch = static_cast<unsigned char*>(ptr);
+  e = cudaDeviceGetAttribute(&n.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) { *what = "cudaDeviceGetAttribute"; return e; }
+  size_t smem = 0;
+  for (int D : {64, 128, 256}) {
+    e = pa::decode_configure(D, PA_CACHE_FP16, &n.dec_ctas[head_index(D)], &smem);
+    if (e != cudaSuccess) { *what = "decode kernel attributes"; return e; }
+  }
+  n.prefill_ok = pa::prefill_configure(64, &smem) == cudaSuccess &&
+                 pa::prefill_configure(128, &smem) == cudaSuccess &&
+                 pa::prefill_configure(256, &smem) == cudaSuccess;
+  cudaGetLastError();
+  if (!encode_fn()) { *what = "cuTensorMapEncodeTiled lookup"; return cudaErrorNotSupported; }
+  n.ready = true;
+  *d = n;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -1116,17 +1189,26 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(nullptr, PA_NOT_SUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
-  NoAllocDevice* nd = no_alloc_setup(dev);
-  if (nd->err != cudaSuccess) return cuda_fail(nullptr, nd->err, nd->what);
+  NoAllocDevice* nd = nullptr;
+  const char* what = "";
+  e = no_alloc_setup(dev, &nd, &what);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, what);
 
   const pa_config& c = *cfg;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = c.head_size, H = c.num_heads, Hk = c.kv_num_heads;
-  const int G = H / Hk, R = rot_dim_of(c);
+  const int G = H / Hk;
   const float scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)D);
   const int kv_cap = c.max_blocks_per_seq * c.block_size;
   const int max_q = c.max_query_len_bound > 0 ? std::min(c.max_query_len_bound, c.max_tokens) : c.max_tokens;
   const int max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
+  // Rows go to the decode kernel iff q_len * G <= 16; the prefill kernel
+  // runs only when the query-length bound lets some sequence have more.
+  const int dec_max_rows = G <= pa::kDecodeRows ? pa::kDecodeRows : 0;
+  const bool pre_launch = (long long)max_q * G > dec_max_rows;
+  if (pre_launch && !nd->prefill_ok)
+    return fail(nullptr, PA_NOT_SUPPORTED,
+                "the query-length bound routes rows to the prefill kernel, which is not available on this device");
   const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
   const int target_pairs = std::max(1, (pa::kDecodeItemsPerCta * dec_grid + Hk - 1) / Hk);
   const int cap_dec = target_pairs + c.max_batch;
@@ -1138,7 +1220,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   // Scratch layout (256-byte aligned pieces), checked against the maximum.
   auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
-  const size_t o_err = off; off = up(off + 64);
+  const size_t o_err = off; off = up(off + 64);  // error bits, wait site
   const size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
   const size_t o_seq = off; off = up(off + sizeof(pa::SeqInfo) * c.max_batch);
   const size_t o_dec = off; off = up(off + sizeof(int2) * cap_dec);
@@ -1154,7 +1236,9 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
                 "(lower max_batch / max_tokens or use pa_create)",
                 off, kNoAllocScratchBytes);
   unsigned char* w = nd->scratch;
-  int* err = device_error ? device_error : reinterpret_cast<int*>(w + o_err);
+  int* err_words = reinterpret_cast<int*>(w + o_err);
+  int* err = device_error ? device_error : err_words;
+  int* err_site = err_words + 1;
   pa::Counters* counters = reinterpret_cast<pa::Counters*>(w + o_cnt);
   pa::SeqInfo* seq = reinterpret_cast<pa::SeqInfo*>(w + o_seq);
   int2* dec_items = reinterpret_cast<int2*>(w + o_dec);
@@ -1162,11 +1246,11 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   int2* comb_rows = reinterpret_cast<int2*>(w + o_cmb);
   float2* part_ml = reinterpret_cast<float2*>(w + o_pml);
   float* part_o = reinterpret_cast<float*>(w + o_po);
-  __half* q_rot = c.do_rotary ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
-  if (!device_error) {
-    e = cudaMemsetAsync(err, 0, sizeof(int), s);  // the shared error word starts clean
-    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemsetAsync(error word)");
-  }
+  __half* q_ws = c.do_rotary ? reinterpret_cast<__half*>(w + o_qr) : nullptr;
+  // the shared error bits (when the caller gives no word of its own) and the
+  // wait-site word start clean
+  e = cudaMemsetAsync(err_words, 0, 2 * sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMemsetAsync(error words)");
 
   const int pool_rows = c.num_blocks * c.block_size;
   const int box_rows = std::min(c.block_size, pa::kStageKeys);
@@ -1185,7 +1269,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.max_kv = max_kv;
   wp.window = c.local_window_size;
   wp.prune = 1;
-  wp.dec_max_rows = G <= pa::kDecodeRows ? pa::kDecodeRows : 0;
+  wp.dec_max_rows = dec_max_rows;
   wp.prefill_tile_tokens = tile_tokens;
   wp.split_keys_fixed = 0;
   wp.target_pairs = target_pairs;
@@ -1206,38 +1290,13 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.dec_ctas_per_sm = std::max(1, dec_grid / nd->num_sms);
   wp.counters = counters;
   wp.err = err;
-  pa::CacheWriteParams cp{};
-  cp.key = static_cast<const __half*>(key);
-  cp.value = static_cast<const __half*>(value);
-  cp.query = static_cast<const __half*>(query);
-  cp.q_stride = H * D;
-  cp.q_rot = q_rot;
-  cp.key_cache = key_cache;
-  cp.value_cache = value_cache;
-  cp.block_table = block_table;
-  cp.cum = cum;
-  cp.past = past;
-  cp.cos_cache = static_cast<const __half*>(cos_cache);
-  cp.sin_cache = static_cast<const __half*>(sin_cache);
-  cp.batch = batch;
-  cp.token_count = token_count;
-  cp.H = H;
-  cp.Hk = Hk;
-  cp.D = D;
-  cp.bs = c.block_size;
-  cp.NB = c.num_blocks;
-  cp.MB = c.max_blocks_per_seq;
-  cp.rotary = c.do_rotary;
-  cp.interleaved = c.rotary_interleaved;
-  cp.rot_dim = R;
-  cp.rot_positions = c.max_rotary_positions;
-  cp.q_heads_per_part = Hk;
-  cp.parts = 1 + (q_rot ? (H + Hk - 1) / Hk : 0);
-  cp.err = err;
+  const pa::CacheWriteParams cp =
+      cache_write_params(c, q_ws, err, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
+                         token_count, cos_cache, sin_cache, &kNoExtra);
   e = pa::launch_prologue(wp, cp, nd->num_sms, s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "prologue launch");
 
-  const __half* q_att = c.do_rotary ? q_rot : static_cast<const __half*>(query);
+  const __half* q_att = c.do_rotary ? q_ws : static_cast<const __half*>(query);
   const int qt = G <= pa::kDecodeRows ? pa::kDecodeRows / G : 1;
   CUtensorMap tq;
   if (!encode_map(&tq, q_att, D, H, token_count, G, qt))
@@ -1253,6 +1312,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   dp.part_o = part_o;
   dp.part_ml = part_ml;
   dp.err = err;
+  dp.err_site = err_site;
   dp.H = H;
   dp.Hk = Hk;
   dp.G = G;
@@ -1267,7 +1327,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   e = pa::launch_decode(D, tk, tv, tq, dp, dec_grid, s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "decode launch");
 
-  if (nd->prefill_ok) {
+  if (pre_launch) {
     CUtensorMap tqp, tkp, tvp;
     const int prow = std::min(c.block_size, pa::prefill_keys_per_tile(D));
     if (!encode_map(&tqp, q_att, D, H, token_count, G, q_tokens) ||
@@ -1281,6 +1341,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
     pp.pre_tiles = pre_tiles;
     pp.counters = counters;
     pp.err = err;
+    pp.err_site = err_site;
     pp.H = H;
     pp.Hk = Hk;
     pp.G = G;
@@ -1297,6 +1358,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
     if (e != cudaSuccess) return cuda_fail(nullptr, e, "prefill launch");
   }
 
+  // The combine kernel waits for its predecessor (the prefill kernel, which
+  // waited for the decode kernel, or the decode kernel itself).
   pa::CombineParams mp{};
   mp.part_o = part_o;
   mp.part_ml = part_ml;
@@ -1308,9 +1371,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   mp.Hk = Hk;
   mp.G = G;
   mp.D = D;
-  mp.pre_exit = &counters->pre_exit;
-  mp.pre_expected = 0;  // the prefill kernel is this kernel's predecessor
   mp.err = err;
+  mp.err_site = err_site;
   e = pa::launch_combine(mp, std::max(1, std::min(nd->num_sms * 4, (cap_comb * H + 7) / 8)), s);
   if (e != cudaSuccess) return cuda_fail(nullptr, e, "combine launch");
   return PA_OK;

@@ -27,10 +27,11 @@
 // dequantization into Q (section 8.5 phase 3).
 //
 // QK-Norm (section 7, before rotary; the normalized K is what is cached):
-// each head's factor r = 1 / sqrt(sum x^2 / D + eps) is reduced by the warp
-// in a fixed order (channel c accumulates in lane c mod 32, k ascending,
-// then an xor butterfly 16, 8, 4, 2, 1; no fused multiply-add; IEEE square
-// root and reciprocal), and every loaded channel becomes fp16((x * r) * w).
+// each head's factor r = 1 / sqrt(sum x^2 / D + eps) takes its fp32 sum of
+// squares as one running sum over the channels in ascending order (one
+// lane per head, one rounding per square and per add, no fused
+// multiply-add; IEEE square root and reciprocal), and every loaded channel
+// becomes fp16((x * r) * w).
 // Packed QKV rows (section 4) are read in place: Q, K and V heads of token
 // t start at t*(H+2Hk)*D, + H*D and + (H+Hk)*D.
 #include <algorithm>
@@ -107,19 +108,24 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
   }
 };
 
-// QK-Norm factors of the nheads heads of one row (all lanes return, lane 0
-// stores rn[h]); the fixed reduction order stated at the top of the file.
+// QK-Norm factors of the nheads (<= 32) heads of one row: lane h sums the
+// squares of head h as one running fp32 sum in channel order (the order
+// stated at the top of the file), then stores rn[h].
 __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, float eps, float* rn, int lane) {
-  for (int h = 0; h < nheads; ++h) {
+  if (lane < nheads) {
+    const __half* x = src + (size_t)lane * D;
     float acc = 0.f;
-    for (int c = lane; c < D; c += 32) {
-      const float x = __half2float(__ldg(src + (size_t)h * D + c));
-      acc = __fadd_rn(acc, __fmul_rn(x, x));
-    }
+    for (int c = 0; c < D; c += 8) {
+      Vec8 v;
+      v.u = __ldg(reinterpret_cast<const uint4*>(x + c));
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
-    const float v = __fadd_rn(__fmul_rn(acc, 1.f / (float)D), eps);
-    if (lane == 0) rn[h] = __frcp_rn(__fsqrt_rn(v));
+      for (int e = 0; e < 8; ++e) {
+        const float f = __half2float(v.h[e]);
+        acc = __fadd_rn(acc, __fmul_rn(f, f));
+      }
+    }
+    const float mean = __fmul_rn(acc, 1.f / (float)D);
+    rn[lane] = __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
   }
   __syncwarp();
 }
@@ -310,7 +316,8 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     row_transform(ksrc,
                   EmitCode{static_cast<uint8_t*>(p.key_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
                            p.k_scale},
-                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w);
+                  p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
+                  p.rot_offset);
     row_transform(vsrc,
                   EmitCode{static_cast<uint8_t*>(p.value_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
                            p.v_scale},

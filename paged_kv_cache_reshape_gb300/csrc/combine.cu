@@ -55,15 +55,18 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     tb0 = p.comb_rows[first / p.H];
     si0 = p.seq[tb0.y];
   }
-  griddep_wait();  // the partials come from the decode kernel
-  // The prefill kernel may still run beside the decode kernel: the step
-  // ends only after every prefill CTA has (CTA 0 waits, bounded).
-  if (p.pre_expected > 0 && blockIdx.x == 0 && threadIdx.x == 0) {
-    const volatile int* done = p.pre_exit;
-    uint32_t i = 0;
-    for (; i < kWaitLimit && *done < p.pre_expected; ++i) __nanosleep(64);
-    if (i == kWaitLimit) atomicOr(p.err, PA_DEVERR_TIMEOUT);
-    __threadfence();
+  // The partials come from the decode kernel.  In a step with prompts the
+  // decode kernel's grid completes only after the prefill grid beside it
+  // (its CTA 0 waits for it before exiting), so once this returns every
+  // kernel of the step before this one has completed.
+  griddep_wait();
+  if (p.probe_flag && blockIdx.x == 0 && threadIdx.x == 0) {
+    // A bounded wait for a flag nothing sets: it runs out after 2 ms and
+    // records the timeout and this site in the error words.
+    const volatile int* f = p.probe_flag;
+    const uint64_t t0 = global_ns();
+    while (*f == 0 && global_ns() - t0 < 2000000ull) __nanosleep(1000);
+    if (*f == 0) note_timeout(p.err, p.err_site, kSiteCombine | 1);
   }
   for (int idx = first; idx < n; idx += gridDim.x * kWarps) {
     const int ci = idx / p.H, h = idx - ci * p.H;

@@ -37,8 +37,9 @@
 //    K fragments come from ldmatrix on the code bytes (each lane gets four
 //    consecutive channels of one key), which fixes the order in which the
 //    16 channels of an m16n8k16 step are contracted, and the Q fragments
-//    (already times k_scale, written by the prologue) are loaded in that
-//    same order; V fragments come from a transposed ldmatrix (two keys x two
+//    (with per-channel scales already times k_scale, written by the
+//    prologue; one per-tensor K scale multiplies the score scale instead)
+//    are loaded in that same order; V fragments come from a transposed ldmatrix (two keys x two
 //    channels per lane), split into an even-channel and an odd-channel MMA;
 //    codes become fp16 pairs with one byte permute and one conversion; the
 //    V scale multiplies the merged output;
@@ -146,9 +147,8 @@ __device__ __forceinline__ void q_frag_perm(const uint8_t* q, int ks, int lane, 
 }
 
 template <int D, int CT>
-__global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
+                                            const DecodeParams& p) {
   using C = DecodeCfg<D, CT>;
   constexpr bool kQ8 = CT != kCacheF16;
   extern __shared__ uint8_t smem_raw[];
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
             tags[stage].u = -1;
             mbar_arrive(&full[stage]);
           } else {
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            note_timeout(p.err, p.err_site, kSiteDecode | 1);
           }
         }
         break;
@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
       // Query rows of the item: box {64, G, qt} at (chunk, k*G, t0).
       if (lane == 0) {
         if (!mbar_wait(&q_empty[qi], (quse[qi] & 1) ^ 1)) {
-          atomicOr(p.err, PA_DEVERR_TIMEOUT);
+          note_timeout(p.err, p.err_site, kSiteDecode | 2);
           ok = false;
         } else {
           mbar_arrive_expect_tx(&q_full[qi], q_bytes);
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
         for (int bx = 0; bx < boxes; ++bx) mask |= ((zb >> (2 * bx)) & 1) << bx;
         if (lane == 0) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            note_timeout(p.err, p.err_site, kSiteDecode | 3);
             ok = false;
           } else {
             StageTag& t = tags[stage];
@@ -327,7 +327,9 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
   int stage = 0;
   uint32_t phase = 0;
   int quse[2] = {0, 0};
-  const float scale = p.scale;
+  // one K scale for the whole cache: exact to fold into the score scale
+  // (section 8.5 phase 3); per-channel K scales are in the query copy
+  const float scale = p.k_scale_tensor ? p.scale * __ldg(p.k_scale_tensor) : p.scale;
   const bool capped = p.softcap > 0.f;
   const float inv_cap = capped ? 1.f / p.softcap : 0.f;
   const int log_r = p.log_box_rows;
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
 
   while (true) {
     if (!mbar_wait(&full[stage], phase)) {
-      if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+      if (lane == 0) note_timeout(p.err, p.err_site, kSiteDecode | 4);
       return;
     }
     const StageTag tg = tags[stage];
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
     if (tg.flags & kFirst) {
       // New item: its query tile, row bounds and a fresh softmax state.
       if (!mbar_wait(&q_full[tg.qi], quse[tg.qi] & 1)) {
-        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        if (lane == 0) note_timeout(p.err, p.err_site, kSiteDecode | 5);
         return;
       }
       quse[tg.qi]++;
@@ -621,6 +623,17 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
       phase ^= 1;
     }
   }
+}
+
+template <int D, int CT>
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
+  decode_body<D, CT>(tm_k, tm_v, tm_q, p);
+  // Beside the prefill kernel (launched after it): this grid may complete
+  // only once the prefill grid has, so the combine kernel, which waits for
+  // this grid, ends the step after both.  One thread of CTA 0 suffices.
+  if (!p.wait_prologue && blockIdx.x == 0 && threadIdx.x == 0) griddep_wait();
 }
 
 template <int D, int CT>

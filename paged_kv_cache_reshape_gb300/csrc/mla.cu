@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tags[stage].u = -1;
             mbar_arrive(&full[stage]);
           } else {
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            note_timeout(p.err, p.err_site, kSiteMla | 1);
           }
         }
         break;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo_min = p.window >= 1 ? max(0, past + 1 - p.window) : 0;
       if (lane == 0) {
         if (!mbar_wait(&q_empty[qi], (quse[qi] & 1) ^ 1)) {
-          atomicOr(p.err, PA_DEVERR_TIMEOUT);
+          note_timeout(p.err, p.err_site, kSiteMla | 2);
           ok = false;
         } else {
           mbar_arrive_expect_tx(&q_full[qi], kQBytes);
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned mask = __ballot_sync(0xffffffffu, lane < boxes && rc == p.oob_row);
         if (lane == 0) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
-            atomicOr(p.err, PA_DEVERR_TIMEOUT);
+            note_timeout(p.err, p.err_site, kSiteMla | 3);
             ok = false;
           } else {
             Tag& t = tags[stage];
@@ -247,14 +247,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint8_t* qcur = qbuf;
   while (true) {
     if (!mbar_wait(&full[stage], phase)) {
-      if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+      if (lane == 0) note_timeout(p.err, p.err_site, kSiteMla | 4);
       return;
     }
     const Tag tg = tags[stage];
     if (tg.u < 0) break;
     if (tg.flags & kFirst) {
       if (!mbar_wait(&q_full[tg.qi], quse[tg.qi] & 1)) {
-        if (lane == 0) atomicOr(p.err, PA_DEVERR_TIMEOUT);
+        if (lane == 0) note_timeout(p.err, p.err_site, kSiteMla | 5);
         return;
       }
       quse[tg.qi]++;

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = tt & 1;
       int u = 0;
       if (lane == 0) {
-        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err, p.err_site, kSiteMlaTc | 13)) u = -2;
         else u = tt == 0 ? (int)blockIdx.x : active + atomicAdd(&p.counters->dec_next, 1);
       }
       u = __shfl_sync(0xffffffffu, u, 0);
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // are free) and its last S has completed (Q's shared-memory part is
         // free); one box {64, 128, 1} per chunk.
         for (int st = 0; st < kStages && ok; ++st)
-          ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err);
-        if (ok) ok = wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err);
+          ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err, p.err_site, kSiteMlaTc | 14);
+        if (ok) ok = wait_or_abort(&ctl->q_empty, (tt & 1) ^ 1, abort, p.err, p.err_site, kSiteMlaTc | 1);
         if (ok) {
           mbar_arrive_expect_tx(&ctl->q_full, kChunks * kQChunkBytes);
           ++q_loads;
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
         if (lane == 0) {
           // the slots that staged Q are reused once its copy into TMEM is done
-          if (i == 1) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err);
-          if (ok) ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err);
+          if (i == 1) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err, p.err_site, kSiteMlaTc | 2);
+          if (ok) ok = wait_or_abort(&ctl->kv_empty[st], ((sp >> st) & 1) ^ 1, abort, p.err, p.err_site, kSiteMlaTc | 15);
           if (ok) {
             ctl->kv_mask[st] = mask;
             mbar_arrive_expect_tx(&ctl->kv_full[st], kTileBytes);
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next unit's Q overwrites the staging slots: a one-tile unit has
       // not waited for its copy into TMEM yet.
       if (ok && n_kv < 2) {
-        if (lane == 0) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err);
+        if (lane == 0) ok = wait_or_abort(&ctl->q_staged, tt & 1, abort, p.err, p.err_site, kSiteMlaTc | 3);
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
@@ -294,10 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (uint32_t tt = 0; ok; ++tt) {
         const int slot = tt & 1;
-        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err, p.err_site, kSiteMlaTc | 4)) break;
         const UnitInfo ti = ctl->info[slot];
         if (ti.u < 0) break;
-        if (!wait_or_abort(&ctl->q_full, tt & 1, abort, p.err)) break;
+        if (!wait_or_abort(&ctl->q_full, tt & 1, abort, p.err, p.err_site, kSiteMlaTc | 5)) break;
         tc_fence_after();
         // Q channels 0..383 into TMEM (after the previous unit's last S in
         // issue order); the staging slots are free once the copies complete.
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whose PV was issued before this.
         auto issue_s = [&](uint32_t gi, int i, bool last) -> bool {
           const int st = slot_of(i);
-          if (!wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err)) return false;
+          if (!wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err, p.err_site, kSiteMlaTc | 6)) return false;
           sp ^= 1u << st;
           tc_fence_after();
           const uint32_t kb = kv_addr + st * kTileBytes;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!wait_or_abort(&ctl->p_full, v & 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->p_full, v & 1, abort, p.err, p.err_site, kSiteMlaTc | 7)) {
             ok = false;
             break;
           }
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[kKeys];
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt & 1;
-      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err, p.err_site, kSiteMlaTc | 8)) break;
       const UnitInfo ti = ctl->info[slot];
       if (ti.u < 0) break;
       const int hi = ti.past;                                // last admitted position
@@ -390,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sb = gi & 1;        // S buffer
         const int st = slot_of(i);    // ring slot of the tile
         const int key0 = ti.key0 + i * kKeys;
-        if (!wait_or_abort(&ctl->s_full[sb], (gi >> 1) & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->s_full[sb], (gi >> 1) & 1, abort, p.err, p.err_site, kSiteMlaTc | 9) ||
+            !wait_or_abort(&ctl->kv_full[st], (sp >> st) & 1, abort, p.err, p.err_site, kSiteMlaTc | 10)) {
           ok = false;
           break;
         }
@@ -434,17 +434,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk[c / 2] = pack_half2(e0, e1);
         }
         l = l * alpha + rs;
-        // PV(gi - 1) must be done before O is rescaled; P(gi) goes to the
-        // other S buffer, so without a rescale the warp does not wait.  (A
-        // skipped wait is safe: o_done cannot run a phase ahead of the one
-        // waited for next, since PV(gi) needs this warp's P(gi).)
-        if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err)) {
+        // Before P(gi) is published, PV(gi - 1) has completed (needed anyway
+        // before O is rescaled).  Waiting on every tile, not only on a
+        // rescale, keeps the barrier phases sound: S(gi + 1) is issued ahead
+        // of PV(gi), so without this wait a warp could finish tile gi + 1
+        // before a slower warp finished tile gi and arrive twice in one phase
+        // of the four-warp p_full barrier (PV(gi) would read a partial P, and
+        // the phases seen by the slower warp would then run two ahead, so its
+        // parity waits stall until they time out); and the epilogue's parity
+        // wait on o_done could see that barrier two phases behind and pass
+        // before the unit's last PVs.  PV(gi - 1) needs P(gi - 1), published a
+        // tile ago, so this wait rarely waits.
+        if (i > 0) {
+          if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err, p.err_site, kSiteMlaTc | 11)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          {
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
             float o[32];
 #pragma unroll 1
             for (int c = 0; c < kHalf / 32; ++c) {
@@ -481,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: O / l -> fp16 output rows, or fp32 partials of a split
-      if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err, p.err_site, kSiteMlaTc | 12)) break;
       tc_fence_after();
       const int h = ti.ht * kRows + r;
       const int c0 = ti.half * kHalf;

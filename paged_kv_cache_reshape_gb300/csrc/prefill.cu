@@ -101,13 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();
   griddep_launch_dependents();  // the decode kernel may start on the SMs this grid leaves free
   const int n_work = p.counters->n_pre * p.Hk;
-  // CTAs beyond the work or beyond the work list's SM split leave at once
-  // (counted, so the step's last kernel can wait for every prefill CTA).
+  // CTAs beyond the work or beyond the work list's SM split leave at once.
   const int active = min(n_work, p.counters->pre_ctas);
-  if ((int)blockIdx.x >= active) {
-    if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
-    return;
-  }
+  if ((int)blockIdx.x >= active) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -154,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u = 0;
       if (lane == 0) {
         // First tile: this CTA's own index; then the shared queue.
-        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err)) u = -2;
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt >> 1) & 1) ^ 1, abort, p.err, p.err_site, kSitePrefill | 11)) u = -2;
         else u = tt == 0 ? (int)blockIdx.x : active + atomicAdd(&p.counters->pre_next, 1);
       }
       u = __shfl_sync(0xffffffffu, u, 0);
@@ -191,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->info_full[slot]);
         // Q tile: box {64, G, tile_tokens} per channel chunk.
         const int qb = tt % C::kQBufs;
-        if (!wait_or_abort(&ctl->q_empty[qb], ((tt / C::kQBufs) & 1) ^ 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->q_empty[qb], ((tt / C::kQBufs) & 1) ^ 1, abort, p.err, p.err_site, kSitePrefill | 13)) {
           ok = false;
         } else {
           mbar_arrive_expect_tx(&ctl->q_full[qb], q_bytes);
@@ -229,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t mask = __ballot_sync(0xffffffffu, lane < pages && rc == p.oob_row);
         if (lane == 0) {
-          if (!wait_or_abort(&ctl->kv_empty[st], ((g >> 1) & 1) ^ 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->kv_empty[st], ((g >> 1) & 1) ^ 1, abort, p.err, p.err_site, kSitePrefill | 12)) {
             ok = false;
           } else {
             ctl->kv_mask[st] = mask;
@@ -272,18 +268,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (uint32_t tt = 0; ok; ++tt) {
         const int slot = tt & 1;
-        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+        if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err, p.err_site, kSitePrefill | 1)) break;
         const TileInfo ti = ctl->info[slot];
         if (ti.u < 0) break;
         const int qb = tt % C::kQBufs;
-        if (!wait_or_abort(&ctl->q_full[qb], (tt / C::kQBufs) & 1, abort, p.err)) break;
+        if (!wait_or_abort(&ctl->q_full[qb], (tt / C::kQBufs) & 1, abort, p.err, p.err_site, kSitePrefill | 2)) break;
         tc_fence_after();
         const uint32_t q_addr = smem_u32(q_s + qb * C::kQBytes);
         // S(i) = Q K_i^T into TMEM columns [kSCol, kSCol + KEYS)
         auto issue_s = [&](uint32_t gi, bool last) -> bool {
           const int st = gi & 1;
-          if (!wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) return false;
-          if (s_issued > 0 && !wait_or_abort(&ctl->s_free, (s_issued - 1) & 1, abort, p.err)) return false;
+          if (!wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err, p.err_site, kSitePrefill | 3)) return false;
+          if (s_issued > 0 && !wait_or_abort(&ctl->s_free, (s_issued - 1) & 1, abort, p.err, p.err_site, kSitePrefill | 4)) return false;
           tc_fence_after();
           const uint32_t kb = kv_addr + st * 2 * C::kTileBytes;
 #pragma unroll
@@ -304,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (!wait_or_abort(&ctl->p_full, v & 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->p_full, v & 1, abort, p.err, p.err_site, kSitePrefill | 5)) {
             ok = false;
             break;
           }
@@ -342,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[KEYS];
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt & 1;
-      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt >> 1) & 1, abort, p.err, p.err_site, kSitePrefill | 6)) break;
       const TileInfo ti = ctl->info[slot];
       if (ti.u < 0) break;
       const int j = r / p.G;
@@ -356,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t gi = g + i;
         const int st = gi & 1;
         const int key0 = ti.key_lo + i * KEYS;
-        if (!wait_or_abort(&ctl->s_full, s_cnt & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->s_full, s_cnt & 1, abort, p.err, p.err_site, kSitePrefill | 7) ||
+            !wait_or_abort(&ctl->kv_full[st], (gi >> 1) & 1, abort, p.err, p.err_site, kSitePrefill | 8)) {
           ok = false;
           break;
         }
@@ -407,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + rs;
         // PV(i-1) must be done before O is rescaled and P is overwritten.
         if (i > 0) {
-          if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->o_done, (v + i - 1) & 1, abort, p.err, p.err_site, kSitePrefill | 9)) {
             ok = false;
             break;
           }
@@ -457,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: O / l -> fp16 output rows
-      if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->o_done, (v + ti.n_kv - 1) & 1, abort, p.err, p.err_site, kSitePrefill | 10)) break;
       tc_fence_after();
       const int t = ti.t0 + j, h = ti.k * p.G + (r - j * p.G);
       // head_sink (section 6.1): exp(s_h - m) joins the denominator
@@ -489,14 +485,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  __threadfence();  // this CTA's output rows are visible before it is counted done
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
 }
 
 template <int D, bool CAP>

@@ -20,9 +20,7 @@
 //     reuse the columns once PV(i) is issued, and a wait on S(i+1) also
 //     covers PV(i);
 //   * the softmax does two fp32 lanes per instruction (f32x2 FMA/ADD) and a
-//     three-input max; part of its exponentials can go to a polynomial on
-//     the FMA pipe instead of the MUFU unit (PA_PREFILL_POLY_OF_4; off by
-//     default, as every fraction measured slower);
+//     three-input max;
 //   * TMEM: S_A, S_B (128 columns each), O_A, O_B (head_size each);
 //   * shared memory: one Q buffer per tile, a ring of K and V tile slots
 //     loaded in the order they are used: K0 V0 K1 V1 ...
@@ -49,10 +47,6 @@ static_assert(2 * kRegSoftmax + kRegEpilogue + kRegControl == 4 * 128, "register
 constexpr int kKeys = 128;  // keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
-#ifndef PA_PREFILL_POLY_OF_4
-#define PA_PREFILL_POLY_OF_4 0  // exponential pairs out of every 4 evaluated by the polynomial
-#endif
-constexpr int kPolyOf4 = PA_PREFILL_POLY_OF_4;
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kCtrlBytes = 2048;
 
@@ -152,36 +146,6 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-
-// 2^x for a pair, on the FMA pipe: x = j + f with j = round(x) and
-// f in [-1/2, 1/2]; 2^f from the degree-3 polynomial that minimises the
-// largest relative error on that interval (Remez exchange: 7.5e-5, under
-// half an fp16 ulp), and j added to its exponent bits.  Arguments are
-// clamped at -120, so a masked -inf gives 2^-120, which rounds to fp16 0.
-__device__ __forceinline__ void exp2_poly(uint64_t x, float& e0, float& e1) {
-  float a, b;
-  unf2(x, a, b);
-  const uint64_t v = f2(fmaxf(a, -120.f), fmaxf(b, -120.f));
-  const uint64_t round_c = f2(12582912.f, 12582912.f);  // 1.5 * 2^23: adding it rounds to an integer
-  const uint64_t t = add2(v, round_c);
-  const uint64_t f = sub2(v, sub2(t, round_c));
-  uint64_t q = fma2(f, f2(0.0551716685f, 0.0551716685f), f2(0.242611125f, 0.242611125f));
-  q = fma2(q, f, f2(0.693260968f, 0.693260968f));
-  q = fma2(q, f, f2(0.999928057f, 0.999928057f));
-  float q0, q1, t0, t1;
-  unf2(q, q0, q1);
-  unf2(t, t0, t1);
-  // the low mantissa bits of t hold j (two's complement); shifted into the
-  // exponent field they scale 2^f by 2^j
-  e0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-  e1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
-}
-
 template <int D, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -199,13 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   griddep_wait();  // the work list and the pool come from the prologue
   griddep_launch_dependents();  // the decode kernel may start on the SMs this grid leaves free
   const int n_work = p.counters->n_pre * p.Hk;
-  // CTAs beyond the work or beyond the work list's SM split leave at once
-  // (counted, so the step's last kernel can wait for every prefill CTA).
+  // CTAs beyond the work or beyond the work list's SM split leave at once.
   const int active = min(n_work, p.counters->pre_ctas);
-  if ((int)blockIdx.x >= active) {
-    if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
-    return;
-  }
+  if ((int)blockIdx.x >= active) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -290,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int slot = tt % kInfoRing;
       if (lane == 0) {
-        if (!wait_or_abort(&ctl->info_empty[slot], ((tt / kInfoRing) & 1) ^ 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->info_empty[slot], ((tt / kInfoRing) & 1) ^ 1, abort, p.err, p.err_site, kSitePrefillPair | 12)) {
           ok = false;
         } else {
           ctl->info[slot] = f;
@@ -298,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Q tile X of unit tt into its buffer once unit tt-1's S_X MMAs are done
         for (int X = 0; X < 2 && ok && f.u >= 0; ++X) {
-          if (!wait_or_abort(&ctl->q_empty[X], (tt & 1) ^ 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->q_empty[X], (tt & 1) ^ 1, abort, p.err, p.err_site, kSitePrefillPair | 1)) {
             ok = false;
           } else {
             mbar_arrive_expect_tx(&ctl->q_full[X], q_bytes);
@@ -334,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_tile = [&](const CUtensorMap* tm, int k, int rc, bool is_v, uint32_t mask) -> bool {
       const int slot = n_loads % S;
       if (lane == 0) {
-        if (!wait_or_abort(&ctl->empty[slot], ((n_loads / S) & 1) ^ 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->empty[slot], ((n_loads / S) & 1) ^ 1, abort, p.err, p.err_site, kSitePrefillPair | 13)) {
           ok = false;
         } else {
           if (!is_v) {
@@ -358,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t tt = 0; ok; ++tt) {
       const int slot = tt % kInfoRing;
       int got = 1;
-      if (lane == 0) got = wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err) ? 1 : 0;
+      if (lane == 0) got = wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err, p.err_site, kSitePrefillPair | 2) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, got, 0)) break;
       const UnitInfo cur = ctl->info[slot];
       if (cur.u < 0) break;
@@ -409,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t kv_addr = smem_u32(kv_s);
     const bool leader = elect_one();
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {
-      return wait_or_abort(bar, parity, abort, p.err);
+      return wait_or_abort(bar, parity, abort, p.err, p.err_site, kSitePrefillPair | 3);
     };
     uint32_t g = 0, pcnt[2] = {0, 0};
     bool ok = leader;
@@ -503,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[kKeys];
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt % kInfoRing;
-      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err, p.err_site, kSitePrefillPair | 4)) break;
       const UnitInfo& ui = ctl->info[slot];
       if (ui.u < 0) break;
       // The unit's fields, read once (shared-memory loads are slow while
@@ -526,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int key0 = key_lo + i * kKeys;
         // s_full(i) also covers PV(i-1): MMAs complete in issue order.  The
         // page mask was published before the tile's K load.
-        if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->mask_full[tile % kMaskRing], (tile / kMaskRing) & 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err, p.err_site, kSitePrefillPair | 5) ||
+            !wait_or_abort(&ctl->mask_full[tile % kMaskRing], (tile / kMaskRing) & 1, abort, p.err, p.err_site, kSitePrefillPair | 6)) {
           ok = false;
           break;
         }
@@ -566,15 +526,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 16; ++q) {
             const uint64_t arg = fma2(f2(x[h + 2 * q], x[h + 2 * q + 1]), mul2, neg_m2);
-            float e0, e1;
-            if ((q & 3) < kPolyOf4) {
-              exp2_poly(arg, e0, e1);
-            } else {
-              float a0, a1;
-              unf2(arg, a0, a1);
-              e0 = ex2(a0);
-              e1 = ex2(a1);
-            }
+            float a0, a1;
+            unf2(arg, a0, a1);
+            const float e0 = ex2(a0), e1 = ex2(a1);
             sum2[q & 3] = add2(sum2[q & 3], f2(e0, e1));
             pk[q] = pack_half2(e0, e1);
           }
@@ -594,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i >= vz_from && (key0 + kKeys > vz_kv_len || key0 < vz_lo_min)) {
           uint8_t* vs = kv_s + sv * C::kSlotBytes;
-          if (!wait_or_abort(&ctl->full[sv], (nv / S) & 1, abort, p.err)) {
+          if (!wait_or_abort(&ctl->full[sv], (nv / S) & 1, abort, p.err, p.err_site, kSitePrefillPair | 7)) {
             ok = false;
             break;
           }
@@ -626,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l += ex2(__half2float(p.head_sink[ui.k * p.G + (r - j * p.G)]) * kLog2e - m_ref);
       // The row sum goes to the epilogue warpgroup (its previous value has
       // been read once l_empty completes).
-      if (!wait_or_abort(&ctl->l_empty[X], (tt & 1) ^ 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->l_empty[X], (tt & 1) ^ 1, abort, p.err, p.err_site, kSitePrefillPair | 8)) break;
       ctl->l_row[X][r] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->l_full[X]);
@@ -644,14 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ocnt[2] = {0, 0};
     for (uint32_t tt = 0;; ++tt) {
       const int slot = tt % kInfoRing;
-      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err)) break;
+      if (!wait_or_abort(&ctl->info_full[slot], (tt / kInfoRing) & 1, abort, p.err, p.err_site, kSitePrefillPair | 9)) break;
       const UnitInfo& ui = ctl->info[slot];
       if (ui.u < 0) break;
       const int j = r / p.G;
       bool ok = true;
       for (int X = 0; X < 2 && ok; ++X) {
-        if (!wait_or_abort(&ctl->o_done[X], ocnt[X] & 1, abort, p.err) ||
-            !wait_or_abort(&ctl->l_full[X], tt & 1, abort, p.err)) {
+        if (!wait_or_abort(&ctl->o_done[X], ocnt[X] & 1, abort, p.err, p.err_site, kSitePrefillPair | 10) ||
+            !wait_or_abort(&ctl->l_full[X], tt & 1, abort, p.err, p.err_site, kSitePrefillPair | 11)) {
           ok = false;
           break;
         }
@@ -694,14 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  __threadfence();  // this CTA's output rows are visible before it is counted done
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (threadIdx.x == 0) atomicAdd(&p.counters->pre_exit, 1);
 }
 
 template <int D, bool CAP>

@@ -123,17 +123,45 @@ __device__ __forceinline__ bool elect_one() {
   return pred != 0;
 }
 
+// Wait sites.  Every bounded wait of every kernel has an id (kernel << 8 |
+// index, the kernel ids below); the first wait of a step that gives up
+// records its id in the site word beside the error word, so a
+// PA_DEVERR_TIMEOUT names the wait that ran out.
+enum WaitKernel {
+  kSiteDecode = 1 << 8,
+  kSiteCombine = 2 << 8,
+  kSitePrefill = 3 << 8,
+  kSitePrefillPair = 4 << 8,
+  kSiteMla = 5 << 8,
+  kSiteMlaTc = 6 << 8
+};
+
+// Records a wait that gave up: the error bit, and the site id if it is the
+// step's first (site_word may be NULL).
+__device__ __forceinline__ void note_timeout(int* err, int* site_word, int site) {
+  atomicOr(err, PA_DEVERR_TIMEOUT);
+  if (site_word) atomicCAS(site_word, 0, site);
+}
+
 // Bounded mbarrier wait of the tcgen05 kernels: gives up (returns false)
 // when another role of the CTA has set *abort, or after kWaitLimit polls,
-// setting *abort and PA_DEVERR_TIMEOUT itself.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
+// setting *abort and recording the timeout (note_timeout) itself.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, int* err,
+                                              int* site_word, int site) {
   for (uint32_t i = 0; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 1023) == 1023 && *abort) return false;
   }
   *abort = 1;
-  atomicOr(err, PA_DEVERR_TIMEOUT);
+  note_timeout(err, site_word, site);
   return false;
+}
+
+// The global nanosecond timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
 }
 
 __device__ __forceinline__ float ex2(float x) {

@@ -55,8 +55,7 @@ struct Counters {
   int pre_next;    // prefill work queue head (reset to 0 by the work-list kernel)
   int pre_ctas;    // prefill CTAs that take work this step; the others exit at once
   int dec_ctas;    // decode CTAs that take work this step
-  int pre_exit;    // prefill CTAs finished this step (the combine kernel waits for all)
-  int pad[3];
+  int pad[4];
 };
 
 struct WorklistParams {
@@ -78,6 +77,7 @@ struct WorklistParams {
   // decides how many of its CTAs keep working; the others exit, and the
   // decode kernel, launched next, runs on the SMs they free, concurrently.
   int split_sms;             // SMs to share (0: no split, every CTA works)
+  int force_pre_ctas;        // > 0: the prefill CTAs kept, instead of the cost model's choice
   int pre_grid, dec_grid;    // launched CTAs of the two kernels
   int dec_ctas_per_sm;
   float dec_bytes_per_key;   // Hk * D * 4 (K and V, once per kv head)
@@ -136,6 +136,8 @@ struct DecodeParams {
   __half* out;      // [T, H*D]
   const __half* head_sink;  // [H] or null
   const float* v_scale;     // 8-bit caches: [1] or [Hk*D]
+  const float* k_scale_tensor;  // 8-bit caches with one K scale: [1], folded into the score scale
+                                // (per-channel K scales are folded into the query copy instead)
   int per_channel;
   int cache_type;
   const int* block_table;
@@ -145,6 +147,7 @@ struct DecodeParams {
   float* part_o;    // [items*Hk*16*D]
   float2* part_ml;  // [items*Hk*16] (max in log2 units, sum)
   int* err;
+  int* err_site;    // first wait that gave up (wait site id), or null
   int H, Hk, G, bs, MB, NB;
   float scale;       // softmax scale
   float softcap;     // 0 = off
@@ -155,8 +158,11 @@ struct DecodeParams {
   int bt_lines;      // 128-byte lines of the block table (batch rows) to pull into L2 first; 0 = none
   int wait_prologue; // 1: the launch before is the prologue (griddepcontrol.wait
                      // on it); 0: it is the prefill kernel, which has waited for
-                     // the prologue before letting this kernel start, and this
-                     // kernel must not wait for it to finish
+                     // the prologue before letting this kernel start: this
+                     // kernel runs beside it and waits for it (griddepcontrol.wait,
+                     // CTA 0) only before exiting, so that this grid completes
+                     // after the prefill grid and the combine kernel, which
+                     // waits for this grid, ends the step after both
 };
 
 struct CombineParams {
@@ -168,9 +174,10 @@ struct CombineParams {
   const Counters* counters;
   __half* out;
   int H, Hk, G, D;
-  int* pre_exit;     // counter of finished prefill CTAs
-  int pre_expected;  // prefill CTAs launched this step (0: none)
   int* err;
+  int* err_site;
+  const int* probe_flag;  // non-null: CTA 0 waits (2 ms at most) for *probe_flag != 0, which
+                          // nothing sets, and records the timeout (exercises the error path)
 };
 
 struct PrefillParams {
@@ -181,6 +188,7 @@ struct PrefillParams {
   const int2* pre_tiles;
   Counters* counters;  // n_pre and the tile queue head
   int* err;
+  int* err_site;
   int H, Hk, G, bs, MB, NB;
   int tile_tokens;  // tokens per 128-row query tile (rows = tile_tokens * G <= 128)
   int log_page_rows;  // log2(min(block_size, keys per KV tile)): pool rows per TMA box
@@ -203,6 +211,7 @@ struct MlaParams {
   float* part_o;         // [items * groups * 16 * 512]
   float2* part_ml;       // [items * groups * 16]
   int* err;
+  int* err_site;
   int H, groups;         // query heads, groups of 16 heads (32 heads per work item)
   int bs, MB, NB;
   float scale, softcap;

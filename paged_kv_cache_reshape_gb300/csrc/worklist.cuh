@@ -142,8 +142,12 @@ __device__ int split_keys_for(const WorklistParams& p, long long total) {
 __device__ void choose_split(const WorklistParams& p, long long dec_keys, long long pre_pairs, Counters* c) {
   c->pre_ctas = p.pre_grid;
   c->dec_ctas = p.dec_grid;
-  c->pre_exit = 0;
   if (p.split_sms < 2 || dec_keys <= 0 || pre_pairs <= 0) return;
+  if (p.force_pre_ctas > 0) {  // a fixed share (a tuning and test option)
+    c->pre_ctas = min(min(p.force_pre_ctas, p.split_sms - 1), p.pre_grid);
+    c->dec_ctas = max(1, min(p.dec_grid, (p.split_sms - c->pre_ctas) * p.dec_ctas_per_sm));
+    return;
+  }
   const float F = (float)pre_pairs * p.pre_flops_per_pair;
   const float B = (float)dec_keys * p.dec_bytes_per_key;
   int best = 1;
@@ -172,7 +176,7 @@ __device__ void write_counters(const WorklistParams& p, bool overflow, Int3 tot,
   c.dec_next = 0;
   c.pre_next = 0;
   choose_split(p, dec_keys, pre_pairs, &c);
-  c.pad[0] = c.pad[1] = c.pad[2] = 0;
+  c.pad[0] = c.pad[1] = c.pad[2] = c.pad[3] = 0;
   *p.counters = c;
 }
 

@@ -78,12 +78,19 @@ def check_full(step_host, step_dev, out, threads=8):
 
 def check_sampled(step_host, step_dev, out, n_rows=192, seed=0, threads=16):
     """Large-step parity: pools bit-exact, a seeded sample of (t, h) rows."""
+    T, H = step_host["token_count"], step_host["num_heads"]
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([rng.integers(0, T * H, n_rows), [0, T * H - 1]]))
+    return check_rows(step_host, step_dev, out, rows, threads=threads)
+
+
+def check_rows(step_host, step_dev, out, rows, threads=16):
+    """Large-step parity: pools bit-exact, the given (t, h) rows (t * H + h)."""
     ref = oracle.forward(step_host, threads=threads, rows=np.zeros(0, dtype=np.int64))
     assert np.array_equal(raw(step_dev["key_cache"]), raw(ref["key_cache"])), "key_cache pool differs"
     assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
     T, H, D = step_host["token_count"], step_host["num_heads"], step_host["head_size"]
-    rng = np.random.default_rng(seed)
-    rows = np.unique(np.concatenate([rng.integers(0, T * H, n_rows), [0, T * H - 1]]))
+    rows = np.asarray(rows, dtype=np.int64)
     o = oracle.attention(ref["query_rot"], ref["key_cache"], ref["value_cache"],
                          step_host["block_table"], step_host["cumulative_sequence_lengths"],
                          step_host["past_sequence_lengths"], H, step_host["kv_num_heads"], D,

@@ -10,7 +10,7 @@ import torch
 
 import paged_kv_cache_reshape_gb300 as pa
 import workloads
-from gpu_util import assert_close, bits, check_full, check_sampled, host_copy, make, run
+from gpu_util import assert_close, bits, check_full, check_rows, check_sampled, host_copy, make, run
 
 pytestmark = pytest.mark.gpu
 
@@ -164,12 +164,58 @@ def test_mixed_routing_in_one_step():
 
 
 def test_full_size_mixed_step():
+    """The 16 x 1024-token prompts beside 240 decodes, as the benchmark runs
+    it (prefill and decode kernels side by side on an SM split): both pools
+    in full, every decode row, every row of two prompts and a seeded sample
+    of the rest."""
     shape = workloads.config_shape(2)
     step = make(shape, device="cuda", gen_device="cuda")
     host = host_copy(step)
     op, out, err = run(step)
     assert err == 0, f"device error {err:#x}"
-    check_sampled(host, step, out, n_rows=160)
+    counts = op.last_step_counts()
+    assert counts["n_pre"] > 0 and counts["n_dec"] > 0
+    assert counts["pre_ctas"] + counts["dec_ctas"] // 2 <= torch.cuda.get_device_properties(0).multi_processor_count
+    H = shape.num_heads
+    cum = host["cumulative_sequence_lengths"].tolist()
+    dec = [b for b in range(shape.batch) if shape.new_lens[b] == 1]
+    prompts = [b for b in range(shape.batch) if shape.new_lens[b] > 1][:2]
+    rows = [np.arange(cum[b] * H, cum[b + 1] * H) for b in dec + prompts]
+    rng = np.random.default_rng(0)
+    rows.append(rng.integers(0, shape.token_count * H, 512))
+    rows = np.unique(np.concatenate(rows))
+    assert len(dec) == 240 and np.isin(np.arange(cum[dec[0]] * H, cum[dec[0]] * H + H), rows).all()
+    check_rows(host, step, out, rows)
+
+
+def _mid_mixed():
+    rng = np.random.default_rng(71)
+    past = [0] * 4 + rng.integers(300, 3000, 60).tolist()
+    new = [300] * 4 + [1] * 60
+    order = rng.permutation(64)
+    return cs("mid_mixed_4x300_60dec", 32, 8, 128, 16, [past[i] for i in order], [new[i] for i in order], seed=72)
+
+
+@pytest.mark.parametrize("prefill_sms", [40, -1])
+def test_mid_mixed_step_with_and_without_sm_split(prefill_sms):
+    """4 prompts of 300 tokens beside 60 decodes, every row against the
+    oracle: once with the prefill kernel held to 40 SMs and the decode
+    kernel beside it on the rest (the split shown active in the work list's
+    counts), once with no split."""
+    shape = _mid_mixed()
+    step = make(shape, device="cuda", gen_device="cpu")
+    host = host_copy(step)
+    op, out, err = run(step, options=[(pa.PA_OPT_PREFILL_SMS, prefill_sms)])
+    assert err == 0, f"device error {err:#x}"
+    counts = op.last_step_counts()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert counts["n_pre"] > 0 and counts["n_dec"] > 0
+    if prefill_sms > 0:
+        assert counts["pre_ctas"] == prefill_sms
+        assert counts["dec_ctas"] <= 2 * (sms - prefill_sms)
+    else:
+        assert counts["pre_ctas"] == sms
+    check_full(host, step, out)
 
 
 @pytest.mark.parametrize("items", [0, 1, 2, 7, 32])
@@ -187,3 +233,20 @@ def test_items_per_cta_option_range():
         with pytest.raises(pa.PAError) as e:
             op.set_option(pa.PA_OPT_DECODE_ITEMS_PER_CTA, bad)
         assert e.value.status == pa.PA_INVALID_ARGUMENT
+
+
+@pytest.mark.parametrize("shape", [
+    cs("rot_off_decode", 8, 2, 128, 16, [5, 260, 31], [1, 2, 1], do_rotary=1, rotary_dim=64, seed=81),
+    cs("rot_off_prefill", 8, 2, 128, 32, [0, 40], [150, 70], do_rotary=1, rotary_dim=64, seed=82),
+    cs("rot_off_interleaved_d256", 4, 2, 256, 64, [0, 300], [90, 1], do_rotary=1, rotary_interleaved=1,
+       rotary_dim=128, seed=83),
+], ids=lambda s: s.name)
+def test_rotary_at_an_offset(shape):
+    """rotary_offset on separate K/V caches: channels [off, off + R) of every
+    Q and K head are rotated, the others copied; pools bit-exact."""
+    step = make(shape, device="cuda", gen_device="cpu")
+    step["rotary_offset"] = 32 if shape.head_size == 128 else 64
+    host = host_copy(step)
+    op, out, err = run(step)
+    assert err == 0, f"device error {err:#x}"
+    check_full(host, step, out)

@@ -137,3 +137,18 @@ def test_scales_required_and_routing_locked():
     with pytest.raises(pa.PAError) as e:
         op.set_option(pa.PA_OPT_DECODE_MAX_ROWS, 4)
     assert e.value.status == pa.PA_NOT_SUPPORTED
+
+
+@pytest.mark.parametrize("cache_dtype", [I8, F8], ids=["int8", "e4m3"])
+@pytest.mark.parametrize("quant_type", [PT, PC], ids=["per_tensor", "per_channel"])
+def test_quantized_rotary_at_an_offset(cache_dtype, quant_type):
+    """Rotary over channels [32, 96) of head_size 128 (rotary_offset 32,
+    rotary_dim 64): the quantized K rows and the scaled query copy rotate
+    the same channels the oracle does."""
+    shape = cs("q_rotary_offset", 8, 2, 128, 16, [3, 90, 400], [1, 2, 1], do_rotary=1, rotary_dim=64, seed=29)
+    step = make(shape, device="cuda", gen_device="cpu", cache_dtype=cache_dtype, quant_type=quant_type)
+    step["rotary_offset"] = 32
+    host = host_copy(step)
+    op, out, err = run(step, max_tokens=step["token_count"], max_query_len_bound=2)
+    assert err == 0, f"device error {err:#x}"
+    check_full(host, step, out)

@@ -92,3 +92,31 @@ def test_offset_rotary_matches_complex_rotation():
                           sin.numpy(), R // 2, 0)
     got = y.view(np.float16).astype(np.float64).reshape(T, nh, D)[:, :, off:off + R]
     assert np.all(np.abs(got - ref) <= _ulp16(ref) + 1e-12)
+
+
+def test_separate_layout_step_rotates_at_its_offset():
+    # a step with separate K/V caches and rotary_offset 32, rotary_dim 64 on
+    # head_size 128: Q and K rows are rotated over channels [32, 96) exactly
+    # as the pinned offset rotation does, every other channel is copied, and
+    # the cached K rows are those rotated rows
+    shape = workloads.custom_shape("sep_offset", 8, 2, 128, 16, [5, 40], [1, 3], do_rotary=1, rotary_dim=64,
+                                   seed=63)
+    step = workloads.make_step(shape)
+    step["rotary_offset"] = 32
+    res = oracle.forward(step)
+    cum, past = step["cumulative_sequence_lengths"], step["past_sequence_lengths"]
+    for name, nh, got in (("query", 8, res["query_rot"]), ("key", 2, res["key_rot"])):
+        x = _bits(step[name])
+        ref = oracle.rotary(x, cum, past, _bits(step["cos_cache"]), _bits(step["sin_cache"]), nh, 128, 0, offset=32)
+        assert np.array_equal(got, ref)
+        xb, gb = x.reshape(-1, nh, 128), got.reshape(-1, nh, 128)
+        assert np.array_equal(gb[:, :, :32], xb[:, :, :32]) and np.array_equal(gb[:, :, 96:], xb[:, :, 96:])
+        assert not np.array_equal(gb[:, :, 32:96], xb[:, :, 32:96])
+    kc = res["key_cache"].reshape(-1, 2 * 128)
+    bt = step["block_table"].numpy()
+    for b, (p0, q) in enumerate(((5, 1), (40, 3))):
+        for j in range(q):
+            pos = p0 + j
+            slot = bt[b, pos // 16] * 16 + pos % 16
+            t = int(cum[b]) + j
+            assert np.array_equal(kc[slot], res["key_rot"].reshape(-1, 256)[t])
