@@ -119,8 +119,10 @@ enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2 };
  * head attends with its D channels and the output is the weighted sum of
  * the first v_head_size channels of the same rows (absorbed multi-head
  * latent attention); an explicit scale is required.  Built: D = 576,
- * v_head_size = 512, num_heads <= 16 or a multiple of 16, one query token
- * per sequence (max_query_len_bound = 1), fp16 cache; output [T, H*512]. */
+ * v_head_size = 512, num_heads <= 16 or a multiple of 16, fp16 cache;
+ * output [T, H*512].  A sequence with several new tokens (chunked prefill,
+ * prefix caching) runs in the same absorbed form, each token attending
+ * causally like a one-token decode row (section 12.8). */
 enum { PA_LAYOUT_SEPARATE = 0, PA_LAYOUT_LATENT = 1 };
 /* Scale granularity (section 8.2, k_quant_type / v_quant_type). */
 enum { PA_QUANT_NONE = 0, PA_QUANT_PER_TENSOR = 1, PA_QUANT_PER_CHANNEL = 2 };
@@ -167,10 +169,11 @@ PA_API void pa_config_init(pa_config* cfg);
  * capacities, quantization NONE exactly for fp16 caches.  Writes a message
  * naming the field into msg (may be NULL).  Returns PA_INVALID_ARGUMENT or
  * PA_NOT_SUPPORTED on failure.  Not built (PA_NOT_SUPPORTED): 8-bit caches
- * with head_size 64, with k_quant_type != v_quant_type, or with a
- * query-length bound (max_query_len_bound, else max_tokens) times
- * num_heads / kv_num_heads above 16 (8-bit caches run the decode kernel
- * only).  Touches no GPU. */
+ * with head_size 64, with k_quant_type != v_quant_type, or with
+ * num_heads / kv_num_heads above 16 (8-bit caches run every query row
+ * through the decode kernel: a sequence whose q_len * num_heads /
+ * kv_num_heads rows exceed one 16-row item runs in chunks of
+ * 16 * kv_num_heads / num_heads tokens, section 8.5).  Touches no GPU. */
 PA_API pa_status pa_validate_config(const pa_config* cfg, char* msg, size_t msg_len);
 
 /* Host-only check of one step's arguments (token_count <= max_tokens,
@@ -253,8 +256,9 @@ PA_API pa_status pa_cache_write_ex(pa_handle h, const void* key, const void* val
                                    void* stream);
 
 /* pa_forward with the optional inputs (extra may be NULL).  8-bit caches
- * are read at their stored width: the K scale is folded into the query
- * (q * k_scale[c], rounded to fp16) and the V scale into the output
+ * are read at their stored width: a per-tensor K scale multiplies the
+ * softmax scale, per-channel K scales are folded into the query
+ * (q * k_scale[c], rounded to fp16), and the V scale multiplies the output
  * (section 8.5 phase 3).  head_sink s_h adds exp(s_h - m) to the softmax
  * denominator of every row of head h, m = max(s_h, max logit) (section
  * 6.1); a row with no admitted key still outputs 0. */

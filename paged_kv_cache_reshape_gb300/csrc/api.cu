@@ -29,6 +29,10 @@ constexpr float kPrefillFlopsPerSmUs = 5.0e6f;
 constexpr float kDecodeBytesPerSmUs = 55.0e3f;
 constexpr float kHbmBytesPerUs = 6.7e6f;
 
+// Largest decode items-per-CTA target (PA_OPT_DECODE_ITEMS_PER_CTA); the
+// split-partial workspace is sized for it.
+constexpr int kMaxItemsPerCta = 8;
+
 thread_local std::string g_last_msg = "no error";
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -107,13 +111,15 @@ struct pa_handle_s {
   bool mla_tc_ready = false;  // the tcgen05 latent kernel can serve this handle (query heads a multiple of 128)
   bool mla_tc = false;        // ... and runs (the default; PA_OPT_LATENT_TCGEN05 = 0 selects the mma.sync kernel)
   size_t dec_smem = 0;
-  int cap_dec = 1, cap_pre = 1, cap_comb = 1;
+  int cap_dec = 1, cap_pre = 1, cap_comb = 1, cap_dseq = 1, cap_part = 1;
+  int chunk_tokens = 0;  // > 0: query rows beyond one decode item run as decode entries of this many tokens
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
   size_t pre_smem = 0;
   bool prefill_ready = false;
   void* ws = nullptr;
   size_t ws_bytes = 0;
-  pa::SeqInfo* seq = nullptr;
+  pa::SeqInfo* seq = nullptr;   // sequence table
+  pa::SeqInfo* dseq = nullptr;  // decode table
   int2* dec_items = nullptr;
   int2* pre_tiles = nullptr;
   int2* comb_rows = nullptr;
@@ -360,10 +366,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
       set_msg(msg, len, "the latent layout is built for num_heads <= 16 or a multiple of 16 (got %d)", c->num_heads);
       return PA_NOT_SUPPORTED;
     }
-    if (qb != 1) {
-      set_msg(msg, len, "the latent layout runs decode steps only: max_query_len_bound (else max_tokens) must be 1");
-      return PA_NOT_SUPPORTED;
-    }
+    (void)qb;  // longer query rows run as one-token decode entries
     set_msg(msg, len, "ok");
     return PA_OK;
   }
@@ -392,11 +395,11 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
       set_msg(msg, len, "8-bit caches are built for head_size 128 and 256 (got 64)");
       return PA_NOT_SUPPORTED;
     }
-    const long long qb = c->max_query_len_bound > 0 ? std::min(c->max_query_len_bound, c->max_tokens) : c->max_tokens;
-    if (qb * (c->num_heads / c->kv_num_heads) > pa::kDecodeRows) {
-      set_msg(msg, len,
-              "8-bit caches run the decode kernel only: max_query_len_bound (else max_tokens) * num_heads / "
-              "kv_num_heads must be <= %d (got %lld)", pa::kDecodeRows, qb * (c->num_heads / c->kv_num_heads));
+    // 8-bit caches run the decode kernel only (longer query rows in chunks of
+    // 16 / G tokens), whose items hold one kv head's group of up to 16 rows
+    if (c->num_heads / c->kv_num_heads > pa::kDecodeRows) {
+      set_msg(msg, len, "8-bit caches are built for num_heads / kv_num_heads <= %d (got %d)", pa::kDecodeRows,
+              c->num_heads / c->kv_num_heads);
       return PA_NOT_SUPPORTED;
     }
   }
@@ -523,10 +526,22 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : 1;
   h->mla_tc = h->mla_tc_ready;
   h->unit_groups = h->mla_tc ? tc_units : h->latent ? pa::mla_item_groups(h->groups) : h->groups;
-  // Room for up to 32 items per CTA (the tuning option's maximum).
-  // (sized for whichever latent kernel makes the most items)
+  // Query rows beyond one decode item: the prefill kernel for fp16 caches
+  // with separate K and V, decode entries of kDecodeRows / G tokens for
+  // 8-bit caches and the latent layout (one token: G is 16 there).
+  const bool quant = c.cache_dtype != PA_CACHE_FP16;
+  h->chunk_tokens = (h->latent || quant) ? std::max(1, pa::kDecodeRows / h->G) : 0;
+  // Decode entries: one per sequence, or one per chunk.
+  h->cap_dseq = c.max_batch + (h->chunk_tokens ? (c.max_tokens + h->chunk_tokens - 1) / h->chunk_tokens : 0);
+  // Decode items: the split targets (room for the items-per-CTA option's
+  // maximum, sized for whichever latent kernel makes the most items) plus
+  // one last split per entry.  Split partials: with automatic split sizes
+  // a step has at most as many full splits as split targets, and at most as
+  // many split entries as full splits.
   const int ug_min = h->mla_tc_ready ? std::min(tc_units, pa::mla_item_groups(h->groups)) : h->unit_groups;
-  h->cap_dec = std::max(1, (32 * h->dec_grid + ug_min - 1) / ug_min) + c.max_batch;
+  const int target_max = std::max(1, (kMaxItemsPerCta * h->dec_grid + ug_min - 1) / ug_min);
+  h->cap_dec = target_max + h->cap_dseq;
+  h->cap_part = 2 * target_max;
   // Prefill work units: unit tokens (the work list's tiles) and the tokens
   // of one 128-row query tile (the Q TMA box).
   h->prefill_tile_tokens = pa::prefill_unit_tokens(c.head_size, h->G);
@@ -543,11 +558,12 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   size_t o_err = off; off = up(off + 64);
   size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
   size_t o_seq = off; off = up(off + sizeof(pa::SeqInfo) * c.max_batch);
+  size_t o_dsq = off; off = up(off + sizeof(pa::SeqInfo) * h->cap_dseq);
   size_t o_dec = off; off = up(off + sizeof(int2) * h->cap_dec);
   size_t o_pre = off; off = up(off + sizeof(int2) * h->cap_pre);
   size_t o_cmb = off; off = up(off + sizeof(int2) * h->cap_comb);
-  size_t o_pml = off; off = up(off + sizeof(float2) * h->cap_dec * Hk * pa::kDecodeRows);
-  size_t o_po = off; off = up(off + sizeof(float) * h->cap_dec * Hk * pa::kDecodeRows * D);
+  size_t o_pml = off; off = up(off + sizeof(float2) * h->cap_part * Hk * pa::kDecodeRows);
+  size_t o_po = off; off = up(off + sizeof(float) * h->cap_part * Hk * pa::kDecodeRows * D);
   size_t o_qr = off;
   // rotated, normalized, unpacked and/or times k_scale
   const bool q_copy = query_copied(c);
@@ -561,6 +577,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->err = reinterpret_cast<int*>(w + o_err);
   h->counters = reinterpret_cast<pa::Counters*>(w + o_cnt);
   h->seq = reinterpret_cast<pa::SeqInfo*>(w + o_seq);
+  h->dseq = reinterpret_cast<pa::SeqInfo*>(w + o_dsq);
   h->dec_items = reinterpret_cast<int2*>(w + o_dec);
   h->pre_tiles = reinterpret_cast<int2*>(w + o_pre);
   h->comb_rows = reinterpret_cast<int2*>(w + o_cmb);
@@ -595,10 +612,12 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
       if (value < 0 || value % pa::kStageKeys != 0)
         return fail(h, PA_INVALID_ARGUMENT, "split keys must be 0 or a positive multiple of %d", pa::kStageKeys);
       if (value > 0) {
-        long long need = (long long)h->cfg.max_batch * ((h->max_kv + value - 1) / value + 1);
-        if (need > h->cap_dec)
+        // every decode entry split at most max_kv / value + 1 ways
+        long long need = (long long)h->cap_dseq * ((h->max_kv + value - 1) / value + 1);
+        if (need > h->cap_dec || need > h->cap_part)
           return fail(h, PA_INVALID_ARGUMENT,
-                      "split keys %d could need %lld decode items; the workspace holds %d", value, need, h->cap_dec);
+                      "split keys %d could need %lld decode items; the workspace holds %d items and %d split "
+                      "partials", value, need, h->cap_dec, h->cap_part);
       }
       h->opt_split_keys = value;
       return PA_OK;
@@ -613,8 +632,9 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
       h->unit_groups = h->mla_tc ? 2 * (h->cfg.num_heads / 128) : pa::mla_item_groups(h->groups);
       return PA_OK;
     case PA_OPT_DECODE_ITEMS_PER_CTA:
-      if (value < 0 || value > 32)
-        return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be 0 (automatic) or in [1, 32]");
+      if (value < 0 || value > kMaxItemsPerCta)
+        return fail(h, PA_INVALID_ARGUMENT, "decode items per CTA must be 0 (automatic) or in [1, %d]",
+                    kMaxItemsPerCta);
       h->opt_items_per_cta = value;
       return PA_OK;
     case PA_OPT_PREFILL_SMS:
@@ -923,10 +943,14 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     // balance gains (measured on the DeepSeek-V3-shaped step: automatic
     // ~1984 keys 109 us, 2048 97 us, no split 136 us).
     p.min_split_keys = h->mla_tc ? 2048 : pa::kStageKeys;
+    p.chunk_tokens = h->chunk_tokens;
     p.cap_dec = h->cap_dec;
     p.cap_pre = h->cap_pre;
     p.cap_comb = h->cap_comb;
+    p.cap_dseq = h->cap_dseq;
+    p.cap_part = h->cap_part;
     p.seq = h->seq;
+    p.dseq = h->dseq;
     p.dec_items = h->dec_items;
     p.pre_tiles = h->pre_tiles;
     p.comb_rows = h->comb_rows;
@@ -961,7 +985,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     pa::MlaParams p{};
     p.out = static_cast<__half*>(output);
     p.block_table = block_table;
-    p.seq = h->seq;
+    p.seq = h->dseq;  // the decode table
     p.dec_items = h->dec_items;
     p.counters = h->counters;
     p.part_o = h->part_o;
@@ -992,7 +1016,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     pa::CombineParams mp{};
     mp.part_o = h->part_o;
     mp.part_ml = h->part_ml;
-    mp.seq = h->seq;
+    mp.seq = h->dseq;  // the decode table
     mp.comb_rows = h->comb_rows;
     mp.counters = h->counters;
     mp.out = static_cast<__half*>(output);
@@ -1060,7 +1084,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.v_scale = x->v_scale;
     p.k_scale_tensor = (quant && c.k_quant_type == PA_QUANT_PER_TENSOR) ? x->k_scale : nullptr;
     p.block_table = block_table;
-    p.seq = h->seq;
+    p.seq = h->dseq;  // the decode table
     p.dec_items = h->dec_items;
     p.counters = h->counters;
     p.part_o = h->part_o;
@@ -1090,7 +1114,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.head_sink = sink;
     p.part_o = h->part_o;
     p.part_ml = h->part_ml;
-    p.seq = h->seq;
+    p.seq = h->dseq;  // the decode table
     p.comb_rows = h->comb_rows;
     p.counters = h->counters;
     p.out = static_cast<__half*>(output);
@@ -1211,7 +1235,9 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
                 "the query-length bound routes rows to the prefill kernel, which is not available on this device");
   const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
   const int target_pairs = std::max(1, (pa::kDecodeItemsPerCta * dec_grid + Hk - 1) / Hk);
-  const int cap_dec = target_pairs + c.max_batch;
+  const int cap_dseq = c.max_batch;  // one decode entry per sequence (no chunks: fp16 caches have the prefill kernel)
+  const int cap_dec = target_pairs + cap_dseq;
+  const int cap_part = 2 * target_pairs;
   const int tile_tokens = pa::prefill_unit_tokens(D, G);
   const int q_tokens = std::max(1, pa::kPrefillRows / G);
   const int cap_pre = (c.max_tokens + tile_tokens - 1) / tile_tokens + c.max_batch;
@@ -1223,11 +1249,12 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   const size_t o_err = off; off = up(off + 64);  // error bits, wait site
   const size_t o_cnt = off; off = up(off + sizeof(pa::Counters));
   const size_t o_seq = off; off = up(off + sizeof(pa::SeqInfo) * c.max_batch);
+  const size_t o_dsq = off; off = up(off + sizeof(pa::SeqInfo) * cap_dseq);
   const size_t o_dec = off; off = up(off + sizeof(int2) * cap_dec);
   const size_t o_pre = off; off = up(off + sizeof(int2) * cap_pre);
   const size_t o_cmb = off; off = up(off + sizeof(int2) * cap_comb);
-  const size_t o_pml = off; off = up(off + sizeof(float2) * (size_t)cap_dec * Hk * pa::kDecodeRows);
-  const size_t o_po = off; off = up(off + sizeof(float) * (size_t)cap_dec * Hk * pa::kDecodeRows * D);
+  const size_t o_pml = off; off = up(off + sizeof(float2) * (size_t)cap_part * Hk * pa::kDecodeRows);
+  const size_t o_po = off; off = up(off + sizeof(float) * (size_t)cap_part * Hk * pa::kDecodeRows * D);
   const size_t o_qr = off;
   if (c.do_rotary) off = up(off + 2 * (size_t)c.max_tokens * H * D);
   if (off > kNoAllocScratchBytes)
@@ -1241,6 +1268,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   int* err_site = err_words + 1;
   pa::Counters* counters = reinterpret_cast<pa::Counters*>(w + o_cnt);
   pa::SeqInfo* seq = reinterpret_cast<pa::SeqInfo*>(w + o_seq);
+  pa::SeqInfo* dseq = reinterpret_cast<pa::SeqInfo*>(w + o_dsq);
   int2* dec_items = reinterpret_cast<int2*>(w + o_dec);
   int2* pre_tiles = reinterpret_cast<int2*>(w + o_pre);
   int2* comb_rows = reinterpret_cast<int2*>(w + o_cmb);
@@ -1274,10 +1302,14 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.split_keys_fixed = 0;
   wp.target_pairs = target_pairs;
   wp.min_split_keys = pa::kStageKeys;
+  wp.chunk_tokens = 0;
   wp.cap_dec = cap_dec;
   wp.cap_pre = cap_pre;
   wp.cap_comb = cap_comb;
+  wp.cap_dseq = cap_dseq;
+  wp.cap_part = cap_part;
   wp.seq = seq;
+  wp.dseq = dseq;
   wp.dec_items = dec_items;
   wp.pre_tiles = pre_tiles;
   wp.comb_rows = comb_rows;
@@ -1306,7 +1338,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   dp.log_box_rows = 31 - __builtin_clz((unsigned)box_rows);
   dp.out = static_cast<__half*>(output);
   dp.block_table = block_table;
-  dp.seq = seq;
+  dp.seq = dseq;
   dp.dec_items = dec_items;
   dp.counters = counters;
   dp.part_o = part_o;
@@ -1363,7 +1395,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   pa::CombineParams mp{};
   mp.part_o = part_o;
   mp.part_ml = part_ml;
-  mp.seq = seq;
+  mp.seq = dseq;
   mp.comb_rows = comb_rows;
   mp.counters = counters;
   mp.out = static_cast<__half*>(output);

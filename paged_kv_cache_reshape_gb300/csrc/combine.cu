@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
     const int k = h / p.G, g = h - k * p.G;
     const int r = j * p.G + g;
     const int ns = si.dec_count;
-    auto row_of = [&](int s) -> size_t { return ((size_t)dec_item_of_split(si, s) * p.Hk + k) * kDecodeRows + r; };
+    auto row_of = [&](int s) -> size_t { return ((size_t)(si.part_first + s) * p.Hk + k) * kDecodeRows + r; };
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.f;

@@ -88,7 +88,8 @@ struct StageTag {
   int nsplit;  // splits of the sequence
   int qi;      // Q buffer
   int lo_min;  // smallest admitted position of any row (0 without a window)
-  int pad[4];
+  int part;    // split-partial slot of this split (a split entry), -1 for an unsplit one
+  int pad[3];
 };
 constexpr int kFirst = 1 << 8, kLast = 1 << 9;
 
@@ -226,9 +227,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         break;
       }
       const int item = u / p.Hk, k = u - item * p.Hk;
-      const int2 bsplit = p.dec_items[item];
-      const int b = bsplit.x;
-      const SeqInfo si = p.seq[b];
+      const int2 bsplit = p.dec_items[item];  // (decode entry, split)
+      const SeqInfo si = p.seq[bsplit.x];
+      const int b = si.b;                      // the entry's sequence: its block_table row
       const int start = si.lo + bsplit.y * split_keys;
       const int end = min(si.kv_len, start + split_keys);
       const int past = si.kv_len - si.q_len;
@@ -298,6 +299,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
             t.nsplit = si.dec_count;
             t.qi = qi;
             t.lo_min = lo_min;
+            t.part = si.part_first >= 0 ? si.part_first + bsplit.y : -1;
             mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           }
         }
@@ -606,7 +608,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           if (p.head_sink && M != -INFINITY) den += exp2f(__half2float(p.head_sink[h]) * kLog2e - M);
           p.out[((size_t)t * p.H + h) * D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
         } else {
-          const size_t row = (size_t)tg.u * kDecodeRows + r;
+          const size_t row = ((size_t)tg.part * p.Hk + tg.k) * kDecodeRows + r;
           p.part_o[row * D + d] = acc;
           if (d == 0) p.part_ml[row] = make_float2(M, den);
         }

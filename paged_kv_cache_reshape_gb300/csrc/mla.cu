@@ -61,7 +61,8 @@ struct Tag {
   int u;       // item * (32-head groups) + group; -1 = no more work
   int key0, end, flags;
   int past, t0, hg, kv_len;
-  int nsplit, qi, lo_min, pad;
+  int nsplit, qi, lo_min;
+  int part;    // split-partial slot of this split, -1 for an unsplit entry
 };
 
 constexpr int kSmemBytes = 1024 + kStages * kTileBytes + 2 * kQBytes + 2 * kPBytes + 2 * kWarps * 16 * 4 +
@@ -147,9 +148,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int item = u / groups32, hg = u - item * groups32;
-      const int2 bsplit = p.dec_items[item];
-      const int b = bsplit.x;
-      const SeqInfo si = p.seq[b];
+      const int2 bsplit = p.dec_items[item];  // (decode entry, split)
+      const SeqInfo si = p.seq[bsplit.x];
+      const int b = si.b;                      // the entry's sequence: its block_table row
       const int start = si.lo + bsplit.y * split_keys;
       const int end = min(si.kv_len, start + split_keys);
       const int past = si.kv_len - si.q_len;
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             t.nsplit = si.dec_count;
             t.qi = qi;
             t.lo_min = lo_min;
+            t.part = si.part_first >= 0 ? si.part_first + bsplit.y : -1;
             mbar_arrive_expect_tx(&full[stage], kTileBytes);
           }
         }
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint32_t*>(dst + nd * 8) = pack_half2(o[nd][2 * i] * inv, o[nd][2 * i + 1] * inv);
         } else {
           // partial rows of 16-head group 2 * hg + wg (h < H keeps it < groups)
-          const size_t prow = ((size_t)(tg.u / groups32) * p.groups + tg.hg * 2 + wg) * kDecodeRows + row;
+          const size_t prow = ((size_t)tg.part * p.groups + tg.hg * 2 + wg) * kDecodeRows + row;
           float* dst = p.part_o + prow * kDV + wi * 128 + cq;
 #pragma unroll
           for (int nd = 0; nd < 16; ++nd)

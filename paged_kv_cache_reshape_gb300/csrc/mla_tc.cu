@@ -76,7 +76,8 @@ struct UnitInfo {
   int lo_min;  // smallest admitted position (window), 0 without one
   int kv_len;  // past + 1
   int nsplit;  // splits of the sequence
-  int pad[4];
+  int part;    // split-partial slot of this split, -1 for an unsplit entry
+  int pad[3];
 };
 
 struct Ctrl {
@@ -181,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int item = u / per_item, rest = u - item * per_item;
       const int ht = rest >> 1, half = rest & 1;
-      const int2 bsplit = p.dec_items[item];
+      const int2 bsplit = p.dec_items[item];  // (decode entry, split)
       const SeqInfo si = p.seq[bsplit.x];
       const int start = si.lo + bsplit.y * split_keys;
       const int end = min(si.kv_len, start + split_keys);
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ti.lo_min = p.window >= 1 ? max(0, past + 1 - p.window) : 0;
         ti.kv_len = si.kv_len;
         ti.nsplit = si.dec_count;
+        ti.part = si.part_first >= 0 ? si.part_first + bsplit.y : -1;
         mbar_arrive(&ctl->info_full[slot]);
         // Q: the previous unit's tiles are all consumed (the staging slots
         // are free) and its last S has completed (Q's shared-memory part is
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // Block ids, 32 block-table rows at a time, one per lane.
-      const int* bt_row = p.block_table + (size_t)bsplit.x * p.MB;
+      const int* bt_row = p.block_table + (size_t)si.b * p.MB;
       auto load_id = [&](int r) -> int { return (r < p.MB && r * p.bs < end) ? __ldg(bt_row + r) : -1; };
       int win = start / p.bs;
       int id = load_id(win + lane);
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         // rows of 16-head group h / 16 of the item, as the combine kernel reads them
-        const size_t prow = ((size_t)ti.item * p.groups + h / kDecodeRows) * kDecodeRows + h % kDecodeRows;
+        const size_t prow = ((size_t)ti.part * p.groups + h / kDecodeRows) * kDecodeRows + h % kDecodeRows;
         float* dst = p.part_o + prow * kDV + c0;
 #pragma unroll 1
         for (int c = 0; c < kHalf / 32; ++c) {

@@ -23,23 +23,34 @@ constexpr int kDecodeItemsPerCta = 2;
 constexpr int kPrefillRows = 128;   // query rows per prefill tile (UMMA M)
 constexpr int kPrefillKeys = 128;   // keys per prefill KV tile (UMMA N of S)
 
-enum Route { kRouteNone = 0, kRouteDecode = 1, kRoutePrefill = 2 };
+// How a sequence's rows are served: one decode entry, decode entries of
+// chunk_tokens tokens each, or the prefill kernel.
+enum Route { kRouteNone = 0, kRouteDecode = 1, kRoutePrefill = 2, kRouteChunked = 3 };
 
-// Per-sequence facts derived on the device each step.
-// Decode items are listed full splits first (every split of every sequence
-// but its last), then the last, usually shorter, split of each sequence, so
-// the dynamic item queue hands out the long items first.
+// Facts derived on the device each step, in two tables.  The sequence
+// table has one entry per sequence (its lengths and prefill tiles).  The
+// decode table has one entry per unit of decode work: a sequence whose
+// q_len * G query rows fit one decode item, or a chunk of chunk_tokens
+// consecutive new tokens of a longer sequence that has no prefill kernel
+// (8-bit caches, the latent layout), each chunk attending causally from
+// its own first token's position.  Decode items and combine rows refer to
+// the decode table.
+// Decode items are listed full splits first (every split of every entry
+// but its last), then the last, usually shorter, split of each entry,
+// longest first, so the dynamic item queue hands out the long items first.
 struct SeqInfo {
-  int q_len;      // new tokens (0 when the sequence is skipped)
-  int kv_len;     // past + q_len
+  int q_len;      // new tokens of the sequence or chunk (0 when the sequence is skipped)
+  int kv_len;     // position of its last new token + 1
   int lo;         // first key position walked (64-aligned window start or 0)
-  int t0;         // first packed row (cum[b])
+  int t0;         // first packed row
   int dec_first;  // item index of split 0 (splits 0..dec_count-2 are consecutive)
-  int dec_count;  // decode splits (0 unless routed to decode)
+  int dec_count;  // decode splits
   int dec_last;   // item index of split dec_count-1
-  int pre_first;  // first prefill tile of this sequence
-  int pre_count;  // prefill query tiles (0 unless routed to prefill)
-  int pad[3];
+  int pre_first;  // first prefill tile of this sequence (sequence table)
+  int pre_count;  // prefill query tiles (sequence table; 0 unless routed to prefill)
+  int comb_first; // first combine row of the entry (decode table)
+  int b;          // the sequence: its block_table row (decode table)
+  int part_first; // split partials of a split entry: slots part_first + split (decode table; -1 unsplit)
 };
 
 __host__ __device__ inline int dec_item_of_split(const SeqInfo& s, int split) {
@@ -71,7 +82,11 @@ struct WorklistParams {
   int split_keys_fixed;    // > 0 forces keys per split
   int target_pairs;        // desired number of decode (b, split) items
   int min_split_keys;      // smallest automatic split (a multiple of 64)
-  int cap_dec, cap_pre, cap_comb;
+  int chunk_tokens;        // > 0: a sequence with q_len * G > dec_max_rows goes to the decode kernel
+                           // in chunks of this many tokens (chunk_tokens * G <= dec_max_rows);
+                           // 0: it goes to the prefill kernel
+  int cap_dec, cap_pre, cap_comb, cap_dseq;
+  int cap_part;            // split-partial slots (one per split of a split decode entry)
   // SM split between the prefill and decode kernels.  With split_sms > 0
   // the prefill kernel is launched first, one CTA per SM, and the work list
   // decides how many of its CTAs keep working; the others exit, and the
@@ -85,10 +100,11 @@ struct WorklistParams {
   float pre_rate_sm;         // prefill FLOP per us per SM
   float dec_rate_sm;         // decode bytes per us per SM
   float hbm_rate;            // bytes per us
-  SeqInfo* seq;
-  int2* dec_items;  // (b, split)
-  int2* pre_tiles;  // (b, tile)
-  int2* comb_rows;  // (t, b)
+  SeqInfo* seq;      // sequence table [batch]
+  SeqInfo* dseq;     // decode table [cap_dseq]
+  int2* dec_items;   // (decode entry, split)
+  int2* pre_tiles;   // (b, tile)
+  int2* comb_rows;   // (t, decode entry)
   Counters* counters;
   int* err;
 };
@@ -141,7 +157,7 @@ struct DecodeParams {
   int per_channel;
   int cache_type;
   const int* block_table;
-  const SeqInfo* seq;
+  const SeqInfo* seq;       // the decode table
   const int2* dec_items;
   Counters* counters;  // n_dec, split_keys, and the item queue head
   float* part_o;    // [items*Hk*16*D]
@@ -169,7 +185,7 @@ struct CombineParams {
   const __half* head_sink;  // [H] or null
   const float* part_o;
   const float2* part_ml;
-  const SeqInfo* seq;
+  const SeqInfo* seq;       // the decode table
   const int2* comb_rows;
   const Counters* counters;
   __half* out;
@@ -184,7 +200,7 @@ struct PrefillParams {
   __half* out;
   const __half* head_sink;  // [H] or null
   const int* block_table;
-  const SeqInfo* seq;
+  const SeqInfo* seq;       // the sequence table
   const int2* pre_tiles;
   Counters* counters;  // n_pre and the tile queue head
   int* err;
@@ -205,7 +221,7 @@ __host__ __device__ inline int mla_item_groups(int groups16) { return (groups16 
 struct MlaParams {
   __half* out;           // [T, H, 512]
   const int* block_table;
-  const SeqInfo* seq;
+  const SeqInfo* seq;    // the decode table
   const int2* dec_items;
   Counters* counters;
   float* part_o;         // [items * groups * 16 * 512]

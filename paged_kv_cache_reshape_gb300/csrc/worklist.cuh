@@ -18,10 +18,11 @@ namespace worklist {
 constexpr int kThreads = 1024;  // the builder runs in one CTA of this size
 
 struct Int3 {
-  int a, b, c, d;  // full decode splits, prefill tiles, combine rows, last decode splits
+  int a, b, c, d, e;  // full decode splits, prefill tiles, combine rows, decode entries (last splits),
+                      // split decode entries
 };
 
-// Exclusive scan of three counters across the block; returns the prefix and
+// Exclusive scan of the five counters across the block; returns the prefix and
 // writes the block totals to *tot.  All threads must call it.
 __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
   __shared__ Int3 warp_sums[32];
@@ -34,11 +35,13 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
     int b = __shfl_up_sync(0xffffffffu, inc.b, o);
     int c = __shfl_up_sync(0xffffffffu, inc.c, o);
     int d = __shfl_up_sync(0xffffffffu, inc.d, o);
+    int e = __shfl_up_sync(0xffffffffu, inc.e, o);
     if (lane >= o) {
       inc.a += a;
       inc.b += b;
       inc.c += c;
       inc.d += d;
+      inc.e += e;
     }
   }
   if (lane == 31) warp_sums[warp] = inc;
@@ -52,20 +55,23 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
       int b = __shfl_up_sync(0xffffffffu, wi.b, o);
       int c = __shfl_up_sync(0xffffffffu, wi.c, o);
       int d = __shfl_up_sync(0xffffffffu, wi.d, o);
+      int e = __shfl_up_sync(0xffffffffu, wi.e, o);
       if (lane >= o) {
         wi.a += a;
         wi.b += b;
         wi.c += c;
         wi.d += d;
+        wi.e += e;
       }
     }
-    warp_sums[lane] = Int3{wi.a - w.a, wi.b - w.b, wi.c - w.c, wi.d - w.d};
+    warp_sums[lane] = Int3{wi.a - w.a, wi.b - w.b, wi.c - w.c, wi.d - w.d, wi.e - w.e};
     if (lane == 31) total = wi;
   }
   __syncthreads();
   *tot = total;
   Int3 base = warp_sums[warp];
-  Int3 out{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c, base.d + inc.d - v.d};
+  Int3 out{base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c, base.d + inc.d - v.d,
+           base.e + inc.e - v.e};
   __syncthreads();
   return out;
 }
@@ -95,6 +101,20 @@ struct Lens {
   int q, past, t0, lo, route;
 };
 
+__device__ int route_of(const WorklistParams& p, int q) {
+  if ((long long)q * p.group <= p.dec_max_rows) return kRouteDecode;
+  return p.chunk_tokens > 0 ? kRouteChunked : kRoutePrefill;
+}
+
+// First key position a row at `past` (the earliest new token) may attend,
+// aligned down to a 64-key stage: with a window W the earliest admitted
+// position is past + 1 - W (section 9.2 block-table pruning).
+__device__ int walk_start(const WorklistParams& p, int past) {
+  int lo = 0;
+  if (p.prune && p.window >= 1) lo = max(0, past + 1 - p.window);
+  return lo & ~(kStageKeys - 1);
+}
+
 __device__ Lens read_lens(const WorklistParams& p, int b, int* err_bits) {
   Lens L{0, 0, 0, 0, kRouteNone};
   int c0 = p.cum[b], c1 = p.cum[b + 1], past = p.past[b];
@@ -111,14 +131,118 @@ __device__ Lens read_lens(const WorklistParams& p, int b, int* err_bits) {
   L.q = q;
   L.past = past;
   L.t0 = c0;
-  // First key any row of this sequence may attend to, aligned down to a
-  // 64-key stage.  With a window W the earliest admitted position of the
-  // first new token is past + 1 - W (section 9.2 block-table pruning).
-  int lo = 0;
-  if (p.prune && p.window >= 1) lo = max(0, past + 1 - p.window);
-  L.lo = lo & ~(kStageKeys - 1);
-  L.route = (q * p.group <= p.dec_max_rows) ? kRouteDecode : kRoutePrefill;
+  L.lo = walk_start(p, past);
+  L.route = route_of(p, q);
   return L;
+}
+
+// Decode-table entries of a sequence: the sequence itself (decode route)
+// or its chunks of chunk_tokens tokens (chunked route).
+struct Entry {
+  int q, past, t0, lo;
+};
+
+__device__ int entry_count(const WorklistParams& p, const Lens& L) {
+  if (L.route == kRouteDecode) return 1;
+  if (L.route == kRouteChunked) return (L.q + p.chunk_tokens - 1) / p.chunk_tokens;
+  return 0;
+}
+
+__device__ Entry entry_of(const WorklistParams& p, const Lens& L, int c) {
+  if (L.route == kRouteDecode) return Entry{L.q, L.past, L.t0, L.lo};
+  const int ct = p.chunk_tokens;
+  Entry e;
+  e.q = min(ct, L.q - c * ct);
+  e.past = L.past + c * ct;
+  e.t0 = L.t0 + c * ct;
+  e.lo = walk_start(p, e.past);
+  return e;
+}
+
+// Keys an entry walks, and its splits.
+__device__ int entry_span(const Entry& e) { return e.past + e.q - e.lo; }
+__device__ int entry_splits(const Entry& e, int split_keys) { return (entry_span(e) + split_keys - 1) / split_keys; }
+
+// Decode keys a sequence's entries walk (they set the split size).
+__device__ long long decode_span(const WorklistParams& p, const Lens& L) {
+  long long span = 0;
+  const int n = entry_count(p, L);
+  for (int c = 0; c < n; ++c) span += entry_span(entry_of(p, L, c));
+  return span;
+}
+
+// Counts of one sequence: a = full decode splits, b = prefill tiles, c =
+// combine rows, d = decode entries (one last split each), e = split
+// entries (a + e split-partial slots).
+__device__ Int3 seq_counts(const WorklistParams& p, const Lens& L, int split_keys) {
+  Int3 cnt{0, 0, 0, 0, 0};
+  const int n = entry_count(p, L);
+  for (int c = 0; c < n; ++c) {
+    const Entry e = entry_of(p, L, c);
+    const int ns = entry_splits(e, split_keys);
+    cnt.a += ns - 1;
+    if (ns > 1) {
+      cnt.c += e.q;
+      cnt.e += 1;
+    }
+  }
+  cnt.d = n;
+  if (L.route == kRoutePrefill) cnt.b = (L.q + p.prefill_tile_tokens - 1) / p.prefill_tile_tokens;
+  return cnt;
+}
+
+// Writes the decode-table entries of sequence b (the first at index v0),
+// their full splits from item a0 on, their combine rows from row c0 on and
+// their split-partial slots from slot s0 on; last_item(c, entry, splits)
+// gives the item index of entry c's last split.
+template <typename LastItem>
+__device__ void write_entries(const WorklistParams& p, const Lens& L, int b, int v0, int a0, int c0, int s0,
+                              int split_keys, LastItem last_item) {
+  const int n = entry_count(p, L);
+  for (int c = 0; c < n; ++c) {
+    const Entry e = entry_of(p, L, c);
+    const int ns = entry_splits(e, split_keys);
+    const int v = v0 + c;
+    SeqInfo d;
+    d.q_len = e.q;
+    d.kv_len = e.past + e.q;
+    d.lo = e.lo;
+    d.t0 = e.t0;
+    d.dec_first = a0;
+    d.dec_count = ns;
+    d.dec_last = last_item(c, e, ns);
+    d.pre_first = 0;
+    d.pre_count = 0;
+    d.comb_first = c0;
+    d.b = b;
+    d.part_first = ns > 1 ? s0 : -1;
+    p.dseq[v] = d;
+    for (int s = 0; s + 1 < ns; ++s) p.dec_items[a0 + s] = make_int2(v, s);
+    p.dec_items[d.dec_last] = make_int2(v, ns - 1);
+    if (ns > 1)
+      for (int j = 0; j < e.q; ++j) p.comb_rows[c0 + j] = make_int2(e.t0 + j, v);
+    a0 += ns - 1;
+    if (ns > 1) {
+      c0 += e.q;
+      s0 += ns;
+    }
+  }
+}
+
+// Sequence-table entry of sequence b.
+__device__ void write_seq(const WorklistParams& p, const Lens& L, int b, int pre_first, int pre_count) {
+  SeqInfo si;
+  si.q_len = L.q;
+  si.kv_len = L.past + L.q;
+  si.lo = L.lo;
+  si.t0 = L.t0;
+  si.dec_first = si.dec_count = si.dec_last = 0;
+  si.pre_first = pre_first;
+  si.pre_count = pre_count;
+  si.comb_first = 0;
+  si.b = b;
+  si.part_first = 0;
+  p.seq[b] = si;
 }
 
 // (query token, admitted key) pairs of a prefill-routed sequence, for the
@@ -187,60 +311,44 @@ __device__ void build_small(const WorklistParams& p) {
   const int b = threadIdx.x;
   Lens L{0, 0, 0, 0, kRouteNone};
   if (b < p.batch) L = read_lens(p, b, &err_bits);
-  const long long span = (L.route == kRouteDecode) ? (long long)(L.past + L.q - L.lo) : 0;
-  const long long dec_keys = block_sum_ll(span);
+  const long long dec_keys = block_sum_ll(decode_span(p, L));
   // the prefill side of the SM split's cost model (no split: not needed)
   const long long pre_pairs = p.split_sms >= 2 ? block_sum_ll(prefill_pairs(L)) : 0;
   const int split_keys = split_keys_for(p, dec_keys);
-  Int3 cnt{0, 0, 0, 0};
-  if (L.route == kRouteDecode) {
-    const int n = (L.past + L.q - L.lo + split_keys - 1) / split_keys;
-    cnt.a = n - 1;
-    cnt.d = 1;
-    if (n > 1) cnt.c = L.q;
-  } else if (L.route == kRoutePrefill) {
-    cnt.b = (L.q + p.prefill_tile_tokens - 1) / p.prefill_tile_tokens;
-  }
+  const Int3 cnt = seq_counts(p, L, split_keys);
   Int3 tot;
   const Int3 pre = block_exclusive_scan3(cnt, &tot);
-  const bool overflow = tot.a + tot.d > p.cap_dec || tot.b > p.cap_pre || tot.c > p.cap_comb;
+  const bool overflow = tot.a + tot.d > p.cap_dec || tot.b > p.cap_pre || tot.c > p.cap_comb ||
+                        tot.d > p.cap_dseq || tot.a + tot.e > p.cap_part;
   // Last splits, longest first: they are the only items shorter than
   // split_keys, so handing them out in decreasing size keeps the dynamic
-  // queue's tail short.  Bucket = 64-key groups, counting sort.
+  // queue's tail short.  Bucket = 64-key groups, counting sort; an entry's
+  // place within its bucket comes from an atomic (the item order does not
+  // change any result).
   __shared__ int hist[kThreads];
   hist[threadIdx.x] = 0;
   __syncthreads();
-  int bucket = 0, rank = 0;
-  if (cnt.d) {
-    const int last = L.past + L.q - L.lo - cnt.a * split_keys;  // keys of the last split, >= 1
-    bucket = kThreads - 1 - min(kThreads - 1, (last - 1) / kStageKeys);
-    rank = atomicAdd(&hist[bucket], 1);
+  const int n_e = cnt.d;
+  auto last_bucket = [&](const Entry& e, int ns) {
+    const int last = entry_span(e) - (ns - 1) * split_keys;  // keys of the last split, >= 1
+    return kThreads - 1 - min(kThreads - 1, (last - 1) / kStageKeys);
+  };
+  for (int c = 0; c < n_e; ++c) {
+    const Entry e = entry_of(p, L, c);
+    atomicAdd(&hist[last_bucket(e, entry_splits(e, split_keys))], 1);
   }
   __syncthreads();
   Int3 htot;
-  const Int3 hpre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
+  const Int3 hpre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0, 0}, &htot);
   __syncthreads();
   hist[threadIdx.x] = hpre.a;
   __syncthreads();
   if (b < p.batch) {
-    SeqInfo si;
-    si.q_len = L.q;
-    si.kv_len = L.past + L.q;
-    si.lo = L.lo;
-    si.t0 = L.t0;
-    si.dec_first = pre.a;
-    si.dec_count = cnt.a + cnt.d;
-    si.dec_last = tot.a + (cnt.d ? hist[bucket] + rank : 0);
-    si.pre_first = pre.b;
-    si.pre_count = cnt.b;
-    si.pad[0] = pre.c;
-    si.pad[1] = si.pad[2] = 0;
-    p.seq[b] = si;
-    if (!overflow) {
-      for (int s = 0; s < cnt.a; ++s) p.dec_items[si.dec_first + s] = make_int2(b, s);
-      if (cnt.d) p.dec_items[si.dec_last] = make_int2(b, cnt.a);
-      for (int j = 0; j < cnt.c; ++j) p.comb_rows[pre.c + j] = make_int2(L.t0 + j, b);
-    }
+    write_seq(p, L, b, pre.b, cnt.b);
+    if (!overflow)
+      write_entries(p, L, b, pre.d, pre.a, pre.c, pre.a + pre.e, split_keys, [&](int, const Entry& e, int ns) {
+        return tot.a + atomicAdd(&hist[last_bucket(e, ns)], 1);
+      });
   }
   // Prefill tiles, costliest first (cost ~ the tile's last position, in
   // 64-key buckets): the same counting sort over every tile of every
@@ -255,7 +363,7 @@ __device__ void build_small(const WorklistParams& p) {
     };
     for (int s = 0; s < cnt.b; ++s) atomicAdd(&hist[tile_bucket(s)], 1);
     __syncthreads();
-    const Int3 ppre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0}, &htot);
+    const Int3 ppre = block_exclusive_scan3(Int3{hist[threadIdx.x], 0, 0, 0, 0}, &htot);
     __syncthreads();
     hist[threadIdx.x] = ppre.a;
     __syncthreads();
@@ -279,8 +387,8 @@ __device__ void build(const WorklistParams& p) {
     int b = base + threadIdx.x;
     if (b < p.batch) {
       int dummy = 0;
-      Lens L = read_lens(p, b, &dummy);
-      if (L.route == kRouteDecode) span += (long long)(L.past + L.q - L.lo);
+      const Lens L = read_lens(p, b, &dummy);
+      span += decode_span(p, L);
       pairs += prefill_pairs(L);
     }
   }
@@ -288,61 +396,53 @@ __device__ void build(const WorklistParams& p) {
   const long long pre_pairs = p.split_sms >= 2 ? block_sum_ll(pairs) : 0;
   const int split_keys = split_keys_for(p, dec_keys);
 
-  // Pass 2: counts and scans; the items are written in pass 3 once the
-  // number of full decode splits (which precede every last split) is known.
-  Int3 carry{0, 0, 0, 0};
+  // Pass 2: counts and scans.  The totals fix where every list starts; the
+  // number of full decode splits (which precede every last split) is known
+  // only at the end, so the items are written in pass 3.  Last splits stay
+  // in entry order here.
+  Int3 carry{0, 0, 0, 0, 0};
   for (int base = 0; base < p.batch; base += kThreads) {
     int b = base + threadIdx.x;
     Lens L{0, 0, 0, 0, kRouteNone};
-    Int3 cnt{0, 0, 0, 0};
+    Int3 cnt{0, 0, 0, 0, 0};
     if (b < p.batch) {
       L = read_lens(p, b, &err_bits);
-      if (L.route == kRouteDecode) {
-        int kv = L.past + L.q;
-        int n = (kv - L.lo + split_keys - 1) / split_keys;
-        cnt.a = n - 1;
-        cnt.d = 1;
-        if (n > 1) cnt.c = L.q;
-      } else if (L.route == kRoutePrefill) {
-        cnt.b = (L.q + p.prefill_tile_tokens - 1) / p.prefill_tile_tokens;
-      }
+      cnt = seq_counts(p, L, split_keys);
     }
     Int3 tot;
-    Int3 pre = block_exclusive_scan3(cnt, &tot);
+    const Int3 pre = block_exclusive_scan3(cnt, &tot);
     if (b < p.batch) {
-      SeqInfo si;
-      si.q_len = L.q;
-      si.kv_len = L.past + L.q;
-      si.lo = L.lo;
-      si.t0 = L.t0;
-      si.dec_first = carry.a + pre.a;
-      si.dec_count = cnt.a + cnt.d;
-      si.dec_last = carry.d + pre.d;  // offset by the full-split total in pass 3
-      si.pre_first = carry.b + pre.b;
-      si.pre_count = cnt.b;
-      si.pad[0] = carry.c + pre.c;    // first combine row
-      si.pad[1] = si.pad[2] = 0;
-      p.seq[b] = si;
+      write_seq(p, L, b, carry.b + pre.b, cnt.b);
+      // the prefixes pass 3 needs, kept in this sequence's entry
+      p.seq[b].dec_first = carry.a + pre.a;
+      p.seq[b].dec_last = carry.d + pre.d;  // first decode entry (and last split, before the full splits)
+      p.seq[b].comb_first = carry.c + pre.c;
+      p.seq[b].part_first = carry.a + carry.e + pre.a + pre.e;
+      p.seq[b].dec_count = cnt.d;
     }
     carry.a += tot.a;
     carry.b += tot.b;
     carry.c += tot.c;
     carry.d += tot.d;
+    carry.e += tot.e;
   }
   const int n_full = carry.a;
-  const bool overflow = carry.a + carry.d > p.cap_dec || carry.b > p.cap_pre || carry.c > p.cap_comb;
+  const bool overflow = carry.a + carry.d > p.cap_dec || carry.b > p.cap_pre || carry.c > p.cap_comb ||
+                        carry.d > p.cap_dseq || carry.a + carry.e > p.cap_part;
   __syncthreads();
-  // Pass 3: work items (skipped entirely if a list would overflow).
+  // Pass 3: decode entries, items and tiles (skipped if a list would overflow).
   if (!overflow) {
     for (int b = threadIdx.x; b < p.batch; b += kThreads) {
-      SeqInfo si = p.seq[b];
+      const SeqInfo si = p.seq[b];
       if (si.dec_count > 0) {
-        si.dec_last += n_full;
-        p.seq[b].dec_last = si.dec_last;
-        for (int s = 0; s + 1 < si.dec_count; ++s) p.dec_items[si.dec_first + s] = make_int2(b, s);
-        p.dec_items[si.dec_last] = make_int2(b, si.dec_count - 1);
-        if (si.dec_count > 1)
-          for (int j = 0; j < si.q_len; ++j) p.comb_rows[si.pad[0] + j] = make_int2(si.t0 + j, b);
+        Lens L;
+        L.q = si.q_len;
+        L.past = si.kv_len - si.q_len;
+        L.t0 = si.t0;
+        L.lo = si.lo;
+        L.route = route_of(p, si.q_len);
+        write_entries(p, L, b, si.dec_last, si.dec_first, si.comb_first, si.part_first, split_keys,
+                      [&](int c, const Entry&, int) { return n_full + si.dec_last + c; });
       }
       for (int s = 0; s < si.pre_count; ++s) p.pre_tiles[si.pre_first + s] = make_int2(b, s);
     }

@@ -84,10 +84,8 @@ def test_config_rule(field, value, status, word):
           v_quant_type=pa.PA_QUANT_PER_TENSOR, head_size=64, max_query_len_bound=1), pa.PA_NOT_SUPPORTED,
      "head_size"),
     (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
-          v_quant_type=pa.PA_QUANT_PER_TENSOR), pa.PA_NOT_SUPPORTED, "decode kernel only"),
-    (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
-          v_quant_type=pa.PA_QUANT_PER_TENSOR, max_query_len_bound=5), pa.PA_NOT_SUPPORTED,
-     "decode kernel only"),
+          v_quant_type=pa.PA_QUANT_PER_TENSOR, num_heads=64, kv_num_heads=2), pa.PA_NOT_SUPPORTED,
+     "num_heads / kv_num_heads <= 16"),
 ])
 def test_quantized_cache_rules(over, status, word):
     st, msg = pa.pa_validate_config(good(**over))
@@ -135,7 +133,6 @@ def latent(**over):
     (dict(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=1, v_quant_type=1), pa.PA_NOT_SUPPORTED, "latent"),
     (dict(head_size=512, v_head_size=448), pa.PA_NOT_SUPPORTED, "576"),
     (dict(num_heads=24), pa.PA_NOT_SUPPORTED, "multiple of 16"),
-    (dict(max_query_len_bound=2), pa.PA_NOT_SUPPORTED, "decode steps only"),
 ])
 def test_latent_rules(over, status, word):
     st, msg = pa.pa_validate_config(latent(**over))
@@ -252,3 +249,17 @@ def test_create_without_gpu_reports_cuda_error():
     with pytest.raises(pa.PAError) as e:
         pa.pa_create(good(block_size=24))
     assert e.value.status == pa.PA_INVALID_ARGUMENT and "block_size" in e.value.message
+
+
+@pytest.mark.parametrize("over", [dict(), dict(max_query_len_bound=5), dict(max_query_len_bound=4096)])
+def test_quantized_cache_takes_prompt_rows(over):
+    # longer query rows run through the decode kernel in chunks of 16 / G tokens
+    st, msg = pa.pa_validate_config(good(cache_dtype=pa.PA_CACHE_FP8_E4M3, k_quant_type=pa.PA_QUANT_PER_TENSOR,
+                                         v_quant_type=pa.PA_QUANT_PER_TENSOR, **over))
+    assert st == pa.PA_OK, msg
+
+
+def test_latent_layout_takes_prompt_rows():
+    # longer query rows run as one-token decode entries (the absorbed form)
+    st, msg = pa.pa_validate_config(latent(max_query_len_bound=64))
+    assert st == pa.PA_OK, msg

@@ -109,3 +109,39 @@ def test_latent_full_size_step_sampled(kernel):
                                 host["cumulative_sequence_lengths"], host["past_sequence_lengths"], H, 576, 512,
                                 64, SCALE, 0.0, -1, rows=rows, threads=16)
     assert_close(out.float().cpu().numpy().reshape(T * H, 512)[rows], o)
+
+
+LATENT_PROMPTS = [
+    # several new tokens per sequence: each token is its own decode entry,
+    # attending causally over the cached rows and the step's earlier tokens
+    cs("mla_h16_prompts", 16, 1, 576, 64, [0, 50, 700], [20, 3, 1], scale=SCALE, do_rotary=1, rotary_dim=64,
+       seed=82),
+    cs("mla_h48_prompts_window_cap", 48, 1, 576, 32, [0, 300], [70, 5], scale=SCALE, softcap=30.0,
+       local_window_size=40, seed=83),
+    cs("mla_tc_h128_prompts", 128, 1, 576, 64, [0, 129, 2000], [33, 2, 1], scale=SCALE, do_rotary=1, rotary_dim=64,
+       seed=84),
+]
+
+
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+@pytest.mark.parametrize("shape", LATENT_PROMPTS, ids=lambda s: s.name)
+def test_latent_prompt_rows_match_oracle(shape, kernel):
+    """Chunked prefill / prefix caching on the latent layout: sequences with
+    many new tokens run in the absorbed form, one token per decode entry."""
+    opts = _kernel_options(kernel, shape.num_heads)
+    step = _step(shape)
+    host = host_copy(step)
+    op, out, err = run(step, options=opts)
+    assert err == 0
+    counts = op.last_step_counts()
+    assert counts["n_pre"] == 0 and counts["n_dec"] >= shape.token_count
+    check_full(host, step, out)
+
+
+def test_latent_prompt_rows_with_splits():
+    shape = cs("mla_prompts_splits", 32, 1, 576, 64, [0, 1000], [40, 2], scale=SCALE, seed=85)
+    step = _step(shape)
+    host = host_copy(step)
+    _, out, err = run(step, options=[(pa.PA_OPT_SPLIT_KEYS, 128), (pa.PA_OPT_LATENT_TCGEN05, 0)])
+    assert err == 0
+    check_full(host, step, out)

@@ -152,3 +152,44 @@ def test_quantized_rotary_at_an_offset(cache_dtype, quant_type):
     op, out, err = run(step, max_tokens=step["token_count"], max_query_len_bound=2)
     assert err == 0, f"device error {err:#x}"
     check_full(host, step, out)
+
+
+QUANT_PROMPTS = [
+    # q_len * G > 16: the rows run through the decode kernel in chunks of
+    # 16 / G tokens, each chunk attending causally from its first token
+    cs("q_prompt_d128_g4", 8, 2, 128, 16, [0, 70, 300, 5], [40, 1, 17, 3], seed=31),
+    cs("q_prompt_d128_g8_bs32", 16, 2, 128, 32, [0, 33], [25, 9], seed=32),
+    cs("q_prompt_d256_g2_window_cap", 4, 2, 256, 64, [0, 100], [60, 11], scale=1 / 16, softcap=50.0,
+       local_window_size=45, seed=33),
+    cs("q_prompt_d128_g1_rotary", 4, 4, 128, 16, [0, 9], [50, 20], do_rotary=1, seed=34),
+]
+
+
+@pytest.mark.parametrize("cache_dtype", [I8, F8], ids=["int8", "e4m3"])
+@pytest.mark.parametrize("quant_type", [PT, PC], ids=["per_tensor", "per_channel"])
+@pytest.mark.parametrize("shape", QUANT_PROMPTS, ids=lambda s: s.name)
+def test_quantized_prompt_rows_match_oracle(shape, cache_dtype, quant_type):
+    """Prompt and mixed steps over 8-bit pools (every token of a quantized
+    cache goes through the decode kernel, which reads the codes at their
+    stored width)."""
+    op, _ = _full(shape, cache_dtype=cache_dtype, quant_type=quant_type, head_sink=True)
+    counts = op.last_step_counts()
+    assert counts["n_pre"] == 0
+
+
+@pytest.mark.parametrize("split_keys", [64, 0])
+def test_quantized_prompt_rows_with_splits(split_keys):
+    shape = cs("q_prompt_splits", 8, 2, 128, 16, [0, 1500, 600], [64, 1, 8], seed=35)
+    _full(shape, options=[(pa.PA_OPT_SPLIT_KEYS, split_keys)], cache_dtype=F8, quant_type=PC)
+
+
+def test_quantized_prompt_rows_large_batch():
+    """More sequences than one work-list block (the multi-pass builder)."""
+    import numpy as np
+    rng = np.random.default_rng(36)
+    B = 1030
+    new = [1] * B
+    for b in rng.choice(B, 12, replace=False):
+        new[b] = int(rng.integers(5, 40))
+    shape = cs("q_prompt_b1030", 8, 2, 128, 16, rng.integers(0, 60, B), new, seed=36)
+    _full(shape, cache_dtype=I8, quant_type=PT)
