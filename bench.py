@@ -59,7 +59,10 @@ sys.path.insert(0, ROOT)
 METRIC = "decode attended-KV GB/s (% of 8 TB/s HBM); mixed-batch tokens/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
-DECODE_ROWS = 16  # query rows of one decode item: q_len * G <= 16 goes to the decode kernel
+def decode_rows(G):
+    """Query rows of one decode item: q_len * G up to this goes to the decode
+    kernel (its row tiles hold 8 rows; two tiles when G > 8)."""
+    return 8 if G <= 8 else 16
 
 
 # 8-bit cache variants of the Llama-3-8B-shaped decode step (per-channel
@@ -134,7 +137,7 @@ def work_of(step, seqs=None):
             w["dec_kv_bytes"] += kv
             w["dec_qo_bytes"] += q[b] * H * (D + Dv) * 2
             w["dec_flops"] += 2 * q[b] * H * adm * (D + Dv)
-        elif q[b] * G <= DECODE_ROWS:
+        elif q[b] * G <= decode_rows(G) or step.get("cache_dtype", 0):
             w["dec_kv_bytes"] += kv
             w["dec_qo_bytes"] += 2 * q[b] * H * D * 2
         else:

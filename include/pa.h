@@ -343,7 +343,8 @@ enum {
   PA_OPT_SPLIT_KEYS = 1,      /* > 0: fixed keys per decode split (multiple of 64); 0 = auto */
   PA_OPT_NO_WINDOW_PRUNE = 2, /* 1: walk the whole context and mask instead of pruning */
   PA_OPT_KERNEL_TIMING = 3,   /* 1: record CUDA events around each kernel of pa_forward */
-  PA_OPT_DECODE_MAX_ROWS = 4, /* route a sequence to the decode kernel iff q_len*G <= value (1..16, default 16; 0 = never) */
+  PA_OPT_DECODE_MAX_ROWS = 4, /* route a sequence to the decode kernel iff q_len*G <= value (0 = never; at most and by
+                                 default the rows of a decode item: 8 when G <= 8, else 16) */
   PA_OPT_DECODE_ITEMS_PER_CTA = 5, /* target decode work items per decode CTA when splits are sized automatically:
                                       1..32, or 0 (default) = per step, 1 when the step's sequences x kv heads
                                       (latent: x work units per sequence) fill the decode grid, else 2 */

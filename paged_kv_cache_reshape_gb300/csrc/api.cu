@@ -113,6 +113,7 @@ struct pa_handle_s {
   size_t dec_smem = 0;
   int cap_dec = 1, cap_pre = 1, cap_comb = 1, cap_dseq = 1, cap_part = 1;
   int chunk_tokens = 0;  // > 0: query rows beyond one decode item run as decode entries of this many tokens
+  int dec_rows = 16;      // query rows a decode item holds (decode_item_rows of the group)
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
   size_t pre_smem = 0;
   bool prefill_ready = false;
@@ -497,7 +498,8 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->G = h->latent ? pa::kDecodeRows : c.num_heads / c.kv_num_heads;
   h->groups = h->latent ? std::max(1, c.num_heads / pa::kDecodeRows) : c.kv_num_heads;
   h->dv = h->latent ? 512 : c.head_size;
-  h->opt_dec_rows = h->G <= pa::kDecodeRows ? pa::kDecodeRows : 0;  // decode items hold <= 16 rows
+  h->dec_rows = pa::decode_item_rows(h->G);  // rows a decode item holds (0: no decode route)
+  h->opt_dec_rows = h->dec_rows;
   h->R = rot_dim_of(c);
   h->scale = c.scale > 0.f ? c.scale : 1.f / std::sqrt((float)c.head_size);
   const int kv_cap = c.max_blocks_per_seq * c.block_size;
@@ -527,10 +529,10 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   h->mla_tc = h->mla_tc_ready;
   h->unit_groups = h->mla_tc ? tc_units : h->latent ? pa::mla_item_groups(h->groups) : h->groups;
   // Query rows beyond one decode item: the prefill kernel for fp16 caches
-  // with separate K and V, decode entries of kDecodeRows / G tokens for
+  // with separate K and V, decode entries of dec_rows / G tokens for
   // 8-bit caches and the latent layout (one token: G is 16 there).
   const bool quant = c.cache_dtype != PA_CACHE_FP16;
-  h->chunk_tokens = (h->latent || quant) ? std::max(1, pa::kDecodeRows / h->G) : 0;
+  h->chunk_tokens = (h->latent || quant) ? std::max(1, h->dec_rows / h->G) : 0;
   // Decode entries: one per sequence, or one per chunk.
   h->cap_dseq = c.max_batch + (h->chunk_tokens ? (c.max_tokens + h->chunk_tokens - 1) / h->chunk_tokens : 0);
   // Decode items: the split targets (room for the items-per-CTA option's
@@ -645,10 +647,10 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
       return PA_OK;
     case PA_OPT_WAIT_PROBE: h->opt_wait_probe = value != 0; return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
-      if (h->cfg.cache_dtype != PA_CACHE_FP16 && value != pa::kDecodeRows)
-        return fail(h, PA_NOT_SUPPORTED, "8-bit caches route every sequence to the decode kernel");
-      if (value < 0 || value > pa::kDecodeRows)
-        return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", pa::kDecodeRows);
+      if ((h->cfg.cache_dtype != PA_CACHE_FP16 || h->latent) && value != h->dec_rows)
+        return fail(h, PA_NOT_SUPPORTED, "8-bit caches and the latent layout route every row to decode items");
+      if (value < 0 || value > h->dec_rows)
+        return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", h->dec_rows);
       h->opt_dec_rows = value;
       return PA_OK;
     default: return fail(h, PA_INVALID_ARGUMENT, "unknown option %d", option);
@@ -1228,7 +1230,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   const int max_kv = c.max_kv_len_bound > 0 ? std::min(c.max_kv_len_bound, kv_cap) : kv_cap;
   // Rows go to the decode kernel iff q_len * G <= 16; the prefill kernel
   // runs only when the query-length bound lets some sequence have more.
-  const int dec_max_rows = G <= pa::kDecodeRows ? pa::kDecodeRows : 0;
+  const int dec_max_rows = pa::decode_item_rows(G);
   const bool pre_launch = (long long)max_q * G > dec_max_rows;
   if (pre_launch && !nd->prefill_ok)
     return fail(nullptr, PA_NOT_SUPPORTED,

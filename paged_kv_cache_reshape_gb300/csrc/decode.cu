@@ -45,6 +45,8 @@
 //    V scale multiplies the merged output;
 //  * head_sink (section 6.1) adds exp(s_h - M) to the final denominator of a
 //    single-split row (split rows get it in the combine kernel).
+#include <algorithm>
+
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -132,22 +134,17 @@ __device__ __forceinline__ uint32_t deq2(uint32_t w) {
   }
 }
 
-// Query fragment of one m16n8k16 step in the channel order of the 8-bit K
-// fragments: lane (g = lane/4, j = lane%4) holds channels 16ks + 4j .. 4j+3
-// of rows g and g+8 (a0/a2 and a1/a3).
-__device__ __forceinline__ void q_frag_perm(const uint8_t* q, int ks, int lane, uint32_t* a) {
-  const int c = ks * 16 + 4 * (lane & 3);
-  const int r0 = lane >> 2, r1 = r0 + 8;
-  const uint32_t off = (c >> 6) * 2048 + ((c & 7) * 2);
-  const uint2 x0 = *reinterpret_cast<const uint2*>(q + off + swz(r0, (c & 63) >> 3));
-  const uint2 x1 = *reinterpret_cast<const uint2*>(q + off + swz(r1, (c & 63) >> 3));
-  a[0] = x0.x;
-  a[2] = x0.y;
-  a[1] = x1.x;
-  a[3] = x1.y;
+// Value channel of element e of O^T accumulator kk (the consumer's fragment
+// coordinates): fp16 pools, 16 channels per accumulator (fg and fg + 8);
+// 8-bit pools, the even (kk even) or odd channels of 32 (2fg + parity, and
+// 16 more).
+template <bool kQ8>
+__device__ __forceinline__ int o_channel(int kk, int e, int fg) {
+  if constexpr (kQ8) return (kk >> 1) * 32 + 2 * fg + (kk & 1) + 16 * (e >> 1);
+  else return kk * 16 + fg + 8 * (e >> 1);
 }
 
-template <int D, int CT>
+template <int D, int CT, int NT>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                                             const DecodeParams& p) {
   using C = DecodeCfg<D, CT>;
@@ -323,9 +320,20 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   }
 
   // -------------------------------------------------------------- consumers
+  // Each warp owns 16 keys of every stage.  S^T = K Q^T puts those keys in
+  // the MMA's M rows and the item's query rows in its N columns (NT tiles
+  // of 8 rows), so a GQA group of up to 8 rows wastes no M rows; the
+  // softmax runs per query row over the keys (row maxima by shuffles
+  // across the 8 key groups of the warp); O^T += V^T P^T puts the value
+  // channels in M.  P^T reaches that MMA's B operand by an in-register
+  // transpose (movmatrix) of the S^T accumulators, packed to fp16.
+  //
+  // Fragment coordinates (m16n8k16): lane = 4 * fg + ft; the S^T
+  // accumulator s[n][e] holds key fg + 8 * (e >> 1) and query row
+  // 8n + 2 ft + (e & 1); o[kk][n][e] holds value channel ch(kk, e) (see
+  // o_channel) and the same query row.
   const int ctid = threadIdx.x;  // 0..127
-  const int r0 = lane >> 2, r1 = r0 + 8;
-  const int cq = 2 * (lane & 3);
+  const int fg = lane >> 2, ft = lane & 3;
   int stage = 0;
   uint32_t phase = 0;
   int quse[2] = {0, 0};
@@ -335,12 +343,36 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   const bool capped = p.softcap > 0.f;
   const float inv_cap = capped ? 1.f / p.softcap : 0.f;
   const int log_r = p.log_box_rows;
+  constexpr int kKS = D / 16;  // 16-channel steps of the contractions
 
-  uint32_t qf[(D <= 128) ? D / 16 : 1][4];
-  float m[2], l[2];
-  float o[D / 8][4];
-  int hi0 = -1, hi1 = -1, lo0 = 0, lo1 = 0;
+  // Q^T as B fragments, per 16-channel step and row tile (D <= 128; wider
+  // heads reload them from shared memory at each use).
+  uint32_t qf[(D <= 128) ? kKS : 1][NT][2];
+  float m[NT][2], l[NT][2];  // per query row 8n + 2ft + j: running max (log2 units), partial sum
+  float o[kKS][NT][4];
+  int hi[NT][2], lo[NT][2];
   const uint8_t* qcur = qbuf;
+
+  // B fragment of Q^T for 16-channel step ks and row tile n: fp16 caches
+  // take channels 16ks + 2ft, +1 (b0) and 16ks + 8 + 2ft, +1 (b1); 8-bit
+  // caches take the contraction order of their K fragments, channels
+  // 16ks + 4ft .. +3 (b0: the first two, b1: the last two).
+  auto load_qf = [&](int ks, int n, uint32_t* b) {
+    const int row = 8 * n + fg;
+    if constexpr (kQ8) {
+      const int c = ks * 16 + 4 * ft;
+      const uint2 x = *reinterpret_cast<const uint2*>(qcur + (c >> 6) * 2048 + ((c & 7) * 2) +
+                                                       swz(row, (c & 63) >> 3));
+      b[0] = x.x;
+      b[1] = x.y;
+    } else {
+      const uint8_t* q = qcur + ((ks * 16) >> 6) * 2048;
+      const __half2 h0 = *reinterpret_cast<const __half2*>(q + swz(row, ((ks * 16) & 63) >> 3) + 4 * ft);
+      const __half2 h1 = *reinterpret_cast<const __half2*>(q + swz(row, ((ks * 16 + 8) & 63) >> 3) + 4 * ft);
+      b[0] = *reinterpret_cast<const uint32_t*>(&h0);
+      b[1] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+  };
 
   while (true) {
     if (!mbar_wait(&full[stage], phase)) {
@@ -351,7 +383,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     if (tg.u < 0) break;
 
     if (tg.flags & kFirst) {
-      // New item: its query tile, row bounds and a fresh softmax state.
+      // New item: its query fragments, row bounds and a fresh softmax state.
       if (!mbar_wait(&q_full[tg.qi], quse[tg.qi] & 1)) {
         if (lane == 0) note_timeout(p.err, p.err_site, kSiteDecode | 5);
         return;
@@ -359,35 +391,31 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       quse[tg.qi]++;
       qcur = qbuf + tg.qi * C::kQBytes;
       if constexpr (D <= 128) {
-        const int mi = lane >> 3, ri = lane & 7;
-        const int row = (mi & 1) * 8 + ri;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          if constexpr (kQ8) {
-            q_frag_perm(qcur, ks, lane, qf[ks]);
-          } else {
-            const int col = ks * 16 + (mi >> 1) * 8;
-            ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), qf[ks][0], qf[ks][1],
-                    qf[ks][2], qf[ks][3]);
-          }
-        }
+        for (int ks = 0; ks < kKS; ++ks)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) load_qf(ks, n, qf[ks][n]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&q_empty[tg.qi]);
       }
-      hi0 = hi1 = -1;
-      lo0 = lo1 = 0;
-      if (r0 < tg.R) {
-        hi0 = tg.past + r0 / p.G;  // last admitted position of the row
-        lo0 = p.window >= 1 ? max(0, hi0 + 1 - p.window) : 0;
-      }
-      if (r1 < tg.R) {
-        hi1 = tg.past + r1 / p.G;
-        lo1 = p.window >= 1 ? max(0, hi1 + 1 - p.window) : 0;
-      }
-      m[0] = m[1] = -INFINITY;
-      l[0] = l[1] = 0.f;
 #pragma unroll
-      for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int r = 8 * n + 2 * ft + j;
+          hi[n][j] = -1;
+          lo[n][j] = 0;
+          if (r < tg.R) {
+            hi[n][j] = tg.past + r / p.G;  // last admitted position of the row
+            lo[n][j] = p.window >= 1 ? max(0, hi[n][j] + 1 - p.window) : 0;
+          }
+          m[n][j] = -INFINITY;
+          l[n][j] = 0.f;
+        }
+#pragma unroll
+      for (int kk = 0; kk < kKS; ++kk)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) o[kk][n][0] = o[kk][n][1] = o[kk][n][2] = o[kk][n][3] = 0.f;
     }
 
     const int key0 = tg.key0, end = tg.end, mask = tg.flags & 0xff;
@@ -413,11 +441,14 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
     }
 
     if (kw < end && kw + 16 > tg.lo_min) {
-      // ---- S = Q K^T for 16 rows x 16 keys
-      float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      // ---- S^T = K Q^T for this warp's 16 keys x the item's query rows
+      float s[NT][4];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
       const int mi = lane >> 3, ri = lane & 7;
       if constexpr (kQ8) {
-        // one ldmatrix per 32 channels: matrix mi = keys (mi&1)*8.., channels +16*(mi>>1)
+        // one ldmatrix per 32 channels: matrix mi = keys (mi&1)*8.., channels
+        // +16*(mi>>1); lane (fg, ft) gets channels 4ft..4ft+3 of key fg (+8)
 #pragma unroll
         for (int ks2 = 0; ks2 < D / 32; ++ks2) {
           const int key = warp * 16 + (mi & 1) * 8 + ri;
@@ -429,125 +460,144 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           for (int hh = 0; hh < 2; ++hh) {
             const int ks = 2 * ks2 + hh;
             uint32_t a[4];
-            if constexpr (D <= 128) {
-              a[0] = qf[ks][0];
-              a[1] = qf[ks][1];
-              a[2] = qf[ks][2];
-              a[3] = qf[ks][3];
-            } else {
-              q_frag_perm(qcur, ks, lane, a);
+            a[0] = deq2<CT, 0, 1>(kb[2 * hh]);
+            a[1] = deq2<CT, 0, 1>(kb[2 * hh + 1]);
+            a[2] = deq2<CT, 2, 3>(kb[2 * hh]);
+            a[3] = deq2<CT, 2, 3>(kb[2 * hh + 1]);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              if constexpr (D <= 128) {
+                hmma16816(s[n], a, qf[ks][n][0], qf[ks][n][1]);
+              } else {
+                uint32_t b[2];
+                load_qf(ks, n, b);
+                hmma16816(s[n], a, b[0], b[1]);
+              }
             }
-            hmma16816(s[0], a, deq2<CT, 0, 1>(kb[2 * hh]), deq2<CT, 2, 3>(kb[2 * hh]));
-            hmma16816(s[1], a, deq2<CT, 0, 1>(kb[2 * hh + 1]), deq2<CT, 2, 3>(kb[2 * hh + 1]));
           }
         }
-      } else
+      } else {
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a[4];
-        if constexpr (D <= 128) {
-          a[0] = qf[ks][0];
-          a[1] = qf[ks][1];
-          a[2] = qf[ks][2];
-          a[3] = qf[ks][3];
-        } else {
-          const int row = (mi & 1) * 8 + ri, col = ks * 16 + (mi >> 1) * 8;
-          ldsm_x4(smem_u32(qcur + (col >> 6) * 2048 + swz(row, (col & 63) >> 3)), a[0], a[1], a[2], a[3]);
+        for (int ks = 0; ks < kKS; ++ks) {
+          // matrix mi = keys (mi&1)*8.., channels 16ks + (mi>>1)*8: a0..a3
+          const int key = warp * 16 + (mi & 1) * 8 + ri;
+          const int d16 = ks * 16 + (mi >> 1) * 8;
+          uint32_t a[4];
+          ldsm_x4(smem_u32(kt + tile_off<C::kChunks>(key, d16 >> 6, (d16 & 63) >> 3, log_r)), a[0], a[1], a[2],
+                  a[3]);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            if constexpr (D <= 128) {
+              hmma16816(s[n], a, qf[ks][n][0], qf[ks][n][1]);
+            } else {
+              uint32_t b[2];
+              load_qf(ks, n, b);
+              hmma16816(s[n], a, b[0], b[1]);
+            }
+          }
         }
-        const int key = warp * 16 + (mi >> 1) * 8 + ri;
-        const int d16 = ks * 16 + (mi & 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(smem_u32(kt + tile_off<C::kChunks>(key, d16 >> 6, (d16 & 63) >> 3, log_r)), b0, b1, b2, b3);
-        hmma16816(s[0], a, b0, b1);
-        hmma16816(s[1], a, b2, b3);
       }
-      // ---- scale, softcap, mask; row max
-      float tmax[2] = {-INFINITY, -INFINITY};
+      // ---- scale, softcap, mask; per-row max over the warp's keys
+      float tmax[NT][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int n = 0; n < NT; ++n) {
+        tmax[n][0] = tmax[n][1] = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int pos = kw + nt * 8 + cq + (e & 1);
-          const int hi = (e < 2) ? hi0 : hi1;
-          const int lo = (e < 2) ? lo0 : lo1;
+          const int j = e & 1;
+          const int pos = kw + fg + 8 * (e >> 1);
           const int box = (pos - key0) >> log_r;
-          const bool ok = pos < end && pos <= hi && pos >= lo && !((mask >> box) & 1);
-          float x = s[nt][e] * scale;
+          const bool ok = pos < end && pos <= hi[n][j] && pos >= lo[n][j] && !((mask >> box) & 1);
+          float x = s[n][e] * scale;
           if (capped) x = p.softcap * tanhf(x * inv_cap);
           x *= kLog2e;
           x = ok ? x : -INFINITY;
-          s[nt][e] = x;
-          tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
+          s[n][e] = x;
+          tmax[n][j] = fmaxf(tmax[n][j], x);
         }
       }
       // Lazy rescale: the reference max m moves only when a score exceeds
       // it by more than 2^kLazyRescale, so P stays <= 256 and O is rescaled
       // on few stages (the final merge works with any reference).
-      float alpha[2], muse[2];
+      float alpha[NT][2], muse[NT][2];
+      bool rescale = false;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 1));
-        tmax[i] = fmaxf(tmax[i], __shfl_xor_sync(0xffffffffu, tmax[i], 2));
-        alpha[i] = 1.f;
-        if (tmax[i] > m[i] + kLazyRescale) {  // also the first finite score (m = -inf)
-          alpha[i] = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - tmax[i]);
-          m[i] = tmax[i];
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float t = tmax[n][j];
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 4));
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 8));
+          t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, 16));
+          alpha[n][j] = 1.f;
+          if (t > m[n][j] + kLazyRescale) {  // also the first finite score (m = -inf)
+            alpha[n][j] = (m[n][j] == -INFINITY) ? 0.f : exp2f(m[n][j] - t);
+            m[n][j] = t;
+            rescale = true;
+          }
+          muse[n][j] = (m[n][j] == -INFINITY) ? 0.f : m[n][j];
         }
-        muse[i] = (m[i] == -INFINITY) ? 0.f : m[i];
-      }
-      float rs[2] = {0.f, 0.f};
+      uint32_t pb[NT][2];  // P^T as B fragments: keys 2ft, +1 (and + 8) of query row 8n + fg
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
+      for (int n = 0; n < NT; ++n) {
+        float pv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pv = exp2f(s[nt][e] - muse[e >> 1]);
-          s[nt][e] = pv;
-          rs[e >> 1] += pv;
-        }
+        for (int e = 0; e < 4; ++e) pv[e] = exp2f(s[n][e] - muse[n][e & 1]);
+        // this lane's keys of rows 8n + 2ft (j = 0) and 8n + 2ft + 1 (j = 1)
+        l[n][0] = l[n][0] * alpha[n][0] + (pv[0] + pv[2]);
+        l[n][1] = l[n][1] * alpha[n][1] + (pv[1] + pv[3]);
+        // the accumulator halves are m8n8 fragments of (key, row); their
+        // transposes are (row, key) pairs, the B fragment of O^T += V^T P^T
+        pb[n][0] = movmatrix_t(pack_half2(pv[0], pv[1]));
+        pb[n][1] = movmatrix_t(pack_half2(pv[2], pv[3]));
       }
-      l[0] = l[0] * alpha[0] + rs[0];
-      l[1] = l[1] * alpha[1] + rs[1];
-      if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+      if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          o[i][0] *= alpha[0];
-          o[i][1] *= alpha[0];
-          o[i][2] *= alpha[1];
-          o[i][3] *= alpha[1];
-        }
+        for (int kk = 0; kk < kKS; ++kk)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            o[kk][n][0] *= alpha[n][0];
+            o[kk][n][1] *= alpha[n][1];
+            o[kk][n][2] *= alpha[n][0];
+            o[kk][n][3] *= alpha[n][1];
+          }
       }
-      uint32_t pa[4];
-      pa[0] = pack_half2(s[0][0], s[0][1]);
-      pa[1] = pack_half2(s[0][2], s[0][3]);
-      pa[2] = pack_half2(s[1][0], s[1][1]);
-      pa[3] = pack_half2(s[1][2], s[1][3]);
-      // ---- O += P V
+      // ---- O^T += V^T P^T
       if constexpr (kQ8) {
-        // matrix mi = keys (mi&1)*8.., channels +16*(mi>>1); lane gets keys
-        // 2j, 2j+1 of channels 2n', 2n'+1: o[4g+2hh] collects the even
-        // channels 32g+16hh+2n', o[4g+2hh+1] the odd ones
+        // matrix mi = keys (mi>>1)*8.., channels +16*(mi&1), transposed: lane
+        // (fg, ft) gets keys 2ft, 2ft+1 of channels 2fg, 2fg+1; the even
+        // channels feed one MMA (o[2g32]), the odd ones another (o[2g32+1])
 #pragma unroll
-        for (int g = 0; g < D / 32; ++g) {
-          const int key = warp * 16 + (mi & 1) * 8 + ri;
-          const int c = g * 32 + (mi >> 1) * 16;
+        for (int g32 = 0; g32 < D / 32; ++g32) {
+          const int key = warp * 16 + (mi >> 1) * 8 + ri;
+          const int c = g32 * 32 + (mi & 1) * 16;
           uint32_t vb[4];
           ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, c >> 7, (c & 127) >> 4, log_r)), vb[0], vb[1], vb[2],
                     vb[3]);
+          uint32_t ae[4], ao[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            hmma16816(o[4 * g + 2 * hh], pa, deq2<CT, 0, 2>(vb[2 * hh]), deq2<CT, 0, 2>(vb[2 * hh + 1]));
-            hmma16816(o[4 * g + 2 * hh + 1], pa, deq2<CT, 1, 3>(vb[2 * hh]), deq2<CT, 1, 3>(vb[2 * hh + 1]));
+          for (int q = 0; q < 4; ++q) {
+            ae[q] = deq2<CT, 0, 2>(vb[q]);
+            ao[q] = deq2<CT, 1, 3>(vb[q]);
+          }
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            hmma16816(o[2 * g32][n], ae, pb[n][0], pb[n][1]);
+            hmma16816(o[2 * g32 + 1][n], ao, pb[n][0], pb[n][1]);
           }
         }
-      } else
+      } else {
 #pragma unroll
-      for (int nd = 0; nd < D / 16; ++nd) {
-        const int key = warp * 16 + (mi & 1) * 8 + ri;
-        const int d = nd * 16 + (mi >> 1) * 8;
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, d >> 6, (d & 63) >> 3, log_r)), b0, b1, b2, b3);
-        hmma16816(o[2 * nd], pa, b0, b1);
-        hmma16816(o[2 * nd + 1], pa, b2, b3);
+        for (int nd = 0; nd < kKS; ++nd) {
+          // matrix mi = keys (mi>>1)*8.., channels 16nd + (mi&1)*8, transposed:
+          // the A fragment of V^T (channels fg, fg + 8; keys 2ft.., 8 + 2ft..)
+          const int key = warp * 16 + (mi >> 1) * 8 + ri;
+          const int d = nd * 16 + (mi & 1) * 8;
+          uint32_t a[4];
+          ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, d >> 6, (d & 63) >> 3, log_r)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+          for (int n = 0; n < NT; ++n) hmma16816(o[nd][n], a, pb[n][0], pb[n][1]);
+        }
       }
     }
 
@@ -557,34 +607,34 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
       if (lane == 0) mbar_arrive(&empty[stage]);
     } else {
       // ---- end of item: merge the four warps through this stage's buffer
-      float lt[2] = {l[0], l[1]};
+      float lt[NT][2];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], 1);
-        lt[i] += __shfl_xor_sync(0xffffffffu, lt[i], 2);
-      }
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          float v = l[n][j];
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 8);
+          v += __shfl_xor_sync(0xffffffffu, v, 16);
+          lt[n][j] = v;
+        }
       named_bar(1, kDecodeWarps * 32);  // every warp is done reading the stage
       float* mrg = reinterpret_cast<float*>(C::kOwnMerge ? merge : kt);
       float* mw = mrg + warp * 16 * D;
-      if constexpr (kQ8) {
 #pragma unroll
-        for (int i = 0; i < D / 8; i += 2) {
-          // o[i] even channels, o[i+1] odd ones: four consecutive channels
-          const int d = (i >> 2) * 32 + ((i >> 1) & 1) * 16 + 2 * cq;
-          *reinterpret_cast<float4*>(mw + r0 * D + d) = make_float4(o[i][0], o[i + 1][0], o[i][1], o[i + 1][1]);
-          *reinterpret_cast<float4*>(mw + r1 * D + d) = make_float4(o[i][2], o[i + 1][2], o[i][3], o[i + 1][3]);
-        }
-      } else {
+      for (int kk = 0; kk < kKS; ++kk)
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          const int d = i * 8 + cq;
-          *reinterpret_cast<float2*>(mw + r0 * D + d) = make_float2(o[i][0], o[i][1]);
-          *reinterpret_cast<float2*>(mw + r1 * D + d) = make_float2(o[i][2], o[i][3]);
-        }
-      }
-      if ((lane & 3) == 0) {
-        mls[warp * 16 + r0] = make_float2(m[0], lt[0]);
-        mls[warp * 16 + r1] = make_float2(m[1], lt[1]);
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = 8 * n + 2 * ft + (e & 1);
+            mw[row * D + o_channel<kQ8>(kk, e, fg)] = o[kk][n][e];
+          }
+      if (fg == 0) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) mls[warp * 16 + 8 * n + 2 * ft + j] = make_float2(m[n][j], lt[n][j]);
       }
       named_bar(1, kDecodeWarps * 32);
       for (int e = ctid; e < tg.R * D; e += kDecodeWarps * 32) {
@@ -627,40 +677,55 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
   }
 }
 
-template <int D, int CT>
+template <int D, int CT, int NT>
 __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
-  decode_body<D, CT>(tm_k, tm_v, tm_q, p);
+  decode_body<D, CT, NT>(tm_k, tm_v, tm_q, p);
   // Beside the prefill kernel (launched after it): this grid may complete
   // only once the prefill grid has, so the combine kernel, which waits for
   // this grid, ends the step after both.  One thread of CTA 0 suffices.
   if (!p.wait_prologue && blockIdx.x == 0 && threadIdx.x == 0) griddep_wait();
 }
 
+template <int D, int CT, int NT>
+cudaError_t configure_nt(size_t* smem, int* ctas) {
+  using C = DecodeCfg<D, CT>;
+  *smem = C::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, CT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<D, CT, NT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, CT, NT>, kThreads, *smem);
+  *ctas = n > 0 ? n : 1;
+  return e;
+}
+
+// Both row-tile variants; the CTAs per SM of the grid are the smaller count.
 template <int D, int CT>
 cudaError_t configure_d(size_t* smem, int* ctas) {
   using C = DecodeCfg<D, CT>;
   static_assert(C::kOwnMerge >= C::kMergeBytes || C::kStageBytes >= C::kMergeBytes, "merge buffer");
   static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
   static_assert(C::kCtasPerSm == 1 || 2 * C::kSmemBytes <= 228 * 1024 - 2 * 1024, "two CTAs per SM");
-  *smem = C::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, CT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)C::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<D, CT>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           (int)cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<D, CT>, kThreads, *smem);
-  *ctas = n > 0 ? n : 1;
+  int c1 = 1, c2 = 1;
+  cudaError_t e = configure_nt<D, CT, 1>(smem, &c1);
+  if (e == cudaSuccess) e = configure_nt<D, CT, 2>(smem, &c2);
+  *ctas = std::min(c1, c2);
   return e;
 }
 
+// One row tile (8 query rows per item) when the GQA group has at most 8
+// heads, two (16 rows) otherwise.
 template <int D, int CT>
 cudaError_t launch_dc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const DecodeParams& p,
                       int grid, cudaStream_t s) {
-  return launch_pdl(decode_kernel<D, CT>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
+  if (p.G <= 8)
+    return launch_pdl(decode_kernel<D, CT, 1>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
+  return launch_pdl(decode_kernel<D, CT, 2>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
 }
 
 }  // namespace

@@ -14,7 +14,11 @@
 namespace pa {
 
 constexpr int kStageKeys = 64;      // keys per decode pipeline stage
-constexpr int kDecodeRows = 16;     // query rows (token x group head) per decode item
+constexpr int kDecodeRows = 16;     // most query rows (token x group head) per decode item
+// Query rows a decode item serves for a GQA group of G heads: the decode
+// kernel's row tiles hold 8 rows, and it runs one tile when G <= 8, two
+// otherwise (G <= 16); larger groups have no decode item (0).
+__host__ __device__ inline int decode_item_rows(int G) { return G <= 8 ? 8 : (G <= kDecodeRows ? kDecodeRows : 0); }
 constexpr int kDecodeWarps = 4;     // consumer warps of the decode kernel
 // Decode work items per decode CTA the automatic split size aims for: 2
 // measured best on the Llama-3-8B- and Llama-70B-shaped decode steps (fewer

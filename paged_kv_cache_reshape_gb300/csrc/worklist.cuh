@@ -22,9 +22,11 @@ struct Int3 {
                       // split decode entries
 };
 
-// Exclusive scan of the five counters across the block; returns the prefix and
+// Exclusive scan of the five counters across the block (out of line: one
+// copy of its code serves every call, which keeps the cold instruction
+// fetches of the builder few); returns the prefix and
 // writes the block totals to *tot.  All threads must call it.
-__device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
+__device__ __noinline__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
   __shared__ Int3 warp_sums[32];
   __shared__ Int3 total;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -76,7 +78,7 @@ __device__ Int3 block_exclusive_scan3(Int3 v, Int3* tot) {
   return out;
 }
 
-__device__ long long block_sum_ll(long long v) {
+__device__ __noinline__ long long block_sum_ll(long long v) {
   __shared__ long long sums[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -374,12 +376,9 @@ __device__ void build_small(const WorklistParams& p) {
   if (err_bits) atomicOr(p.err, err_bits);
 }
 
-// Body of the builder; must be executed by all kThreads threads of one CTA.
-__device__ void build(const WorklistParams& p) {
-  if (p.batch <= kThreads) {
-    build_small(p);
-    return;
-  }
+// Batches of more than one CTA's width (kept out of line: its code is not
+// fetched on the small-batch path).
+__device__ __noinline__ void build_large(const WorklistParams& p) {
   int err_bits = 0;
   // Pass 1: total decode span, which sets the keys per split.
   long long span = 0, pairs = 0;
@@ -449,6 +448,12 @@ __device__ void build(const WorklistParams& p) {
   }
   if (threadIdx.x == 0) write_counters(p, overflow, carry, split_keys, dec_keys, pre_pairs, &err_bits);
   if (err_bits) atomicOr(p.err, err_bits);
+}
+
+// Body of the builder; must be executed by all kThreads threads of one CTA.
+__device__ void build(const WorklistParams& p) {
+  if (p.batch <= kThreads) build_small(p);
+  else build_large(p);
 }
 
 }  // namespace worklist
