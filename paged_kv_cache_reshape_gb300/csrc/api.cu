@@ -513,7 +513,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
     if (e == cudaSuccess && h->mla_tc_ready) e = pa::mla_tc_configure(&tc_smem);
     h->dec_ctas_per_sm = 1;
   } else {
-    e = pa::decode_configure(c.head_size, c.cache_dtype, &h->dec_ctas_per_sm, &h->dec_smem);
+    e = pa::decode_configure(c.head_size, c.cache_dtype, h->G, &h->dec_ctas_per_sm, &h->dec_smem);
   }
   if (e != cudaSuccess) { delete h; return cuda_fail(nullptr, e, "decode kernel attributes"); }
   size_t psmem = 0;
@@ -1153,7 +1153,7 @@ struct NoAllocDevice {
   bool ready = false;                // set-up done (a failed set-up is retried on the next call)
   unsigned char* scratch = nullptr;  // device address of g_no_alloc_scratch
   int num_sms = 0;
-  int dec_ctas[3] = {1, 1, 1};  // decode CTAs per SM for head_size 64, 128, 256
+  int dec_ctas[3][2] = {{1, 1}, {1, 1}, {1, 1}};  // decode CTAs per SM: head_size 64, 128, 256 x G <= 8, G <= 16
   bool prefill_ok = false;
 };
 NoAllocDevice g_no_alloc_dev[kMaxDevices];
@@ -1180,7 +1180,8 @@ cudaError_t no_alloc_setup(int dev, NoAllocDevice** out, const char** what) {
   if (e != cudaSuccess) { *what = "cudaDeviceGetAttribute"; return e; }
   size_t smem = 0;
   for (int D : {64, 128, 256}) {
-    e = pa::decode_configure(D, PA_CACHE_FP16, &n.dec_ctas[head_index(D)], &smem);
+    for (int t = 0; t < 2 && e == cudaSuccess; ++t)
+      e = pa::decode_configure(D, PA_CACHE_FP16, t ? 16 : 8, &n.dec_ctas[head_index(D)][t], &smem);
     if (e != cudaSuccess) { *what = "decode kernel attributes"; return e; }
   }
   n.prefill_ok = pa::prefill_configure(64, &smem) == cudaSuccess &&
@@ -1235,7 +1236,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   if (pre_launch && !nd->prefill_ok)
     return fail(nullptr, PA_NOT_SUPPORTED,
                 "the query-length bound routes rows to the prefill kernel, which is not available on this device");
-  const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)];
+  const int dec_grid = nd->num_sms * nd->dec_ctas[head_index(D)][G <= 8 ? 0 : 1];
   const int target_pairs = std::max(1, (pa::kDecodeItemsPerCta * dec_grid + Hk - 1) / Hk);
   const int cap_dseq = c.max_batch;  // one decode entry per sequence (no chunks: fp16 caches have the prefill kernel)
   const int cap_dec = target_pairs + cap_dseq;

@@ -58,7 +58,7 @@ constexpr int kThreads = (kDecodeWarps + 1) * 32;  // 4 consumer warps + 1 produ
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated before rescaling
 
-template <int D, int CT>
+template <int D, int CT, int NT>
 struct DecodeCfg {
   static constexpr int kEb = CT == kCacheF16 ? 2 : 1;      // bytes per cache element
   static constexpr int kChunks = D * kEb / 128;             // 128-byte chunks per K/V row
@@ -67,11 +67,13 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
   static constexpr int kStages = CT == kCacheF16 ? ((D == 256) ? 3 : (D == 128 ? 3 : 6)) : 4;
   static constexpr int kQBytes = kQChunks * 2048;           // 16 rows x 128 B per chunk
-  static constexpr int kCtasPerSm = (D == 256) ? 1 : 2;
-  // End-of-item merge: the four warps' 16 x D fp32 partial outputs.  An
-  // fp16 stage holds exactly that much and is reused; an 8-bit stage is half
-  // the size, so 8-bit caches get their own region.
-  static constexpr int kMergeBytes = kDecodeWarps * 16 * D * 4;
+  // End-of-item merge: the four warps' 8 * NT x D fp32 partial outputs, in
+  // the last stage's buffer when it is large enough, else in a region of
+  // their own.
+  static constexpr int kMergeBytes = kDecodeWarps * 8 * NT * D * 4;
+  // 8-bit pools with one row tile fit three CTAs on an SM (the merge reuses
+  // a stage buffer and the registers stay within a third of the file).
+  static constexpr int kCtasPerSm = (D == 256) ? 1 : ((CT != kCacheF16 && NT == 1) ? 3 : 2);
   static constexpr int kOwnMerge = kMergeBytes > kStageBytes ? kMergeBytes : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOwnMerge + 2 * kQBytes + 4 * 16 * 8 +
                                     kStages * 64 + (2 * kStages + 4) * 8;
@@ -147,7 +149,7 @@ __device__ __forceinline__ int o_channel(int kk, int e, int fg) {
 template <int D, int CT, int NT>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                                             const DecodeParams& p) {
-  using C = DecodeCfg<D, CT>;
+  using C = DecodeCfg<D, CT, NT>;
   constexpr bool kQ8 = CT != kCacheF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -620,7 +622,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         }
       named_bar(1, kDecodeWarps * 32);  // every warp is done reading the stage
       float* mrg = reinterpret_cast<float*>(C::kOwnMerge ? merge : kt);
-      float* mw = mrg + warp * 16 * D;
+      constexpr int kRows = 8 * NT;  // rows of a warp's partial output in the merge buffer
+      float* mw = mrg + warp * kRows * D;
 #pragma unroll
       for (int kk = 0; kk < kKS; ++kk)
 #pragma unroll
@@ -637,7 +640,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           for (int j = 0; j < 2; ++j) mls[warp * 16 + 8 * n + 2 * ft + j] = make_float2(m[n][j], lt[n][j]);
       }
       named_bar(1, kDecodeWarps * 32);
-      for (int e = ctid; e < tg.R * D; e += kDecodeWarps * 32) {
+      // (the routing keeps R <= kRows; the bound keeps every access inside
+      // the merge buffer regardless)
+      for (int e = ctid; e < min(tg.R, kRows) * D; e += kDecodeWarps * 32) {
         const int r = e / D, d = e - r * D;
         float M = -INFINITY;
 #pragma unroll
@@ -649,7 +654,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
             const float2 ml = mls[w * 16 + r];
             const float f = exp2f(ml.x - M);
             den += f * ml.y;
-            acc += f * mrg[(w * 16 + r) * D + d];
+            acc += f * mrg[(w * kRows + r) * D + d];
           }
         }
         if constexpr (kQ8) acc *= __ldg(p.v_scale + (p.per_channel ? tg.k * D + d : 0));
@@ -678,7 +683,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
 }
 
 template <int D, int CT, int NT>
-__global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT, NT>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_q, const DecodeParams p) {
   decode_body<D, CT, NT>(tm_k, tm_v, tm_q, p);
@@ -690,7 +695,10 @@ __global__ void __launch_bounds__(kThreads, DecodeCfg<D, CT>::kCtasPerSm)
 
 template <int D, int CT, int NT>
 cudaError_t configure_nt(size_t* smem, int* ctas) {
-  using C = DecodeCfg<D, CT>;
+  using C = DecodeCfg<D, CT, NT>;
+  static_assert(C::kOwnMerge >= C::kMergeBytes || C::kStageBytes >= C::kMergeBytes, "merge buffer");
+  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(C::kCtasPerSm * (C::kSmemBytes + 1024) <= 228 * 1024, "CTAs per SM");
   *smem = C::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, CT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)C::kSmemBytes);
@@ -704,18 +712,10 @@ cudaError_t configure_nt(size_t* smem, int* ctas) {
   return e;
 }
 
-// Both row-tile variants; the CTAs per SM of the grid are the smaller count.
+// The row-tile variant a GQA group of G heads runs (one tile when G <= 8).
 template <int D, int CT>
-cudaError_t configure_d(size_t* smem, int* ctas) {
-  using C = DecodeCfg<D, CT>;
-  static_assert(C::kOwnMerge >= C::kMergeBytes || C::kStageBytes >= C::kMergeBytes, "merge buffer");
-  static_assert(C::kSmemBytes <= 227 * 1024, "shared memory");
-  static_assert(C::kCtasPerSm == 1 || 2 * C::kSmemBytes <= 228 * 1024 - 2 * 1024, "two CTAs per SM");
-  int c1 = 1, c2 = 1;
-  cudaError_t e = configure_nt<D, CT, 1>(smem, &c1);
-  if (e == cudaSuccess) e = configure_nt<D, CT, 2>(smem, &c2);
-  *ctas = std::min(c1, c2);
-  return e;
+cudaError_t configure_d(int G, size_t* smem, int* ctas) {
+  return G <= 8 ? configure_nt<D, CT, 1>(smem, ctas) : configure_nt<D, CT, 2>(smem, ctas);
 }
 
 // One row tile (8 query rows per item) when the GQA group has at most 8
@@ -724,26 +724,26 @@ template <int D, int CT>
 cudaError_t launch_dc(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq, const DecodeParams& p,
                       int grid, cudaStream_t s) {
   if (p.G <= 8)
-    return launch_pdl(decode_kernel<D, CT, 1>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
-  return launch_pdl(decode_kernel<D, CT, 2>, grid, kThreads, DecodeCfg<D, CT>::kSmemBytes, s, tk, tv, tq, p);
+    return launch_pdl(decode_kernel<D, CT, 1>, grid, kThreads, DecodeCfg<D, CT, 1>::kSmemBytes, s, tk, tv, tq, p);
+  return launch_pdl(decode_kernel<D, CT, 2>, grid, kThreads, DecodeCfg<D, CT, 2>::kSmemBytes, s, tk, tv, tq, p);
 }
 
 }  // namespace
 
 // 8-bit caches are built for head_size 128 and 256.
-cudaError_t decode_configure(int head_size, int cache_type, int* ctas_per_sm, size_t* smem) {
+cudaError_t decode_configure(int head_size, int cache_type, int group, int* ctas_per_sm, size_t* smem) {
   if (cache_type == kCacheF16) {
     switch (head_size) {
-      case 64: return configure_d<64, kCacheF16>(smem, ctas_per_sm);
-      case 128: return configure_d<128, kCacheF16>(smem, ctas_per_sm);
-      case 256: return configure_d<256, kCacheF16>(smem, ctas_per_sm);
+      case 64: return configure_d<64, kCacheF16>(group, smem, ctas_per_sm);
+      case 128: return configure_d<128, kCacheF16>(group, smem, ctas_per_sm);
+      case 256: return configure_d<256, kCacheF16>(group, smem, ctas_per_sm);
       default: return cudaErrorInvalidValue;
     }
   }
   const bool i8 = cache_type == kCacheI8;
   switch (head_size) {
-    case 128: return i8 ? configure_d<128, kCacheI8>(smem, ctas_per_sm) : configure_d<128, kCacheE4M3>(smem, ctas_per_sm);
-    case 256: return i8 ? configure_d<256, kCacheI8>(smem, ctas_per_sm) : configure_d<256, kCacheE4M3>(smem, ctas_per_sm);
+    case 128: return i8 ? configure_d<128, kCacheI8>(group, smem, ctas_per_sm) : configure_d<128, kCacheE4M3>(group, smem, ctas_per_sm);
+    case 256: return i8 ? configure_d<256, kCacheI8>(group, smem, ctas_per_sm) : configure_d<256, kCacheE4M3>(group, smem, ctas_per_sm);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -269,7 +269,9 @@ cudaError_t launch_cache_write(const CacheWriteParams& p, cudaStream_t s);
 // The prologue spreads its (token, part) warps over up to num_sms - 1 blocks
 // (a block holds a whole SM: its builder CTA needs every register).
 cudaError_t launch_prologue(const WorklistParams& wp, const CacheWriteParams& cp, int num_sms, cudaStream_t s);
-cudaError_t decode_configure(int head_size, int cache_type, int* ctas_per_sm, size_t* smem);
+// CTAs per SM and shared memory of the decode kernel a GQA group of `group`
+// heads runs (its row tiles follow the group).
+cudaError_t decode_configure(int head_size, int cache_type, int group, int* ctas_per_sm, size_t* smem);
 cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tq, const DecodeParams& p, int grid, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s);
