@@ -795,7 +795,11 @@ pa::CacheWriteParams cache_write_params(const pa_config& c, __half* q_ws, int* e
   // Spread a token over several warps when Q is rotated too: one for the
   // K/V rows and one per kv_num_heads query heads (same size as a K row).
   p.q_heads_per_part = c.kv_num_heads;
-  p.parts = 1 + (p.q_rot ? (c.num_heads + p.q_heads_per_part - 1) / p.q_heads_per_part : 0);
+  // 8-bit caches divide every element by its scale: their K and V rows go
+  // to separate warps, each for up to half the kv heads
+  p.kv_heads_per_part = quant ? std::max(1, (c.kv_num_heads + 1) / 2) : c.kv_num_heads;
+  p.kv_parts = quant ? 2 * ((c.kv_num_heads + p.kv_heads_per_part - 1) / p.kv_heads_per_part) : 1;
+  p.parts = p.kv_parts + (p.q_rot ? (c.num_heads + p.q_heads_per_part - 1) / p.q_heads_per_part : 0);
   p.err = err;
   return p;
 }

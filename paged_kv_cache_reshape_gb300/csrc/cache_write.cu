@@ -252,8 +252,8 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   const __half* cos_row = rotate ? p.cos_cache + (size_t)pos * half : nullptr;
   const __half* sin_row = rotate ? p.sin_cache + (size_t)pos * half : nullptr;
 
-  if (part > 0) {
-    const int h0 = (part - 1) * p.q_heads_per_part;
+  if (part >= p.kv_parts) {
+    const int h0 = (part - p.kv_parts) * p.q_heads_per_part;
     const int nh = min(p.q_heads_per_part, p.H - h0);
     const __half* qsrc = p.query + (size_t)t * p.q_stride + (size_t)h0 * p.D;
     const size_t qoff = ((size_t)t * p.H + h0) * p.D;
@@ -300,6 +300,31 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   const __half* ksrc = p.packed ? p.query + (size_t)t * p.q_stride + (size_t)p.H * p.D : p.key + (size_t)t * kv_row;
   const __half* vsrc =
       p.packed ? p.query + (size_t)t * p.q_stride + (size_t)(p.H + p.Hk) * p.D : p.value + (size_t)t * kv_row;
+  if (p.kv_parts > 1) {
+    // 8-bit caches: part 2i quantizes K heads [i*hp, (i+1)*hp), part 2i+1
+    // the same V heads (the per-element division spread over more warps)
+    const int hp = p.kv_heads_per_part, h0 = (part >> 1) * hp, nh = min(hp, p.Hk - h0);
+    if (nh <= 0) return;
+    const size_t doff = slot * kv_row + (size_t)h0 * p.D;
+    if ((part & 1) == 0) {
+      const float* krn = nullptr;
+      if (p.qk_norm) {
+        norm_factors(ksrc + (size_t)h0 * p.D, nh, p.D, p.qk_eps, rn, lane);
+        krn = rn;
+      }
+      row_transform(ksrc + (size_t)h0 * p.D,
+                    EmitCode{static_cast<uint8_t*>(p.key_cache) + doff, p.D, p.cache_type, p.per_channel, h0,
+                             p.k_scale},
+                    nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
+                    p.rot_offset);
+    } else {
+      row_transform(vsrc + (size_t)h0 * p.D,
+                    EmitCode{static_cast<uint8_t*>(p.value_cache) + doff, p.D, p.cache_type, p.per_channel, h0,
+                             p.v_scale},
+                    nh, p.D, false, 0, 0, nullptr, nullptr, lane);
+    }
+    return;
+  }
   const float* krn = nullptr;
   if (p.qk_norm) {
     norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane);

@@ -147,7 +147,10 @@ struct CacheWriteParams {
                              // the 64-channel chunks holding them; the kernels read the rest from
                              // the query itself)
   int q_scale;           // 1: the query copy is multiplied by k_scale (8-bit caches)
-  int parts;             // warps per token: 1 (K/V) + query parts when Q is transformed
+  int parts;             // warps per token: K/V parts + query parts when Q is transformed
+  int kv_parts;          // warps per token for the K and V rows: 1 (both rows), or K and V warps per
+                         // kv_heads_per_part heads (8-bit caches)
+  int kv_heads_per_part;
   int q_heads_per_part;  // query heads per query part
   int* err;
 };
