@@ -986,7 +986,11 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
         (q_split && !encode_map(&tqr, q_att, D, c.num_heads, token_count, q_rows, qt)))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the query");
     if (!q_split) tqr = tq;
-    if (h->mla_tc && !encode_map(&tl, key_cache, D, 1, pool_rows, 1, tile_rows))
+    // 32-row pages: one 4-D box per tile holds all nine channel chunks
+    // ([chunk][key][128 B], the ring slot's layout); smaller pages: one
+    // 3-D box per (page, chunk)
+    if (h->mla_tc && !(tile_rows == 32 ? encode_pool_map(&tl, key_cache, D, 1, pool_rows, tile_rows)
+                                       : encode_map(&tl, key_cache, D, 1, pool_rows, 1, tile_rows)))
       return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the latent pool");
     pa::MlaParams p{};
     p.out = static_cast<__half*>(output);

@@ -22,8 +22,8 @@
 // TMEM (512 columns): Q channels 0..383 as fp16 pairs [0, 192), S/P of even
 // and odd tiles [192, 224) and [224, 256), O [256, 512).  Shared memory: Q
 // channels 384..575 (48 KB) and a 4-deep ring of 32-key latent tiles (36 KB
-// each, [chunk][key][128 B], 128-byte swizzle, one TMA box per page and
-// chunk).  At a unit's start, once the previous unit's tiles are consumed,
+// each, [chunk][key][128 B], 128-byte swizzle; one 4-D TMA box per tile
+// with pages of 32 rows or more, else one box per page and chunk).  At a unit's start, once the previous unit's tiles are consumed,
 // Q's TMEM part is staged through the first three ring slots and copied
 // into TMEM (tcgen05.cp, in issue order before the unit's first S), then
 // the ring refills from slot 0.  MMAs issued by one thread complete in
@@ -255,14 +255,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         sp ^= 1u << st;
         used |= 1u << st;
-        // one box {64, 1, 2^log_r} per (page, chunk); lane -> (page, chunk)
-        for (int base = 0; base < pages * kChunks; base += 32) {
-          const int bx = base + lane;
-          const int lp = min(bx / kChunks, 31), lc = bx % kChunks;
-          const int prc = __shfl_sync(0xffffffffu, rc, lp);
-          if (bx < pages * kChunks)
-            tma_load_3d(kv_s + st * kTileBytes + lc * (kKeys * 128) + ((uint32_t)lp << (log_r + 7)), &tm_l,
-                        lc * 64, 0, prc, &ctl->kv_full[st]);
+        if (log_r == 5) {
+          // one page of 32 keys: one box {64, 32, 9, 1} of the 4-D view
+          if (lane == 0) tma_load_4d(kv_s + st * kTileBytes, &tm_l, 0, rc, 0, 0, &ctl->kv_full[st]);
+        } else {
+          // one box {64, 1, 2^log_r} per (page, chunk); lane -> (page, chunk)
+          for (int base = 0; base < pages * kChunks; base += 32) {
+            const int bx = base + lane;
+            const int lp = min(bx / kChunks, 31), lc = bx % kChunks;
+            const int prc = __shfl_sync(0xffffffffu, rc, lp);
+            if (bx < pages * kChunks)
+              tma_load_3d(kv_s + st * kTileBytes + lc * (kKeys * 128) + ((uint32_t)lp << (log_r + 7)), &tm_l,
+                          lc * 64, 0, prc, &ctl->kv_full[st]);
+          }
         }
       }
       // The next unit's Q overwrites the staging slots: a one-tile unit has
