@@ -113,6 +113,7 @@ struct pa_handle_s {
   size_t dec_smem = 0;
   int cap_dec = 1, cap_pre = 1, cap_comb = 1, cap_dseq = 1, cap_part = 1;
   int chunk_tokens = 0;  // > 0: query rows beyond one decode item run as decode entries of this many tokens
+  int chunk_rows_max = 0;  // > 0: ... for sequences of at most this many rows (fp16 caches: the others prefill)
   int dec_rows = 16;      // query rows a decode item holds (decode_item_rows of the group)
   int prefill_tile_tokens = 1, prefill_q_tokens = 1, pre_grid = 1, comb_grid = 1;
   size_t pre_smem = 0;
@@ -528,13 +529,21 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   const int tc_units = h->mla_tc_ready ? 2 * (c.num_heads / 128) : 1;
   h->mla_tc = h->mla_tc_ready;
   h->unit_groups = h->mla_tc ? tc_units : h->latent ? pa::mla_item_groups(h->groups) : h->groups;
-  // Query rows beyond one decode item: the prefill kernel for fp16 caches
-  // with separate K and V, decode entries of dec_rows / G tokens for
-  // 8-bit caches and the latent layout (one token: G is 16 there).
+  // Query rows beyond one decode item: decode entries of dec_rows / G
+  // tokens for 8-bit caches and the latent layout (one token: G is 16
+  // there); with fp16 caches only for short multi-token sequences (two
+  // chunks at most: each chunk reads the sequence's keys again, and the
+  // prefill kernel's fixed cost is not repaid by a few rows), longer ones
+  // take the prefill kernel.
   const bool quant = c.cache_dtype != PA_CACHE_FP16;
-  h->chunk_tokens = (h->latent || quant) ? std::max(1, h->dec_rows / h->G) : 0;
-  // Decode entries: one per sequence, or one per chunk.
-  h->cap_dseq = c.max_batch + (h->chunk_tokens ? (c.max_tokens + h->chunk_tokens - 1) / h->chunk_tokens : 0);
+  h->chunk_tokens = h->dec_rows > 0 ? std::max(1, h->dec_rows / h->G) : 0;
+  h->chunk_rows_max = (h->latent || quant) ? 0 : 2 * h->chunk_tokens * h->G;
+  // Decode entries: one per sequence, or one per chunk (with fp16 caches a
+  // chunked sequence has more than chunk_tokens tokens and two entries).
+  if (h->chunk_rows_max > 0)
+    h->cap_dseq = c.max_batch + std::min(c.max_batch, c.max_tokens / (h->chunk_tokens + 1));
+  else
+    h->cap_dseq = c.max_batch + (h->chunk_tokens ? (c.max_tokens + h->chunk_tokens - 1) / h->chunk_tokens : 0);
   // Decode items: the split targets (room for the items-per-CTA option's
   // maximum, sized for whichever latent kernel makes the most items) plus
   // one last split per entry.  Split partials: with automatic split sizes
@@ -909,10 +918,13 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     return fail(h, PA_CUDA_ERROR, "cuTensorMapEncodeTiled failed for the K/V pool");
 
   // The prefill kernel launches unless the query-length bound already routes
-  // every sequence to the decode kernel (always so for 8-bit caches).  When
+  // every sequence to the decode kernel (always so for 8-bit caches; with
+  // fp16 caches, up to chunk_rows_max rows while the chunking is on).  When
   // it does, it goes first and the decode kernel runs beside it on the SMs
   // the work list leaves it.
-  const bool needs_prefill = !h->latent && !quant && (long long)h->max_q * h->G > h->opt_dec_rows;
+  const bool fp16_chunks = h->chunk_rows_max > 0 && h->opt_dec_rows == h->dec_rows;
+  const int decode_rows_max = fp16_chunks ? std::max(h->opt_dec_rows, h->chunk_rows_max) : h->opt_dec_rows;
+  const bool needs_prefill = !h->latent && !quant && (long long)h->max_q * h->G > decode_rows_max;
   if (needs_prefill && !h->prefill_ready)
     return fail(h, PA_NOT_SUPPORTED,
                 "the query-length bound routes rows to the prefill kernel, which is not available on this device");
@@ -949,7 +961,10 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     // balance gains (measured on the DeepSeek-V3-shaped step: automatic
     // ~1984 keys 109 us, 2048 97 us, no split 136 us).
     p.min_split_keys = h->mla_tc ? 2048 : pa::kStageKeys;
-    p.chunk_tokens = h->chunk_tokens;
+    // (a lowered decode row limit, an option that sends rows to the prefill
+    // kernel, turns the fp16 chunking off)
+    p.chunk_tokens = (h->chunk_rows_max == 0 || fp16_chunks) ? h->chunk_tokens : 0;
+    p.chunk_rows_max = h->chunk_rows_max;
     p.cap_dec = h->cap_dec;
     p.cap_pre = h->cap_pre;
     p.cap_comb = h->cap_comb;
@@ -1314,6 +1329,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   wp.target_pairs = target_pairs;
   wp.min_split_keys = pa::kStageKeys;
   wp.chunk_tokens = 0;
+  wp.chunk_rows_max = 0;
   wp.cap_dec = cap_dec;
   wp.cap_pre = cap_pre;
   wp.cap_comb = cap_comb;

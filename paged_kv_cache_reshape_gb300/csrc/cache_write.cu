@@ -82,6 +82,10 @@ __device__ __forceinline__ uint32_t code8(__half x, float s, int type) {
   return c & 0xffu;
 }
 
+// (The scales are read with ordinary loads: with the read-only-cache form
+// inside this inlined emitter, one build of the prologue faulted on the
+// rotated 8-bit K rows with cudaErrorInvalidAddressSpace, reproducibly, while
+// the same loads as plain loads or from an out-of-line emitter ran clean.)
 struct EmitCode {  // 8-bit codes; scale[0] or scale[(head0 + h) * D + c]
   uint8_t* dst;
   int D, type, per_channel, head0;
@@ -90,7 +94,7 @@ struct EmitCode {  // 8-bit codes; scale[0] or scale[(head0 + h) * D + c]
     const float* sc = scale + (per_channel ? (size_t)(head0 + h) * D + ch : 0);
     uint32_t w[2] = {0, 0};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) w[e >> 2] |= code8(v.h[e], __ldg(sc + (per_channel ? e : 0)), type) << (8 * (e & 3));
+    for (int e = 0; e < 8; ++e) w[e >> 2] |= code8(v.h[e], sc[per_channel ? e : 0], type) << (8 * (e & 3));
     *reinterpret_cast<uint2*>(dst + (size_t)h * D + ch) = make_uint2(w[0], w[1]);
   }
 };
@@ -103,7 +107,7 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
     const float* sc = scale + (per_channel ? (size_t)((head0 + h) / G) * D + ch : 0);
     Vec8 y;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(__fmul_rn(__half2float(v.h[e]), __ldg(sc + (per_channel ? e : 0))));
+    for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(__fmul_rn(__half2float(v.h[e]), sc[per_channel ? e : 0]));
     *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = y.u;
   }
 };

@@ -89,6 +89,8 @@ struct WorklistParams {
   int chunk_tokens;        // > 0: a sequence with q_len * G > dec_max_rows goes to the decode kernel
                            // in chunks of this many tokens (chunk_tokens * G <= dec_max_rows);
                            // 0: it goes to the prefill kernel
+  int chunk_rows_max;      // > 0: only sequences of at most this many rows (q_len * G) are chunked,
+                           // longer ones go to the prefill kernel; 0: every one (no prefill kernel)
   int cap_dec, cap_pre, cap_comb, cap_dseq;
   int cap_part;            // split-partial slots (one per split of a split decode entry)
   // SM split between the prefill and decode kernels.  With split_sms > 0

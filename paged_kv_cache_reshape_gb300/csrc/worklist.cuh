@@ -104,8 +104,10 @@ struct Lens {
 };
 
 __device__ int route_of(const WorklistParams& p, int q) {
-  if ((long long)q * p.group <= p.dec_max_rows) return kRouteDecode;
-  return p.chunk_tokens > 0 ? kRouteChunked : kRoutePrefill;
+  const long long rows = (long long)q * p.group;
+  if (rows <= p.dec_max_rows) return kRouteDecode;
+  if (p.chunk_tokens > 0 && (p.chunk_rows_max <= 0 || rows <= p.chunk_rows_max)) return kRouteChunked;
+  return kRoutePrefill;
 }
 
 // First key position a row at `past` (the earliest new token) may attend,

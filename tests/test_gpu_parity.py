@@ -163,6 +163,20 @@ def test_mixed_routing_in_one_step():
     _full(workloads.config_shape(0), options=[(pa.PA_OPT_DECODE_MAX_ROWS, 4)])
 
 
+def test_short_prompts_take_chunked_decode_entries():
+    """Multi-token sequences of at most two decode items' rows run as two
+    decode entries (chunks of 8 / G tokens) instead of a prefill tile: the
+    tiny step's 5-token sequence (10 rows at G = 2) and, at G = 4, prompts
+    of 3 and 4 tokens, while a 5-token prompt (20 rows) takes the prefill
+    kernel."""
+    op, _ = _full(workloads.config_shape(0))
+    counts = op.last_step_counts()
+    assert counts["n_pre"] == 0 and counts["n_dec"] >= 4
+    op, _ = _full(cs("short_prompts_g4", 8, 2, 128, 16, [0, 100, 37, 5], [4, 5, 3, 1], seed=73))
+    counts = op.last_step_counts()
+    assert counts["n_pre"] > 0 and counts["n_dec"] >= 5
+
+
 def test_full_size_mixed_step():
     """The 16 x 1024-token prompts beside 240 decodes, as the benchmark runs
     it (prefill and decode kernels side by side on an SM split): both pools
