@@ -5,8 +5,10 @@ the CPU-baseline leg of bench.py.  The library under test never imports it.
 
 The C file is compiled with gcc (-O2 -ffp-contract=off, so that the fp32
 rotary keeps one rounding per operation) into liboracle.so beside it.
-Arrays cross the boundary as numpy buffers; fp16 tensors travel as their
-uint16 bit patterns.
+Arrays cross the boundary as numpy buffers; fp16 and bfloat16 tensors travel
+as their uint16 bit patterns.  A step whose cache_dtype is CACHE_BF16 has
+bfloat16 activations throughout (query, key, value, both pools, the rotary
+tables and head_sink).
 """
 
 from __future__ import annotations
@@ -28,7 +30,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, BAD_ARGUMENT, BAD_DEVICE_DATA = 0, 1, 2
-CACHE_FP16, CACHE_INT8, CACHE_FP8 = 0, 1, 2
+CACHE_FP16, CACHE_INT8, CACHE_FP8, CACHE_BF16 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -77,6 +79,12 @@ def lib():
             L.oracle_rotary_offset.restype = I
             L.oracle_attention_latent.argtypes = [P, P, P, I, P, P, I, I, I, I, I, I, I, Dd, Dd, I, LL, LL, P]
             L.oracle_attention_latent.restype = I
+            L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_double.restype = Dd
+            L.oracle_double_to_bf16.argtypes = [Dd]
+            L.oracle_double_to_bf16.restype = ctypes.c_uint16
+            L.oracle_rotary_bf16.argtypes = [P, P, I, I, I, P, P, I, P, P, I, I, I, I]
+            L.oracle_rotary_bf16.restype = I
             _lib = L
     return _lib
 
@@ -114,6 +122,16 @@ def double_to_half_bits(x: np.ndarray) -> np.ndarray:
     return f(np.asarray(x, dtype=np.float64))
 
 
+def bf16_bits_to_double(bits: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lib().oracle_bf16_to_double, otypes=[np.float64])
+    return f(np.asarray(bits, dtype=np.uint16))
+
+
+def double_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    f = np.vectorize(lambda v: lib().oracle_double_to_bf16(float(v)), otypes=[np.uint16])
+    return f(np.asarray(x, dtype=np.float64))
+
+
 def e4m3_to_double(codes: np.ndarray) -> np.ndarray:
     f = np.vectorize(lambda c: lib().oracle_e4m3_to_double(int(c)), otypes=[np.float64])
     return f(np.asarray(codes, dtype=np.uint8))
@@ -148,17 +166,18 @@ def split_packed_qkv(query, num_heads, kv_num_heads, head_size):
             np.ascontiguousarray(qa[:, (H + Hk) * D:]))
 
 
-def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved, offset=0):
-    """Rotated copy of x ([T, nheads*D] fp16 bits) at positions past_b + j;
-    the rotated channels are [offset, offset + 2 * cos_cache.shape[1])."""
+def rotary(x, cum, past, cos_cache, sin_cache, nheads, head_size, interleaved, offset=0, bf16=False):
+    """Rotated copy of x ([T, nheads*D] fp16 bits, or bfloat16 bits with
+    bfloat16 tables when bf16) at positions past_b + j; the rotated channels
+    are [offset, offset + 2 * cos_cache.shape[1])."""
     xa = _np(x, np.uint16)
     cum_a, past_a = _np(cum, np.int32), _np(past, np.int32)
     cos_a, sin_a = _np(cos_cache, np.uint16), _np(sin_cache, np.uint16)
     T = xa.shape[0]
     y = np.empty_like(xa)
-    st = lib().oracle_rotary_offset(_p(xa), _p(y), T, nheads, head_size, _p(cum_a), _p(past_a),
-                                    past_a.shape[0], _p(cos_a), _p(sin_a), cos_a.shape[1],
-                                    cos_a.shape[0], interleaved, int(offset))
+    fn = lib().oracle_rotary_bf16 if bf16 else lib().oracle_rotary_offset
+    st = fn(_p(xa), _p(y), T, nheads, head_size, _p(cum_a), _p(past_a), past_a.shape[0], _p(cos_a), _p(sin_a),
+            cos_a.shape[1], cos_a.shape[0], interleaved, int(offset))
     _check(st, "rotary")
     return y
 
@@ -207,7 +226,7 @@ def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
     arrays ([1], or [Hk*D] when per_channel).  slot_mapping ([T] int32, -1 =
     no write) replaces the slot derivation when given."""
     sm = _np(slot_mapping, np.int32) if slot_mapping is not None else None
-    if cache_dtype != CACHE_FP16:
+    if cache_dtype not in (CACHE_FP16, CACHE_BF16):  # a 16-bit write is a copy of the bits
         ka, va = _np(key, np.uint16), _np(value, np.uint16)
         kc = _np(key_cache, np.uint8).copy()
         vc = _np(value_cache, np.uint8).copy()
@@ -243,10 +262,11 @@ def attention(query, key_cache, value_cache, block_table, cum, past, num_heads,
     `rows` is an int array of r = t*H + h and the result is [len(rows), D].
     Row ranges run on `threads` Python threads (the C call releases the GIL).
     8-bit caches are code arrays dequantized with k_scale / v_scale;
+    CACHE_BF16 reads query, both caches and head_sink as bfloat16 bits;
     head_sink ([H] fp16) adds the sink term to every row's denominator.
     """
     qa = _np(query, np.uint16)
-    cdt = np.uint16 if cache_dtype == CACHE_FP16 else np.uint8
+    cdt = np.uint16 if cache_dtype in (CACHE_FP16, CACHE_BF16) else np.uint8
     kc, vc = _np(key_cache, cdt), _np(value_cache, cdt)
     ks = _np(k_scale, np.float32) if k_scale is not None else None
     vs = _np(v_scale, np.float32) if v_scale is not None else None
@@ -320,13 +340,13 @@ def forward(step, threads=None, rows=None):
         eps = step.get("qk_norm_epsilon", 1e-6)
         q = qk_norm(q, H, D, step["q_norm_weight"], eps)
         k = qk_norm(k, Hk, D, step["k_norm_weight"], eps)
+    cdt = step.get("cache_dtype", CACHE_FP16)
     if step["do_rotary"]:
         off = step.get("rotary_offset", 0)  # first rotated channel of a head
         q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D,
-                   step["rotary_interleaved"], off)
+                   step["rotary_interleaved"], off, bf16=cdt == CACHE_BF16)
         k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
-                   step["rotary_interleaved"], off)
-    cdt = step.get("cache_dtype", CACHE_FP16)
+                   step["rotary_interleaved"], off, bf16=cdt == CACHE_BF16)
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)
     kc, vc = cache_write(k, v, step["key_cache"], step["value_cache"],

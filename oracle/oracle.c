@@ -54,6 +54,15 @@
  * precision open (they report host and device rotary differing by one fp16
  * ulp); fixing the op order is the reading this project takes.
  *
+ * bfloat16.  The kernel is registered for fp16 and bfloat16 activations,
+ * each with a cache of its own type or an 8-bit one ("PagedAttention - CUDA
+ * Design Document", section 8.2); this oracle covers bfloat16 with a
+ * bfloat16 cache.  With
+ * bfloat16 every 16-bit input (query, key, value, the pools, the cos/sin
+ * tables, head_sink) is read as bfloat16 (exact in fp64), rotary runs the
+ * same fp32 operation order and rounds each y to bfloat16 to nearest-even,
+ * and the cache write copies the bits.
+ *
  * Layouts (row-major): query [T, H*D]; key, value [T, Hk*D];
  * key_cache, value_cache [NB, bs, Hk, D]; block_table [B, MB];
  * cum [B+1]; past [B]; cos/sin [P, R/2].
@@ -110,6 +119,54 @@ uint16_t oracle_double_to_half(double x) {
   return sign | (uint16_t)((ee + 15) << 10) | (uint16_t)((int)m - 1024);
 }
 
+/* ---- bfloat16 conversions, written from the format definition ---- */
+
+/* Exact bfloat16 -> double.  1 sign bit, 8 exponent bits (bias 127), 7
+ * fraction bits: the upper half of an IEEE binary32 word. */
+double oracle_bf16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xff;
+  int f = h & 0x7f;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)f, -133); /* subnormal: fraction * 2^(1 - 127 - 7) */
+  } else if (e == 255) {
+    v = f ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(128 + f), e - 134);
+  }
+  return sign ? -v : v;
+}
+
+/* double -> bfloat16, round to nearest, ties to even (single rounding). */
+uint16_t oracle_double_to_bf16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  if (isnan(x)) return sign | 0x7fc0;
+  double a = fabs(x);
+  /* largest finite 0x7f7f = (2 - 2^-7) * 2^127; halfway to 2^128 rounds up */
+  if (a >= ldexp(2.0 - ldexp(1.0, -8), 127)) return sign | 0x7f80;
+  if (a < ldexp(1.0, -126)) {
+    /* subnormal quantum is 2^-133; scaling by 2^133 is exact */
+    double m = nearbyint(ldexp(a, 133));
+    return sign | (uint16_t)m; /* m == 128 encodes the smallest normal */
+  }
+  int e;
+  (void)frexp(a, &e); /* a = f * 2^e with f in [0.5, 1) */
+  double m = nearbyint(ldexp(a, 8 - e)); /* significand in [128, 256] */
+  int ee = e - 1;
+  if (m == 256.0) {
+    m = 128.0;
+    ee += 1;
+  }
+  if (ee > 127) return sign | 0x7f80;
+  return sign | (uint16_t)((ee + 127) << 7) | (uint16_t)((int)m - 128);
+}
+
+/* A 16-bit element (fp16 or bf16 bits) as a double. */
+static double elem16_to_double(uint16_t v, int bf16) {
+  return bf16 ? oracle_bf16_to_double(v) : oracle_half_to_double(v);
+}
+
 /* ---- float8 e4m3fn, written from the format definition ---- */
 
 /* Exact e4m3fn -> double.  1 sign bit, 4 exponent bits (bias 7), 3 fraction
@@ -159,6 +216,7 @@ uint8_t oracle_float_to_e4m3(float x) {
 #define ORACLE_CACHE_FP16 0
 #define ORACLE_CACHE_INT8 1
 #define ORACLE_CACHE_FP8 2
+#define ORACLE_CACHE_BF16 3 /* 16-bit cache of bfloat16 elements */
 
 /* Code of fp16 value h under scale s (reading stated in the header). */
 uint8_t oracle_quantize(uint16_t h, float s, int cache_dtype) {
@@ -175,6 +233,7 @@ uint8_t oracle_quantize(uint16_t h, float s, int cache_dtype) {
  * double: code * scale for the 8-bit types. */
 static double cache_value(const void* row, int i, int cache_dtype, double scale) {
   if (cache_dtype == ORACLE_CACHE_FP16) return oracle_half_to_double(((const uint16_t*)row)[i]);
+  if (cache_dtype == ORACLE_CACHE_BF16) return oracle_bf16_to_double(((const uint16_t*)row)[i]);
   uint8_t c = ((const uint8_t*)row)[i];
   if (cache_dtype == ORACLE_CACHE_INT8) return (double)(int8_t)c * scale;
   return oracle_e4m3_to_double(c) * scale;
@@ -225,10 +284,31 @@ int oracle_rotary(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
 /* Rotary over channels [offset, offset + 2*half_rot) of every head (CUDA
  * design section 12.5, rotary_offset; the pairs are taken inside that
  * range), every other channel copied. */
+static int rotary_impl(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const int32_t* cum,
+                       const int32_t* past, int B, const uint16_t* cos_cache, const uint16_t* sin_cache,
+                       int half_rot, int max_position, int interleaved, int offset, int bf16);
+
 int oracle_rotary_offset(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
                          const int32_t* cum, const int32_t* past, int B,
                          const uint16_t* cos_cache, const uint16_t* sin_cache,
                          int half_rot, int max_position, int interleaved, int offset) {
+  return rotary_impl(x, y, T, nheads, D, cum, past, B, cos_cache, sin_cache, half_rot, max_position, interleaved,
+                     offset, 0);
+}
+
+/* The same rotation of bfloat16 rows with bfloat16 tables: each y rounded
+ * to bfloat16 to nearest-even. */
+int oracle_rotary_bf16(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
+                       const int32_t* cum, const int32_t* past, int B,
+                       const uint16_t* cos_cache, const uint16_t* sin_cache,
+                       int half_rot, int max_position, int interleaved, int offset) {
+  return rotary_impl(x, y, T, nheads, D, cum, past, B, cos_cache, sin_cache, half_rot, max_position, interleaved,
+                     offset, 1);
+}
+
+static int rotary_impl(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const int32_t* cum,
+                       const int32_t* past, int B, const uint16_t* cos_cache, const uint16_t* sin_cache,
+                       int half_rot, int max_position, int interleaved, int offset, int bf16) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
   if (offset < 0 || offset + 2 * half_rot > D || half_rot < 0) return ORACLE_BAD_ARGUMENT;
@@ -245,18 +325,18 @@ int oracle_rotary_offset(const uint16_t* x, uint16_t* y, int T, int nheads, int 
       for (int i = 0; i < half_rot; ++i) {
         int i1 = offset + (interleaved ? 2 * i : i);
         int i2 = offset + (interleaved ? 2 * i + 1 : i + half_rot);
-        float x1 = (float)oracle_half_to_double(xr[i1]);
-        float x2 = (float)oracle_half_to_double(xr[i2]);
-        float c = (float)oracle_half_to_double(cos_cache[(size_t)pos * half_rot + i]);
-        float s = (float)oracle_half_to_double(sin_cache[(size_t)pos * half_rot + i]);
+        float x1 = (float)elem16_to_double(xr[i1], bf16);
+        float x2 = (float)elem16_to_double(xr[i2], bf16);
+        float c = (float)elem16_to_double(cos_cache[(size_t)pos * half_rot + i], bf16);
+        float s = (float)elem16_to_double(sin_cache[(size_t)pos * half_rot + i], bf16);
         float t1 = x1 * c;
         float t2 = x2 * s;
         float y1 = t1 - t2;
         float t3 = x2 * c;
         float t4 = x1 * s;
         float y2 = t3 + t4;
-        tmp[i1] = oracle_double_to_half((double)y1);
-        tmp[i2] = oracle_double_to_half((double)y2);
+        tmp[i1] = bf16 ? oracle_double_to_bf16((double)y1) : oracle_double_to_half((double)y1);
+        tmp[i2] = bf16 ? oracle_double_to_bf16((double)y2) : oracle_double_to_half((double)y2);
       }
       memcpy(yr, tmp, sizeof(uint16_t) * D);
     }
@@ -395,7 +475,8 @@ int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
  * optionally x_p = softcap * tanh(x_p / softcap); out = sum_p w_p V_p / sum_p w_p
  * with w_p = exp(x_p - max_p x_p); no admitted position gives out = 0.
  * scale == 0 selects 1/sqrt(D). */
-/* General form.  key_cache / value_cache hold fp16 bits (cache_dtype 0)
+/* General form.  key_cache / value_cache hold fp16 bits (cache_dtype 0),
+ * bfloat16 bits (cache_dtype 3: query and head_sink are then bfloat16 too)
  * or 8-bit codes dequantized as code * scale with k_scale / v_scale indexed
  * by [k * D + c] (per_channel = 1) or [0]; head_sink ([H] fp16, may be NULL)
  * adds exp(s_h - m) to the denominator, m = max(s_h, max_p x_p). */
@@ -415,8 +496,9 @@ int oracle_attention_ex(const uint16_t* query, const void* key_cache,
   if (row_begin < 0 || row_end > (long long)T * H || row_begin > row_end)
     return ORACLE_BAD_ARGUMENT;
   if (scale == 0.0) scale = 1.0 / sqrt((double)D);
-  if (cache_dtype != ORACLE_CACHE_FP16 && (k_scale == NULL || v_scale == NULL)) return ORACLE_BAD_ARGUMENT;
-  size_t esize = cache_dtype == ORACLE_CACHE_FP16 ? 2 : 1;
+  const int bf16 = cache_dtype == ORACLE_CACHE_BF16; /* bfloat16 query, cache and sink */
+  if (cache_dtype != ORACLE_CACHE_FP16 && !bf16 && (k_scale == NULL || v_scale == NULL)) return ORACLE_BAD_ARGUMENT;
+  size_t esize = (cache_dtype == ORACLE_CACHE_FP16 || bf16) ? 2 : 1;
   int G = H / Hk;
   double q[1024];
   if (D > 1024) return ORACLE_BAD_ARGUMENT;
@@ -430,7 +512,7 @@ int oracle_attention_ex(const uint16_t* query, const void* key_cache,
     if (window >= 1 && kv_len - window > 0) lo = kv_len - window;
     double* o = out + (size_t)(r - row_begin) * D;
     for (int c = 0; c < D; ++c) {
-      q[c] = oracle_half_to_double(query[((size_t)t * H + h) * D + c]);
+      q[c] = elem16_to_double(query[((size_t)t * H + h) * D + c], bf16);
       o[c] = 0.0;
     }
     /* pass 1: scores and their maximum */
@@ -451,7 +533,7 @@ int oracle_attention_ex(const uint16_t* query, const void* key_cache,
       any = 1;
     }
     if (!any) continue; /* fully masked row: output stays 0 */
-    double sink = head_sink ? oracle_half_to_double(head_sink[h]) : -INFINITY;
+    double sink = head_sink ? elem16_to_double(head_sink[h], bf16) : -INFINITY;
     if (sink > xmax) xmax = sink;
     /* pass 2: weights and the weighted sum of V */
     double denom = 0.0;

@@ -10,9 +10,9 @@ without its outer factor, the default 1/sqrt(D) scale, the head_sink term,
 the sign and pairing of the rotation and its channel offset, the slot
 derivation, the binary16 and e4m3fn roundings, int8 rounding and
 clipping, the per-channel scale index, the QK-Norm epsilon, weight and the
-order and precision of its sum of squares, and
-the latent layout (scores over all 576 channels, values from the first
-512).
+order and precision of its sum of squares, the latent layout (scores over
+all 576 channels, values from the first 512), and the bfloat16 paths
+(decode exponent, rounding, bfloat16 read as fp16, rotary rounded to fp16).
 """
 
 import os
@@ -26,7 +26,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PIN_FILES = [os.path.join(ROOT, "tests", f) for f in (
     "test_oracle_pins.py", "test_oracle_quant_pins.py", "test_oracle_slot_pins.py",
-    "test_oracle_qknorm_pins.py", "test_oracle_mla_pins.py")]
+    "test_oracle_qknorm_pins.py", "test_oracle_mla_pins.py", "test_oracle_bf16_pins.py")]
 
 # (name, text in oracle.c, replacement, occurrences of the text, indices replaced or None = all)
 MUTANTS = [
@@ -64,6 +64,16 @@ MUTANTS = [
      "o[c] += w * oracle_half_to_double(lr[c + D - Dv]);", 1, None),
     ("latent scores over the V channels only", "for (int c = 0; c < D; ++c) x += q[c] * oracle_half_to_double(lr[c]);",
      "for (int c = 0; c < Dv; ++c) x += q[c] * oracle_half_to_double(lr[c]);", 2, None),
+    ("bfloat16 exponent bias", "v = ldexp((double)(128 + f), e - 134);", "v = ldexp((double)(128 + f), e - 133);",
+     1, None),
+    ("bfloat16 truncation", "double m = nearbyint(ldexp(a, 8 - e));", "double m = floor(ldexp(a, 8 - e));", 1,
+     None),
+    ("bfloat16 query read as fp16", "q[c] = elem16_to_double(query[((size_t)t * H + h) * D + c], bf16);",
+     "q[c] = oracle_half_to_double(query[((size_t)t * H + h) * D + c]);", 1, None),
+    ("bfloat16 sink read as fp16", "elem16_to_double(head_sink[h], bf16)", "oracle_half_to_double(head_sink[h])", 1,
+     None),
+    ("bfloat16 rotary rounded to fp16", "tmp[i1] = bf16 ? oracle_double_to_bf16((double)y1)",
+     "tmp[i1] = 0 ? oracle_double_to_bf16((double)y1)", 1, None),
 ]
 
 

@@ -29,6 +29,11 @@ to +-127; e4m3fn: random sign, exponent field 0..10 and fraction bits, so
 magnitudes up to 15), unused slots the code 0x80 (int8 -128, a loud value)
 or 0x7F (e4m3fn NaN); k_scale / v_scale are fp32 [1] or [Hk*D], drawn
 around 1/32 (int8) or 1/16 (e4m3fn).  head_sink is fp16 [H], N(0, 2^2).
+
+bfloat16 steps (cache_dtype CACHE_BF16; the kernel is registered for fp16
+and bfloat16 activations, CUDA design section 8.2): the same draws rounded to bfloat16 for
+every 16-bit tensor (query, key, value, both pools, cos/sin, head_sink);
+unused pool slots hold the bfloat16 NaN pattern 0x7FC0.
 """
 
 from __future__ import annotations
@@ -40,6 +45,7 @@ from typing import Optional
 import torch
 
 NAN_SENTINEL_BITS = 0x7E00
+BF16_NAN_SENTINEL_BITS = 0x7FC0
 
 
 @dataclasses.dataclass(frozen=True)
@@ -132,10 +138,11 @@ def custom_shape(name, num_heads, kv_num_heads, head_size, block_size,
 
 
 def _fill_sentinel(t: torch.Tensor) -> torch.Tensor:
-    return t.view(torch.int16).fill_(NAN_SENTINEL_BITS).view(torch.float16)
+    pattern = BF16_NAN_SENTINEL_BITS if t.dtype == torch.bfloat16 else NAN_SENTINEL_BITS
+    return t.view(torch.int16).fill_(pattern).view(t.dtype)
 
 
-CACHE_FP16, CACHE_INT8, CACHE_FP8 = 0, 1, 2
+CACHE_FP16, CACHE_INT8, CACHE_FP8, CACHE_BF16 = 0, 1, 2, 3
 QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL = 0, 1, 2
 
 
@@ -148,7 +155,8 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     Random values are drawn with a torch.Generator on `gen_device` (default:
     `device`), so a CPU run and a CUDA run of the same shape share lengths
     and block tables (drawn on the CPU) but not necessarily values.
-    cache_dtype / quant_type select 8-bit pools with their scales; head_sink
+    cache_dtype / quant_type select 8-bit pools with their scales, or
+    (CACHE_BF16) bfloat16 activations and pools; head_sink
     adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16,
     1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
     query tensor with key and value None.  latent_v_head_size > 0 makes a
@@ -184,18 +192,19 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     T = int(cum[-1])
 
     vg = torch.Generator(device=gen_device).manual_seed(1000 + shape.seed)
+    act = torch.bfloat16 if cache_dtype == CACHE_BF16 else torch.float16
 
     def randn(*size):
         return torch.randn(*size, generator=vg, device=gen_device,
-                           dtype=torch.float32).to(torch.float16).to(device)
+                           dtype=torch.float32).to(act).to(device)
 
     query = randn(T, H * D)
     key = randn(T, Hk * D)
     value = randn(T, Hk * D)
 
-    if cache_dtype == CACHE_FP16:
-        key_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
-        value_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=torch.float16, device=device))
+    if cache_dtype in (CACHE_FP16, CACHE_BF16):
+        key_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=act, device=device))
+        value_cache = _fill_sentinel(torch.empty(NB, bs, Hk, D, dtype=act, device=device))
         draw = randn
     else:
         fill = 0x80 if cache_dtype == CACHE_INT8 else 0x7F
@@ -238,9 +247,11 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     )
     if shape.do_rotary:
         R = shape.rotary_dim or D
-        cos, sin = rotary_tables(MB * bs, R)
+        cos, sin = rotary_tables(MB * bs, R, dtype=act)
         out.update(cos_cache=cos.to(device), sin_cache=sin.to(device), rotary_dim=R)
-    if cache_dtype != CACHE_FP16:
+    if cache_dtype == CACHE_BF16:
+        out.update(cache_dtype=cache_dtype)
+    elif cache_dtype != CACHE_FP16:
         sg = torch.Generator().manual_seed(4000 + shape.seed)
         n = Hk * D if quant_type == QUANT_PER_CHANNEL else 1
         base = 1.0 / 32.0 if cache_dtype == CACHE_INT8 else 1.0 / 16.0
@@ -250,7 +261,7 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
                    k_scale=ks.float().to(device), v_scale=vs.float().to(device))
     if head_sink:
         hg = torch.Generator().manual_seed(5000 + shape.seed)
-        out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).half().to(device))
+        out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).to(act).to(device))
     if qk_norm:
         ng = torch.Generator().manual_seed(6000 + shape.seed)
         out.update(q_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).half().to(device),
@@ -267,16 +278,16 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     return out
 
 
-def rotary_tables(max_position: int, rotary_dim: int, base: float = 10000.0):
-    """cos/sin tables [max_position, rotary_dim/2] as fp16.
+def rotary_tables(max_position: int, rotary_dim: int, base: float = 10000.0, dtype=torch.float16):
+    """cos/sin tables [max_position, rotary_dim/2] as fp16 (or `dtype`).
 
     theta_i = base^(-2i/rotary_dim); entry (p, i) = cos/sin(p * theta_i),
-    evaluated in fp64 and rounded to fp16.  These are op inputs (the model's
+    evaluated in fp64 and rounded to the table type.  These are op inputs (the model's
     rotary cache), not part of the op.
     """
     half = rotary_dim // 2
     i = torch.arange(half, dtype=torch.float64)
     inv = base ** (-2.0 * i / rotary_dim)
     ang = torch.arange(max_position, dtype=torch.float64)[:, None] * inv[None, :]
-    return torch.cos(ang).to(torch.float16), torch.sin(ang).to(torch.float16)
+    return torch.cos(ang).to(dtype), torch.sin(ang).to(dtype)
 
