@@ -112,8 +112,17 @@ enum {
 /* Cache element types (section 8.2, T_CACHE).  8-bit codes are signed and
  * zero-symmetric; writing a value x stores code = Q(x / scale) with the
  * division in fp32 and Q = round to nearest-even saturated to [-128, 127]
- * (int8) or to +-448 (e4m3fn). */
-enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2 };
+ * (int8) or to +-448 (e4m3fn).
+ * PA_CACHE_BF16 selects bfloat16 activations with a bfloat16 cache (section
+ * 8.2 registers the kernel for fp16 and bfloat16 activations): query, key,
+ * value, both pools, cos_cache / sin_cache, head_sink and the output are
+ * then bfloat16 wherever this header says fp16.  Rotary rounds each rotated
+ * value to bfloat16 (nearest-even) after the same fp32 arithmetic; the
+ * attention contractions take bfloat16 operands (the softmax weights P are
+ * rounded to bfloat16 for the P*V contraction) with fp32 accumulation.
+ * Built for separate caches without packed_qkv or qk_norm; the latent
+ * layout and pa_forward_no_alloc are fp16 only (PA_NOT_SUPPORTED). */
+enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2, PA_CACHE_BF16 = 3 };
 /* Cache layout (section 12).  LATENT: one cache key_cache [NB, bs, 1, D] of
  * latent rows (value and value_cache NULL, kv_num_heads 1); every query
  * head attends with its D channels and the output is the weighted sum of
@@ -148,7 +157,7 @@ typedef struct {
   int max_query_len_bound; /* 0 => max_tokens; upper bound on any q_len */
   int max_kv_len_bound;    /* 0 => MB*bs; upper bound on any past + q_len */
   int cache_dtype;         /* PA_CACHE_*: element type of key_cache / value_cache */
-  int k_quant_type;        /* PA_QUANT_*: NONE for fp16 caches, else PER_TENSOR / PER_CHANNEL */
+  int k_quant_type;        /* PA_QUANT_*: NONE for 16-bit caches, else PER_TENSOR / PER_CHANNEL */
   int v_quant_type;        /* must equal k_quant_type */
   int packed_qkv;          /* 1: pa_forward's query rows are [Q heads | K heads | V heads], key/value NULL */
   int qk_norm;             /* 1: QK-Norm of Q and K before rotary (q/k_norm_weight required) */
@@ -166,14 +175,15 @@ PA_API void pa_config_init(pa_config* cfg);
 /* Host-only check of a configuration against the validation rules
  * (section 15): H % Hk == 0, D % 8 == 0, bs a power of two >= 16,
  * softcap >= 0, window == -1 or >= 1, rotary_dim even and <= D, positive
- * capacities, quantization NONE exactly for fp16 caches.  Writes a message
+ * capacities, quantization NONE exactly for 16-bit caches.  Writes a message
  * naming the field into msg (may be NULL).  Returns PA_INVALID_ARGUMENT or
  * PA_NOT_SUPPORTED on failure.  Not built (PA_NOT_SUPPORTED): 8-bit caches
  * with head_size 64, with k_quant_type != v_quant_type, or with
  * num_heads / kv_num_heads above 16 (8-bit caches run every query row
  * through the decode kernel: a sequence whose q_len * num_heads /
  * kv_num_heads rows exceed one 16-row item runs in chunks of
- * 16 * kv_num_heads / num_heads tokens, section 8.5).  Touches no GPU. */
+ * 16 * kv_num_heads / num_heads tokens, section 8.5); a bfloat16 cache
+ * with packed_qkv, qk_norm or the latent layout.  Touches no GPU. */
 PA_API pa_status pa_validate_config(const pa_config* cfg, char* msg, size_t msg_len);
 
 /* Host-only check of one step's arguments (token_count <= max_tokens,
@@ -228,7 +238,7 @@ PA_API pa_status pa_forward(pa_handle h, const void* query, const void* key,
  * pointer may be NULL where its feature is off. */
 typedef struct {
   const void* head_sink;  /* [H] fp16, device; NULL = no sink */
-  const float* k_scale;   /* device fp32, [1] or [Hk*D]; required iff cache_dtype != PA_CACHE_FP16 */
+  const float* k_scale;   /* device fp32, [1] or [Hk*D]; required iff the cache is 8-bit */
   const float* v_scale;   /* likewise for value_cache */
   const int32_t* slot_mapping; /* [T] int32, device; NULL = derive the write slot from block_table */
   const void* q_norm_weight;   /* [D] fp16, device; required iff qk_norm (with k_norm_weight) */
@@ -318,7 +328,7 @@ PA_API pa_status pa_destroy(pa_handle h);
  * to a word inside the shared scratch, cleared at the start of each call,
  * that the caller cannot read (so is the wait-site id of a timeout).
  *
- * It runs separate fp16 K/V caches without head_sink; an 8-bit
+ * It runs separate fp16 K/V caches without head_sink; an 8-bit or bfloat16
  * cache_dtype, packed_qkv, qk_norm or kv_cache_layout PA_LAYOUT_LATENT
  * returns PA_NOT_SUPPORTED (pa_forward_ex takes all of them and the sink).
  *

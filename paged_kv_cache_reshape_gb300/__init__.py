@@ -34,7 +34,7 @@ PA_STEP_COUNTS = 6
 STEP_COUNT_NAMES = ("n_dec", "n_pre", "n_comb", "split_keys", "pre_ctas", "dec_ctas")
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
-PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 = 0, 1, 2
+PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3, PA_CACHE_BF16 = 0, 1, 2, 3
 PA_QUANT_NONE, PA_QUANT_PER_TENSOR, PA_QUANT_PER_CHANNEL = 0, 1, 2
 PA_LAYOUT_SEPARATE, PA_LAYOUT_LATENT = 0, 1
 

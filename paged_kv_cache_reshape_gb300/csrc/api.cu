@@ -81,6 +81,9 @@ const char* wait_kernel_name(int k) {
   }
 }
 
+// 8-bit code caches (quantized); the 16-bit ones are fp16 and bfloat16.
+bool quantized(int cache_dtype) { return cache_dtype == PA_CACHE_INT8 || cache_dtype == PA_CACHE_FP8_E4M3; }
+
 int rot_dim_of(const pa_config& c) {
   if (!c.do_rotary) return 0;
   return c.rotary_dim > 0 ? c.rotary_dim : c.head_size;
@@ -91,7 +94,7 @@ int rot_dim_of(const pa_config& c) {
 // than the query itself.  A single per-tensor K scale multiplies the score
 // scale instead (exact, CUDA design section 8.5 phase 3).
 bool query_copied(const pa_config& c) {
-  const bool per_channel_k = c.cache_dtype != PA_CACHE_FP16 && c.k_quant_type == PA_QUANT_PER_CHANNEL;
+  const bool per_channel_k = quantized(c.cache_dtype) && c.k_quant_type == PA_QUANT_PER_CHANNEL;
   return c.do_rotary || per_channel_k || c.packed_qkv || c.qk_norm;
 }
 
@@ -289,8 +292,9 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "max_query_len_bound and max_kv_len_bound must be >= 0");
     return PA_INVALID_ARGUMENT;
   }
-  if (c->cache_dtype < PA_CACHE_FP16 || c->cache_dtype > PA_CACHE_FP8_E4M3) {
-    set_msg(msg, len, "cache_dtype must be PA_CACHE_FP16, PA_CACHE_INT8 or PA_CACHE_FP8_E4M3 (got %d)", c->cache_dtype);
+  if (c->cache_dtype < PA_CACHE_FP16 || c->cache_dtype > PA_CACHE_BF16) {
+    set_msg(msg, len, "cache_dtype must be PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 or PA_CACHE_BF16 (got %d)",
+            c->cache_dtype);
     return PA_INVALID_ARGUMENT;
   }
   for (int qt : {c->k_quant_type, c->v_quant_type})
@@ -298,11 +302,11 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
       set_msg(msg, len, "k_quant_type / v_quant_type must be PA_QUANT_NONE, PER_TENSOR or PER_CHANNEL (got %d)", qt);
       return PA_INVALID_ARGUMENT;
     }
-  if (c->cache_dtype == PA_CACHE_FP16 && (c->k_quant_type != PA_QUANT_NONE || c->v_quant_type != PA_QUANT_NONE)) {
-    set_msg(msg, len, "k_quant_type / v_quant_type must be PA_QUANT_NONE with an fp16 cache");
+  if (!quantized(c->cache_dtype) && (c->k_quant_type != PA_QUANT_NONE || c->v_quant_type != PA_QUANT_NONE)) {
+    set_msg(msg, len, "k_quant_type / v_quant_type must be PA_QUANT_NONE with a 16-bit cache");
     return PA_INVALID_ARGUMENT;
   }
-  if (c->cache_dtype != PA_CACHE_FP16 && (c->k_quant_type == PA_QUANT_NONE || c->v_quant_type == PA_QUANT_NONE)) {
+  if (quantized(c->cache_dtype) && (c->k_quant_type == PA_QUANT_NONE || c->v_quant_type == PA_QUANT_NONE)) {
     set_msg(msg, len, "an 8-bit cache needs k_quant_type and v_quant_type PER_TENSOR or PER_CHANNEL");
     return PA_INVALID_ARGUMENT;
   }
@@ -339,7 +343,7 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
       return PA_INVALID_ARGUMENT;
     }
     if (c->k_quant_type != PA_QUANT_NONE || c->v_quant_type != PA_QUANT_NONE || c->cache_dtype != PA_CACHE_FP16) {
-      set_msg(msg, len, "a quantized latent cache is not built (fp16 only)");
+      set_msg(msg, len, "the latent layout is built for an fp16 cache only");
       return PA_NOT_SUPPORTED;
     }
   }
@@ -388,7 +392,11 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "qk_norm is built for kv_num_heads <= 32 (got %d)", c->kv_num_heads);
     return PA_NOT_SUPPORTED;
   }
-  if (c->cache_dtype != PA_CACHE_FP16) {
+  if (c->cache_dtype == PA_CACHE_BF16 && (c->packed_qkv || c->qk_norm)) {
+    set_msg(msg, len, "bfloat16 activations are built without packed_qkv and qk_norm");
+    return PA_NOT_SUPPORTED;
+  }
+  if (quantized(c->cache_dtype)) {
     if (c->k_quant_type != c->v_quant_type) {
       set_msg(msg, len, "k_quant_type and v_quant_type must match in this library");
       return PA_NOT_SUPPORTED;
@@ -535,7 +543,7 @@ pa_status pa_create(const pa_config* cfg, pa_handle* out) {
   // chunks at most: each chunk reads the sequence's keys again, and the
   // prefill kernel's fixed cost is not repaid by a few rows), longer ones
   // take the prefill kernel.
-  const bool quant = c.cache_dtype != PA_CACHE_FP16;
+  const bool quant = quantized(c.cache_dtype);
   h->chunk_tokens = h->dec_rows > 0 ? std::max(1, h->dec_rows / h->G) : 0;
   h->chunk_rows_max = (h->latent || quant) ? 0 : 2 * h->chunk_tokens * h->G;
   // Decode entries: one per sequence, or one per chunk (with fp16 caches a
@@ -656,7 +664,7 @@ pa_status pa_set_option(pa_handle h, int option, int value) {
       return PA_OK;
     case PA_OPT_WAIT_PROBE: h->opt_wait_probe = value != 0; return PA_OK;
     case PA_OPT_DECODE_MAX_ROWS:
-      if ((h->cfg.cache_dtype != PA_CACHE_FP16 || h->latent) && value != h->dec_rows)
+      if ((quantized(h->cfg.cache_dtype) || h->latent) && value != h->dec_rows)
         return fail(h, PA_NOT_SUPPORTED, "8-bit caches and the latent layout route every row to decode items");
       if (value < 0 || value > h->dec_rows)
         return fail(h, PA_INVALID_ARGUMENT, "decode max rows must be in [0, %d]", h->dec_rows);
@@ -752,7 +760,7 @@ pa::CacheWriteParams cache_write_params(const pa_config& c, __half* q_ws, int* e
                                         const int32_t* block_table, const int32_t* cum, const int32_t* past,
                                         int batch, int token_count, const void* cos_cache, const void* sin_cache,
                                         const pa_extra_inputs* x) {
-  const bool quant = c.cache_dtype != PA_CACHE_FP16;
+  const bool quant = quantized(c.cache_dtype);
   const bool latent = c.kv_cache_layout == PA_LAYOUT_LATENT;
   const int R = rot_dim_of(c);
   const bool q_scaled = quant && c.k_quant_type == PA_QUANT_PER_CHANNEL;
@@ -818,11 +826,11 @@ const pa_extra_inputs kNoExtra = {nullptr, nullptr, nullptr, nullptr, nullptr, n
 // The optional inputs against the configuration: scales exactly for 8-bit
 // caches, element alignment.
 pa_status check_extra(pa_handle h, const pa_extra_inputs* x) {
-  const bool quant = h->cfg.cache_dtype != PA_CACHE_FP16;
+  const bool quant = quantized(h->cfg.cache_dtype);
   if (quant && (!x->k_scale || !x->v_scale))
     return fail(h, PA_INVALID_ARGUMENT, "k_scale and v_scale are required with an 8-bit cache");
   if (!quant && (x->k_scale || x->v_scale))
-    return fail(h, PA_INVALID_ARGUMENT, "k_scale / v_scale given but the cache is fp16");
+    return fail(h, PA_INVALID_ARGUMENT, "k_scale / v_scale given but the cache is 16-bit");
   if ((reinterpret_cast<uintptr_t>(x->k_scale) | reinterpret_cast<uintptr_t>(x->v_scale)) % 4)
     return fail(h, PA_INVALID_ARGUMENT, "k_scale and v_scale must be 4-byte aligned");
   if (reinterpret_cast<uintptr_t>(x->head_sink) % 2)
@@ -898,7 +906,8 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   const pa_extra_inputs* x = extra ? extra : &kNoExtra;
   st = check_extra(h, x);
   if (st != PA_OK) return st;
-  const bool quant = h->cfg.cache_dtype != PA_CACHE_FP16;
+  const bool quant = quantized(h->cfg.cache_dtype);
+  const int bf16 = h->cfg.cache_dtype == PA_CACHE_BF16 ? 1 : 0;
   const __half* sink = static_cast<const __half*>(x->head_sink);
   h->last_launches = 0;
   for (bool& r : h->stage_ran) r = false;
@@ -1070,6 +1079,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     pa::PrefillParams p{};
     p.out = static_cast<__half*>(output);
     p.head_sink = sink;
+    p.bf16 = bf16;
     p.block_table = block_table;
     p.seq = h->seq;
     p.pre_tiles = h->pre_tiles;
@@ -1137,6 +1147,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   {
     pa::CombineParams p{};
     p.head_sink = sink;
+    p.bf16 = bf16;
     p.part_o = h->part_o;
     p.part_ml = h->part_ml;
     p.seq = h->dseq;  // the decode table
@@ -1231,7 +1242,7 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->packed_qkv || cfg->qk_norm || cfg->kv_cache_layout != PA_LAYOUT_SEPARATE)
     return fail(nullptr, PA_NOT_SUPPORTED,
                 "pa_forward_no_alloc runs separate fp16 K/V caches without packed QKV or QK-Norm (no latent "
-                "layout); use pa_forward_ex");
+                "layout, no 8-bit or bfloat16 cache); use pa_forward_ex");
   if (device_error && reinterpret_cast<uintptr_t>(device_error) % 4)
     return fail(nullptr, PA_INVALID_ARGUMENT, "device_error must be 4-byte aligned");
   if (token_count == 0) return PA_OK;

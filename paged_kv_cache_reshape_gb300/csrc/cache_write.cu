@@ -12,7 +12,10 @@
 //
 // Rotary arithmetic is fixed so the pool is bit-reproducible: per pair,
 //   y1 = rn(rn(x1*c) - rn(x2*s)),  y2 = rn(rn(x2*c) + rn(x1*s))
-// in fp32 (no fused multiply-add), then fp16 round-to-nearest-even.
+// in fp32 (no fused multiply-add), then fp16 round-to-nearest-even.  With
+// bfloat16 activations (section 8.2) the inputs and tables are bfloat16,
+// the same fp32 steps run and each y is rounded to bfloat16 (nearest-even);
+// a 16-bit row that is not rotated is copied bit for bit either way.
 //
 // Every row moves as 16-byte vectors: the NHD pool stores a token's
 // [Hk, D] slice contiguously, so a warp writes one contiguous run of
@@ -37,6 +40,7 @@
 #include <algorithm>
 #include <type_traits>
 
+#include "ptx.cuh"
 #include "step.h"
 #include "worklist.cuh"
 #include "../../include/pa.h"
@@ -46,14 +50,14 @@ namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
-__device__ __forceinline__ void rotate_pair(__half x1, __half x2, __half c, __half s, __half& y1,
-                                            __half& y2) {
-  float fx1 = __half2float(x1), fx2 = __half2float(x2);
-  float fc = __half2float(c), fs = __half2float(s);
+__device__ __forceinline__ void rotate_pair(__half x1, __half x2, __half c, __half s, __half& y1, __half& y2,
+                                            bool bf16) {
+  float fx1 = elem16_to_float(x1, bf16), fx2 = elem16_to_float(x2, bf16);
+  float fc = elem16_to_float(c, bf16), fs = elem16_to_float(s, bf16);
   float a = __fsub_rn(__fmul_rn(fx1, fc), __fmul_rn(fx2, fs));
   float b = __fadd_rn(__fmul_rn(fx2, fc), __fmul_rn(fx1, fs));
-  y1 = __float2half_rn(a);
-  y2 = __float2half_rn(b);
+  y1 = float_to_elem16(a, bf16);
+  y2 = float_to_elem16(b, bf16);
 }
 
 union Vec8 {
@@ -139,12 +143,13 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
 // nw (the [D] weight), every loaded value is first normalized.  R % 16 == 0
 // is checked on the host.  Channels outside [keep_lo, keep_hi) that are not
 // rotated are not emitted at all (a latent query's copy keeps only the
-// 64-channel chunks that hold its rotated channels).
+// 64-channel chunks that hold its rotated channels).  bf16: the row and the
+// tables hold bfloat16 (rotation only; QK-Norm is fp16).
 template <typename Emit>
 __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
                               int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
                               const float* rn = nullptr, const __half* nw = nullptr, int off = 0, int keep_lo = 0,
-                              int keep_hi = 1 << 30) {
+                              int keep_hi = 1 << 30, bool bf16 = false) {
   const bool keep_all = keep_lo <= 0 && keep_hi >= D;
   const int chunks_per_head = D / 8;
   auto ld8 = [&](int h, int ch) -> Vec8 {
@@ -189,7 +194,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
         cs.u = __ldg(reinterpret_cast<const uint4*>(cos_row + 8 * c));
         sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
 #pragma unroll
-        for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e]);
+        for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e], bf16);
         emit(h, off + 8 * c, ya);
         emit(h, off + half + 8 * c, yb);
       } else {
@@ -213,7 +218,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
         const __half* sv = reinterpret_cast<const __half*>(&su);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          rotate_pair(a.h[2 * e], a.h[2 * e + 1], cv[e], sv[e], y.h[2 * e], y.h[2 * e + 1]);
+          rotate_pair(a.h[2 * e], a.h[2 * e + 1], cv[e], sv[e], y.h[2 * e], y.h[2 * e + 1], bf16);
       } else {
         y.u = a.u;
       }
@@ -272,7 +277,8 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
                     p.rot_offset);
     else
       row_transform(qsrc, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
-                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset, p.q_keep_lo, p.q_keep_hi);
+                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset, p.q_keep_lo, p.q_keep_hi,
+                    p.cache_type == kCacheBF16);
     return;
   }
 
@@ -334,10 +340,10 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane);
     krn = rn;
   }
-  if (p.cache_type == kCacheF16) {
+  if (p.cache_type == kCacheF16 || p.cache_type == kCacheBF16) {
     row_transform(ksrc, EmitHalf{static_cast<__half*>(p.key_cache) + slot * kv_row, p.D},
                   p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
-                  p.rot_offset);
+                  p.rot_offset, 0, 1 << 30, p.cache_type == kCacheBF16);
     if (p.value_cache)  // none for a latent cache (V is part of the latent rows)
       row_transform(vsrc, EmitHalf{static_cast<__half*>(p.value_cache) + slot * kv_row, p.D}, p.Hk, p.D, false,
                     0, 0, nullptr, nullptr, lane);

@@ -7,7 +7,8 @@
 // 8 implementation note P5).  Maxima are kept in log2 units by the decode
 // kernel, hence base-2 exponentials.  A row whose splits are all empty
 // outputs 0.  With head_sink (same CUDA design, section 6.1) the row's
-// denominator also gets exp(s_h - M), the sink in log2 units.
+// denominator also gets exp(s_h - M), the sink in log2 units.  BF: the
+// sink and the output are bfloat16 (bfloat16 activations, section 8.2).
 //
 // One warp per (packed row, query head); the work list holds only the rows
 // of sequences that were split, so the grid is a small persistent one.
@@ -40,7 +41,7 @@ __device__ __forceinline__ void axpy(float* acc, float f, const float* po) {
   }
 }
 
-template <int D>
+template <int D, bool BF>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
   constexpr int kPer = D / 32;  // channels per lane
   const int lane = threadIdx.x & 31;
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
       den = dl;
-      if (p.head_sink && M != -INFINITY) den += exp2f(__half2float(p.head_sink[h]) * kLog2eC - M);
+      if (p.head_sink && M != -INFINITY) den += exp2f(elem16_to_float(p.head_sink[h], BF) * kLog2eC - M);
       for (int s0 = 0; s0 < ns; s0 += 4) {
         float f[4];
         const float* po[4];
@@ -121,7 +122,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
           den += f * ml.y;
           axpy<kPer>(acc, f, p.part_o + row_of(s) * D + lane * kPer);
         }
-        if (p.head_sink) den += exp2f(__half2float(p.head_sink[h]) * kLog2eC - M);
+        if (p.head_sink) den += exp2f(elem16_to_float(p.head_sink[h], BF) * kLog2eC - M);
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
@@ -130,13 +131,11 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
 #pragma unroll
       for (int i = 0; i < kPer; i += 8)
         *reinterpret_cast<uint4*>(out + i) =
-            make_uint4(pack_half2(acc[i] * inv, acc[i + 1] * inv), pack_half2(acc[i + 2] * inv, acc[i + 3] * inv),
-                       pack_half2(acc[i + 4] * inv, acc[i + 5] * inv), pack_half2(acc[i + 6] * inv, acc[i + 7] * inv));
+            make_uint4(pack2<BF>(acc[i] * inv, acc[i + 1] * inv), pack2<BF>(acc[i + 2] * inv, acc[i + 3] * inv),
+                       pack2<BF>(acc[i + 4] * inv, acc[i + 5] * inv), pack2<BF>(acc[i + 6] * inv, acc[i + 7] * inv));
     } else {
 #pragma unroll
-      for (int i = 0; i < kPer; i += 2) {
-        *reinterpret_cast<__half2*>(out + i) = __floats2half2_rn(acc[i] * inv, acc[i + 1] * inv);
-      }
+      for (int i = 0; i < kPer; i += 2) *reinterpret_cast<uint32_t*>(out + i) = pack2<BF>(acc[i] * inv, acc[i + 1] * inv);
     }
   }
 }
@@ -144,11 +143,19 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineParams p) {
 }  // namespace
 
 cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t s) {
+  if (p.bf16) {
+    switch (p.D) {  // (the latent layout's 512-channel rows are fp16 only)
+      case 64: return launch_pdl(combine_kernel<64, true>, grid, kWarps * 32, 0, s, p);
+      case 128: return launch_pdl(combine_kernel<128, true>, grid, kWarps * 32, 0, s, p);
+      case 256: return launch_pdl(combine_kernel<256, true>, grid, kWarps * 32, 0, s, p);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (p.D) {
-    case 64: return launch_pdl(combine_kernel<64>, grid, kWarps * 32, 0, s, p);
-    case 128: return launch_pdl(combine_kernel<128>, grid, kWarps * 32, 0, s, p);
-    case 256: return launch_pdl(combine_kernel<256>, grid, kWarps * 32, 0, s, p);
-    case 512: return launch_pdl(combine_kernel<512>, grid, kWarps * 32, 0, s, p);
+    case 64: return launch_pdl(combine_kernel<64, false>, grid, kWarps * 32, 0, s, p);
+    case 128: return launch_pdl(combine_kernel<128, false>, grid, kWarps * 32, 0, s, p);
+    case 256: return launch_pdl(combine_kernel<256, false>, grid, kWarps * 32, 0, s, p);
+    case 512: return launch_pdl(combine_kernel<512, false>, grid, kWarps * 32, 0, s, p);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,7 +44,10 @@
 //    codes become fp16 pairs with one byte permute and one conversion; the
 //    V scale multiplies the merged output;
 //  * head_sink (section 6.1) adds exp(s_h - M) to the final denominator of a
-//    single-split row (split rows get it in the combine kernel).
+//    single-split row (split rows get it in the combine kernel);
+//  * bfloat16 activations with a bfloat16 cache (section 8.2) run the fp16
+//    layout and schedule with bfloat16 MMAs: Q and K as stored, P rounded
+//    to bfloat16 for O += P V, bfloat16 output and sink.
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -60,12 +63,13 @@ constexpr float kLazyRescale = 8.f;  // log2 of the largest P value tolerated be
 
 template <int D, int CT, int NT>
 struct DecodeCfg {
-  static constexpr int kEb = CT == kCacheF16 ? 2 : 1;      // bytes per cache element
+  static constexpr bool k16 = CT == kCacheF16 || CT == kCacheBF16;  // 16-bit cache elements
+  static constexpr int kEb = k16 ? 2 : 1;                   // bytes per cache element
   static constexpr int kChunks = D * kEb / 128;             // 128-byte chunks per K/V row
   static constexpr int kQChunks = D / 64;                   // 128-byte chunks per fp16 query row
   static constexpr int kTileBytes = kStageKeys * D * kEb;   // K (or V) bytes per stage
   static constexpr int kStageBytes = 2 * kTileBytes;        // K + V
-  static constexpr int kStages = CT == kCacheF16 ? ((D == 256) ? 3 : (D == 128 ? 3 : 6)) : 4;
+  static constexpr int kStages = k16 ? ((D == 256) ? 3 : (D == 128 ? 3 : 6)) : 4;
   static constexpr int kQBytes = kQChunks * 2048;           // 16 rows x 128 B per chunk
   // End-of-item merge: the four warps' 8 * NT x D fp32 partial outputs, in
   // the last stage's buffer when it is large enough, else in a region of
@@ -73,7 +77,7 @@ struct DecodeCfg {
   static constexpr int kMergeBytes = kDecodeWarps * 8 * NT * D * 4;
   // 8-bit pools with one row tile fit three CTAs on an SM (the merge reuses
   // a stage buffer and the registers stay within a third of the file).
-  static constexpr int kCtasPerSm = (D == 256) ? 1 : ((CT != kCacheF16 && NT == 1) ? 3 : 2);
+  static constexpr int kCtasPerSm = (D == 256) ? 1 : ((!k16 && NT == 1) ? 3 : 2);
   static constexpr int kOwnMerge = kMergeBytes > kStageBytes ? kMergeBytes : 0;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kOwnMerge + 2 * kQBytes + 4 * 16 * 8 +
                                     kStages * 64 + (2 * kStages + 4) * 8;
@@ -150,7 +154,8 @@ template <int D, int CT, int NT>
 __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
                                             const DecodeParams& p) {
   using C = DecodeCfg<D, CT, NT>;
-  constexpr bool kQ8 = CT != kCacheF16;
+  constexpr bool kQ8 = !C::k16;
+  constexpr bool kBF = CT == kCacheBF16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -490,11 +495,11 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
             if constexpr (D <= 128) {
-              hmma16816(s[n], a, qf[ks][n][0], qf[ks][n][1]);
+              mma16816<kBF>(s[n], a, qf[ks][n][0], qf[ks][n][1]);
             } else {
               uint32_t b[2];
               load_qf(ks, n, b);
-              hmma16816(s[n], a, b[0], b[1]);
+              mma16816<kBF>(s[n], a, b[0], b[1]);
             }
           }
         }
@@ -550,8 +555,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         l[n][1] = l[n][1] * alpha[n][1] + (pv[1] + pv[3]);
         // the accumulator halves are m8n8 fragments of (key, row); their
         // transposes are (row, key) pairs, the B fragment of O^T += V^T P^T
-        pb[n][0] = movmatrix_t(pack_half2(pv[0], pv[1]));
-        pb[n][1] = movmatrix_t(pack_half2(pv[2], pv[3]));
+        pb[n][0] = movmatrix_t(pack2<kBF>(pv[0], pv[1]));
+        pb[n][1] = movmatrix_t(pack2<kBF>(pv[2], pv[3]));
       }
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
@@ -598,7 +603,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
           uint32_t a[4];
           ldsm_x4_t(smem_u32(vt + tile_off<C::kChunks>(key, d >> 6, (d & 63) >> 3, log_r)), a[0], a[1], a[2], a[3]);
 #pragma unroll
-          for (int n = 0; n < NT; ++n) hmma16816(o[nd][n], a, pb[n][0], pb[n][1]);
+          for (int n = 0; n < NT; ++n) mma16816<kBF>(o[nd][n], a, pb[n][0], pb[n][1]);
         }
       }
     }
@@ -660,8 +665,8 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if constexpr (kQ8) acc *= __ldg(p.v_scale + (p.per_channel ? tg.k * D + d : 0));
         if (tg.nsplit == 1) {
           const int t = tg.t0 + r / p.G, h = tg.k * p.G + r % p.G;
-          if (p.head_sink && M != -INFINITY) den += exp2f(__half2float(p.head_sink[h]) * kLog2e - M);
-          p.out[((size_t)t * p.H + h) * D + d] = __float2half_rn(den > 0.f ? acc / den : 0.f);
+          if (p.head_sink && M != -INFINITY) den += exp2f(elem16_to_float(p.head_sink[h], kBF) * kLog2e - M);
+          p.out[((size_t)t * p.H + h) * D + d] = float_to_elem16(den > 0.f ? acc / den : 0.f, kBF);
         } else {
           const size_t row = ((size_t)tg.part * p.Hk + tg.k) * kDecodeRows + r;
           p.part_o[row * D + d] = acc;
@@ -740,6 +745,14 @@ cudaError_t decode_configure(int head_size, int cache_type, int group, int* ctas
       default: return cudaErrorInvalidValue;
     }
   }
+  if (cache_type == kCacheBF16) {
+    switch (head_size) {
+      case 64: return configure_d<64, kCacheBF16>(group, smem, ctas_per_sm);
+      case 128: return configure_d<128, kCacheBF16>(group, smem, ctas_per_sm);
+      case 256: return configure_d<256, kCacheBF16>(group, smem, ctas_per_sm);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   const bool i8 = cache_type == kCacheI8;
   switch (head_size) {
     case 128: return i8 ? configure_d<128, kCacheI8>(group, smem, ctas_per_sm) : configure_d<128, kCacheE4M3>(group, smem, ctas_per_sm);
@@ -755,6 +768,14 @@ cudaError_t launch_decode(int head_size, const CUtensorMap& tk, const CUtensorMa
       case 64: return launch_dc<64, kCacheF16>(tk, tv, tq, p, grid, s);
       case 128: return launch_dc<128, kCacheF16>(tk, tv, tq, p, grid, s);
       case 256: return launch_dc<256, kCacheF16>(tk, tv, tq, p, grid, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (p.cache_type == kCacheBF16) {
+    switch (head_size) {
+      case 64: return launch_dc<64, kCacheBF16>(tk, tv, tq, p, grid, s);
+      case 128: return launch_dc<128, kCacheBF16>(tk, tv, tq, p, grid, s);
+      case 256: return launch_dc<256, kCacheBF16>(tk, tv, tq, p, grid, s);
       default: return cudaErrorInvalidValue;
     }
   }

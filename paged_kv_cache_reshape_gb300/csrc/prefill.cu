@@ -30,6 +30,8 @@
 //   warp 5     TMEM owner and MMA issuer (one elected thread)
 // S for KV tile i+1 is computed while the softmax warps work on tile i, and
 // the softmax computes P for tile i while P V of tile i-1 is still running.
+// BF: bfloat16 activations (section 8.2): bfloat16 A/B in the MMA
+// instruction descriptors, P stored as bfloat16, bfloat16 sink and output.
 #include "ptx.cuh"
 #include "step.h"
 #include "../../include/pa.h"
@@ -82,7 +84,7 @@ struct Ctrl {
   int abort;
 };
 
-template <int D, bool CAP>
+template <int D, bool CAP, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -261,8 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (one elect.sync-chosen lane: MMAs issued under it cost far fewer
     // cycles than under a lane-index branch)
     if (elect_one()) {
-      constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, KEYS, 0, 0);
-      constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
+      constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, KEYS, 0, 0, BF ? 1 : 0);
+      constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1, BF ? 1 : 0);
       const uint32_t p_addr = smem_u32(p_s), kv_addr = smem_u32(kv_s);
       uint32_t g = 0, s_issued = 0, v = 0;
       bool ok = true;
@@ -439,10 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c8 = 0; c8 < KEYS / 8; ++c8) {
           uint4 w;
-          w.x = pack_half2(x[8 * c8 + 0], x[8 * c8 + 1]);
-          w.y = pack_half2(x[8 * c8 + 2], x[8 * c8 + 3]);
-          w.z = pack_half2(x[8 * c8 + 4], x[8 * c8 + 5]);
-          w.w = pack_half2(x[8 * c8 + 6], x[8 * c8 + 7]);
+          w.x = pack2<BF>(x[8 * c8 + 0], x[8 * c8 + 1]);
+          w.y = pack2<BF>(x[8 * c8 + 2], x[8 * c8 + 3]);
+          w.z = pack2<BF>(x[8 * c8 + 4], x[8 * c8 + 5]);
+          w.w = pack2<BF>(x[8 * c8 + 6], x[8 * c8 + 7]);
           const int kc = c8 >> 3, col16 = c8 & 7;
           *reinterpret_cast<uint4*>(p_s + kc * (kPrefillRows * 128) + r * 128 + ((col16 ^ (r & 7)) << 4)) = w;
         }
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int t = ti.t0 + j, h = ti.k * p.G + (r - j * p.G);
       // head_sink (section 6.1): exp(s_h - m) joins the denominator
-      if (p.head_sink && m_ref != -INFINITY) l += ex2(__half2float(p.head_sink[h]) * kLog2e - m_ref);
+      if (p.head_sink && m_ref != -INFINITY) l += ex2(elem16_to_float(p.head_sink[h], BF) * kLog2e - m_ref);
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       __half* dst = p.out + ((size_t)t * p.H + h) * D;
 #pragma unroll 1
@@ -469,10 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-            w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-            w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-            w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+            w.x = pack2<BF>(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
+            w.y = pack2<BF>(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
+            w.z = pack2<BF>(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
+            w.w = pack2<BF>(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
             *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
           }
         }
@@ -497,7 +499,10 @@ template <int D, bool CAP>
 cudaError_t configure_dc() {
   static_assert(sizeof(Ctrl) <= 1024, "control block");
   static_assert(PrefillCfg<D>::kSmemBytes <= 227 * 1024, "shared memory");
-  return cudaFuncSetAttribute(prefill_kernel<D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, CAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)PrefillCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_kernel<D, CAP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PrefillCfg<D>::kSmemBytes);
 }
 
@@ -508,12 +513,18 @@ cudaError_t configure_d(size_t* smem) {
   return e != cudaSuccess ? e : configure_dc<D, true>();
 }
 
+template <int D, bool BF>
+cudaError_t launch_db(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                      int grid, cudaStream_t s) {
+  if (p.softcap > 0.f)
+    return launch_pdl(prefill_kernel<D, true, BF>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return launch_pdl(prefill_kernel<D, false, BF>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+}
+
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      int grid, cudaStream_t s) {
-  if (p.softcap > 0.f)
-    return launch_pdl(prefill_kernel<D, true>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
-  return launch_pdl(prefill_kernel<D, false>, grid, kThreads, PrefillCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return p.bf16 ? launch_db<D, true>(tq, tk, tv, p, grid, s) : launch_db<D, false>(tq, tk, tv, p, grid, s);
 }
 
 }  // namespace

@@ -22,6 +22,9 @@
 //   * the softmax does two fp32 lanes per instruction (f32x2 FMA/ADD) and a
 //     three-input max;
 //   * TMEM: S_A, S_B (128 columns each), O_A, O_B (head_size each);
+//   * bfloat16 activations (section 8.2; BF): the same kernel with bfloat16
+//     A/B in the MMA instruction descriptors, P packed as bfloat16 pairs,
+//     bfloat16 sink and output;
 //   * shared memory: one Q buffer per tile, a ring of K and V tile slots
 //     loaded in the order they are used: K0 V0 K1 V1 ...
 //
@@ -146,7 +149,7 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-template <int D, bool CAP>
+template <int D, bool CAP, bool BF>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
@@ -362,8 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // One lane, elected with elect.sync, runs the whole loop: it waits on
     // the barriers alone (a warp-wide wait and vote per barrier costs several
     // times more) and issues the tcgen05 instructions.
-    constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, kKeys, 0, 0);
-    constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1);
+    constexpr uint32_t idesc_s = umma_idesc_f16(kPrefillRows, kKeys, 0, 0, BF ? 1 : 0);
+    constexpr uint32_t idesc_o = umma_idesc_f16(kPrefillRows, D, 0, 1, BF ? 1 : 0);
     const uint64_t desc_k = smem_desc_sw128(0, 16, 1024);           // K-major Q and K, + (address >> 4)
     const uint64_t desc_v = smem_desc_sw128(0, kKeys * 128, 1024);  // MN-major V, + (address >> 4)
     const uint32_t kv_addr = smem_u32(kv_s);
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             unf2(arg, a0, a1);
             const float e0 = ex2(a0), e1 = ex2(a1);
             sum2[q & 3] = add2(sum2[q & 3], f2(e0, e1));
-            pk[q] = pack_half2(e0, e1);
+            pk[q] = pack2<BF>(e0, e1);
           }
           // P_X -> TMEM over S_X: keys h..h+31 as 16 columns of fp16 pairs
           tmem_st16(lane_addr + C::s_col(X) + h / 2, pk);
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head_sink (section 6.1): one more denominator term, exp(s_h - m), in
       // log2 units relative to the row's reference maximum
       if (p.head_sink && m_ref != -INFINITY)
-        l += ex2(__half2float(p.head_sink[ui.k * p.G + (r - j * p.G)]) * kLog2e - m_ref);
+        l += ex2(elem16_to_float(p.head_sink[ui.k * p.G + (r - j * p.G)], BF) * kLog2e - m_ref);
       // The row sum goes to the epilogue warpgroup (its previous value has
       // been read once l_empty completes).
       if (!wait_or_abort(&ctl->l_empty[X], (tt & 1) ^ 1, abort, p.err, p.err_site, kSitePrefillPair | 8)) break;
@@ -633,10 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint4 w;
-              w.x = pack_half2(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
-              w.y = pack_half2(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
-              w.z = pack_half2(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
-              w.w = pack_half2(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
+              w.x = pack2<BF>(o[8 * q + 0] * inv_l, o[8 * q + 1] * inv_l);
+              w.y = pack2<BF>(o[8 * q + 2] * inv_l, o[8 * q + 3] * inv_l);
+              w.z = pack2<BF>(o[8 * q + 4] * inv_l, o[8 * q + 5] * inv_l);
+              w.w = pack2<BF>(o[8 * q + 6] * inv_l, o[8 * q + 7] * inv_l);
               *reinterpret_cast<uint4*>(dst + 32 * c + 8 * q) = w;
             }
           }
@@ -663,16 +666,25 @@ cudaError_t configure_dc() {
   static_assert(PairCfg<D>::kSlots >= 3, "K/V ring");
   static_assert(PairCfg<D>::kSlots / 2 + 2 <= kMaskRing, "page mask ring");
   static_assert(2 * kKeys + 2 * D <= PairCfg<D>::kTmemCols, "tensor memory");
-  return cudaFuncSetAttribute(prefill_pair_kernel<D, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(prefill_pair_kernel<D, CAP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)PairCfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(prefill_pair_kernel<D, CAP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)PairCfg<D>::kSmemBytes);
+}
+
+template <int D, bool BF>
+cudaError_t launch_db(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                      int grid, cudaStream_t s) {
+  if (p.softcap > 0.f)
+    return launch_pdl(prefill_pair_kernel<D, true, BF>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return launch_pdl(prefill_pair_kernel<D, false, BF>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
 }
 
 template <int D>
 cudaError_t launch_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      int grid, cudaStream_t s) {
-  if (p.softcap > 0.f)
-    return launch_pdl(prefill_pair_kernel<D, true>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
-  return launch_pdl(prefill_pair_kernel<D, false>, grid, kThreads, PairCfg<D>::kSmemBytes, s, tq, tk, tv, p);
+  return p.bf16 ? launch_db<D, true>(tq, tk, tv, p, grid, s) : launch_db<D, false>(tq, tk, tv, p, grid, s);
 }
 
 }  // namespace

@@ -2,6 +2,7 @@
 // proxy fences, ldmatrix and the m16n8k16 HMMA used by the decode kernel.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -232,6 +233,22 @@ __device__ __forceinline__ void hmma16816(float* d, const uint32_t* a, uint32_t 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// The same MMA with bfloat16 A and B.
+__device__ __forceinline__ void bmma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// fp16 (BF = false) or bfloat16 (BF = true) operands.
+template <bool BF>
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (BF) bmma16816(d, a, b0, b1);
+  else hmma16816(d, a, b0, b1);
+}
+
 // ---------------------------------------------------------------- tcgen05
 // Tensor memory (TMEM) and the 5th-generation MMA, cta_group::1.
 
@@ -334,11 +351,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor for kind::f16 with fp16 A/B and fp32 D.
-// a_mn / b_mn select MN-major (transposed) operands.
-__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4)                        // D format: f32
-         | (0u << 7) | (0u << 10)         // A, B format: f16
+// Instruction descriptor for kind::f16 with fp16 (bf16 = 0) or bfloat16
+// (bf16 = 1) A/B and fp32 D.  a_mn / b_mn select MN-major (transposed)
+// operands.
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, int b_mn, int bf16 = 0) {
+  return (1u << 4)                                          // D format: f32
+         | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10)   // A, B format: f16 (0) or bf16 (1)
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
@@ -346,6 +364,29 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, in
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two floats as a bfloat16 pair (lo in the low half), each rounded to
+// nearest-even.
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF) return pack_bf162(lo, hi);
+  else return pack_half2(lo, hi);
+}
+
+// A 16-bit element (fp16 or bfloat16 bits) as a float (exact).
+__device__ __forceinline__ float elem16_to_float(__half x, bool bf16) {
+  return bf16 ? __uint_as_float((uint32_t)__half_as_ushort(x) << 16) : __half2float(x);
+}
+
+// A float rounded to nearest-even as fp16 or bfloat16 bits.
+__device__ __forceinline__ __half float_to_elem16(float v, bool bf16) {
+  return bf16 ? __ushort_as_half(__bfloat16_as_ushort(__float2bfloat16_rn(v))) : __float2half_rn(v);
 }
 
 }  // namespace pa

@@ -115,8 +115,10 @@ struct WorklistParams {
   int* err;
 };
 
-// Cache element types (pa.h PA_CACHE_*).
-enum CacheType { kCacheF16 = 0, kCacheI8 = 1, kCacheE4M3 = 2 };
+// Cache element types (pa.h PA_CACHE_*).  kCacheBF16: bfloat16 activations
+// and cache; every 16-bit tensor of the step (declared __half below, bits
+// only) then holds bfloat16.
+enum CacheType { kCacheF16 = 0, kCacheI8 = 1, kCacheE4M3 = 2, kCacheBF16 = 3 };
 
 struct CacheWriteParams {
   const __half* key;    // [T, Hk*D]
@@ -192,6 +194,7 @@ struct DecodeParams {
 
 struct CombineParams {
   const __half* head_sink;  // [H] or null
+  int bf16;                 // 1: head_sink and out are bfloat16
   const float* part_o;
   const float2* part_ml;
   const SeqInfo* seq;       // the decode table
@@ -208,6 +211,7 @@ struct CombineParams {
 struct PrefillParams {
   __half* out;
   const __half* head_sink;  // [H] or null
+  int bf16;                 // 1: query, pools, head_sink and out are bfloat16
   const int* block_table;
   const SeqInfo* seq;       // the sequence table
   const int2* pre_tiles;

@@ -9,6 +9,23 @@ import paged_kv_cache_reshape_gb300 as pa
 import workloads
 
 RTOL, ATOL = 1e-2, 2e-3   # |gpu - oracle| <= ATOL + RTOL * |oracle|
+# bfloat16 activations: the output's own rounding is at most 2^-9 |o|, and
+# the P*V contraction takes P rounded to bfloat16 (relative error 2^-9 per
+# weight) while the denominator sums the unrounded P, so the output moves by
+# at most 2^-9 max|V| (|V| < 8 for the N(0,1) draws); hence
+# |gpu - oracle| <= 2^-6 + 2^-8 |oracle|.
+RTOL_BF16, ATOL_BF16 = 2.0 ** -8, 2.0 ** -6
+
+
+def tolerance(step):
+    """(rtol, atol) for a step's output."""
+    if step.get("cache_dtype", 0) == workloads.CACHE_BF16:
+        return RTOL_BF16, ATOL_BF16
+    return RTOL, ATOL
+
+
+def out_dtype(step):
+    return torch.bfloat16 if step.get("cache_dtype", 0) == workloads.CACHE_BF16 else torch.float16
 
 
 def bits(t):
@@ -44,20 +61,22 @@ def run(step, options=(), max_batch=None, max_tokens=None, **bounds):
         op.set_option(k, v)
     width = step.get("v_head_size") or step["head_size"]
     out = torch.full((step["token_count"], step["num_heads"] * width), float("nan"),
-                     dtype=torch.float16, device=step["query"].device)
+                     dtype=out_dtype(step), device=step["query"].device)
     op.forward(step, out)
     torch.cuda.synchronize()
     err = op.device_error()
     return op, out, err
 
 
-def assert_close(got, ref, what="output"):
+def assert_close(got, ref, what="output", rtol=RTOL, atol=ATOL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape
+    # (a NaN reference would pass every comparison below vacuously)
+    assert not np.isnan(ref).any(), f"{what}: NaN in the oracle's result (the step reads a NaN input)"
     assert not np.isnan(got).any(), f"{what}: NaN in GPU result"
     diff = np.abs(got - ref)
-    bad = diff > ATOL + RTOL * np.abs(ref)
+    bad = diff > atol + rtol * np.abs(ref)
     big = np.abs(ref) >= 1e-3
     rel = (diff[big] / np.abs(ref[big])).max() if big.any() else 0.0
     assert not bad.any(), (f"{what}: {bad.sum()} of {bad.size} elements outside tolerance; "
@@ -73,7 +92,8 @@ def check_full(step_host, step_dev, out, threads=8):
         assert np.array_equal(raw(step_dev["value_cache"]), raw(ref["value_cache"])), "value_cache pool differs"
     T, H = step_host["token_count"], step_host["num_heads"]
     D = step_host.get("v_head_size") or step_host["head_size"]
-    return assert_close(out.float().cpu().numpy().reshape(T, H, D), ref["out"])
+    rtol, atol = tolerance(step_host)
+    return assert_close(out.float().cpu().numpy().reshape(T, H, D), ref["out"], rtol=rtol, atol=atol)
 
 
 def check_sampled(step_host, step_dev, out, n_rows=192, seed=0, threads=16):
@@ -100,4 +120,5 @@ def check_rows(step_host, step_dev, out, rows, threads=16):
                          v_scale=step_host.get("v_scale"), per_channel=step_host.get("quant_type", 0) == 2,
                          head_sink=step_host.get("head_sink"))
     got = out.float().cpu().numpy().reshape(T * H, D)[rows]
-    return assert_close(got, o)
+    rtol, atol = tolerance(step_host)
+    return assert_close(got, o, rtol=rtol, atol=atol)

@@ -73,10 +73,15 @@ def test_config_rule(field, value, status, word):
 
 
 @pytest.mark.parametrize("over,status,word", [
-    (dict(cache_dtype=3), pa.PA_INVALID_ARGUMENT, "cache_dtype"),
+    (dict(cache_dtype=4), pa.PA_INVALID_ARGUMENT, "cache_dtype"),
+    (dict(cache_dtype=-1), pa.PA_INVALID_ARGUMENT, "cache_dtype"),
     (dict(k_quant_type=4), pa.PA_INVALID_ARGUMENT, "k_quant_type"),
     (dict(k_quant_type=pa.PA_QUANT_PER_TENSOR, v_quant_type=pa.PA_QUANT_PER_TENSOR),
-     pa.PA_INVALID_ARGUMENT, "fp16 cache"),
+     pa.PA_INVALID_ARGUMENT, "16-bit cache"),
+    (dict(cache_dtype=pa.PA_CACHE_BF16, k_quant_type=pa.PA_QUANT_PER_TENSOR, v_quant_type=pa.PA_QUANT_PER_TENSOR),
+     pa.PA_INVALID_ARGUMENT, "16-bit cache"),
+    (dict(cache_dtype=pa.PA_CACHE_BF16, packed_qkv=1), pa.PA_NOT_SUPPORTED, "bfloat16"),
+    (dict(cache_dtype=pa.PA_CACHE_BF16, qk_norm=1), pa.PA_NOT_SUPPORTED, "bfloat16"),
     (dict(cache_dtype=pa.PA_CACHE_INT8), pa.PA_INVALID_ARGUMENT, "8-bit cache needs"),
     (dict(cache_dtype=pa.PA_CACHE_INT8, k_quant_type=pa.PA_QUANT_PER_TENSOR,
           v_quant_type=pa.PA_QUANT_PER_CHANNEL, max_query_len_bound=1), pa.PA_NOT_SUPPORTED, "must match"),
@@ -90,6 +95,14 @@ def test_config_rule(field, value, status, word):
 def test_quantized_cache_rules(over, status, word):
     st, msg = pa.pa_validate_config(good(**over))
     assert st == status and word in msg, (st, msg)
+
+
+def test_bf16_config_passes_and_latent_rejects_it():
+    assert pa.pa_validate_config(good(cache_dtype=pa.PA_CACHE_BF16)) == (pa.PA_OK, "ok")
+    cfg = pa.make_config(128, 1, 576, 64, 100, 8, 4, 4, scale=0.1, cache_dtype=pa.PA_CACHE_BF16,
+                         kv_cache_layout=pa.PA_LAYOUT_LATENT, v_head_size=512)
+    st, msg = pa.pa_validate_config(cfg)
+    assert st == pa.PA_NOT_SUPPORTED and "fp16" in msg, (st, msg)
 
 
 @pytest.mark.parametrize("over,status,word", [
@@ -164,6 +177,17 @@ def test_no_alloc_rejects_latent_layout():
                                       None, None, P(a["output"]), None, ctypes.c_void_p(0))
     assert st == pa.PA_NOT_SUPPORTED
     assert "latent" in pa.lib().pa_last_error_message(None).decode()
+
+
+def test_no_alloc_rejects_bf16_cache():
+    a = step_args()
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    st = pa.lib().pa_forward_no_alloc(ctypes.byref(good(cache_dtype=pa.PA_CACHE_BF16)), P(a["query"]), P(a["key"]),
+                                      P(a["value"]), P(a["key_cache"]), P(a["value_cache"]), P(a["block_table"]),
+                                      P(a["cumulative_sequence_lengths"]), P(a["past_sequence_lengths"]), 4, 4,
+                                      None, None, P(a["output"]), None, ctypes.c_void_p(0))
+    assert st == pa.PA_NOT_SUPPORTED
+    assert "bfloat16" in pa.lib().pa_last_error_message(None).decode()
 
 
 def test_quantized_decode_config_passes():

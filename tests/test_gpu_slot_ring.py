@@ -68,6 +68,14 @@ def test_slot_mapping_skips_and_redirects(cache):
     # token 0: redirected into a block no table row names; token 1: no write;
     # token 2: its derived slot
     s = _derived_slots(step)
+    # the derived slots of tokens 0 and 1 are not written but still read
+    # through the block table (the tokens' own positions): give them finite
+    # stale content instead of the NaN sentinel
+    for slot in s[:2].tolist():
+        for pool in (step["key_cache"], step["value_cache"]):
+            row = pool.view(-1, *pool.shape[2:])[slot]
+            row.copy_(torch.randn(row.shape, generator=torch.Generator().manual_seed(slot)).to(row.device).to(
+                row.dtype) if cache == "fp16" else torch.randint(0, 0x70, row.shape, dtype=torch.uint8).to(row.device))
     s[0], s[1] = spare * bs + 3, -1
     step["slot_mapping"] = s.cuda()
     host = host_copy(step)
