@@ -68,6 +68,14 @@ def decode_rows(G):
 # 8-bit cache variants of the Llama-3-8B-shaped decode step (per-channel
 # scales, the quantized cache of the CUDA design, section 8)
 QUANT_WORKLOADS = {"decode_fp8": 2, "decode_int8": 1}
+# bfloat16 activations and cache (the CUDA design registers the kernel for
+# fp16 and bfloat16 activations, section 8.2) on the fp16 workloads' shapes
+BF16_WORKLOADS = {"decode_bf16": "decode", "mixed_bf16": "mixed", "prefill_bf16": "prefill"}
+CACHE_BF16 = 3
+
+
+def quantized(step):
+    return step.get("cache_dtype", 0) in (1, 2)
 
 
 MLA_SCALE = 0.0723  # an explicit softmax scale (the latent width is not the model's head width)
@@ -80,6 +88,8 @@ def workload_shape(name):
     index = {"tiny": 0, "decode": 1, "mixed": 2, "long_window": 3, "rotary_decode": 4}
     if name in QUANT_WORKLOADS:
         return workloads.config_shape(1)
+    if name in BF16_WORKLOADS:
+        return workload_shape(BF16_WORKLOADS[name])
     if name == "mla_decode":
         g = torch.Generator().manual_seed(3000 + 77)
         past = torch.randint(512, 4097, (64,), generator=g).tolist()
@@ -97,12 +107,16 @@ def workload_options(name):
     """make_step keywords of a workload (8-bit cache variants)."""
     if name in QUANT_WORKLOADS:
         return dict(cache_dtype=QUANT_WORKLOADS[name], quant_type=2)
+    if name in BF16_WORKLOADS:
+        return dict(cache_dtype=CACHE_BF16)
     if name == "mla_decode":
         return dict(latent_v_head_size=512)
     return {}
 
 
 def shape_name(name, shape):
+    if name in BF16_WORKLOADS:
+        return shape.name + "_bf16"
     return shape.name + ({2: "_e4m3_cache", 1: "_int8_cache"}[QUANT_WORKLOADS[name]] if name in QUANT_WORKLOADS else "")
 
 
@@ -121,7 +135,7 @@ def work_of(step, seqs=None):
     past, q = seq_lengths(step)
     W, G = step["local_window_size"], step["num_heads"] // step["kv_num_heads"]
     Hk, H, D = step["kv_num_heads"], step["num_heads"], step["head_size"]
-    eb = 1 if step.get("cache_dtype", 0) else 2  # bytes per cache element
+    eb = 1 if quantized(step) else 2  # bytes per cache element
     latent = step.get("kv_cache_layout", 0) == 1
     Dv = step.get("v_head_size") or D
     w = dict(kv_bytes=0, dec_kv_bytes=0, dec_qo_bytes=0, pre_flops=0, tokens=0, dec_flops=0)
@@ -137,7 +151,7 @@ def work_of(step, seqs=None):
             w["dec_kv_bytes"] += kv
             w["dec_qo_bytes"] += q[b] * H * (D + Dv) * 2
             w["dec_flops"] += 2 * q[b] * H * adm * (D + Dv)
-        elif q[b] * G <= decode_rows(G) or step.get("cache_dtype", 0):
+        elif q[b] * G <= decode_rows(G) or quantized(step):
             w["dec_kv_bytes"] += kv
             w["dec_qo_bytes"] += 2 * q[b] * H * D * 2
         else:
@@ -329,7 +343,8 @@ def run_ours(args, rank, world, local_rank):
     # decode step it lets the host skip launching the prefill kernel.
     op = pa.PagedAttention.for_step(step, max_query_len_bound=max(qlens))
     out_width = step["num_heads"] * (step.get("v_head_size") or step["head_size"])
-    out = torch.empty(step["token_count"], out_width, dtype=torch.float16, device=dev)
+    out = torch.empty(step["token_count"], out_width, device=dev,
+                      dtype=torch.bfloat16 if step.get("cache_dtype", 0) == CACHE_BF16 else torch.float16)
     # A stream of the step's own (as a serving loop has): work on the legacy
     # default stream carries its implicit synchronisation with every other
     # blocking stream (measured: the decode step 104.4 us there, 98.9 us here).
@@ -434,7 +449,7 @@ def run_ours(args, rank, world, local_rank):
     if ker_ms[pa.PA_STAGE_DECODE] and work["dec_kv_bytes"]:
         t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
         alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
-        ct = {0: "", 1: ", int8", 2: ", e4m3"}[host.get("cache_dtype", 0)]
+        ct = {0: "", 1: ", int8", 2: ", e4m3", 3: ", bf16"}[host.get("cache_dtype", 0)]
         latent = host.get("kv_cache_layout", 0) == 1
         latent_tc = latent and shape.num_heads % 128 == 0  # the tcgen05 latent kernel serves these
         kname = (("mla_tc_kernel" if latent_tc else "mla_decode_kernel") if latent
@@ -460,13 +475,15 @@ def run_ours(args, rank, world, local_rank):
         ach = work["pre_flops"] / (t * 1e-3) / 1e12
         # head_size 64/128 run the two-tile kernel, 256 the one-tile kernel
         pair = shape.head_size <= 128
+        bf = ", bf16" if host.get("cache_dtype", 0) == CACHE_BF16 else ""
         rooflines["prefill"] = {
             "bound": "tensor",
-            "kernel": f"prefill_pair_kernel<{shape.head_size}>" if pair else f"prefill_kernel<{shape.head_size}>",
+            "kernel": (f"prefill_pair_kernel<{shape.head_size}{bf}>" if pair
+                       else f"prefill_kernel<{shape.head_size}{bf}>"),
             "achieved": ach, "peak": tflops,
             "peak_kind": f"{peak_kind} bf16 matmul burst; fp16 has the same nominal dense rate",
             "unit": "TFLOP/s", "frac": ach / tflops,
-            "traffic": committed_traffic("prefill_pair.cu" if pair else "prefill.cu", shape.name),
+            "traffic": committed_traffic("prefill_pair.cu" if pair else "prefill.cu", shape_name(args.workload, shape)),
             "algorithmic_flops_per_launch": work["pre_flops"], "launch_ms": t}
     dominant = max(rooflines, key=lambda k: rooflines[k]["launch_ms"]) if rooflines else None
 
@@ -501,7 +518,8 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "bf16" if host.get("cache_dtype", 0) == CACHE_BF16 else "f16",
+        "data": "synthetic",
         "config": {"workload": shape_name(args.workload, shape), "batch": shape.batch,
                    "token_count": shape.token_count,
                    "num_heads": shape.num_heads, "kv_num_heads": shape.kv_num_heads,
@@ -547,7 +565,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed",
                     choices=["decode", "mixed", "long_window", "rotary_decode", "prefill", "tiny"]
-                    + sorted(QUANT_WORKLOADS) + ["mla_decode"])
+                    + sorted(QUANT_WORKLOADS) + sorted(BF16_WORKLOADS) + ["mla_decode"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch pa_forward directly instead of a graph replay")
     ap.add_argument("--soak-s", type=float, default=1.5, help="seconds of untimed replays under the clock sampler")
