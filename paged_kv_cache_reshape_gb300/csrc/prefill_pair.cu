@@ -487,16 +487,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t nv = 2 * (g + i) + 1, tile = g + i;
         const int sv = nv % S;
         const int key0 = key_lo + i * kKeys;
-        // s_full(i) also covers PV(i-1): MMAs complete in issue order.  The
-        // page mask was published before the tile's K load.
-        if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err, p.err_site, kSitePrefillPair | 5) ||
-            !wait_or_abort(&ctl->mask_full[tile % kMaskRing], (tile / kMaskRing) & 1, abort, p.err, p.err_site, kSitePrefillPair | 6)) {
+        // The page mask was published before the tile's K load: it is read
+        // before the wait for S, which hides the shared-memory load (read
+        // after it, the load stalled the diagonal tile's rows for ~1800
+        // cycles while the next unit's Q tile streamed in).  s_full(i) also
+        // covers PV(i-1): MMAs complete in issue order.
+        if (!wait_or_abort(&ctl->mask_full[tile % kMaskRing], (tile / kMaskRing) & 1, abort, p.err, p.err_site,
+                           kSitePrefillPair | 6)) {
+          ok = false;
+          break;
+        }
+        const uint32_t mask = ctl->kv_mask[tile % kMaskRing];
+        if (!wait_or_abort(&ctl->s_full[X], scnt & 1, abort, p.err, p.err_site, kSitePrefillPair | 5)) {
           ok = false;
           break;
         }
         ++scnt;
         tc_fence_after();
-        const uint32_t mask = ctl->kv_mask[tile % kMaskRing];
 #pragma unroll
         for (int c = 0; c < kKeys; c += 32) tmem_ld32(lane_addr + C::s_col(X) + c, x + c);
         tmem_ld_wait();
