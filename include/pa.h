@@ -119,9 +119,9 @@ enum {
  * then bfloat16 wherever this header says fp16.  Rotary rounds each rotated
  * value to bfloat16 (nearest-even) after the same fp32 arithmetic; the
  * attention contractions take bfloat16 operands (the softmax weights P are
- * rounded to bfloat16 for the P*V contraction) with fp32 accumulation.
- * Built for separate caches without packed_qkv or qk_norm; the latent
- * layout and pa_forward_no_alloc are fp16 only (PA_NOT_SUPPORTED). */
+ * rounded to bfloat16 for the P*V contraction) with fp32 accumulation;
+ * QK-Norm weights are bfloat16 and its outputs rounded to bfloat16.  The
+ * latent layout and pa_forward_no_alloc are fp16 only (PA_NOT_SUPPORTED). */
 enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2, PA_CACHE_BF16 = 3 };
 /* Cache layout (section 12).  LATENT: one cache key_cache [NB, bs, 1, D] of
  * latent rows (value and value_cache NULL, kv_num_heads 1); every query
@@ -183,7 +183,7 @@ PA_API void pa_config_init(pa_config* cfg);
  * through the decode kernel: a sequence whose q_len * num_heads /
  * kv_num_heads rows exceed one 16-row item runs in chunks of
  * 16 * kv_num_heads / num_heads tokens, section 8.5); a bfloat16 cache
- * with packed_qkv, qk_norm or the latent layout.  Touches no GPU. */
+ * with the latent layout.  Touches no GPU. */
 PA_API pa_status pa_validate_config(const pa_config* cfg, char* msg, size_t msg_len);
 
 /* Host-only check of one step's arguments (token_count <= max_tokens,

@@ -85,6 +85,8 @@ def lib():
             L.oracle_double_to_bf16.restype = ctypes.c_uint16
             L.oracle_rotary_bf16.argtypes = [P, P, I, I, I, P, P, I, P, P, I, I, I, I]
             L.oracle_rotary_bf16.restype = I
+            L.oracle_qk_norm_bf16.argtypes = [P, P, I, I, I, P, ctypes.c_float]
+            L.oracle_qk_norm_bf16.restype = I
             _lib = L
     return _lib
 
@@ -149,12 +151,14 @@ def quantize(bits: np.ndarray, scale: float, cache_dtype: int) -> np.ndarray:
     return f(np.asarray(bits, dtype=np.uint16))
 
 
-def qk_norm(x, nheads, head_size, weight, eps):
-    """Per-head RMS-normalized copy of x ([T, nheads*D] fp16 bits)."""
+def qk_norm(x, nheads, head_size, weight, eps, bf16=False):
+    """Per-head RMS-normalized copy of x ([T, nheads*D] fp16 bits, or
+    bfloat16 bits with a bfloat16 weight when bf16)."""
     xa = _np(x, np.uint16)
     wa = _np(weight, np.uint16)
     y = np.empty_like(xa)
-    _check(lib().oracle_qk_norm(_p(xa), _p(y), xa.shape[0], nheads, head_size, _p(wa), float(eps)), "qk_norm")
+    fn = lib().oracle_qk_norm_bf16 if bf16 else lib().oracle_qk_norm
+    _check(fn(_p(xa), _p(y), xa.shape[0], nheads, head_size, _p(wa), float(eps)), "qk_norm")
     return y
 
 
@@ -338,8 +342,9 @@ def forward(step, threads=None, rows=None):
         q, k, v = _np(step["query"], np.uint16), _np(step["key"], np.uint16), _np(step["value"], np.uint16)
     if step.get("q_norm_weight") is not None:
         eps = step.get("qk_norm_epsilon", 1e-6)
-        q = qk_norm(q, H, D, step["q_norm_weight"], eps)
-        k = qk_norm(k, Hk, D, step["k_norm_weight"], eps)
+        bf = step.get("cache_dtype", CACHE_FP16) == CACHE_BF16
+        q = qk_norm(q, H, D, step["q_norm_weight"], eps, bf16=bf)
+        k = qk_norm(k, Hk, D, step["k_norm_weight"], eps, bf16=bf)
     cdt = step.get("cache_dtype", CACHE_FP16)
     if step["do_rotary"]:
         off = step.get("rotary_offset", 0)  # first rotated channel of a head

@@ -354,7 +354,8 @@ static int rotary_impl(const uint16_t* x, uint16_t* y, int T, int nheads, int D,
  * over the channels in ascending order, one rounding per square and per
  * add.  The mean is the sum times 1/D (exact: D is a power of two), then
  * + eps, IEEE square root, IEEE reciprocal. */
-int oracle_qk_norm(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const uint16_t* w, float eps) {
+static int qk_norm_impl(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const uint16_t* w, float eps,
+                        int bf16) {
   if (D <= 0 || D > 1024 || (D & (D - 1)) != 0) return ORACLE_BAD_ARGUMENT;
   for (int t = 0; t < T; ++t) {
     for (int h = 0; h < nheads; ++h) {
@@ -362,7 +363,7 @@ int oracle_qk_norm(const uint16_t* x, uint16_t* y, int T, int nheads, int D, con
       uint16_t* yr = y + ((size_t)t * nheads + h) * D;
       float sum = 0.0f;
       for (int c = 0; c < D; ++c) {
-        float v = (float)oracle_half_to_double(xr[c]);
+        float v = (float)elem16_to_double(xr[c], bf16);
         float sq = v * v;
         sum = sum + sq;
       }
@@ -371,14 +372,24 @@ int oracle_qk_norm(const uint16_t* x, uint16_t* y, int T, int nheads, int D, con
       float r = 1.0f / sqrtf(v);
       uint16_t tmp[1024];
       for (int c = 0; c < D; ++c) {
-        float a = (float)oracle_half_to_double(xr[c]) * r;
-        float b = a * (float)oracle_half_to_double(w[c]);
-        tmp[c] = oracle_double_to_half((double)b);
+        float a = (float)elem16_to_double(xr[c], bf16) * r;
+        float b = a * (float)elem16_to_double(w[c], bf16);
+        tmp[c] = bf16 ? oracle_double_to_bf16((double)b) : oracle_double_to_half((double)b);
       }
       memcpy(yr, tmp, sizeof(uint16_t) * D);
     }
   }
   return ORACLE_OK;
+}
+
+int oracle_qk_norm(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const uint16_t* w, float eps) {
+  return qk_norm_impl(x, y, T, nheads, D, w, eps, 0);
+}
+
+/* The same normalization of bfloat16 rows with a bfloat16 weight, each
+ * output rounded to bfloat16 to nearest-even. */
+int oracle_qk_norm_bf16(const uint16_t* x, uint16_t* y, int T, int nheads, int D, const uint16_t* w, float eps) {
+  return qk_norm_impl(x, y, T, nheads, D, w, eps, 1);
 }
 
 /* ---- reshape_and_cache (CUDA design section 5.1 derived slot, 5.2

@@ -392,10 +392,6 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
     set_msg(msg, len, "qk_norm is built for kv_num_heads <= 32 (got %d)", c->kv_num_heads);
     return PA_NOT_SUPPORTED;
   }
-  if (c->cache_dtype == PA_CACHE_BF16 && (c->packed_qkv || c->qk_norm)) {
-    set_msg(msg, len, "bfloat16 activations are built without packed_qkv and qk_norm");
-    return PA_NOT_SUPPORTED;
-  }
   if (quantized(c->cache_dtype)) {
     if (c->k_quant_type != c->v_quant_type) {
       set_msg(msg, len, "k_quant_type and v_quant_type must match in this library");

@@ -34,7 +34,7 @@
 // squares as one running sum over the channels in ascending order (one
 // lane per head, one rounding per square and per add, no fused
 // multiply-add; IEEE square root and reciprocal), and every loaded channel
-// becomes fp16((x * r) * w).
+// becomes fp16((x * r) * w) (bfloat16 with bfloat16 activations).
 // Packed QKV rows (section 4) are read in place: Q, K and V heads of token
 // t start at t*(H+2Hk)*D, + H*D and + (H+Hk)*D.
 #include <algorithm>
@@ -118,8 +118,10 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
 
 // QK-Norm factors of the nheads (<= 32) heads of one row: lane h sums the
 // squares of head h as one running fp32 sum in channel order (the order
-// stated at the top of the file), then stores rn[h].
-__device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, float eps, float* rn, int lane) {
+// stated at the top of the file), then stores rn[h].  bf16: the row holds
+// bfloat16.
+__device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, float eps, float* rn, int lane,
+                             bool bf16) {
   if (lane < nheads) {
     const __half* x = src + (size_t)lane * D;
     float acc = 0.f;
@@ -128,7 +130,7 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
       v.u = __ldg(reinterpret_cast<const uint4*>(x + c));
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const float f = __half2float(v.h[e]);
+        const float f = elem16_to_float(v.h[e], bf16);
         acc = __fadd_rn(acc, __fmul_rn(f, f));
       }
     }
@@ -143,8 +145,8 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
 // nw (the [D] weight), every loaded value is first normalized.  R % 16 == 0
 // is checked on the host.  Channels outside [keep_lo, keep_hi) that are not
 // rotated are not emitted at all (a latent query's copy keeps only the
-// 64-channel chunks that hold its rotated channels).  bf16: the row and the
-// tables hold bfloat16 (rotation only; QK-Norm is fp16).
+// 64-channel chunks that hold its rotated channels).  bf16: the row, the
+// weight and the tables hold bfloat16.
 template <typename Emit>
 __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
                               int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
@@ -161,7 +163,8 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
       w.u = __ldg(reinterpret_cast<const uint4*>(nw + ch));
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        v.h[e] = __float2half_rn(__fmul_rn(__fmul_rn(__half2float(v.h[e]), r), __half2float(w.h[e])));
+        v.h[e] = float_to_elem16(__fmul_rn(__fmul_rn(elem16_to_float(v.h[e], bf16), r), elem16_to_float(w.h[e], bf16)),
+                                 bf16);
     }
     return v;
   };
@@ -268,7 +271,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     const size_t qoff = ((size_t)t * p.H + h0) * p.D;
     const float* qrn = nullptr;
     if (p.qk_norm) {
-      norm_factors(qsrc, nh, p.D, p.qk_eps, rn, lane);
+      norm_factors(qsrc, nh, p.D, p.qk_eps, rn, lane, p.cache_type == kCacheBF16);
       qrn = rn;
     }
     if (p.q_scale)
@@ -319,7 +322,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     if ((part & 1) == 0) {
       const float* krn = nullptr;
       if (p.qk_norm) {
-        norm_factors(ksrc + (size_t)h0 * p.D, nh, p.D, p.qk_eps, rn, lane);
+        norm_factors(ksrc + (size_t)h0 * p.D, nh, p.D, p.qk_eps, rn, lane, false);
         krn = rn;
       }
       row_transform(ksrc + (size_t)h0 * p.D,
@@ -337,7 +340,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   }
   const float* krn = nullptr;
   if (p.qk_norm) {
-    norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane);
+    norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane, p.cache_type == kCacheBF16);
     krn = rn;
   }
   if (p.cache_type == kCacheF16 || p.cache_type == kCacheBF16) {

@@ -80,8 +80,6 @@ def test_config_rule(field, value, status, word):
      pa.PA_INVALID_ARGUMENT, "16-bit cache"),
     (dict(cache_dtype=pa.PA_CACHE_BF16, k_quant_type=pa.PA_QUANT_PER_TENSOR, v_quant_type=pa.PA_QUANT_PER_TENSOR),
      pa.PA_INVALID_ARGUMENT, "16-bit cache"),
-    (dict(cache_dtype=pa.PA_CACHE_BF16, packed_qkv=1), pa.PA_NOT_SUPPORTED, "bfloat16"),
-    (dict(cache_dtype=pa.PA_CACHE_BF16, qk_norm=1), pa.PA_NOT_SUPPORTED, "bfloat16"),
     (dict(cache_dtype=pa.PA_CACHE_INT8), pa.PA_INVALID_ARGUMENT, "8-bit cache needs"),
     (dict(cache_dtype=pa.PA_CACHE_INT8, k_quant_type=pa.PA_QUANT_PER_TENSOR,
           v_quant_type=pa.PA_QUANT_PER_CHANNEL, max_query_len_bound=1), pa.PA_NOT_SUPPORTED, "must match"),
@@ -99,6 +97,7 @@ def test_quantized_cache_rules(over, status, word):
 
 def test_bf16_config_passes_and_latent_rejects_it():
     assert pa.pa_validate_config(good(cache_dtype=pa.PA_CACHE_BF16)) == (pa.PA_OK, "ok")
+    assert pa.pa_validate_config(good(cache_dtype=pa.PA_CACHE_BF16, packed_qkv=1, qk_norm=1)) == (pa.PA_OK, "ok")
     cfg = pa.make_config(128, 1, 576, 64, 100, 8, 4, 4, scale=0.1, cache_dtype=pa.PA_CACHE_BF16,
                          kv_cache_layout=pa.PA_LAYOUT_LATENT, v_head_size=512)
     st, msg = pa.pa_validate_config(cfg)

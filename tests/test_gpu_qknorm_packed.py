@@ -54,3 +54,18 @@ def test_qk_norm_packed_over_8bit_cache(cache_dtype):
     _, out, err = run(step, max_query_len_bound=2)
     assert err == 0
     check_full(host, step, out)
+
+
+@pytest.mark.parametrize("mode", ["qk_norm", "packed", "packed_qk_norm"])
+@pytest.mark.parametrize("shape", [SHAPES[0], SHAPES[2], SHAPES[3], SHAPES[4]], ids=lambda s: s.name)
+def test_fused_prologue_bf16(shape, mode):
+    """The same prologue on bfloat16 rows (bfloat16 weights, one bfloat16
+    rounding per normalized and rotated value), on the decode kernel and
+    both prefill kernels."""
+    step = make(shape, device="cuda", gen_device="cpu", cache_dtype=workloads.CACHE_BF16, qk_norm="qk_norm" in mode,
+                packed_qkv="packed" in mode)
+    host = host_copy(step)
+    _, out, err = run(step)
+    assert err == 0
+    assert out.dtype == torch.bfloat16
+    check_full(host, step, out)

@@ -227,3 +227,54 @@ def test_bf16_step_writes_rotated_key_and_value_bits():
     # rotation changed something away from position 0, and the output is finite
     assert not np.array_equal(k_rot[2:], bits(st["key"])[2:])
     assert np.isfinite(r["out"]).all()
+
+
+# --------------------------------------------------------------- QK-Norm -----
+
+def test_bf16_qk_norm_matches_torch_rms_norm():
+    """bfloat16 QK-Norm: fp32 arithmetic, one bfloat16 rounding: within one
+    bfloat16 ulp of torch's rms_norm evaluated in fp64 (a weight or an
+    epsilon left out, or an fp16 rounding, would miss it)."""
+    g = torch.Generator().manual_seed(7)
+    for D, nh in ((64, 3), (128, 4), (256, 2)):
+        x = (torch.randn(7, nh * D, generator=g) * (0.1 + 3 * torch.rand(7, 1, generator=g))).bfloat16()
+        w = (1 + 0.5 * torch.randn(D, generator=g)).bfloat16()
+        got = from_bits(oracle.qk_norm(bits(x), nh, D, bits(w), 1e-6, bf16=True)).double().numpy()
+        ref = F.rms_norm(x.double().view(7, nh, D), (D,), w.double(), eps=1e-6).view(7, nh * D).numpy()
+        assert np.all(np.abs(got - ref) <= _ulp_bf16(ref) + 1e-30)
+        assert np.array_equal(got, from_bits(oracle.double_to_bf16_bits(got)).double().numpy())
+
+
+def test_bf16_qk_norm_constant_rows_closed_form():
+    D = 128
+    for a in (2.0, -0.375, 17.0):
+        x = torch.full((1, D), a).bfloat16()
+        w = torch.ones(D).bfloat16()
+        got = from_bits(oracle.qk_norm(bits(x), 1, D, bits(w), 1e-6, bf16=True)).double().numpy()
+        ref = torch.tensor(a / math.sqrt(a * a + 1e-6)).bfloat16().double().item()
+        assert np.all(got == ref), (a, got[0, 0], ref)
+
+
+def test_bf16_packed_qk_norm_step_pools():
+    """A bfloat16 step with packed QKV rows and QK-Norm: the key pool holds
+    the normalized, rotated K rows and the value pool the V bits."""
+    shape = workloads.custom_shape("bf16_pk", 4, 2, 64, 16, [3, 20], [2, 1], do_rotary=1, seed=9)
+    st = workloads.make_step(shape, cache_dtype=BF16, qk_norm=True, packed_qkv=True)
+    assert st["key"] is None and st["q_norm_weight"].dtype == torch.bfloat16
+    r = oracle.forward(st)
+    q, k, v = oracle.split_packed_qkv(st["query"], 4, 2, 64)
+    kn = oracle.qk_norm(k, 2, 64, st["k_norm_weight"], 1e-6, bf16=True)
+    kr = oracle.rotary(kn, st["cumulative_sequence_lengths"], st["past_sequence_lengths"], st["cos_cache"],
+                       st["sin_cache"], 2, 64, 0, bf16=True)
+    assert np.array_equal(r["key_rot"], kr)
+    bt = st["block_table"].numpy()
+    kc = r["key_cache"].reshape(st["num_blocks"], 16, 128)
+    vc = r["value_cache"].reshape(st["num_blocks"], 16, 128)
+    t = 0
+    for b, (p0, n) in enumerate(zip([3, 20], [2, 1])):
+        for j in range(n):
+            pos = p0 + j
+            assert np.array_equal(kc[bt[b, pos // 16], pos % 16], kr[t])
+            assert np.array_equal(vc[bt[b, pos // 16], pos % 16], v[t])
+            t += 1
+    assert np.isfinite(r["out"]).all()

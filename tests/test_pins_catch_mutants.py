@@ -56,9 +56,11 @@ MUTANTS = [
     ("K quantized with the V scale", "oracle_quantize(key[(size_t)t * row + e], k_scale[si]",
      "oracle_quantize(key[(size_t)t * row + e], v_scale[si]", 1, None),
     ("QK-Norm without epsilon", "float v = mean + eps;", "float v = mean;", 1, None),
-    ("QK-Norm without weight", "float b = a * (float)oracle_half_to_double(w[c]);", "float b = a;", 1, None),
-    ("QK-Norm sum from the last channel", "for (int c = 0; c < D; ++c) {\n        float v = (float)oracle_half_to_double(xr[c]);",
-     "for (int c = D - 1; c >= 0; --c) {\n        float v = (float)oracle_half_to_double(xr[c]);", 1, None),
+    ("QK-Norm without weight", "float b = a * (float)elem16_to_double(w[c], bf16);", "float b = a;", 1, None),
+    ("QK-Norm sum from the last channel", "for (int c = 0; c < D; ++c) {\n        float v = (float)elem16_to_double(xr[c], bf16);",
+     "for (int c = D - 1; c >= 0; --c) {\n        float v = (float)elem16_to_double(xr[c], bf16);", 1, None),
+    ("bfloat16 QK-Norm rounded to fp16", "tmp[c] = bf16 ? oracle_double_to_bf16((double)b)",
+     "tmp[c] = 0 ? oracle_double_to_bf16((double)b)", 1, None),
     ("QK-Norm sum in fp64", "float sum = 0.0f;", "double sum = 0.0;", 1, None),
     ("latent V from the last channels", "o[c] += w * oracle_half_to_double(lr[c]);",
      "o[c] += w * oracle_half_to_double(lr[c + D - Dv]);", 1, None),

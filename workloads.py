@@ -157,8 +157,8 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     and block tables (drawn on the CPU) but not necessarily values.
     cache_dtype / quant_type select 8-bit pools with their scales, or
     (CACHE_BF16) bfloat16 activations and pools; head_sink
-    adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16,
-    1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
+    adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16 or
+    bfloat16, 1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
     query tensor with key and value None.  latent_v_head_size > 0 makes a
     multi-head latent attention step (CUDA design section 12): one kv head,
     key rows of head_size latent channels, value and value_cache None, V the
@@ -264,8 +264,8 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
         out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).to(act).to(device))
     if qk_norm:
         ng = torch.Generator().manual_seed(6000 + shape.seed)
-        out.update(q_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).half().to(device),
-                   k_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).half().to(device),
+        out.update(q_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).to(act).to(device),
+                   k_norm_weight=(1.0 + 0.3 * torch.randn(D, generator=ng)).to(act).to(device),
                    qk_norm_epsilon=1e-6)
     if packed_qkv:
         out.update(query=torch.cat([out["query"], out["key"], out["value"]], dim=1).contiguous(),
