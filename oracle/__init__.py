@@ -8,7 +8,9 @@ rotary keeps one rounding per operation) into liboracle.so beside it.
 Arrays cross the boundary as numpy buffers; fp16 and bfloat16 tensors travel
 as their uint16 bit patterns.  A step whose cache_dtype is CACHE_BF16 has
 bfloat16 activations throughout (query, key, value, both pools, the rotary
-tables and head_sink).
+tables and head_sink); a step with an 8-bit cache and "act_bf16" set has
+bfloat16 activations over 8-bit pools (ACT_BF16 is then added to the cache
+type handed to the C functions).
 """
 
 from __future__ import annotations
@@ -31,6 +33,13 @@ _lib = None
 
 OK, BAD_ARGUMENT, BAD_DEVICE_DATA = 0, 1, 2
 CACHE_FP16, CACHE_INT8, CACHE_FP8, CACHE_BF16 = 0, 1, 2, 3
+ACT_BF16 = 16  # added to an 8-bit cache type: bfloat16 activations
+
+
+def act_bf16(step) -> bool:
+    """True when the step's activations (query, key, value, tables, sink,
+    norm weights and the output) are bfloat16."""
+    return step.get("cache_dtype", CACHE_FP16) == CACHE_BF16 or bool(step.get("act_bf16", False))
 
 
 def build(force: bool = False) -> str:
@@ -145,7 +154,8 @@ def float_to_e4m3(x: np.ndarray) -> np.ndarray:
 
 
 def quantize(bits: np.ndarray, scale: float, cache_dtype: int) -> np.ndarray:
-    """8-bit codes of fp16 values (bit patterns) under one scale."""
+    """8-bit codes of fp16 values (bit patterns; bfloat16 with ACT_BF16 added
+    to cache_dtype) under one scale."""
     f = np.vectorize(lambda h: lib().oracle_quantize(int(h), float(scale), int(cache_dtype)),
                      otypes=[np.uint8])
     return f(np.asarray(bits, dtype=np.uint16))
@@ -227,7 +237,8 @@ def cache_write(key, value, key_cache, value_cache, block_table, cum, past,
     key/value are fp16 bit arrays [T, Hk*D] (key already rotated when rotary
     is on); the input caches are copied, not modified.  With an 8-bit
     cache_dtype the caches are uint8 code arrays and k_scale / v_scale fp32
-    arrays ([1], or [Hk*D] when per_channel).  slot_mapping ([T] int32, -1 =
+    arrays ([1], or [Hk*D] when per_channel); ACT_BF16 added to it reads key
+    and value as bfloat16 bits.  slot_mapping ([T] int32, -1 =
     no write) replaces the slot derivation when given."""
     sm = _np(slot_mapping, np.int32) if slot_mapping is not None else None
     if cache_dtype not in (CACHE_FP16, CACHE_BF16):  # a 16-bit write is a copy of the bits
@@ -267,6 +278,7 @@ def attention(query, key_cache, value_cache, block_table, cum, past, num_heads,
     Row ranges run on `threads` Python threads (the C call releases the GIL).
     8-bit caches are code arrays dequantized with k_scale / v_scale;
     CACHE_BF16 reads query, both caches and head_sink as bfloat16 bits;
+    ACT_BF16 added to an 8-bit type reads query and head_sink so;
     head_sink ([H] fp16) adds the sink term to every row's denominator.
     """
     qa = _np(query, np.uint16)
@@ -342,16 +354,19 @@ def forward(step, threads=None, rows=None):
         q, k, v = _np(step["query"], np.uint16), _np(step["key"], np.uint16), _np(step["value"], np.uint16)
     if step.get("q_norm_weight") is not None:
         eps = step.get("qk_norm_epsilon", 1e-6)
-        bf = step.get("cache_dtype", CACHE_FP16) == CACHE_BF16
+        bf = act_bf16(step)
         q = qk_norm(q, H, D, step["q_norm_weight"], eps, bf16=bf)
         k = qk_norm(k, Hk, D, step["k_norm_weight"], eps, bf16=bf)
     cdt = step.get("cache_dtype", CACHE_FP16)
+    bf = act_bf16(step)
     if step["do_rotary"]:
         off = step.get("rotary_offset", 0)  # first rotated channel of a head
         q = rotary(q, cum, past, step["cos_cache"], step["sin_cache"], H, D,
-                   step["rotary_interleaved"], off, bf16=cdt == CACHE_BF16)
+                   step["rotary_interleaved"], off, bf16=bf)
         k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
-                   step["rotary_interleaved"], off, bf16=cdt == CACHE_BF16)
+                   step["rotary_interleaved"], off, bf16=bf)
+    if bf and cdt in (CACHE_INT8, CACHE_FP8):
+        cdt |= ACT_BF16
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)
     kc, vc = cache_write(k, v, step["key_cache"], step["value_cache"],

@@ -217,11 +217,17 @@ uint8_t oracle_float_to_e4m3(float x) {
 #define ORACLE_CACHE_INT8 1
 #define ORACLE_CACHE_FP8 2
 #define ORACLE_CACHE_BF16 3 /* 16-bit cache of bfloat16 elements */
+/* Added to an 8-bit cache type: the activations (query, key, value,
+ * head_sink) are bfloat16 (section 8.2 registers bfloat16 activations with
+ * int8 and float8 caches too); a bfloat16 cache implies it. */
+#define ORACLE_ACT_BF16 16
+#define ORACLE_CACHE_TYPE(t) ((t) & 15)
 
-/* Code of fp16 value h under scale s (reading stated in the header). */
+/* Code of 16-bit value h (fp16, or bfloat16 with ORACLE_ACT_BF16) under
+ * scale s (reading stated in the header). */
 uint8_t oracle_quantize(uint16_t h, float s, int cache_dtype) {
-  float y = (float)oracle_half_to_double(h) / s;
-  if (cache_dtype == ORACLE_CACHE_FP8) return oracle_float_to_e4m3(y);
+  float y = (float)elem16_to_double(h, (cache_dtype & ORACLE_ACT_BF16) != 0) / s;
+  if (ORACLE_CACHE_TYPE(cache_dtype) == ORACLE_CACHE_FP8) return oracle_float_to_e4m3(y);
   float r = nearbyintf(y);
   if (r != r) r = 0.0f; /* int8 has no NaN: a NaN value stores code 0 */
   if (r > 127.0f) r = 127.0f;
@@ -456,7 +462,8 @@ int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
                              int Hk, int D, int bs, int NB, const int32_t* slot_mapping) {
   int st = check_lengths(cum, past, B, T);
   if (st) return st;
-  if (cache_dtype != ORACLE_CACHE_INT8 && cache_dtype != ORACLE_CACHE_FP8) return ORACLE_BAD_ARGUMENT;
+  if (ORACLE_CACHE_TYPE(cache_dtype) != ORACLE_CACHE_INT8 && ORACLE_CACHE_TYPE(cache_dtype) != ORACLE_CACHE_FP8)
+    return ORACLE_BAD_ARGUMENT;
   size_t row = (size_t)Hk * D;
   for (int b = 0; b < B; ++b) {
     for (int t = cum[b]; t < cum[b + 1]; ++t) {
@@ -488,7 +495,8 @@ int oracle_cache_write_quant(const uint16_t* key, const uint16_t* value,
  * scale == 0 selects 1/sqrt(D). */
 /* General form.  key_cache / value_cache hold fp16 bits (cache_dtype 0),
  * bfloat16 bits (cache_dtype 3: query and head_sink are then bfloat16 too)
- * or 8-bit codes dequantized as code * scale with k_scale / v_scale indexed
+ * or 8-bit codes (cache_dtype 1, 2; + ORACLE_ACT_BF16 for a bfloat16 query
+ * and sink) dequantized as code * scale with k_scale / v_scale indexed
  * by [k * D + c] (per_channel = 1) or [0]; head_sink ([H] fp16, may be NULL)
  * adds exp(s_h - m) to the denominator, m = max(s_h, max_p x_p). */
 int oracle_attention_ex(const uint16_t* query, const void* key_cache,
@@ -507,9 +515,12 @@ int oracle_attention_ex(const uint16_t* query, const void* key_cache,
   if (row_begin < 0 || row_end > (long long)T * H || row_begin > row_end)
     return ORACLE_BAD_ARGUMENT;
   if (scale == 0.0) scale = 1.0 / sqrt((double)D);
-  const int bf16 = cache_dtype == ORACLE_CACHE_BF16; /* bfloat16 query, cache and sink */
-  if (cache_dtype != ORACLE_CACHE_FP16 && !bf16 && (k_scale == NULL || v_scale == NULL)) return ORACLE_BAD_ARGUMENT;
-  size_t esize = (cache_dtype == ORACLE_CACHE_FP16 || bf16) ? 2 : 1;
+  /* bfloat16 query and sink: a bfloat16 cache, or ORACLE_ACT_BF16 with an 8-bit one */
+  const int bf16 = cache_dtype == ORACLE_CACHE_BF16 || (cache_dtype & ORACLE_ACT_BF16) != 0;
+  cache_dtype = ORACLE_CACHE_TYPE(cache_dtype);
+  const int c16 = cache_dtype == ORACLE_CACHE_FP16 || cache_dtype == ORACLE_CACHE_BF16;
+  if (!c16 && (k_scale == NULL || v_scale == NULL)) return ORACLE_BAD_ARGUMENT;
+  size_t esize = c16 ? 2 : 1;
   int G = H / Hk;
   double q[1024];
   if (D > 1024) return ORACLE_BAD_ARGUMENT;

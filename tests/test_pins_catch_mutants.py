@@ -12,7 +12,8 @@ derivation, the binary16 and e4m3fn roundings, int8 rounding and
 clipping, the per-channel scale index, the QK-Norm epsilon, weight and the
 order and precision of its sum of squares, the latent layout (scores over
 all 576 channels, values from the first 512), and the bfloat16 paths
-(decode exponent, rounding, bfloat16 read as fp16, rotary rounded to fp16).
+(decode exponent, rounding, bfloat16 read as fp16, rotary rounded to fp16,
+bfloat16 activations over an 8-bit cache quantized or attended as fp16).
 """
 
 import os
@@ -26,7 +27,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 PIN_FILES = [os.path.join(ROOT, "tests", f) for f in (
     "test_oracle_pins.py", "test_oracle_quant_pins.py", "test_oracle_slot_pins.py",
-    "test_oracle_qknorm_pins.py", "test_oracle_mla_pins.py", "test_oracle_bf16_pins.py")]
+    "test_oracle_qknorm_pins.py", "test_oracle_mla_pins.py", "test_oracle_bf16_pins.py",
+    "test_oracle_bf16_quant_pins.py")]
 
 # (name, text in oracle.c, replacement, occurrences of the text, indices replaced or None = all)
 MUTANTS = [
@@ -74,6 +76,11 @@ MUTANTS = [
      "q[c] = oracle_half_to_double(query[((size_t)t * H + h) * D + c]);", 1, None),
     ("bfloat16 sink read as fp16", "elem16_to_double(head_sink[h], bf16)", "oracle_half_to_double(head_sink[h])", 1,
      None),
+    ("bfloat16 activations quantized as fp16", "(float)elem16_to_double(h, (cache_dtype & ORACLE_ACT_BF16) != 0) / s",
+     "(float)elem16_to_double(h, 0) / s", 1, None),
+    ("bfloat16 activations over 8-bit pools attended as fp16",
+     "cache_dtype == ORACLE_CACHE_BF16 || (cache_dtype & ORACLE_ACT_BF16) != 0;",
+     "cache_dtype == ORACLE_CACHE_BF16;", 1, None),
     ("bfloat16 rotary rounded to fp16", "tmp[i1] = bf16 ? oracle_double_to_bf16((double)y1)",
      "tmp[i1] = 0 ? oracle_double_to_bf16((double)y1)", 1, None),
 ]

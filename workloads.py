@@ -33,7 +33,8 @@ around 1/32 (int8) or 1/16 (e4m3fn).  head_sink is fp16 [H], N(0, 2^2).
 bfloat16 steps (cache_dtype CACHE_BF16; the kernel is registered for fp16
 and bfloat16 activations, CUDA design section 8.2): the same draws rounded to bfloat16 for
 every 16-bit tensor (query, key, value, both pools, cos/sin, head_sink);
-unused pool slots hold the bfloat16 NaN pattern 0x7FC0.
+unused pool slots hold the bfloat16 NaN pattern 0x7FC0.  With act_bf16 an
+8-bit step draws its activations the same way over the 8-bit pools above.
 """
 
 from __future__ import annotations
@@ -149,14 +150,15 @@ QUANT_NONE, QUANT_PER_TENSOR, QUANT_PER_CHANNEL = 0, 1, 2
 def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
               cache_dtype: int = CACHE_FP16, quant_type: int = QUANT_NONE,
               head_sink: bool = False, qk_norm: bool = False, packed_qkv: bool = False,
-              latent_v_head_size: int = 0):
+              latent_v_head_size: int = 0, act_bf16: bool = False):
     """Build every input tensor of one step on `device`.
 
     Random values are drawn with a torch.Generator on `gen_device` (default:
     `device`), so a CPU run and a CUDA run of the same shape share lengths
     and block tables (drawn on the CPU) but not necessarily values.
     cache_dtype / quant_type select 8-bit pools with their scales, or
-    (CACHE_BF16) bfloat16 activations and pools; head_sink
+    (CACHE_BF16) bfloat16 activations and pools; act_bf16 with an 8-bit
+    cache_dtype makes the activations bfloat16 over 8-bit pools; head_sink
     adds a per-head sink input; qk_norm adds q/k norm weights ([D] fp16 or
     bfloat16, 1 + 0.3 N(0,1)); packed_qkv lays Q, K and V out as one [T, (H+2Hk)*D]
     query tensor with key and value None.  latent_v_head_size > 0 makes a
@@ -192,7 +194,9 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
     T = int(cum[-1])
 
     vg = torch.Generator(device=gen_device).manual_seed(1000 + shape.seed)
-    act = torch.bfloat16 if cache_dtype == CACHE_BF16 else torch.float16
+    if act_bf16 and cache_dtype not in (CACHE_INT8, CACHE_FP8):
+        raise ValueError("act_bf16 goes with an 8-bit cache (CACHE_BF16 is the 16-bit form)")
+    act = torch.bfloat16 if cache_dtype == CACHE_BF16 or act_bf16 else torch.float16
 
     def randn(*size):
         return torch.randn(*size, generator=vg, device=gen_device,
@@ -259,6 +263,8 @@ def make_step(shape: StepShape, device="cpu", gen_device: Optional[str] = None,
         vs = base * (0.8 + 0.4 * torch.rand(n, generator=sg))
         out.update(cache_dtype=cache_dtype, quant_type=quant_type,
                    k_scale=ks.float().to(device), v_scale=vs.float().to(device))
+        if act_bf16:
+            out.update(act_bf16=True)
     if head_sink:
         hg = torch.Generator().manual_seed(5000 + shape.seed)
         out.update(head_sink=(2.0 * torch.randn(H, generator=hg)).to(act).to(device))
