@@ -17,7 +17,8 @@ batch 64, past lengths uniform 512..4096, block_size 16), `long_window`
 tokens alone), `tiny`,
 `decode_fp8` / `decode_int8` (the default decode step over an e4m3fn / int8
 paged cache with per-channel scales; its K/V bytes count one byte per
-element), `mla_decode` (DeepSeek-V3-shaped latent decode: 64 sequences,
+element; `decode_fp8_bf16` / `decode_int8_bf16` the same with bfloat16
+activations), `mla_decode` (DeepSeek-V3-shaped latent decode: 64 sequences,
 128 heads, one 576-channel latent cache, block_size 64, past lengths
 U{512..4096}; its K/V bytes are the latent rows, read once).
 
@@ -67,7 +68,7 @@ def decode_rows(G):
 
 # 8-bit cache variants of the Llama-3-8B-shaped decode step (per-channel
 # scales, the quantized cache of the CUDA design, section 8)
-QUANT_WORKLOADS = {"decode_fp8": 2, "decode_int8": 1}
+QUANT_WORKLOADS = {"decode_fp8": 2, "decode_int8": 1, "decode_fp8_bf16": 2, "decode_int8_bf16": 1}
 # bfloat16 activations and cache (the CUDA design registers the kernel for
 # fp16 and bfloat16 activations, section 8.2) on the fp16 workloads' shapes
 BF16_WORKLOADS = {"decode_bf16": "decode", "mixed_bf16": "mixed", "prefill_bf16": "prefill"}
@@ -76,6 +77,11 @@ CACHE_BF16 = 3
 
 def quantized(step):
     return step.get("cache_dtype", 0) in (1, 2)
+
+
+def act_bf16(step):
+    """bfloat16 activations: a bfloat16 cache, or bfloat16 over 8-bit codes."""
+    return step.get("cache_dtype", 0) == CACHE_BF16 or bool(step.get("act_bf16", False))
 
 
 MLA_SCALE = 0.0723  # an explicit softmax scale (the latent width is not the model's head width)
@@ -106,7 +112,7 @@ def workload_shape(name):
 def workload_options(name):
     """make_step keywords of a workload (8-bit cache variants)."""
     if name in QUANT_WORKLOADS:
-        return dict(cache_dtype=QUANT_WORKLOADS[name], quant_type=2)
+        return dict(cache_dtype=QUANT_WORKLOADS[name], quant_type=2, act_bf16=name.endswith("_bf16"))
     if name in BF16_WORKLOADS:
         return dict(cache_dtype=CACHE_BF16)
     if name == "mla_decode":
@@ -117,7 +123,10 @@ def workload_options(name):
 def shape_name(name, shape):
     if name in BF16_WORKLOADS:
         return shape.name + "_bf16"
-    return shape.name + ({2: "_e4m3_cache", 1: "_int8_cache"}[QUANT_WORKLOADS[name]] if name in QUANT_WORKLOADS else "")
+    if name in QUANT_WORKLOADS:
+        tag = {2: "_e4m3_cache", 1: "_int8_cache"}[QUANT_WORKLOADS[name]]
+        return shape.name + tag + ("_bf16" if name.endswith("_bf16") else "")
+    return shape.name
 
 
 def seq_lengths(step):
@@ -344,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     op = pa.PagedAttention.for_step(step, max_query_len_bound=max(qlens))
     out_width = step["num_heads"] * (step.get("v_head_size") or step["head_size"])
     out = torch.empty(step["token_count"], out_width, device=dev,
-                      dtype=torch.bfloat16 if step.get("cache_dtype", 0) == CACHE_BF16 else torch.float16)
+                      dtype=torch.bfloat16 if act_bf16(step) else torch.float16)
     # A stream of the step's own (as a serving loop has): work on the legacy
     # default stream carries its implicit synchronisation with every other
     # blocking stream (measured: the decode step 104.4 us there, 98.9 us here).
@@ -475,7 +484,7 @@ def run_ours(args, rank, world, local_rank):
         ach = work["pre_flops"] / (t * 1e-3) / 1e12
         # head_size 64/128 run the two-tile kernel, 256 the one-tile kernel
         pair = shape.head_size <= 128
-        bf = ", bf16" if host.get("cache_dtype", 0) == CACHE_BF16 else ""
+        bf = ", bf16" if act_bf16(host) else ""
         rooflines["prefill"] = {
             "bound": "tensor",
             "kernel": (f"prefill_pair_kernel<{shape.head_size}{bf}>" if pair

@@ -123,6 +123,18 @@ enum {
  * QK-Norm weights are bfloat16 and its outputs rounded to bfloat16.  The
  * latent layout and pa_forward_no_alloc are fp16 only (PA_NOT_SUPPORTED). */
 enum { PA_CACHE_FP16 = 0, PA_CACHE_INT8 = 1, PA_CACHE_FP8_E4M3 = 2, PA_CACHE_BF16 = 3 };
+
+/* Activation types (section 8.2 registers fp16 and bfloat16 activations
+ * with every cache type).  PA_ACT_DEFAULT: fp16, or bfloat16 with
+ * PA_CACHE_BF16.  PA_ACT_BF16 with an 8-bit cache: query, key, value,
+ * cos_cache / sin_cache, head_sink, the QK-Norm weights and the output are
+ * bfloat16, transformed (QK-Norm, rotary) with the bfloat16 roundings above;
+ * the codes are those of the bfloat16 values (division in fp32).  The
+ * attention contractions run on fp16 operands as for fp16 activations (the
+ * query is copied as fp16, exact for bfloat16 values in fp16's normal range;
+ * |q| beyond 65504 overflows there).  With PA_CACHE_FP16 it is
+ * PA_INVALID_ARGUMENT; pa_forward_no_alloc takes PA_ACT_DEFAULT only. */
+enum { PA_ACT_DEFAULT = 0, PA_ACT_BF16 = 1 };
 /* Cache layout (section 12).  LATENT: one cache key_cache [NB, bs, 1, D] of
  * latent rows (value and value_cache NULL, kv_num_heads 1); every query
  * head attends with its D channels and the output is the weighted sum of
@@ -165,6 +177,7 @@ typedef struct {
   int kv_cache_layout;     /* PA_LAYOUT_SEPARATE (key_cache + value_cache) or PA_LAYOUT_LATENT */
   int v_head_size;         /* 0 => head_size; != head_size only with PA_LAYOUT_LATENT */
   int rotary_offset;       /* first rotated channel of a head (multiple of 8; latent: v_head_size) */
+  int act_dtype;           /* PA_ACT_*: activation type (PA_ACT_BF16 with an 8-bit cache) */
 } pa_config;
 
 /* Fills *cfg with the attribute defaults (scale 0, softcap 0, window -1,

@@ -35,6 +35,7 @@ STEP_COUNT_NAMES = ("n_dec", "n_pre", "n_comb", "split_keys", "pre_ctas", "dec_c
 PA_STAGE_WORKLIST, PA_STAGE_CACHE_WRITE, PA_STAGE_DECODE, PA_STAGE_PREFILL, PA_STAGE_COMBINE = range(5)
 STAGES = ("worklist", "cache_write", "decode", "prefill", "combine")
 PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3, PA_CACHE_BF16 = 0, 1, 2, 3
+PA_ACT_DEFAULT, PA_ACT_BF16 = 0, 1
 PA_QUANT_NONE, PA_QUANT_PER_TENSOR, PA_QUANT_PER_CHANNEL = 0, 1, 2
 PA_LAYOUT_SEPARATE, PA_LAYOUT_LATENT = 0, 1
 
@@ -53,7 +54,7 @@ class pa_config(ctypes.Structure):
                                     "max_query_len_bound", "max_kv_len_bound", "cache_dtype",
                                     "k_quant_type", "v_quant_type", "packed_qkv", "qk_norm")] + [
         ("qk_norm_epsilon", ctypes.c_float)] + [
-        (n, ctypes.c_int) for n in ("kv_cache_layout", "v_head_size", "rotary_offset")]
+        (n, ctypes.c_int) for n in ("kv_cache_layout", "v_head_size", "rotary_offset", "act_dtype")]
 
 
 class pa_extra_inputs(ctypes.Structure):
@@ -129,7 +130,7 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                 rotary_interleaved=0, rotary_dim=0, max_rotary_positions=0, max_query_len_bound=0,
                 max_kv_len_bound=0, cache_dtype=0, k_quant_type=0, v_quant_type=0, packed_qkv=0,
                 qk_norm=0, qk_norm_epsilon=1e-6, kv_cache_layout=0, v_head_size=0,
-                rotary_offset=0) -> pa_config:
+                rotary_offset=0, act_dtype=0) -> pa_config:
     c = pa_config()
     lib().pa_config_init(ctypes.byref(c))
     for k, v in dict(num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
@@ -143,7 +144,7 @@ def make_config(num_heads, kv_num_heads, head_size, block_size, num_blocks, max_
                      max_kv_len_bound=max_kv_len_bound, cache_dtype=cache_dtype,
                      k_quant_type=k_quant_type, v_quant_type=v_quant_type, packed_qkv=packed_qkv,
                      qk_norm=qk_norm, qk_norm_epsilon=qk_norm_epsilon, kv_cache_layout=kv_cache_layout,
-                     v_head_size=v_head_size, rotary_offset=rotary_offset).items():
+                     v_head_size=v_head_size, rotary_offset=rotary_offset, act_dtype=act_dtype).items():
         setattr(c, k, v)
     return c
 
@@ -309,6 +310,7 @@ class PagedAttention:
                           packed_qkv=int(step.get("key") is None),
                           kv_cache_layout=step.get("kv_cache_layout", 0), v_head_size=step.get("v_head_size", 0),
                           rotary_offset=step.get("rotary_offset", 0),
+                          act_dtype=PA_ACT_BF16 if step.get("act_bf16") else PA_ACT_DEFAULT,
                           qk_norm=int(step.get("q_norm_weight") is not None),
                           qk_norm_epsilon=step.get("qk_norm_epsilon", 1e-6), **bounds)
         return cls(cfg)

@@ -84,6 +84,9 @@ const char* wait_kernel_name(int k) {
 // 8-bit code caches (quantized); the 16-bit ones are fp16 and bfloat16.
 bool quantized(int cache_dtype) { return cache_dtype == PA_CACHE_INT8 || cache_dtype == PA_CACHE_FP8_E4M3; }
 
+// bfloat16 activations: a bfloat16 cache, or act_dtype PA_ACT_BF16 over an 8-bit one.
+bool act_bf16(const pa_config& c) { return c.cache_dtype == PA_CACHE_BF16 || c.act_dtype == PA_ACT_BF16; }
+
 int rot_dim_of(const pa_config& c) {
   if (!c.do_rotary) return 0;
   return c.rotary_dim > 0 ? c.rotary_dim : c.head_size;
@@ -92,10 +95,12 @@ int rot_dim_of(const pa_config& c) {
 // Whether attention reads a transformed copy of the query (rotated, QK-Norm
 // normalized, unpacked from QKV rows, or times per-channel K scales) rather
 // than the query itself.  A single per-tensor K scale multiplies the score
-// scale instead (exact, CUDA design section 8.5 phase 3).
+// scale instead (exact, CUDA design section 8.5 phase 3).  A bfloat16 query
+// over an 8-bit cache is copied as fp16 (the operand type of that kernel).
 bool query_copied(const pa_config& c) {
   const bool per_channel_k = quantized(c.cache_dtype) && c.k_quant_type == PA_QUANT_PER_CHANNEL;
-  return c.do_rotary || per_channel_k || c.packed_qkv || c.qk_norm;
+  const bool bf16_over_codes = quantized(c.cache_dtype) && c.act_dtype == PA_ACT_BF16;
+  return c.do_rotary || per_channel_k || c.packed_qkv || c.qk_norm || bf16_over_codes;
 }
 
 }  // namespace
@@ -295,6 +300,15 @@ pa_status pa_validate_config(const pa_config* c, char* msg, size_t len) {
   if (c->cache_dtype < PA_CACHE_FP16 || c->cache_dtype > PA_CACHE_BF16) {
     set_msg(msg, len, "cache_dtype must be PA_CACHE_FP16, PA_CACHE_INT8, PA_CACHE_FP8_E4M3 or PA_CACHE_BF16 (got %d)",
             c->cache_dtype);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->act_dtype != PA_ACT_DEFAULT && c->act_dtype != PA_ACT_BF16) {
+    set_msg(msg, len, "act_dtype must be PA_ACT_DEFAULT or PA_ACT_BF16 (got %d)", c->act_dtype);
+    return PA_INVALID_ARGUMENT;
+  }
+  if (c->act_dtype == PA_ACT_BF16 && c->cache_dtype == PA_CACHE_FP16) {
+    set_msg(msg, len, "act_dtype PA_ACT_BF16 needs an int8, e4m3 or bfloat16 cache (bfloat16 activations "
+                      "with 16-bit pools are cache_dtype PA_CACHE_BF16)");
     return PA_INVALID_ARGUMENT;
   }
   for (int qt : {c->k_quant_type, c->v_quant_type})
@@ -768,6 +782,7 @@ pa::CacheWriteParams cache_write_params(const pa_config& c, __half* q_ws, int* e
   p.key_cache = key_cache;
   p.value_cache = value_cache;
   p.cache_type = c.cache_dtype;
+  p.act_bf16 = (quant && c.act_dtype == PA_ACT_BF16) ? 1 : 0;
   p.per_channel = c.k_quant_type == PA_QUANT_PER_CHANNEL;
   p.k_scale = quant ? x->k_scale : nullptr;
   p.v_scale = quant ? x->v_scale : nullptr;
@@ -903,7 +918,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
   st = check_extra(h, x);
   if (st != PA_OK) return st;
   const bool quant = quantized(h->cfg.cache_dtype);
-  const int bf16 = h->cfg.cache_dtype == PA_CACHE_BF16 ? 1 : 0;
+  const int bf16 = act_bf16(h->cfg) ? 1 : 0;  // head_sink and output are bfloat16
   const __half* sink = static_cast<const __half*>(x->head_sink);
   h->last_launches = 0;
   for (bool& r : h->stage_ran) r = false;
@@ -1111,6 +1126,7 @@ pa_status pa_forward_ex(pa_handle h, const void* query, const void* key, const v
     p.out = static_cast<__half*>(output);
     p.head_sink = sink;
     p.cache_type = c.cache_dtype;
+    p.act_bf16 = (quant && bf16) ? 1 : 0;
     p.per_channel = c.v_quant_type == PA_QUANT_PER_CHANNEL;
     p.v_scale = x->v_scale;
     p.k_scale_tensor = (quant && c.k_quant_type == PA_QUANT_PER_TENSOR) ? x->k_scale : nullptr;
@@ -1235,7 +1251,8 @@ extern "C" pa_status pa_forward_no_alloc(const pa_config* cfg, const void* query
   pa_status st = pa_check_step(cfg, 1, query, key, value, key_cache, value_cache, block_table, cum, past, batch,
                                token_count, cos_cache, sin_cache, output, msg, sizeof(msg));
   if (st != PA_OK) return fail(nullptr, st, "%s", msg);
-  if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->packed_qkv || cfg->qk_norm || cfg->kv_cache_layout != PA_LAYOUT_SEPARATE)
+  if (cfg->cache_dtype != PA_CACHE_FP16 || cfg->act_dtype != PA_ACT_DEFAULT || cfg->packed_qkv || cfg->qk_norm ||
+      cfg->kv_cache_layout != PA_LAYOUT_SEPARATE)
     return fail(nullptr, PA_NOT_SUPPORTED,
                 "pa_forward_no_alloc runs separate fp16 K/V caches without packed QKV or QK-Norm (no latent "
                 "layout, no 8-bit or bfloat16 cache); use pa_forward_ex");

@@ -22,12 +22,15 @@
 // Hk*D*2 bytes per tensor (fully coalesced).
 //
 // 8-bit caches (section 8.4, quantize as the rows are scattered): each fp16
-// value x (after rotary) is stored as the code of y = x / scale, the
+// (or bfloat16) value x (after rotary) is stored as the code of y = x / scale, the
 // division in fp32 (IEEE), rounded to nearest-even and saturated to
 // [-128, 127] (int8) or to +-448 (e4m3fn); scale is k_scale / v_scale[0] or
 // [k*D + c] per channel.  The query copy for attention is then multiplied by
 // the K scale (fp32 product rounded to fp16), which folds the K
-// dequantization into Q (section 8.5 phase 3).
+// dequantization into Q (section 8.5 phase 3).  With bfloat16 activations
+// the rows are transformed in bfloat16 as for a bfloat16 cache and the
+// query copy is written as fp16 (the score contraction over 8-bit codes
+// takes fp16 operands).
 //
 // QK-Norm (section 7, before rotary; the normalized K is what is cached):
 // each head's factor r = 1 / sqrt(sum x^2 / D + eps) takes its fp32 sum of
@@ -75,8 +78,9 @@ struct EmitHalf {  // fp16 row
   }
 };
 
-__device__ __forceinline__ uint32_t code8(__half x, float s, int type) {
-  const float y = __fdiv_rn(__half2float(x), s);
+// Code of the 16-bit value x (fp16, or bfloat16 bits when bf16).
+__device__ __forceinline__ uint32_t code8(__half x, float s, int type, bool bf16) {
+  const float y = __fdiv_rn(elem16_to_float(x, bf16), s);
   if (type == kCacheI8) {
     const int r = min(max(__float2int_rn(y), -128), 127);
     return (uint32_t)r & 0xffu;
@@ -94,11 +98,12 @@ struct EmitCode {  // 8-bit codes; scale[0] or scale[(head0 + h) * D + c]
   uint8_t* dst;
   int D, type, per_channel, head0;
   const float* scale;
+  bool bf16;  // the row holds bfloat16 activations
   __device__ void operator()(int h, int ch, const Vec8& v) const {
     const float* sc = scale + (per_channel ? (size_t)(head0 + h) * D + ch : 0);
     uint32_t w[2] = {0, 0};
 #pragma unroll
-    for (int e = 0; e < 8; ++e) w[e >> 2] |= code8(v.h[e], sc[per_channel ? e : 0], type) << (8 * (e & 3));
+    for (int e = 0; e < 8; ++e) w[e >> 2] |= code8(v.h[e], sc[per_channel ? e : 0], type, bf16) << (8 * (e & 3));
     *reinterpret_cast<uint2*>(dst + (size_t)h * D + ch) = make_uint2(w[0], w[1]);
   }
 };
@@ -107,11 +112,27 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
   __half* dst;
   int D, G, per_channel, head0;
   const float* scale;
+  bool bf16;  // the row holds bfloat16 activations (the copy is fp16 all the same)
   __device__ void operator()(int h, int ch, const Vec8& v) const {
     const float* sc = scale + (per_channel ? (size_t)((head0 + h) / G) * D + ch : 0);
     Vec8 y;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(__fmul_rn(__half2float(v.h[e]), sc[per_channel ? e : 0]));
+    for (int e = 0; e < 8; ++e)
+      y.h[e] = __float2half_rn(__fmul_rn(elem16_to_float(v.h[e], bf16), sc[per_channel ? e : 0]));
+    *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = y.u;
+  }
+};
+
+// bfloat16 row stored as fp16 (the query copy of a bfloat16 step over an
+// 8-bit cache, whose score contraction runs on fp16 operands): the
+// conversion is exact for every bfloat16 value inside fp16's normal range.
+struct EmitHalfOfBf16 {
+  __half* dst;
+  int D;
+  __device__ void operator()(int h, int ch, const Vec8& v) const {
+    Vec8 y;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(elem16_to_float(v.h[e], true));
     *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = y.u;
   }
 };
@@ -264,6 +285,8 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   const __half* cos_row = rotate ? p.cos_cache + (size_t)pos * half : nullptr;
   const __half* sin_row = rotate ? p.sin_cache + (size_t)pos * half : nullptr;
 
+  // bfloat16 activations: a bfloat16 cache, or act_bf16 over an 8-bit one
+  const bool abf = p.cache_type == kCacheBF16 || p.act_bf16;
   if (part >= p.kv_parts) {
     const int h0 = (part - p.kv_parts) * p.q_heads_per_part;
     const int nh = min(p.q_heads_per_part, p.H - h0);
@@ -271,13 +294,16 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     const size_t qoff = ((size_t)t * p.H + h0) * p.D;
     const float* qrn = nullptr;
     if (p.qk_norm) {
-      norm_factors(qsrc, nh, p.D, p.qk_eps, rn, lane, p.cache_type == kCacheBF16);
+      norm_factors(qsrc, nh, p.D, p.qk_eps, rn, lane, abf);
       qrn = rn;
     }
     if (p.q_scale)
-      row_transform(qsrc, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale},
+      row_transform(qsrc, EmitScaledHalf{p.q_rot + qoff, p.D, p.H / p.Hk, p.per_channel, h0, p.k_scale, abf},
                     nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, qrn, p.q_norm_w,
-                    p.rot_offset);
+                    p.rot_offset, 0, 1 << 30, abf);
+    else if (p.act_bf16)
+      row_transform(qsrc, EmitHalfOfBf16{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
+                    cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset, 0, 1 << 30, true);
     else
       row_transform(qsrc, EmitHalf{p.q_rot + qoff, p.D}, nh, p.D, rotate, p.rot_dim, p.interleaved,
                     cos_row, sin_row, lane, qrn, p.q_norm_w, p.rot_offset, p.q_keep_lo, p.q_keep_hi,
@@ -322,25 +348,25 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
     if ((part & 1) == 0) {
       const float* krn = nullptr;
       if (p.qk_norm) {
-        norm_factors(ksrc + (size_t)h0 * p.D, nh, p.D, p.qk_eps, rn, lane, false);
+        norm_factors(ksrc + (size_t)h0 * p.D, nh, p.D, p.qk_eps, rn, lane, abf);
         krn = rn;
       }
       row_transform(ksrc + (size_t)h0 * p.D,
                     EmitCode{static_cast<uint8_t*>(p.key_cache) + doff, p.D, p.cache_type, p.per_channel, h0,
-                             p.k_scale},
+                             p.k_scale, abf},
                     nh, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
-                    p.rot_offset);
+                    p.rot_offset, 0, 1 << 30, abf);
     } else {
       row_transform(vsrc + (size_t)h0 * p.D,
                     EmitCode{static_cast<uint8_t*>(p.value_cache) + doff, p.D, p.cache_type, p.per_channel, h0,
-                             p.v_scale},
+                             p.v_scale, abf},
                     nh, p.D, false, 0, 0, nullptr, nullptr, lane);
     }
     return;
   }
   const float* krn = nullptr;
   if (p.qk_norm) {
-    norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane, p.cache_type == kCacheBF16);
+    norm_factors(ksrc, p.Hk, p.D, p.qk_eps, rn, lane, abf);
     krn = rn;
   }
   if (p.cache_type == kCacheF16 || p.cache_type == kCacheBF16) {
@@ -353,12 +379,12 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   } else {
     row_transform(ksrc,
                   EmitCode{static_cast<uint8_t*>(p.key_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
-                           p.k_scale},
+                           p.k_scale, abf},
                   p.Hk, p.D, rotate, p.rot_dim, p.interleaved, cos_row, sin_row, lane, krn, p.k_norm_w,
-                  p.rot_offset);
+                  p.rot_offset, 0, 1 << 30, abf);
     row_transform(vsrc,
                   EmitCode{static_cast<uint8_t*>(p.value_cache) + slot * kv_row, p.D, p.cache_type, p.per_channel, 0,
-                           p.v_scale},
+                           p.v_scale, abf},
                   p.Hk, p.D, false, 0, 0, nullptr, nullptr, lane);
   }
 }

@@ -665,8 +665,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_k, const CUten
         if constexpr (kQ8) acc *= __ldg(p.v_scale + (p.per_channel ? tg.k * D + d : 0));
         if (tg.nsplit == 1) {
           const int t = tg.t0 + r / p.G, h = tg.k * p.G + r % p.G;
-          if (p.head_sink && M != -INFINITY) den += exp2f(elem16_to_float(p.head_sink[h], kBF) * kLog2e - M);
-          p.out[((size_t)t * p.H + h) * D + d] = float_to_elem16(den > 0.f ? acc / den : 0.f, kBF);
+          // bfloat16 sink and output: a bfloat16 cache, or bfloat16 activations over 8-bit codes
+          const bool obf = kBF || (kQ8 && p.act_bf16);
+          if (p.head_sink && M != -INFINITY) den += exp2f(elem16_to_float(p.head_sink[h], obf) * kLog2e - M);
+          p.out[((size_t)t * p.H + h) * D + d] = float_to_elem16(den > 0.f ? acc / den : 0.f, obf);
         } else {
           const size_t row = ((size_t)tg.part * p.Hk + tg.k) * kDecodeRows + r;
           p.part_o[row * D + d] = acc;

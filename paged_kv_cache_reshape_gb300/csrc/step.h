@@ -128,6 +128,8 @@ struct CacheWriteParams {
   void* key_cache;      // fp16 or 8-bit codes (cache_type)
   void* value_cache;
   int cache_type;       // CacheType
+  int act_bf16;         // 8-bit caches: 1 = bfloat16 activations (query, key, value, tables,
+                        // norm weights); the query copy is fp16 either way
   int per_channel;      // scales [Hk*D] (1) or [1] (0)
   const float* k_scale; // 8-bit caches: quantization / dequantization scales
   const float* v_scale;
@@ -167,6 +169,8 @@ struct DecodeParams {
                                 // (per-channel K scales are folded into the query copy instead)
   int per_channel;
   int cache_type;
+  int act_bf16;             // 8-bit caches: 1 = head_sink and out are bfloat16 (the query
+                            // copy the kernel reads is fp16 either way)
   const int* block_table;
   const SeqInfo* seq;       // the decode table
   const int2* dec_items;

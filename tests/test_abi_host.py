@@ -104,6 +104,36 @@ def test_bf16_config_passes_and_latent_rejects_it():
     assert st == pa.PA_NOT_SUPPORTED and "fp16" in msg, (st, msg)
 
 
+Q8 = dict(cache_dtype=pa.PA_CACHE_INT8, k_quant_type=pa.PA_QUANT_PER_TENSOR, v_quant_type=pa.PA_QUANT_PER_TENSOR)
+
+
+def test_bf16_activation_rules():
+    """act_dtype: bfloat16 activations go with an 8-bit or a bfloat16 cache."""
+    for cdt in (pa.PA_CACHE_INT8, pa.PA_CACHE_FP8_E4M3):
+        for qt in (pa.PA_QUANT_PER_TENSOR, pa.PA_QUANT_PER_CHANNEL):
+            assert pa.pa_validate_config(good(cache_dtype=cdt, k_quant_type=qt, v_quant_type=qt,
+                                              act_dtype=pa.PA_ACT_BF16)) == (pa.PA_OK, "ok")
+    assert pa.pa_validate_config(good(act_dtype=pa.PA_ACT_BF16, packed_qkv=1, qk_norm=1, **Q8)) == (pa.PA_OK, "ok")
+    assert pa.pa_validate_config(good(cache_dtype=pa.PA_CACHE_BF16, act_dtype=pa.PA_ACT_BF16)) == (pa.PA_OK, "ok")
+    st, msg = pa.pa_validate_config(good(act_dtype=pa.PA_ACT_BF16))
+    assert st == pa.PA_INVALID_ARGUMENT and "PA_CACHE_BF16" in msg, (st, msg)
+    for bad in (2, -1):
+        st, msg = pa.pa_validate_config(good(act_dtype=bad, **Q8))
+        assert st == pa.PA_INVALID_ARGUMENT and "act_dtype" in msg, (st, msg)
+
+
+def test_no_alloc_rejects_bf16_activations():
+    a = step_args()
+    P = lambda v: None if v is None else ctypes.c_void_p(v)  # noqa: E731
+    cfg = good(act_dtype=pa.PA_ACT_BF16, **Q8)
+    assert pa.pa_validate_config(cfg) == (pa.PA_OK, "ok")
+    st = pa.lib().pa_forward_no_alloc(ctypes.byref(cfg), P(a["query"]), P(a["key"]),
+                                      P(a["value"]), P(a["key_cache"]), P(a["value_cache"]), P(a["block_table"]),
+                                      P(a["cumulative_sequence_lengths"]), P(a["past_sequence_lengths"]), 4, 4,
+                                      None, None, P(a["output"]), None, ctypes.c_void_p(0))
+    assert st == pa.PA_NOT_SUPPORTED
+
+
 @pytest.mark.parametrize("over,status,word", [
     (dict(packed_qkv=2), pa.PA_INVALID_ARGUMENT, "packed_qkv"),
     (dict(qk_norm=3), pa.PA_INVALID_ARGUMENT, "qk_norm"),
