@@ -287,7 +287,7 @@ def oracle_sample(step, budget_s, start_seq=0):
             oracle.attention(base["query_rot"], base["key_cache"], base["value_cache"], step["block_table"],
                              cum, step["past_sequence_lengths"], H, step["kv_num_heads"], step["head_size"],
                              step["block_size"], step["scale"], step["softcap"], step["local_window_size"],
-                             rows=rows, threads=cores, cache_dtype=step.get("cache_dtype", 0),
+                             rows=rows, threads=cores, cache_dtype=oracle.step_cache_dtype(step),
                              k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                              per_channel=step.get("quant_type", 0) == 2, head_sink=step.get("head_sink"))
         seqs.append(b)
@@ -459,6 +459,8 @@ def run_ours(args, rank, world, local_rank):
         t = statistics.mean(ker_ms[pa.PA_STAGE_DECODE])
         alg = work["dec_kv_bytes"] + work["dec_qo_bytes"]
         ct = {0: "", 1: ", int8", 2: ", e4m3", 3: ", bf16"}[host.get("cache_dtype", 0)]
+        if quantized(host) and act_bf16(host):
+            ct += ", bf16 out"
         latent = host.get("kv_cache_layout", 0) == 1
         latent_tc = latent and shape.num_heads % 128 == 0  # the tcgen05 latent kernel serves these
         kname = (("mla_tc_kernel" if latent_tc else "mla_decode_kernel") if latent

@@ -42,6 +42,15 @@ def act_bf16(step) -> bool:
     return step.get("cache_dtype", CACHE_FP16) == CACHE_BF16 or bool(step.get("act_bf16", False))
 
 
+def step_cache_dtype(step) -> int:
+    """The cache type handed to the C functions for a step: its cache_dtype,
+    plus ACT_BF16 for bfloat16 activations over an 8-bit cache."""
+    cdt = step.get("cache_dtype", CACHE_FP16)
+    if act_bf16(step) and cdt in (CACHE_INT8, CACHE_FP8):
+        cdt |= ACT_BF16
+    return cdt
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c -> liboracle.so (plain gcc, no CUDA)."""
     if (not force and os.path.exists(_LIB)
@@ -357,7 +366,7 @@ def forward(step, threads=None, rows=None):
         bf = act_bf16(step)
         q = qk_norm(q, H, D, step["q_norm_weight"], eps, bf16=bf)
         k = qk_norm(k, Hk, D, step["k_norm_weight"], eps, bf16=bf)
-    cdt = step.get("cache_dtype", CACHE_FP16)
+    cdt = step_cache_dtype(step)
     bf = act_bf16(step)
     if step["do_rotary"]:
         off = step.get("rotary_offset", 0)  # first rotated channel of a head
@@ -365,8 +374,6 @@ def forward(step, threads=None, rows=None):
                    step["rotary_interleaved"], off, bf16=bf)
         k = rotary(k, cum, past, step["cos_cache"], step["sin_cache"], Hk, D,
                    step["rotary_interleaved"], off, bf16=bf)
-    if bf and cdt in (CACHE_INT8, CACHE_FP8):
-        cdt |= ACT_BF16
     quant = dict(cache_dtype=cdt, k_scale=step.get("k_scale"), v_scale=step.get("v_scale"),
                  per_channel=step.get("quant_type", 0) == 2)
     kc, vc = cache_write(k, v, step["key_cache"], step["value_cache"],

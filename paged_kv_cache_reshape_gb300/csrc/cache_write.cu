@@ -68,12 +68,19 @@ union Vec8 {
   __half h[8];
 };
 
+// An ordinary (generic) load: this file reads no input through the
+// read-only data cache (see the note at EmitCode).
+template <typename T>
+__device__ __forceinline__ T ld_plain(const T* ptr) {
+  return *ptr;
+}
+
 // Emitters: where the eight fp16 values of channels [ch, ch + 8) of head h
 // of a transformed row go.
 struct EmitHalf {  // fp16 row
   __half* dst;
   int D;
-  __device__ void operator()(int h, int ch, const Vec8& v) const {
+  __device__ __forceinline__ void operator()(int h, int ch, const Vec8& v) const {
     *reinterpret_cast<uint4*>(dst + (size_t)h * D + ch) = v.u;
   }
 };
@@ -90,16 +97,19 @@ __device__ __forceinline__ uint32_t code8(__half x, float s, int type, bool bf16
   return c & 0xffu;
 }
 
-// (The scales are read with ordinary loads: with the read-only-cache form
-// inside this inlined emitter, one build of the prologue faulted on the
-// rotated 8-bit K rows with cudaErrorInvalidAddressSpace, reproducibly, while
-// the same loads as plain loads or from an out-of-line emitter ran clean.)
+// (Every load of this file is an ordinary load (ld_plain) and every function
+// and emitter is inlined into the kernels, the emitters passed by value, so
+// that no address of a kernel parameter or of a local object reaches a
+// load: two builds of the prologue whose rotated 8-bit K rows went through
+// row_transform with read-only-cache loads and an emitter passed by
+// reference stopped with cudaErrorInvalidAddressSpace, each reproducibly,
+// while every input address was a device tensor in range.)
 struct EmitCode {  // 8-bit codes; scale[0] or scale[(head0 + h) * D + c]
   uint8_t* dst;
   int D, type, per_channel, head0;
   const float* scale;
   bool bf16;  // the row holds bfloat16 activations
-  __device__ void operator()(int h, int ch, const Vec8& v) const {
+  __device__ __forceinline__ void operator()(int h, int ch, const Vec8& v) const {
     const float* sc = scale + (per_channel ? (size_t)(head0 + h) * D + ch : 0);
     uint32_t w[2] = {0, 0};
 #pragma unroll
@@ -113,7 +123,7 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
   int D, G, per_channel, head0;
   const float* scale;
   bool bf16;  // the row holds bfloat16 activations (the copy is fp16 all the same)
-  __device__ void operator()(int h, int ch, const Vec8& v) const {
+  __device__ __forceinline__ void operator()(int h, int ch, const Vec8& v) const {
     const float* sc = scale + (per_channel ? (size_t)((head0 + h) / G) * D + ch : 0);
     Vec8 y;
 #pragma unroll
@@ -129,7 +139,7 @@ struct EmitScaledHalf {  // fp16 row times the K scale of its kv head (query hea
 struct EmitHalfOfBf16 {
   __half* dst;
   int D;
-  __device__ void operator()(int h, int ch, const Vec8& v) const {
+  __device__ __forceinline__ void operator()(int h, int ch, const Vec8& v) const {
     Vec8 y;
 #pragma unroll
     for (int e = 0; e < 8; ++e) y.h[e] = __float2half_rn(elem16_to_float(v.h[e], true));
@@ -141,14 +151,14 @@ struct EmitHalfOfBf16 {
 // squares of head h as one running fp32 sum in channel order (the order
 // stated at the top of the file), then stores rn[h].  bf16: the row holds
 // bfloat16.
-__device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, float eps, float* rn, int lane,
+__device__ __forceinline__ void norm_factors(const __half* src, int nheads, int D, float eps, float* rn, int lane,
                              bool bf16) {
   if (lane < nheads) {
     const __half* x = src + (size_t)lane * D;
     float acc = 0.f;
     for (int c = 0; c < D; c += 8) {
       Vec8 v;
-      v.u = __ldg(reinterpret_cast<const uint4*>(x + c));
+      v.u = ld_plain(reinterpret_cast<const uint4*>(x + c));
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float f = elem16_to_float(v.h[e], bf16);
@@ -169,7 +179,7 @@ __device__ void norm_factors(const __half* __restrict__ src, int nheads, int D, 
 // 64-channel chunks that hold its rotated channels).  bf16: the row, the
 // weight and the tables hold bfloat16.
 template <typename Emit>
-__device__ void row_transform(const __half* __restrict__ src, const Emit& emit, int nheads, int D, bool rotate,
+__device__ __forceinline__ void row_transform(const __half* src, const Emit emit, int nheads, int D, bool rotate,
                               int R, int interleaved, const __half* cos_row, const __half* sin_row, int lane,
                               const float* rn = nullptr, const __half* nw = nullptr, int off = 0, int keep_lo = 0,
                               int keep_hi = 1 << 30, bool bf16 = false) {
@@ -177,11 +187,11 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
   const int chunks_per_head = D / 8;
   auto ld8 = [&](int h, int ch) -> Vec8 {
     Vec8 v;
-    v.u = __ldg(reinterpret_cast<const uint4*>(src + (size_t)h * D + ch));
+    v.u = ld_plain(reinterpret_cast<const uint4*>(src + (size_t)h * D + ch));
     if (rn) {
       const float r = rn[h];
       Vec8 w;
-      w.u = __ldg(reinterpret_cast<const uint4*>(nw + ch));
+      w.u = ld_plain(reinterpret_cast<const uint4*>(nw + ch));
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         v.h[e] = float_to_elem16(__fmul_rn(__fmul_rn(elem16_to_float(v.h[e], bf16), r), elem16_to_float(w.h[e], bf16)),
@@ -194,7 +204,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
       if (!rn && keep_all) {  // plain copy of a contiguous [nheads, D] row
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(emit.dst);
-        for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = __ldg(s4 + i);
+        for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = ld_plain(s4 + i);
         return;
       }
     }
@@ -215,8 +225,8 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
       int h = i / per_head, c = i % per_head;
       if (c < pairs) {
         Vec8 a = ld8(h, off + 8 * c), b = ld8(h, off + half + 8 * c), cs, sn, ya, yb;
-        cs.u = __ldg(reinterpret_cast<const uint4*>(cos_row + 8 * c));
-        sn.u = __ldg(reinterpret_cast<const uint4*>(sin_row + 8 * c));
+        cs.u = ld_plain(reinterpret_cast<const uint4*>(cos_row + 8 * c));
+        sn.u = ld_plain(reinterpret_cast<const uint4*>(sin_row + 8 * c));
 #pragma unroll
         for (int e = 0; e < 8; ++e) rotate_pair(a.h[e], b.h[e], cs.h[e], sn.h[e], ya.h[e], yb.h[e], bf16);
         emit(h, off + 8 * c, ya);
@@ -236,8 +246,8 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
       if (!rot && (8 * c < keep_lo || 8 * c >= keep_hi)) continue;
       Vec8 a = ld8(h, 8 * c), y;
       if (rot) {
-        uint2 cu = __ldg(reinterpret_cast<const uint2*>(cos_row + 4 * (c - c0)));
-        uint2 su = __ldg(reinterpret_cast<const uint2*>(sin_row + 4 * (c - c0)));
+        uint2 cu = ld_plain(reinterpret_cast<const uint2*>(cos_row + 4 * (c - c0)));
+        uint2 su = ld_plain(reinterpret_cast<const uint2*>(sin_row + 4 * (c - c0)));
         const __half* cv = reinterpret_cast<const __half*>(&cu);
         const __half* sv = reinterpret_cast<const __half*>(&su);
 #pragma unroll
@@ -256,7 +266,7 @@ __device__ void row_transform(const __half* __restrict__ src, const Emit& emit, 
 // into the rotated-query workspace (only with rotary in pa_forward).  `cum`
 // is the cumulative length array, either the caller's (global) or a
 // shared-memory copy.
-__device__ void write_token(const CacheWriteParams& p, const int* cum, int t, int part, int lane, float* rn) {
+__device__ __forceinline__ void write_token(const CacheWriteParams& p, const int* cum, int t, int part, int lane, float* rn) {
   // Owner sequence: largest b with cum[b] <= t.
   int lo = 0, hi = p.batch;
   while (hi - lo > 1) {
@@ -266,7 +276,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   }
   const int b = lo;
   const int c0 = cum[b], c1 = cum[b + 1];
-  const int past = __ldg(p.past + b);
+  const int past = ld_plain(p.past + b);
   if (t < c0 || t >= c1 || c0 < 0) {
     if (lane == 0 && part == 0) atomicOr(p.err, PA_DEVERR_CUM);
     return;
@@ -314,7 +324,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
   size_t slot;
   if (p.slot_mapping) {
     // explicit slot (section 5.2): authoritative, -1 = no write
-    const int s = __ldg(p.slot_mapping + t);
+    const int s = ld_plain(p.slot_mapping + t);
     if (s == -1) return;
     if (s < -1 || (long long)s >= (long long)p.NB * p.bs) {
       if (lane == 0) atomicOr(p.err, PA_DEVERR_SLOT);
@@ -327,7 +337,7 @@ __device__ void write_token(const CacheWriteParams& p, const int* cum, int t, in
       if (lane == 0) atomicOr(p.err, PA_DEVERR_KV_BOUND);
       return;
     }
-    const int blk = __ldg(p.block_table + (size_t)b * p.MB + row);
+    const int blk = ld_plain(p.block_table + (size_t)b * p.MB + row);
     if (blk == -1) return;  // not mapped: no write
     if (blk < -1 || blk >= p.NB) {
       if (lane == 0) atomicOr(p.err, PA_DEVERR_BLOCK_ID);
@@ -395,7 +405,7 @@ constexpr int kCumCache = 4096;
 
 __device__ const int* stage_cum(const CacheWriteParams& p, int* cum_s) {
   if (p.batch + 1 > kCumCache) return p.cum;
-  for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cum_s[i] = __ldg(p.cum + i);
+  for (int i = threadIdx.x; i <= p.batch; i += blockDim.x) cum_s[i] = ld_plain(p.cum + i);
   __syncthreads();
   return cum_s;
 }

@@ -121,7 +121,7 @@ def check_rows(step_host, step_dev, out, rows, threads=16):
                          step_host["past_sequence_lengths"], H, step_host["kv_num_heads"], D,
                          step_host["block_size"], step_host["scale"], step_host["softcap"],
                          step_host["local_window_size"], rows=rows, threads=threads,
-                         cache_dtype=step_host.get("cache_dtype", 0), k_scale=step_host.get("k_scale"),
+                         cache_dtype=oracle.step_cache_dtype(step_host), k_scale=step_host.get("k_scale"),
                          v_scale=step_host.get("v_scale"), per_channel=step_host.get("quant_type", 0) == 2,
                          head_sink=step_host.get("head_sink"))
     got = out.float().cpu().numpy().reshape(T * H, D)[rows]
