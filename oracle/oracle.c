@@ -56,12 +56,14 @@
  *
  * bfloat16.  The kernel is registered for fp16 and bfloat16 activations,
  * each with a cache of its own type or an 8-bit one ("PagedAttention - CUDA
- * Design Document", section 8.2); this oracle covers bfloat16 with a
- * bfloat16 cache.  With
- * bfloat16 every 16-bit input (query, key, value, the pools, the cos/sin
- * tables, head_sink) is read as bfloat16 (exact in fp64), rotary runs the
- * same fp32 operation order and rounds each y to bfloat16 to nearest-even,
- * and the cache write copies the bits.
+ * Design Document", section 8.2); this oracle covers both.  With a
+ * bfloat16 cache every 16-bit input (query, key, value, the pools, the
+ * cos/sin tables, head_sink) is read as bfloat16 (exact in fp64), rotary
+ * runs the same fp32 operation order and rounds each y to bfloat16 to
+ * nearest-even, and the cache write copies the bits.  Over an 8-bit cache
+ * (ORACLE_ACT_BF16 added to the cache type) the activations are bfloat16
+ * the same way and each written value is quantized from its bfloat16 value
+ * exactly as an fp16 value would be.
  *
  * Layouts (row-major): query [T, H*D]; key, value [T, Hk*D];
  * key_cache, value_cache [NB, bs, Hk, D]; block_table [B, MB];
