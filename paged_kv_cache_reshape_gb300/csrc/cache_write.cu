@@ -204,7 +204,19 @@ __device__ __forceinline__ void row_transform(const __half* src, const Emit emit
       if (!rn && keep_all) {  // plain copy of a contiguous [nheads, D] row
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         uint4* d4 = reinterpret_cast<uint4*>(emit.dst);
-        for (int i = lane; i < nheads * chunks_per_head; i += 32) d4[i] = ld_plain(s4 + i);
+        const int n = nheads * chunks_per_head;
+        // Four loads per lane in flight before their stores: the source and
+        // the pool are separate tensors, which the compiler cannot assume
+        // for ordinary loads, so a load-store loop would wait on each load.
+        for (int i0 = lane; i0 < n; i0 += 4 * 32) {
+          uint4 v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (i0 + 32 * k < n) v[k] = ld_plain(s4 + i0 + 32 * k);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (i0 + 32 * k < n) d4[i0 + 32 * k] = v[k];
+        }
         return;
       }
     }
